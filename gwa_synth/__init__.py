@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module holds no arithmetic of the projection itself: it draws packed
+words, bf16 scales/biases, activations and MoE routings with the value
+distributions of the workloads below, and hands the same arrays to both the
+CUDA library and the CPU oracle.
+
+Recipe (every draw from numpy's PCG64 with an explicit seed):
+  * activations x: bf16(N(0, 1));
+  * packed weights: uniform random uint32 words, so every b-bit field of every
+    word is an independent uniform code in 0 .. 2^b - 1;
+  * scales: bf16(U(0.005, 0.02)), one per row per group of 64 inputs;
+  * biases: bf16(-8 * scale + N(0, 1e-3)) with the stored (bf16) scale;
+  * MoE: top-k expert ids drawn uniformly without replacement per token;
+    routing weights are the softmax of N(0, 1) logits over the k selected
+    slots (fp32).
+
+bf16 values are carried as their uint16 bit patterns.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+GROUP = 64
+
+
+def rng_for(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(int(seed)))
+
+
+def seed_for(config: int, layer: int = 0, tensor: int = 0) -> int:
+    """Seed of one tensor: 1000*config + 10*layer + tensor."""
+    return 1000 * int(config) + 10 * int(layer) + int(tensor)
+
+
+def bf16_bits(a) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (uint16), round to nearest even.
+
+    Only used to encode inputs; NaN does not occur in these draws."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_values(h) -> np.ndarray:
+    """bf16 bit patterns -> float32 values (exact)."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class QWeight:
+    """One affine group-quantized weight in the packed layout.
+
+    wq:     uint32 [rows, K*bits/32]  (codes packed along the input axis)
+    scales: uint16 (bf16 bits) [rows, K/64]
+    biases: uint16 (bf16 bits) [rows, K/64]
+    """
+    wq: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    N: int
+    K: int
+    bits: int
+    group: int = GROUP
+
+    @property
+    def nbytes(self) -> int:
+        return self.wq.nbytes + self.scales.nbytes + self.biases.nbytes
+
+
+def activations(seed: int, M: int, K: int) -> np.ndarray:
+    """x bf16 [M, K] ~ N(0, 1)."""
+    r = rng_for(seed)
+    return bf16_bits(r.standard_normal((M, K), dtype=np.float32))
+
+
+def packed_words(rng: np.random.Generator, N: int, K: int,
+                 bits: int) -> np.ndarray:
+    wpr = K * bits // 32
+    return rng.integers(0, 2**32, size=(N, wpr), dtype=np.uint32)
+
+
+def scale_bias(rng: np.random.Generator, N: int, K: int, group: int = GROUP):
+    G = K // group
+    s = bf16_bits(rng.uniform(0.005, 0.02, size=(N, G)).astype(np.float32))
+    noise = rng.normal(0.0, 1e-3, size=(N, G)).astype(np.float32)
+    b = bf16_bits(-8.0 * bf16_values(s) + noise)
+    return s, b
+
+
+def qweight(seed: int, N: int, K: int, bits: int = 4,
+            group: int = GROUP) -> QWeight:
+    """A seeded packed weight of N output rows and K inputs."""
+    if K % group or (K * bits) % 32:
+        raise ValueError("K must be a multiple of the group and of 32/bits")
+    r = rng_for(seed)
+    wq = packed_words(r, N, K, bits)
+    s, b = scale_bias(r, N, K, group)
+    return QWeight(wq, s, b, N, K, bits, group)
+
+
+def stack_rows(parts) -> QWeight:
+    """Concatenate weights along the output axis (host side)."""
+    K, bits, group = parts[0].K, parts[0].bits, parts[0].group
+    if any(p.K != K or p.bits != bits or p.group != group for p in parts):
+        raise ValueError("parts must share K, bits and group")
+    return QWeight(np.concatenate([p.wq for p in parts]),
+                   np.concatenate([p.scales for p in parts]),
+                   np.concatenate([p.biases for p in parts]),
+                   sum(p.N for p in parts), K, bits, group)
+
+
+def routing(seed: int, M: int, topk: int, E: int):
+    """Top-k expert ids (int32 [M, topk], distinct per token) and routing
+    weights (float32 [M, topk], softmax of N(0,1) logits over the slots)."""
+    r = rng_for(seed)
+    ids = np.stack([r.choice(E, size=topk, replace=False)
+                    for _ in range(M)]).astype(np.int32).reshape(M, topk)
+    logits = r.standard_normal((M, topk)).astype(np.float64)
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+    return ids, w
+
+
+# Workload shapes (sizes only).
+TINY_QKV = dict(M=1, K=512, sections=(512, 128, 128), bits=4)
+QKV_5120 = dict(M=1, K=5120, sections=(5120, 1024, 1024), bits=4)
+GATE_UP_5120 = dict(K=5120, I=13824, bits=4)
+STACK_LAYER = dict(hidden=5120, qkv=(5120, 1024, 1024), o=5120,
+                   intermediate=13824, layers=48)
+MOE_2048 = dict(hidden=2048, experts=256, I=512, topk=8, bits=4)

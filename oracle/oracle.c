@@ -1,0 +1,260 @@
+/*
+ * oracle.c -- plain fp64 CPU reference for MLX-style affine group-quantized
+ * projections.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or constant with the CUDA
+ * library; both sides see the same seeded inputs and nothing else.
+ *
+ * What it computes is the plain definition, written out with no blocking,
+ * fusion or reordering:
+ *
+ *   code   q[n,k] = (Wq[n, k/P] >> (b*(k mod P))) & (2^b - 1),  P = 32/b
+ *   weight w[n,k] = S[n, k/G] * q[n,k] + B[n, k/G]                (fp64)
+ *   output y[m,n] = sum_k x[m,k] * w[n,k]      (fp64, summed in k order)
+ *
+ * Sources (page title, section):
+ *   "Sanctum-MLX", server diagram ("4-bit quantized inference:
+ *       QuantizedLinear group_size=64") and the model parameter table
+ *       ("Quantization 4-bit, group_size=64").
+ *   "The Cathedral Doubled Itself", "The two fusions": the fused QKV weight
+ *       is [q_out + 2*kv_out, hidden/8] -- eight 4-bit codes per 32-bit word
+ *       along the input axis -- and its one matmul output is split back into
+ *       Q, K, V on the last axis; the gate+up fusion applies the same recipe
+ *       to gate_proj and up_proj ahead of SiLU and the multiply.
+ *   "saragossa", "Quantization formats": MLX affine integer weights at group
+ *       size 64 with bf16 scales and biases; u4 ~4.5 bpw and u8 ~8.5 bpw,
+ *       i.e. two 16-bit parameters per 64 weights.
+ *   "Sanctum-MLX" and "Four Candles For The Cathedral": 3-D switch_mlp expert
+ *       grids with per-expert gate_proj / up_proj (MoE routed experts).
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes):
+ *   - bit order inside a word: code k mod P sits at bits [b*(k mod P), +b),
+ *     lowest bits first;
+ *   - codes are unsigned, 0 .. 2^b-1; the affine bias carries any offset;
+ *   - the dequantized weight is scale*q + bias;
+ *   - gate rows come first, then up rows; SiLU(g) = g / (1 + exp(-g));
+ *   - MoE: gate+up mode gives h[t,j,:] = SiLU(Wg[e] x_t) * (Wu[e] x_t) for
+ *     e = ids[t,j]; down mode gives y[t,:] = sum_j r[t,j] * (Wd[e] h[t,j,:]),
+ *     summed over j in slot order.
+ *
+ * bf16 values arrive as their 16-bit patterns; widening bf16 -> fp32 -> fp64
+ * is exact.  Compile with -ffp-contract=off so no multiply-add is fused.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_BAD_ARG (-1)
+
+/* Exact widening of a bf16 bit pattern: the 16 bits are the top half of an
+ * IEEE binary32. */
+double orc_bf16_to_f64(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int bits_ok(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+
+/* The integer code at (row n, input k): field k mod P of word k / P. */
+static inline uint32_t code_at(const uint32_t *wq, int64_t words_per_row,
+                               int64_t n, int64_t k, int bits) {
+    int64_t per_word = 32 / bits;
+    uint32_t word = wq[n * words_per_row + k / per_word];
+    uint32_t shift = (uint32_t)(bits * (k % per_word));
+    uint32_t mask = (1u << bits) - 1u;
+    return (word >> shift) & mask;
+}
+
+static int shape_ok(int64_t N, int64_t K, int bits, int group) {
+    if (N < 0 || K < 0 || !bits_ok(bits) || group <= 0) return 0;
+    if (K % group != 0) return 0;
+    if (K % (32 / bits) != 0) return 0;
+    return 1;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Step 1 -- unpack: codes[n*K + k] = q[n,k]. */
+int orc_unpack(const uint32_t *wq, int64_t N, int64_t K, int bits,
+               uint8_t *codes) {
+    if (!shape_ok(N, K, bits, 1)) return ORC_BAD_ARG;
+    int64_t wpr = K * bits / 32;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            codes[n * K + k] = (uint8_t)code_at(wq, wpr, n, k, bits);
+    return ORC_OK;
+}
+
+/* Step 2 -- dequantize: w[n*K + k] = S[n,k/G] * q[n,k] + B[n,k/G], fp64. */
+int orc_dequant(const uint32_t *wq, const uint16_t *scales,
+                const uint16_t *biases, int64_t N, int64_t K, int bits,
+                int group, double *w) {
+    if (!shape_ok(N, K, bits, group)) return ORC_BAD_ARG;
+    int64_t wpr = K * bits / 32, gpr = K / group;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            double s = orc_bf16_to_f64(scales[n * gpr + k / group]);
+            double b = orc_bf16_to_f64(biases[n * gpr + k / group]);
+            double q = (double)code_at(wq, wpr, n, k, bits);
+            w[n * K + k] = s * q + b;
+        }
+    return ORC_OK;
+}
+
+/* One output: sum over k, in k order, of x[k] * (S*q + B). */
+static double dot_row(const uint16_t *xrow, const uint32_t *wq,
+                      const uint16_t *scales, const uint16_t *biases,
+                      int64_t n, int64_t K, int bits, int group) {
+    int64_t wpr = K * bits / 32, gpr = K / group;
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double s = orc_bf16_to_f64(scales[n * gpr + k / group]);
+        double b = orc_bf16_to_f64(biases[n * gpr + k / group]);
+        double q = (double)code_at(wq, wpr, n, k, bits);
+        double w = s * q + b;
+        acc += orc_bf16_to_f64(xrow[k]) * w;
+    }
+    return acc;
+}
+
+/* Step 3 -- y[m, i] = sum_k x[m,k] * w[rows[i], k] for i < n_rows.
+ * rows == NULL means every row 0..N-1 (then n_rows must equal N).
+ * x is bf16 [M, K] row-major; y is fp64 [M, n_rows] row-major. */
+int orc_qmv(const uint16_t *x, int64_t M, const uint32_t *wq,
+            const uint16_t *scales, const uint16_t *biases, int64_t N,
+            int64_t K, int bits, int group, const int64_t *rows,
+            int64_t n_rows, double *y, int nthreads) {
+    if (!shape_ok(N, K, bits, group) || M < 0 || n_rows < 0)
+        return ORC_BAD_ARG;
+    if (rows == NULL && n_rows != N) return ORC_BAD_ARG;
+    for (int64_t i = 0; i < n_rows; ++i)
+        if (rows && (rows[i] < 0 || rows[i] >= N)) return ORC_BAD_ARG;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        for (int64_t m = 0; m < M; ++m)
+            y[m * n_rows + i] =
+                dot_row(x + m * K, wq, scales, biases, n, K, bits, group);
+    }
+    return ORC_OK;
+}
+
+/* SiLU(g) = g / (1 + exp(-g)) in fp64. */
+double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* Step 5 -- fused gate+up with the SiLU(gate)*up epilogue.  The weight has
+ * 2*I rows: rows [0, I) are gate_proj, rows [I, 2I) are up_proj.
+ * h[m, i] = SiLU(g) * u with g = row cols[i] and u = row I + cols[i];
+ * cols == NULL means every column 0..I-1. */
+int orc_gate_up_silu(const uint16_t *x, int64_t M, const uint32_t *wq,
+                     const uint16_t *scales, const uint16_t *biases,
+                     int64_t N2, int64_t K, int bits, int group,
+                     const int64_t *cols, int64_t n_cols, double *h,
+                     int nthreads) {
+    if (!shape_ok(N2, K, bits, group) || N2 % 2 != 0 || M < 0)
+        return ORC_BAD_ARG;
+    int64_t I = N2 / 2;
+    if (cols == NULL && n_cols != I) return ORC_BAD_ARG;
+    for (int64_t i = 0; i < n_cols; ++i)
+        if (cols && (cols[i] < 0 || cols[i] >= I)) return ORC_BAD_ARG;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n_cols; ++i) {
+        int64_t c = cols ? cols[i] : i;
+        for (int64_t m = 0; m < M; ++m) {
+            double g = dot_row(x + m * K, wq, scales, biases, c, K, bits,
+                               group);
+            double u = dot_row(x + m * K, wq, scales, biases, I + c, K, bits,
+                               group);
+            h[m * n_cols + i] = orc_silu(g) * u;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Step 6a -- MoE gate+up: stacked expert weights, expert e occupies rows
+ * [e*N2, (e+1)*N2) of wq/scales/biases (each expert is a 2*I x K fused
+ * gate+up matrix).  h[t, j, i] = SiLU(g) * u for expert ids[t, j];
+ * h is fp64 [M, topk, I]. */
+int orc_moe_gate_up_silu(const uint16_t *x, int64_t M, int64_t topk,
+                         const int32_t *ids, const uint32_t *wq,
+                         const uint16_t *scales, const uint16_t *biases,
+                         int64_t E, int64_t N2, int64_t K, int bits,
+                         int group, double *h, int nthreads) {
+    if (!shape_ok(N2, K, bits, group) || N2 % 2 != 0 || M < 0 || topk < 0)
+        return ORC_BAD_ARG;
+    for (int64_t p = 0; p < M * topk; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return ORC_BAD_ARG;
+    int64_t I = N2 / 2;
+    int64_t wpr = K * bits / 32, gpr = K / group;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t t = 0; t < M; ++t)
+        for (int64_t j = 0; j < topk; ++j) {
+            int64_t e = ids[t * topk + j];
+            const uint32_t *we = wq + e * N2 * wpr;
+            const uint16_t *se = scales + e * N2 * gpr;
+            const uint16_t *be = biases + e * N2 * gpr;
+            for (int64_t i = 0; i < I; ++i) {
+                double g = dot_row(x + t * K, we, se, be, i, K, bits, group);
+                double u =
+                    dot_row(x + t * K, we, se, be, I + i, K, bits, group);
+                h[(t * topk + j) * I + i] = orc_silu(g) * u;
+            }
+        }
+    return ORC_OK;
+}
+
+/* Step 6b -- MoE down + routed combine.  hin is bf16 [M, topk, K]; expert e
+ * occupies rows [e*N, (e+1)*N).  y[t, n] = sum_j r[t,j] * (Wd[e] hin[t,j])[n]
+ * with the sum over j in slot order; y is fp64 [M, N]. */
+int orc_moe_down_combine(const uint16_t *hin, int64_t M, int64_t topk,
+                         const int32_t *ids, const float *route_w,
+                         const uint32_t *wq, const uint16_t *scales,
+                         const uint16_t *biases, int64_t E, int64_t N,
+                         int64_t K, int bits, int group, double *y,
+                         int nthreads) {
+    if (!shape_ok(N, K, bits, group) || M < 0 || topk < 0) return ORC_BAD_ARG;
+    for (int64_t p = 0; p < M * topk; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return ORC_BAD_ARG;
+    int64_t wpr = K * bits / 32, gpr = K / group;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t t = 0; t < M; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < topk; ++j) {
+                int64_t e = ids[t * topk + j];
+                double d = dot_row(hin + (t * topk + j) * K, wq + e * N * wpr,
+                                   scales + e * N * gpr, biases + e * N * gpr,
+                                   n, K, bits, group);
+                acc += (double)route_w[t * topk + j] * d;
+            }
+            y[t * N + n] = acc;
+        }
+    return ORC_OK;
+}
