@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the affine group-quantized projection path.
+
+Workload (one step): a 48-layer dense projection stack at M=1 token, u4
+codes, group 64, bf16 scales/biases.  Each layer runs four library calls:
+  fused QKV   5120 -> 5120+1024+1024  (gwa_qmv_fused_sections, Q/K/V buffers)
+  o_proj      5120 -> 5120            (gwa_qmv_affine, reads Q)
+  gate+up     5120 -> 2x13824, SiLU   (gwa_qmv_gate_up_silu, reads o)
+  down        13824 -> 5120           (gwa_qmv_affine, reads h)
+so 192 launches and 7.43 GB of packed weights per step, far above the 129 MB
+L2: every step streams its weights from HBM.  Each layer's QKV reads the step
+input x.  The launches of one projection type are captured in one CUDA graph
+(48 launches) and a step replays the four graphs in dependency order, with
+CUDA events between them, so the per-kernel durations come from the same
+timed region as the step time.
+
+Metric: achieved HBM GB/s of algorithmic bytes (packed codes + scales +
+biases + activations) and the equivalent 48-layer decode steps/s.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload: one layer's four projections per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HIDDEN, QOUT, KVOUT, INTER, LAYERS = 5120, 5120, 1024, 13824, 48
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gwa", choices=["gwa", "reference"])
+    ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload
+def proj_bytes(rows: int, K: int, bits: int, M: int) -> int:
+    """Algorithmic bytes of one projection call: packed codes + scales +
+    biases + activations (outputs excluded)."""
+    return rows * K * bits // 8 + 2 * 2 * rows * (K // 64) + 2 * M * K
+
+
+def layer_shapes():
+    return [("qkv", QOUT + 2 * KVOUT, HIDDEN), ("o", HIDDEN, QOUT),
+            ("gate_up", 2 * INTER, HIDDEN), ("down", HIDDEN, INTER)]
+
+
+def layer_bytes(bits: int, M: int) -> dict:
+    return {n: proj_bytes(r, k, bits, M) for n, r, k in layer_shapes()}
+
+
+def workload_config(args) -> dict:
+    return {
+        "workload": (f"{args.layers}-layer dense decode projection stack, "
+                     f"M={args.tokens}, u{args.bits} group 64 bf16 scale/bias:"
+                     " fused QKV 5120->5120+1024+1024, o_proj 5120->5120, "
+                     "fused gate+up 5120->2x13824 with SiLU(gate)*up, "
+                     "down 13824->5120; 4 calls per layer"),
+        "layers": args.layers, "M": args.tokens, "bits": args.bits,
+        "group": 64, "hidden": HIDDEN, "intermediate": INTER,
+        "l2": "inputs larger than L2: every step streams "
+              f"{sum(layer_bytes(args.bits, args.tokens).values()) * args.layers / 1e9:.2f}"
+              " GB of distinct weights (L2 is 129 MB)",
+        "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single",
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gwa(args, rank: int, world: int, local_rank: int):
+    import torch
+    import group_wise_affine_gb300 as gwa
+    import gwa_synth as synth
+
+    gwa.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    M, bits, L = args.tokens, args.bits, args.layers
+
+    # weights: one seeded draw per layer and projection, on the device
+    W = []
+    for l in range(L):
+        layer = {}
+        for p, (name, rows, K) in enumerate(layer_shapes()):
+            wq, s, b = synth.device_qweight(synth.stack_seed(l, p, bits), rows,
+                                            K, bits, device=dev)
+            layer[name] = gwa.QWeight(wq, s, b, rows, K, bits, 64)
+        W.append(layer)
+    g = torch.Generator(device=dev)
+    g.manual_seed(12345 + rank)
+    x = torch.randn((M, HIDDEN), generator=g, device=dev).to(torch.bfloat16)
+    bufs = []
+    for l in range(L):
+        bufs.append(dict(
+            q=torch.empty((M, QOUT), dtype=torch.bfloat16, device=dev),
+            k=torch.empty((M, KVOUT), dtype=torch.bfloat16, device=dev),
+            v=torch.empty((M, KVOUT), dtype=torch.bfloat16, device=dev),
+            o=torch.empty((M, HIDDEN), dtype=torch.bfloat16, device=dev),
+            h=torch.empty((M, INTER), dtype=torch.bfloat16, device=dev),
+            y=torch.empty((M, HIDDEN), dtype=torch.bfloat16, device=dev)))
+    ws = gwa.make_workspace(M, INTER, dev)   # None at decode sizes
+
+    def call(kind, l, stream=None):
+        w, b = W[l], bufs[l]
+        if kind == "qkv":
+            gwa.qmv_fused_sections(x, w["qkv"], (QOUT, KVOUT, KVOUT),
+                                   outs=[b["q"], b["k"], b["v"]],
+                                   workspace=ws, stream=stream)
+        elif kind == "o":
+            gwa.qmv_affine(b["q"], w["o"], y=b["o"], workspace=ws,
+                           stream=stream)
+        elif kind == "gate_up":
+            gwa.qmv_gate_up_silu(b["o"], w["gate_up"], h=b["h"], workspace=ws,
+                                 stream=stream)
+        else:
+            gwa.qmv_affine(b["h"], w["down"], y=b["y"], workspace=ws,
+                           stream=stream)
+
+    kinds = ["qkv", "o", "gate_up", "down"]
+    for k in kinds:                       # eager warm-up (sets up the library)
+        call(k, 0)
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream(device=dev)
+    graphs = {}
+    for k in kinds:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=side):
+            for l in range(L):
+                call(k, l)
+        graphs[k] = gr
+    torch.cuda.synchronize()
+
+    def step():
+        for k in kinds:
+            graphs[k].replay()
+
+    st = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank if world == 1 else
+                          int(os.environ.get("LOCAL_RANK", 0)))
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+          for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(st)
+    for i in range(K):
+        ev[i][0].record(st)
+        for j, k in enumerate(kinds):
+            graphs[k].replay()
+            ev[i][j + 1].record(st)
+    end.record(st)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    total_ms = start.elapsed_time(end)
+    per_kind_ms = {k: sum(ev[i][j].elapsed_time(ev[i][j + 1])
+                          for i in range(K)) for j, k in enumerate(kinds)}
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+
+    # end to end: pinned host input in, step, result back out
+    x_host = torch.empty((M, HIDDEN), dtype=torch.bfloat16).pin_memory()
+    x_host.copy_(x.cpu())
+    y_host = torch.empty((M, HIDDEN), dtype=torch.bfloat16).pin_memory()
+    KE = max(3, min(K, 50))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    e0.record(st)
+    for _ in range(KE):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(bufs[-1]["y"], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    e2e_ms = e0.elapsed_time(e1) / KE
+    return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
+                e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
+                h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
+                launches=K * 4 * L)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_layer_prep(bits: int, M: int):
+    """Host copies of layer 0's four projections (same seeded recipe, drawn
+    on the host) and activations, for the CPU oracle."""
+    import gwa_synth as synth
+    shapes = layer_shapes()
+    ws = [synth.qweight(synth.stack_seed(0, p, bits), rows, K, bits)
+          for p, (_, rows, K) in enumerate(shapes)]
+    xs = {K: synth.activations(777 + K, M, K) for _, _, K in shapes}
+    return shapes, ws, xs
+
+
+def oracle_layer_pass(prep, bits: int):
+    import oracle
+    shapes, ws, xs = prep
+    for (name, rows, K), w in zip(shapes, ws):
+        if name == "gate_up":
+            oracle.gate_up_silu(xs[K], w.wq, w.scales, w.biases, rows, K, bits)
+        else:
+            oracle.qmv(xs[K], w.wq, w.scales, w.biases, rows, K, bits)
+
+
+def oracle_layer_sample(bits: int, M: int, seconds: float, max_reps: int,
+                        prep=None):
+    """Times the oracle on layer 0's four projections, repeated until
+    `seconds` have passed or `max_reps` passes ran."""
+    import oracle
+    oracle.build()
+    prep = prep or oracle_layer_prep(bits, M)
+    nthreads = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer_pass(prep, bits)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= max_reps:
+            break
+    return reps, el, nthreads
+
+
+def cpu_baseline(args):
+    reps, el, nthreads = oracle_layer_sample(args.bits, args.tokens, 10.0, 48)
+    lb = sum(layer_bytes(args.bits, args.tokens).values())
+    return {"value": round(reps * lb / el / 1e9, 4), "unit": "GB/s",
+            "cores": nthreads, "kind": "oracle",
+            "steps_per_s": round(reps / el / args.layers, 6),
+            "sample": (f"{reps} pass(es) of layer 0's four projections "
+                       f"(fp64 C oracle, {nthreads} OpenMP threads), "
+                       f"{el:.1f} s; GB/s of the same algorithmic bytes")}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    lb = sum(layer_bytes(args.bits, args.tokens).values())
+    prep = oracle_layer_prep(args.bits, args.tokens)
+    for _ in range(args.warmup):
+        oracle_layer_pass(prep, args.bits)
+    reps, el, nthreads = oracle_layer_sample(args.bits, args.tokens,
+                                             math.inf, args.steps, prep)
+    gbs = reps * lb / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4),
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * el / reps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": workload_config(args),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
+                         "cores": nthreads, "kind": "oracle",
+                         "sample": "each step: layer 0's four projections, "
+                                   "fp64 C oracle (same seeded recipe)"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "steps_per_s": round(reps / el / args.layers, 6),
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = ("quantized GEMV achieved HBM GB/s (% of GB300 peak); "
+          "48-layer decode steps/s")
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "gwa" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    r = run_gwa(args, rank, world, local_rank)
+    import torch
+    total_ms = r["total_ms"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    K, L, M, bits = args.steps, args.layers, args.tokens, args.bits
+    lb = layer_bytes(bits, M)
+    step_bytes = sum(lb.values()) * L
+    ms_step = total_ms / K
+    gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    kernels = {}
+    for kind, ms in r["per_kind_ms"].items():
+        per_launch_us = 1e3 * ms / (K * L)
+        a = lb[kind] / (per_launch_us * 1e-6) / 1e9
+        kernels[kind] = {"us_per_launch": round(per_launch_us, 3),
+                         "bytes_per_launch": lb[kind],
+                         "GB/s": round(a, 1),
+                         "frac_of_measured": round(a / peak, 4)}
+    dom = max(r["per_kind_ms"], key=lambda k: r["per_kind_ms"][k])
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(args),
+        "steps_per_s": round(world * 1e3 / ms_step, 2),
+        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * gbs / world / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": dom,
+                     "achieved": kernels[dom]["GB/s"], "peak": peak,
+                     "unit": "GB/s",
+                     "frac": round(kernels[dom]["GB/s"] / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": None},
+        "kernels": kernels,
+        "e2e": {"value": round(world * step_bytes / (r["e2e_ms"] * 1e-3) / 1e9,
+                               1),
+                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": round(r["e2e_ms"], 4),
+                "how": "pinned x in, 4 graph replays of the public API calls, "
+                       "last layer's y out, per step"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

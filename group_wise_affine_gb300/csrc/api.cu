@@ -1,0 +1,409 @@
+// C ABI of libgwa.so (declared in include/gwa.h): argument validation,
+// kernel selection and launch.  Nothing here allocates, synchronizes or
+// aborts; every problem becomes a status code plus a thread-local message.
+#include <mutex>
+#include <map>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string>
+#include <tuple>
+
+#include "../../include/gwa.h"
+#include "internal.h"
+#include "qmm.h"
+
+namespace gwa {
+
+static thread_local std::string g_last_error;
+
+int set_error(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+#define fail set_error
+
+static int cuda_fail(cudaError_t e, const char *what) {
+    return fail(GWA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool aligned(const void *p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// ------------------------------------------------------------ device info
+static std::mutex g_mu;
+
+static int current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    return GWA_OK;
+}
+
+int num_sms() {
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n;
+    return n;
+}
+
+// The kernels are built for sm_103a only.
+static int check_device() {
+    static std::map<int, int> ok;
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = ok.find(dev);
+        if (it != ok.end())
+            return it->second ? GWA_OK
+                              : fail(GWA_ERR_CUDA, "device %d is not sm_103", dev);
+    }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    const bool good = major == 10 && minor == 3;
+    std::lock_guard<std::mutex> lk(g_mu);
+    ok[dev] = good;
+    return good ? GWA_OK
+                : fail(GWA_ERR_CUDA, "device %d has compute capability %d.%d; "
+                       "this library is built for sm_103a", dev, major, minor);
+}
+
+cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
+                           int *grid) {
+    static std::map<std::tuple<int, const void *, size_t, int>, int> cache;
+    static std::map<std::pair<int, const void *>, bool> attr_set;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int sms = num_sms();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, kernel, smem, threads);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *grid = it->second;
+        return cudaSuccess;
+    }
+    if (!attr_set[std::make_pair(dev, kernel)]) {
+        // dynamic + static shared memory must stay within the opt-in limit
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        int optin = 0;
+        e = cudaDeviceGetAttribute(&optin,
+                                   cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        const int maxdyn = optin - (int)fa.sharedSizeBytes;
+        if (maxdyn <= 0) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 maxdyn);
+        if (e != cudaSuccess) return e;
+        attr_set[std::make_pair(dev, kernel)] = true;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
+                                                      smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    *grid = per_sm * sms;
+    cache[key] = *grid;
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------ validation
+static int check_qweight(const gwa_qweight &w, const char *fn) {
+    if (w.bits != 4 && w.bits != 8)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 4, 8)", fn,
+                    (int)w.bits);
+    if (w.group != 64)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: group=%d (supported: 64)", fn,
+                    (int)w.group);
+    if (w.N < 0 || w.K <= 0 || w.K % 64 != 0)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: N=%lld K=%lld (need N >= 0, K a positive multiple "
+                    "of 64)", fn, (long long)w.N, (long long)w.K);
+    if (w.K > (1 << 20))
+        return fail(GWA_ERR_INVALID_ARG, "%s: K=%lld exceeds 2^20", fn,
+                    (long long)w.K);
+    if (w.N > 0 && (!w.wq || !w.scales || !w.biases))
+        return fail(GWA_ERR_INVALID_ARG, "%s: null weight pointer", fn);
+    if (!aligned(w.wq, 16))
+        return fail(GWA_ERR_MISALIGNED, "%s: wq must be 16-byte aligned", fn);
+    if (!aligned(w.scales, 2) || !aligned(w.biases, 2))
+        return fail(GWA_ERR_MISALIGNED,
+                    "%s: scales/biases must be 2-byte aligned", fn);
+    return GWA_OK;
+}
+
+static int check_x(const uint16_t *x, int64_t M, const char *fn) {
+    if (M < 0) return fail(GWA_ERR_INVALID_ARG, "%s: M=%lld", fn, (long long)M);
+    if (M > 0 && !x) return fail(GWA_ERR_INVALID_ARG, "%s: null x", fn);
+    if (!aligned(x, 16))
+        return fail(GWA_ERR_MISALIGNED, "%s: x must be 16-byte aligned", fn);
+    return GWA_OK;
+}
+
+static DenseParams dense_base(const uint16_t *x, int64_t M,
+                              const gwa_qweight &w) {
+    DenseParams p{};
+    p.x = x;
+    p.M = (int)M;
+    p.K = (int)w.K;
+    p.bits = w.bits;
+    p.wq = w.wq;
+    p.sc = w.scales;
+    p.bi = w.biases;
+    p.N = w.N;
+    p.nch = (int)(w.K * w.bits / 128);
+    p.G = (int)(w.K / 64);
+    return p;
+}
+
+// Runs the decode kernels over token passes that fit in shared memory.
+static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
+                     const int64_t *sec_sizes, cudaStream_t st,
+                     const char *fn) {
+    const int mt = dense_max_tokens(p.bits, p.nch);
+    if (mt < 1)
+        return fail(GWA_ERR_INVALID_ARG, "%s: K=%d too large for staging", fn,
+                    p.K);
+    for (int64_t t0 = 0; t0 < M; t0 += mt) {
+        DenseParams q = p;
+        q.M = (int)((M - t0) < mt ? (M - t0) : mt);
+        q.x = p.x + t0 * p.K;
+        if (mode == 1) {
+            for (int s = 0; s < p.nsec; ++s)
+                q.sec_out[s] = p.sec_out[s] ? p.sec_out[s] + t0 * sec_sizes[s]
+                                            : nullptr;
+        } else {
+            q.y = p.y + t0 * out_stride;
+        }
+        cudaError_t e = launch_dense(mode, q, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return GWA_OK;
+}
+
+}  // namespace gwa
+
+using namespace gwa;
+
+extern "C" {
+
+const char *gwa_last_error(void) { return g_last_error.c_str(); }
+
+size_t gwa_workspace_bytes(int64_t M, int64_t K) {
+    if (M <= 8 || K <= 0) return 0;
+    return qmm_workspace_bytes(M, K);
+}
+
+int gwa_qmv_affine(const uint16_t *x, int64_t M, gwa_qweight w, uint16_t *y,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "gwa_qmv_affine";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (!rc) rc = check_x(x, M, fn);
+    if (rc) return rc;
+    if (M == 0 || w.N == 0) return GWA_OK;
+    if (!y) return fail(GWA_ERR_INVALID_ARG, "%s: null y", fn);
+    if (!aligned(y, 2)) return fail(GWA_ERR_MISALIGNED, "%s: y alignment", fn);
+    if ((rc = check_device())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 8) {
+        QmmArgs a{};
+        a.x = x; a.M = M; a.w = w; a.mode = 0; a.y = y;
+        return qmm_run(a, workspace, workspace_bytes, st);
+    }
+    DenseParams p = dense_base(x, M, w);
+    p.y = y;
+    return run_dense(0, p, M, w.N, nullptr, st, fn);
+}
+
+int gwa_qmv_fused_sections(const uint16_t *x, int64_t M, gwa_qweight w,
+                           int32_t n_sections, const int64_t *section_sizes,
+                           uint16_t *const *outs,
+                           const uint16_t *const *out_bias, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    const char *fn = "gwa_qmv_fused_sections";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (!rc) rc = check_x(x, M, fn);
+    if (rc) return rc;
+    if (n_sections < 1 || n_sections > kMaxSections)
+        return fail(GWA_ERR_INVALID_ARG, "%s: n_sections=%d (1..%d)", fn,
+                    (int)n_sections, kMaxSections);
+    if (!section_sizes || !outs)
+        return fail(GWA_ERR_INVALID_ARG, "%s: null section arrays", fn);
+    int64_t total = 0;
+    for (int s = 0; s < n_sections; ++s) {
+        if (section_sizes[s] < 0)
+            return fail(GWA_ERR_INVALID_ARG, "%s: section %d size %lld", fn, s,
+                        (long long)section_sizes[s]);
+        if (section_sizes[s] > 0 && M > 0 && !outs[s])
+            return fail(GWA_ERR_INVALID_ARG, "%s: null output %d", fn, s);
+        if (!aligned(outs[s], 2))
+            return fail(GWA_ERR_MISALIGNED, "%s: output %d alignment", fn, s);
+        if (out_bias && !aligned(out_bias[s], 2))
+            return fail(GWA_ERR_MISALIGNED, "%s: bias %d alignment", fn, s);
+        total += section_sizes[s];
+    }
+    if (total != w.N)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: section sizes add up to %lld, weight has %lld rows",
+                    fn, (long long)total, (long long)w.N);
+    if (M == 0 || w.N == 0) return GWA_OK;
+    if ((rc = check_device())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DenseParams p = dense_base(x, M, w);
+    p.nsec = n_sections;
+    p.sec_start[0] = 0;
+    for (int s = 0; s < n_sections; ++s) {
+        p.sec_start[s + 1] = p.sec_start[s] + section_sizes[s];
+        p.sec_out[s] = outs[s];
+        p.sec_bias[s] = out_bias ? out_bias[s] : nullptr;
+    }
+    if (M > 8) {
+        QmmArgs a{};
+        a.x = x; a.M = M; a.w = w; a.mode = 1;
+        a.nsec = n_sections;
+        for (int s = 0; s <= n_sections; ++s) a.sec_start[s] = p.sec_start[s];
+        for (int s = 0; s < n_sections; ++s) {
+            a.sec_out[s] = p.sec_out[s];
+            a.sec_bias[s] = p.sec_bias[s];
+        }
+        return qmm_run(a, workspace, workspace_bytes, st);
+    }
+    return run_dense(1, p, M, 0, section_sizes, st, fn);
+}
+
+int gwa_qmv_gate_up_silu(const uint16_t *x, int64_t M, gwa_qweight w,
+                         uint16_t *h, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    const char *fn = "gwa_qmv_gate_up_silu";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (!rc) rc = check_x(x, M, fn);
+    if (rc) return rc;
+    if (w.N % 2 != 0)
+        return fail(GWA_ERR_INVALID_ARG, "%s: N=%lld must be even (gate; up)",
+                    fn, (long long)w.N);
+    if (M == 0 || w.N == 0) return GWA_OK;
+    if (!h) return fail(GWA_ERR_INVALID_ARG, "%s: null h", fn);
+    if (!aligned(h, 2)) return fail(GWA_ERR_MISALIGNED, "%s: h alignment", fn);
+    if ((rc = check_device())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 8) {
+        QmmArgs a{};
+        a.x = x; a.M = M; a.w = w; a.mode = 2; a.y = h;
+        return qmm_run(a, workspace, workspace_bytes, st);
+    }
+    DenseParams p = dense_base(x, M, w);
+    p.y = h;
+    p.I = w.N / 2;
+    return run_dense(2, p, M, w.N / 2, nullptr, st, fn);
+}
+
+int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
+                       const int32_t *expert_ids, const float *route_w,
+                       gwa_qweight w, int32_t num_experts, int32_t mode,
+                       uint16_t *out, int32_t *status, void *stream) {
+    const char *fn = "gwa_moe_qmv_gather";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (!rc) rc = check_x(x, M, fn);
+    if (rc) return rc;
+    if (mode != GWA_MOE_GATE_UP_SILU && mode != GWA_MOE_DOWN_COMBINE)
+        return fail(GWA_ERR_INVALID_ARG, "%s: mode=%d", fn, (int)mode);
+    if (M > 8)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: M=%lld (decode path: M <= 8)", fn,
+                    (long long)M);
+    if (topk < 1 || topk > 32)
+        return fail(GWA_ERR_INVALID_ARG, "%s: topk=%d (1..32)", fn, (int)topk);
+    if (num_experts < 1)
+        return fail(GWA_ERR_INVALID_ARG, "%s: num_experts=%d", fn,
+                    (int)num_experts);
+    if (mode == GWA_MOE_GATE_UP_SILU && w.N % 2 != 0)
+        return fail(GWA_ERR_INVALID_ARG, "%s: gate+up rows per expert must be "
+                    "even", fn);
+    if (M == 0 || w.N == 0) return GWA_OK;
+    if (!expert_ids || !out)
+        return fail(GWA_ERR_INVALID_ARG, "%s: null ids or output", fn);
+    if (mode == GWA_MOE_DOWN_COMBINE && !route_w)
+        return fail(GWA_ERR_INVALID_ARG, "%s: down mode needs route_w", fn);
+    if (!aligned(expert_ids, 4) || !aligned(route_w, 4) ||
+        !aligned(status, 4) || !aligned(out, 2))
+        return fail(GWA_ERR_MISALIGNED, "%s: ids/route_w/status/out alignment",
+                    fn);
+    const int nch = (int)(w.K * w.bits / 128);
+    const int cap = moe_max_tokens(w.bits, nch, mode);
+    if ((mode == 0 && cap < 1) || (mode == 1 && cap < M * topk))
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: M*topk=%lld inputs of K=%lld do not fit in shared "
+                    "memory", fn, (long long)(M * topk), (long long)w.K);
+    if ((rc = check_device())) return rc;
+    MoeParams p{};
+    p.x = x;
+    p.M = (int)M;
+    p.topk = topk;
+    p.K = (int)w.K;
+    p.bits = w.bits;
+    p.ids = expert_ids;
+    p.route_w = route_w;
+    p.wq = w.wq;
+    p.sc = w.scales;
+    p.bi = w.biases;
+    p.N = w.N;
+    p.E = num_experts;
+    p.nch = nch;
+    p.G = (int)(w.K / 64);
+    p.out = out;
+    p.status = status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mode == GWA_MOE_GATE_UP_SILU ? launch_moe_gate_up(p, st)
+                                                 : launch_moe_down(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return GWA_OK;
+}
+
+int gwa_debug_unpack(gwa_qweight w, uint8_t *codes, void *stream) {
+    const char *fn = "gwa_debug_unpack";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (rc) return rc;
+    if (w.N == 0) return GWA_OK;
+    if (!codes) return fail(GWA_ERR_INVALID_ARG, "%s: null codes", fn);
+    if ((rc = check_device())) return rc;
+    cudaError_t e = launch_debug_unpack(w.wq, w.N, w.K, w.bits, codes,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
+}
+
+int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream) {
+    const char *fn = "gwa_debug_dequant";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (rc) return rc;
+    if (w.N == 0) return GWA_OK;
+    if (!wf) return fail(GWA_ERR_INVALID_ARG, "%s: null output", fn);
+    if (!aligned(wf, 4)) return fail(GWA_ERR_MISALIGNED, "%s: alignment", fn);
+    if ((rc = check_device())) return rc;
+    cudaError_t e = launch_debug_dequant(w.wq, w.scales, w.biases, w.N, w.K,
+                                         w.bits, wf,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
+}
+
+}  // extern "C"

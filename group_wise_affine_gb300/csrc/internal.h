@@ -1,0 +1,75 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gwa {
+
+constexpr int kDenseThreads = 512;
+// Shared-memory budget (bytes) above which staged activations are kept as
+// bf16 instead of fp32.
+constexpr size_t kDenseF32StageMax = 96 * 1024;
+// Dynamic shared memory the launchers budget per CTA: the sm_103a opt-in
+// limit (227 KB) less room for the kernels' static arrays.
+constexpr size_t kMaxDynSmem = 216 * 1024;
+constexpr int kMaxSections = 8;
+
+struct DenseParams {
+    const uint16_t *x;   // [M, K] bf16
+    int M;               // tokens in this launch (<= 8)
+    int K;
+    int bits;
+    const uint32_t *wq;  // [N, K*bits/32]
+    const uint16_t *sc;  // [N, K/64]
+    const uint16_t *bi;  // [N, K/64]
+    int64_t N;           // weight rows
+    int nch;             // 16-byte chunks per row
+    int G;               // groups per row
+    int64_t nblocks;     // warp blocks (set by the launcher)
+    uint16_t *y;         // plain: [M, N]; gate+up: [M, I]
+    int64_t I;           // gate+up: N / 2
+    int nsec;
+    int64_t sec_start[kMaxSections + 1];
+    uint16_t *sec_out[kMaxSections];
+    const uint16_t *sec_bias[kMaxSections];
+};
+
+// Blocks for a persistent grid: SMs x resident CTAs of `kernel`.
+cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
+                           int *grid);
+int num_sms();
+
+cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st);
+int dense_max_tokens(int bits, int nch);
+
+struct MoeParams {
+    const uint16_t *x;      // gate+up: [M, K]; down: [M, topk, K]
+    int M;
+    int topk;
+    int K;
+    int bits;
+    const int32_t *ids;     // [M, topk]
+    const float *route_w;   // [M, topk] (down)
+    const uint32_t *wq;     // [E, N, K*bits/32]
+    const uint16_t *sc;     // [E, N, K/64]
+    const uint16_t *bi;
+    int64_t N;              // rows per expert
+    int E;
+    int nch;
+    int G;
+    uint16_t *out;
+    int32_t *status;
+};
+cudaError_t launch_moe_gate_up(const MoeParams &p, cudaStream_t st);
+cudaError_t launch_moe_down(const MoeParams &p, cudaStream_t st);
+int moe_max_tokens(int bits, int nch, int mode);
+
+cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
+                                int bits, uint8_t *codes, cudaStream_t st);
+cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
+                                 const uint16_t *bi, int64_t N, int64_t K,
+                                 int bits, float *wf, cudaStream_t st);
+
+}  // namespace gwa

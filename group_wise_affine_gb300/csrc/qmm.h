@@ -1,0 +1,32 @@
+// Prefill-shaped (M > 8) path: tensor-core (tcgen05) kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gwa.h"
+#include "internal.h"
+
+namespace gwa {
+
+struct QmmArgs {
+    const uint16_t *x;  // [M, K] bf16
+    int64_t M;
+    gwa_qweight w;
+    int mode;           // 0 plain, 1 sections, 2 gate+up SwiGLU
+    uint16_t *y;        // plain: [M, N]; gate+up: [M, N/2]
+    int nsec;
+    int64_t sec_start[kMaxSections + 1];
+    uint16_t *sec_out[kMaxSections];
+    const uint16_t *sec_bias[kMaxSections];
+};
+
+size_t qmm_workspace_bytes(int64_t M, int64_t K);
+int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
+            cudaStream_t st);
+
+// Records the thread's last error text and returns `code`.
+int set_error(int code, const char *fmt, ...);
+
+}  // namespace gwa

@@ -126,6 +126,39 @@ def routing(seed: int, M: int, topk: int, E: int):
     return ids, w
 
 
+# ---------------------------------------------------------------- on device
+def device_qweight(seed: int, N: int, K: int, bits: int = 4,
+                   group: int = GROUP, device="cuda"):
+    """The same recipe drawn on the GPU with torch's generator, for weights
+    too large to draw on the host (the 48-layer stack).  Returns the raw
+    tensors (wq int32 [N, K*bits/32], scales/biases bfloat16 [N, K/group]);
+    a test copies a sampled layer back to the host for the oracle."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    wpr = K * bits // 32
+    wq = torch.randint(0, 2**32, (N, wpr), generator=g, device=device,
+                       dtype=torch.int64).to(torch.int32)
+    G = K // group
+    s = (torch.rand((N, G), generator=g, device=device) * 0.015 + 0.005)
+    s = s.to(torch.bfloat16)
+    noise = torch.randn((N, G), generator=g, device=device) * 1e-3
+    b = (-8.0 * s.float() + noise).to(torch.bfloat16)
+    return wq, s, b
+
+
+def stack_layer_shapes(hidden=5120, q=5120, kv=1024, intermediate=13824):
+    """(name, rows, K) of the four projections of one dense layer:
+    fused QKV, o_proj, fused gate+up, down."""
+    return [("qkv", q + 2 * kv, hidden), ("o", hidden, q),
+            ("gate_up", 2 * intermediate, hidden),
+            ("down", hidden, intermediate)]
+
+
+def stack_seed(layer: int, proj: int, bits: int) -> int:
+    return seed_for(3, layer, proj) + 100000 * bits
+
+
 # Workload shapes (sizes only).
 TINY_QKV = dict(M=1, K=512, sections=(512, 128, 128), bits=4)
 QKV_5120 = dict(M=1, K=5120, sections=(5120, 1024, 1024), bits=4)

@@ -1,0 +1,146 @@
+/*
+ * gwa.h -- C ABI of libgwa.so: affine group-quantized linear projections on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (MLX-style affine integer weights):
+ *   code   q[n,k] = (Wq[n, k/P] >> (b*(k mod P))) & (2^b - 1),  P = 32/b
+ *   weight w[n,k] = scale[n, k/64] * q[n,k] + bias[n, k/64]
+ *   output y[m,n] = sum_k x[m,k] * w[n,k]   (fp32 accumulation, bf16 out)
+ * Defined by: "Sanctum-MLX", server diagram and model parameter table
+ * (4-bit QuantizedLinear, group_size=64); "saragossa", "Quantization
+ * formats" (MLX affine u4/u8, group size 64, bf16 scales/biases, ~4.5 and
+ * ~8.5 bits per weight); "The Cathedral Doubled Itself", "The two fusions"
+ * (packed weight [rows, hidden/8] uint32 for 4-bit codes, codes packed along
+ * the input axis).  Inside a word the first code sits in the lowest bits.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; arrays of
+ *     pointers (section outputs/biases) and section sizes are HOST arrays.
+ *     The library allocates nothing, keeps no pointer after the call returns,
+ *     and never synchronizes: work is enqueued on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) and the call returns at once.
+ *   - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *   - All matrices are row-major and contiguous.  x is [M, K].
+ *   - Wq, x and the workspace must be 16-byte aligned; scales, biases and
+ *     outputs 2-byte aligned.  K must be a multiple of 64.
+ *   - bits is 4 or 8; group must be 64.
+ *   - M <= 8 runs the decode (GEMV) kernels on the CUDA cores and needs no
+ *     workspace (pass NULL, 0).  M > 8 runs the tensor-core (tcgen05) kernels
+ *     and needs `gwa_workspace_bytes(M, K)` bytes of device workspace, which
+ *     the call overwrites; calls sharing one workspace must not overlap on
+ *     the GPU.
+ *   - Return value: GWA_OK or an error code; nothing aborts, traps or exits.
+ *     On error nothing was enqueued and gwa_last_error() (thread-local) holds
+ *     one line of text.  Errors raised by the GPU while the work runs surface
+ *     from the next CUDA call that observes them, as usual for CUDA.
+ */
+#ifndef GWA_H_
+#define GWA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    GWA_OK = 0,
+    GWA_ERR_INVALID_ARG = 1, /* null pointer, bad size, sizes not adding up */
+    GWA_ERR_UNSUPPORTED = 2, /* bits not in {4,8}, group != 64             */
+    GWA_ERR_MISALIGNED = 3,  /* a pointer breaks the alignment rules       */
+    GWA_ERR_CUDA = 4,        /* launch failed or no usable sm_103a device   */
+    GWA_ERR_WORKSPACE = 5    /* M > 8 and the workspace is null or small    */
+};
+
+/* One packed weight of N output rows and K inputs.
+ *   wq:     uint32 [N, K*bits/32]
+ *   scales: bf16   [N, K/group]
+ *   biases: bf16   [N, K/group]                                          */
+typedef struct gwa_qweight {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *biases;
+    int64_t N;
+    int64_t K;
+    int32_t bits;
+    int32_t group;
+} gwa_qweight;
+
+/* y[M, N] (bf16) = x[M, K] . dequant(w)^T.
+ * The quantized linear layer itself ("Sanctum-MLX": QuantizedLinear
+ * group_size=64; "The Cathedral Doubled Itself": quantized_matmul). */
+int gwa_qmv_affine(const uint16_t *x, int64_t M, gwa_qweight w, uint16_t *y,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Fused projection over output-axis-concatenated weights, written back as
+ * SEPARATE contiguous buffers.  ("The Cathedral Doubled Itself", "The two
+ * fusions" and "The trap that ate three hours": one quantized_matmul over
+ * [q_out + 2*kv_out, hidden/8], split on the last axis; split views with a
+ * non-zero offset and the parent's strides corrupted RoPE, so every section
+ * here is its own offset-0 row-major buffer.)
+ *   w.N == sum(section_sizes[0 .. n_sections-1]); 1 <= n_sections <= 8.
+ *   outs[s]:     device bf16 [M, section_sizes[s]], contiguous; rows
+ *                [start_s, start_s + size_s) of the fused weight land there.
+ *   out_bias:    NULL, or a host array of n_sections device pointers (each
+ *                NULL or bf16 [section_sizes[s]]) added to that section's
+ *                output in fp32 before rounding (the additive q/k/v bias of
+ *                the qwen2 layout).
+ * The buffers must not overlap each other or x. */
+int gwa_qmv_fused_sections(const uint16_t *x, int64_t M, gwa_qweight w,
+                           int32_t n_sections, const int64_t *section_sizes,
+                           uint16_t *const *outs,
+                           const uint16_t *const *out_bias, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* Fused gate+up projection with the SwiGLU epilogue.  ("The Cathedral
+ * Doubled Itself", "The two fusions", Phase 1B: gate_proj and up_proj fused
+ * the same way, ahead of SiLU and the multiply; no additive bias.)
+ *   w has 2*I rows: rows [0, I) are gate_proj, rows [I, 2I) are up_proj.
+ *   h[M, I] (bf16) = SiLU(g) * u with g, u the fp32 projections and
+ *   SiLU(g) = g / (1 + exp(-g)), rounded to bf16 once. */
+int gwa_qmv_gate_up_silu(const uint16_t *x, int64_t M, gwa_qweight w,
+                         uint16_t *h, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Workspace bytes the three dense entry points need for M tokens of K
+ * inputs (0 when M <= 8). */
+size_t gwa_workspace_bytes(int64_t M, int64_t K);
+
+enum { GWA_MOE_GATE_UP_SILU = 0, GWA_MOE_DOWN_COMBINE = 1 };
+
+/* Top-k MoE expert projection over stacked expert weights ("Sanctum-MLX":
+ * 3-D switch_mlp expert grids; "Four Candles For The Cathedral", "What's not
+ * in this batch": per-expert gate_proj/up_proj of the routed experts).
+ *   w: stacked experts -- expert e owns rows [e*w.N, (e+1)*w.N) of wq,
+ *      scales and biases, i.e. wq is [num_experts, w.N, K*bits/32].
+ *   expert_ids: device int32 [M, topk].
+ *   mode GWA_MOE_GATE_UP_SILU: x is [M, K]; each expert's w.N = 2*I rows are
+ *      [gate; up]; out[M, topk, I] (bf16) = SiLU(Wg[e] x_t) * (Wu[e] x_t)
+ *      for e = expert_ids[t, j].  route_w is ignored (may be NULL).
+ *   mode GWA_MOE_DOWN_COMBINE: x is [M, topk, K] (one input per slot, e.g.
+ *      the gate+up output); route_w is device fp32 [M, topk];
+ *      out[M, w.N] (bf16) = sum_j route_w[t,j] * (W[e] x[t,j]), in fp32.
+ *   Each distinct expert is streamed from memory once per call, however many
+ *   tokens chose it.  1 <= M <= 8 and 1 <= topk <= 32.
+ *   status: NULL, or a device int32 the kernels set to 1 (atomic OR) when an
+ *      expert id lies outside [0, num_experts); such a slot contributes zero
+ *      (gate+up mode writes zeros for it).  The caller clears it. */
+int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
+                       const int32_t *expert_ids, const float *route_w,
+                       gwa_qweight w, int32_t num_experts, int32_t mode,
+                       uint16_t *out, int32_t *status, void *stream);
+
+/* Text of the last error raised on this thread ("" if none). */
+const char *gwa_last_error(void);
+
+/* Test exports.  codes[N, K] (uint8) = q[n,k]; wf[N, K] (fp32) =
+ * fmaf(scale, (float)q, bias): the dequantized weight rounded once to fp32.
+ * Both are written on `stream`; the caller owns codes / wf. */
+int gwa_debug_unpack(gwa_qweight w, uint8_t *codes, void *stream);
+int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GWA_H_ */
