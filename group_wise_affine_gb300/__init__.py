@@ -37,7 +37,7 @@ GWA_MOE_DOWN_COMBINE = 1
 
 EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
-           "gwa_debug_unpack", "gwa_debug_dequant")
+           "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant")
 
 
 class GwaError(RuntimeError):
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH):
                                        vp, vp]
     lib.gwa_last_error.argtypes = []
     lib.gwa_last_error.restype = ctypes.c_char_p
+    lib.gwa_pipeline_status.argtypes = [vp, i32]
+    lib.gwa_pipeline_status.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
     lib.gwa_debug_dequant.argtypes = [_QW, vp, vp]
     for f in ("gwa_qmv_affine", "gwa_qmv_fused_sections",
@@ -95,6 +97,14 @@ def load(path: str = LIB_PATH):
 
 def last_error() -> str:
     return load().gwa_last_error().decode()
+
+
+def pipeline_status(reset: bool = True) -> int:
+    """Pipeline waits that ran out of time since the last reset (synchronizes
+    the device)."""
+    out = ctypes.c_uint32(0)
+    _check(load().gwa_pipeline_status(ctypes.byref(out), int(reset)))
+    return int(out.value)
 
 
 def _check(rc: int) -> None:

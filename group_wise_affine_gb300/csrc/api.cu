@@ -191,7 +191,9 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         } else {
             q.y = p.y + t0 * out_stride;
         }
-        cudaError_t e = launch_dense(mode, q, st);
+        bool used = false;
+        cudaError_t e = launch_stream(mode, q, st, &used);
+        if (e == cudaSuccess && !used) e = launch_dense(mode, q, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     return GWA_OK;
@@ -204,6 +206,16 @@ using namespace gwa;
 extern "C" {
 
 const char *gwa_last_error(void) { return g_last_error.c_str(); }
+
+int gwa_pipeline_status(uint32_t *timeouts, int32_t reset) {
+    g_last_error.clear();
+    if (!timeouts) return fail(GWA_ERR_INVALID_ARG, "gwa_pipeline_status: null");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "gwa_pipeline_status");
+    *timeouts = stream_timeouts(reset != 0);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, "gwa_pipeline_status");
+}
 
 size_t gwa_workspace_bytes(int64_t M, int64_t K) {
     if (M <= 8 || K <= 0) return 0;

@@ -27,7 +27,7 @@ constexpr int kGroup = 64;
 constexpr int kWarp = 32;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    return __uint_as_float(static_cast<uint32_t>(h) * 65536u);
 }
 // The two bf16 halves of a 32-bit word, widened exactly.
 __device__ __forceinline__ float bf16_lo(uint32_t v) {
@@ -66,21 +66,26 @@ constexpr float kU4Even = 16.0f;
 //   p[0] = (256+q3, 16+q4)   p[1] = (256+q5, 16+q6)
 //   p[2] = (256+q1, 16+q2)   p[3] = (256+q7, 16+q0)
 // Activations are stored in the matching order x3 x4 x5 x6 | x1 x2 x7 x0.
+// The shifts are written as multiplies so they run on the FMA pipe (the
+// logic pipe, which executes the eight AND-ORs, is half rate); one 64-bit
+// product yields both w << 19 (low word) and w >> 13 (high word).
 __device__ __forceinline__ void unpack_u4(uint32_t w, float2 (&p)[4]) {
     const uint32_t lo_mask = 0x00078000u, lo_magic = 0x43800000u;  // 2^8
     const uint32_t hi_mask = 0x00780000u, hi_magic = 0x41800000u;  // 2^4
-    uint32_t t0 = w << 3;                       // q3 -> [15,19), q4 -> [19,23)
-    uint32_t t1 = w >> 5;                       // q5, q6
-    uint32_t t2 = w << 11;                      // q1, q2
-    uint32_t t3 = __funnelshift_l(w, w, 19);    // q7 -> [15,19), q0 -> [19,23)
+    const uint32_t t0 = w * 8u;                  // q3 -> [15,19), q4 -> [19,23)
+    const uint32_t t1 = __umulhi(w, 1u << 27);   // w >> 5: q5, q6
+    const uint32_t t2 = w * 2048u;               // w << 11: q1, q2
+    const unsigned long long t3 = (unsigned long long)w * (1ull << 19);
+    const uint32_t t3lo = (uint32_t)t3;          // q0 -> [19,23)
+    const uint32_t t3hi = (uint32_t)(t3 >> 32);  // q7 -> [15,19)
     p[0] = make_float2(__uint_as_float((t0 & lo_mask) | lo_magic),
                        __uint_as_float((t0 & hi_mask) | hi_magic));
     p[1] = make_float2(__uint_as_float((t1 & lo_mask) | lo_magic),
                        __uint_as_float((t1 & hi_mask) | hi_magic));
     p[2] = make_float2(__uint_as_float((t2 & lo_mask) | lo_magic),
                        __uint_as_float((t2 & hi_mask) | hi_magic));
-    p[3] = make_float2(__uint_as_float((t3 & lo_mask) | lo_magic),
-                       __uint_as_float((t3 & hi_mask) | hi_magic));
+    p[3] = make_float2(__uint_as_float((t3hi & lo_mask) | lo_magic),
+                       __uint_as_float((t3lo & hi_mask) | hi_magic));
 }
 // Position of the activation that pairs with slot i of the unpacked word.
 __device__ __forceinline__ int u4_perm(int i) {
@@ -92,12 +97,13 @@ __device__ __forceinline__ int u4_perm(int i) {
 constexpr float kU8Const = 256.0f;
 
 // Four 8-bit codes of one word -> two pairs (256+q0, 256+q1), (256+q2, 256+q3).
+// Shifts as multiplies, as for u4.
 __device__ __forceinline__ void unpack_u8(uint32_t w, float2 (&p)[2]) {
     const uint32_t mask = 0x007f8000u, magic = 0x43800000u;  // [15,23), 2^8
-    p[0] = make_float2(__uint_as_float(((w << 15) & mask) | magic),
-                       __uint_as_float(((w << 7) & mask) | magic));
-    p[1] = make_float2(__uint_as_float(((w >> 1) & mask) | magic),
-                       __uint_as_float(((w >> 9) & mask) | magic));
+    p[0] = make_float2(__uint_as_float(((w * 32768u) & mask) | magic),
+                       __uint_as_float(((w * 128u) & mask) | magic));
+    p[1] = make_float2(__uint_as_float((__umulhi(w, 1u << 31) & mask) | magic),
+                       __uint_as_float((__umulhi(w, 1u << 23) & mask) | magic));
 }
 
 template <int BITS>
@@ -117,6 +123,199 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+}  // namespace gwa
+
+// ---------------------------------------------------------------- integer dot
+namespace gwa {
+// The decode kernels form each group's sum of code x activation as an exact
+// integer.  Activations are encoded per group of 64 as int16 with a
+// power-of-two scale 2^E chosen from the group's largest exponent (the
+// largest magnitude maps into [2^14, 2^15)).  A bf16 value carries 8
+// significant bits, so every value within 2^7 of the group's largest
+// exponent is represented exactly; smaller ones round to the group's quantum
+// (at most 2^-15 of the largest magnitude).  Codes stay unsigned bytes, and
+// dp2a forms two 16x8-bit products per instruction into an int32 (at most
+// 64 * 255 * 32640 < 2^31 per group).  Per group:
+//   y += (scale * 2^E) * D + bias * sum_k x_k,   D = sum_k q_k * xi_k.
+__device__ __forceinline__ int dp2a_lo(uint32_t a16, uint32_t b8, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a16), "r"(b8), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a16, uint32_t b8, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a16), "r"(b8), "r"(c));
+    return d;
+}
+
+// Exponent field (biased, 0..255) of an fp32 value.
+__device__ __forceinline__ int f32_exp_field(float v) {
+    return (int)((__float_as_uint(v) >> 23) & 0xffu);
+}
+
+// Scale of a group whose largest exponent field is ef: f = 2^E and 1/f.
+// Groups whose magnitudes all lie below 2^-112 are encoded as zero (their
+// contribution is below 64 * 2^-112 * |w|); their plain sum still feeds the
+// bias term.
+__device__ __forceinline__ void group_scale(int ef, float &f, float &finv) {
+    if (ef < 15) {
+        f = 0.f;
+        finv = 0.f;
+    } else {
+        f = __uint_as_float((uint32_t)(ef - 14) << 23);      // 2^(ef-141)
+        finv = __uint_as_float((uint32_t)(268 - ef) << 23);  // 2^(141-ef)
+    }
+}
+
+// int16 pair (lo = a, hi = b) of two activations already multiplied by 1/f.
+__device__ __forceinline__ uint32_t i16_pair(float a, float b) {
+    return ((uint32_t)__float2int_rn(a) & 0xffffu) |
+           ((uint32_t)__float2int_rn(b) << 16);
+}
+
+// u4: the four int16 pairs of one word's activations, in dp2a order:
+//   (x0,x2) (x4,x6) (x1,x3) (x5,x7)  [x scaled by finv]
+__device__ __forceinline__ void u4_pairs(const float *v, float finv,
+                                         uint32_t (&pr)[4]) {
+    pr[0] = i16_pair(v[0] * finv, v[2] * finv);
+    pr[1] = i16_pair(v[4] * finv, v[6] * finv);
+    pr[2] = i16_pair(v[1] * finv, v[3] * finv);
+    pr[3] = i16_pair(v[5] * finv, v[7] * finv);
+}
+// u8: the two pairs of one word: (x0,x1) (x2,x3).
+__device__ __forceinline__ void u8_pairs(const float *v, float finv,
+                                         uint32_t (&pr)[2]) {
+    pr[0] = i16_pair(v[0] * finv, v[1] * finv);
+    pr[1] = i16_pair(v[2] * finv, v[3] * finv);
+}
+
+// Integer dot of one packed word with its activation pairs.
+__device__ __forceinline__ int word_dot_u4(uint32_t w, const uint32_t *pr,
+                                           int acc) {
+    const uint32_t lo = w & 0x0f0f0f0fu;          // q0 q2 q4 q6
+    const uint32_t hi = (w >> 4) & 0x0f0f0f0fu;   // q1 q3 q5 q7
+    acc = dp2a_lo(pr[0], lo, acc);
+    acc = dp2a_hi(pr[1], lo, acc);
+    acc = dp2a_lo(pr[2], hi, acc);
+    return dp2a_hi(pr[3], hi, acc);
+}
+__device__ __forceinline__ int word_dot_u8(uint32_t w, const uint32_t *pr,
+                                           int acc) {
+    acc = dp2a_lo(pr[0], w, acc);
+    return dp2a_hi(pr[1], w, acc);
+}
+
+}  // namespace gwa
+
+// ---------------------------------------------------------------- async copy
+// mbarrier + bulk-copy helpers (sm_90+ PTX).  Every wait is bounded by the
+// global timer: after kWaitLimitNs the wait gives up and reports failure, so
+// a broken pipeline returns an error instead of hanging the GPU.
+namespace gwa {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// Contiguous global -> shared copy completing on `bar` (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
+                                         uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Recursive-halving transpose reduction of V values (V a power of two, at
+// most 32) across the 32 lanes of a warp.  Afterwards lane l holds the
+// warp-wide sum of value index (l >> (5 - log2 V)), and lanes whose low
+// (5 - log2 V) bits are zero hold each index once.  Costs 31 shuffles in
+// total for V = 32 instead of 5 per value.
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
+    static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V");
+#pragma unroll
+    for (int half = V / 2, bit = 16; half >= 1; half /= 2, bit /= 2) {
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const bool up = (lane & bit) != 0;
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int bit = 16 / V; bit >= 1; bit /= 2)
+        r += __shfl_xor_sync(0xffffffffu, r, bit);
+    return r;
 }
 
 }  // namespace gwa

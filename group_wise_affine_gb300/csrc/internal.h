@@ -15,6 +15,10 @@ constexpr size_t kDenseF32StageMax = 96 * 1024;
 // limit (227 KB) less room for the kernels' static arrays.
 constexpr size_t kMaxDynSmem = 216 * 1024;
 constexpr int kMaxSections = 8;
+// Streaming decode kernel: largest CTA, and the shared-memory ring size it
+// aims for per CTA.
+constexpr int kStreamMaxThreads = 512;
+constexpr size_t kStreamRingTarget = 72 * 1024;
 
 struct DenseParams {
     const uint16_t *x;   // [M, K] bf16
@@ -36,12 +40,35 @@ struct DenseParams {
     const uint16_t *sec_bias[kMaxSections];
 };
 
+// Launches `kernel` on `st` with programmatic stream serialization: it may
+// start while the previous kernel in the stream drains; the kernel itself
+// waits (griddepcontrol.wait) before touching anything that kernel wrote.
+template <typename... Args>
+cudaError_t launch_pdl(const void *kernel, unsigned grid, unsigned threads,
+                       size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *argv[] = {reinterpret_cast<void *>(&args)...};
+    return cudaLaunchKernelExC(&cfg, kernel, argv);
+}
+
 // Blocks for a persistent grid: SMs x resident CTAs of `kernel`.
 cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
                            int *grid);
 int num_sms();
 
 cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st);
+cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
+                          bool *used);
+unsigned int stream_timeouts(bool reset);
 int dense_max_tokens(int bits, int nch);
 
 struct MoeParams {

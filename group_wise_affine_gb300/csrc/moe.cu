@@ -21,13 +21,13 @@
 
 namespace gwa {
 
-constexpr int kMoeThreads = 512;
+constexpr int kMoeThreads = 256;
 constexpr int kMoeDownThreads = 256;
 constexpr int kMoeMaxSlots = 256;
 constexpr int kMoeRP = 2;  // gate/up row pairs per warp
 
 // ------------------------------------------------------------ gate + up
-template <int BITS, int MT, bool XF32>
+template <int BITS, int MT>
 __device__ __forceinline__ void moe_gate_up_body(const MoeParams &p,
                                                  const WView &v,
                                                  const int *list, int mt,
@@ -47,7 +47,7 @@ __device__ __forceinline__ void moe_gate_up_body(const MoeParams &p,
 #pragma unroll
     for (int m = 0; m < MT; ++m) midx[m] = m;
     float acc[R][MT];
-    rows_dot<BITS, MT, R, XF32>(v, rows, midx, MT, xs, lane, acc);
+    rows_dot<BITS, MT, R>(v, rows, midx, MT, xs, lane, acc);
     warp_reduce<R, MT>(acc);
 #pragma unroll
     for (int r = 0; r < kMoeRP; ++r)
@@ -60,7 +60,7 @@ __device__ __forceinline__ void moe_gate_up_body(const MoeParams &p,
         }
 }
 
-template <int BITS, bool XF32>
+template <int BITS>
 __global__ void __launch_bounds__(kMoeThreads)
     moe_gate_up_kernel(MoeParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -104,30 +104,29 @@ __global__ void __launch_bounds__(kMoeThreads)
     const WView v{reinterpret_cast<const uint4 *>(p.wq) + e * p.N * p.nch,
                   p.sc + e * p.N * p.G, p.bi + e * p.N * p.G, p.nch, p.G};
     const int cnt = s_cnt;
-    for (int base = 0; base < cnt; base += 8) {
-        const int mt = min(8, cnt - base);
-        const int mtb = mt <= 1 ? 1 : mt <= 2 ? 2 : mt <= 4 ? 4 : 8;
+    // tokens of this expert in passes of at most four
+    for (int base = 0; base < cnt; base += 4) {
+        const int mt = min(4, cnt - base);
+        const int mtb = mt <= 1 ? 1 : mt <= 2 ? 2 : 4;
         if (threadIdx.x < 8)
             tok[threadIdx.x] =
                 threadIdx.x < mt ? list[base + threadIdx.x] / p.topk : -1;
         __syncthreads();
-        stage_x<BITS, XF32>(p.x, p.K, tok, mtb, p.nch, smem);
+        stage_x<BITS>(p.x, p.K, tok, mtb, p.nch, smem);
         __syncthreads();
         const int *l = list + base;
         if (mtb == 1)
-            moe_gate_up_body<BITS, 1, XF32>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 1>(p, v, l, mt, i0, smem);
         else if (mtb == 2)
-            moe_gate_up_body<BITS, 2, XF32>(p, v, l, mt, i0, smem);
-        else if (mtb == 4)
-            moe_gate_up_body<BITS, 4, XF32>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 2>(p, v, l, mt, i0, smem);
         else
-            moe_gate_up_body<BITS, 8, XF32>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 4>(p, v, l, mt, i0, smem);
         __syncthreads();
     }
 }
 
 // ------------------------------------------------------------ down + combine
-template <int BITS, bool XF32, int L, int D>
+template <int BITS, int L, int D>
 __global__ void __launch_bounds__(kMoeDownThreads)
     moe_down_kernel(MoeParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(kMoeDownThreads)
         for (int s = f; s < t; ++s) rank += (s_first[s] == f);
         s_order[s_gstart[s_gidx[f]] + rank] = t;
     }
-    stage_x<BITS, XF32>(p.x, p.K, s_tok, S, p.nch, smem);
+    stage_x<BITS>(p.x, p.K, s_tok, S, p.nch, smem);
     __syncthreads();
 
     const int lane = t & 31, warp = t >> 5;
@@ -199,7 +198,7 @@ __global__ void __launch_bounds__(kMoeDownThreads)
     const int64_t rows[1] = {row < p.N ? row : -1};
     const int cpl = (p.nch + L - 1) / L;
     const int nitems = s_ng * cpl;
-    const float2 *sums = x_sums<BITS, XF32>(smem, S, p.nch);
+    const float2 *aux = x_aux<BITS>(smem, S, p.nch);
 
     float acc[8];
 #pragma unroll
@@ -235,8 +234,8 @@ __global__ void __launch_bounds__(kMoeDownThreads)
                     const int s = s_order[q];
                     const int midx[1] = {s};
                     float part[1][1] = {{0.f}};
-                    chunk_fma<BITS, 1, 1, XF32>(ring[k], c, p.nch, midx, sums,
-                                                smem, part);
+                    chunk_fma<BITS, 1, 1>(ring[k], c, p.nch, midx, aux, smem,
+                                          part);
                     const int tk = s / p.topk;
                     const float v = s_rw[s] * part[0][0];
 #pragma unroll
@@ -257,38 +256,33 @@ __global__ void __launch_bounds__(kMoeDownThreads)
 
 // ------------------------------------------------------------ host side
 template <int BITS>
-static size_t gate_up_stage_bytes(int nch, bool *xf32) {
-    const size_t f = XStage<BITS, true>::bytes(8, nch);
-    *xf32 = f <= kDenseF32StageMax;
-    return *xf32 ? f : XStage<BITS, false>::bytes(8, nch);
+static size_t gate_up_stage_bytes(int nch) {
+    return XStage<BITS>::bytes(4, nch);
 }
 
 template <int BITS>
-static size_t down_stage_bytes(int S, int nch, bool *xf32) {
-    const size_t f = XStage<BITS, true>::bytes(S, nch);
-    *xf32 = f <= kDenseF32StageMax;
-    return *xf32 ? f : XStage<BITS, false>::bytes(S, nch);
+static size_t down_stage_bytes(int S, int nch) {
+    return XStage<BITS>::bytes(S, nch);
 }
 
 int moe_max_tokens(int bits, int nch, int mode) {
     // largest slot count (down) / token bucket (gate+up) whose staging fits
-    bool f;
     if (mode == 0) {
-        size_t b = bits == 4 ? gate_up_stage_bytes<4>(nch, &f)
-                             : gate_up_stage_bytes<8>(nch, &f);
+        const size_t b = bits == 4 ? gate_up_stage_bytes<4>(nch)
+                                   : gate_up_stage_bytes<8>(nch);
         return b <= kMaxDynSmem ? kMoeMaxSlots : 0;
     }
     int S = kMoeMaxSlots;
-    while (S > 0 && (bits == 4 ? down_stage_bytes<4>(S, nch, &f)
-                               : down_stage_bytes<8>(S, nch, &f)) > kMaxDynSmem)
+    while (S > 0 && (bits == 4 ? down_stage_bytes<4>(S, nch)
+                               : down_stage_bytes<8>(S, nch)) > kMaxDynSmem)
         --S;
     return S;
 }
 
-template <int BITS, bool XF32>
-static cudaError_t launch_gu(const MoeParams &p, size_t smem,
-                             cudaStream_t st) {
-    auto kern = moe_gate_up_kernel<BITS, XF32>;
+template <int BITS>
+static cudaError_t launch_gu(const MoeParams &p, cudaStream_t st) {
+    auto kern = moe_gate_up_kernel<BITS>;
+    const size_t smem = gate_up_stage_bytes<BITS>(p.nch);
     int dummy;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    kMoeThreads, smem, &dummy);
@@ -302,19 +296,13 @@ static cudaError_t launch_gu(const MoeParams &p, size_t smem,
 }
 
 cudaError_t launch_moe_gate_up(const MoeParams &p, cudaStream_t st) {
-    bool f;
-    if (p.bits == 4) {
-        const size_t b = gate_up_stage_bytes<4>(p.nch, &f);
-        return f ? launch_gu<4, true>(p, b, st) : launch_gu<4, false>(p, b, st);
-    }
-    const size_t b = gate_up_stage_bytes<8>(p.nch, &f);
-    return f ? launch_gu<8, true>(p, b, st) : launch_gu<8, false>(p, b, st);
+    return p.bits == 4 ? launch_gu<4>(p, st) : launch_gu<8>(p, st);
 }
 
-template <int BITS, bool XF32, int L>
-static cudaError_t launch_dn(const MoeParams &p, size_t smem,
-                             cudaStream_t st) {
-    auto kern = moe_down_kernel<BITS, XF32, L, 8>;
+template <int BITS, int L>
+static cudaError_t launch_dn(const MoeParams &p, cudaStream_t st) {
+    auto kern = moe_down_kernel<BITS, L, 8>;
+    const size_t smem = down_stage_bytes<BITS>(p.M * p.topk, p.nch);
     int dummy;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    kMoeDownThreads, smem, &dummy);
@@ -325,24 +313,15 @@ static cudaError_t launch_dn(const MoeParams &p, size_t smem,
     return cudaGetLastError();
 }
 
-template <int BITS, bool XF32>
-static cudaError_t launch_dn_l(const MoeParams &p, size_t smem,
-                               cudaStream_t st) {
-    if (p.nch >= 32) return launch_dn<BITS, XF32, 32>(p, smem, st);
-    if (p.nch >= 16) return launch_dn<BITS, XF32, 16>(p, smem, st);
-    return launch_dn<BITS, XF32, 8>(p, smem, st);
+template <int BITS>
+static cudaError_t launch_dn_l(const MoeParams &p, cudaStream_t st) {
+    if (p.nch >= 32) return launch_dn<BITS, 32>(p, st);
+    if (p.nch >= 16) return launch_dn<BITS, 16>(p, st);
+    return launch_dn<BITS, 8>(p, st);
 }
 
 cudaError_t launch_moe_down(const MoeParams &p, cudaStream_t st) {
-    bool f;
-    const int S = p.M * p.topk;
-    if (p.bits == 4) {
-        const size_t b = down_stage_bytes<4>(S, p.nch, &f);
-        return f ? launch_dn_l<4, true>(p, b, st)
-                 : launch_dn_l<4, false>(p, b, st);
-    }
-    const size_t b = down_stage_bytes<8>(S, p.nch, &f);
-    return f ? launch_dn_l<8, true>(p, b, st) : launch_dn_l<8, false>(p, b, st);
+    return p.bits == 4 ? launch_dn_l<4>(p, st) : launch_dn_l<8>(p, st);
 }
 
 }  // namespace gwa

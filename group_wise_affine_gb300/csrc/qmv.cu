@@ -22,7 +22,7 @@ namespace gwa {
 
 enum DenseMode { kPlain = 0, kSections = 1, kGateUp = 2 };
 
-template <int BITS, int MT, int R, bool XF32, int MODE>
+template <int BITS, int MT, int R, int MODE>
 __global__ void __launch_bounds__(kDenseThreads)
     qmv_dense_kernel(DenseParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kDenseThreads)
     if (threadIdx.x < 8)
         tok[threadIdx.x] = (int)threadIdx.x < p.M ? (int)threadIdx.x : -1;
     __syncthreads();
-    stage_x<BITS, XF32>(p.x, p.K, tok, MT, p.nch, smem);
+    stage_x<BITS>(p.x, p.K, tok, MT, p.nch, smem);
     __syncthreads();
 
     const int lane = threadIdx.x & (kWarp - 1);
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kDenseThreads)
 #pragma unroll
         for (int m = 0; m < MT; ++m) midx[m] = m;
         float acc[R][MT];
-        rows_dot<BITS, MT, R, XF32>(v, rows, midx, MT, smem, lane, acc);
+        rows_dot<BITS, MT, R>(v, rows, midx, MT, smem, lane, acc);
         warp_reduce<R, MT>(acc);
 
 #pragma unroll
@@ -85,10 +85,10 @@ __global__ void __launch_bounds__(kDenseThreads)
 }
 
 // ------------------------------------------------------------ host side
-template <int BITS, int MT, int R, bool XF32, int MODE>
+template <int BITS, int MT, int R, int MODE>
 static cudaError_t launch_dense_t(const DenseParams &p, cudaStream_t st) {
-    auto kern = qmv_dense_kernel<BITS, MT, R, XF32, MODE>;
-    const size_t smem = XStage<BITS, XF32>::bytes(MT, p.nch);
+    auto kern = qmv_dense_kernel<BITS, MT, R, MODE>;
+    const size_t smem = XStage<BITS>::bytes(MT, p.nch);
     int grid = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    kDenseThreads, smem, &grid);
@@ -102,32 +102,25 @@ static cudaError_t launch_dense_t(const DenseParams &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <int BITS, int MT, int R, int MODE>
-static cudaError_t launch_dense_x(const DenseParams &p, cudaStream_t st) {
-    if (XStage<BITS, true>::bytes(MT, p.nch) <= kDenseF32StageMax)
-        return launch_dense_t<BITS, MT, R, true, MODE>(p, st);
-    return launch_dense_t<BITS, MT, R, false, MODE>(p, st);
-}
-
 template <int BITS, int MODE>
 static cudaError_t launch_dense_m(const DenseParams &p, cudaStream_t st) {
     // gate+up uses R/2 gate rows + R/2 up rows per warp block
-    if (p.M <= 1) return launch_dense_x<BITS, 1, 4, MODE>(p, st);
-    if (p.M <= 2) return launch_dense_x<BITS, 2, 4, MODE>(p, st);
-    if (p.M <= 4) return launch_dense_x<BITS, 4, 4, MODE>(p, st);
-    return launch_dense_x<BITS, 8, 2, MODE>(p, st);
+    if (p.M <= 1) return launch_dense_t<BITS, 1, 4, MODE>(p, st);
+    if (p.M <= 2) return launch_dense_t<BITS, 2, 4, MODE>(p, st);
+    if (p.M <= 4) return launch_dense_t<BITS, 4, 4, MODE>(p, st);
+    return launch_dense_t<BITS, 8, 2, MODE>(p, st);
 }
 
 // Largest token count per launch whose staged activations fit in shared
-// memory (bf16 staging).
+// memory.
 int dense_max_tokens(int bits, int nch) {
     const size_t cap = kMaxDynSmem;
     int mt = 8;
-    while (mt > 1 && (bits == 4 ? XStage<4, false>::bytes(mt, nch)
-                                : XStage<8, false>::bytes(mt, nch)) > cap)
+    while (mt > 1 && (bits == 4 ? XStage<4>::bytes(mt, nch)
+                                : XStage<8>::bytes(mt, nch)) > cap)
         mt /= 2;
-    const size_t one = bits == 4 ? XStage<4, false>::bytes(1, nch)
-                                 : XStage<8, false>::bytes(1, nch);
+    const size_t one = bits == 4 ? XStage<4>::bytes(1, nch)
+                                 : XStage<8>::bytes(1, nch);
     return one > cap ? 0 : mt;
 }
 

@@ -4,12 +4,12 @@
 //
 // Work split: a warp owns a block of R weight rows; its 32 lanes walk the
 // 16-byte chunks of those rows (chunk c = lane, lane+32, ...), so each warp
-// load instruction moves 512 contiguous bytes per row.  A lane unpacks each
-// word once per row and reuses it for every token; it reads the staged
-// activations of a chunk once and reuses them for all R rows.  Per chunk the
-// lane keeps fp32 pair accumulators, removes the magic constants with the
-// precomputed chunk sums and applies the group's scale and bias:
-//   y += s * (sum_k x_k f_k - sum_k C_k x_k) + b * sum_k x_k.
+// load instruction moves 512 contiguous bytes per row.  A lane splits each
+// word into code bytes once per row and reuses them for every token; it reads
+// the staged activations of a chunk once and reuses them for all R rows.
+// Per chunk the lane forms exact integer dots (dp2a) and applies the group's
+// scale and bias in fp32 (see common.cuh):
+//   y += (s * 2^E) * D + b * sum_k x_k.
 // Lanes are reduced with warp shuffles at the end of the row block.
 #pragma once
 
@@ -18,42 +18,43 @@
 namespace gwa {
 
 // ------------------------------------------------------------ staging
-// Shared-memory image of the activations of `mt` tokens, chunk-major so that
-// the 32 lanes of a warp read 32 consecutive 16-byte slots:
-//   XF32:  float4 q[m][e][c], e < kChunkCodes/4  (fp32, in unpack order)
-//   bf16:  uint4  q[m][e][c], e < kChunkCodes/8  (bf16 pairs, unpack order)
-// followed by float2 sums[m][c] = (sum_k C_k x_k, sum_k x_k) per chunk.
-template <int BITS, bool XF32>
+// Shared-memory image of the activations of `mt` tokens, encoded for the
+// integer dot (int16 pairs in dp2a order, see common.cuh), chunk-major so
+// that the 32 lanes of a warp read 32 consecutive 16-byte slots:
+//   uint4 q[m][e][c], e < kChunkCodes/8
+// followed by float2 aux[m][c] = (group scale 2^E, sum of the chunk's x).
+template <int BITS>
 struct XStage {
-    static constexpr int kQuads =
-        XF32 ? Fmt<BITS>::kChunkCodes / 4 : Fmt<BITS>::kChunkCodes / 8;
+    static constexpr int kQuads = Fmt<BITS>::kChunkCodes / 8;
     static __host__ __device__ size_t bytes(int mt, int nch) {
         return (size_t)mt * nch * (16 * kQuads + sizeof(float2));
     }
 };
 
 // Stage tokens `tok[0..mt)` (rows of x, K = nch * chunk codes) into shared
-// memory; token slots with tok[m] < 0 are zero-filled.  Called by the whole
-// CTA; the caller synchronizes afterwards.
-template <int BITS, bool XF32>
+// memory; token slots with tok[m] < 0 are zero-filled.  One item per
+// (token, group of 64).  Called by the whole CTA; the caller synchronizes.
+template <int BITS>
 __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
                                         int64_t x_row_stride,
                                         const int *tok, int mt, int nch,
                                         unsigned char *smem) {
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
-    constexpr int Q = XStage<BITS, XF32>::kQuads;
-    float2 *sums = reinterpret_cast<float2 *>(
-        smem + (size_t)mt * nch * Q * 16);
-    const int items = mt * nch;
+    constexpr int CPG = kGroup / CODES;  // chunks per group
+    constexpr int Q = XStage<BITS>::kQuads;
+    uint4 *q = reinterpret_cast<uint4 *>(smem);
+    float2 *aux = reinterpret_cast<float2 *>(smem + (size_t)mt * nch * Q * 16);
+    const int G = nch / CPG;
+    const int items = mt * G;
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int m = it / nch, c = it - m * nch;
-        float v[CODES];
+        const int m = it / G, g = it - m * G;
+        float v[kGroup];
         if (tok[m] >= 0) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                x + (int64_t)tok[m] * x_row_stride + (int64_t)c * CODES);
+                x + (int64_t)tok[m] * x_row_stride + (int64_t)g * kGroup);
 #pragma unroll
-            for (int i = 0; i < CODES / 8; ++i) {
-                uint4 u = src[i];
+            for (int i = 0; i < kGroup / 8; ++i) {
+                const uint4 u = src[i];
                 v[8 * i + 0] = bf16_lo(u.x);
                 v[8 * i + 1] = bf16_hi(u.x);
                 v[8 * i + 2] = bf16_lo(u.y);
@@ -65,99 +66,70 @@ __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < CODES; ++i) v[i] = 0.f;
+            for (int i = 0; i < kGroup; ++i) v[i] = 0.f;
         }
-        // values in unpack order
-        float o[CODES];
-        float csum = 0.f, xsum = 0.f;
-        if constexpr (BITS == 4) {
+        int ef = 0;
 #pragma unroll
-            for (int wd = 0; wd < CODES / 8; ++wd)
+        for (int i = 0; i < kGroup; ++i) ef = max(ef, f32_exp_field(v[i]));
+        float f, finv;
+        group_scale(ef, f, finv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[8 * wd + i] = v[8 * wd + u4_perm(i)];
-            float odd = 0.f, even = 0.f;
+        for (int cg = 0; cg < CPG; ++cg) {
+            const int c = g * CPG + cg;
+            const float *vc = v + cg * CODES;
+            uint32_t pr[CODES / 2];
+            float xs = 0.f;
 #pragma unroll
-            for (int i = 0; i < CODES; i += 2) {
-                even += v[i];
-                odd += v[i + 1];
+            for (int wd = 0; wd < 4; ++wd) {
+                if constexpr (BITS == 4) {
+                    uint32_t t[4];
+                    u4_pairs(vc + 8 * wd, finv, t);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pr[4 * wd + i] = t[i];
+                } else {
+                    uint32_t t[2];
+                    u8_pairs(vc + 4 * wd, finv, t);
+                    pr[2 * wd] = t[0];
+                    pr[2 * wd + 1] = t[1];
+                }
             }
-            csum = kU4Odd * odd + kU4Even * even;
-            xsum = odd + even;
-        } else {
 #pragma unroll
-            for (int i = 0; i < CODES; ++i) {
-                o[i] = v[i];
-                xsum += v[i];
-            }
-            csum = kU8Const * xsum;
-        }
-        if constexpr (XF32) {
-            float4 *q = reinterpret_cast<float4 *>(smem);
+            for (int i = 0; i < CODES; ++i) xs += vc[i];
 #pragma unroll
             for (int e = 0; e < Q; ++e)
                 q[((size_t)m * Q + e) * nch + c] =
-                    make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2],
-                                o[4 * e + 3]);
-        } else {
-            uint4 *q = reinterpret_cast<uint4 *>(smem);
-#pragma unroll
-            for (int e = 0; e < Q; ++e) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w4[i] = (uint32_t)f32_to_bf16_bits(o[8 * e + 2 * i]) |
-                            ((uint32_t)f32_to_bf16_bits(o[8 * e + 2 * i + 1])
-                             << 16);
-                q[((size_t)m * Q + e) * nch + c] =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+                    make_uint4(pr[4 * e], pr[4 * e + 1], pr[4 * e + 2],
+                               pr[4 * e + 3]);
+            aux[(size_t)m * nch + c] = make_float2(f, xs);
         }
-        sums[(size_t)m * nch + c] = make_float2(csum, xsum);
     }
 }
 
-// Pairs of staged activations for word `wd` of chunk `c`, token m.
-template <int BITS, bool XF32>
+// Activation pairs of word `wd` of chunk `c`, staged token m.
+template <int BITS>
 __device__ __forceinline__ void x_pairs(const unsigned char *smem, int m,
                                         int nch, int c, int wd,
-                                        float2 (&xp)[BITS == 4 ? 4 : 2]) {
-    constexpr int Q = XStage<BITS, XF32>::kQuads;
-    if constexpr (XF32) {
-        const float4 *q = reinterpret_cast<const float4 *>(smem);
-        if constexpr (BITS == 4) {
-            float4 a = q[((size_t)m * Q + 2 * wd) * nch + c];
-            float4 b = q[((size_t)m * Q + 2 * wd + 1) * nch + c];
-            xp[0] = make_float2(a.x, a.y);
-            xp[1] = make_float2(a.z, a.w);
-            xp[2] = make_float2(b.x, b.y);
-            xp[3] = make_float2(b.z, b.w);
-        } else {
-            float4 a = q[((size_t)m * Q + wd) * nch + c];
-            xp[0] = make_float2(a.x, a.y);
-            xp[1] = make_float2(a.z, a.w);
-        }
+                                        uint32_t (&pr)[BITS == 4 ? 4 : 2]) {
+    constexpr int Q = XStage<BITS>::kQuads;
+    const uint4 *q = reinterpret_cast<const uint4 *>(smem);
+    if constexpr (BITS == 4) {
+        const uint4 a = q[((size_t)m * Q + wd) * nch + c];
+        pr[0] = a.x;
+        pr[1] = a.y;
+        pr[2] = a.z;
+        pr[3] = a.w;
     } else {
-        const uint4 *q = reinterpret_cast<const uint4 *>(smem);
-        if constexpr (BITS == 4) {
-            uint4 a = q[((size_t)m * Q + wd) * nch + c];
-            xp[0] = make_float2(bf16_lo(a.x), bf16_hi(a.x));
-            xp[1] = make_float2(bf16_lo(a.y), bf16_hi(a.y));
-            xp[2] = make_float2(bf16_lo(a.z), bf16_hi(a.z));
-            xp[3] = make_float2(bf16_lo(a.w), bf16_hi(a.w));
-        } else {
-            uint4 a = q[((size_t)m * Q + (wd >> 1)) * nch + c];
-            uint32_t lo = (wd & 1) ? a.z : a.x, hi = (wd & 1) ? a.w : a.y;
-            xp[0] = make_float2(bf16_lo(lo), bf16_hi(lo));
-            xp[1] = make_float2(bf16_lo(hi), bf16_hi(hi));
-        }
+        const uint4 a = q[((size_t)m * Q + (wd >> 1)) * nch + c];
+        pr[0] = (wd & 1) ? a.z : a.x;
+        pr[1] = (wd & 1) ? a.w : a.y;
     }
 }
 
-template <int BITS, bool XF32>
-__device__ __forceinline__ const float2 *x_sums(const unsigned char *smem,
-                                                int mt, int nch) {
+template <int BITS>
+__device__ __forceinline__ const float2 *x_aux(const unsigned char *smem,
+                                               int mt, int nch) {
     return reinterpret_cast<const float2 *>(
-        smem + (size_t)mt * nch * XStage<BITS, XF32>::kQuads * 16);
+        smem + (size_t)mt * nch * XStage<BITS>::kQuads * 16);
 }
 
 // ------------------------------------------------------------ row dots
@@ -199,56 +171,50 @@ __device__ __forceinline__ void load_chunk(const WView &v,
 
 // One 16-byte chunk of R rows against MT staged tokens (stage slots
 // midx[m]); adds the scaled, bias-corrected chunk dot into acc.
-template <int BITS, int MT, int R, bool XF32>
+template <int BITS, int MT, int R>
 __device__ __forceinline__ void chunk_fma(const ChunkRegs<R> &cr, int c,
                                           int nch, const int (&midx)[MT],
-                                          const float2 *sums,
+                                          const float2 *aux,
                                           const unsigned char *xs,
                                           float (&acc)[R][MT]) {
     constexpr int PAIRS = BITS == 4 ? 4 : 2;
-    float2 a2[R][MT];
+    int d[R][MT][2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) a2[r][m] = make_float2(0.f, 0.f);
+        for (int m = 0; m < MT; ++m) d[r][m][0] = d[r][m][1] = 0;
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
-        float2 xp[MT][PAIRS];
+        uint32_t xp[MT][PAIRS];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-            x_pairs<BITS, XF32>(xs, midx[m], nch, c, wd, xp[m]);
+            x_pairs<BITS>(xs, midx[m], nch, c, wd, xp[m]);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint32_t word = wd == 0   ? cr.w[r].x
                                   : wd == 1 ? cr.w[r].y
                                   : wd == 2 ? cr.w[r].z
                                             : cr.w[r].w;
-            float2 p[PAIRS];
-            if constexpr (BITS == 4)
-                unpack_u4(word, p);
-            else
-                unpack_u8(word, p);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int i = 0; i < PAIRS; ++i)
-                    a2[r][m] = __ffma2_rn(p[i], xp[m][i], a2[r][m]);
+                d[r][m][wd & 1] = BITS == 4
+                                      ? word_dot_u4(word, xp[m], d[r][m][wd & 1])
+                                      : word_dot_u8(word, xp[m], d[r][m][wd & 1]);
         }
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const float2 cx = sums[(size_t)midx[m] * nch + c];
+        const float2 fa = aux[(size_t)midx[m] * nch + c];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float d = (a2[r][m].x + a2[r][m].y) - cx.x;
-            acc[r][m] = fmaf(cr.s[r], d, fmaf(cr.b[r], cx.y, acc[r][m]));
-        }
+        for (int r = 0; r < R; ++r)
+            acc[r][m] = fmaf(cr.s[r] * fa.x, (float)(d[r][m][0] + d[r][m][1]),
+                             fmaf(cr.b[r], fa.y, acc[r][m]));
     }
 }
 
 // Partial sums of this lane for R rows and MT staged tokens (not reduced).
 // L lanes share a row: the lane walks chunks (lane % L), +L, ...
-template <int BITS, int MT, int R, bool XF32, int L = kWarp>
+template <int BITS, int MT, int R, int L = kWarp>
 __device__ __forceinline__ void rows_dot(const WView &v,
                                          const int64_t (&rows)[R],
                                          const int (&midx)[MT], int mt_stage,
@@ -260,7 +226,7 @@ __device__ __forceinline__ void rows_dot(const WView &v,
         for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
     int c = lane % L;
     if (c >= v.nch) return;
-    const float2 *sums = x_sums<BITS, XF32>(xs, mt_stage, v.nch);
+    const float2 *aux = x_aux<BITS>(xs, mt_stage, v.nch);
     ChunkRegs<R> cur;
     load_chunk<BITS, R>(v, rows, c, cur);
     while (true) {
@@ -268,7 +234,7 @@ __device__ __forceinline__ void rows_dot(const WView &v,
         const bool more = cn < v.nch;
         ChunkRegs<R> nxt;
         if (more) load_chunk<BITS, R>(v, rows, cn, nxt);
-        chunk_fma<BITS, MT, R, XF32>(cur, c, v.nch, midx, sums, xs, acc);
+        chunk_fma<BITS, MT, R>(cur, c, v.nch, midx, aux, xs, acc);
         if (!more) break;
         c = cn;
         cur = nxt;

@@ -134,6 +134,14 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
 /* Text of the last error raised on this thread ("" if none). */
 const char *gwa_last_error(void);
 
+/* Pipeline health.  The streaming and tensor-core kernels bound every wait
+ * on their shared-memory pipelines (2 s); a wait that runs out is counted on
+ * the device and the kernel returns early instead of hanging (its outputs
+ * are then undefined).  Writes the count of such timeouts on the current
+ * device since the last reset to *timeouts, and clears it if `reset`.
+ * Synchronizes the current device (a diagnostics call, not for hot loops). */
+int gwa_pipeline_status(uint32_t *timeouts, int32_t reset);
+
 /* Test exports.  codes[N, K] (uint8) = q[n,k]; wf[N, K] (fp32) =
  * fmaf(scale, (float)q, bias): the dequantized weight rounded once to fp32.
  * Both are written on `stream`; the caller owns codes / wf. */

@@ -71,15 +71,27 @@ def test_qmv_uneven_grid_covers_every_row():
     assert_close(bf16_to_f64(y), ref, "N=4099")
 
 
-def test_token_counts_agree_bitwise():
-    # one token at a time and eight at once run the same per-row arithmetic
+@pytest.mark.parametrize("bits", [4, 8])
+def test_token_counts_agree(bits):
+    # one token at a time (streaming kernel), two (streaming), four and eight
+    # at once (staged kernel): same results within the output tolerance
     N, K = 512, 2048
-    w = dev_qweight(synth.qweight(311, N, K, 4))
-    x = dev_bf16(synth.activations(312, 8, K))
-    y8 = gwa.qmv_affine(x, w)
-    y4 = torch.cat([gwa.qmv_affine(x[i:i + 4], w) for i in (0, 4)])
-    y1 = torch.cat([gwa.qmv_affine(x[i:i + 1], w) for i in range(8)])
-    assert torch.equal(y1, y4) and torch.equal(y1, y8)
+    w = synth.qweight(311, N, K, bits)
+    dw = dev_qweight(w)
+    xh = synth.activations(312, 8, K)
+    x = dev_bf16(xh)
+    ref = oracle.qmv(xh, w.wq, w.scales, w.biases, N, K, bits)
+    runs = {
+        8: gwa.qmv_affine(x, dw),
+        4: torch.cat([gwa.qmv_affine(x[i:i + 4], dw) for i in (0, 4)]),
+        2: torch.cat([gwa.qmv_affine(x[i:i + 2], dw) for i in range(0, 8, 2)]),
+        1: torch.cat([gwa.qmv_affine(x[i:i + 1], dw) for i in range(8)]),
+    }
+    for m, y in runs.items():
+        assert_close(bf16_to_f64(y), ref, f"{m} tokens per call")
+    # same kernel, same per-row arithmetic: bitwise equal
+    y1b = torch.cat([gwa.qmv_affine(x[i:i + 1], dw) for i in range(8)])
+    assert torch.equal(runs[1], y1b)
 
 
 # ---------------------------------------------------------------- a4
