@@ -191,20 +191,26 @@ __device__ __forceinline__ void u8_pairs(const float *v, float finv,
     pr[1] = i16_pair(v[2] * finv, v[3] * finv);
 }
 
-// Integer dot of one packed word with its activation pairs.
-__device__ __forceinline__ int word_dot_u4(uint32_t w, const uint32_t *pr,
-                                           int acc) {
-    const uint32_t lo = w & 0x0f0f0f0fu;          // q0 q2 q4 q6
-    const uint32_t hi = (w >> 4) & 0x0f0f0f0fu;   // q1 q3 q5 q7
-    acc = dp2a_lo(pr[0], lo, acc);
-    acc = dp2a_hi(pr[1], lo, acc);
-    acc = dp2a_lo(pr[2], hi, acc);
-    return dp2a_hi(pr[3], hi, acc);
+// Integer dot of one packed word with its activation pairs, into two
+// accumulators.  u4: the low nibbles (q0 q2 q4 q6) go to acc[0]; the high
+// nibbles stay in place as 16*q (q1 q3 q5 q7, no shift needed) and go to
+// acc[1], which therefore holds 16x its sum, exactly (at most
+// 32 * 240 * 32640 < 2^31 per chunk).  Combine with dot_total.
+__device__ __forceinline__ void word_dot_u4(uint32_t w, const uint32_t *pr,
+                                            int (&acc)[2]) {
+    const uint32_t lo = w & 0x0f0f0f0fu;
+    const uint32_t hi = w & 0xf0f0f0f0u;
+    acc[0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, acc[0]));
+    acc[1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, acc[1]));
 }
-__device__ __forceinline__ int word_dot_u8(uint32_t w, const uint32_t *pr,
-                                           int acc) {
-    acc = dp2a_lo(pr[0], w, acc);
-    return dp2a_hi(pr[1], w, acc);
+__device__ __forceinline__ void word_dot_u8(uint32_t w, const uint32_t *pr,
+                                            int (&acc)[2]) {
+    acc[0] = dp2a_lo(pr[0], w, acc[0]);
+    acc[1] = dp2a_hi(pr[1], w, acc[1]);
+}
+template <int BITS>
+__device__ __forceinline__ int dot_total(const int (&acc)[2]) {
+    return BITS == 4 ? acc[0] + (acc[1] >> 4) : acc[0] + acc[1];
 }
 
 }  // namespace gwa

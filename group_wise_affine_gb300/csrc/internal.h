@@ -18,7 +18,7 @@ constexpr int kMaxSections = 8;
 // Streaming decode kernel: largest CTA, and the shared-memory ring size it
 // aims for per CTA.
 constexpr int kStreamMaxThreads = 512;
-constexpr size_t kStreamRingTarget = 72 * 1024;
+constexpr size_t kStreamRingTarget = 96 * 1024;
 
 struct DenseParams {
     const uint16_t *x;   // [M, K] bf16

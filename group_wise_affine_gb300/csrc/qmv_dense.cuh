@@ -196,10 +196,12 @@ __device__ __forceinline__ void chunk_fma(const ChunkRegs<R> &cr, int c,
                                   : wd == 2 ? cr.w[r].z
                                             : cr.w[r].w;
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                d[r][m][wd & 1] = BITS == 4
-                                      ? word_dot_u4(word, xp[m], d[r][m][wd & 1])
-                                      : word_dot_u8(word, xp[m], d[r][m][wd & 1]);
+            for (int m = 0; m < MT; ++m) {
+                if constexpr (BITS == 4)
+                    word_dot_u4(word, xp[m], d[r][m]);
+                else
+                    word_dot_u8(word, xp[m], d[r][m]);
+            }
         }
     }
 #pragma unroll
@@ -207,7 +209,7 @@ __device__ __forceinline__ void chunk_fma(const ChunkRegs<R> &cr, int c,
         const float2 fa = aux[(size_t)midx[m] * nch + c];
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            acc[r][m] = fmaf(cr.s[r] * fa.x, (float)(d[r][m][0] + d[r][m][1]),
+            acc[r][m] = fmaf(cr.s[r] * fa.x, (float)dot_total<BITS>(d[r][m]),
                              fmaf(cr.b[r], fa.y, acc[r][m]));
     }
 }

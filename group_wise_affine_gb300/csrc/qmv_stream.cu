@@ -126,16 +126,14 @@ __device__ __forceinline__ void batch_dot(const uint4 (&w)[R],
                                   : wd == 2 ? w[r].z
                                             : w[r].w;
             if constexpr (BITS == 4) {
+                // high nibbles stay in place (16 * q) and are summed apart
                 const uint32_t lo = word & 0x0f0f0f0fu;
-                const uint32_t hi = (word >> 4) & 0x0f0f0f0fu;
+                const uint32_t hi = word & 0xf0f0f0f0u;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     const uint32_t *pr = xr.pr[m] + 4 * wd;
-                    int a = d[r][m][wd & 1];
-                    a = dp2a_lo(pr[0], lo, a);
-                    a = dp2a_hi(pr[1], lo, a);
-                    a = dp2a_lo(pr[2], hi, a);
-                    d[r][m][wd & 1] = dp2a_hi(pr[3], hi, a);
+                    d[r][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, d[r][m][0]));
+                    d[r][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, d[r][m][1]));
                 }
             } else {
 #pragma unroll
@@ -151,28 +149,49 @@ __device__ __forceinline__ void batch_dot(const uint4 (&w)[R],
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-            out[r][m] = fmaf(s[r] * xr.f[m], (float)(d[r][m][0] + d[r][m][1]),
-                             b[r] * xr.xs[m]);
+        for (int m = 0; m < MT; ++m) {
+            // u4: the high-nibble sum is 16x the true sum, exactly
+            const int dsum = BITS == 4 ? d[r][m][0] + (d[r][m][1] >> 4)
+                                       : d[r][m][0] + d[r][m][1];
+            out[r][m] = fmaf(s[r] * xr.f[m], (float)dsum, b[r] * xr.xs[m]);
+        }
 }
 
-// RBU units per stage; a gate+up unit is one gate row plus one up row.
-template <int BITS, int MT, int MODE, int RBU>
+// Sum of the per-warp slots of one output, in a fixed order.
+__device__ __forceinline__ float red_total(const float *red, int idx, int nwh) {
+    float t = 0.f;
+    for (int w = 0; w < nwh; ++w) t += red[idx * nwh + w];
+    return t;
+}
+
+// A stage holds UPS = RS * UPT units (rows, or gate/up row pairs); the
+// consumer threads form RS row groups, each owning UPT units of the stage
+// (RPH = 4 weight rows), and within a group thread c owns chunk c.  Grid:
+// one CTA per SM with a ~96 KB ring, so that the next kernel's CTA fits
+// beside it and prefetches its first stages while this one drains (2 CTAs
+// per SM, 2 or 8 rows per thread and up to 20 consumer warps were measured
+// and were slower on the 48-layer stack).
+constexpr int kRowsPerThread = 4;
+
+template <int BITS, int MT, int MODE, int RPH>
 __global__ void __launch_bounds__(kStreamMaxThreads)
-    qmv_stream_kernel(DenseParams p, int stages, int64_t units) {
+    qmv_stream_kernel(DenseParams p, int stages, int64_t units, int rs) {
     constexpr int HALVES = MODE == kSGateUp ? 2 : 1;
-    constexpr int ROWS = HALVES * RBU;  // weight rows per stage
-    constexpr int V = ROWS * MT;        // values reduced per warp per stage
-    constexpr int RBATCH = MT == 1 ? 8 : 4;  // rows computed together
+    constexpr int UPT = RPH / HALVES;     // units per thread per stage
+    constexpr int V = RPH * MT;           // values reduced per warp per stage
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
     const int ncons = blockDim.x - kWarp;
+    const int ncpad = ncons / rs;          // threads per row group
+    const int nwh = ncpad / kWarp;         // warps per row group
     const int lane = tid & (kWarp - 1);
+    const int ups = rs * UPT;              // units per stage
     const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
     const uint32_t sbrow = (uint32_t)p.G * 2;
-    const uint32_t stage_bytes = ROWS * (rowbytes + 2 * sbrow);
+    const uint32_t rows_stage = (uint32_t)(HALVES * ups);
+    const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
     uint64_t *empty = full + stages;
     float *red = reinterpret_cast<float *>(empty + stages);
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
     const int64_t u0 = units * blockIdx.x / gridDim.x;
     const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
     const int nu = (int)(u1 - u0);
-    const int nst = (nu + RBU - 1) / RBU;
+    const int nst = (nu + ups - 1) / ups;
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -189,14 +208,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
             mbar_init(&empty[s], ncons / kWarp);
         }
         fence_mbar_init();
-    }
-    if (tid == 0) {
         s_issued = 0;
         s_consumed = nst;
         // let the next kernel in the stream start its own weight prefetch
         pdl_launch_dependents();
     }
-    const int nwarps = ncons / kWarp;
     __syncthreads();
 
     if (tid >= ncons) {
@@ -220,22 +236,21 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
                     atomicAdd(&g_stream_timeouts, 1u);
                     break;
                 }
-                const int64_t ua = u0 + (int64_t)st * RBU;
-                const int n = (int)min((int64_t)RBU, u1 - ua);
+                const int64_t ua = u0 + (int64_t)st * ups;
+                const int n = (int)min((int64_t)ups, u1 - ua);
                 unsigned char *base = smem + (size_t)s * stage_bytes;
-                unsigned char *dcodes = base;
-                unsigned char *dsc = base + ROWS * rowbytes;
-                unsigned char *dbi = dsc + ROWS * sbrow;
+                unsigned char *dsc = base + rows_stage * rowbytes;
+                unsigned char *dbi = dsc + rows_stage * sbrow;
                 mbar_expect_tx(&full[s], (uint32_t)(HALVES * n) *
                                              (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
                     const int64_t r = ua + (h ? p.I : 0);
-                    bulk_g2s(dcodes + h * RBU * rowbytes, wq + r * rowbytes,
+                    bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
                              n * rowbytes, &full[s]);
-                    bulk_g2s(dsc + h * RBU * sbrow, sc + r * sbrow, n * sbrow,
+                    bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
                              &full[s]);
-                    bulk_g2s(dbi + h * RBU * sbrow, bi + r * sbrow, n * sbrow,
+                    bulk_g2s(dbi + h * ups * sbrow, bi + r * sbrow, n * sbrow,
                              &full[s]);
                 }
                 s_issued = st + 1;
@@ -243,15 +258,30 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
         }
     } else {
         // ------------------------------------------------ consumers
-        const int c = tid;
+        const int hg = tid / ncpad;          // row group
+        const int c = tid - hg * ncpad;      // chunk
+        const int wh = c / kWarp;            // warp within the row group
         const bool active = c < p.nch;
-        XRegs<BITS, MT> xr;
-        pdl_wait_primary();  // x may be the previous kernel's output
-        load_x_regs<BITS, MT>(p.x, p.M, p.K, c, active, xr);
         // lanes past the row end use chunk 0 (and its group) with zero
         // activations, so every value they read is a finite weight
         const int cc = active ? c : 0;
         const int g = (cc * CODES) / kGroup;
+        XRegs<BITS, MT> xr;
+        pdl_wait_primary();  // x may be the previous kernel's output
+        load_x_regs<BITS, MT>(p.x, p.M, p.K, c, active, xr);
+        // This thread's rows are unit hg*UPT + u of each half of a stage;
+        // their shared-memory offsets are the same in every stage.  Row
+        // slots past the stage end hold stale data; their totals are
+        // dropped below.
+        uint32_t offw[RPH], offs[RPH];
+        const uint32_t sb_delta = rows_stage * (uint32_t)p.G * 2u;
+#pragma unroll
+        for (int j = 0; j < RPH; ++j) {
+            const uint32_t srow =
+                (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
+            offw[j] = srow * rowbytes + (uint32_t)cc * 16u;
+            offs[j] = rows_stage * rowbytes + (srow * (uint32_t)p.G + g) * 2u;
+        }
         for (int st = 0; st < nst; ++st) {
             const int s = st % stages;
             if (!mbar_wait(&full[s], (st / stages) & 1)) {
@@ -259,38 +289,27 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
                 atomicMin(&s_consumed, st);
                 break;
             }
-            const int64_t ua = u0 + (int64_t)st * RBU;
-            const int n = (int)min((int64_t)RBU, u1 - ua);
-            const unsigned char *base = smem + (size_t)s * stage_bytes;
-            const uint16_t *ssc =
-                reinterpret_cast<const uint16_t *>(base + ROWS * rowbytes);
-            const uint16_t *sbi = ssc + ROWS * p.G;
-            float v[V];
-            // Rows are processed in batches with every load issued first and
-            // no per-row branches, so the unpack/FMA chains of the rows in a
-            // batch interleave.  Row slots past the stage end hold stale
-            // data; their totals are dropped below.  Lanes past the row end
-            // read chunk 0 with zero activations and contribute zero.
-            const unsigned char *rowp = base + (size_t)cc * 16;
+            const int64_t ua = u0 + (int64_t)st * ups;
+            const int n = (int)min((int64_t)ups, u1 - ua);
+            const unsigned char *base = smem + (uint32_t)s * stage_bytes;
+            uint4 w[RPH];
+            float sv[RPH], bv[RPH];
 #pragma unroll
-            for (int j0 = 0; j0 < ROWS; j0 += RBATCH) {
-                uint4 w[RBATCH];
-                float sv[RBATCH], bv[RBATCH];
-#pragma unroll
-                for (int jj = 0; jj < RBATCH; ++jj) {
-                    const int j = j0 + jj;
-                    w[jj] = *reinterpret_cast<const uint4 *>(
-                        rowp + (size_t)j * rowbytes);
-                    sv[jj] = bf16_bits_to_f32(ssc[j * p.G + g]);
-                    bv[jj] = bf16_bits_to_f32(sbi[j * p.G + g]);
-                }
-                float o[RBATCH][MT];
-                batch_dot<BITS, MT, RBATCH>(w, sv, bv, xr, o);
-#pragma unroll
-                for (int jj = 0; jj < RBATCH; ++jj)
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) v[(j0 + jj) * MT + m] = o[jj][m];
+            for (int j = 0; j < RPH; ++j) {
+                w[j] = *reinterpret_cast<const uint4 *>(base + offw[j]);
+                sv[j] = bf16_bits_to_f32(
+                    *reinterpret_cast<const uint16_t *>(base + offs[j]));
+                bv[j] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(
+                    base + offs[j] + sb_delta));
             }
+            float o[RPH][MT];
+            batch_dot<BITS, MT, RPH>(w, sv, bv, xr, o);
+            float v[V];
+#pragma unroll
+            for (int j = 0; j < RPH; ++j)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) v[j * MT + m] = o[j][m];
+            // every lane's reads of this stage are done: release the slot
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             const float tot = transpose_reduce<V>(v, lane);
@@ -298,11 +317,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
             if ((lane & (SPREAD - 1)) == 0) {
                 const int idx = lane / SPREAD;  // j * MT + m
                 const int j = idx / MT, m = idx % MT;
-                const int uj = j % RBU, h = j / RBU;
+                const int u = hg * UPT + (j % UPT), h = j / UPT;
                 // per-warp slot: the epilogue adds the warps in a fixed order
-                if (uj < n)
-                    red[(((st * RBU + uj) * HALVES + h) * MT + m) * nwarps +
-                        tid / kWarp] = tot;
+                if (u < n)
+                    red[((((st * ups + u) * HALVES + h) * MT + m) * nwh) + wh] =
+                        tot;
             }
         }
     }
@@ -318,28 +337,24 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
     __syncthreads();
 
     // ---------------------------------------------------- epilogue
-    auto total = [&](int idx) {
-        float t = 0.f;
-        for (int w = 0; w < nwarps; ++w) t += red[idx * nwarps + w];
-        return t;
-    };
     for (int i = tid; i < nu * MT; i += blockDim.x) {
         const int lu = i / MT, m = i % MT;
         if (m >= p.M) continue;
         const int64_t n = u0 + lu;
         if constexpr (MODE == kSGateUp) {
-            const float gv = total((lu * 2 + 0) * MT + m);
-            const float uv = total((lu * 2 + 1) * MT + m);
+            const float gv = red_total(red, (lu * 2 + 0) * MT + m, nwh);
+            const float uv = red_total(red, (lu * 2 + 1) * MT + m, nwh);
             p.y[(int64_t)m * p.I + n] = f32_to_bf16_bits(
                 gv / (1.0f + __expf(-gv)) * uv);
         } else if constexpr (MODE == kSPlain) {
-            p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(total(lu * MT + m));
+            p.y[(int64_t)m * p.N + n] =
+                f32_to_bf16_bits(red_total(red, lu * MT + m, nwh));
         } else {
             int s = 0;
             while (s + 1 < p.nsec && n >= p.sec_start[s + 1]) ++s;
             const int64_t j = n - p.sec_start[s];
             const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
-            float val = total(lu * MT + m);
+            float val = red_total(red, lu * MT + m, nwh);
             if (p.sec_bias[s]) val += bf16_bits_to_f32(p.sec_bias[s][j]);
             p.sec_out[s][(int64_t)m * size + j] = f32_to_bf16_bits(val);
         }
@@ -347,38 +362,46 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
 }
 
 // ------------------------------------------------------------ host side
-template <int BITS, int MT, int MODE, int RBU>
-static cudaError_t launch_stream_t(const DenseParams &p, cudaStream_t st,
+template <int BITS, int MT, int MODE, int RPH>
+static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
                                    bool *used) {
     constexpr int HALVES = MODE == kSGateUp ? 2 : 1;
+    constexpr int UPT = RPH / HALVES;
     const int64_t units = MODE == kSGateUp ? p.I : p.N;
     const size_t rowbytes = (size_t)p.K * BITS / 8;
     const size_t sbrow = (size_t)p.G * 2;
-    const size_t stage_bytes = HALVES * RBU * (rowbytes + 2 * sbrow);
+    const int nwh = (p.nch + kWarp - 1) / kWarp;
+    // row groups: aim for about ten consumer warps per CTA
+    int rs = 1;
+    while (rs < 4 && nwh * rs * 2 <= 12) rs *= 2;
+    const int threads = nwh * kWarp * rs + kWarp;
+    if (threads > kStreamMaxThreads) return cudaSuccess;  // not used
+    const size_t stage_bytes = (size_t)HALVES * rs * UPT * (rowbytes + 2 * sbrow);
     int stages = (int)(kStreamRingTarget / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
-    const int ncons = ((p.nch + kWarp - 1) / kWarp) * kWarp;
-    const int threads = ncons + kWarp;
-    if (threads > kStreamMaxThreads) return cudaSuccess;  // not used
-    auto kern = qmv_stream_kernel<BITS, MT, MODE, RBU>;
-    // first pass: occupancy with a generous accumulator estimate
-    const int sms = num_sms();
-    const int nwarps = ncons / kWarp;
-    size_t red_bytes =
-        (size_t)((units + sms - 1) / sms + 1) * HALVES * MT * 4 * nwarps;
-    size_t smem = stages * stage_bytes + 16 * stages + red_bytes;
-    if (smem > kMaxDynSmem) return cudaSuccess;
-    int grid = 0;
-    cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
-                                   threads, smem, &grid);
-    if (e != cudaSuccess) return e;
+    // one CTA per SM, so the next kernel's CTA fits beside it and can
+    // prefetch while this one drains
+    int grid = num_sms();
     if ((int64_t)grid > units) grid = (int)units;
-    red_bytes = (size_t)((units + grid - 1) / grid) * HALVES * MT * 4 * nwarps;
-    smem = stages * stage_bytes + 16 * stages + red_bytes;
+    const size_t red_bytes =
+        (size_t)((units + grid - 1) / grid) * HALVES * MT * 4 * nwh;
+    const size_t smem = stages * stage_bytes + 16 * stages + red_bytes;
+    if (smem > kMaxDynSmem) return cudaSuccess;
+    auto kern = qmv_stream_kernel<BITS, MT, MODE, RPH>;
+    int dummy = 0;
+    cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
+                                   threads, smem, &dummy);
+    if (e != cudaSuccess) return e;
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,
-                      smem, st, p, stages, units);
+                      smem, st, p, stages, units, rs);
+}
+
+template <int BITS, int MT, int MODE>
+static cudaError_t launch_stream_t(const DenseParams &p, cudaStream_t st,
+                                   bool *used) {
+    return launch_stream_r<BITS, MT, MODE, kRowsPerThread>(p, st, used);
 }
 
 static bool aligned16(const void *q) {
@@ -396,10 +419,10 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
         return cudaSuccess;
 #define GWA_STREAM_CASE(B, MTV)                                              \
     if (p.bits == B && (MTV == 1 ? p.M == 1 : p.M == 2)) {                   \
-        if (mode == kSPlain) return launch_stream_t<B, MTV, kSPlain, 8>(p, st, used); \
+        if (mode == kSPlain) return launch_stream_t<B, MTV, kSPlain>(p, st, used); \
         if (mode == kSSections)                                              \
-            return launch_stream_t<B, MTV, kSSections, 8>(p, st, used);      \
-        return launch_stream_t<B, MTV, kSGateUp, 4>(p, st, used);            \
+            return launch_stream_t<B, MTV, kSSections>(p, st, used);         \
+        return launch_stream_t<B, MTV, kSGateUp>(p, st, used);               \
     }
     GWA_STREAM_CASE(4, 1)
     GWA_STREAM_CASE(4, 2)
