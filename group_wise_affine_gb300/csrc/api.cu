@@ -212,7 +212,7 @@ int gwa_pipeline_status(uint32_t *timeouts, int32_t reset) {
     if (!timeouts) return fail(GWA_ERR_INVALID_ARG, "gwa_pipeline_status: null");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "gwa_pipeline_status");
-    *timeouts = stream_timeouts(reset != 0);
+    *timeouts = stream_timeouts(reset != 0) + qmm_timeouts(reset != 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, "gwa_pipeline_status");
 }

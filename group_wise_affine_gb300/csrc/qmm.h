@@ -26,6 +26,9 @@ size_t qmm_workspace_bytes(int64_t M, int64_t K);
 int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
             cudaStream_t st);
 
+// Tensor-core pipeline waits that ran out of time (read, optionally reset).
+unsigned int qmm_timeouts(bool reset);
+
 // Records the thread's last error text and returns `code`.
 int set_error(int code, const char *fmt, ...);
 

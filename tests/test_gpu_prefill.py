@@ -1,0 +1,129 @@
+"""GPU parity of the prefill-shaped path (M > 8, tcgen05 tensor cores)
+against the CPU oracle, on ragged shapes and on sampled rows of the 48-layer
+stack's projection shapes at M = 512."""
+import numpy as np
+import pytest
+import torch
+
+import group_wise_affine_gb300 as gwa
+import gwa_synth as synth
+import oracle
+from helpers import bf16_to_f64, dev_bf16, dev_qweight
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gwa.build()
+    gwa.load()
+
+
+def assert_close(got, ref, what=""):
+    ok, max_err, worst = oracle.within_tolerance(got, ref, TOL)
+    assert ok, f"{what}: max |err| {max_err:.3g}, worst err/bound {worst:.3g}"
+
+
+def status_of(ws):
+    return int(ws[:4].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [9, 16, 128, 130, 300])
+@pytest.mark.parametrize("N,K", [(384, 512), (300, 1024), (256, 576)])
+def test_qmm_affine_matches_oracle(bits, M, N, K):
+    w = synth.qweight(1300 + N + bits, N, K, bits)
+    x = synth.activations(1400 + M, M, K)
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
+    torch.cuda.synchronize()
+    assert status_of(ws) == 0
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+    assert_close(bf16_to_f64(y), ref, f"M={M} N={N} K={K} u{bits}")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [16, 200])
+def test_qmm_sections_and_bias(bits, M):
+    K, secs = 1024, (256, 64, 64, 40)
+    parts = [synth.qweight(1500 + i, n, K, bits) for i, n in enumerate(secs)]
+    fused = synth.stack_rows(parts)
+    x = synth.activations(1510 + M, M, K)
+    bias = [synth.activations(1520 + i, 1, n)[0] for i, n in enumerate(secs)]
+    bias[2] = None
+    outs = gwa.qmv_fused_sections(
+        dev_bf16(x), dev_qweight(fused), secs,
+        out_bias=[dev_bf16(b) if b is not None else None for b in bias])
+    refs = oracle.fused_sections(x, fused.wq, fused.scales, fused.biases, secs,
+                                 K, bits, out_bias=bias)
+    for o, r in zip(outs, refs):
+        assert o.is_contiguous() and o.storage_offset() == 0
+        assert_close(bf16_to_f64(o), r, "qmm sections")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [16, 129])
+def test_qmm_gate_up_silu(bits, M):
+    K, I = 576, 200
+    w = synth.qweight(1600 + bits, 2 * I, K, bits)
+    x = synth.activations(1610 + M, M, K)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
+    ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits)
+    assert_close(bf16_to_f64(h), ref, f"qmm gate_up M={M} u{bits}")
+
+
+def test_tensor_core_and_decode_paths_agree():
+    # the first 8 tokens through the decode kernel and all 16 through the
+    # tensor-core kernel
+    N, K = 512, 2048
+    w = dev_qweight(synth.qweight(1700, N, K, 4))
+    x = dev_bf16(synth.activations(1701, 16, K))
+    y16 = gwa.qmv_affine(x, w)
+    y8 = gwa.qmv_affine(x[:8], w)
+    assert_close(bf16_to_f64(y16[:8]), bf16_to_f64(y8), "tc vs decode")
+
+
+@pytest.mark.parametrize("name,rows,K,cols", [
+    ("qkv", 7168, 5120, None), ("down", 5120, 13824, None),
+    ("gate_up", 27648, 5120, [0, 1, 127, 128, 5000, 13823])])
+def test_stack_shapes_at_prefill_size(name, rows, K, cols):
+    # the 48-layer stack's projections at M = 512 (layer 0 recipe, drawn on
+    # the host), checked on sampled outputs the oracle computes one by one
+    M = 512
+    w = synth.qweight(synth.stack_seed(0, 0, 4) + rows, rows, K, 4)
+    x = synth.activations(1800 + rows, M, K)
+    dw = dev_qweight(w)
+    if name == "gate_up":
+        h = gwa.qmv_gate_up_silu(dev_bf16(x), dw)
+        ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, rows, K, 4,
+                                  cols=cols)
+        got = bf16_to_f64(h)[:, cols]
+    else:
+        y = gwa.qmv_affine(dev_bf16(x), dw)
+        sample = [0, 1, 127, 128, 255, 256, rows // 2, rows - 1]
+        ref = oracle.qmv(x, w.wq, w.scales, w.biases, rows, K, 4, rows=sample)
+        got = bf16_to_f64(y)[:, sample]
+    assert_close(got, ref, f"{name} M=512")
+
+
+def test_missing_workspace_is_an_error_not_a_fault():
+    w = dev_qweight(synth.qweight(1900, 64, 128, 4))
+    x = dev_bf16(synth.activations(1901, 32, 128))
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gwa.GwaError) as e:
+        gwa.qmv_affine(x, w, workspace=small)
+    assert e.value.code == gwa.GWA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+
+
+def test_fp16_range_is_flagged():
+    # an activation beyond fp16's range sets the status bit; nothing faults
+    w = dev_qweight(synth.qweight(1910, 128, 128, 4))
+    xh = synth.activations(1911, 32, 128)
+    xh[3, 5] = synth.bf16_bits(np.array([1.0e6], np.float32))[0]
+    ws = gwa.make_workspace(32, 128)
+    gwa.qmv_affine(dev_bf16(xh), w, workspace=ws)
+    torch.cuda.synchronize()
+    assert status_of(ws) & 2
+    assert gwa.pipeline_status() == 0
