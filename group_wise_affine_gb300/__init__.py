@@ -32,12 +32,14 @@ GWA_ERR_UNSUPPORTED = 2
 GWA_ERR_MISALIGNED = 3
 GWA_ERR_CUDA = 4
 GWA_ERR_WORKSPACE = 5
+GWA_NOALLOC_SCRATCH_BYTES = 8 << 20
 GWA_MOE_GATE_UP_SILU = 0
 GWA_MOE_DOWN_COMBINE = 1
 
 EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
-           "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant")
+           "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant",
+           "gwa_qmv_affine_noalloc")
 
 
 class GwaError(RuntimeError):
@@ -83,6 +85,8 @@ def load(path: str = LIB_PATH):
                                        vp, vp]
     lib.gwa_last_error.argtypes = []
     lib.gwa_last_error.restype = ctypes.c_char_p
+    lib.gwa_qmv_affine_noalloc.argtypes = [vp, i64, _QW, vp, vp]
+    lib.gwa_qmv_affine_noalloc.restype = ctypes.c_int
     lib.gwa_pipeline_status.argtypes = [vp, i32]
     lib.gwa_pipeline_status.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
@@ -239,6 +243,21 @@ def qmv_affine(x: torch.Tensor, w: QWeight, y: Optional[torch.Tensor] = None,
     wp, wn = _ws(workspace)
     _check(load().gwa_qmv_affine(_ptr(x), M, w.c(), _ptr(y), wp, wn,
                                  _stream(stream)))
+    return y
+
+
+def qmv_affine_noalloc(x: torch.Tensor, w: QWeight, y: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """gwa_qmv_affine_noalloc: the same projection without a workspace, for
+    callers that cannot allocate device memory on this path (the library's
+    built-in scratch is used instead; see include/gwa.h).  `y` is required,
+    since creating it here would allocate."""
+    x = _bf16(x, "x")
+    _check_weight(w)
+    M = x.numel() // w.K
+    _check_out(y, M * w.N, "y")
+    _check(load().gwa_qmv_affine_noalloc(_ptr(x), M, w.c(), _ptr(y),
+                                         _stream(stream)))
     return y
 
 

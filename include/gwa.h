@@ -131,6 +131,32 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
                        gwa_qweight w, int32_t num_experts, int32_t mode,
                        uint16_t *out, int32_t *status, void *stream);
 
+/* Allocation-free variant of gwa_qmv_affine, for callers that cannot
+ * allocate device memory: for example a plug-in inside a host framework that
+ * owns all device memory, or a serving loop that must not make allocation
+ * calls (they can synchronize the device or fail under memory pressure in
+ * the middle of a request).  Those callers cannot supply the workspace that
+ * the tensor-core path (M > 8) needs, so this entry point uses a scratch
+ * buffer of GWA_NOALLOC_SCRATCH_BYTES that the library itself holds in
+ * device memory on every GPU that loads it, until the process exits.  It
+ * allocates nothing and frees nothing.  (The pages have no counterpart:
+ * this is a property of this library's interface, not of the method.)
+ *   Same arguments, layout and results as gwa_qmv_affine, minus the
+ *   workspace.  M <= 8 needs no scratch; for M > 8 the problem must fit:
+ *   gwa_workspace_bytes(M, K) <= GWA_NOALLOC_SCRATCH_BYTES, otherwise the
+ *   call returns GWA_ERR_WORKSPACE and enqueues nothing.
+ *   The first call on each device looks up the scratch's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one scratch buffer and leaves its
+ *   contents behind (the status word is cleared at the start of each call):
+ *   calls that can overlap on the GPU -- on different streams, or from
+ *   different host threads -- race on it and must be serialized by the
+ *   caller. */
+#define GWA_NOALLOC_SCRATCH_BYTES (8u << 20)
+int gwa_qmv_affine_noalloc(const uint16_t *x, int64_t M, gwa_qweight w,
+                           uint16_t *y, void *stream);
+
 /* Text of the last error raised on this thread ("" if none). */
 const char *gwa_last_error(void);
 
