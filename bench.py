@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the secondary workloads (M=4, M=512, MoE)")
     return ap.parse_args()
 
 
@@ -82,6 +84,48 @@ def workload_config(args) -> dict:
               " GB of distinct weights (L2 is 129 MB)",
         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single",
     }
+
+
+def kernel_sources_sha256() -> str:
+    """Hash of the decode kernel's sources; a recorded ncu traffic figure is
+    only reported while the sources it was taken on are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("qmv_stream.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "group_wise_affine_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch (read + write) recorded from one ncu capture in
+    profiles/, or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "qmv_stream_gate_up_27648x5120_m1.md")
+    if kernel != "gate_up" or not os.path.exists(path):
+        return None
+    traffic = sha = None
+    with open(path) as f:
+        for ln in f:
+            if ln.startswith("traffic per launch (bytes):"):
+                traffic = int(ln.split(":")[1].strip())
+            if ln.startswith("kernel sources sha256:"):
+                sha = ln.split(":")[1].strip()
+    if traffic is None or sha != kernel_sources_sha256():
+        return None
+    return traffic
+
+
+def _measured_tflops():
+    """Dense fp16/bf16 tensor peak for a kernel timed inside a long step
+    (the sustained figure; fp16 and bf16 share the nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured sustained bf16"
+    except Exception:
+        return 1700.0, "fallback sustained"
 
 
 def measured_peak():
@@ -278,10 +322,148 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     e2e_ms = e0.elapsed_time(e1) / KE
+    extras = {}
+    if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
+        extras["stack_M4"] = run_stack_extra(W, 4, dev, 50, 3)
+        extras["prefill_stack_M512"] = run_stack_extra(W, 512, dev, 5, 2)
+        extras["moe"] = run_moe_extra(dev, 50, 3)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
                 h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
-                launches=K * 4 * L)
+                launches=K * 4 * L, extras=extras)
+
+
+# ---------------------------------------------------------------- extras
+def time_graphs(graphs, steps, warmup):
+    """Replays the graphs in order `steps` times; returns (total ms, per-graph
+    ms summed over steps), timed with CUDA events on the current stream."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(st)
+        for j, g in enumerate(graphs):
+            g.replay()
+            ev[i][j + 1].record(st)
+    torch.cuda.synchronize()
+    per = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+           for j in range(len(graphs))]
+    return sum(per), per
+
+
+def capture(fn):
+    import torch
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    return g
+
+
+def run_stack_extra(W, M, dev, steps, warmup):
+    """The same 48-layer stack (same weights) at M tokens per call."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    L = len(W)
+    g = torch.Generator(device=dev)
+    g.manual_seed(777 + M)
+    x = torch.randn((M, HIDDEN), generator=g, device=dev).to(torch.bfloat16)
+    mk = lambda n: torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+    bufs = [dict(q=mk(QOUT), k=mk(KVOUT), v=mk(KVOUT), o=mk(HIDDEN),
+                 h=mk(INTER), y=mk(HIDDEN)) for _ in range(L)]
+    ws = gwa.make_workspace(M, INTER, dev)
+
+    def call(kind, l):
+        w, b = W[l], bufs[l]
+        if kind == "qkv":
+            gwa.qmv_fused_sections(x, w["qkv"], (QOUT, KVOUT, KVOUT),
+                                   outs=[b["q"], b["k"], b["v"]], workspace=ws)
+        elif kind == "o":
+            gwa.qmv_affine(b["q"], w["o"], y=b["o"], workspace=ws)
+        elif kind == "gate_up":
+            gwa.qmv_gate_up_silu(b["o"], w["gate_up"], h=b["h"], workspace=ws)
+        else:
+            gwa.qmv_affine(b["h"], w["down"], y=b["y"], workspace=ws)
+
+    kinds = ["qkv", "o", "gate_up", "down"]
+    for k in kinds:
+        call(k, 0)
+    torch.cuda.synchronize()
+    graphs = [capture(lambda k=k: [call(k, l) for l in range(L)]) for k in kinds]
+    total, per = time_graphs(graphs, steps, warmup)
+    ms = total / steps
+    shapes = {n: (r, k) for n, r, k in layer_shapes()}
+    out = {"M": M, "ms_per_step": round(ms, 4),
+           "steps_per_s": round(1e3 / ms, 2), "kernels": {}}
+    flops = 0
+    bytes_ = 0
+    for (kind, t) in zip(kinds, per):
+        rows, K = shapes[kind]
+        us = 1e3 * t / (steps * L)
+        f = 2.0 * M * rows * K
+        b = proj_bytes(rows, K, W[0][kind].bits, M)
+        flops += f * L
+        bytes_ += b * L
+        out["kernels"][kind] = {"us_per_launch": round(us, 3),
+                                "TFLOP/s": round(f / us / 1e6, 1),
+                                "GB/s": round(b / us / 1e3, 1)}
+    out["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
+    out["GB/s"] = round(bytes_ / (ms * 1e-3) / 1e9, 1)
+    return out
+
+
+def run_moe_extra(dev, steps, warmup, layers=16, E=256, H=2048, I=512,
+                  topk=8, tokens=(1, 8)):
+    """MoE expert GEMV: per layer one gate+up SiLU call and one down+combine
+    call over that layer's own stacked experts (16 layers x 256 experts, so
+    replays do not find the touched experts still in L2)."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    import gwa_synth as synth
+    pools = []
+    for l in range(layers):
+        gu = gwa.QWeight(*synth.device_qweight(50000 + 2 * l, E * 2 * I, H, 4,
+                                               device=dev), E * 2 * I, H, 4, 64)
+        dn = gwa.QWeight(*synth.device_qweight(50001 + 2 * l, E * H, I, 4,
+                                               device=dev), E * H, I, 4, 64)
+        pools.append((gwa.expert_view(gu, E), gwa.expert_view(dn, E)))
+    res = {}
+    per_expert = proj_bytes(2 * I, H, 4, 0) + proj_bytes(H, I, 4, 0)
+    for M in tokens:
+        ids_l, rw_l, bufs = [], [], []
+        distinct = 0
+        for l in range(layers):
+            ids, rw = synth.routing(60000 + 100 * M + l, M, topk, E)
+            distinct += len(set(ids.reshape(-1).tolist()))
+            ids_l.append(torch.from_numpy(ids).to(dev))
+            rw_l.append(torch.from_numpy(rw).to(dev))
+            bufs.append(dict(
+                x=torch.randn((M, H), device=dev).to(torch.bfloat16),
+                h=torch.empty((M, topk, I), dtype=torch.bfloat16, device=dev),
+                y=torch.empty((M, H), dtype=torch.bfloat16, device=dev)))
+
+        def step():
+            for l in range(layers):
+                gu, dn = pools[l]
+                b = bufs[l]
+                gwa.moe_qmv_gather(b["x"], ids_l[l], gu, E, 0, out=b["h"])
+                gwa.moe_qmv_gather(b["h"], ids_l[l], dn, E, 1,
+                                   route_w=rw_l[l], out=b["y"])
+        step()
+        torch.cuda.synchronize()
+        total, _ = time_graphs([capture(step)], steps, warmup)
+        ms = total / steps
+        act = layers * (M * H * 2 + M * topk * I * 2)
+        byt = distinct * per_expert + act
+        res[f"M{M}"] = {"us_per_layer": round(1e3 * ms / layers, 3),
+                        "distinct_experts_per_layer": round(distinct / layers, 2),
+                        "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -427,7 +609,8 @@ def main():
                      "frac": round(kernels[dom]["GB/s"] / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": None},
+                     "traffic": recorded_traffic(dom),
+                     "algorithmic_bytes": lb[dom]},
         "kernels": kernels,
         "e2e": {"value": round(world * step_bytes / (r["e2e_ms"] * 1e-3) / 1e9,
                                1),
@@ -439,6 +622,15 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if r["extras"]:
+        ex = dict(r["extras"])
+        pf = ex.get("prefill_stack_M512")
+        if pf:
+            bf = _measured_tflops()
+            pf["peak_TFLOP/s"] = bf[0]
+            pf["frac_of_peak"] = round(pf["TFLOP/s"] / bf[0], 4)
+            pf["peak_source"] = bf[1]
+        line["extras"] = ex
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line), flush=True)

@@ -176,10 +176,17 @@ static DenseParams dense_base(const uint16_t *x, int64_t M,
 static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
                      const int64_t *sec_sizes, cudaStream_t st,
                      const char *fn) {
-    const int mt = dense_max_tokens(p.bits, p.nch);
+    int mt = dense_max_tokens(p.bits, p.nch);
     if (mt < 1)
         return fail(GWA_ERR_INVALID_ARG, "%s: K=%d too large for staging", fn,
                     p.K);
+    // The streaming kernel (up to four tokens a pass) outruns the staged one
+    // even when it has to stream the weights twice for 5..8 tokens.
+    {
+        DenseParams probe = p;
+        probe.M = 1;
+        if (stream_eligible(probe)) mt = mt < 4 ? mt : 4;
+    }
     for (int64_t t0 = 0; t0 < M; t0 += mt) {
         DenseParams q = p;
         q.M = (int)((M - t0) < mt ? (M - t0) : mt);

@@ -1,20 +1,11 @@
-// Device helpers shared by the decode (GEMV) kernels.
+// Device helpers shared by the kernels: bf16 conversions, the integer dot
+// used by the decode kernels, and mbarrier / bulk-copy / PDL wrappers.
 //
 // Packed layout (MLX affine integer weights, "saragossa", "Quantization
 // formats"; "The Cathedral Doubled Itself", "The two fusions"): a row of K
 // inputs is K*bits/32 uint32 words, code k mod P of word k/P at bits
 // [bits*(k mod P), +bits), lowest bits first.  One bf16 scale and one bf16
 // bias per 64 inputs: w = scale*q + bias.
-//
-// Exact code -> fp32 conversion without an int->float instruction: OR the
-// code into the mantissa of a power of two.  A 4-bit code placed at mantissa
-// bits [15,19) under exponent 2^8 reads as 256 + q; placed at bits [19,23)
-// under exponent 2^4 it reads as 16 + q.  One shift of the packed word lines
-// up two codes at once (one in each window), so eight codes cost four shifts
-// and eight AND-OR (LOP3) operations and land as four fp32 pairs that feed
-// packed fp32x2 FMAs.  The constants are removed once per chunk:
-//   sum_k x_k (C_k + q_k) = sum_k x_k q_k + sum_k C_k x_k,
-// with sum_k C_k x_k precomputed per chunk of activations.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,57 +44,6 @@ __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p) {
     uint16_t v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
-}
-
-// ---------------------------------------------------------------- u4
-// Constants the magic windows add, per code position inside a word:
-// odd positions read as 256 + q, even positions as 16 + q.
-constexpr float kU4Odd = 256.0f;
-constexpr float kU4Even = 16.0f;
-
-// Eight 4-bit codes of one word -> four pairs (odd-position value,
-// even-position value):
-//   p[0] = (256+q3, 16+q4)   p[1] = (256+q5, 16+q6)
-//   p[2] = (256+q1, 16+q2)   p[3] = (256+q7, 16+q0)
-// Activations are stored in the matching order x3 x4 x5 x6 | x1 x2 x7 x0.
-// The shifts are written as multiplies so they run on the FMA pipe (the
-// logic pipe, which executes the eight AND-ORs, is half rate); one 64-bit
-// product yields both w << 19 (low word) and w >> 13 (high word).
-__device__ __forceinline__ void unpack_u4(uint32_t w, float2 (&p)[4]) {
-    const uint32_t lo_mask = 0x00078000u, lo_magic = 0x43800000u;  // 2^8
-    const uint32_t hi_mask = 0x00780000u, hi_magic = 0x41800000u;  // 2^4
-    const uint32_t t0 = w * 8u;                  // q3 -> [15,19), q4 -> [19,23)
-    const uint32_t t1 = __umulhi(w, 1u << 27);   // w >> 5: q5, q6
-    const uint32_t t2 = w * 2048u;               // w << 11: q1, q2
-    const unsigned long long t3 = (unsigned long long)w * (1ull << 19);
-    const uint32_t t3lo = (uint32_t)t3;          // q0 -> [19,23)
-    const uint32_t t3hi = (uint32_t)(t3 >> 32);  // q7 -> [15,19)
-    p[0] = make_float2(__uint_as_float((t0 & lo_mask) | lo_magic),
-                       __uint_as_float((t0 & hi_mask) | hi_magic));
-    p[1] = make_float2(__uint_as_float((t1 & lo_mask) | lo_magic),
-                       __uint_as_float((t1 & hi_mask) | hi_magic));
-    p[2] = make_float2(__uint_as_float((t2 & lo_mask) | lo_magic),
-                       __uint_as_float((t2 & hi_mask) | hi_magic));
-    p[3] = make_float2(__uint_as_float((t3hi & lo_mask) | lo_magic),
-                       __uint_as_float((t3lo & hi_mask) | hi_magic));
-}
-// Position of the activation that pairs with slot i of the unpacked word.
-__device__ __forceinline__ int u4_perm(int i) {
-    // x3 x4 x5 x6 x1 x2 x7 x0
-    return (0x07216543 >> (4 * i)) & 0xf;
-}
-
-// ---------------------------------------------------------------- u8
-constexpr float kU8Const = 256.0f;
-
-// Four 8-bit codes of one word -> two pairs (256+q0, 256+q1), (256+q2, 256+q3).
-// Shifts as multiplies, as for u4.
-__device__ __forceinline__ void unpack_u8(uint32_t w, float2 (&p)[2]) {
-    const uint32_t mask = 0x007f8000u, magic = 0x43800000u;  // [15,23), 2^8
-    p[0] = make_float2(__uint_as_float(((w * 32768u) & mask) | magic),
-                       __uint_as_float(((w * 128u) & mask) | magic));
-    p[1] = make_float2(__uint_as_float((__umulhi(w, 1u << 31) & mask) | magic),
-                       __uint_as_float((__umulhi(w, 1u << 23) & mask) | magic));
 }
 
 template <int BITS>

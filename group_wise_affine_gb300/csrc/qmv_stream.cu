@@ -1,4 +1,4 @@
-// Streaming decode kernels (M <= 2): the weight rows a CTA owns are copied
+// Streaming decode kernels (M <= 4): the weight rows a CTA owns are copied
 // into a shared-memory ring by the bulk-copy engine while the consumer
 // threads compute, so HBM sees a deep queue of large contiguous reads and the
 // consumers never wait on a per-thread load.
@@ -401,24 +401,27 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
 template <int BITS, int MT, int MODE>
 static cudaError_t launch_stream_t(const DenseParams &p, cudaStream_t st,
                                    bool *used) {
-    return launch_stream_r<BITS, MT, MODE, kRowsPerThread>(p, st, used);
+    // four tokens hold 64 registers of activations: two rows per thread
+    return launch_stream_r<BITS, MT, MODE, MT == 4 ? 2 : kRowsPerThread>(
+        p, st, used);
 }
 
 static bool aligned16(const void *q) {
     return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
 }
 
-// Launches the streaming kernel when the shape allows it (M <= 2, row
+// Launches the streaming kernel when the shape allows it (M <= 4, row
 // strides of scales multiple of 16 bytes, 16-byte aligned bases); *used
 // tells the caller whether it ran.
 cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
                           bool *used) {
     *used = false;
-    if (p.M > 2 || (p.G % 8) != 0 || !aligned16(p.sc) || !aligned16(p.bi) ||
+    if (p.M > 4 || (p.G % 8) != 0 || !aligned16(p.sc) || !aligned16(p.bi) ||
         !aligned16(p.wq))
         return cudaSuccess;
+    const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;
 #define GWA_STREAM_CASE(B, MTV)                                              \
-    if (p.bits == B && (MTV == 1 ? p.M == 1 : p.M == 2)) {                   \
+    if (p.bits == B && mt == MTV) {                                          \
         if (mode == kSPlain) return launch_stream_t<B, MTV, kSPlain>(p, st, used); \
         if (mode == kSSections)                                              \
             return launch_stream_t<B, MTV, kSSections>(p, st, used);         \
@@ -426,10 +429,20 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
     }
     GWA_STREAM_CASE(4, 1)
     GWA_STREAM_CASE(4, 2)
+    GWA_STREAM_CASE(4, 4)
     GWA_STREAM_CASE(8, 1)
     GWA_STREAM_CASE(8, 2)
+    GWA_STREAM_CASE(8, 4)
 #undef GWA_STREAM_CASE
     return cudaSuccess;
+}
+
+bool stream_eligible(const DenseParams &p) {
+    if ((p.G % 8) != 0 || !aligned16(p.sc) || !aligned16(p.bi) ||
+        !aligned16(p.wq))
+        return false;
+    const int nwh = (p.nch + kWarp - 1) / kWarp;
+    return nwh * kWarp + kWarp <= kStreamMaxThreads;
 }
 
 unsigned int stream_timeouts(bool reset) {
