@@ -43,6 +43,7 @@ constexpr int kQmmXStages = 6;       // activation ring depth
 constexpr int kXStageBytes = kQmmTok * 64 * 2;   // 16 KB, 128-byte swizzle
 constexpr size_t kQmmSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr int kStatusBytes = 256;
+constexpr int kQmmPrefetch = 4;      // code blocks loaded ahead per thread
 
 // status word bits
 constexpr unsigned kStTimeout = 1u;
@@ -265,12 +266,35 @@ struct QmmParams {
     unsigned int *status;
 };
 
+// Raw inputs of one K block for one weight row: the packed words and the
+// group's bf16 scale and bias (code blocks only).
+template <int BITS>
+struct RawBlock {
+    uint4 w[BITS == 4 ? 2 : 4];
+    uint16_t s, b;
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_raw(const QmmParams &p, int64_t n, int kb,
+                                         RawBlock<BITS> &r) {
+    constexpr int NV = BITS == 4 ? 2 : 4;  // 16-byte vectors per 64 codes
+    if (n < 0 || kb >= p.G) return;
+    const int64_t wpr = (int64_t)p.K * BITS / 32;
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(p.wq + n * wpr) + (int64_t)kb * NV;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.w[i] = ld_stream(src + i);
+    r.s = ld_u16(p.sc + n * p.G + kb);
+    r.b = ld_u16(p.bi + n * p.G + kb);
+}
+
 // fp16 dequantized columns of one K block for one weight row (the A tile
 // row), in the k order of the pre-pass.  u4: 32 columns; u8: 64 columns
 // (16s(qh-8) in the first 32, s(ql-8) in the last 32).
 template <int BITS>
 __device__ __forceinline__ void dequant_block(const QmmParams &p, int64_t n,
-                                              int kb, uint32_t (&a)[64],
+                                              int kb, const RawBlock<BITS> &r,
+                                              uint32_t (&a)[64],
                                               unsigned &flags) {
     constexpr int W = BITS == 4 ? 8 : 16;  // words per 64 codes
     constexpr int NC = BITS == 4 ? 32 : 64;
@@ -279,20 +303,16 @@ __device__ __forceinline__ void dequant_block(const QmmParams &p, int64_t n,
         for (int i = 0; i < NC; ++i) a[i] = 0u;
         return;
     }
-    const int64_t wpr = (int64_t)p.K * BITS / 32;
     if (kb < p.G) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.wq + n * wpr +
-                                                           (int64_t)kb * W);
         uint32_t w[W];
 #pragma unroll
         for (int i = 0; i < W / 4; ++i) {
-            const uint4 u = ld_stream(src + i);
-            w[4 * i] = u.x;
-            w[4 * i + 1] = u.y;
-            w[4 * i + 2] = u.z;
-            w[4 * i + 3] = u.w;
+            w[4 * i] = r.w[i].x;
+            w[4 * i + 1] = r.w[i].y;
+            w[4 * i + 2] = r.w[i].z;
+            w[4 * i + 3] = r.w[i].w;
         }
-        const float s = bf16_bits_to_f32(p.sc[n * p.G + kb]);
+        const float s = bf16_bits_to_f32(r.s);
         if (!(fabsf(s) <= 511.f) || (s != 0.f && fabsf(s) < 6.103515625e-05f))
             flags |= kStFp16Range;
         const __half2 off = __floats2half2_rn(1032.f, 1032.f);
@@ -463,34 +483,48 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             n = i < p.N ? i : -1;
         }
         unsigned flags = 0;
+        // A ring of raw code blocks, loaded kQmmPrefetch blocks ahead so
+        // the HBM latency of the codes overlaps the tensor-core work.
+        RawBlock<BITS> ring[kQmmPrefetch];
+#pragma unroll
+        for (int i = 0; i < kQmmPrefetch; ++i)
+            if (i < p.nkb) load_raw<BITS>(p, n, i, ring[i]);
         bool ok = true;  // pipeline healthy
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
-            const int sa = kb % SA;
-            // warp-uniform: tcgen05.st below is a warp-collective
-            if (kb >= SA &&
-                !__all_sync(0xffffffffu,
-                            qmm_wait(&aempty[sa], ((kb / SA) & 1) ^ 1, p.status))) {
-                ok = false;
-                break;
-            }
-            uint32_t a[64];
-            dequant_block<BITS>(p, n, kb, a, flags);
-            const uint32_t col = tmem_a + sa * (2 * AW) + tile * AW;
-            const uint32_t taddr = col + ((uint32_t)(q * 32) << 16);
-            uint32_t v0[32];
+        for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kQmmPrefetch) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v0[i] = a[i];
-            tc_st32(taddr, v0);
-            if constexpr (BITS == 8) {
-                uint32_t v1[32];
+            for (int i = 0; i < kQmmPrefetch; ++i) {
+                const int kb = kb0 + i;
+                if (kb >= p.nkb) break;
+                const int sa = kb % SA;
+                // warp-uniform: tcgen05.st below is a warp-collective
+                if (kb >= SA &&
+                    !__all_sync(0xffffffffu, qmm_wait(&aempty[sa],
+                                                      ((kb / SA) & 1) ^ 1,
+                                                      p.status))) {
+                    ok = false;
+                    break;
+                }
+                uint32_t a[64];
+                dequant_block<BITS>(p, n, kb, ring[i], a, flags);
+                if (kb + kQmmPrefetch < p.nkb)
+                    load_raw<BITS>(p, n, kb + kQmmPrefetch, ring[i]);
+                const uint32_t col = tmem_a + sa * (2 * AW) + tile * AW;
+                const uint32_t taddr = col + ((uint32_t)(q * 32) << 16);
+                uint32_t v0[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v1[i] = a[32 + i];
-                tc_st32(taddr + 32, v1);
+                for (int j = 0; j < 32; ++j) v0[j] = a[j];
+                tc_st32(taddr, v0);
+                if constexpr (BITS == 8) {
+                    uint32_t v1[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v1[j] = a[32 + j];
+                    tc_st32(taddr + 32, v1);
+                }
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[sa]);
             }
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[sa]);
         }
         if (flags) atomicOr(p.status, flags);
 
