@@ -199,7 +199,8 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
             q.y = p.y + t0 * out_stride;
         }
         bool used = false;
-        cudaError_t e = launch_stream(mode, q, st, &used);
+        cudaError_t e = launch_group(mode, q, st, &used);
+        if (e == cudaSuccess && !used) e = launch_stream(mode, q, st, &used);
         if (e == cudaSuccess && !used) e = launch_dense(mode, q, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
@@ -219,7 +220,8 @@ int gwa_pipeline_status(uint32_t *timeouts, int32_t reset) {
     if (!timeouts) return fail(GWA_ERR_INVALID_ARG, "gwa_pipeline_status: null");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "gwa_pipeline_status");
-    *timeouts = stream_timeouts(reset != 0) + qmm_timeouts(reset != 0);
+    *timeouts = group_timeouts(reset != 0) + stream_timeouts(reset != 0) +
+                qmm_timeouts(reset != 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, "gwa_pipeline_status");
 }

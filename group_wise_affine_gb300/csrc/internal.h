@@ -69,6 +69,10 @@ cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st);
 cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
                           bool *used);
 unsigned int stream_timeouts(bool reset);
+// One-token kernel with one quantization group per lane (qmv_group.cu).
+cudaError_t launch_group(int mode, const DenseParams &p, cudaStream_t st,
+                         bool *used);
+unsigned int group_timeouts(bool reset);
 // Whether the streaming kernel can run this shape (alignment, group count,
 // row length); M is ignored.
 bool stream_eligible(const DenseParams &p);
