@@ -123,6 +123,25 @@ cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
     return cudaSuccess;
 }
 
+// The streaming kernels ask for the largest shared-memory carveout: an SM
+// keeps one configuration from one of them to the next, so the next
+// kernel's CTA can start beside this one's (programmatic dependent launch)
+// instead of waiting for the SM to drain and reconfigure.
+cudaError_t prefer_max_shared(const void *kernel) {
+    static std::map<std::pair<int, const void *>, bool> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, kernel);
+    if (done[key]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) done[key] = true;
+    return e;
+}
+
 // ------------------------------------------------------------ validation
 static int check_qweight(const gwa_qweight &w, const char *fn) {
     if (w.bits != 4 && w.bits != 8)
@@ -221,7 +240,7 @@ int gwa_pipeline_status(uint32_t *timeouts, int32_t reset) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "gwa_pipeline_status");
     *timeouts = group_timeouts(reset != 0) + stream_timeouts(reset != 0) +
-                qmm_timeouts(reset != 0);
+                moe_stream_timeouts(reset != 0) + qmm_timeouts(reset != 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, "gwa_pipeline_status");
 }
@@ -369,11 +388,6 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
         return fail(GWA_ERR_MISALIGNED, "%s: ids/route_w/status/out alignment",
                     fn);
     const int nch = (int)(w.K * w.bits / 128);
-    const int cap = moe_max_tokens(w.bits, nch, mode);
-    if ((mode == 0 && cap < 1) || (mode == 1 && cap < M * topk))
-        return fail(GWA_ERR_UNSUPPORTED,
-                    "%s: M*topk=%lld inputs of K=%lld do not fit in shared "
-                    "memory", fn, (long long)(M * topk), (long long)w.K);
     if ((rc = check_device())) return rc;
     MoeParams p{};
     p.x = x;
@@ -393,8 +407,18 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
     p.out = out;
     p.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mode == GWA_MOE_GATE_UP_SILU ? launch_moe_gate_up(p, st)
-                                                 : launch_moe_down(p, st);
+    bool used = false;
+    cudaError_t e = launch_moe_stream(mode, p, st, &used);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (used) return GWA_OK;
+    // rows longer than the streaming kernel handles: staged kernels
+    const int cap = moe_max_tokens(w.bits, nch, mode);
+    if ((mode == 0 && cap < 1) || (mode == 1 && cap < M * topk))
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: M*topk=%lld inputs of K=%lld do not fit in shared "
+                    "memory", fn, (long long)(M * topk), (long long)w.K);
+    e = mode == GWA_MOE_GATE_UP_SILU ? launch_moe_gate_up(p, st)
+                                     : launch_moe_down(p, st);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return GWA_OK;
 }

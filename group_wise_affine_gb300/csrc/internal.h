@@ -60,10 +60,36 @@ cudaError_t launch_pdl(const void *kernel, unsigned grid, unsigned threads,
     return cudaLaunchKernelExC(&cfg, kernel, argv);
 }
 
+// The same with thread-block clusters of `cluster` CTAs along x (grid a
+// multiple of it).
+template <typename... Args>
+cudaError_t launch_pdl_cluster(const void *kernel, unsigned grid,
+                               unsigned cluster, unsigned threads,
+                               size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    void *argv[] = {reinterpret_cast<void *>(&args)...};
+    return cudaLaunchKernelExC(&cfg, kernel, argv);
+}
+
 // Blocks for a persistent grid: SMs x resident CTAs of `kernel`.
 cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
                            int *grid);
 int num_sms();
+// Largest shared-memory carveout for a streaming kernel (once per device).
+cudaError_t prefer_max_shared(const void *kernel);
 
 cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st);
 cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
@@ -99,6 +125,10 @@ struct MoeParams {
 cudaError_t launch_moe_gate_up(const MoeParams &p, cudaStream_t st);
 cudaError_t launch_moe_down(const MoeParams &p, cudaStream_t st);
 int moe_max_tokens(int bits, int nch, int mode);
+// Streaming MoE kernels (moe_stream.cu) for rows of up to 2048 inputs.
+cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
+                              bool *used);
+unsigned int moe_stream_timeouts(bool reset);
 
 cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
                                 int bits, uint8_t *codes, cudaStream_t st);

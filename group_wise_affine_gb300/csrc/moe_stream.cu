@@ -1,0 +1,633 @@
+// Streaming top-k MoE expert GEMV ("Sanctum-MLX": 3-D switch_mlp expert
+// grids; "Four Candles For The Cathedral", "What's not in this batch":
+// routed experts with per-expert gate_proj / up_proj, and the 6x regression
+// that came from duplicating expert weights).  Every distinct expert of the
+// call is read once, in place, from the caller's stacked tensor.
+//
+// Same pipeline as the one-token decode kernel (qmv_group.cu): a producer
+// thread fills a shared-memory ring with packed expert rows by bulk copy,
+// and consumer lanes each own one group of 64 inputs and form exact integer
+// dots (group_dot.cuh).  A row's groups fit in one slice of W lanes (W = 8,
+// 16 or 32 >= K/64), so a slice reduction yields the full row dot.  A bulk
+// copy costs the copy engine about 0.2 us whatever its size up to ~8 KB, so
+// only the codes travel by bulk copy, in copies of 10-30 KB; each lane reads
+// its rows' scale and bias with plain read-only loads issued two passes
+// ahead.
+//
+// Routing.  Each CTA first groups the slots (token, k) by expert, in
+// first-occurrence order, slots in slot order within a group.  Expert ids,
+// route weights and weights are inputs no kernel of this library writes, and
+// a kernel of any other kind completes before one of ours starts, so the
+// grouping and the weight prefetch run before the wait on the previous
+// kernel; only the activations (x, or the gate+up output h) wait for it.
+//
+// Gate+up mode.  Work units are (expert group, gate/up row pair); a CTA takes
+// an even share of the units, and a stage holds up to UPS pairs of one
+// expert (two copies: the gate rows and the up rows).  For every slot of the
+// stage's expert the consumers form the gate and up dots of its token and
+// write h[slot, i] = SiLU(g) * u.
+//
+// Down mode.  Clusters of CL CTAs (CL = 1, 2 or 4, as many as the GPU keeps
+// resident in one wave): a cluster owns a block of output rows, and its CTA
+// of rank c streams that block of the expert groups c, c + CL, ... (one copy
+// per expert), adding route_w[slot] *
+// (W[e] h[slot]) into its own accumulator of the slot's token.  At the end
+// the CTAs of the cluster add the accumulators of ranks 0, 1, ... through
+// distributed shared memory, so the combine is deterministic and needs no
+// atomics or global scratch.
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "group_dot.cuh"
+#include "internal.h"
+
+namespace gwa {
+
+static __device__ unsigned int g_moe_timeouts;
+
+// Eight warps at up to 128 registers: two CTAs (this kernel and the next one
+// in the stream) fit in an SM's 64K registers.
+constexpr int kMsConsumerWarps = 7;
+constexpr int kMsThreads = (kMsConsumerWarps + 1) * kWarp;
+// Dynamic shared memory per CTA: two CTAs per SM (228 KB, 1 KB reserved
+// each) less the static routing tables.
+constexpr size_t kMsSmemCap = 100 * 1024;
+constexpr int kMsMaxSlots = 256;
+constexpr int kMsMaxStages = 16;
+constexpr int kMsMaxCluster = 4;    // down: CTAs sharing a row block
+constexpr int kMsMaxRows = 128;     // down: output rows per cluster
+constexpr size_t kMsStageTarget = 32 * 1024;
+
+struct MsTables {
+    int ids[kMsMaxSlots];
+    int first[kMsMaxSlots];      // earliest slot with the same valid id, or -1
+    int gidx[kMsMaxSlots];       // group of a first slot
+    int gexp[kMsMaxSlots];       // expert of a group
+    int gstart[kMsMaxSlots + 1]; // slot range of a group in `order`
+    int order[kMsMaxSlots];      // slots grouped by expert
+    int imgrow[kMsMaxSlots];     // image row holding a slot's activations
+    int imgsrc[kMsMaxSlots];     // down: slot (source row) of an image row
+    float rw[kMsMaxSlots];
+    int ng, nimg;
+};
+
+// Stage k of this CTA: expert group, first unit, unit count.  Gate+up units
+// are pairs of group gi; down units are output rows of the cluster's block.
+struct MsStage {
+    int gi, u, n;
+};
+
+// A CTA's stages in order; producer and consumers walk the same sequence.
+// Gate+up: units [u0, u1) of ng*I, cut at group ends.  Down: groups g0,
+// g0 + step, ..., each the row block [u0, u1) in chunks of ups rows.
+struct MsWalk {
+    int mode, ups, step, g0, ng, nchunk;
+    int64_t I, u0, u1, cur;
+    __device__ bool next(MsStage &s) {
+        if (mode == 0) {
+            if (cur >= u1) return false;
+            const int gi = (int)(cur / I);
+            const int64_t ia = cur - (int64_t)gi * I;
+            const int64_t n = min(min((int64_t)ups, I - ia), u1 - cur);
+            s.gi = gi;
+            s.u = (int)ia;
+            s.n = (int)n;
+            cur += n;
+            return true;
+        }
+        const int64_t mine = ng > g0 ? (ng - g0 + step - 1) / step : 0;
+        if (cur >= mine * nchunk) return false;
+        const int j = (int)(cur / nchunk), c = (int)(cur - (int64_t)j * nchunk);
+        s.gi = g0 + j * step;
+        s.u = (int)u0 + c * ups;
+        s.n = (int)min((int64_t)ups, u1 - s.u);
+        ++cur;
+        return true;
+    }
+};
+
+// One pass of the consumers over a stage: rows [sb, sb + sbu) of each half.
+struct MsTask {
+    MsStage sg;
+    int k, sb;
+    bool last;  // the stage's final pass
+};
+
+struct MsTasks {
+    MsWalk w;
+    MsStage sg;
+    int k, sb, sbu;
+    bool have;
+    __device__ void init(const MsWalk &w0, int sbu_) {
+        w = w0;
+        sbu = sbu_;
+        k = 0;
+        sb = 0;
+        have = w.next(sg);
+    }
+    __device__ bool next(MsTask &t) {
+        if (!have) return false;
+        t.sg = sg;
+        t.k = k;
+        t.sb = sb;
+        t.last = sb + sbu >= sg.n;
+        sb += sbu;
+        if (sb >= sg.n) {
+            sb = 0;
+            ++k;
+            have = w.next(sg);
+        }
+        return true;
+    }
+};
+
+template <int RPH>
+struct MsScales {
+    uint16_t s[RPH], b[RPH];
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release;\n"
+        "barrier.cluster.wait.acquire;" ::
+            : "memory");
+}
+// fp32 at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float *local,
+                                                uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(a)
+                 : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+template <int BITS, int MODE, int W>
+__global__ void __maxnreg__(128)
+    moe_stream_kernel(MoeParams p, int stages, int rs, int ups, int cl,
+                      uint32_t img_off, uint32_t acc_off) {
+    constexpr int HALVES = MODE == 0 ? 2 : 1;
+    constexpr int UPT = MODE == 0 ? 1 : 2;  // units per row group and pass
+    constexpr int RPH = HALVES * UPT;       // rows per lane and pass (2)
+    constexpr int GB = BITS * 8;            // code bytes per row and group
+    const int CL = MODE == 0 ? 1 : cl;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ MsTables tb;
+    __shared__ int s_issued, s_consumed;
+    // down: accumulators [row of the cluster block][token]
+    float *acc = reinterpret_cast<float *>(smem + acc_off);
+
+    const int tid = threadIdx.x;
+    const int ncons = kMsConsumerWarps * kWarp;
+    const int lane = tid & (kWarp - 1);
+    const int S = p.M * p.topk;
+    const int64_t I = p.N / 2;
+    const int sbu = rs * UPT;
+    const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
+    const uint32_t stage_bytes = (uint32_t)(HALVES * ups) * rowbytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
+    uint64_t *empty = full + stages;
+    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+    const int64_t blk0 = MODE == 1 ? p.N * cid / ncl : 0;
+    const int64_t blk1 = MODE == 1 ? p.N * (cid + 1) / ncl : 0;
+    const int nblk = (int)(blk1 - blk0);
+
+    // ---------------------------------------------------- routing tables
+    for (int s = tid; s < S; s += blockDim.x) {
+        tb.ids[s] = p.ids[s];
+        tb.rw[s] = MODE == 1 ? p.route_w[s] : 0.f;
+    }
+    if (MODE == 1)
+        for (int i = tid; i < nblk * p.M; i += blockDim.x) acc[i] = 0.f;
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kMsConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    for (int s = tid; s < S; s += blockDim.x) {
+        const int e = tb.ids[s];
+        int f = -1;
+        if (e >= 0 && e < p.E) {
+            f = s;
+            for (int q = 0; q < s; ++q)
+                if (tb.ids[q] == e) {
+                    f = q;
+                    break;
+                }
+        } else if (p.status && blockIdx.x == 0) {
+            atomicOr(p.status, 1);
+        }
+        tb.first[s] = f;
+    }
+    __syncthreads();
+    for (int s = tid; s < S; s += blockDim.x) {
+        if (tb.first[s] != s) continue;
+        int gi = 0, start = 0;
+        for (int q = 0; q < S; ++q) {
+            gi += (q < s && tb.first[q] == q);
+            start += (tb.first[q] >= 0 && tb.first[q] < s);
+        }
+        tb.gidx[s] = gi;
+        tb.gexp[gi] = tb.ids[s];
+        tb.gstart[gi] = start;
+    }
+    if (tid == 0) {
+        int ng = 0, valid = 0;
+        for (int q = 0; q < S; ++q) {
+            ng += (tb.first[q] == q);
+            valid += (tb.first[q] >= 0);
+        }
+        tb.ng = ng;
+        tb.gstart[ng] = valid;
+        s_issued = 0;
+        s_consumed = 1 << 30;
+    }
+    __syncthreads();
+    for (int s = tid; s < S; s += blockDim.x) {
+        const int f = tb.first[s];
+        if (f < 0) continue;
+        int rank_in = 0;
+        for (int q = f; q < s; ++q) rank_in += (tb.first[q] == f);
+        tb.order[tb.gstart[tb.gidx[f]] + rank_in] = s;
+    }
+    __syncthreads();
+    // image rows: gate+up, the tokens; down, this CTA's slots in group order
+    if (tid == 0) {
+        if (MODE == 0) {
+            for (int s = 0; s < S; ++s) tb.imgrow[s] = s / p.topk;
+            tb.nimg = p.M;
+        } else {
+            int n = 0;
+            for (int gi = rank; gi < tb.ng; gi += CL)
+                for (int q = tb.gstart[gi]; q < tb.gstart[gi + 1]; ++q) {
+                    tb.imgrow[tb.order[q]] = n;
+                    tb.imgsrc[n++] = tb.order[q];
+                }
+            tb.nimg = n;
+        }
+        pdl_launch_dependents();
+    }
+    __syncthreads();
+
+    // this CTA's stages
+    MsWalk walk{};
+    walk.mode = MODE;
+    walk.ups = ups;
+    walk.I = I;
+    walk.ng = tb.ng;
+    walk.step = CL;
+    walk.g0 = rank;
+    if (MODE == 0) {
+        const int64_t units = (int64_t)tb.ng * I;
+        walk.u0 = units * blockIdx.x / gridDim.x;
+        walk.u1 = units * (blockIdx.x + 1) / gridDim.x;
+        walk.cur = walk.u0;
+    } else {
+        walk.u0 = blk0;
+        walk.u1 = blk1;
+        walk.nchunk = (int)((nblk + ups - 1) / ups);
+        if (nblk <= 0) walk.ng = 0;
+        walk.cur = 0;
+    }
+
+    if (tid >= ncons) {
+        // ------------------------------------------------ producer
+        if (tid == ncons) {
+            const unsigned char *wq =
+                reinterpret_cast<const unsigned char *>(p.wq);
+            MsWalk w = walk;
+            MsStage sg;
+            int k = 0;
+            while (w.next(sg)) {
+                const int s = k % stages;
+                if (k >= stages &&
+                    !mbar_wait(&empty[s], ((k / stages) & 1) ^ 1)) {
+                    atomicAdd(&g_moe_timeouts, 1u);
+                    break;
+                }
+                const int64_t e = tb.gexp[sg.gi];
+                unsigned char *base = smem + (size_t)s * stage_bytes;
+                mbar_expect_tx(&full[s], (uint32_t)(HALVES * sg.n) * rowbytes);
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    const int64_t r = e * p.N + sg.u + (h ? I : 0);
+                    bulk_g2s(base + (size_t)h * ups * rowbytes,
+                             wq + r * rowbytes, sg.n * rowbytes, &full[s]);
+                }
+                s_issued = ++k;
+            }
+        }
+    } else {
+        // ------------------------------------------------ consumers
+        const int hg = tid / W;                 // row group
+        const bool in_group = hg < rs;
+        const int hgc = in_group ? hg : 0;
+        const int g = tid & (W - 1);
+        const bool active = in_group && g < p.G;
+        const int gg = active ? g : 0;
+        unsigned char *img = smem + img_off;
+
+        // the lane's scale and bias of a pass (rows clamped into the stage)
+        auto fetch = [&](const MsTask &t, MsScales<RPH> &q) {
+            const int64_t e = tb.gexp[t.sg.gi];
+#pragma unroll
+            for (int j = 0; j < RPH; ++j) {
+                const int pos =
+                    min(t.sb + hgc * UPT + (j % UPT), t.sg.n - 1);
+                const int64_t row = e * p.N + t.sg.u + pos + (j / UPT ? I : 0);
+                q.s[j] = ld_u16(p.sc + row * p.G + gg);
+                q.b[j] = ld_u16(p.bi + row * p.G + gg);
+            }
+        };
+        MsTasks ahead;
+        ahead.init(walk, sbu);
+        MsTask ta, tb2;
+        MsScales<RPH> qa, qb;
+        bool ha = ahead.next(ta);
+        if (ha) fetch(ta, qa);
+        bool hb = ahead.next(tb2);
+        if (hb) fetch(tb2, qb);
+
+        pdl_wait_primary();  // x / h may be the previous kernel's output
+        encode_rows_shared<BITS>(p.x, tb.nimg, tb.nimg, p.K, p.G, tid, ncons,
+                                 img, MODE == 1 ? tb.imgsrc : nullptr);
+        asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
+
+        GroupX<1> gx;
+        int cached = -1;
+        // one pass; false when a wait ran out
+        auto process = [&](const MsTask &t, const MsScales<RPH> &q) -> bool {
+            const int s = t.k % stages;
+            if (t.sb == 0 && !mbar_wait(&full[s], (t.k / stages) & 1)) {
+                atomicAdd(&g_moe_timeouts, 1u);
+                atomicMin(&s_consumed, t.k);
+                return false;
+            }
+            const unsigned char *base = smem + (size_t)s * stage_bytes;
+            const int pos = t.sb + hgc * UPT;
+            uint4 wv[RPH][BITS / 2];
+            float sv[RPH], bv[RPH];
+#pragma unroll
+            for (int j = 0; j < RPH; ++j) {
+                const int r = (j / UPT) * ups +
+                              min(pos + (j % UPT), t.sg.n - 1);
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    base + (size_t)r * rowbytes + (size_t)gg * GB);
+#pragma unroll
+                for (int i = 0; i < BITS / 2; ++i) wv[j][i] = src[i];
+                sv[j] = bf16_bits_to_f32(q.s[j]);
+                bv[j] = bf16_bits_to_f32(q.b[j]);
+            }
+            if (t.last) {
+                // every lane's reads of this stage are done: release it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            for (int qi = tb.gstart[t.sg.gi]; qi < tb.gstart[t.sg.gi + 1]; ++qi) {
+                const int slot = tb.order[qi];
+                const int row = tb.imgrow[slot];
+                if (row != cached) {
+                    load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx);
+                    cached = row;
+                }
+                float v[RPH];
+#pragma unroll
+                for (int j = 0; j < RPH; ++j) {
+                    int d[1];
+                    group_dot<BITS, 1>(wv[j], gx, d);
+                    v[j] = fmaf(sv[j] * gx.f[0], (float)d[0], bv[j] * gx.xs[0]);
+                }
+                // slice lane 0 gets the total of row value 0; value 1 sits
+                // W/2 lanes up
+                const float tot = sub_reduce<W, RPH>(v, lane);
+                const float tot1 = __shfl_down_sync(0xffffffffu, tot, W / 2);
+                if (in_group && g == 0 && pos < t.sg.n) {
+                    if (MODE == 0) {
+                        p.out[(int64_t)slot * I + t.sg.u + pos] =
+                            f32_to_bf16_bits(tot / (1.0f + __expf(-tot)) * tot1);
+                    } else {
+                        const int tk = slot / p.topk;
+                        const float r = tb.rw[slot];
+                        float *a = acc + (size_t)(t.sg.u - blk0 + pos) * p.M + tk;
+                        a[0] += r * tot;
+                        if (pos + 1 < t.sg.n) a[p.M] += r * tot1;
+                    }
+                }
+            }
+            return true;
+        };
+        // two passes in flight: the scales of pass t+2 load while pass t runs
+        while (ha) {
+            if (!process(ta, qa)) break;
+            ha = ahead.next(ta);
+            if (ha) fetch(ta, qa);
+            if (!hb) break;
+            if (!process(tb2, qb)) break;
+            hb = ahead.next(tb2);
+            if (hb) fetch(tb2, qb);
+        }
+    }
+    __syncthreads();
+    pdl_wait_primary();  // outputs may alias the previous kernel's inputs
+    // A timed-out pipeline must not leave bulk copies landing in shared
+    // memory after the CTA exits: wait (again bounded) for every stage that
+    // was issued but not consumed.
+    if (tid == ncons && s_consumed < s_issued) {
+        for (int k = s_consumed; k < s_issued; ++k)
+            if (!mbar_wait(&full[k % stages], (k / stages) & 1)) break;
+    }
+
+    if (MODE == 0) {
+        // slots with an invalid expert: zero outputs, split over the CTAs
+        const int64_t i0 = I * blockIdx.x / gridDim.x;
+        const int64_t i1 = I * (blockIdx.x + 1) / gridDim.x;
+        for (int s = 0; s < S; ++s) {
+            if (tb.first[s] >= 0) continue;
+            for (int64_t i = i0 + tid; i < i1; i += blockDim.x)
+                p.out[(int64_t)s * I + i] = 0;
+        }
+    } else {
+        // every CTA of the cluster has finished its accumulators; rank c
+        // writes its share of the block, adding the ranks in order
+        cluster_sync_all();
+        const int r0 = nblk * rank / CL, r1 = nblk * (rank + 1) / CL;
+        for (int i = tid; i < (r1 - r0) * p.M; i += blockDim.x) {
+            const int r = r0 + i / p.M, t = i % p.M;
+            float y = 0.f;
+            for (int q = 0; q < CL; ++q)
+                y += ld_cluster_f32(acc + (size_t)r * p.M + t, (uint32_t)q);
+            p.out[(int64_t)t * p.N + blk0 + r] = f32_to_bf16_bits(y);
+        }
+        // no CTA leaves while another still reads its accumulators
+        cluster_sync_all();
+    }
+}
+
+// ------------------------------------------------------------ host side
+// Clusters of `cl` CTAs (one per SM) the GPU can keep resident at once
+// (cached per device, kernel, cluster size and shared memory).
+static int resident_clusters(const void *kern, int cl, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, kern, cl, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
+    cfg.blockDim = dim3(kMsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+template <int BITS, int MODE, int W>
+static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
+    constexpr int HALVES = MODE == 0 ? 2 : 1;
+    constexpr int UPT = MODE == 0 ? 1 : 2;
+    const int S = p.M * p.topk;
+    const size_t rowbytes = (size_t)p.K * BITS / 8;
+    const int rs = kMsConsumerWarps * kWarp / W;  // row groups per pass
+    const int sbu = rs * UPT;
+    int grid, ups, img_rows, nblk = 0, cl = 1;
+    if (MODE == 0) {
+        grid = num_sms();
+        // a stage holds whole passes, about kMsStageTarget bytes, and no
+        // more than a CTA's share
+        int passes = (int)(kMsStageTarget / ((size_t)HALVES * rowbytes * sbu));
+        if (passes < 1) passes = 1;
+        ups = passes * sbu;
+        const int64_t share = ((int64_t)S * (p.N / 2) + grid - 1) / grid;
+        if ((int64_t)ups > share) ups = (int)(share > 0 ? share : 1);
+        img_rows = p.M;
+    } else {
+        // clusters of up to kMsMaxCluster CTAs, one CTA per SM; the largest
+        // size whose clusters all fit in one wave is chosen below
+        cl = kMsMaxCluster;
+        int clusters = num_sms() / cl;
+        if ((int64_t)clusters > p.N) clusters = (int)p.N;
+        nblk = (int)((p.N + clusters - 1) / clusters);
+        ups = (nblk + UPT - 1) / UPT * UPT;  // one stage per expert
+        img_rows = S;
+        grid = clusters * cl;
+    }
+    auto kern = moe_stream_kernel<BITS, MODE, W>;
+    const size_t img = ximg_bytes(img_rows, p.G);
+    size_t stage_bytes, accb, img_off, acc_off, smem;
+    int stages;
+    cudaError_t e;
+    for (;;) {
+        stage_bytes = (size_t)HALVES * ups * rowbytes;
+        accb = MODE == 1 ? (size_t)nblk * p.M * 4 : 0;
+        const size_t fixed = 16 * kMsMaxStages + ((img + 15) / 16) * 16 + accb;
+        if (fixed >= kMsSmemCap) return cudaSuccess;
+        stages = (int)((kMsSmemCap - fixed) / stage_bytes);
+        if (stages > kMsMaxStages) stages = kMsMaxStages;
+        img_off = stages * stage_bytes + 16 * stages;
+        acc_off = img_off + ((img + 15) / 16) * 16;
+        smem = acc_off + accb;
+        const bool fits = stages >= 2 && (MODE == 0 || nblk <= kMsMaxRows);
+        if (fits) {
+            int dummy = 0;
+            e = occupancy_grid(reinterpret_cast<const void *>(kern),
+                               kMsThreads, smem, &dummy);
+            if (e != cudaSuccess) return e;
+        }
+        if (MODE == 0) {
+            if (!fits) return cudaSuccess;  // not used
+            break;
+        }
+        // down: keep this cluster size if all its clusters are resident
+        // at once, else try half of it
+        if (fits && (cl == 1 || resident_clusters(reinterpret_cast<const void *>(
+                                                      kern),
+                                                  cl, smem) >= grid / cl))
+            break;
+        if (cl == 1) return cudaSuccess;  // not used
+        cl /= 2;
+        int clusters = num_sms() / cl;
+        if ((int64_t)clusters > p.N) clusters = (int)p.N;
+        nblk = (int)((p.N + clusters - 1) / clusters);
+        ups = (nblk + UPT - 1) / UPT * UPT;
+        grid = clusters * cl;
+    }
+    e = prefer_max_shared(reinterpret_cast<const void *>(kern));
+    if (e != cudaSuccess) return e;
+    *used = true;
+    if (MODE == 0)
+        return launch_pdl(reinterpret_cast<const void *>(kern), grid,
+                          kMsThreads, smem, st, p, stages, rs, ups, 1,
+                          (uint32_t)img_off, (uint32_t)acc_off);
+    return launch_pdl_cluster(reinterpret_cast<const void *>(kern), grid,
+                              (unsigned)cl, kMsThreads, smem, st, p, stages,
+                              rs, ups, cl, (uint32_t)img_off,
+                              (uint32_t)acc_off);
+}
+
+template <int BITS, int MODE>
+static cudaError_t launch_ms_w(const MoeParams &p, cudaStream_t st,
+                               bool *used) {
+    if (p.G <= 8) return launch_ms<BITS, MODE, 8>(p, st, used);
+    if (p.G <= 16) return launch_ms<BITS, MODE, 16>(p, st, used);
+    return launch_ms<BITS, MODE, 32>(p, st, used);
+}
+
+// Launches the streaming MoE kernel when the shape allows it (K <= 2048,
+// 16-byte aligned codes and activations, the encoded activations within the
+// shared-memory budget); *used tells the caller whether it ran.
+cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
+                              bool *used) {
+    *used = false;
+    auto a16 = [](const void *q) {
+        return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
+    };
+    if (p.G > 32 || (p.G % 8) != 0 || !a16(p.wq) || !a16(p.x) ||
+        p.M * p.topk > kMsMaxSlots)
+        return cudaSuccess;
+    if (mode == 0)
+        return p.bits == 4 ? launch_ms_w<4, 0>(p, st, used)
+                           : launch_ms_w<8, 0>(p, st, used);
+    return p.bits == 4 ? launch_ms_w<4, 1>(p, st, used)
+                       : launch_ms_w<8, 1>(p, st, used);
+}
+
+unsigned int moe_stream_timeouts(bool reset) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_moe_timeouts, sizeof v);
+    if (reset) {
+        const unsigned int z = 0;
+        cudaMemcpyToSymbol(g_moe_timeouts, &z, sizeof z);
+    }
+    return v;
+}
+
+}  // namespace gwa

@@ -162,3 +162,89 @@ def test_out_of_range_expert_sets_status_and_contributes_zero():
                                  n_exp, 96, K, 4)
     assert_close(bf16_to_f64(y[0:1]), y0, "down bad slot 0")
     assert_close(bf16_to_f64(y[1:2]), y1, "down bad slot 1")
+
+
+def _valid_refs(ids, n_exp):
+    """ids with out-of-range entries replaced by expert 0, and the mask of
+    the valid slots (the oracle takes only valid ids)."""
+    valid = (ids >= 0) & (ids < n_exp)
+    return np.where(valid, ids, 0).astype(np.int32), valid
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K", [512, 1024, 2048])
+def test_streaming_repeats_invalid_ragged(bits, K):
+    # K/64 = 8, 16, 32 groups (one 8-, 16- or 32-lane slice per row); ids
+    # repeat within and across tokens and include out-of-range entries;
+    # rows per expert off every stage size
+    n_exp, I2, N = 7, 2 * 75, 133
+    gu = experts(1000 + K + bits, n_exp, I2, K, bits)
+    dn = experts(1100 + K + bits, n_exp, N, K, bits)
+    ids = np.array([[3, 3, 5, 9], [5, 1, 3, -2], [0, 5, 5, 6]], np.int32)
+    M, topk = ids.shape
+    good, valid = _valid_refs(ids, n_exp)
+    dids = torch.from_numpy(ids).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = synth.activations(1200 + K, M, K)
+    out = gwa.moe_qmv_gather(dev_bf16(x), dids,
+                             gwa.expert_view(dev_qweight(gu), n_exp), n_exp, 0,
+                             status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    ref = oracle.moe_gate_up_silu(x, good, gu.wq, gu.scales, gu.biases, n_exp,
+                                  I2, K, bits)
+    ref[~valid] = 0.0
+    o = bf16_to_f64(out)
+    assert np.all(o[~valid] == 0)
+    assert_close(o, ref, f"gate_up stream K={K} u{bits}")
+    rw = synth.bf16_values(synth.activations(1300 + K, M, topk)).copy()
+    hin = synth.activations(1400 + K, M * topk, K).reshape(M, topk, K)
+    status.zero_()
+    y = gwa.moe_qmv_gather(dev_bf16(hin), dids,
+                           gwa.expert_view(dev_qweight(dn), n_exp), n_exp, 1,
+                           route_w=torch.from_numpy(rw).cuda(), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    yref = oracle.moe_down_combine(hin, good, np.where(valid, rw, 0.0), dn.wq,
+                                   dn.scales, dn.biases, n_exp, N, K, bits)
+    assert_close(bf16_to_f64(y), yref, f"down stream K={K} u{bits}")
+
+
+def test_streaming_is_deterministic(moe_weights):
+    _, _, dgu, ddn = moe_weights
+    M = 8
+    ids, rw = synth.routing(synth.seed_for(4, 8, 0), M, TOPK, E)
+    dids = torch.from_numpy(ids).cuda()
+    x = dev_bf16(synth.activations(synth.seed_for(4, 9, 0), M, H))
+    h1 = gwa.moe_qmv_gather(x, dids, dgu, E, gwa.GWA_MOE_GATE_UP_SILU)
+    h2 = gwa.moe_qmv_gather(x, dids, dgu, E, gwa.GWA_MOE_GATE_UP_SILU)
+    assert torch.equal(h1, h2)
+    r = torch.from_numpy(rw).cuda()
+    y1 = gwa.moe_qmv_gather(h1, dids, ddn, E, gwa.GWA_MOE_DOWN_COMBINE,
+                            route_w=r)
+    y2 = gwa.moe_qmv_gather(h1, dids, ddn, E, gwa.GWA_MOE_DOWN_COMBINE,
+                            route_w=r)
+    assert torch.equal(y1, y2)
+
+
+def test_long_rows_use_the_staged_kernels():
+    # K = 2560 (40 groups) is past the streaming kernel's slice
+    n_exp, K, I2, N = 3, 2560, 2 * 40, 72
+    gu = experts(1500, n_exp, I2, K)
+    dn = experts(1510, n_exp, N, K)
+    ids = np.array([[2, 0], [1, 2]], np.int32)
+    M, topk = ids.shape
+    x = synth.activations(1520, M, K)
+    out = gwa.moe_qmv_gather(dev_bf16(x), torch.from_numpy(ids).cuda(),
+                             gwa.expert_view(dev_qweight(gu), n_exp), n_exp, 0)
+    ref = oracle.moe_gate_up_silu(x, ids, gu.wq, gu.scales, gu.biases, n_exp,
+                                  I2, K, 4)
+    assert_close(bf16_to_f64(out), ref, "gate_up long rows")
+    rw = np.array([[0.75, 0.25], [0.5, 0.5]], np.float32)
+    hin = synth.activations(1521, M * topk, K).reshape(M, topk, K)
+    y = gwa.moe_qmv_gather(dev_bf16(hin), torch.from_numpy(ids).cuda(),
+                           gwa.expert_view(dev_qweight(dn), n_exp), n_exp, 1,
+                           route_w=torch.from_numpy(rw).cuda())
+    yref = oracle.moe_down_combine(hin, ids, rw, dn.wq, dn.scales, dn.biases,
+                                   n_exp, N, K, 4)
+    assert_close(bf16_to_f64(y), yref, "down long rows")
