@@ -94,7 +94,7 @@ def kernel_sources_sha256() -> str:
     only reported while the sources it was taken on are unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("qmv_stream.cu", "common.cuh"):
+    for f in ("qmv_group.cu", "group_dot.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "group_wise_affine_gb300", "csrc", f),
                   "rb") as fh:
             h.update(fh.read())
@@ -104,7 +104,7 @@ def kernel_sources_sha256() -> str:
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch (read + write) recorded from one ncu capture in
     profiles/, or None when absent or taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", "qmv_stream_gate_up_27648x5120_m1.md")
+    path = os.path.join(ROOT, "profiles", "qmv_group_gate_up_27648x5120_m1.md")
     if kernel != "gate_up" or not os.path.exists(path):
         return None
     traffic = sha = None

@@ -123,10 +123,10 @@ cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
     return cudaSuccess;
 }
 
-// The streaming kernels ask for the largest shared-memory carveout: an SM
-// keeps one configuration from one of them to the next, so the next
-// kernel's CTA can start beside this one's (programmatic dependent launch)
-// instead of waiting for the SM to drain and reconfigure.
+// Largest shared-memory carveout for a kernel whose CTAs (about 110 KB each)
+// must sit two to an SM: the next kernel's CTA then starts beside this
+// one's (programmatic dependent launch) instead of waiting for the SM to
+// drain and reconfigure.
 cudaError_t prefer_max_shared(const void *kernel) {
     static std::map<std::pair<int, const void *>, bool> done;
     int dev = 0;

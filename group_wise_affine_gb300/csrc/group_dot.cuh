@@ -150,11 +150,35 @@ __device__ __forceinline__ void encode_rows_shared(
     }
 }
 
-// Image rows r0 .. r0+MT-1 of group g into registers (zeros when !active).
+// Bank-conflict-free reads of a row's group.  Lane g reads its group's
+// 16-byte code chunks starting at chunk rot(g), so the lanes whose groups
+// lie 128 bytes apart (4 apart for u4, 2 apart for u8) read different banks
+// in the same instruction.  Its activation pairs are loaded in the same
+// rotated order (image chunk shift), so the dot is unchanged.
+template <int BITS>
+__device__ __forceinline__ int chunk_rot(int g) {
+    return BITS == 4 ? (g >> 2) & 1 : (g >> 1) & 3;
+}
+template <int BITS>
+__device__ __forceinline__ int image_shift(int g) {
+    return (BITS == 4 ? 4 : 2) * chunk_rot<BITS>(g);
+}
+template <int BITS>
+__device__ __forceinline__ void lds_group(const unsigned char *src, int rot,
+                                          uint4 (&w)[BITS / 2]) {
+    constexpr int NV = BITS / 2;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        w[i] = reinterpret_cast<const uint4 *>(src)[(i + rot) & (NV - 1)];
+}
+
+// Image rows r0 .. r0+MT-1 of group g into registers (zeros when !active),
+// image chunks rotated by `shift` (see chunk_rot).
 template <int MT>
 __device__ __forceinline__ void load_group_rows(const unsigned char *img,
                                                 int R, int G, int r0, int g,
-                                                bool active, GroupX<MT> &gx) {
+                                                bool active, GroupX<MT> &gx,
+                                                int shift = 0) {
     const uint4 *pairs = reinterpret_cast<const uint4 *>(img);
     const float *xf = reinterpret_cast<const float *>(pairs + (size_t)R * 8 * G);
     const float *xsm = xf + (size_t)R * G;
@@ -163,7 +187,7 @@ __device__ __forceinline__ void load_group_rows(const unsigned char *img,
         const int r = r0 + m;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 t = pairs[((size_t)r * 8 + c) * G + g];
+            const uint4 t = pairs[((size_t)r * 8 + ((c + shift) & 7)) * G + g];
             gx.pr[m][4 * c] = t.x;
             gx.pr[m][4 * c + 1] = t.y;
             gx.pr[m][4 * c + 2] = t.z;

@@ -337,6 +337,7 @@ __global__ void __maxnreg__(128)
         const int g = tid & (W - 1);
         const bool active = in_group && g < p.G;
         const int gg = active ? g : 0;
+        const int rot = chunk_rot<BITS>(gg);
         unsigned char *img = smem + img_off;
 
         // the lane's scale and bias of a pass (rows clamped into the stage)
@@ -383,10 +384,8 @@ __global__ void __maxnreg__(128)
             for (int j = 0; j < RPH; ++j) {
                 const int r = (j / UPT) * ups +
                               min(pos + (j % UPT), t.sg.n - 1);
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    base + (size_t)r * rowbytes + (size_t)gg * GB);
-#pragma unroll
-                for (int i = 0; i < BITS / 2; ++i) wv[j][i] = src[i];
+                lds_group<BITS>(base + (size_t)r * rowbytes + (size_t)gg * GB,
+                                rot, wv[j]);
                 sv[j] = bf16_bits_to_f32(q.s[j]);
                 bv[j] = bf16_bits_to_f32(q.b[j]);
             }
@@ -399,7 +398,8 @@ __global__ void __maxnreg__(128)
                 const int slot = tb.order[qi];
                 const int row = tb.imgrow[slot];
                 if (row != cached) {
-                    load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx);
+                    load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx,
+                                       image_shift<BITS>(gg));
                     cached = row;
                 }
                 float v[RPH];

@@ -144,7 +144,9 @@ __global__ void __maxnreg__(88)
         // the consumer warps only (the producer is in its copy loop)
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
         GroupX<MT> gx;
-        load_group_rows<MT>(xenc, MT, p.G, 0, gg, active, gx);
+        const int rot = chunk_rot<BITS>(gg);
+        load_group_rows<MT>(xenc, MT, p.G, 0, gg, active, gx,
+                            image_shift<BITS>(gg));
         uint32_t offw[RPH], offs[RPH];
         const uint32_t sb_delta = rows_stage * (uint32_t)p.G * 2u;
 #pragma unroll
@@ -168,9 +170,7 @@ __global__ void __maxnreg__(88)
 #pragma unroll
             for (int j = 0; j < RPH; ++j) {
                 uint4 w[BITS / 2];
-#pragma unroll
-                for (int i = 0; i < BITS / 2; ++i)
-                    w[i] = reinterpret_cast<const uint4 *>(base + offw[j])[i];
+                lds_group<BITS>(base + offw[j], rot, w);
                 const float sv = bf16_bits_to_f32(
                     *reinterpret_cast<const uint16_t *>(base + offs[j]));
                 const float bv = bf16_bits_to_f32(
@@ -271,8 +271,6 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     int dummy = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    threads, smem, &dummy);
-    if (e != cudaSuccess) return e;
-    e = prefer_max_shared(reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,

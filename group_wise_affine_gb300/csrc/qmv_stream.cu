@@ -393,8 +393,6 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    threads, smem, &dummy);
     if (e != cudaSuccess) return e;
-    e = prefer_max_shared(reinterpret_cast<const void *>(kern));
-    if (e != cudaSuccess) return e;
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,
                       smem, st, p, stages, units, rs);
