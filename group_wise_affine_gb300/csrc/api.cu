@@ -226,6 +226,26 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
     return GWA_OK;
 }
 
+// M > 8: the tensor-core kernel when the shape allows it, else the decode
+// kernels in passes of up to eight tokens.  The workspace contract is the
+// same either way.
+static int run_prefill(const QmmArgs &a, int mode, const DenseParams &p,
+                       int64_t out_stride, const int64_t *sec_sizes,
+                       void *workspace, size_t workspace_bytes,
+                       cudaStream_t st, const char *fn) {
+    if (qmm_eligible(a)) return qmm_run(a, workspace, workspace_bytes, st);
+    const size_t need = qmm_workspace_bytes(a.M, a.w.K);
+    if (!workspace || workspace_bytes < need)
+        return fail(GWA_ERR_WORKSPACE,
+                    "%s: M=%lld K=%lld needs %zu bytes of workspace (got %zu)",
+                    fn, (long long)a.M, (long long)a.w.K, need,
+                    workspace_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return fail(GWA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned",
+                    fn);
+    return run_dense(mode, p, a.M, out_stride, sec_sizes, st, fn);
+}
+
 }  // namespace gwa
 
 using namespace gwa;
@@ -262,13 +282,14 @@ int gwa_qmv_affine(const uint16_t *x, int64_t M, gwa_qweight w, uint16_t *y,
     if (!aligned(y, 2)) return fail(GWA_ERR_MISALIGNED, "%s: y alignment", fn);
     if ((rc = check_device())) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DenseParams p = dense_base(x, M, w);
+    p.y = y;
     if (M > 8) {
         QmmArgs a{};
         a.x = x; a.M = M; a.w = w; a.mode = 0; a.y = y;
-        return qmm_run(a, workspace, workspace_bytes, st);
+        return run_prefill(a, 0, p, w.N, nullptr, workspace, workspace_bytes,
+                           st, fn);
     }
-    DenseParams p = dense_base(x, M, w);
-    p.y = y;
     return run_dense(0, p, M, w.N, nullptr, st, fn);
 }
 
@@ -324,7 +345,8 @@ int gwa_qmv_fused_sections(const uint16_t *x, int64_t M, gwa_qweight w,
             a.sec_out[s] = p.sec_out[s];
             a.sec_bias[s] = p.sec_bias[s];
         }
-        return qmm_run(a, workspace, workspace_bytes, st);
+        return run_prefill(a, 1, p, 0, section_sizes, workspace,
+                           workspace_bytes, st, fn);
     }
     return run_dense(1, p, M, 0, section_sizes, st, fn);
 }
@@ -345,14 +367,15 @@ int gwa_qmv_gate_up_silu(const uint16_t *x, int64_t M, gwa_qweight w,
     if (!aligned(h, 2)) return fail(GWA_ERR_MISALIGNED, "%s: h alignment", fn);
     if ((rc = check_device())) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M > 8) {
-        QmmArgs a{};
-        a.x = x; a.M = M; a.w = w; a.mode = 2; a.y = h;
-        return qmm_run(a, workspace, workspace_bytes, st);
-    }
     DenseParams p = dense_base(x, M, w);
     p.y = h;
     p.I = w.N / 2;
+    if (M > 8) {
+        QmmArgs a{};
+        a.x = x; a.M = M; a.w = w; a.mode = 2; a.y = h;
+        return run_prefill(a, 2, p, w.N / 2, nullptr, workspace,
+                           workspace_bytes, st, fn);
+    }
     return run_dense(2, p, M, w.N / 2, nullptr, st, fn);
 }
 

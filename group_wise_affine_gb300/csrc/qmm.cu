@@ -15,15 +15,21 @@
 // are converted to fp16 once per call by a pre-pass (exact for |x| in fp16's
 // normal range); products are exact and accumulate in fp32 in tensor memory.
 //
-// Kernel shape.  A CTA computes two 128-row weight tiles (for gate+up: the
-// gate tile and the matching up tile) against 128 tokens:
-//   warp 0    allocates tensor memory, loads the activation tile of each
-//             64-wide K block with TMA (128-byte swizzle) into a smem ring;
+// Kernel shape.  A CTA computes one 128-row weight tile (for gate+up: 64 gate
+// rows and the matching 64 up rows) against NT = 128 or 256 tokens, one MMA
+// of M = 128, N = NT, K = 16 per 16 columns:
+//   warp 0    allocates tensor memory and, from one thread, loads with TMA
+//             per 64-wide K block the activation tile (128-byte swizzle),
+//             the packed code tile of the 128 rows, and per 8 K blocks the
+//             rows' scale and bias tiles, into shared-memory rings;
 //   warp 1    issues tcgen05.mma (A from tensor memory, B from smem);
-//   warps 2-9 dequantize: thread (tile, row) turns its row's 64 codes of the
-//             K block into 32 fp16 pairs and writes them to tensor memory
-//             with tcgen05.st (the A operand), then reads the fp32
-//             accumulators back with tcgen05.ld for the epilogue.
+//   warps 2-17 dequantize: four warps per tensor-memory lane quarter take
+//             every fourth K block, so each has four MMA periods for its
+//             block; a thread turns its row's codes into fp16 pairs and
+//             writes them to tensor memory with tcgen05.st (the A operand),
+//             then reads the fp32 accumulators back with tcgen05.ld for the
+//             epilogue (gate+up: the gate warps pass their values to the up
+//             warps through shared memory).
 // Every wait is bounded (2 s); a wait that runs out flags the workspace
 // status word and the kernel unwinds without hanging.
 #include <cuda.h>
@@ -36,14 +42,12 @@
 
 namespace gwa {
 
-constexpr int kQmmThreads = 320;     // 10 warps
-constexpr int kQmmTok = 128;         // tokens per CTA (MMA N)
-constexpr int kQmmRows = 128;        // rows per weight tile (MMA M)
-constexpr int kQmmXStages = 6;       // activation ring depth
-constexpr int kXStageBytes = kQmmTok * 64 * 2;   // 16 KB, 128-byte swizzle
-constexpr size_t kQmmSmem = 120 * 1024;  // > half an SM: one CTA per SM
+constexpr int kQmmDeqWarps = 16;     // four per tensor-memory lane quarter
+constexpr int kQmmThreads = (2 + kQmmDeqWarps) * 32;
+constexpr int kQmmRows = 128;        // weight rows per CTA (MMA M)
+constexpr int kQmmWStages = 8;       // code-tile ring
+constexpr int kQmmSStages = 2;       // scale/bias-tile ring (8 K blocks each)
 constexpr int kStatusBytes = 256;
-constexpr int kQmmPrefetch = 4;      // code blocks loaded ahead per thread
 
 // status word bits
 constexpr unsigned kStTimeout = 1u;
@@ -97,20 +101,6 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem,
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, "
-        "%7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
-        "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-            taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
-        "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
-        "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
-        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
 __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -156,11 +146,30 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
-// N = 128 tokens, M = 128 rows.
-constexpr uint32_t kIdesc = (1u << 4)                    // D format f32
-                            | (0u << 7) | (0u << 10)     // A, B: f16
-                            | ((uint32_t)(kQmmTok >> 3) << 17)
-                            | ((uint32_t)(kQmmRows >> 4) << 24);
+// N = NT tokens, M = 128 rows.
+template <int NT>
+__device__ __forceinline__ constexpr uint32_t qmm_idesc() {
+    return (1u << 4)                           // D format f32
+           | (0u << 7) | (0u << 10)            // A, B: f16
+           | ((uint32_t)(NT >> 3) << 17)       // N
+           | ((uint32_t)(kQmmRows >> 4) << 24);  // M
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, "
+        "%7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
+        "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+        "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+        "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) {
     return *reinterpret_cast<uint32_t *>(&h);
@@ -249,11 +258,9 @@ __global__ void qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M,
 struct QmmParams {
     int64_t M;
     int K;
-    int64_t kext;
     int nkb;             // K blocks including the bias blocks
     int G;
-    const uint32_t *wq;
-    const uint16_t *sc;
+    const uint16_t *sc;  // [N, G] (bias blocks read it directly)
     const uint16_t *bi;
     int64_t N;           // weight rows
     int64_t I;           // gate+up: N / 2
@@ -266,202 +273,213 @@ struct QmmParams {
     unsigned int *status;
 };
 
-// Raw inputs of one K block for one weight row: the packed words and the
-// group's bf16 scale and bias (code blocks only).
-template <int BITS>
-struct RawBlock {
-    uint4 w[BITS == 4 ? 2 : 4];
-    uint16_t s, b;
+// Shared-memory layout (1024-byte aligned regions).
+template <int BITS, int NT>
+struct QmmLayout {
+    static constexpr int AW = BITS == 4 ? 32 : 64;  // A columns per K block
+    static constexpr int SA = (512 - NT) / AW > 8 ? 8 : (512 - NT) / AW;
+    static constexpr int XS = NT == 256 ? 4 : 6;      // activation tiles
+    static constexpr int XBYTES = NT * 128;           // 64 fp16 per token
+    static constexpr int WBYTES = kQmmRows * BITS * 8;  // 64 codes per row
+    static constexpr int SBYTES = kQmmRows * 16;      // 8 bf16 per row
+    static constexpr size_t XOFF = 0;
+    static constexpr size_t WOFF = XOFF + (size_t)XS * XBYTES;
+    static constexpr size_t SOFF = WOFF + (size_t)kQmmWStages * WBYTES;
+    static constexpr size_t BYTES = SOFF + (size_t)kQmmSStages * SBYTES;
+    static constexpr size_t SMEM = BYTES + 1024;      // alignment slack
 };
 
+// fp16 columns of one code K block for one weight row, in the pre-pass's
+// k order.  u4: 8 words -> 32 columns; u8: 16 words -> 32 columns of
+// 16s(qh-8) and 32 of s(ql-8).
 template <int BITS>
-__device__ __forceinline__ void load_raw(const QmmParams &p, int64_t n, int kb,
-                                         RawBlock<BITS> &r) {
-    constexpr int NV = BITS == 4 ? 2 : 4;  // 16-byte vectors per 64 codes
-    if (n < 0 || kb >= p.G) return;
-    const int64_t wpr = (int64_t)p.K * BITS / 32;
-    const uint4 *src =
-        reinterpret_cast<const uint4 *>(p.wq + n * wpr) + (int64_t)kb * NV;
+__device__ __forceinline__ void dequant_row(const uint32_t *w, float s,
+                                            uint32_t *hi, uint32_t *lo) {
+    const __half2 off = __floats2half2_rn(1032.f, 1032.f);
+    if constexpr (BITS == 4) {
+        const __half2 s2 = __floats2half2_rn(s, s);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) r.w[i] = ld_stream(src + i);
-    r.s = ld_u16(p.sc + n * p.G + kb);
-    r.b = ld_u16(p.bi + n * p.G + kb);
-}
-
-// fp16 dequantized columns of one K block for one weight row (the A tile
-// row), in the k order of the pre-pass.  u4: 32 columns; u8: 64 columns
-// (16s(qh-8) in the first 32, s(ql-8) in the last 32).
-template <int BITS>
-__device__ __forceinline__ void dequant_block(const QmmParams &p, int64_t n,
-                                              int kb, const RawBlock<BITS> &r,
-                                              uint32_t (&a)[64],
-                                              unsigned &flags) {
-    constexpr int W = BITS == 4 ? 8 : 16;  // words per 64 codes
-    constexpr int NC = BITS == 4 ? 32 : 64;
-    if (n < 0) {
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int i = 0; i < NC; ++i) a[i] = 0u;
-        return;
-    }
-    if (kb < p.G) {
-        uint32_t w[W];
-#pragma unroll
-        for (int i = 0; i < W / 4; ++i) {
-            w[4 * i] = r.w[i].x;
-            w[4 * i + 1] = r.w[i].y;
-            w[4 * i + 2] = r.w[i].z;
-            w[4 * i + 3] = r.w[i].w;
-        }
-        const float s = bf16_bits_to_f32(r.s);
-        if (!(fabsf(s) <= 511.f) || (s != 0.f && fabsf(s) < 6.103515625e-05f))
-            flags |= kStFp16Range;
-        const __half2 off = __floats2half2_rn(1032.f, 1032.f);
-        if constexpr (BITS == 4) {
-            const __half2 s2 = __floats2half2_rn(s, s);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // (1024 + q_i, 1024 + q_{i+4}) -> s * (q - 8), exact
-                    uint32_t t = ((w[j] >> (4 * i)) & 0x000f000fu) | 0x64006400u;
-                    __half2 h = *reinterpret_cast<__half2 *>(&t);
-                    a[4 * j + i] = h2_bits(__hmul2(__hsub2(h, off), s2));
-                }
-        } else {
-            const __half2 s1 = __floats2half2_rn(s, s);
-            const __half2 s16 = __floats2half2_rn(16.f * s, 16.f * s);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                // bytes (q0, q1, q2, q3); pairs in k order (0,2) (1,3)
-                uint32_t l0 = (w[j] & 0x000f000fu) | 0x64006400u;          // ql0 ql2
-                uint32_t l1 = ((w[j] >> 8) & 0x000f000fu) | 0x64006400u;   // ql1 ql3
-                uint32_t h0 = ((w[j] >> 4) & 0x000f000fu) | 0x64006400u;   // qh0 qh2
-                uint32_t h1 = ((w[j] >> 12) & 0x000f000fu) | 0x64006400u;  // qh1 qh3
-                a[2 * j] = h2_bits(
-                    __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&h0), off), s16));
-                a[2 * j + 1] = h2_bits(
-                    __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&h1), off), s16));
-                a[32 + 2 * j] = h2_bits(
-                    __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&l0), off), s1));
-                a[32 + 2 * j + 1] = h2_bits(
-                    __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&l1), off), s1));
+            for (int i = 0; i < 4; ++i) {
+                // (1024 + q_i, 1024 + q_{i+4}) -> s * (q - 8), exact
+                uint32_t t = ((w[j] >> (4 * i)) & 0x000f000fu) | 0x64006400u;
+                __half2 h = *reinterpret_cast<__half2 *>(&t);
+                hi[4 * j + i] = h2_bits(__hmul2(__hsub2(h, off), s2));
             }
-        }
     } else {
-        // bias block: column pair c holds bias columns 2c, 2c+1 of this
-        // block; bias column j belongs to group j/3 (hi, hi, lo)
-        const int base = (kb - p.G) * 64;
-        const float k8 = BITS == 4 ? 8.f : 136.f;
+        const __half2 s1 = __floats2half2_rn(s, s);
+        const __half2 s16 = __floats2half2_rn(16.f * s, 16.f * s);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            float e[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = base + 2 * c + h;
-                const int g = j / 3, which = j - 3 * g;
-                float val = 0.f;
-                if (g < p.G) {
-                    const float s = bf16_bits_to_f32(p.sc[n * p.G + g]);
-                    const float b = bf16_bits_to_f32(p.bi[n * p.G + g]);
-                    const float bp = fmaf(k8, s, b);
-                    const float hi = __half2float(__float2half_rn(bp));
-                    val = which < 2 ? hi : bp - hi;
-                    if (fabsf(bp) > 65504.f) flags |= kStFp16Range;
-                }
-                e[h] = val;
-            }
-            a[c] = h2_bits(__floats2half2_rn(e[0], e[1]));
-        }
-        if constexpr (BITS == 8) {
-#pragma unroll
-            for (int c = 32; c < 64; ++c) a[c] = 0u;
+        for (int j = 0; j < 16; ++j) {
+            // bytes (q0, q1, q2, q3); pairs in k order (0,2) (1,3)
+            uint32_t l0 = (w[j] & 0x000f000fu) | 0x64006400u;
+            uint32_t l1 = ((w[j] >> 8) & 0x000f000fu) | 0x64006400u;
+            uint32_t h0 = ((w[j] >> 4) & 0x000f000fu) | 0x64006400u;
+            uint32_t h1 = ((w[j] >> 12) & 0x000f000fu) | 0x64006400u;
+            hi[2 * j] = h2_bits(
+                __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&h0), off), s16));
+            hi[2 * j + 1] = h2_bits(
+                __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&h1), off), s16));
+            lo[2 * j] = h2_bits(
+                __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&l0), off), s1));
+            lo[2 * j + 1] = h2_bits(
+                __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&l1), off), s1));
         }
     }
 }
 
+// Bias block (K block kb >= G) for row n: column pair c holds bias columns
+// 2c, 2c+1 of the block; bias column j belongs to group j/3 (hi, hi, lo of
+// b' = b + 8s or b + 136s).
 template <int BITS>
+__device__ __forceinline__ void bias_row(const QmmParams &p, int64_t n, int kb,
+                                         uint32_t *a, unsigned &flags) {
+    const int base = (kb - p.G) * 64;
+    const float k8 = BITS == 4 ? 8.f : 136.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        float e[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int j = base + 2 * c + hh;
+            const int g = j / 3, which = j - 3 * g;
+            float val = 0.f;
+            if (n >= 0 && g < p.G) {
+                const float s = bf16_bits_to_f32(ld_u16(p.sc + n * p.G + g));
+                const float b = bf16_bits_to_f32(ld_u16(p.bi + n * p.G + g));
+                const float bp = fmaf(k8, s, b);
+                const float hi = __half2float(__float2half_rn(bp));
+                val = which < 2 ? hi : bp - hi;
+                if (fabsf(bp) > 65504.f) flags |= kStFp16Range;
+            }
+            e[hh] = val;
+        }
+        a[c] = h2_bits(__floats2half2_rn(e[0], e[1]));
+    }
+}
+
+template <int BITS, int NT>
 __global__ void __launch_bounds__(kQmmThreads, 1)
-    qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, QmmParams p) {
-    constexpr int AW = BITS == 4 ? 32 : 64;     // A columns per tile per block
-    constexpr int SA = 256 / (2 * AW);          // A stages in tensor memory
+    qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                  const __grid_constant__ CUtensorMap wmap,
+                  const __grid_constant__ CUtensorMap smap, QmmParams p) {
+    using L = QmmLayout<BITS, NT>;
+    constexpr int AW = L::AW, SA = L::SA, XS = L::XS;
+    constexpr int WS = kQmmWStages, SS = kQmmSStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte aligned ring for the 128-byte swizzle atoms
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t xfull[kQmmXStages], xempty[kQmmXStages];
-    __shared__ uint64_t afull[SA], aempty[SA], dfull;
+    __shared__ uint64_t xfull[XS], xempty[XS], wfull[WS], wempty[WS];
+    __shared__ uint64_t sfull[SS], sempty[SS], afull[SA], aempty[SA], dfull;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_xissued, s_xconsumed;
+    __shared__ int s_xn, s_wn, s_sn;  // TMA loads issued per ring
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * kQmmTok;
+    const int64_t m0 = (int64_t)blockIdx.y * NT;
     const bool gate_up = p.mode == 2;
-    const int64_t r0 = (int64_t)blockIdx.x * (gate_up ? kQmmRows : 2 * kQmmRows);
+    // first row of the tile (gate+up: first gate/up pair)
+    const int64_t r0 = (int64_t)blockIdx.x * (gate_up ? kQmmRows / 2 : kQmmRows);
+    const int G = p.G;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kQmmXStages; ++i) {
+        for (int i = 0; i < XS; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
+        for (int i = 0; i < WS; ++i) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wempty[i], 4);
+        }
+        for (int i = 0; i < SS; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], kQmmDeqWarps);
+        }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(&afull[i], 8);
+            mbar_init(&afull[i], 4);
             mbar_init(&aempty[i], 1);
         }
         mbar_init(&dfull, 1);
         fence_mbar_init();
-        s_xissued = 0;
-        s_xconsumed = p.nkb;
-        asm volatile("prefetch.tensormap [%0];" ::"l"(
-                         reinterpret_cast<uint64_t>(&xmap))
-                     : "memory");
+        s_xn = s_wn = s_sn = 0;
+        const CUtensorMap *maps[3] = {&xmap, &wmap, &smap};
+        for (int i = 0; i < 3; ++i)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(
+                             reinterpret_cast<uint64_t>(maps[i]))
+                         : "memory");
     }
     if (warp == 0) tmem_alloc(&s_tmem, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tmem_d = tmem;          // D0: cols [0,128), D1: [128,256)
-    const uint32_t tmem_a = tmem + 256;    // A stages
+    const uint32_t tmem_d = tmem;       // accumulators: cols [0, NT)
+    const uint32_t tmem_a = tmem + NT;  // A stages
 
     if (warp == 0) {
-        // -------------------------------------------- activation loader
+        // -------------------------------------------- TMA loader
         if (lane == 0) {
+            const int rows = gate_up ? kQmmRows / 2 : kQmmRows;
             for (int kb = 0; kb < p.nkb; ++kb) {
-                const int s = kb % kQmmXStages;
-                if (kb >= kQmmXStages &&
-                    !qmm_wait(&xempty[s], ((kb / kQmmXStages) & 1) ^ 1, p.status))
+                if (kb < G && kb % 8 == 0) {
+                    // scale tiles of K blocks kb .. kb+7 (the code blocks'
+                    // biases enter through the bias columns)
+                    const int sb = kb / 8, s = sb % SS;
+                    if (sb >= SS &&
+                        !qmm_wait(&sempty[s], ((sb / SS) & 1) ^ 1, p.status))
+                        break;
+                    unsigned char *ds = smem + L::SOFF + (size_t)s * L::SBYTES;
+                    mbar_expect_tx(&sfull[s], L::SBYTES);
+                    tma_load_2d(ds, &smap, kb, (int)r0, &sfull[s]);
+                    if (gate_up)
+                        tma_load_2d(ds + rows * 16, &smap, kb, (int)(p.I + r0),
+                                    &sfull[s]);
+                    s_sn = sb + 1;
+                }
+                if (kb < G) {
+                    // packed codes of the tile's rows
+                    const int s = kb % WS;
+                    if (kb >= WS &&
+                        !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status))
+                        break;
+                    unsigned char *dw = smem + L::WOFF + (size_t)s * L::WBYTES;
+                    const int wx = kb * BITS * 2;  // 32-bit words
+                    mbar_expect_tx(&wfull[s], L::WBYTES);
+                    tma_load_2d(dw, &wmap, wx, (int)r0, &wfull[s]);
+                    if (gate_up)
+                        tma_load_2d(dw + rows * BITS * 8, &wmap, wx,
+                                    (int)(p.I + r0), &wfull[s]);
+                    s_wn = kb + 1;
+                }
+                const int sx = kb % XS;
+                if (kb >= XS &&
+                    !qmm_wait(&xempty[sx], ((kb / XS) & 1) ^ 1, p.status))
                     break;
-                mbar_expect_tx(&xfull[s], kXStageBytes);
-                tma_load_2d(smem + s * kXStageBytes, &xmap, kb * 64, (int)m0,
-                            &xfull[s]);
-                s_xissued = kb + 1;
+                mbar_expect_tx(&xfull[sx], L::XBYTES);
+                tma_load_2d(smem + L::XOFF + (size_t)sx * L::XBYTES, &xmap,
+                            kb * 64, (int)m0, &xfull[sx]);
+                s_xn = kb + 1;
             }
         }
     } else if (warp == 1) {
         // -------------------------------------------- MMA issuer
         if (lane == 0) {
-            int kb = 0;
-            for (; kb < p.nkb; ++kb) {
-                const int sx = kb % kQmmXStages, sa = kb % SA;
-                if (!qmm_wait(&xfull[sx], (kb / kQmmXStages) & 1, p.status) ||
-                    !qmm_wait(&afull[sa], (kb / SA) & 1, p.status)) {
-                    atomicMin(&s_xconsumed, kb);
+            constexpr uint32_t idesc = qmm_idesc<NT>();
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                const int sx = kb % XS, sa = kb % SA;
+                if (!qmm_wait(&xfull[sx], (kb / XS) & 1, p.status) ||
+                    !qmm_wait(&afull[sa], (kb / SA) & 1, p.status))
                     break;
-                }
                 tc_fence_after();
-                const uint32_t xs = smem_u32(smem + sx * kXStageBytes);
-                const int subs = (BITS == 8 && kb < p.G) ? 2 : 1;
+                const uint32_t xs = smem_u32(smem + L::XOFF + (size_t)sx * L::XBYTES);
+                const int subs = (BITS == 8 && kb < G) ? 2 : 1;
+                for (int sub = 0; sub < subs; ++sub)
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
-                    for (int sub = 0; sub < subs; ++sub)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t a = tmem_a + sa * (2 * AW) + t * AW +
-                                               sub * 32 + kk * 8;
-                            const uint64_t bdesc = smem_desc_sw128(xs + kk * 32);
-                            tc_mma_ts(tmem_d + t * kQmmTok, a, bdesc, kIdesc,
-                                      (kb | sub | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a = tmem_a + sa * AW + sub * 32 + kk * 8;
+                        const uint64_t bdesc = smem_desc_sw128(xs + kk * 32);
+                        tc_mma_ts(tmem_d, a, bdesc, idesc, (kb | sub | kk) != 0);
+                    }
                 tc_commit(&xempty[sx]);
                 tc_commit(&aempty[sa]);
             }
@@ -470,106 +488,129 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         }
     } else {
         // -------------------------------------------- dequantizers
-        const int pw = warp - 2;              // 0..7
-        const int tile = pw / 4;              // weight tile 0 or 1
         const int q = warp & 3;               // tensor-memory lane quarter
+        const int ph = (warp - 2) / 4;        // K blocks ph, ph+4, ...
         const int r = q * 32 + lane;          // row within the tile
-        int64_t n;                            // weight row
+        int64_t n;                            // weight row (-1: none)
         if (gate_up) {
-            const int64_t i = r0 + r;
-            n = i < p.I ? (tile ? p.I + i : i) : -1;
+            const int64_t i = r0 + (r & 63);
+            n = i < p.I ? (r < 64 ? i : p.I + i) : -1;
         } else {
-            const int64_t i = r0 + tile * kQmmRows + r;
-            n = i < p.N ? i : -1;
+            n = r0 + r < p.N ? r0 + r : -1;
         }
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         unsigned flags = 0;
-        // A ring of raw code blocks, loaded kQmmPrefetch blocks ahead so
-        // the HBM latency of the codes overlaps the tensor-core work.
-        RawBlock<BITS> ring[kQmmPrefetch];
-#pragma unroll
-        for (int i = 0; i < kQmmPrefetch; ++i)
-            if (i < p.nkb) load_raw<BITS>(p, n, i, ring[i]);
-        bool ok = true;  // pipeline healthy
-        for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kQmmPrefetch) {
-#pragma unroll
-            for (int i = 0; i < kQmmPrefetch; ++i) {
-                const int kb = kb0 + i;
-                if (kb >= p.nkb) break;
-                const int sa = kb % SA;
-                // warp-uniform: tcgen05.st below is a warp-collective
-                if (kb >= SA &&
-                    !__all_sync(0xffffffffu, qmm_wait(&aempty[sa],
-                                                      ((kb / SA) & 1) ^ 1,
-                                                      p.status))) {
-                    ok = false;
+        for (int kb = ph; kb < p.nkb; kb += 4) {
+            const int sa = kb % SA;
+            uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
+            if (kb < G) {
+                const int ss = (kb / 8) % SS;
+                if ((kb & 7) == ph &&
+                    !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (kb / 8 / SS) & 1,
+                                                      p.status)))
                     break;
-                }
-                uint32_t a[64];
-                dequant_block<BITS>(p, n, kb, ring[i], a, flags);
-                if (kb + kQmmPrefetch < p.nkb)
-                    load_raw<BITS>(p, n, kb + kQmmPrefetch, ring[i]);
-                const uint32_t col = tmem_a + sa * (2 * AW) + tile * AW;
-                const uint32_t taddr = col + ((uint32_t)(q * 32) << 16);
-                uint32_t v0[32];
+                const int sw = kb % WS;
+                if (!__all_sync(0xffffffffu,
+                                qmm_wait(&wfull[sw], (kb / WS) & 1, p.status)))
+                    break;
+                const uint4 *ws = reinterpret_cast<const uint4 *>(
+                    smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
+                uint32_t w[BITS * 2];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v0[j] = a[j];
-                tc_st32(taddr, v0);
-                if constexpr (BITS == 8) {
-                    uint32_t v1[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v1[j] = a[32 + j];
-                    tc_st32(taddr + 32, v1);
+                for (int v = 0; v < BITS / 2; ++v) {
+                    const uint4 c = ws[v];
+                    w[4 * v] = c.x; w[4 * v + 1] = c.y;
+                    w[4 * v + 2] = c.z; w[4 * v + 3] = c.w;
                 }
-                tc_wait_st();
-                tc_fence_before();
+                const uint16_t *st = reinterpret_cast<const uint16_t *>(
+                    smem + L::SOFF + (size_t)ss * L::SBYTES);
+                const float s = bf16_bits_to_f32(st[r * 8 + (kb & 7)]);
+                // the codes and scale of this block are in registers
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[sa]);
+                if (lane == 0) {
+                    mbar_arrive(&wempty[sw]);
+                    if ((kb & 7) == 4 + ph || kb == G - 1) mbar_arrive(&sempty[ss]);
+                }
+                if (n >= 0 &&
+                    (!(fabsf(s) <= 511.f) || (s != 0.f && fabsf(s) < 6.103515625e-05f)))
+                    flags |= kStFp16Range;
+                dequant_row<BITS>(w, s, hi, lo);
+            } else {
+                bias_row<BITS>(p, n, kb, hi, flags);
+                if constexpr (BITS == 8)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) lo[i] = 0u;
             }
+            // warp-uniform: tcgen05.st below is a warp-collective
+            if (kb >= SA &&
+                !__all_sync(0xffffffffu, qmm_wait(&aempty[sa], ((kb / SA) & 1) ^ 1,
+                                                  p.status)))
+                break;
+            const uint32_t col = tmem_a + sa * AW + lane_off;
+            tc_st32(col, hi);
+            if constexpr (BITS == 8) tc_st32(col + 32, lo);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[sa]);
         }
         if (flags) atomicOr(p.status, flags);
 
         // -------------------------------------------- epilogue
-        if (__all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status))) {
-            tc_fence_after();
-            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-            if (gate_up) {
-                // tile-0 warps take tokens 0-63, tile-1 warps 64-127
-                const int64_t i = r0 + r;
-                for (int c0 = tile * 64; c0 < tile * 64 + 64; c0 += 32) {
-                    float g[32], u[32];
+        const bool done = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
+        if (done) tc_fence_after();
+        const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
+        if (gate_up) {
+            // gate warps (rows 0-63) hand their accumulators to the up
+            // warps through the (now idle) activation ring
+            float *gbuf = reinterpret_cast<float *>(smem + L::XOFF);
+            constexpr int GS = NT + 1;  // padded row stride: no bank conflicts
+            if (done && r < 64) {
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                    float g[32];
                     tc_ld32(tmem_d + lane_off + c0, g);
-                    tc_ld32(tmem_d + kQmmTok + lane_off + c0, u);
-                    if (i < p.I)
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t m = m0 + c0 + j;
-                            if (m < p.M)
-                                p.y[m * p.I + i] = f32_to_bf16_bits(
-                                    g[j] / (1.0f + __expf(-g[j])) * u[j]);
-                        }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) gbuf[r * GS + c0 + j] = g[j];
                 }
-            } else {
-                int sidx = 0;
-                if (p.mode == 1 && n >= 0)
-                    while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1])
-                        ++sidx;
-                for (int c0 = 0; c0 < kQmmTok; c0 += 32) {
-                    float d[32];
-                    tc_ld32(tmem_d + tile * kQmmTok + lane_off + c0, d);
-                    if (n < 0) continue;
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
+            if (done && r >= 64) {
+                const int pr = r - 64;
+                const int64_t i = r0 + pr;
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                    float u[32];
+                    tc_ld32(tmem_d + lane_off + c0, u);
+                    if (i >= p.I) continue;
                     for (int j = 0; j < 32; ++j) {
                         const int64_t m = m0 + c0 + j;
                         if (m >= p.M) break;
-                        if (p.mode == 0) {
-                            p.y[m * p.N + n] = f32_to_bf16_bits(d[j]);
-                        } else {
-                            const int64_t jj = n - p.sec_start[sidx];
-                            const int64_t size =
-                                p.sec_start[sidx + 1] - p.sec_start[sidx];
-                            float val = d[j];
-                            if (p.sec_bias[sidx])
-                                val += bf16_bits_to_f32(p.sec_bias[sidx][jj]);
-                            p.sec_out[sidx][m * size + jj] = f32_to_bf16_bits(val);
-                        }
+                        const float g = gbuf[pr * GS + c0 + j];
+                        p.y[m * p.I + i] =
+                            f32_to_bf16_bits(g / (1.0f + __expf(-g)) * u[j]);
+                    }
+                }
+            }
+        } else if (done) {
+            int sidx = 0;
+            if (p.mode == 1 && n >= 0)
+                while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1]) ++sidx;
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                float d[32];
+                tc_ld32(tmem_d + lane_off + c0, d);
+                if (n < 0) continue;
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t m = m0 + c0 + j;
+                    if (m >= p.M) break;
+                    if (p.mode == 0) {
+                        p.y[m * p.N + n] = f32_to_bf16_bits(d[j]);
+                    } else {
+                        const int64_t jj = n - p.sec_start[sidx];
+                        const int64_t size =
+                            p.sec_start[sidx + 1] - p.sec_start[sidx];
+                        float val = d[j];
+                        if (p.sec_bias[sidx])
+                            val += bf16_bits_to_f32(p.sec_bias[sidx][jj]);
+                        p.sec_out[sidx][m * size + jj] = f32_to_bf16_bits(val);
                     }
                 }
             }
@@ -580,10 +621,14 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
-        // nothing may still be landing in shared memory or tensor memory
-        for (int kb = s_xconsumed; kb < s_xissued; ++kb)
-            if (!mbar_wait(&xfull[kb % kQmmXStages], (kb / kQmmXStages) & 1))
-                break;
+        // nothing may still be landing in shared memory or tensor memory:
+        // the last loads of each ring (all complete unless a wait ran out)
+        for (int k = max(0, s_xn - XS); k < s_xn; ++k)
+            if (!mbar_wait(&xfull[k % XS], (k / XS) & 1)) break;
+        for (int k = max(0, s_wn - WS); k < s_wn; ++k)
+            if (!mbar_wait(&wfull[k % WS], (k / WS) & 1)) break;
+        for (int k = max(0, s_sn - SS); k < s_sn; ++k)
+            if (!mbar_wait(&sfull[k % SS], (k / SS) & 1)) break;
         mbar_wait(&dfull, 0);
     }
     __syncthreads();
@@ -607,9 +652,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-template <int BITS>
+// 2-D tensor map over a row-major [rows, cols] array.
+static int encode_2d(CUtensorMap *map, CUtensorMapDataType type, int esize,
+                     const void *base, int64_t cols, int64_t rows,
+                     uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapSwizzle swz, const char *what) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+    if (!encode)
+        return set_error(GWA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)cols * esize};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult cr = encode(map, type, 2, const_cast<void *>(base), gdim, gstride,
+                         box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+        return set_error(GWA_ERR_CUDA, "tensor map (%s) encode failed (%d)",
+                         what, (int)cr);
+    return GWA_OK;
+}
+
+template <int BITS, int NT>
 static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
-    const int64_t M = a.M, K = a.w.K;
+    using L = QmmLayout<BITS, NT>;
+    const int64_t M = a.M, K = a.w.K, G = K / 64;
     const int64_t kext = qmm_kext(K);
     unsigned int *status = reinterpret_cast<unsigned int *>(ws);
     __half *xe = reinterpret_cast<__half *>(ws + kStatusBytes);
@@ -618,7 +686,7 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm status reset: %s",
                          cudaGetErrorString(e));
-    const int64_t items = M * (K / 64);
+    const int64_t items = M * G;
     const int pthreads = 128;
     int64_t pblocks = (items + pthreads - 1) / pthreads;
     if (pblocks > (int64_t)num_sms() * 16) pblocks = (int64_t)num_sms() * 16;
@@ -628,29 +696,26 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm pre-pass: %s", cudaGetErrorString(e));
 
-    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-    if (!encode)
-        return set_error(GWA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    CUtensorMap map;
-    const cuuint64_t gdim[2] = {(cuuint64_t)kext, (cuuint64_t)M};
-    const cuuint64_t gstride[1] = {(cuuint64_t)kext * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kQmmTok};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xe, gdim,
-                         gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS)
-        return set_error(GWA_ERR_CUDA, "tensor map encode failed (%d)", (int)cr);
+    const bool gate_up = a.mode == 2;
+    const uint32_t box_rows = gate_up ? kQmmRows / 2 : kQmmRows;
+    CUtensorMap xmap, wmap, smap;
+    int rc = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xe, kext, M,
+                       64, NT, CU_TENSOR_MAP_SWIZZLE_128B, "activations");
+    if (!rc)
+        rc = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a.w.wq,
+                       K * BITS / 32, a.w.N, BITS * 2, box_rows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "codes");
+    if (!rc)
+        rc = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, a.w.scales, G,
+                       a.w.N, 8, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       "scales");
+    if (rc) return rc;
 
     QmmParams p{};
     p.M = M;
     p.K = (int)K;
-    p.kext = kext;
     p.nkb = (int)(kext / 64);
-    p.G = (int)(K / 64);
-    p.wq = a.w.wq;
+    p.G = (int)G;
     p.sc = a.w.scales;
     p.bi = a.w.biases;
     p.N = a.w.N;
@@ -665,21 +730,31 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     }
     p.status = status;
 
-    auto kern = qmm_tc_kernel<BITS>;
+    auto kern = qmm_tc_kernel<BITS, NT>;
     int dummy = 0;
     e = occupancy_grid(reinterpret_cast<const void *>(kern), kQmmThreads,
-                       kQmmSmem, &dummy);
+                       L::SMEM, &dummy);
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm setup: %s", cudaGetErrorString(e));
-    const int64_t rows = a.mode == 2 ? p.I : p.N;
-    const int64_t per_cta = a.mode == 2 ? kQmmRows : 2 * kQmmRows;
-    dim3 grid((unsigned)((rows + per_cta - 1) / per_cta),
-              (unsigned)((M + kQmmTok - 1) / kQmmTok));
-    kern<<<grid, kQmmThreads, kQmmSmem, st>>>(map, p);
+    const int64_t rows = gate_up ? p.I : p.N;
+    dim3 grid((unsigned)((rows + box_rows - 1) / box_rows),
+              (unsigned)((M + NT - 1) / NT));
+    kern<<<grid, kQmmThreads, L::SMEM, st>>>(xmap, wmap, smap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm launch: %s", cudaGetErrorString(e));
     return GWA_OK;
+}
+
+bool qmm_eligible(const QmmArgs &a) {
+    auto a16 = [](const void *q) {
+        return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
+    };
+    // the scale tiles need rows of whole 16-byte units (K/64 a multiple of
+    // 8); TMA wants 16-byte aligned bases
+    return (a.w.K / 64) % 8 == 0 && a16(a.w.wq) && a16(a.w.scales) &&
+           a16(a.w.biases) && a.M <= 0x7fffffffLL && a.w.N <= 0x7fffffffLL &&
+           (a.w.bits == 4 || a.w.bits == 8);
 }
 
 int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
@@ -695,7 +770,10 @@ int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
     if (a.M > 0x7fffffffLL)
         return set_error(GWA_ERR_INVALID_ARG, "M too large");
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    return a.w.bits == 4 ? qmm_launch<4>(a, ws, st) : qmm_launch<8>(a, ws, st);
+    const bool wide = a.M > 128;  // 256-token tiles once there are enough
+    if (a.w.bits == 4)
+        return wide ? qmm_launch<4, 256>(a, ws, st) : qmm_launch<4, 128>(a, ws, st);
+    return wide ? qmm_launch<8, 256>(a, ws, st) : qmm_launch<8, 128>(a, ws, st);
 }
 
 unsigned int qmm_timeouts(bool reset) {

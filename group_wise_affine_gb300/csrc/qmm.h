@@ -23,6 +23,10 @@ struct QmmArgs {
 };
 
 size_t qmm_workspace_bytes(int64_t M, int64_t K);
+// Whether the tensor-core kernel takes this shape (K a multiple of 512,
+// 16-byte aligned weights); otherwise M > 8 runs on the decode kernels in
+// passes of up to eight tokens.
+bool qmm_eligible(const QmmArgs &a);
 int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
             cudaStream_t st);
 

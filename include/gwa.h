@@ -25,10 +25,13 @@
  *     outputs 2-byte aligned.  K must be a multiple of 64.
  *   - bits is 4 or 8; group must be 64.
  *   - M <= 8 runs the decode (GEMV) kernels on the CUDA cores and needs no
- *     workspace (pass NULL, 0).  M > 8 runs the tensor-core (tcgen05) kernels
- *     and needs `gwa_workspace_bytes(M, K)` bytes of device workspace, which
- *     the call overwrites; calls sharing one workspace must not overlap on
- *     the GPU.
+ *     workspace (pass NULL, 0).  M > 8 needs `gwa_workspace_bytes(M, K)`
+ *     bytes of device workspace, which the call overwrites; calls sharing one
+ *     workspace must not overlap on the GPU.  It runs the tensor-core
+ *     (tcgen05) kernels when K is a multiple of 512 and Wq, scales and
+ *     biases are 16-byte aligned (the workspace's first word then holds the
+ *     call's status: 1 = a pipeline wait ran out, 2 = a value outside fp16's
+ *     range), and otherwise the decode kernels in passes of up to 8 tokens.
  *   - Return value: GWA_OK or an error code; nothing aborts, traps or exits.
  *     On error nothing was enqueued and gwa_last_error() (thread-local) holds
  *     one line of text.  Errors raised by the GPU while the work runs surface

@@ -119,10 +119,11 @@ def test_missing_workspace_is_an_error_not_a_fault():
 
 def test_fp16_range_is_flagged():
     # an activation beyond fp16's range sets the status bit; nothing faults
-    w = dev_qweight(synth.qweight(1910, 128, 128, 4))
-    xh = synth.activations(1911, 32, 128)
+    # (K = 512: the tensor-core kernel, which writes the status word)
+    w = dev_qweight(synth.qweight(1910, 128, 512, 4))
+    xh = synth.activations(1911, 32, 512)
     xh[3, 5] = synth.bf16_bits(np.array([1.0e6], np.float32))[0]
-    ws = gwa.make_workspace(32, 128)
+    ws = gwa.make_workspace(32, 512)
     gwa.qmv_affine(dev_bf16(xh), w, workspace=ws)
     torch.cuda.synchronize()
     assert status_of(ws) & 2
