@@ -219,6 +219,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
+// The same wait with a suspend-time hint: a thread whose phase is not yet
+// complete sleeps (up to `hint_ns`, woken early when the phase completes)
+// instead of polling, which leaves the issue slots to the working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar,
+                                                    uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
+                                                uint32_t parity) {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 1000000u))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
 // Contiguous global -> shared copy completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,

@@ -45,7 +45,6 @@ namespace gwa {
 constexpr int kQmmDeqWarps = 16;     // four per tensor-memory lane quarter
 constexpr int kQmmThreads = (2 + kQmmDeqWarps) * 32;
 constexpr int kQmmRows = 128;        // weight rows per CTA (MMA M)
-constexpr int kQmmWStages = 8;       // code-tile ring
 constexpr int kQmmSStages = 2;       // scale/bias-tile ring (8 K blocks each)
 constexpr int kStatusBytes = 256;
 
@@ -177,7 +176,7 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) {
 
 __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
                                          unsigned int *status) {
-    if (mbar_wait(bar, parity)) return true;
+    if (mbar_wait_sleep(bar, parity)) return true;
     atomicAdd(&g_qmm_timeouts, 1u);
     atomicOr(status, kStTimeout);
     return false;
@@ -279,12 +278,13 @@ struct QmmLayout {
     static constexpr int AW = BITS == 4 ? 32 : 64;  // A columns per K block
     static constexpr int SA = (512 - NT) / AW > 8 ? 8 : (512 - NT) / AW;
     static constexpr int XS = NT == 256 ? 4 : 6;      // activation tiles
+    static constexpr int WS = 8;      // code tiles
     static constexpr int XBYTES = NT * 128;           // 64 fp16 per token
     static constexpr int WBYTES = kQmmRows * BITS * 8;  // 64 codes per row
     static constexpr int SBYTES = kQmmRows * 16;      // 8 bf16 per row
     static constexpr size_t XOFF = 0;
     static constexpr size_t WOFF = XOFF + (size_t)XS * XBYTES;
-    static constexpr size_t SOFF = WOFF + (size_t)kQmmWStages * WBYTES;
+    static constexpr size_t SOFF = WOFF + (size_t)WS * WBYTES;
     static constexpr size_t BYTES = SOFF + (size_t)kQmmSStages * SBYTES;
     static constexpr size_t SMEM = BYTES + 1024;      // alignment slack
 };
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                   const __grid_constant__ CUtensorMap smap, QmmParams p) {
     using L = QmmLayout<BITS, NT>;
     constexpr int AW = L::AW, SA = L::SA, XS = L::XS;
-    constexpr int WS = kQmmWStages, SS = kQmmSStages;
+    constexpr int WS = L::WS, SS = kQmmSStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -417,11 +417,24 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const uint32_t tmem_a = tmem + NT;  // A stages
 
     if (warp == 0) {
-        // -------------------------------------------- TMA loader
+        // -------------------------------------------- TMA loaders
+        // lane 0: activation tiles (paced by the MMA); lane 1: code and
+        // scale tiles, which run ahead as far as their own rings allow
         if (lane == 0) {
-            const int rows = gate_up ? kQmmRows / 2 : kQmmRows;
             for (int kb = 0; kb < p.nkb; ++kb) {
-                if (kb < G && kb % 8 == 0) {
+                const int sx = kb % XS;
+                if (kb >= XS &&
+                    !qmm_wait(&xempty[sx], ((kb / XS) & 1) ^ 1, p.status))
+                    break;
+                mbar_expect_tx(&xfull[sx], L::XBYTES);
+                tma_load_2d(smem + L::XOFF + (size_t)sx * L::XBYTES, &xmap,
+                            kb * 64, (int)m0, &xfull[sx]);
+                s_xn = kb + 1;
+            }
+        } else if (lane == 1) {
+            const int rows = gate_up ? kQmmRows / 2 : kQmmRows;
+            for (int kb = 0; kb < G; ++kb) {
+                if (kb % 8 == 0) {
                     // scale tiles of K blocks kb .. kb+7 (the code blocks'
                     // biases enter through the bias columns)
                     const int sb = kb / 8, s = sb % SS;
@@ -436,29 +449,19 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                                     &sfull[s]);
                     s_sn = sb + 1;
                 }
-                if (kb < G) {
-                    // packed codes of the tile's rows
-                    const int s = kb % WS;
-                    if (kb >= WS &&
-                        !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status))
-                        break;
-                    unsigned char *dw = smem + L::WOFF + (size_t)s * L::WBYTES;
-                    const int wx = kb * BITS * 2;  // 32-bit words
-                    mbar_expect_tx(&wfull[s], L::WBYTES);
-                    tma_load_2d(dw, &wmap, wx, (int)r0, &wfull[s]);
-                    if (gate_up)
-                        tma_load_2d(dw + rows * BITS * 8, &wmap, wx,
-                                    (int)(p.I + r0), &wfull[s]);
-                    s_wn = kb + 1;
-                }
-                const int sx = kb % XS;
-                if (kb >= XS &&
-                    !qmm_wait(&xempty[sx], ((kb / XS) & 1) ^ 1, p.status))
+                // packed codes of the tile's rows
+                const int s = kb % WS;
+                if (kb >= WS &&
+                    !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status))
                     break;
-                mbar_expect_tx(&xfull[sx], L::XBYTES);
-                tma_load_2d(smem + L::XOFF + (size_t)sx * L::XBYTES, &xmap,
-                            kb * 64, (int)m0, &xfull[sx]);
-                s_xn = kb + 1;
+                unsigned char *dw = smem + L::WOFF + (size_t)s * L::WBYTES;
+                const int wx = kb * BITS * 2;  // 32-bit words
+                mbar_expect_tx(&wfull[s], L::WBYTES);
+                tma_load_2d(dw, &wmap, wx, (int)r0, &wfull[s]);
+                if (gate_up)
+                    tma_load_2d(dw + rows * BITS * 8, &wmap, wx, (int)(p.I + r0),
+                                &wfull[s]);
+                s_wn = kb + 1;
             }
         }
     } else if (warp == 1) {
@@ -516,11 +519,21 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 const uint4 *ws = reinterpret_cast<const uint4 *>(
                     smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
                 uint32_t w[BITS * 2];
+                if constexpr (BITS == 4) {
+                    // rows 128 bytes apart read their two 16-byte chunks in
+                    // opposite order (different banks in one instruction)
+                    const bool rot = (r >> 2) & 1;
+                    const uint4 c0 = ws[rot ? 1 : 0], c1 = ws[rot ? 0 : 1];
+                    const uint4 lo4 = rot ? c1 : c0, hi4 = rot ? c0 : c1;
+                    w[0] = lo4.x; w[1] = lo4.y; w[2] = lo4.z; w[3] = lo4.w;
+                    w[4] = hi4.x; w[5] = hi4.y; w[6] = hi4.z; w[7] = hi4.w;
+                } else {
 #pragma unroll
-                for (int v = 0; v < BITS / 2; ++v) {
-                    const uint4 c = ws[v];
-                    w[4 * v] = c.x; w[4 * v + 1] = c.y;
-                    w[4 * v + 2] = c.z; w[4 * v + 3] = c.w;
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 c = ws[v];
+                        w[4 * v] = c.x; w[4 * v + 1] = c.y;
+                        w[4 * v + 2] = c.z; w[4 * v + 3] = c.w;
+                    }
                 }
                 const uint16_t *st = reinterpret_cast<const uint16_t *>(
                     smem + L::SOFF + (size_t)ss * L::SBYTES);
