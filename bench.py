@@ -215,15 +215,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(dev)
     M, bits, L = args.tokens, args.bits, args.layers
 
-    # weights: one seeded draw per layer and projection, on the device
-    W = []
-    for l in range(L):
-        layer = {}
-        for p, (name, rows, K) in enumerate(layer_shapes()):
-            wq, s, b = synth.device_qweight(synth.stack_seed(l, p, bits), rows,
-                                            K, bits, device=dev)
-            layer[name] = gwa.QWeight(wq, s, b, rows, K, bits, 64)
-        W.append(layer)
+    W = stack_weights(bits, L, dev)
     g = torch.Generator(device=dev)
     g.manual_seed(12345 + rank)
     x = torch.randn((M, HIDDEN), generator=g, device=dev).to(torch.bfloat16)
@@ -343,6 +335,13 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
         extras["stack_M4"] = run_stack_extra(W, 4, dev, 50, 3)
         extras["prefill_stack_M512"] = run_stack_extra(W, 512, dev, 5, 2)
+        # the same stack with u8 codes (its own 14 GB of weights)
+        W8 = stack_weights(8, L, dev)
+        extras["stack_u8_M1"] = run_stack_extra(W8, 1, dev, 50, 3)
+        extras["stack_u8_M4"] = run_stack_extra(W8, 4, dev, 30, 3)
+        extras["prefill_stack_u8_M512"] = run_stack_extra(W8, 512, dev, 5, 2)
+        del W8
+        torch.cuda.empty_cache()
         extras["moe"] = run_moe_extra(dev, 50, 3)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
@@ -380,6 +379,22 @@ def capture(fn):
     with torch.cuda.graph(g, stream=side):
         fn()
     return g
+
+
+def stack_weights(bits: int, L: int, dev):
+    """The stack's weights: one seeded draw per layer and projection, made
+    on the device."""
+    import group_wise_affine_gb300 as gwa
+    import gwa_synth as synth
+    W = []
+    for l in range(L):
+        layer = {}
+        for p, (name, rows, K) in enumerate(layer_shapes()):
+            wq, s, b = synth.device_qweight(synth.stack_seed(l, p, bits), rows,
+                                            K, bits, device=dev)
+            layer[name] = gwa.QWeight(wq, s, b, rows, K, bits, 64)
+        W.append(layer)
+    return W
 
 
 def run_stack_extra(W, M, dev, steps, warmup):
@@ -431,6 +446,9 @@ def run_stack_extra(W, M, dev, steps, warmup):
                                 "GB/s": round(b / us / 1e3, 1)}
     out["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
     out["GB/s"] = round(bytes_ / (ms * 1e-3) / 1e9, 1)
+    out["bits"] = W[0]["qkv"].bits
+    out["frac_of_measured_hbm"] = round(out["GB/s"] / measured_peak()[0], 4)
+    out["timing"] = "per projection type: one graph of its 48 launches"
     return out
 
 
@@ -644,12 +662,13 @@ def main():
     }
     if r["extras"]:
         ex = dict(r["extras"])
-        pf = ex.get("prefill_stack_M512")
-        if pf:
-            bf = _measured_tflops()
-            pf["peak_TFLOP/s"] = bf[0]
-            pf["frac_of_peak"] = round(pf["TFLOP/s"] / bf[0], 4)
-            pf["peak_source"] = bf[1]
+        for key in ("prefill_stack_M512", "prefill_stack_u8_M512"):
+            pf = ex.get(key)
+            if pf:
+                bf = _measured_tflops()
+                pf["peak_TFLOP/s"] = bf[0]
+                pf["frac_of_peak"] = round(pf["TFLOP/s"] / bf[0], 4)
+                pf["peak_source"] = bf[1]
         line["extras"] = ex
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
