@@ -218,3 +218,36 @@ def test_bad_arguments_raise_status_not_fault():
     assert e.value.code == gwa.GWA_ERR_MISALIGNED
     torch.cuda.synchronize()          # the context is still healthy
     assert gwa.qmv_affine(x, w).shape == (1, 16)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [1, 3])
+def test_sections_bias_streaming_kernels(bits, M):
+    # K = 1024: the one-token lane-per-group kernel (M = 1) and the chunk
+    # streaming kernel (M = 3), ragged section sizes, optional biases
+    K, secs = 1024, (200, 56, 56, 9)
+    parts = [synth.qweight(440 + i + bits, n, K, bits)
+             for i, n in enumerate(secs)]
+    fused = synth.stack_rows(parts)
+    x = synth.activations(450 + M, M, K)
+    bias = [synth.activations(451 + i, 1, n)[0] for i, n in enumerate(secs)]
+    bias[2] = None
+    outs = gwa.qmv_fused_sections(
+        dev_bf16(x), dev_qweight(fused), secs,
+        out_bias=[dev_bf16(b) if b is not None else None for b in bias])
+    refs = oracle.fused_sections(x, fused.wq, fused.scales, fused.biases, secs,
+                                 K, bits, out_bias=bias)
+    for o, r in zip(outs, refs):
+        assert_close(bf16_to_f64(o), r, f"sections+bias M={M} u{bits}")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_gate_up_lane_per_group_kernel(bits):
+    # K = 1536 (24 groups: two 16-lane slices per row, one partly idle),
+    # I off every stage size
+    K, I = 1536, 777
+    w = synth.qweight(520 + bits, 2 * I, K, bits)
+    x = synth.activations(530, 1, K)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
+    ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits)
+    assert_close(bf16_to_f64(h), ref, f"gate_up lane-per-group u{bits}")

@@ -64,8 +64,10 @@ def test_qmm_sections_and_bias(bits, M):
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("M", [16, 129])
-def test_qmm_gate_up_silu(bits, M):
-    K, I = 576, 200
+@pytest.mark.parametrize("K,I", [(576, 200), (1024, 200), (2048, 65)])
+def test_qmm_gate_up_silu(bits, M, K, I):
+    # K = 576: decode kernels in token passes; K = 1024 / 2048: tensor cores
+    # (64-pair tiles, the last one partial)
     w = synth.qweight(1600 + bits, 2 * I, K, bits)
     x = synth.activations(1610 + M, M, K)
     h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
