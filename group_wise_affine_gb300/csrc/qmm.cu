@@ -278,7 +278,10 @@ struct QmmLayout {
     static constexpr int AW = BITS == 4 ? 32 : 64;  // A columns per K block
     static constexpr int SA = (512 - NT) / AW > 8 ? 8 : (512 - NT) / AW;
     static constexpr int XS = NT == 256 ? 4 : 6;      // activation tiles
-    static constexpr int WS = 8;      // code tiles
+    // code tiles; a smaller footprint leaves more of the SM's 256 KB to L1
+    // (the bias blocks read scales and biases through it), and above
+    // ~180 KB per CTA the kernel ran twice as slow
+    static constexpr int WS = 4;
     static constexpr int XBYTES = NT * 128;           // 64 fp16 per token
     static constexpr int WBYTES = kQmmRows * BITS * 8;  // 64 codes per row
     static constexpr int SBYTES = kQmmRows * 16;      // 8 bf16 per row
