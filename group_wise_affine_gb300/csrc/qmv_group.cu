@@ -95,15 +95,15 @@ __global__ void __maxnreg__(88)
                 reinterpret_cast<const unsigned char *>(p.sc);
             const unsigned char *bi =
                 reinterpret_cast<const unsigned char *>(p.bi);
+            int s = 0;        // ring slot of stage st
+            uint32_t ph = 0;  // its use count parity
             for (int st = 0; st < nst; ++st) {
-                const int s = st % stages;
                 // Weights are never written by this library's kernels, and a
                 // kernel of any other kind completes before one of ours starts
                 // (it never triggers an early launch), so the first `stages`
                 // stages can be fetched before the previous grid finishes.
                 if (st == stages) pdl_wait_primary();
-                if (st >= stages &&
-                    !mbar_wait(&empty[s], ((st / stages) & 1) ^ 1)) {
+                if (st >= stages && !mbar_wait(&empty[s], ph ^ 1)) {
                     atomicAdd(&g_group_timeouts, 1u);
                     break;
                 }
@@ -125,6 +125,10 @@ __global__ void __maxnreg__(88)
                              &full[s]);
                 }
                 s_issued = st + 1;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
         }
     } else {
@@ -156,15 +160,27 @@ __global__ void __maxnreg__(88)
             offw[j] = srow * rowbytes + (uint32_t)gg * GB;
             offs[j] = rows_stage * rowbytes + (srow * (uint32_t)p.G + gg) * 2u;
         }
+        // this lane's slot of the partial sums: value index idx = j*MT + m
+        // of unit u (stage-relative), half h
+        constexpr int SPREAD = kSlice / V;
+        const bool stores = in_group && (lane & (SPREAD - 1)) == 0;
+        int lu, roff;
+        {
+            const int idx = (lane & (kSlice - 1)) / SPREAD;
+            const int j = idx / MT, m = idx % MT;
+            const int u = hg * UPT + (j % UPT), h = j / UPT;
+            lu = u;
+            roff = ((u * HALVES + h) * MT + m) * slices + sl;
+        }
+        const int rstep = ups * HALVES * MT * slices;
+        int s = 0;
+        uint32_t ph = 0;
         for (int st = 0; st < nst; ++st) {
-            const int s = st % stages;
-            if (!mbar_wait(&full[s], (st / stages) & 1)) {
+            if (!mbar_wait(&full[s], ph)) {
                 atomicAdd(&g_group_timeouts, 1u);
                 atomicMin(&s_consumed, st);
                 break;
             }
-            const int64_t ua = u0 + (int64_t)st * ups;
-            const int n = (int)min((int64_t)ups, u1 - ua);
             const unsigned char *base = smem + (uint32_t)s * stage_bytes;
             float v[V];
 #pragma unroll
@@ -187,14 +203,12 @@ __global__ void __maxnreg__(88)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             const float tot = sub_reduce<kSlice, V>(v, lane);
-            constexpr int SPREAD = kSlice / V;
-            if (in_group && (lane & (SPREAD - 1)) == 0) {
-                const int idx = (lane & (kSlice - 1)) / SPREAD;  // j*MT + m
-                const int j = idx / MT, m = idx % MT;
-                const int u = hg * UPT + (j % UPT), h = j / UPT;
-                if (u < n)
-                    red[((((st * ups + u) * HALVES + h) * MT + m) * slices) +
-                        sl] = tot;
+            if (stores && lu < nu) red[roff] = tot;
+            lu += ups;
+            roff += rstep;
+            if (++s == stages) {
+                s = 0;
+                ph ^= 1;
             }
         }
     }
