@@ -244,15 +244,6 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
     return true;
 }
 
-// Bulk prefetch of [src, src + bytes) into L2: no shared memory and no
-// completion signal (16-byte aligned address, size a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src,
-                                                 uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
-                 "r"(bytes)
-                 : "memory");
-}
-
 // Contiguous global -> shared copy completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
