@@ -5,14 +5,14 @@
 // call is read once, in place, from the caller's stacked tensor.
 //
 // Same pipeline as the one-token decode kernel (qmv_group.cu): a producer
-// thread fills a shared-memory ring with packed expert rows by bulk copy,
-// and consumer lanes each own one group of 64 inputs and form exact integer
-// dots (group_dot.cuh).  A row's groups fit in one slice of W lanes (W = 8,
-// 16 or 32 >= K/64), so a slice reduction yields the full row dot.  A bulk
-// copy costs the copy engine about 0.2 us whatever its size up to ~8 KB, so
-// only the codes travel by bulk copy, in copies of 10-30 KB; each lane reads
-// its rows' scale and bias with plain read-only loads issued two passes
-// ahead.
+// thread fills a shared-memory ring
+// with packed expert rows and their scales and biases by bulk copy, and
+// consumer lanes each own one group of 64 inputs and form exact integer dots
+// (group_dot.cuh).  A row's groups fit in one slice of W lanes (W = 8, 16 or
+// 32 >= K/64), so a slice reduction yields the full row dot.  Scales and
+// biases travel in the same stage as the codes: a pass then waits on shared
+// memory only, where reading them from global memory a pass or two ahead
+// left each short pass waiting a DRAM round trip.
 //
 // Routing.  Each CTA first groups the slots (token, k) by expert, in
 // first-occurrence order, slots in slot order within a group.  Expert ids,
@@ -142,11 +142,6 @@ struct MsTasks {
     }
 };
 
-template <int RPH>
-struct MsScales {
-    uint16_t s[RPH], b[RPH];
-};
-
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -175,8 +170,10 @@ __global__ void __maxnreg__(128)
     moe_stream_kernel(MoeParams p, int stages, int rs, int ups, int cl,
                       uint32_t img_off, uint32_t acc_off) {
     constexpr int HALVES = MODE == 0 ? 2 : 1;
-    constexpr int UPT = MODE == 0 ? 1 : 2;  // units per row group and pass
-    constexpr int RPH = HALVES * UPT;       // rows per lane and pass (2)
+    // units per row group and pass (gate+up: row pairs, down: rows): two,
+    // half the passes of one; more do not fit in the registers
+    constexpr int UPT = 2;
+    constexpr int RPH = HALVES * UPT;       // rows per lane and pass
     constexpr int GB = BITS * 8;            // code bytes per row and group
     const int CL = MODE == 0 ? 1 : cl;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -192,7 +189,11 @@ __global__ void __maxnreg__(128)
     const int64_t I = p.N / 2;
     const int sbu = rs * UPT;
     const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
-    const uint32_t stage_bytes = (uint32_t)(HALVES * ups) * rowbytes;
+    const uint32_t sbrow = (uint32_t)p.G * 2;  // scale (bias) bytes per row
+    // a stage: codes [half][ups rows], then scales, then biases, same order
+    const uint32_t sc_off = (uint32_t)(HALVES * ups) * rowbytes;
+    const uint32_t bi_off = sc_off + (uint32_t)(HALVES * ups) * sbrow;
+    const uint32_t stage_bytes = bi_off + (uint32_t)(HALVES * ups) * sbrow;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
     uint64_t *empty = full + stages;
     const int rank = CL > 1 ? (int)cluster_rank() : 0;
@@ -307,26 +308,38 @@ __global__ void __maxnreg__(128)
         if (tid == ncons) {
             const unsigned char *wq =
                 reinterpret_cast<const unsigned char *>(p.wq);
+            const unsigned char *sc =
+                reinterpret_cast<const unsigned char *>(p.sc);
+            const unsigned char *bi =
+                reinterpret_cast<const unsigned char *>(p.bi);
             MsWalk w = walk;
             MsStage sg;
-            int k = 0;
+            int k = 0, s = 0;
+            uint32_t ph = 0;  // use count parity of slot s
             while (w.next(sg)) {
-                const int s = k % stages;
-                if (k >= stages &&
-                    !mbar_wait(&empty[s], ((k / stages) & 1) ^ 1)) {
+                if (k >= stages && !mbar_wait(&empty[s], ph ^ 1)) {
                     atomicAdd(&g_moe_timeouts, 1u);
                     break;
                 }
                 const int64_t e = tb.gexp[sg.gi];
                 unsigned char *base = smem + (size_t)s * stage_bytes;
-                mbar_expect_tx(&full[s], (uint32_t)(HALVES * sg.n) * rowbytes);
+                mbar_expect_tx(&full[s], (uint32_t)(HALVES * sg.n) *
+                                             (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
                     const int64_t r = e * p.N + sg.u + (h ? I : 0);
                     bulk_g2s(base + (size_t)h * ups * rowbytes,
                              wq + r * rowbytes, sg.n * rowbytes, &full[s]);
+                    bulk_g2s(base + sc_off + (size_t)h * ups * sbrow,
+                             sc + r * sbrow, sg.n * sbrow, &full[s]);
+                    bulk_g2s(base + bi_off + (size_t)h * ups * sbrow,
+                             bi + r * sbrow, sg.n * sbrow, &full[s]);
                 }
                 s_issued = ++k;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
         }
     } else {
@@ -340,26 +353,8 @@ __global__ void __maxnreg__(128)
         const int rot = chunk_rot<BITS>(gg);
         unsigned char *img = smem + img_off;
 
-        // the lane's scale and bias of a pass (rows clamped into the stage)
-        auto fetch = [&](const MsTask &t, MsScales<RPH> &q) {
-            const int64_t e = tb.gexp[t.sg.gi];
-#pragma unroll
-            for (int j = 0; j < RPH; ++j) {
-                const int pos =
-                    min(t.sb + hgc * UPT + (j % UPT), t.sg.n - 1);
-                const int64_t row = e * p.N + t.sg.u + pos + (j / UPT ? I : 0);
-                q.s[j] = ld_u16(p.sc + row * p.G + gg);
-                q.b[j] = ld_u16(p.bi + row * p.G + gg);
-            }
-        };
-        MsTasks ahead;
-        ahead.init(walk, sbu);
-        MsTask ta, tb2;
-        MsScales<RPH> qa, qb;
-        bool ha = ahead.next(ta);
-        if (ha) fetch(ta, qa);
-        bool hb = ahead.next(tb2);
-        if (hb) fetch(tb2, qb);
+        MsTasks tasks;
+        tasks.init(walk, sbu);
 
         pdl_wait_primary();  // x / h may be the previous kernel's output
         encode_rows_shared<BITS>(p.x, tb.nimg, tb.nimg, p.K, p.G, tid, ncons,
@@ -368,32 +363,21 @@ __global__ void __maxnreg__(128)
 
         GroupX<1> gx;
         int cached = -1;
-        // one pass; false when a wait ran out
-        auto process = [&](const MsTask &t, const MsScales<RPH> &q) -> bool {
-            const int s = t.k % stages;
-            if (t.sb == 0 && !mbar_wait(&full[s], (t.k / stages) & 1)) {
-                atomicAdd(&g_moe_timeouts, 1u);
-                atomicMin(&s_consumed, t.k);
-                return false;
+        int s = -1;       // ring slot of the current stage
+        uint32_t ph = 1;  // its use count parity
+        MsTask t;
+        while (tasks.next(t)) {
+            if (t.sb == 0) {
+                if (++s == stages) s = 0;
+                if (s == 0) ph ^= 1;
+                if (!mbar_wait(&full[s], ph)) {
+                    atomicAdd(&g_moe_timeouts, 1u);
+                    atomicMin(&s_consumed, t.k);
+                    break;
+                }
             }
             const unsigned char *base = smem + (size_t)s * stage_bytes;
             const int pos = t.sb + hgc * UPT;
-            uint4 wv[RPH][BITS / 2];
-            float sv[RPH], bv[RPH];
-#pragma unroll
-            for (int j = 0; j < RPH; ++j) {
-                const int r = (j / UPT) * ups +
-                              min(pos + (j % UPT), t.sg.n - 1);
-                lds_group<BITS>(base + (size_t)r * rowbytes + (size_t)gg * GB,
-                                rot, wv[j]);
-                sv[j] = bf16_bits_to_f32(q.s[j]);
-                bv[j] = bf16_bits_to_f32(q.b[j]);
-            }
-            if (t.last) {
-                // every lane's reads of this stage are done: release it
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
             for (int qi = tb.gstart[t.sg.gi]; qi < tb.gstart[t.sg.gi + 1]; ++qi) {
                 const int slot = tb.order[qi];
                 const int row = tb.imgrow[slot];
@@ -405,19 +389,39 @@ __global__ void __maxnreg__(128)
                 float v[RPH];
 #pragma unroll
                 for (int j = 0; j < RPH; ++j) {
+                    // stage row of value j (rows past the stage's end read
+                    // its last row, finite, and are not stored)
+                    const uint32_t roj = (uint32_t)((j / UPT) * ups +
+                                                    min(pos + (j % UPT), t.sg.n - 1));
+                    uint4 wv[BITS / 2];
+                    lds_group<BITS>(base + roj * rowbytes + (uint32_t)gg * GB,
+                                    rot, wv);
+                    const uint32_t so = (roj * (uint32_t)p.G + gg) * 2u;
+                    const float sv = bf16_bits_to_f32(
+                        *reinterpret_cast<const uint16_t *>(base + sc_off + so));
+                    const float bv = bf16_bits_to_f32(
+                        *reinterpret_cast<const uint16_t *>(base + bi_off + so));
                     int d[1];
-                    group_dot<BITS, 1>(wv[j], gx, d);
-                    v[j] = fmaf(sv[j] * gx.f[0], (float)d[0], bv[j] * gx.xs[0]);
+                    group_dot<BITS, 1>(wv, gx, d);
+                    v[j] = fmaf(sv * gx.f[0], (float)d[0], bv * gx.xs[0]);
+                    // keep the next row's loads after this dot (registers)
+                    asm volatile("" ::: "memory");
                 }
-                // slice lane 0 gets the total of row value 0; value 1 sits
-                // W/2 lanes up
+                // value j ends in slice lane j * (W / RPH); the second half's
+                // values (up rows, or down's odd rows) sit W/2 lanes up
                 const float tot = sub_reduce<W, RPH>(v, lane);
                 const float tot1 = __shfl_down_sync(0xffffffffu, tot, W / 2);
-                if (in_group && g == 0 && pos < t.sg.n) {
+                constexpr int SPREAD = W / RPH;
+                const int j = g / SPREAD;  // value index of this lane
+                if (in_group && g % SPREAD == 0 && g < W / 2) {
                     if (MODE == 0) {
-                        p.out[(int64_t)slot * I + t.sg.u + pos] =
-                            f32_to_bf16_bits(tot / (1.0f + __expf(-tot)) * tot1);
-                    } else {
+                        // pair pos + j: gate value j, up value UPT + j
+                        if (pos + j < t.sg.n)
+                            p.out[(int64_t)slot * I + t.sg.u + pos + j] =
+                                f32_to_bf16_bits(tot / (1.0f + __expf(-tot)) *
+                                                 tot1);
+                    } else if (j == 0 && pos < t.sg.n) {
+                        // rows pos (value 0) and pos + 1 (value 1)
                         const int tk = slot / p.topk;
                         const float r = tb.rw[slot];
                         float *a = acc + (size_t)(t.sg.u - blk0 + pos) * p.M + tk;
@@ -426,21 +430,17 @@ __global__ void __maxnreg__(128)
                     }
                 }
             }
-            return true;
-        };
-        // two passes in flight: the scales of pass t+2 load while pass t runs
-        while (ha) {
-            if (!process(ta, qa)) break;
-            ha = ahead.next(ta);
-            if (ha) fetch(ta, qa);
-            if (!hb) break;
-            if (!process(tb2, qb)) break;
-            hb = ahead.next(tb2);
-            if (hb) fetch(tb2, qb);
+            if (t.last) {
+                // every lane's reads of this stage are done: release it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
         }
     }
     __syncthreads();
-    pdl_wait_primary();  // outputs may alias the previous kernel's inputs
+    // Outputs are written by consumer threads only: they passed the
+    // dependency wait before reading the activations, so the previous grid
+    // (which may read what the outputs alias) is complete.
     // A timed-out pipeline must not leave bulk copies landing in shared
     // memory after the CTA exits: wait (again bounded) for every stage that
     // was issued but not consumed.
@@ -453,9 +453,9 @@ __global__ void __maxnreg__(128)
         // slots with an invalid expert: zero outputs, split over the CTAs
         const int64_t i0 = I * blockIdx.x / gridDim.x;
         const int64_t i1 = I * (blockIdx.x + 1) / gridDim.x;
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < S && tid < ncons; ++s) {
             if (tb.first[s] >= 0) continue;
-            for (int64_t i = i0 + tid; i < i1; i += blockDim.x)
+            for (int64_t i = i0 + tid; i < i1; i += ncons)
                 p.out[(int64_t)s * I + i] = 0;
         }
     } else {
@@ -463,11 +463,19 @@ __global__ void __maxnreg__(128)
         // writes its share of the block, adding the ranks in order
         cluster_sync_all();
         const int r0 = nblk * rank / CL, r1 = nblk * (rank + 1) / CL;
-        for (int i = tid; i < (r1 - r0) * p.M; i += blockDim.x) {
+        for (int i = tid; i < (r1 - r0) * p.M && tid < ncons; i += ncons) {
             const int r = r0 + i / p.M, t = i % p.M;
+            // all ranks' loads in flight at once, then added in rank order
+            float part[kMsMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMsMaxCluster; ++q)
+                part[q] = q < CL ? ld_cluster_f32(acc + (size_t)r * p.M + t,
+                                                  (uint32_t)q)
+                                 : 0.f;
             float y = 0.f;
-            for (int q = 0; q < CL; ++q)
-                y += ld_cluster_f32(acc + (size_t)r * p.M + t, (uint32_t)q);
+#pragma unroll
+            for (int q = 0; q < kMsMaxCluster; ++q)
+                if (q < CL) y += part[q];
             p.out[(int64_t)t * p.N + blk0 + r] = f32_to_bf16_bits(y);
         }
         // no CTA leaves while another still reads its accumulators
@@ -513,9 +521,10 @@ static int resident_clusters(const void *kern, int cl, size_t smem) {
 template <int BITS, int MODE, int W>
 static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
     constexpr int HALVES = MODE == 0 ? 2 : 1;
-    constexpr int UPT = MODE == 0 ? 1 : 2;
+    constexpr int UPT = 2;
     const int S = p.M * p.topk;
     const size_t rowbytes = (size_t)p.K * BITS / 8;
+    const size_t sbrow = (size_t)p.G * 2;
     const int rs = kMsConsumerWarps * kWarp / W;  // row groups per pass
     const int sbu = rs * UPT;
     int grid, ups, img_rows, nblk = 0, cl = 1;
@@ -523,7 +532,8 @@ static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
         grid = num_sms();
         // a stage holds whole passes, about kMsStageTarget bytes, and no
         // more than a CTA's share
-        int passes = (int)(kMsStageTarget / ((size_t)HALVES * rowbytes * sbu));
+        int passes = (int)(kMsStageTarget /
+                           ((size_t)HALVES * (rowbytes + 2 * sbrow) * sbu));
         if (passes < 1) passes = 1;
         ups = passes * sbu;
         const int64_t share = ((int64_t)S * (p.N / 2) + grid - 1) / grid;
@@ -546,7 +556,7 @@ static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
     int stages;
     cudaError_t e;
     for (;;) {
-        stage_bytes = (size_t)HALVES * ups * rowbytes;
+        stage_bytes = (size_t)HALVES * ups * (rowbytes + 2 * sbrow);
         accb = MODE == 1 ? (size_t)nblk * p.M * 4 : 0;
         const size_t fixed = 16 * kMsMaxStages + ((img + 15) / 16) * 16 + accb;
         if (fixed >= kMsSmemCap) return cudaSuccess;
@@ -601,8 +611,9 @@ static cudaError_t launch_ms_w(const MoeParams &p, cudaStream_t st,
     return launch_ms<BITS, MODE, 32>(p, st, used);
 }
 
-// Launches the streaming MoE kernel when the shape allows it (K <= 2048,
-// 16-byte aligned codes and activations, the encoded activations within the
+// Launches the streaming MoE kernel when the shape allows it (K <= 2048 and
+// a multiple of 512, 16-byte aligned codes, scales, biases and activations,
+// the encoded activations within the
 // shared-memory budget); *used tells the caller whether it ran.
 cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
                               bool *used) {
@@ -610,8 +621,8 @@ cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
     auto a16 = [](const void *q) {
         return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
     };
-    if (p.G > 32 || (p.G % 8) != 0 || !a16(p.wq) || !a16(p.x) ||
-        p.M * p.topk > kMsMaxSlots)
+    if (p.G > 32 || (p.G % 8) != 0 || !a16(p.wq) || !a16(p.sc) ||
+        !a16(p.bi) || !a16(p.x) || p.M * p.topk > kMsMaxSlots)
         return cudaSuccess;
     if (mode == 0)
         return p.bits == 4 ? launch_ms_w<4, 0>(p, st, used)
