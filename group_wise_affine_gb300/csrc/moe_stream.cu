@@ -55,7 +55,7 @@ constexpr int kMsThreads = (kMsConsumerWarps + 1) * kWarp;
 constexpr size_t kMsSmemCap = 100 * 1024;
 constexpr int kMsMaxSlots = 256;
 constexpr int kMsMaxStages = 16;
-constexpr int kMsMaxCluster = 4;    // down: CTAs sharing a row block
+constexpr int kMsMaxCluster = 8;    // down: CTAs sharing a row block
 constexpr int kMsMaxRows = 128;     // down: output rows per cluster
 constexpr size_t kMsStageTarget = 32 * 1024;
 
@@ -66,6 +66,7 @@ struct MsTables {
     int gexp[kMsMaxSlots];       // expert of a group
     int gstart[kMsMaxSlots + 1]; // slot range of a group in `order`
     int order[kMsMaxSlots];      // slots grouped by expert
+    int2 slotrow[kMsMaxSlots];   // order[q] and the image row of that slot
     int imgrow[kMsMaxSlots];     // image row holding a slot's activations
     int imgsrc[kMsMaxSlots];     // down: slot (source row) of an image row
     float rw[kMsMaxSlots];
@@ -78,31 +79,61 @@ struct MsStage {
     int gi, u, n;
 };
 
-// A CTA's stages in order; producer and consumers walk the same sequence.
-// Gate+up: units [u0, u1) of ng*I, cut at group ends.  Down: groups g0,
-// g0 + step, ..., each the row block [u0, u1) in chunks of ups rows.
+// A CTA's stages in order; producer and consumers walk the same sequence
+// (incremental, no division per stage).  Gate+up: units [u0, u1) of ng*I,
+// cut at group ends.  Down: groups g0, g0 + step, ..., each the row block
+// [u0, u1) in chunks of ups rows.
 struct MsWalk {
-    int mode, ups, step, g0, ng, nchunk;
-    int64_t I, u0, u1, cur;
+    int mode, ups;
+    int gi, ia, I;       // gate+up: group and unit within it
+    int64_t cur, u1;     // gate+up: next unit, end
+    int j, c, mine;      // down: group index among this rank's, chunk
+    int g0, step, nchunk, r0, r1;
+    __device__ void init_gate_up(int ups_, int64_t u0_, int64_t u1_, int I_) {
+        mode = 0;
+        ups = ups_;
+        I = I_;
+        cur = u0_;
+        u1 = u1_;
+        gi = (int)(u0_ / I_);
+        ia = (int)(u0_ - (int64_t)gi * I_);
+    }
+    __device__ void init_down(int ups_, int ng, int g0_, int step_, int r0_,
+                              int r1_) {
+        mode = 1;
+        ups = ups_;
+        g0 = g0_;
+        step = step_;
+        r0 = r0_;
+        r1 = r1_;
+        nchunk = r1_ > r0_ ? (r1_ - r0_ + ups_ - 1) / ups_ : 0;
+        mine = ng > g0_ && nchunk > 0 ? (ng - g0_ + step_ - 1) / step_ : 0;
+        j = 0;
+        c = 0;
+    }
     __device__ bool next(MsStage &s) {
         if (mode == 0) {
             if (cur >= u1) return false;
-            const int gi = (int)(cur / I);
-            const int64_t ia = cur - (int64_t)gi * I;
-            const int64_t n = min(min((int64_t)ups, I - ia), u1 - cur);
+            const int n = (int)min((int64_t)min(ups, I - ia), u1 - cur);
             s.gi = gi;
-            s.u = (int)ia;
-            s.n = (int)n;
+            s.u = ia;
+            s.n = n;
             cur += n;
+            ia += n;
+            if (ia == I) {
+                ++gi;
+                ia = 0;
+            }
             return true;
         }
-        const int64_t mine = ng > g0 ? (ng - g0 + step - 1) / step : 0;
-        if (cur >= mine * nchunk) return false;
-        const int j = (int)(cur / nchunk), c = (int)(cur - (int64_t)j * nchunk);
+        if (j >= mine) return false;
         s.gi = g0 + j * step;
-        s.u = (int)u0 + c * ups;
-        s.n = (int)min((int64_t)ups, u1 - s.u);
-        ++cur;
+        s.u = r0 + c * ups;
+        s.n = min(ups, r1 - s.u);
+        if (++c == nchunk) {
+            c = 0;
+            ++j;
+        }
         return true;
     }
 };
@@ -281,26 +312,20 @@ __global__ void __maxnreg__(128)
         pdl_launch_dependents();
     }
     __syncthreads();
+    for (int q = tid; q < tb.gstart[tb.ng]; q += blockDim.x) {
+        const int slot = tb.order[q];
+        tb.slotrow[q] = make_int2(slot, tb.imgrow[slot]);
+    }
+    __syncthreads();
 
     // this CTA's stages
     MsWalk walk{};
-    walk.mode = MODE;
-    walk.ups = ups;
-    walk.I = I;
-    walk.ng = tb.ng;
-    walk.step = CL;
-    walk.g0 = rank;
     if (MODE == 0) {
         const int64_t units = (int64_t)tb.ng * I;
-        walk.u0 = units * blockIdx.x / gridDim.x;
-        walk.u1 = units * (blockIdx.x + 1) / gridDim.x;
-        walk.cur = walk.u0;
+        walk.init_gate_up(ups, units * blockIdx.x / gridDim.x,
+                          units * (blockIdx.x + 1) / gridDim.x, (int)I);
     } else {
-        walk.u0 = blk0;
-        walk.u1 = blk1;
-        walk.nchunk = (int)((nblk + ups - 1) / ups);
-        if (nblk <= 0) walk.ng = 0;
-        walk.cur = 0;
+        walk.init_down(ups, tb.ng, rank, CL, (int)blk0, (int)blk1);
     }
 
     if (tid >= ncons) {
@@ -378,9 +403,10 @@ __global__ void __maxnreg__(128)
             }
             const unsigned char *base = smem + (size_t)s * stage_bytes;
             const int pos = t.sb + hgc * UPT;
-            for (int qi = tb.gstart[t.sg.gi]; qi < tb.gstart[t.sg.gi + 1]; ++qi) {
-                const int slot = tb.order[qi];
-                const int row = tb.imgrow[slot];
+            const int q1 = tb.gstart[t.sg.gi + 1];
+            for (int qi = tb.gstart[t.sg.gi]; qi < q1; ++qi) {
+                const int2 sr = tb.slotrow[qi];
+                const int slot = sr.x, row = sr.y;
                 if (row != cached) {
                     load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx,
                                        image_shift<BITS>(gg));
@@ -540,55 +566,66 @@ static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
         if ((int64_t)ups > share) ups = (int)(share > 0 ? share : 1);
         img_rows = p.M;
     } else {
-        // clusters of up to kMsMaxCluster CTAs, one CTA per SM; the largest
-        // size whose clusters all fit in one wave is chosen below
-        cl = kMsMaxCluster;
-        int clusters = num_sms() / cl;
-        if ((int64_t)clusters > p.N) clusters = (int)p.N;
-        nblk = (int)((p.N + clusters - 1) / clusters);
-        ups = (nblk + UPT - 1) / UPT * UPT;  // one stage per expert
         img_rows = S;
-        grid = clusters * cl;
     }
     auto kern = moe_stream_kernel<BITS, MODE, W>;
     const size_t img = ximg_bytes(img_rows, p.G);
-    size_t stage_bytes, accb, img_off, acc_off, smem;
-    int stages;
+    size_t stage_bytes = 0, accb = 0, img_off = 0, acc_off = 0, smem = 0;
+    int stages = 0;
     cudaError_t e;
-    for (;;) {
+    // shared-memory layout for a stage of `ups` units; false if the ring
+    // gets fewer than two stages (or a down block exceeds kMsMaxRows)
+    auto layout = [&]() -> bool {
         stage_bytes = (size_t)HALVES * ups * (rowbytes + 2 * sbrow);
         accb = MODE == 1 ? (size_t)nblk * p.M * 4 : 0;
         const size_t fixed = 16 * kMsMaxStages + ((img + 15) / 16) * 16 + accb;
-        if (fixed >= kMsSmemCap) return cudaSuccess;
+        if (fixed >= kMsSmemCap) return false;
         stages = (int)((kMsSmemCap - fixed) / stage_bytes);
         if (stages > kMsMaxStages) stages = kMsMaxStages;
         img_off = stages * stage_bytes + 16 * stages;
         acc_off = img_off + ((img + 15) / 16) * 16;
         smem = acc_off + accb;
-        const bool fits = stages >= 2 && (MODE == 0 || nblk <= kMsMaxRows);
-        if (fits) {
-            int dummy = 0;
-            e = occupancy_grid(reinterpret_cast<const void *>(kern),
-                               kMsThreads, smem, &dummy);
-            if (e != cudaSuccess) return e;
+        return stages >= 2 && (MODE == 0 || nblk <= kMsMaxRows);
+    };
+    if (MODE == 0) {
+        if (!layout()) return cudaSuccess;  // not used
+        int dummy = 0;
+        e = occupancy_grid(reinterpret_cast<const void *>(kern), kMsThreads,
+                           smem, &dummy);
+        if (e != cudaSuccess) return e;
+    } else {
+        // Clusters of up to kMsMaxCluster CTAs, one CTA per SM: the largest
+        // size of which one wave keeps at least 90% of the SMs busy.  Only
+        // the clusters one wave holds are launched (a GPC whose SM count
+        // the size does not divide leaves a few SMs out).
+        bool ok = false;
+        for (cl = kMsMaxCluster; cl >= 1 && !ok; cl /= 2) {
+            int clusters = num_sms() / cl;
+            if ((int64_t)clusters > p.N) clusters = (int)p.N;
+            for (int round = 0; round < 2 && !ok; ++round) {
+                nblk = (int)((p.N + clusters - 1) / clusters);
+                ups = (nblk + UPT - 1) / UPT * UPT;  // one stage per expert
+                if (!layout()) break;
+                int dummy = 0;
+                e = occupancy_grid(reinterpret_cast<const void *>(kern),
+                                   kMsThreads, smem, &dummy);
+                if (e != cudaSuccess) return e;
+                const int res =
+                    cl == 1 ? clusters
+                            : resident_clusters(
+                                  reinterpret_cast<const void *>(kern), cl, smem);
+                if (res >= clusters) {
+                    ok = true;
+                    grid = clusters * cl;
+                    break;
+                }
+                // longer blocks over fewer clusters, if enough SMs stay busy
+                if ((int64_t)res * cl * 10 < (int64_t)num_sms() * 9) break;
+                clusters = res;
+            }
+            if (ok) break;
         }
-        if (MODE == 0) {
-            if (!fits) return cudaSuccess;  // not used
-            break;
-        }
-        // down: keep this cluster size if all its clusters are resident
-        // at once, else try half of it
-        if (fits && (cl == 1 || resident_clusters(reinterpret_cast<const void *>(
-                                                      kern),
-                                                  cl, smem) >= grid / cl))
-            break;
-        if (cl == 1) return cudaSuccess;  // not used
-        cl /= 2;
-        int clusters = num_sms() / cl;
-        if ((int64_t)clusters > p.N) clusters = (int)p.N;
-        nblk = (int)((p.N + clusters - 1) / clusters);
-        ups = (nblk + UPT - 1) / UPT * UPT;
-        grid = clusters * cl;
+        if (!ok) return cudaSuccess;  // not used
     }
     e = prefer_max_shared(reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
@@ -622,7 +659,8 @@ cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
         return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
     };
     if (p.G > 32 || (p.G % 8) != 0 || !a16(p.wq) || !a16(p.sc) ||
-        !a16(p.bi) || !a16(p.x) || p.M * p.topk > kMsMaxSlots)
+        !a16(p.bi) || !a16(p.x) || p.M * p.topk > kMsMaxSlots ||
+        p.N >= (int64_t)1 << 30)
         return cudaSuccess;
     if (mode == 0)
         return p.bits == 4 ? launch_ms_w<4, 0>(p, st, used)
