@@ -84,9 +84,11 @@ def _load():
         lib.orc_moe_down_combine.argtypes = [_u16p, _i64, _i64, _i32p, _f32p,
                                              _u32p, _u16p, _u16p, _i64, _i64,
                                              _i64, _int, _int, _f64p, _int]
+        lib.orc_quantize_affine.argtypes = [_u16p, _i64, _i64, _int, _int,
+                                            _u32p, _u16p, _u16p]
         for name in ("orc_unpack", "orc_dequant", "orc_qmv",
                      "orc_gate_up_silu", "orc_moe_gate_up_silu",
-                     "orc_moe_down_combine"):
+                     "orc_moe_down_combine", "orc_quantize_affine"):
             getattr(lib, name).restype = _int
         _lib = lib
         return lib
@@ -221,6 +223,21 @@ def moe_down_combine(hin, ids, route_w, wq, scales, biases, E: int, N: int,
                                         group, y, nthreads),
            "moe_down_combine")
     return y
+
+
+def quantize_affine(w, N: int, K: int, bits: int, group: int = 64):
+    """Affine group quantization of bf16 weights w [N, K] (uint16 bit
+    patterns): returns (wq uint32 [N, K*bits/32], scales, biases uint16
+    [N, K/group]).  Per group: scale = bf16_rn((max - min) / (2^bits - 1)),
+    bias = min, code = clamp(rint((w - bias) / scale)) in fp32 (see
+    oracle.c for the reading and its source)."""
+    w = _c(w, np.uint16)
+    wq = np.empty((N, K * bits // 32), dtype=np.uint32)
+    sc = np.empty((N, K // group), dtype=np.uint16)
+    bi = np.empty((N, K // group), dtype=np.uint16)
+    _check(_load().orc_quantize_affine(w, N, K, bits, group, wq, sc, bi),
+           "quantize_affine")
+    return wq, sc, bi
 
 
 def within_tolerance(got, ref, rel: float = 1e-2):

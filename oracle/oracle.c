@@ -258,3 +258,84 @@ int orc_moe_down_combine(const uint16_t *hin, int64_t M, int64_t topk,
         }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------
+ * Affine quantization, the requantize step of "Sanctum-MLX", "The April 2026
+ * cutover" (LoRA merge at load: dequantize, add the delta, requantize at
+ * group size 64 and 4 bits; "File map": lora.rs merges quantized and
+ * switch_mlp expert weights).  The pages give no rounding rule; the plainest
+ * reading, per group of G consecutive inputs of a row:
+ *
+ *   lo = min w, hi = max w          (the bf16 values, exact in fp32)
+ *   s  = bf16_rn((hi - lo) / (2^b - 1))        fp32 subtract, divide (RN)
+ *   z  = lo                         (a bf16 value already: stored as is)
+ *   q  = clamp(rint((w - z) / s), 0, 2^b - 1)  fp32, round half to even;
+ *        q = 0 for every input when s == 0
+ *
+ * and the codes are packed lowest bits first, P = 32/b per word.  A code is
+ * an integer decided in floating point, so this step runs in the kernel's
+ * precision (IEEE fp32, round to nearest even) instead of fp64; both sides
+ * then reach the same code.  Inputs must be finite.
+ */
+
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even (finite input):
+ * add half an ulp of the kept part, plus one when the kept part is odd,
+ * then truncate to the top 16 bits. */
+static uint16_t f32_to_bf16_rn(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* w: bf16 [N, K]; out wq [N, K*b/32], scales and biases bf16 [N, K/G]. */
+int orc_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int bits,
+                        int group, uint32_t *wq, uint16_t *scales,
+                        uint16_t *biases) {
+    if (!shape_ok(N, K, bits, group)) return ORC_BAD_ARG;
+    const int64_t gpr = K / group, wpr = K * bits / 32;
+    const int per_word = 32 / bits;
+    const uint32_t qmax = (1u << bits) - 1u;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t w0 = 0; w0 < wpr; ++w0) wq[n * wpr + w0] = 0u;
+        for (int64_t g = 0; g < gpr; ++g) {
+            const uint16_t *src = w + n * K + g * group;
+            float lo = bf16_to_f32(src[0]), hi = lo;
+            for (int i = 1; i < group; ++i) {
+                const float v = bf16_to_f32(src[i]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            const float range = hi - lo;
+            const uint16_t sbits = f32_to_bf16_rn(range / (float)qmax);
+            const float s = bf16_to_f32(sbits);
+            uint16_t zbits;
+            {
+                uint32_t u;
+                memcpy(&u, &lo, sizeof u);
+                zbits = (uint16_t)(u >> 16);
+            }
+            scales[n * gpr + g] = sbits;
+            biases[n * gpr + g] = zbits;
+            for (int i = 0; i < group; ++i) {
+                uint32_t q = 0u;
+                if (s != 0.0f) {
+                    const float t = rintf((bf16_to_f32(src[i]) - lo) / s);
+                    q = t <= 0.0f ? 0u : t >= (float)qmax ? qmax : (uint32_t)t;
+                }
+                const int64_t k = g * group + i;
+                wq[n * wpr + k / per_word] |=
+                    q << (uint32_t)(bits * (k % per_word));
+            }
+        }
+    }
+    return ORC_OK;
+}
+
