@@ -343,6 +343,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
         del W8
         torch.cuda.empty_cache()
         extras["moe"] = run_moe_extra(dev, 50, 3)
+        extras["quantize"] = run_quantize_extra(dev, 20, 3)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
                 h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
@@ -498,6 +499,31 @@ def run_moe_extra(dev, steps, warmup, layers=16, E=256, H=2048, I=512,
         res[f"M{M}"] = {"us_per_layer": round(1e3 * ms / layers, 3),
                         "distinct_experts_per_layer": round(distinct / layers, 2),
                         "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
+    return res
+
+
+def run_quantize_extra(dev, steps, warmup, N=27648, K=5120):
+    """Affine quantization (the requantize step of a LoRA merge) of the
+    gate+up weight, bf16 [N, K] -> u4 and u8: bandwidth-bound, bytes = the
+    bf16 input read plus codes, scales and biases written.  The input (283
+    MB) exceeds L2, so back-to-back launches stream from HBM."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    g = torch.Generator(device=dev).manual_seed(4242)
+    w = (torch.randn((N, K), generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    peak, _ = measured_peak()
+    res = {}
+    for bits in (4, 8):
+        out = gwa.quantize_affine(w, bits=bits)
+        graph = capture(lambda: gwa.quantize_affine(w, bits=bits, out=out))
+        total, _ = time_graphs([graph], steps, warmup)
+        us = 1e3 * total / steps
+        byt = N * K * 2 + N * K * bits // 8 + N * (K // 64) * 4
+        gbs = byt / (us * 1e-6) / 1e9
+        res[f"u{bits}"] = {"shape": [N, K], "us_per_launch": round(us, 2),
+                           "bytes_per_launch": byt, "GB/s": round(gbs, 1),
+                           "frac_of_measured_hbm": round(gbs / peak, 4)}
+    del w
     return res
 
 

@@ -8,8 +8,8 @@ arithmetic runs in the library's sm_103a kernels.  There is no fallback: if
 
 Names mirror the C entry points without the ``gwa_`` prefix:
 ``qmv_affine``, ``qmv_fused_sections``, ``qmv_gate_up_silu``,
-``moe_qmv_gather``, ``workspace_bytes``, ``last_error``, ``debug_unpack``,
-``debug_dequant``.
+``moe_qmv_gather``, ``quantize_affine``, ``workspace_bytes``, ``last_error``,
+``debug_unpack``, ``debug_dequant``.
 
 Weights: ``wq`` int32 [N, K*bits/32] (the packed uint32 words), ``scales`` and
 ``biases`` bfloat16 [N, K/64].  Activations and outputs are bfloat16.
@@ -39,7 +39,7 @@ GWA_MOE_DOWN_COMBINE = 1
 EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
            "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant",
-           "gwa_qmv_affine_noalloc")
+           "gwa_qmv_affine_noalloc", "gwa_quantize_affine")
 
 
 class GwaError(RuntimeError):
@@ -89,6 +89,9 @@ def load(path: str = LIB_PATH):
     lib.gwa_qmv_affine_noalloc.restype = ctypes.c_int
     lib.gwa_pipeline_status.argtypes = [vp, i32]
     lib.gwa_pipeline_status.restype = ctypes.c_int
+    lib.gwa_quantize_affine.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp,
+                                        vp]
+    lib.gwa_quantize_affine.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
     lib.gwa_debug_dequant.argtypes = [_QW, vp, vp]
     for f in ("gwa_qmv_affine", "gwa_qmv_fused_sections",
@@ -353,6 +356,33 @@ def moe_qmv_gather(x: torch.Tensor, expert_ids: torch.Tensor, w: QWeight,
                                      _ptr(route_w), w.c(), num_experts, mode,
                                      _ptr(out), _ptr(status),
                                      _stream(stream)))
+    return out
+
+
+def quantize_affine(w: torch.Tensor, bits: int = 4, group: int = 64,
+                    out: Optional[QWeight] = None, stream=None) -> QWeight:
+    """gwa_quantize_affine: bf16 weights w [N, K] -> packed QWeight (codes,
+    bf16 scales and biases per 64 inputs).  Allocates the outputs unless
+    ``out`` (N, K, bits and group matching) is given."""
+    w = _bf16(w, "w")
+    if w.dim() != 2:
+        raise ValueError("w must be [N, K]")
+    N, K = w.shape
+    if out is None:
+        dev = w.device
+        out = QWeight(
+            torch.empty((N, max(K * bits // 32, 0)), dtype=torch.int32,
+                        device=dev),
+            torch.empty((N, max(K // group, 0)), dtype=torch.bfloat16,
+                        device=dev),
+            torch.empty((N, max(K // group, 0)), dtype=torch.bfloat16,
+                        device=dev),
+            N, K, bits, group)
+    elif (out.N, out.K, out.bits, out.group) != (N, K, bits, group):
+        raise ValueError("out does not match w's shape, bits and group")
+    _check(load().gwa_quantize_affine(_ptr(w), N, K, bits, group,
+                                      _ptr(out.wq), _ptr(out.scales),
+                                      _ptr(out.biases), _stream(stream)))
     return out
 
 

@@ -459,6 +459,26 @@ int gwa_debug_unpack(gwa_qweight w, uint8_t *codes, void *stream) {
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
 }
 
+int gwa_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int32_t bits,
+                        int32_t group, uint32_t *wq, uint16_t *scales,
+                        uint16_t *biases, void *stream) {
+    const char *fn = "gwa_quantize_affine";
+    g_last_error.clear();
+    // the output weight's checks are the projections' (bits, group, shape,
+    // alignment of wq / scales / biases)
+    const gwa_qweight out{wq, scales, biases, N, K, bits, group};
+    int rc = check_qweight(out, fn);
+    if (rc) return rc;
+    if (N == 0) return GWA_OK;
+    if (!w) return fail(GWA_ERR_INVALID_ARG, "%s: null w", fn);
+    if (!aligned(w, 16))
+        return fail(GWA_ERR_MISALIGNED, "%s: w must be 16-byte aligned", fn);
+    if ((rc = check_device())) return rc;
+    cudaError_t e = launch_quantize(w, N, K, bits, wq, scales, biases,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
+}
+
 int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream) {
     const char *fn = "gwa_debug_dequant";
     g_last_error.clear();

@@ -130,6 +130,11 @@ cudaError_t launch_moe_stream(int mode, const MoeParams &p, cudaStream_t st,
                               bool *used);
 unsigned int moe_stream_timeouts(bool reset);
 
+// Affine group quantization of bf16 weights (quantize.cu).
+cudaError_t launch_quantize(const uint16_t *w, int64_t N, int64_t K, int bits,
+                            uint32_t *wq, uint16_t *sc, uint16_t *bi,
+                            cudaStream_t st);
+
 cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
                                 int bits, uint8_t *codes, cudaStream_t st);
 cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,

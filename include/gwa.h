@@ -160,6 +160,29 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
 int gwa_qmv_affine_noalloc(const uint16_t *x, int64_t M, gwa_qweight w,
                            uint16_t *y, void *stream);
 
+/* gwa_quantize_affine -- affine group quantization of bf16 weights into the
+ * packed format every projection above reads: the requantize step of
+ * "Sanctum-MLX", "The April 2026 cutover" (LoRA merge at load dequantizes,
+ * adds the delta and requantizes at group size 64, 4 bits; "File map":
+ * lora.rs).  The pages state no rounding rule; this library's reading, per
+ * group of 64 consecutive inputs of a row, in IEEE fp32:
+ *   scale = bf16_rn((max - min) / (2^bits - 1)), bias = min (exact; a zero
+ *   minimum is stored as +0), code = clamp(rint((w - bias) / scale), 0,
+ *   2^bits - 1), round half to even, and code = 0 when scale == 0.
+ * So dequantizing gives back w within scale/2 + (2^bits - 1)|scale - (max -
+ * min)/(2^bits - 1)| per input.
+ *   w       bf16 [N, K] row-major (device), 16-byte aligned, finite values.
+ *   wq      out uint32 [N, K*bits/32]: codes lowest bits first (as read by
+ *           the projections); 16-byte aligned.
+ *   scales, biases  out bf16 [N, K/64]; 2-byte aligned.
+ *   bits 4 or 8, group 64, K a positive multiple of 64 (<= 2^20), N >= 0.
+ * The caller owns every buffer; the kernel runs on `stream`.  Errors:
+ * GWA_ERR_UNSUPPORTED (bits, group), GWA_ERR_INVALID_ARG (shape, null),
+ * GWA_ERR_MISALIGNED; nothing is enqueued on error. */
+int gwa_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int32_t bits,
+                        int32_t group, uint32_t *wq, uint16_t *scales,
+                        uint16_t *biases, void *stream);
+
 /* Text of the last error raised on this thread ("" if none). */
 const char *gwa_last_error(void);
 

@@ -268,7 +268,8 @@ int orc_moe_down_combine(const uint16_t *hin, int64_t M, int64_t topk,
  *
  *   lo = min w, hi = max w          (the bf16 values, exact in fp32)
  *   s  = bf16_rn((hi - lo) / (2^b - 1))        fp32 subtract, divide (RN)
- *   z  = lo                         (a bf16 value already: stored as is)
+ *   z  = lo                         (a bf16 value already: stored as is,
+ *                                    a zero as +0)
  *   q  = clamp(rint((w - z) / s), 0, 2^b - 1)  fp32, round half to even;
  *        q = 0 for every input when s == 0
  *
@@ -313,6 +314,9 @@ int orc_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int bits,
                 if (v < lo) lo = v;
                 if (v > hi) hi = v;
             }
+            /* a minimum of zero is stored as +0 whichever zeros occur
+             * (-0 + +0 = +0 in round to nearest) */
+            lo = lo + 0.0f;
             const float range = hi - lo;
             const uint16_t sbits = f32_to_bf16_rn(range / (float)qmax);
             const float s = bf16_to_f32(sbits);

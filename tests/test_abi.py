@@ -131,3 +131,20 @@ def test_binding_refuses_mismatched_sizes_before_any_call():
                                            dtype=torch.bfloat16))
     per_expert = gwa.expert_view(w, 4)
     assert per_expert.N == 2
+
+
+@needs_nvcc
+def test_quantize_arguments_are_checked(lib):
+    q = lambda **k: lib.gwa_quantize_affine(
+        k.get("w", 0x4000), k.get("N", 8), k.get("K", 128), k.get("bits", 4),
+        k.get("group", 64), k.get("wq", 0x1000), k.get("sc", 0x2000),
+        k.get("bi", 0x3000), None)
+    assert q(bits=3) == 2
+    assert q(group=32) == 2
+    assert q(K=100) == 1
+    assert q(N=-1) == 1
+    assert q(w=None) == 1
+    assert q(w=0x4008) == 3
+    assert q(wq=0x1004) == 3
+    assert q(sc=0x2001) == 3
+    assert q(N=0) == 0   # nothing to do, no device needed

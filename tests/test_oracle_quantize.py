@@ -155,3 +155,15 @@ def test_codes_are_monotone_in_the_weights(bits):
     codes = oracle.unpack(wq, 4, 64, bits).astype(int)
     assert np.all(np.diff(codes, axis=1) >= 0)
     assert np.all(codes[:, 0] == 0) and np.all(codes[:, -1] == (1 << bits) - 1)
+
+
+def test_zero_minimum_is_stored_as_positive_zero():
+    """-0 and +0 compare equal; whichever occurs, a zero minimum is stored
+    as +0 (bits 0x0000), so the stored bias does not depend on input order."""
+    vals = np.zeros((2, 64), dtype=np.float32)
+    vals[:, 5] = 1.0
+    vals[0, 0] = -0.0          # -0 first
+    vals[1, 7] = -0.0          # +0 first, -0 later
+    wq, sc, bi = oracle.quantize_affine(bf16_bits(vals), 2, 64, 4)
+    assert list(bi[:, 0]) == [0, 0]
+
