@@ -86,9 +86,12 @@ def _load():
                                              _i64, _int, _int, _f64p, _int]
         lib.orc_quantize_affine.argtypes = [_u16p, _i64, _i64, _int, _int,
                                             _u32p, _u16p, _u16p]
+        lib.orc_rope.argtypes = [_f64p, _i64, _i64, _i64, ctypes.c_double,
+                                 _i32p]
         for name in ("orc_unpack", "orc_dequant", "orc_qmv",
                      "orc_gate_up_silu", "orc_moe_gate_up_silu",
-                     "orc_moe_down_combine", "orc_quantize_affine"):
+                     "orc_moe_down_combine", "orc_quantize_affine",
+                     "orc_rope"):
             getattr(lib, name).restype = _int
         _lib = lib
         return lib
@@ -238,6 +241,27 @@ def quantize_affine(w, N: int, K: int, bits: int, group: int = 64):
     _check(_load().orc_quantize_affine(w, N, K, bits, group, wq, sc, bi),
            "quantize_affine")
     return wq, sc, bi
+
+
+def rope(y, head_dim: int, base: float, positions) -> np.ndarray:
+    """Rotary embedding (rotate-half pairing) of y [M, width] (fp64, width a
+    multiple of head_dim) at positions[m]; returns a new array."""
+    out = np.array(y, dtype=np.float64, order="C", copy=True)
+    M, width = out.shape
+    pos = _c(positions, np.int32)
+    _check(_load().orc_rope(out, M, width, head_dim, float(base), pos), "rope")
+    return out
+
+
+def qkv_rope(x, wq, scales, biases, q_size: int, kv_size: int, K: int,
+             bits: int, head_dim: int, base: float, positions, out_bias=None,
+             group: int = 64):
+    """The fused QKV projection split into Q, K, V (optional additive bias
+    per output), then RoPE on Q and K.  Returns [Q, K, V] (fp64)."""
+    q, k, v = fused_sections(x, wq, scales, biases, [q_size, kv_size, kv_size],
+                             K, bits, group=group, out_bias=out_bias)
+    return [rope(q, head_dim, base, positions), rope(k, head_dim, base, positions),
+            v]
 
 
 def within_tolerance(got, ref, rel: float = 1e-2):

@@ -343,3 +343,42 @@ int orc_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int bits,
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------
+ * Rotary position embedding of the fused QKV output ("The Cathedral Doubled
+ * Itself", "The kernel that worked and the kernel that won't": the next step
+ * after the fused projection is a kernel that also applies RoPE to the
+ * materialized Q and K, which the pages designed but did not ship; "The trap
+ * that ate three hours": RoPE consumes Q and K per head at the cache offset).
+ * The pages give no formula; the textbook form with the rotate-half pairing
+ * (element i of a head with element i + d/2):
+ *
+ *   theta_i = pos * base^(-2i/d),  i = 0 .. d/2 - 1
+ *   y'[i]       = y[i] cos theta_i - y[i + d/2] sin theta_i
+ *   y'[i + d/2] = y[i + d/2] cos theta_i + y[i] sin theta_i
+ *
+ * for every head of Q and of K (d = head_dim), in place on fp64 rows;
+ * pos = positions[m] for token m.  V is not rotated.
+ */
+int orc_rope(double *y, int64_t M, int64_t width, int64_t head_dim,
+             double base, const int32_t *positions) {
+    if (M < 0 || width < 0 || head_dim <= 0 || head_dim % 2 != 0 ||
+        width % head_dim != 0 || !(base > 0.0))
+        return ORC_BAD_ARG;
+    const int64_t half = head_dim / 2;
+    for (int64_t m = 0; m < M; ++m) {
+        const double pos = (double)positions[m];
+        for (int64_t h = 0; h < width / head_dim; ++h) {
+            double *row = y + m * width + h * head_dim;
+            for (int64_t i = 0; i < half; ++i) {
+                const double theta =
+                    pos * pow(base, -2.0 * (double)i / (double)head_dim);
+                const double c = cos(theta), sn = sin(theta);
+                const double a = row[i], b = row[i + half];
+                row[i] = a * c - b * sn;
+                row[i + half] = b * c + a * sn;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
