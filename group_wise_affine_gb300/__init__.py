@@ -8,7 +8,8 @@ arithmetic runs in the library's sm_103a kernels.  There is no fallback: if
 
 Names mirror the C entry points without the ``gwa_`` prefix:
 ``qmv_affine``, ``qmv_fused_sections``, ``qmv_gate_up_silu``,
-``moe_qmv_gather``, ``quantize_affine``, ``workspace_bytes``, ``last_error``,
+``qmv_qkv_rope``, ``moe_qmv_gather``, ``quantize_affine``, ``workspace_bytes``,
+``last_error``,
 ``debug_unpack``, ``debug_dequant``.
 
 Weights: ``wq`` int32 [N, K*bits/32] (the packed uint32 words), ``scales`` and
@@ -39,7 +40,8 @@ GWA_MOE_DOWN_COMBINE = 1
 EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
            "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant",
-           "gwa_qmv_affine_noalloc", "gwa_quantize_affine")
+           "gwa_qmv_affine_noalloc", "gwa_quantize_affine", "gwa_qmv_qkv_rope",
+           "gwa_qkv_rope_workspace_bytes")
 
 
 class GwaError(RuntimeError):
@@ -91,6 +93,12 @@ def load(path: str = LIB_PATH):
     lib.gwa_pipeline_status.restype = ctypes.c_int
     lib.gwa_quantize_affine.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp,
                                         vp]
+    lib.gwa_qmv_qkv_rope.argtypes = [vp, i64, _QW, i64, i64, i32,
+                                     ctypes.c_double, vp, vp, vp, vp, vp, vp,
+                                     sz, vp]
+    lib.gwa_qmv_qkv_rope.restype = ctypes.c_int
+    lib.gwa_qkv_rope_workspace_bytes.argtypes = [i64, i32]
+    lib.gwa_qkv_rope_workspace_bytes.restype = sz
     lib.gwa_quantize_affine.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
     lib.gwa_debug_dequant.argtypes = [_QW, vp, vp]
@@ -297,6 +305,46 @@ def qmv_fused_sections(x: torch.Tensor, w: QWeight, sections: Sequence[int],
     _check(load().gwa_qmv_fused_sections(
         _ptr(x), M, w.c(), n, ctypes.cast(sizes, ctypes.c_void_p),
         ctypes.cast(optrs, ctypes.c_void_p),
+        ctypes.cast(bptrs, ctypes.c_void_p) if bptrs is not None else None,
+        wp, wn, _stream(stream)))
+    return list(outs)
+
+
+def qmv_qkv_rope(x: torch.Tensor, w: QWeight, q_size: int, kv_size: int,
+                 head_dim: int, rope_base: float, positions: torch.Tensor,
+                 outs: Optional[List[torch.Tensor]] = None,
+                 out_bias: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                 workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> List[torch.Tensor]:
+    """gwa_qmv_qkv_rope: the fused QKV projection into contiguous Q, K, V,
+    with the rotary embedding of Q and K at ``positions`` (int32 [M] on the
+    device)."""
+    x = _bf16(x, "x")
+    _check_weight(w)
+    M = x.numel() // w.K
+    sections = (q_size, kv_size, kv_size)
+    if positions.dtype != torch.int32 or positions.numel() < M:
+        raise ValueError("positions must be int32 with one entry per token")
+    if outs is None:
+        outs = [torch.empty((M, s), dtype=torch.bfloat16, device=x.device)
+                for s in sections]
+    if len(outs) != 3:
+        raise ValueError("three outputs: Q, K, V")
+    for i, (o, size) in enumerate(zip(outs, sections)):
+        _check_out(o, M * size, f"outs[{i}]")
+    bptrs = None
+    if out_bias is not None:
+        for i, (b, size) in enumerate(zip(out_bias, sections)):
+            if b is not None:
+                _check_out(b, size, f"out_bias[{i}]")
+        bptrs = (ctypes.c_void_p * 3)(*[_ptr(b) for b in out_bias])
+    if workspace is None and M > 1:
+        n = int(load().gwa_qkv_rope_workspace_bytes(M, head_dim))
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    wp, wn = _ws(workspace)
+    _check(load().gwa_qmv_qkv_rope(
+        _ptr(x), M, w.c(), q_size, kv_size, head_dim, float(rope_base),
+        _ptr(positions), _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]),
         ctypes.cast(bptrs, ctypes.c_void_p) if bptrs is not None else None,
         wp, wn, _stream(stream)))
     return list(outs)

@@ -210,7 +210,11 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         DenseParams q = p;
         q.M = (int)((M - t0) < mt ? (M - t0) : mt);
         q.x = p.x + t0 * p.K;
-        if (mode == 1) {
+        if (mode == 3) {
+            q.rope_pos = p.rope_pos + t0;
+            q.rope_cs = p.rope_cs + t0 * (p.rope_hd / 2);
+        }
+        if (mode == 1 || mode == 3) {
             for (int s = 0; s < p.nsec; ++s)
                 q.sec_out[s] = p.sec_out[s] ? p.sec_out[s] + t0 * sec_sizes[s]
                                             : nullptr;
@@ -219,7 +223,9 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         }
         bool used = false;
         cudaError_t e = launch_group(mode, q, st, &used);
-        if (e == cudaSuccess && !used) e = launch_stream(mode, q, st, &used);
+        // the streaming kernel has no rotary-embedding mode
+        if (e == cudaSuccess && !used && mode != 3)
+            e = launch_stream(mode, q, st, &used);
         if (e == cudaSuccess && !used) e = launch_dense(mode, q, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
@@ -349,6 +355,93 @@ int gwa_qmv_fused_sections(const uint16_t *x, int64_t M, gwa_qweight w,
                            workspace_bytes, st, fn);
     }
     return run_dense(1, p, M, 0, section_sizes, st, fn);
+}
+
+int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
+                     int64_t q_size, int64_t kv_size, int32_t head_dim,
+                     double rope_base, const int32_t *positions, uint16_t *q,
+                     uint16_t *k, uint16_t *v,
+                     const uint16_t *const *out_bias, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    const char *fn = "gwa_qmv_qkv_rope";
+    g_last_error.clear();
+    int rc = check_qweight(w, fn);
+    if (!rc) rc = check_x(x, M, fn);
+    if (rc) return rc;
+    if (head_dim < 2 || head_dim % 2 != 0 || head_dim > 256)
+        return fail(GWA_ERR_INVALID_ARG, "%s: head_dim=%d (even, 2..256)", fn,
+                    (int)head_dim);
+    if (q_size < 0 || kv_size < 0 || q_size % head_dim != 0 ||
+        kv_size % head_dim != 0)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: q_size=%lld kv_size=%lld (multiples of head_dim)", fn,
+                    (long long)q_size, (long long)kv_size);
+    if (q_size + 2 * kv_size != w.N)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: q_size + 2*kv_size = %lld, weight has %lld rows", fn,
+                    (long long)(q_size + 2 * kv_size), (long long)w.N);
+    if (!(rope_base > 0.0) || rope_base > 1e30)
+        return fail(GWA_ERR_INVALID_ARG, "%s: rope_base=%g", fn, rope_base);
+    uint16_t *outs[3] = {q, k, v};
+    const int64_t sizes[3] = {q_size, kv_size, kv_size};
+    for (int s = 0; s < 3; ++s) {
+        if (sizes[s] > 0 && M > 0 && !outs[s])
+            return fail(GWA_ERR_INVALID_ARG, "%s: null output %d", fn, s);
+        if (!aligned(outs[s], 2))
+            return fail(GWA_ERR_MISALIGNED, "%s: output %d alignment", fn, s);
+        if (out_bias && !aligned(out_bias[s], 2))
+            return fail(GWA_ERR_MISALIGNED, "%s: bias %d alignment", fn, s);
+    }
+    if (M > 0 && !positions)
+        return fail(GWA_ERR_INVALID_ARG, "%s: null positions", fn);
+    if (!aligned(positions, 4))
+        return fail(GWA_ERR_MISALIGNED, "%s: positions alignment", fn);
+    if (M == 0 || w.N == 0) return GWA_OK;
+    if ((rc = check_device())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DenseParams p = dense_base(x, M, w);
+    p.nsec = 3;
+    p.sec_start[0] = 0;
+    for (int s = 0; s < 3; ++s) {
+        p.sec_start[s + 1] = p.sec_start[s] + sizes[s];
+        p.sec_out[s] = outs[s];
+        p.sec_bias[s] = out_bias ? out_bias[s] : nullptr;
+    }
+    DenseParams r = p;
+    r.rope_hd = head_dim;
+    r.rope_end = q_size + kv_size;
+    r.rope_pos = positions;
+    r.rope_base = rope_base;
+    if (M == 1) {
+        // the one-token kernel forms its own (cos, sin) and rotates Q and K
+        // in its epilogue
+        bool used = false;
+        cudaError_t e = launch_group(3, r, st, &used);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        if (used) return GWA_OK;
+    }
+    // otherwise a (cos, sin) table in the workspace, then the staged kernels
+    // rotate in their epilogues, in passes of up to eight tokens
+    const size_t need = gwa_qkv_rope_workspace_bytes(M, head_dim);
+    if (!workspace || workspace_bytes < need)
+        return fail(GWA_ERR_WORKSPACE,
+                    "%s: M=%lld head_dim=%d needs %zu bytes of workspace (got "
+                    "%zu)", fn, (long long)M, (int)head_dim, need,
+                    workspace_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return fail(GWA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned",
+                    fn);
+    float2 *cs = static_cast<float2 *>(workspace);
+    cudaError_t e = launch_rope_table(cs, M, head_dim, rope_base, positions, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    r.rope_cs = cs;
+    return run_dense(3, r, M, 0, sizes, st, fn);
+}
+
+size_t gwa_qkv_rope_workspace_bytes(int64_t M, int32_t head_dim) {
+    if (M < 1 || head_dim < 2) return 0;
+    const size_t b = (size_t)M * (size_t)(head_dim / 2) * 8;
+    return (b + 255) / 256 * 256;
 }
 
 int gwa_qmv_gate_up_silu(const uint16_t *x, int64_t M, gwa_qweight w,

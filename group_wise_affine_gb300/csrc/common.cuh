@@ -244,6 +244,23 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
     return true;
 }
 
+// cos and sin of the rotary angle theta = pos * base^(-2i/d) (textbook
+// RoPE, pair index i of a head of d).  theta is formed and reduced modulo
+// 2 pi in fp64 (2 pi split in two doubles), so the fp32 sincos sees an
+// argument within [-pi, pi] accurate to ~1e-15 even at positions of 10^5
+// and more; an fp32 angle would be off by ~1e-2 rad at position 32K.
+__device__ __forceinline__ float2 rope_cos_sin(int pos, int i, int d,
+                                              double base) {
+    const double theta =
+        (double)pos * pow(base, -2.0 * (double)i / (double)d);
+    const double k = rint(theta * 0.15915494309189535);  // 1 / (2 pi)
+    double r = fma(-k, 6.283185307179586, theta);
+    r = fma(-k, 2.4492935982947064e-16, r);
+    float sn, cs;
+    sincosf((float)r, &sn, &cs);
+    return make_float2(cs, sn);
+}
+
 // Contiguous global -> shared copy completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,

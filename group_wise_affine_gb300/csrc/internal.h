@@ -38,7 +38,18 @@ struct DenseParams {
     int64_t sec_start[kMaxSections + 1];
     uint16_t *sec_out[kMaxSections];
     const uint16_t *sec_bias[kMaxSections];
+    // rotary embedding (one-token kernel, QKV mode): rows [0, rope_end) are
+    // rotated in heads of rope_hd at positions rope_pos[m]
+    int rope_hd;
+    int64_t rope_end;
+    const int32_t *rope_pos;  // one-token kernel: forms its own (cos, sin)
+    double rope_base;
+    const float2 *rope_cs;    // staged kernel: (cos, sin) [M, rope_hd / 2]
 };
+
+// (cos, sin) table of the rotary embedding, cs[m * d/2 + i] (rope.cu).
+cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double base,
+                              const int32_t *positions, cudaStream_t st);
 
 // Launches `kernel` on `st` with programmatic stream serialization: it may
 // start while the previous kernel in the stream drains; the kernel itself
@@ -96,6 +107,8 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
                           bool *used);
 unsigned int stream_timeouts(bool reset);
 // One-token kernel with one quantization group per lane (qmv_group.cu).
+// mode: 0 plain, 1 sections, 2 gate+up SiLU, 3 QKV sections with the
+// rotary embedding of rows [0, p.rope_end)
 cudaError_t launch_group(int mode, const DenseParams &p, cudaStream_t st,
                          bool *used);
 unsigned int group_timeouts(bool reset);

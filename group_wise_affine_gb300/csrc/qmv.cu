@@ -20,7 +20,14 @@
 
 namespace gwa {
 
-enum DenseMode { kPlain = 0, kSections = 1, kGateUp = 2 };
+enum DenseMode { kPlain = 0, kSections = 1, kGateUp = 2, kRope = 3 };
+
+// QKV sections with the rotary embedding: a pair is rows (i, i + d/2) of a
+// head (d = p.rope_hd), laid out like a gate/up pair.
+__device__ __forceinline__ int64_t rope_pair_row(int64_t n, int h, int d) {
+    const int64_t half = d / 2;
+    return (n / half) * d + (n % half) + h * half;
+}
 
 template <int BITS, int MT, int R, int MODE>
 __global__ void __launch_bounds__(kDenseThreads)
@@ -37,7 +44,8 @@ __global__ void __launch_bounds__(kDenseThreads)
     const int warp = threadIdx.x / kWarp;
     const WView v{reinterpret_cast<const uint4 *>(p.wq), p.sc, p.bi, p.nch,
                   p.G};
-    constexpr int RP = MODE == kGateUp ? R / 2 : R;  // output rows per block
+    constexpr bool PAIRS = MODE == kGateUp || MODE == kRope;
+    constexpr int RP = PAIRS ? R / 2 : R;  // output units per block
 
     for (int64_t b = blockIdx.x + (int64_t)gridDim.x * warp; b < p.nblocks;
          b += (int64_t)gridDim.x * (kDenseThreads / kWarp)) {
@@ -47,6 +55,9 @@ __global__ void __launch_bounds__(kDenseThreads)
             if constexpr (MODE == kGateUp) {
                 const int64_t n = b * RP + (r % RP);
                 rows[r] = n < p.I ? (r < RP ? n : p.I + n) : -1;
+            } else if constexpr (MODE == kRope) {
+                const int64_t n = b * RP + (r % RP);  // pair
+                rows[r] = n < p.N / 2 ? rope_pair_row(n, r / RP, p.rope_hd) : -1;
             } else {
                 const int64_t n = b * R + r;
                 rows[r] = n < p.N ? n : -1;
@@ -64,9 +75,34 @@ __global__ void __launch_bounds__(kDenseThreads)
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (lane != r * MT + m || m >= p.M) continue;
-                const int64_t n = MODE == kGateUp ? b * RP + r : rows[r];
-                if (n < 0 || (MODE == kGateUp && n >= p.I)) continue;
-                if constexpr (MODE == kPlain) {
+                const int64_t n = PAIRS ? b * RP + r : rows[r];
+                if (n < 0 || (MODE == kGateUp && n >= p.I) ||
+                    (MODE == kRope && n >= p.N / 2))
+                    continue;
+                if constexpr (MODE == kRope) {
+                    // pair n: rows r0 and r0 + d/2 of one head; sections
+                    // are whole heads
+                    const int half = p.rope_hd / 2;
+                    const int64_t r0 = rope_pair_row(n, 0, p.rope_hd);
+                    int s = 0;
+                    while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
+                    const int64_t j = r0 - p.sec_start[s];
+                    const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+                    float a = acc[r][m], c = acc[RP + r][m];
+                    if (p.sec_bias[s]) {
+                        a += bf16_bits_to_f32(p.sec_bias[s][j]);
+                        c += bf16_bits_to_f32(p.sec_bias[s][j + half]);
+                    }
+                    if (r0 < p.rope_end) {
+                        const float2 t = p.rope_cs[(int64_t)m * half + n % half];
+                        const float a2 = a * t.x - c * t.y;
+                        c = c * t.x + a * t.y;
+                        a = a2;
+                    }
+                    uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
+                    o[0] = f32_to_bf16_bits(a);
+                    o[half] = f32_to_bf16_bits(c);
+                } else if constexpr (MODE == kPlain) {
                     p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(acc[r][m]);
                 } else if constexpr (MODE == kGateUp) {
                     p.y[(int64_t)m * p.I + n] =
@@ -95,6 +131,7 @@ static cudaError_t launch_dense_t(const DenseParams &p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     DenseParams q = p;
     q.nblocks = MODE == kGateUp ? (p.I + R / 2 - 1) / (R / 2)
+                : MODE == kRope ? (p.N / 2 + R / 2 - 1) / (R / 2)
                                 : (p.N + R - 1) / R;
     if ((int64_t)grid > q.nblocks) grid = (int)q.nblocks;
     if (grid < 1) grid = 1;
@@ -125,6 +162,9 @@ int dense_max_tokens(int bits, int nch) {
 }
 
 cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st) {
+    if (mode == kRope)
+        return p.bits == 4 ? launch_dense_m<4, kRope>(p, st)
+                           : launch_dense_m<8, kRope>(p, st);
     if (p.bits == 4) {
         if (mode == kPlain) return launch_dense_m<4, kPlain>(p, st);
         if (mode == kSections) return launch_dense_m<4, kSections>(p, st);

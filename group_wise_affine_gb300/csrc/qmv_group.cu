@@ -25,7 +25,15 @@ namespace gwa {
 
 static __device__ unsigned int g_group_timeouts;
 
-enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2 };
+enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2, kGRope = 3 };
+
+// QKV with the rotary embedding: a unit is the pair of rows (i, i + d/2) of
+// a head (d = p.rope_hd), the pairing the rotation needs, laid out like a
+// gate/up pair; units are cut into stages of whole pairs within one head.
+__device__ __forceinline__ int64_t rope_row(int64_t u, int h, int d) {
+    const int64_t half = d / 2;
+    return (u / half) * d + (u % half) + h * half;
+}
 
 constexpr int kSlice = 16;  // lanes per reduction slice
 // Two CTAs per SM (this one and the next kernel's) must fit in registers.
@@ -48,8 +56,8 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
 template <int BITS, int MT, int MODE, int RPH>
 __global__ void __maxnreg__(88)
     qmv_group_kernel(DenseParams p, int stages, int64_t units, int rs,
-                     int slices, uint32_t xenc_off) {
-    constexpr int HALVES = MODE == kGGateUp ? 2 : 1;
+                     int slices, uint32_t xenc_off, uint32_t rope_off) {
+    constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;
     constexpr int V = RPH * MT;
     constexpr int GB = BITS * 8;  // bytes of codes per row and group
@@ -68,8 +76,10 @@ __global__ void __maxnreg__(88)
     float *red = reinterpret_cast<float *>(empty + stages);
     __shared__ int s_issued, s_consumed;
 
-    const int64_t u0 = units * blockIdx.x / gridDim.x;
-    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+    // rope: whole stages per CTA (ups divides d/2), so no stage crosses a head
+    const int64_t ualign = MODE == kGRope ? rs * UPT : 1;
+    const int64_t u0 = units / ualign * blockIdx.x / gridDim.x * ualign;
+    const int64_t u1 = units / ualign * (blockIdx.x + 1) / gridDim.x * ualign;
     const int nu = (int)(u1 - u0);
     const int nst = (nu + ups - 1) / ups;
 
@@ -88,6 +98,19 @@ __global__ void __maxnreg__(88)
 
     if (tid >= ncons) {
         // ------------------------------------------------ producer
+        if (MODE == kGRope && tid > ncons) {
+            // the other lanes of the producer warp: the CTA's (cos, sin)
+            // table, before the wait (positions are an input no kernel of
+            // this library writes), off the critical path
+            float2 *cs = reinterpret_cast<float2 *>(smem + rope_off);
+            const int half = p.rope_hd / 2;
+            for (int e = tid - ncons - 1; e < nu * MT; e += kWarp - 1) {
+                const int64_t n = u0 + e / MT;
+                if (rope_row(n, 0, p.rope_hd) < p.rope_end)
+                    cs[e] = rope_cos_sin(p.rope_pos[e % MT], (int)(n % half),
+                                         p.rope_hd, p.rope_base);
+            }
+        }
         if (tid == ncons) {
             const unsigned char *wq =
                 reinterpret_cast<const unsigned char *>(p.wq);
@@ -116,7 +139,8 @@ __global__ void __maxnreg__(88)
                                              (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                    const int64_t r = ua + (h ? p.I : 0);
+                    const int64_t r = MODE == kGRope ? rope_row(ua, h, p.rope_hd)
+                                                     : ua + (h ? p.I : 0);
                     bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
                              n * rowbytes, &full[s]);
                     bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
@@ -233,6 +257,30 @@ __global__ void __maxnreg__(88)
             const float uv = slot_total(red, (lu * 2 + 1) * MT + m, slices);
             p.y[(int64_t)m * p.I + n] =
                 f32_to_bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+        } else if constexpr (MODE == kGRope) {
+            // pair (r0, r0 + d/2) of a head; sections are whole heads
+            const int half = p.rope_hd / 2;
+            float a = slot_total(red, (lu * 2 + 0) * MT + m, slices);
+            float b = slot_total(red, (lu * 2 + 1) * MT + m, slices);
+            const int64_t r0 = rope_row(n, 0, p.rope_hd);
+            int s = 0;
+            while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
+            const int64_t j = r0 - p.sec_start[s];
+            const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+            if (p.sec_bias[s]) {
+                a += bf16_bits_to_f32(p.sec_bias[s][j]);
+                b += bf16_bits_to_f32(p.sec_bias[s][j + half]);
+            }
+            if (r0 < p.rope_end) {
+                const float2 c =
+                    reinterpret_cast<const float2 *>(smem + rope_off)[i];
+                const float a2 = a * c.x - b * c.y;
+                b = b * c.x + a * c.y;
+                a = a2;
+            }
+            uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
+            o[0] = f32_to_bf16_bits(a);
+            o[half] = f32_to_bf16_bits(b);
         } else if constexpr (MODE == kGPlain) {
             p.y[(int64_t)m * p.N + n] =
                 f32_to_bf16_bits(slot_total(red, lu * MT + m, slices));
@@ -252,9 +300,10 @@ __global__ void __maxnreg__(88)
 template <int BITS, int MT, int MODE, int RPH>
 static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
                                   bool *used) {
-    constexpr int HALVES = MODE == kGGateUp ? 2 : 1;
+    constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;
-    const int64_t units = MODE == kGGateUp ? p.I : p.N;
+    const int64_t units =
+        MODE == kGGateUp ? p.I : MODE == kGRope ? p.N / 2 : p.N;
     const size_t rowbytes = (size_t)p.K * BITS / 8;
     const size_t sbrow = (size_t)p.G * 2;
     const int slices = (p.G + kSlice - 1) / kSlice;
@@ -265,21 +314,30 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     const int ncons = ((rs * slices * kSlice + kWarp - 1) / kWarp) * kWarp;
     const int threads = ncons + kWarp;
     if (threads > kGroupMaxThreads) return cudaSuccess;  // not used
+    // rope: stages of whole pairs within one head
+    if (MODE == kGRope && ((p.rope_hd / 2) % (rs * UPT)) != 0)
+        return cudaSuccess;  // not used
     const size_t stage_bytes = (size_t)HALVES * rs * UPT * (rowbytes + 2 * sbrow);
     // one CTA per SM, so the next kernel's CTA fits beside it and can
     // prefetch while this one drains
     int grid = num_sms();
     if ((int64_t)grid > units) grid = (int)units;
-    const size_t red_bytes =
-        (size_t)((units + grid - 1) / grid) * HALVES * MT * 4 * slices;
-    const size_t fixed = 16 * 8 + ((red_bytes + 15) / 16) * 16 +
+    // units per CTA, at most (rope: plus one stage for the alignment)
+    const int64_t umax = (units + grid - 1) / grid + (MODE == kGRope ? rs * UPT : 0);
+    const size_t red_bytes = (size_t)umax * HALVES * MT * 4 * slices;
+    // (cos, sin) per pair and token; rounded to 16 bytes, since the
+    // activation image after it is read and written in 16-byte units
+    const size_t rope_bytes =
+        MODE == kGRope ? ((size_t)umax * MT * 8 + 15) / 16 * 16 : 0;
+    const size_t fixed = 16 * 8 + ((red_bytes + 15) / 16) * 16 + rope_bytes +
                          ximg_bytes(MT, p.G);
     if (fixed >= kGroupSmemCap) return cudaSuccess;
     int stages = (int)((kGroupSmemCap - fixed) / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) return cudaSuccess;  // rows too long for the ring
-    const size_t xenc_off =
+    const size_t rope_off =
         stages * stage_bytes + 16 * stages + ((red_bytes + 15) / 16) * 16;
+    const size_t xenc_off = rope_off + rope_bytes;
     const size_t smem = xenc_off + ximg_bytes(MT, p.G);
     auto kern = qmv_group_kernel<BITS, MT, MODE, RPH>;
     int dummy = 0;
@@ -289,7 +347,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,
                       smem, st, p, stages, units, rs, slices,
-                      (uint32_t)xenc_off);
+                      (uint32_t)xenc_off, (uint32_t)rope_off);
 }
 
 static bool aligned16g(const void *q) {
@@ -305,6 +363,9 @@ cudaError_t launch_group(int mode, const DenseParams &p, cudaStream_t st,
     if (p.M != 1 || (p.G % 8) != 0 || !aligned16g(p.sc) ||
         !aligned16g(p.bi) || !aligned16g(p.wq))
         return cudaSuccess;
+    if (mode == kGRope)
+        return p.bits == 4 ? launch_group_r<4, 1, kGRope, 2>(p, st, used)
+                           : launch_group_r<8, 1, kGRope, 2>(p, st, used);
     if (p.bits == 4) {
         if (mode == kGPlain) return launch_group_r<4, 1, kGPlain, 2>(p, st, used);
         if (mode == kGSections)

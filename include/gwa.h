@@ -160,6 +160,49 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
 int gwa_qmv_affine_noalloc(const uint16_t *x, int64_t M, gwa_qweight w,
                            uint16_t *y, void *stream);
 
+/* gwa_qmv_qkv_rope -- the fused QKV projection (gwa_qmv_fused_sections with
+ * the three sections Q, K, V) followed by the rotary position embedding of Q
+ * and K: the step the pages design after the fused projection ("The
+ * Cathedral Doubled Itself", "The kernel that worked and the kernel that
+ * won't": RoPE on the materialized Q and K; "The trap that ate three hours":
+ * RoPE runs per head at the cache offset).  The pages give no formula; this
+ * library uses the textbook one with the rotate-half pairing: for every head
+ * of head_dim = d in Q and in K, and i < d/2,
+ *   t = positions[m] * rope_base^(-2i/d),
+ *   (y[i], y[i + d/2]) -> (y[i] cos t - y[i + d/2] sin t,
+ *                          y[i + d/2] cos t + y[i] sin t),
+ * applied after the optional per-output bias; V is not rotated.  No frequency
+ * scaling (YaRN and the like) is applied.
+ *   w          fused weight, rows [0, q_size) = Q, then K, then V (kv_size
+ *              each); q_size and kv_size multiples of head_dim.
+ *   head_dim   even, 2..256.  rope_base > 0 (e.g. 10000 or 1e6).
+ *   positions  int32 [M] on the device: the position of each token (cache
+ *              offset + index); read as an input (no kernel of this library
+ *              writes it).
+ *   q, k, v    outputs [M, q_size], [M, kv_size], [M, kv_size], contiguous.
+ *   out_bias   NULL or three bias pointers (each NULL or bf16 [size]).
+ *   workspace  at least gwa_qkv_rope_workspace_bytes(M, head_dim) bytes,
+ *              256-byte aligned, for M > 1 (a (cos, sin) table); M = 1 needs
+ *              none when K is a multiple of 512 and the weight 16-byte
+ *              aligned (otherwise as M > 1).  Not read by the caller after.
+ * Every path rotates the fp32 projection before rounding to bf16.  One
+ * token runs in one kernel (the rotation in the epilogue, its (cos, sin)
+ * formed by the kernel); more tokens run a small kernel that fills the table
+ * (angles in fp64, reduced modulo 2 pi) and the staged decode kernels in
+ * passes of up to eight tokens.  Errors as gwa_qmv_fused_sections, plus
+ * GWA_ERR_INVALID_ARG for head_dim, sizes, rope_base or a null positions
+ * pointer, and GWA_ERR_WORKSPACE for a missing or short workspace. */
+int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
+                     int64_t q_size, int64_t kv_size, int32_t head_dim,
+                     double rope_base, const int32_t *positions, uint16_t *q,
+                     uint16_t *k, uint16_t *v,
+                     const uint16_t *const *out_bias, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* Workspace bytes gwa_qmv_qkv_rope needs for M tokens and heads of
+ * head_dim (0 for M < 1). */
+size_t gwa_qkv_rope_workspace_bytes(int64_t M, int32_t head_dim);
+
 /* gwa_quantize_affine -- affine group quantization of bf16 weights into the
  * packed format every projection above reads: the requantize step of
  * "Sanctum-MLX", "The April 2026 cutover" (LoRA merge at load dequantizes,

@@ -148,3 +148,21 @@ def test_quantize_arguments_are_checked(lib):
     assert q(wq=0x1004) == 3
     assert q(sc=0x2001) == 3
     assert q(N=0) == 0   # nothing to do, no device needed
+
+
+@needs_nvcc
+def test_qkv_rope_arguments_are_checked(lib):
+    import group_wise_affine_gb300 as gwa
+    w = _qw(gwa, N=256, K=128)   # q 128 + 2 * kv 64
+    call = lambda **k: lib.gwa_qmv_qkv_rope(
+        0x4000, k.get("M", 1), w, k.get("q", 128), k.get("kv", 64),
+        k.get("d", 64), k.get("base", 10000.0), k.get("pos", 0x9000),
+        0x5000, 0x6000, 0x7000, None, None, 0, None)
+    assert call(d=63) == 1          # odd head_dim
+    assert call(d=512) == 1         # too wide
+    assert call(q=96) == 1          # q + 2 kv != N
+    assert call(kv=48, q=160) == 1  # not a multiple of head_dim
+    assert call(base=0.0) == 1
+    assert call(pos=None) == 1
+    assert call(pos=0x9002) == 3
+    assert call(M=0) == 0           # nothing to do, no device needed
