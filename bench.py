@@ -334,6 +334,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     extras = {}
     if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
         extras["stack_M4"] = run_stack_extra(W, 4, dev, 50, 3)
+        extras["qkv_rope"] = run_rope_extra(W, dev, 20, 3)
         extras["prefill_stack_M512"] = run_stack_extra(W, 512, dev, 5, 2)
         # the same stack with u8 codes (its own 14 GB of weights)
         W8 = stack_weights(8, L, dev)
@@ -499,6 +500,47 @@ def run_moe_extra(dev, steps, warmup, layers=16, E=256, H=2048, I=512,
         res[f"M{M}"] = {"us_per_layer": round(1e3 * ms / layers, 3),
                         "distinct_experts_per_layer": round(distinct / layers, 2),
                         "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
+    return res
+
+
+def run_rope_extra(W, dev, steps, warmup, tokens=(1, 4, 512),
+                   head_dim=128, base=1e6):
+    """The 48 layers' fused QKV projections with the rotary embedding of Q
+    and K (heads of 128, base 1e6, positions 1000 + m), against the same
+    projections without it: per-launch time of each and the difference."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    L = len(W)
+    res = {}
+    for M in tokens:
+        g = torch.Generator(device=dev).manual_seed(4000 + M)
+        x = torch.randn((M, HIDDEN), generator=g, device=dev).to(torch.bfloat16)
+        pos = torch.arange(1000, 1000 + M, dtype=torch.int32, device=dev)
+        mk = lambda n: torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        outs = [[mk(QOUT), mk(KVOUT), mk(KVOUT)] for _ in range(L)]
+        ws = gwa.make_workspace(M, HIDDEN, dev)
+        rws = torch.empty(max(int(gwa.load().gwa_qkv_rope_workspace_bytes(
+            M, HIDDEN, head_dim)), 256), dtype=torch.uint8, device=dev)
+
+        def plain():
+            for l in range(L):
+                gwa.qmv_fused_sections(x, W[l]["qkv"], (QOUT, KVOUT, KVOUT),
+                                       outs=outs[l], workspace=ws)
+
+        def rope():
+            for l in range(L):
+                gwa.qmv_qkv_rope(x, W[l]["qkv"], QOUT, KVOUT, head_dim, base,
+                                 pos, outs=outs[l], workspace=rws)
+        plain()
+        rope()
+        torch.cuda.synchronize()
+        total, per = time_graphs([capture(plain), capture(rope)], steps, warmup)
+        us = [1e3 * t / (steps * L) for t in per]
+        byt = proj_bytes(QOUT + 2 * KVOUT, HIDDEN, W[0]["qkv"].bits, M)
+        res[f"M{M}"] = {"us_per_launch_rope": round(us[1], 3),
+                        "us_per_launch_plain": round(us[0], 3),
+                        "rope_extra_us": round(us[1] - us[0], 3),
+                        "GB/s_rope": round(byt / (us[1] * 1e-6) / 1e9, 1)}
     return res
 
 

@@ -97,7 +97,7 @@ def load(path: str = LIB_PATH):
                                      ctypes.c_double, vp, vp, vp, vp, vp, vp,
                                      sz, vp]
     lib.gwa_qmv_qkv_rope.restype = ctypes.c_int
-    lib.gwa_qkv_rope_workspace_bytes.argtypes = [i64, i32]
+    lib.gwa_qkv_rope_workspace_bytes.argtypes = [i64, i64, i32]
     lib.gwa_qkv_rope_workspace_bytes.restype = sz
     lib.gwa_quantize_affine.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
@@ -339,7 +339,7 @@ def qmv_qkv_rope(x: torch.Tensor, w: QWeight, q_size: int, kv_size: int,
                 _check_out(b, size, f"out_bias[{i}]")
         bptrs = (ctypes.c_void_p * 3)(*[_ptr(b) for b in out_bias])
     if workspace is None and M > 1:
-        n = int(load().gwa_qkv_rope_workspace_bytes(M, head_dim))
+        n = int(load().gwa_qkv_rope_workspace_bytes(M, w.K, head_dim))
         workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
     wp, wn = _ws(workspace)
     _check(load().gwa_qmv_qkv_rope(

@@ -1,6 +1,7 @@
 // C ABI of libgwa.so (declared in include/gwa.h): argument validation,
 // kernel selection and launch.  Nothing here allocates, synchronizes or
 // aborts; every problem becomes a status code plus a thread-local message.
+#include <math.h>
 #include <mutex>
 #include <map>
 #include <stdarg.h>
@@ -380,6 +381,9 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
         return fail(GWA_ERR_INVALID_ARG,
                     "%s: q_size + 2*kv_size = %lld, weight has %lld rows", fn,
                     (long long)(q_size + 2 * kv_size), (long long)w.N);
+    if (w.N >= ((int64_t)1 << 30))
+        return fail(GWA_ERR_INVALID_ARG, "%s: N=%lld (< 2^30)", fn,
+                    (long long)w.N);
     if (!(rope_base > 0.0) || rope_base > 1e30)
         return fail(GWA_ERR_INVALID_ARG, "%s: rope_base=%g", fn, rope_base);
     uint16_t *outs[3] = {q, k, v};
@@ -411,7 +415,7 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
     r.rope_hd = head_dim;
     r.rope_end = q_size + kv_size;
     r.rope_pos = positions;
-    r.rope_base = rope_base;
+    r.rope_r = pow(rope_base, -2.0 / (double)head_dim);
     if (M == 1) {
         // the one-token kernel forms its own (cos, sin) and rotates Q and K
         // in its epilogue
@@ -420,28 +424,49 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
         if (e != cudaSuccess) return cuda_fail(e, fn);
         if (used) return GWA_OK;
     }
-    // otherwise a (cos, sin) table in the workspace, then the staged kernels
-    // rotate in their epilogues, in passes of up to eight tokens
-    const size_t need = gwa_qkv_rope_workspace_bytes(M, head_dim);
+    // otherwise a (cos, sin) table in the workspace (after the tensor-core
+    // path's area), then the kernels rotate in their epilogues
+    const size_t need = gwa_qkv_rope_workspace_bytes(M, w.K, head_dim);
     if (!workspace || workspace_bytes < need)
         return fail(GWA_ERR_WORKSPACE,
-                    "%s: M=%lld head_dim=%d needs %zu bytes of workspace (got "
-                    "%zu)", fn, (long long)M, (int)head_dim, need,
-                    workspace_bytes);
+                    "%s: M=%lld K=%lld head_dim=%d needs %zu bytes of workspace "
+                    "(got %zu)", fn, (long long)M, (long long)w.K, (int)head_dim,
+                    need, workspace_bytes);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
         return fail(GWA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned",
                     fn);
-    float2 *cs = static_cast<float2 *>(workspace);
-    cudaError_t e = launch_rope_table(cs, M, head_dim, rope_base, positions, st);
+    const size_t qmm_area = M > 8 ? (qmm_workspace_bytes(M, w.K) + 255) / 256 * 256 : 0;
+    float2 *cs = reinterpret_cast<float2 *>(static_cast<unsigned char *>(workspace) +
+                                            qmm_area);
+    cudaError_t e = launch_rope_table(cs, M, head_dim, r.rope_r, positions, st);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     r.rope_cs = cs;
+    if (M > 8) {
+        // tensor cores when the shape allows it and each head and section
+        // is whole inside the 128-row tiles
+        QmmArgs a{};
+        a.x = x; a.M = M; a.w = w; a.mode = 3;
+        a.nsec = 3;
+        for (int s = 0; s <= 3; ++s) a.sec_start[s] = p.sec_start[s];
+        for (int s = 0; s < 3; ++s) {
+            a.sec_out[s] = p.sec_out[s];
+            a.sec_bias[s] = p.sec_bias[s];
+        }
+        a.rope_hd = head_dim;
+        a.rope_end = q_size + kv_size;
+        a.rope_cs = cs;
+        if (qmm_eligible(a) && 128 % head_dim == 0 && q_size % 128 == 0 &&
+            kv_size % 128 == 0)
+            return qmm_run(a, workspace, workspace_bytes, st);
+    }
     return run_dense(3, r, M, 0, sizes, st, fn);
 }
 
-size_t gwa_qkv_rope_workspace_bytes(int64_t M, int32_t head_dim) {
-    if (M < 1 || head_dim < 2) return 0;
+size_t gwa_qkv_rope_workspace_bytes(int64_t M, int64_t K, int32_t head_dim) {
+    if (M < 1 || head_dim < 2 || K < 1) return 0;
+    const size_t qmm_area = M > 8 ? (qmm_workspace_bytes(M, K) + 255) / 256 * 256 : 0;
     const size_t b = (size_t)M * (size_t)(head_dim / 2) * 8;
-    return (b + 255) / 256 * 256;
+    return qmm_area + (b + 255) / 256 * 256;
 }
 
 int gwa_qmv_gate_up_silu(const uint16_t *x, int64_t M, gwa_qweight w,

@@ -245,19 +245,25 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
 }
 
 // cos and sin of the rotary angle theta = pos * base^(-2i/d) (textbook
-// RoPE, pair index i of a head of d).  theta is formed and reduced modulo
-// 2 pi in fp64 (2 pi split in two doubles), so the fp32 sincos sees an
-// argument within [-pi, pi] accurate to ~1e-15 even at positions of 10^5
-// and more; an fp32 angle would be off by ~1e-2 rad at position 32K.
-__device__ __forceinline__ float2 rope_cos_sin(int pos, int i, int d,
-                                              double base) {
-    const double theta =
-        (double)pos * pow(base, -2.0 * (double)i / (double)d);
+// RoPE, pair index i of a head of d), given r = base^(-2/d) in fp64:
+// base^(-2i/d) = r^i by repeated squaring (a dozen fp64 products; relative
+// error ~1e-15), and theta is reduced modulo 2 pi in fp64 (2 pi split in two
+// doubles), so the fp32 sincos sees an argument within [-pi, pi] accurate to
+// ~1e-14 even at positions of 10^5 and more.  An fp32 angle would be off by
+// ~1e-2 rad at position 32K; an fp64 pow per angle costs several times more
+// on this GPU, whose fp64 rate is low.
+__device__ __forceinline__ float2 rope_cos_sin(int pos, int i, double r) {
+    double f = 1.0, b = r;
+    for (int e = i; e > 0; e >>= 1) {
+        if (e & 1) f *= b;
+        b *= b;
+    }
+    const double theta = (double)pos * f;
     const double k = rint(theta * 0.15915494309189535);  // 1 / (2 pi)
-    double r = fma(-k, 6.283185307179586, theta);
-    r = fma(-k, 2.4492935982947064e-16, r);
+    double t = fma(-k, 6.283185307179586, theta);
+    t = fma(-k, 2.4492935982947064e-16, t);
     float sn, cs;
-    sincosf((float)r, &sn, &cs);
+    sincosf((float)t, &sn, &cs);
     return make_float2(cs, sn);
 }
 

@@ -43,12 +43,12 @@ struct DenseParams {
     int rope_hd;
     int64_t rope_end;
     const int32_t *rope_pos;  // one-token kernel: forms its own (cos, sin)
-    double rope_base;
+    double rope_r;            // base^(-2/d), in fp64
     const float2 *rope_cs;    // staged kernel: (cos, sin) [M, rope_hd / 2]
 };
 
 // (cos, sin) table of the rotary embedding, cs[m * d/2 + i] (rope.cu).
-cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double base,
+cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double r,
                               const int32_t *positions, cudaStream_t st);
 
 // Launches `kernel` on `st` with programmatic stream serialization: it may

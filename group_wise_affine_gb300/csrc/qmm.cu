@@ -263,12 +263,15 @@ struct QmmParams {
     const uint16_t *bi;
     int64_t N;           // weight rows
     int64_t I;           // gate+up: N / 2
-    int mode;            // 0 plain, 1 sections, 2 gate+up
+    int mode;            // 0 plain, 1 sections, 2 gate+up, 3 sections + RoPE
     uint16_t *y;
     int nsec;
     int64_t sec_start[kMaxSections + 1];
     uint16_t *sec_out[kMaxSections];
     const uint16_t *sec_bias[kMaxSections];
+    int rope_hd;
+    int64_t rope_end;
+    const float2 *rope_cs;
     unsigned int *status;
 };
 
@@ -606,6 +609,62 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     }
                 }
             }
+        } else if (p.mode == 3) {
+            // rotary embedding: a row and its partner (i, i + d/2 of one
+            // head, in this tile as d divides 128) exchange their values
+            // through the (now idle) rings, padded rows of NT + 1 floats
+            float *buf = reinterpret_cast<float *>(smem + L::XOFF);
+            constexpr int GS = NT + 1;
+            static_assert((size_t)kQmmRows * GS * 4 <= L::BYTES,
+                          "the exchange rows must fit in the rings");
+            int sidx = 0;
+            float bias = 0.f;
+            if (n >= 0) {
+                while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1]) ++sidx;
+                if (p.sec_bias[sidx])
+                    bias = bf16_bits_to_f32(
+                        p.sec_bias[sidx][n - p.sec_start[sidx]]);
+            }
+            if (done) {
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                    float d[32];
+                    tc_ld32(tmem_d + lane_off + c0, d);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) buf[r * GS + c0 + j] = d[j] + bias;
+                }
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
+            if (done && n >= 0) {
+                const int half = p.rope_hd / 2;
+                const int rr = r % p.rope_hd;
+                const bool first = rr < half;
+                const int pr = first ? r + half : r - half;
+                const int i = first ? rr : rr - half;
+                const bool rot = n < p.rope_end;
+                const int64_t jj = n - p.sec_start[sidx];
+                const int64_t size = p.sec_start[sidx + 1] - p.sec_start[sidx];
+                for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                    // 16 (cos, sin) loads in flight together
+                    float2 tv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t m = min(m0 + c0 + j, p.M - 1);
+                        tv[j] = rot ? p.rope_cs[m * half + i]
+                                    : make_float2(1.0f, 0.0f);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t m = m0 + c0 + j;
+                        if (m < p.M) {
+                            const float own = buf[r * GS + c0 + j];
+                            const float oth = buf[pr * GS + c0 + j];
+                            const float val = first ? own * tv[j].x - oth * tv[j].y
+                                                    : own * tv[j].x + oth * tv[j].y;
+                            p.sec_out[sidx][m * size + jj] = f32_to_bf16_bits(val);
+                        }
+                    }
+                }
+            }
         } else if (done) {
             int sidx = 0;
             if (p.mode == 1 && n >= 0)
@@ -739,11 +798,15 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     p.mode = a.mode;
     p.y = a.y;
     p.nsec = a.nsec;
-    for (int s = 0; s <= a.nsec && a.mode == 1; ++s) p.sec_start[s] = a.sec_start[s];
-    for (int s = 0; s < a.nsec && a.mode == 1; ++s) {
+    const bool secs = a.mode == 1 || a.mode == 3;
+    for (int s = 0; s <= a.nsec && secs; ++s) p.sec_start[s] = a.sec_start[s];
+    for (int s = 0; s < a.nsec && secs; ++s) {
         p.sec_out[s] = a.sec_out[s];
         p.sec_bias[s] = a.sec_bias[s];
     }
+    p.rope_hd = a.rope_hd;
+    p.rope_end = a.rope_end;
+    p.rope_cs = a.rope_cs;
     p.status = status;
 
     auto kern = qmm_tc_kernel<BITS, NT>;

@@ -14,12 +14,18 @@ struct QmmArgs {
     const uint16_t *x;  // [M, K] bf16
     int64_t M;
     gwa_qweight w;
-    int mode;           // 0 plain, 1 sections, 2 gate+up SwiGLU
+    int mode;           // 0 plain, 1 sections, 2 gate+up SwiGLU,
+                        // 3 sections with the rotary embedding
     uint16_t *y;        // plain: [M, N]; gate+up: [M, N/2]
     int nsec;
     int64_t sec_start[kMaxSections + 1];
     uint16_t *sec_out[kMaxSections];
     const uint16_t *sec_bias[kMaxSections];
+    // mode 3: rows [0, rope_end) rotate in heads of rope_hd (dividing 128,
+    // sections whole 128-row tiles) with (cos, sin) rope_cs[m * hd/2 + i]
+    int rope_hd;
+    int64_t rope_end;
+    const float2 *rope_cs;
 };
 
 size_t qmm_workspace_bytes(int64_t M, int64_t K);

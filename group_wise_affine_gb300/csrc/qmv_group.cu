@@ -31,8 +31,8 @@ enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2, kGRope = 3 };
 // a head (d = p.rope_hd), the pairing the rotation needs, laid out like a
 // gate/up pair; units are cut into stages of whole pairs within one head.
 __device__ __forceinline__ int64_t rope_row(int64_t u, int h, int d) {
-    const int64_t half = d / 2;
-    return (u / half) * d + (u % half) + h * half;
+    const int half = d / 2, uu = (int)u;  // pairs < 2^31 (rows < 2^30)
+    return (int64_t)(uu / half) * d + (uu % half) + h * half;
 }
 
 constexpr int kSlice = 16;  // lanes per reduction slice
@@ -98,19 +98,6 @@ __global__ void __maxnreg__(88)
 
     if (tid >= ncons) {
         // ------------------------------------------------ producer
-        if (MODE == kGRope && tid > ncons) {
-            // the other lanes of the producer warp: the CTA's (cos, sin)
-            // table, before the wait (positions are an input no kernel of
-            // this library writes), off the critical path
-            float2 *cs = reinterpret_cast<float2 *>(smem + rope_off);
-            const int half = p.rope_hd / 2;
-            for (int e = tid - ncons - 1; e < nu * MT; e += kWarp - 1) {
-                const int64_t n = u0 + e / MT;
-                if (rope_row(n, 0, p.rope_hd) < p.rope_end)
-                    cs[e] = rope_cos_sin(p.rope_pos[e % MT], (int)(n % half),
-                                         p.rope_hd, p.rope_base);
-            }
-        }
         if (tid == ncons) {
             const unsigned char *wq =
                 reinterpret_cast<const unsigned char *>(p.wq);
@@ -167,6 +154,19 @@ __global__ void __maxnreg__(88)
         // activations, so their values are exact zeros
         const int gg = active ? g : 0;
         unsigned char *xenc = smem + xenc_off;
+        if constexpr (MODE == kGRope) {
+            // the CTA's (cos, sin) table, while the previous kernel drains
+            // (positions are an input no kernel of this library writes); it
+            // is read in the epilogue, after the block barrier
+            float2 *cs = reinterpret_cast<float2 *>(smem + rope_off);
+            const int half = p.rope_hd / 2;
+            for (int e = tid; e < nu * MT; e += ncons) {
+                const int64_t n = u0 + e / MT;
+                if (rope_row(n, 0, p.rope_hd) < p.rope_end)
+                    cs[e] = rope_cos_sin(p.rope_pos[e % MT], (int)(n % half),
+                                         p.rope_r);
+            }
+        }
         pdl_wait_primary();  // x may be the previous kernel's output
         encode_rows_shared<BITS>(p.x, p.M, MT, p.K, p.G, tid, ncons, xenc);
         // the consumer warps only (the producer is in its copy loop)

@@ -7,8 +7,9 @@
 // rotate the fp32 results before rounding to bf16 (rotating the rounded
 // outputs would leave errors relative to the inputs' magnitude, above the
 // output tolerance where the rotated value is small).  Each entry's angle is
-// formed in fp64 (see rope_cos_sin); the table is formed once per token and
-// frequency, not per head, because fp64 is slow on this GPU.
+// formed in fp64 from r = base^(-2/d) (see rope_cos_sin); the table is
+// formed once per token and frequency, not per head, because fp64 is slow
+// on this GPU.
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,7 +17,7 @@ namespace gwa {
 
 __global__ void __launch_bounds__(256)
     rope_table_kernel(float2 *__restrict__ cs, int64_t entries, int d,
-                      double base, const int32_t *__restrict__ positions) {
+                      double r, const int32_t *__restrict__ positions) {
     if (threadIdx.x == 0) pdl_launch_dependents();
     // positions are an input no kernel of this library writes, so the first
     // entry's (slow, fp64) angle is formed before the wait; the stores wait,
@@ -26,14 +27,14 @@ __global__ void __launch_bounds__(256)
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     float2 v = make_float2(1.0f, 0.0f);
     if (e < entries)
-        v = rope_cos_sin(positions[e / half], (int)(e % half), d, base);
+        v = rope_cos_sin(positions[e / half], (int)(e % half), r);
     pdl_wait_primary();
     if (e < entries) cs[e] = v;
     for (e += step; e < entries; e += step)
-        cs[e] = rope_cos_sin(positions[e / half], (int)(e % half), d, base);
+        cs[e] = rope_cos_sin(positions[e / half], (int)(e % half), r);
 }
 
-cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double base,
+cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double r,
                               const int32_t *positions, cudaStream_t st) {
     const int64_t entries = M * (head_dim / 2);
     if (entries <= 0) return cudaSuccess;
@@ -41,7 +42,7 @@ cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double base,
     const int64_t cap = (int64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     return launch_pdl(reinterpret_cast<const void *>(rope_table_kernel),
-                      (unsigned)grid, 256u, 0, st, cs, entries, head_dim, base,
+                      (unsigned)grid, 256u, 0, st, cs, entries, head_dim, r,
                       positions);
 }
 

@@ -181,15 +181,18 @@ int gwa_qmv_affine_noalloc(const uint16_t *x, int64_t M, gwa_qweight w,
  *              writes it).
  *   q, k, v    outputs [M, q_size], [M, kv_size], [M, kv_size], contiguous.
  *   out_bias   NULL or three bias pointers (each NULL or bf16 [size]).
- *   workspace  at least gwa_qkv_rope_workspace_bytes(M, head_dim) bytes,
- *              256-byte aligned, for M > 1 (a (cos, sin) table); M = 1 needs
- *              none when K is a multiple of 512 and the weight 16-byte
- *              aligned (otherwise as M > 1).  Not read by the caller after.
+ *   workspace  at least gwa_qkv_rope_workspace_bytes(M, K, head_dim)
+ *              bytes, 256-byte aligned, for M > 1 (a (cos, sin) table, and
+ *              for M > 8 the tensor-core path's area); M = 1 needs none when
+ *              K is a multiple of 512 and the weight 16-byte aligned
+ *              (otherwise as M > 1).  Its contents are scratch.
  * Every path rotates the fp32 projection before rounding to bf16.  One
  * token runs in one kernel (the rotation in the epilogue, its (cos, sin)
  * formed by the kernel); more tokens run a small kernel that fills the table
- * (angles in fp64, reduced modulo 2 pi) and the staged decode kernels in
- * passes of up to eight tokens.  Errors as gwa_qmv_fused_sections, plus
+ * (angles in fp64, reduced modulo 2 pi), then the staged decode kernels (up
+ * to eight tokens a pass) or, for M > 8 with head_dim dividing 128 and
+ * q_size, kv_size multiples of 128, the tensor-core kernel, each rotating in
+ * its epilogue.  Errors as gwa_qmv_fused_sections, plus
  * GWA_ERR_INVALID_ARG for head_dim, sizes, rope_base or a null positions
  * pointer, and GWA_ERR_WORKSPACE for a missing or short workspace. */
 int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
@@ -199,9 +202,9 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
                      const uint16_t *const *out_bias, void *workspace,
                      size_t workspace_bytes, void *stream);
 
-/* Workspace bytes gwa_qmv_qkv_rope needs for M tokens and heads of
- * head_dim (0 for M < 1). */
-size_t gwa_qkv_rope_workspace_bytes(int64_t M, int32_t head_dim);
+/* Workspace bytes gwa_qmv_qkv_rope needs for M tokens of K inputs and
+ * heads of head_dim (0 for M < 1). */
+size_t gwa_qkv_rope_workspace_bytes(int64_t M, int64_t K, int32_t head_dim);
 
 /* gwa_quantize_affine -- affine group quantization of bf16 weights into the
  * packed format every projection above reads: the requantize step of

@@ -93,3 +93,12 @@ def test_positions_per_token_are_used():
     # position 0 is the identity: token 0's Q equals the plain projection
     assert torch.equal(got[0][0], plain[0][0])
     assert not torch.equal(got[0][1], plain[0][1])
+
+
+@pytest.mark.parametrize("M,d,bits", [(33, 64, 4), (300, 128, 4), (40, 128, 8),
+                                      (24, 256, 4)])
+def test_prefill_head_widths(M, d, bits):
+    # heads dividing 128 rotate in the tensor-core epilogue (300 tokens:
+    # 256-token tiles); heads of 256 take the staged kernels
+    pos = np.arange(M) * 13 + 7
+    run_case(M, 1024, 256, 512, d, bits, 1e4, pos, seed=M + d)
