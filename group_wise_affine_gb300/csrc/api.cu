@@ -224,9 +224,7 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         }
         bool used = false;
         cudaError_t e = launch_group(mode, q, st, &used);
-        // the streaming kernel has no rotary-embedding mode
-        if (e == cudaSuccess && !used && mode != 3)
-            e = launch_stream(mode, q, st, &used);
+        if (e == cudaSuccess && !used) e = launch_stream(mode, q, st, &used);
         if (e == cudaSuccess && !used) e = launch_dense(mode, q, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }

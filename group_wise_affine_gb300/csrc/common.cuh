@@ -244,6 +244,14 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
     return true;
 }
 
+// Rotary embedding pairs: unit u is the pair of rows (i, i + d/2) of head
+// u / (d/2), i = u mod d/2; row of half h (0 or 1).  The projections lay such
+// a pair out like a gate/up pair (pairs < 2^31: rows < 2^30).
+__device__ __forceinline__ int64_t rope_pair_row(int64_t u, int h, int d) {
+    const int half = d / 2, uu = (int)u;
+    return (int64_t)(uu / half) * d + (uu % half) + h * half;
+}
+
 // cos and sin of the rotary angle theta = pos * base^(-2i/d) (textbook
 // RoPE, pair index i of a head of d), given r = base^(-2/d) in fp64:
 // base^(-2i/d) = r^i by repeated squaring (a dozen fp64 products; relative

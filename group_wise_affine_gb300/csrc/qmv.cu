@@ -22,12 +22,8 @@ namespace gwa {
 
 enum DenseMode { kPlain = 0, kSections = 1, kGateUp = 2, kRope = 3 };
 
-// QKV sections with the rotary embedding: a pair is rows (i, i + d/2) of a
-// head (d = p.rope_hd), laid out like a gate/up pair.
-__device__ __forceinline__ int64_t rope_pair_row(int64_t n, int h, int d) {
-    const int64_t half = d / 2;
-    return (n / half) * d + (n % half) + h * half;
-}
+// kRope: QKV sections with the rotary embedding, pairs of rows (i, i + d/2)
+// of a head (rope_pair_row) laid out like gate/up pairs.
 
 template <int BITS, int MT, int R, int MODE>
 __global__ void __launch_bounds__(kDenseThreads)

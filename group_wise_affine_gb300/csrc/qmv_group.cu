@@ -27,13 +27,9 @@ static __device__ unsigned int g_group_timeouts;
 
 enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2, kGRope = 3 };
 
-// QKV with the rotary embedding: a unit is the pair of rows (i, i + d/2) of
-// a head (d = p.rope_hd), the pairing the rotation needs, laid out like a
-// gate/up pair; units are cut into stages of whole pairs within one head.
-__device__ __forceinline__ int64_t rope_row(int64_t u, int h, int d) {
-    const int half = d / 2, uu = (int)u;  // pairs < 2^31 (rows < 2^30)
-    return (int64_t)(uu / half) * d + (uu % half) + h * half;
-}
+// QKV with the rotary embedding (kGRope): a unit is the pair of rows
+// (i, i + d/2) of a head (rope_pair_row), cut into stages of whole pairs
+// within one head.
 
 constexpr int kSlice = 16;  // lanes per reduction slice
 // Two CTAs per SM (this one and the next kernel's) must fit in registers.
@@ -126,7 +122,7 @@ __global__ void __maxnreg__(88)
                                              (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                    const int64_t r = MODE == kGRope ? rope_row(ua, h, p.rope_hd)
+                    const int64_t r = MODE == kGRope ? rope_pair_row(ua, h, p.rope_hd)
                                                      : ua + (h ? p.I : 0);
                     bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
                              n * rowbytes, &full[s]);
@@ -162,7 +158,7 @@ __global__ void __maxnreg__(88)
             const int half = p.rope_hd / 2;
             for (int e = tid; e < nu * MT; e += ncons) {
                 const int64_t n = u0 + e / MT;
-                if (rope_row(n, 0, p.rope_hd) < p.rope_end)
+                if (rope_pair_row(n, 0, p.rope_hd) < p.rope_end)
                     cs[e] = rope_cos_sin(p.rope_pos[e % MT], (int)(n % half),
                                          p.rope_r);
             }
@@ -262,7 +258,7 @@ __global__ void __maxnreg__(88)
             const int half = p.rope_hd / 2;
             float a = slot_total(red, (lu * 2 + 0) * MT + m, slices);
             float b = slot_total(red, (lu * 2 + 1) * MT + m, slices);
-            const int64_t r0 = rope_row(n, 0, p.rope_hd);
+            const int64_t r0 = rope_pair_row(n, 0, p.rope_hd);
             int s = 0;
             while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
             const int64_t j = r0 - p.sec_start[s];

@@ -28,7 +28,11 @@ namespace gwa {
 
 static __device__ unsigned int g_stream_timeouts;
 
-enum StreamMode { kSPlain = 0, kSSections = 1, kSGateUp = 2 };
+// kSRope: QKV sections with the rotary embedding, pairs of rows
+// (i, i + d/2) of a head (rope_pair_row) laid out like gate/up pairs, in
+// stages of whole pairs within one head; the epilogue rotates with the
+// (cos, sin) table p.rope_cs.
+enum StreamMode { kSPlain = 0, kSSections = 1, kSGateUp = 2, kSRope = 3 };
 
 // A thread's activations for its chunk, encoded for the integer dot (see
 // common.cuh): int16 pairs in dp2a order, the group scale 2^E and the plain
@@ -176,7 +180,7 @@ constexpr int kRowsPerThread = 4;
 template <int BITS, int MT, int MODE, int RPH>
 __global__ void __launch_bounds__(kStreamMaxThreads)
     qmv_stream_kernel(DenseParams p, int stages, int64_t units, int rs) {
-    constexpr int HALVES = MODE == kSGateUp ? 2 : 1;
+    constexpr int HALVES = (MODE == kSGateUp || MODE == kSRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;     // units per thread per stage
     constexpr int V = RPH * MT;           // values reduced per warp per stage
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
@@ -197,8 +201,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
     float *red = reinterpret_cast<float *>(empty + stages);
     __shared__ int s_issued, s_consumed;
 
-    const int64_t u0 = units * blockIdx.x / gridDim.x;
-    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+    // rope: whole stages per CTA (ups divides d/2), so no stage crosses a head
+    const int64_t ualign = MODE == kSRope ? ups : 1;
+    const int64_t u0 = units / ualign * blockIdx.x / gridDim.x * ualign;
+    const int64_t u1 = units / ualign * (blockIdx.x + 1) / gridDim.x * ualign;
     const int nu = (int)(u1 - u0);
     const int nst = (nu + ups - 1) / ups;
 
@@ -245,7 +251,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
                                              (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                    const int64_t r = ua + (h ? p.I : 0);
+                    const int64_t r = MODE == kSRope
+                                          ? rope_pair_row(ua, h, p.rope_hd)
+                                          : ua + (h ? p.I : 0);
                     bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
                              n * rowbytes, &full[s]);
                     bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
@@ -346,6 +354,28 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
             const float uv = red_total(red, (lu * 2 + 1) * MT + m, nwh);
             p.y[(int64_t)m * p.I + n] = f32_to_bf16_bits(
                 gv / (1.0f + __expf(-gv)) * uv);
+        } else if constexpr (MODE == kSRope) {
+            const int half = p.rope_hd / 2;
+            float a = red_total(red, (lu * 2 + 0) * MT + m, nwh);
+            float b = red_total(red, (lu * 2 + 1) * MT + m, nwh);
+            const int64_t r0 = rope_pair_row(n, 0, p.rope_hd);
+            int s = 0;
+            while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
+            const int64_t j = r0 - p.sec_start[s];
+            const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+            if (p.sec_bias[s]) {
+                a += bf16_bits_to_f32(p.sec_bias[s][j]);
+                b += bf16_bits_to_f32(p.sec_bias[s][j + half]);
+            }
+            if (r0 < p.rope_end) {
+                const float2 t = p.rope_cs[(int64_t)m * half + (int)(n % half)];
+                const float a2 = a * t.x - b * t.y;
+                b = b * t.x + a * t.y;
+                a = a2;
+            }
+            uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
+            o[0] = f32_to_bf16_bits(a);
+            o[half] = f32_to_bf16_bits(b);
         } else if constexpr (MODE == kSPlain) {
             p.y[(int64_t)m * p.N + n] =
                 f32_to_bf16_bits(red_total(red, lu * MT + m, nwh));
@@ -365,9 +395,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
 template <int BITS, int MT, int MODE, int RPH>
 static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
                                    bool *used) {
-    constexpr int HALVES = MODE == kSGateUp ? 2 : 1;
+    constexpr int HALVES = (MODE == kSGateUp || MODE == kSRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;
-    const int64_t units = MODE == kSGateUp ? p.I : p.N;
+    const int64_t units =
+        MODE == kSGateUp ? p.I : MODE == kSRope ? p.N / 2 : p.N;
     const size_t rowbytes = (size_t)p.K * BITS / 8;
     const size_t sbrow = (size_t)p.G * 2;
     const int nwh = (p.nch + kWarp - 1) / kWarp;
@@ -376,6 +407,8 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     while (rs < 4 && nwh * rs * 2 <= 12) rs *= 2;
     const int threads = nwh * kWarp * rs + kWarp;
     if (threads > kStreamMaxThreads) return cudaSuccess;  // not used
+    if (MODE == kSRope && ((p.rope_hd / 2) % (rs * UPT)) != 0)
+        return cudaSuccess;  // not used: stages would cross heads
     const size_t stage_bytes = (size_t)HALVES * rs * UPT * (rowbytes + 2 * sbrow);
     int stages = (int)(kStreamRingTarget / stage_bytes);
     if (stages > 8) stages = 8;
@@ -384,8 +417,10 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     // prefetch while this one drains
     int grid = num_sms();
     if ((int64_t)grid > units) grid = (int)units;
-    const size_t red_bytes =
-        (size_t)((units + grid - 1) / grid) * HALVES * MT * 4 * nwh;
+    // units per CTA, at most (rope: plus one stage for the alignment)
+    const int64_t umax =
+        (units + grid - 1) / grid + (MODE == kSRope ? rs * UPT : 0);
+    const size_t red_bytes = (size_t)umax * HALVES * MT * 4 * nwh;
     const size_t smem = stages * stage_bytes + 16 * stages + red_bytes;
     if (smem > kMaxDynSmem) return cudaSuccess;
     auto kern = qmv_stream_kernel<BITS, MT, MODE, RPH>;
@@ -425,6 +460,8 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
         if (mode == kSPlain) return launch_stream_t<B, MTV, kSPlain>(p, st, used); \
         if (mode == kSSections)                                              \
             return launch_stream_t<B, MTV, kSSections>(p, st, used);         \
+        if (mode == kSRope)                                                  \
+            return launch_stream_t<B, MTV, kSRope>(p, st, used);             \
         return launch_stream_t<B, MTV, kSGateUp>(p, st, used);               \
     }
     GWA_STREAM_CASE(4, 1)
