@@ -345,6 +345,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
         torch.cuda.empty_cache()
         extras["moe"] = run_moe_extra(dev, 50, 3)
         extras["quantize"] = run_quantize_extra(dev, 20, 3)
+        extras["formats"] = run_formats_extra(dev, 10, 2)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
                 h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
@@ -541,6 +542,37 @@ def run_rope_extra(W, dev, steps, warmup, tokens=(1, 4, 512),
                         "us_per_launch_plain": round(us[0], 3),
                         "rope_extra_us": round(us[1] - us[0], 3),
                         "GB/s_rope": round(byt / (us[1] * 1e-6) / 1e9, 1)}
+    return res
+
+
+def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
+                      formats=((2, 64), (4, 32), (4, 128))):
+    """The gate+up shape (27648 x 5120, one token, SiLU epilogue) in code
+    widths and group sizes outside the tuned kernels: the general-format
+    decode kernel, eight back-to-back launches over distinct weights so
+    the timed bytes stream from HBM."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    import gwa_synth as synth
+    peak, _ = measured_peak()
+    g = torch.Generator(device=dev).manual_seed(55)
+    x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16)
+    h = torch.empty((1, N // 2), dtype=torch.bfloat16, device=dev)
+    res = {}
+    for bits, group in formats:
+        ws = [gwa.QWeight(*synth.device_qweight(7000 + 10 * bits + group + c, N,
+                                                K, bits, group, device=dev),
+                          N, K, bits, group) for c in range(8)]
+        graph = capture(lambda: [gwa.qmv_gate_up_silu(x, w, h=h) for w in ws])
+        total, _ = time_graphs([graph], steps, warmup)
+        us = 1e3 * total / (steps * len(ws))
+        byt = proj_bytes(N, K, bits, 1) if group == 64 else (
+            N * K * bits // 8 + N * (K // group) * 4 + K * 2)
+        gbs = byt / (us * 1e-6) / 1e9
+        res[f"u{bits}_g{group}"] = {"us_per_launch": round(us, 2),
+                                     "GB/s": round(gbs, 1),
+                                     "frac_of_measured_hbm": round(gbs / peak, 4)}
+        del ws
     return res
 
 

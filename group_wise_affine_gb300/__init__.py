@@ -201,7 +201,7 @@ def _check_weight(w: QWeight, copies: int = 1) -> None:
     """The library cannot see buffer sizes: refuse tensors whose sizes do not
     match (N, K, bits, group), so a wrong shape raises instead of reading
     past the end of a buffer.  `copies` = number of stacked experts."""
-    if w.bits not in (4, 8) or w.group <= 0 or w.K % w.group:
+    if w.bits not in (2, 4, 8) or w.group <= 0 or w.K % w.group:
         return                                   # the C ABI reports these
     words = copies * w.N * w.K * w.bits // 32
     groups = copies * w.N * (w.K // w.group)
@@ -338,7 +338,10 @@ def qmv_qkv_rope(x: torch.Tensor, w: QWeight, q_size: int, kv_size: int,
             if b is not None:
                 _check_out(b, size, f"out_bias[{i}]")
         bptrs = (ctypes.c_void_p * 3)(*[_ptr(b) for b in out_bias])
-    if workspace is None and M > 1:
+    # one token of a u4/u8 group-64 weight needs none (its kernel forms its
+    # own (cos, sin)); every other case takes a table in the workspace
+    tuned = w.bits in (4, 8) and w.group == 64
+    if workspace is None and (M > 1 or not tuned):
         n = int(load().gwa_qkv_rope_workspace_bytes(M, w.K, head_dim))
         workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
     wp, wn = _ws(workspace)

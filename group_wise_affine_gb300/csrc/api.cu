@@ -144,17 +144,24 @@ cudaError_t prefer_max_shared(const void *kernel) {
 }
 
 // ------------------------------------------------------------ validation
+// The tuned kernels take u4/u8 codes in groups of 64; the other widths and
+// group sizes run on the general-format decode kernel.
+static bool tuned_format(int bits, int group) {
+    return (bits == 4 || bits == 8) && group == 64;
+}
+
 static int check_qweight(const gwa_qweight &w, const char *fn) {
-    if (w.bits != 4 && w.bits != 8)
-        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 4, 8)", fn,
-                    (int)w.bits);
-    if (w.group != 64)
-        return fail(GWA_ERR_UNSUPPORTED, "%s: group=%d (supported: 64)", fn,
-                    (int)w.group);
-    if (w.N < 0 || w.K <= 0 || w.K % 64 != 0)
+    if (w.bits != 2 && w.bits != 4 && w.bits != 8)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 2, 4, 8)",
+                    fn, (int)w.bits);
+    if (w.group != 32 && w.group != 64 && w.group != 128)
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: group=%d (supported: 32, 64, 128)", fn, (int)w.group);
+    if (w.N < 0 || w.K <= 0 || w.K % w.group != 0 || w.K % 64 != 0)
         return fail(GWA_ERR_INVALID_ARG,
                     "%s: N=%lld K=%lld (need N >= 0, K a positive multiple "
-                    "of 64)", fn, (long long)w.N, (long long)w.K);
+                    "of 64 and of the group)", fn, (long long)w.N,
+                    (long long)w.K);
     if (w.K > (1 << 20))
         return fail(GWA_ERR_INVALID_ARG, "%s: K=%lld exceeds 2^20", fn,
                     (long long)w.K);
@@ -188,7 +195,8 @@ static DenseParams dense_base(const uint16_t *x, int64_t M,
     p.bi = w.biases;
     p.N = w.N;
     p.nch = (int)(w.K * w.bits / 128);
-    p.G = (int)(w.K / 64);
+    p.group = (int)w.group;
+    p.G = (int)(w.K / w.group);
     return p;
 }
 
@@ -196,13 +204,14 @@ static DenseParams dense_base(const uint16_t *x, int64_t M,
 static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
                      const int64_t *sec_sizes, cudaStream_t st,
                      const char *fn) {
-    int mt = dense_max_tokens(p.bits, p.nch);
+    const bool generic = !tuned_format(p.bits, p.group);
+    int mt = generic ? generic_max_tokens() : dense_max_tokens(p.bits, p.nch);
     if (mt < 1)
         return fail(GWA_ERR_INVALID_ARG, "%s: K=%d too large for staging", fn,
                     p.K);
     // The streaming kernel (up to four tokens a pass) outruns the staged one
     // even when it has to stream the weights twice for 5..8 tokens.
-    {
+    if (!generic) {
         DenseParams probe = p;
         probe.M = 1;
         if (stream_eligible(probe)) mt = mt < 4 ? mt : 4;
@@ -223,6 +232,11 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
             q.y = p.y + t0 * out_stride;
         }
         bool used = false;
+        if (generic) {
+            cudaError_t e = launch_generic(mode, q, st);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+            continue;
+        }
         cudaError_t e = launch_group(mode, q, st, &used);
         if (e == cudaSuccess && !used) e = launch_stream(mode, q, st, &used);
         if (e == cudaSuccess && !used) e = launch_dense(mode, q, st);
@@ -414,7 +428,7 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
     r.rope_end = q_size + kv_size;
     r.rope_pos = positions;
     r.rope_r = pow(rope_base, -2.0 / (double)head_dim);
-    if (M == 1) {
+    if (M == 1 && tuned_format(w.bits, w.group)) {
         // the one-token kernel forms its own (cos, sin) and rotates Q and K
         // in its epilogue
         bool used = false;
@@ -506,6 +520,10 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
     if (rc) return rc;
     if (mode != GWA_MOE_GATE_UP_SILU && mode != GWA_MOE_DOWN_COMBINE)
         return fail(GWA_ERR_INVALID_ARG, "%s: mode=%d", fn, (int)mode);
+    if (!tuned_format(w.bits, w.group))
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: bits=%d group=%d (experts: u4 or u8, group 64)", fn,
+                    (int)w.bits, (int)w.group);
     if (M > 8)
         return fail(GWA_ERR_UNSUPPORTED, "%s: M=%lld (decode path: M <= 8)", fn,
                     (long long)M);
@@ -585,6 +603,10 @@ int gwa_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int32_t bits,
     const gwa_qweight out{wq, scales, biases, N, K, bits, group};
     int rc = check_qweight(out, fn);
     if (rc) return rc;
+    if (!tuned_format(bits, group))
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: bits=%d group=%d (quantization: u4 or u8, group 64)",
+                    fn, (int)bits, (int)group);
     if (N == 0) return GWA_OK;
     if (!w) return fail(GWA_ERR_INVALID_ARG, "%s: null w", fn);
     if (!aligned(w, 16))
@@ -605,7 +627,7 @@ int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream) {
     if (!aligned(wf, 4)) return fail(GWA_ERR_MISALIGNED, "%s: alignment", fn);
     if ((rc = check_device())) return rc;
     cudaError_t e = launch_debug_dequant(w.wq, w.scales, w.biases, w.N, w.K,
-                                         w.bits, wf,
+                                         w.bits, (int)w.group, wf,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
 }

@@ -25,7 +25,7 @@ __global__ void debug_dequant_kernel(const uint32_t *__restrict__ wq,
                                      const uint16_t *__restrict__ sc,
                                      const uint16_t *__restrict__ bi,
                                      int64_t words, int64_t words_per_row,
-                                     int64_t G, int bits,
+                                     int64_t G, int group, int bits,
                                      float *__restrict__ wf) {
     const int per = 32 / bits;
     const uint32_t mask = (1u << bits) - 1u;
@@ -35,8 +35,8 @@ __global__ void debug_dequant_kernel(const uint32_t *__restrict__ wq,
         const uint32_t w = wq[i];
         for (int j = 0; j < per; ++j) {
             const int64_t k = wi * per + j;
-            const float s = bf16_bits_to_f32(sc[n * G + k / kGroup]);
-            const float b = bf16_bits_to_f32(bi[n * G + k / kGroup]);
+            const float s = bf16_bits_to_f32(sc[n * G + k / group]);
+            const float b = bf16_bits_to_f32(bi[n * G + k / group]);
             wf[i * per + j] = fmaf(s, (float)((w >> (bits * j)) & mask), b);
         }
     }
@@ -59,10 +59,11 @@ cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
 
 cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
                                  const uint16_t *bi, int64_t N, int64_t K,
-                                 int bits, float *wf, cudaStream_t st) {
+                                 int bits, int group, float *wf,
+                                 cudaStream_t st) {
     const int64_t words = N * K * bits / 32;
     debug_dequant_kernel<<<grid_for(words, 256), 256, 0, st>>>(
-        wq, sc, bi, words, K * bits / 32, K / kGroup, bits, wf);
+        wq, sc, bi, words, K * bits / 32, K / group, group, bits, wf);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ struct DenseParams {
     int64_t N;           // weight rows
     int nch;             // 16-byte chunks per row
     int G;               // groups per row
+    int group;           // inputs per group (the tuned kernels: 64)
     int64_t nblocks;     // warp blocks (set by the launcher)
     uint16_t *y;         // plain: [M, N]; gate+up: [M, I]
     int64_t I;           // gate+up: N / 2
@@ -46,6 +47,12 @@ struct DenseParams {
     double rope_r;            // base^(-2/d), in fp64
     const float2 *rope_cs;    // staged kernel: (cos, sin) [M, rope_hd / 2]
 };
+
+// General-format decode kernel (qmv_generic.cu): u2/u4/u8 codes, groups of
+// 32/64/128, up to generic_max_tokens() tokens per launch, modes as the
+// other decode kernels (0 plain, 1 sections, 2 gate+up, 3 rotary sections).
+cudaError_t launch_generic(int mode, const DenseParams &p, cudaStream_t st);
+int generic_max_tokens();
 
 // (cos, sin) table of the rotary embedding, cs[m * d/2 + i] (rope.cu).
 cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double r,
@@ -152,6 +159,7 @@ cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
                                 int bits, uint8_t *codes, cudaStream_t st);
 cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
                                  const uint16_t *bi, int64_t N, int64_t K,
-                                 int bits, float *wf, cudaStream_t st);
+                                 int bits, int group, float *wf,
+                                 cudaStream_t st);
 
 }  // namespace gwa

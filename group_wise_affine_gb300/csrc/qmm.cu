@@ -831,7 +831,8 @@ bool qmm_eligible(const QmmArgs &a) {
     };
     // the scale tiles need rows of whole 16-byte units (K/64 a multiple of
     // 8); TMA wants 16-byte aligned bases
-    return (a.w.K / 64) % 8 == 0 && a16(a.w.wq) && a16(a.w.scales) &&
+    return a.w.group == 64 && (a.w.K / 64) % 8 == 0 && a16(a.w.wq) &&
+           a16(a.w.scales) &&
            a16(a.w.biases) && a.M <= 0x7fffffffLL && a.w.N <= 0x7fffffffLL &&
            (a.w.bits == 4 || a.w.bits == 8);
 }

@@ -50,16 +50,26 @@ extern "C" {
 enum {
     GWA_OK = 0,
     GWA_ERR_INVALID_ARG = 1, /* null pointer, bad size, sizes not adding up */
-    GWA_ERR_UNSUPPORTED = 2, /* bits not in {4,8}, group != 64             */
+    GWA_ERR_UNSUPPORTED = 2, /* bits not in {2,4,8}, group not in
+                                {32,64,128}; or a format an entry point does
+                                not take (experts, quantization: u4/u8 at
+                                group 64)                                  */
     GWA_ERR_MISALIGNED = 3,  /* a pointer breaks the alignment rules       */
     GWA_ERR_CUDA = 4,        /* launch failed or no usable sm_103a device   */
     GWA_ERR_WORKSPACE = 5    /* M > 8 and the workspace is null or small    */
 };
 
-/* One packed weight of N output rows and K inputs.
- *   wq:     uint32 [N, K*bits/32]
+/* One packed weight of N output rows and K inputs (K a multiple of 64 and
+ * of the group).
+ *   wq:     uint32 [N, K*bits/32]: 32/bits codes per word along the input
+ *           axis, lowest bits first
  *   scales: bf16   [N, K/group]
- *   biases: bf16   [N, K/group]                                          */
+ *   biases: bf16   [N, K/group]
+ * bits 4 or 8 with group 64 run the tuned kernels; bits 2, 4, 8 with groups
+ * of 32 or 128 (and u2 at 64) run a general decode kernel for the dense
+ * projections (all of gwa_qmv_affine, gwa_qmv_fused_sections,
+ * gwa_qmv_gate_up_silu, gwa_qmv_qkv_rope, the debug exports); the experts
+ * and the quantization take u4/u8 at group 64 only.                      */
 typedef struct gwa_qweight {
     const uint32_t *wq;
     const uint16_t *scales;

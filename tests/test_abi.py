@@ -52,7 +52,8 @@ def _qw(gwa, bits=4, group=64, N=16, K=128, wq=0x1000, sc=0x2000, bi=0x3000):
 
 @needs_nvcc
 @pytest.mark.parametrize("kw,code", [
-    (dict(bits=3), 2), (dict(bits=2), 2), (dict(group=32), 2),
+    (dict(bits=3), 2), (dict(bits=6), 2), (dict(group=48), 2),
+    (dict(group=256), 2),
     (dict(K=100), 1), (dict(K=0), 1), (dict(N=-1), 1),
     (dict(wq=0x1004), 3), (dict(sc=0x2001), 3),
 ])
@@ -166,3 +167,19 @@ def test_qkv_rope_arguments_are_checked(lib):
     assert call(pos=None) == 1
     assert call(pos=0x9002) == 3
     assert call(M=0) == 0           # nothing to do, no device needed
+
+
+@needs_nvcc
+def test_formats_outside_the_tuned_kernels_are_refused_where_unsupported(lib):
+    import group_wise_affine_gb300 as gwa
+    # experts and quantization: u4/u8 at group 64 only
+    w2 = _qw(gwa, bits=2, N=8)
+    assert lib.gwa_moe_qmv_gather(0x4000, 1, 2, 0x9000, None, w2, 4, 0,
+                                  0xB000, None, None) == 2
+    assert lib.gwa_quantize_affine(0x4000, 8, 128, 4, 32, 0x1000, 0x2000,
+                                   0x3000, None) == 2
+    # u2 and groups of 32 / 128 are accepted by the projections (empty call)
+    for bits, group in ((2, 64), (4, 32), (8, 128)):
+        assert lib.gwa_qmv_affine(0x4000, 0, _qw(gwa, bits=bits, group=group),
+                                  0x5000, None, 0, None) == 0
+

@@ -1,0 +1,94 @@
+"""GPU parity of the code widths and group sizes outside the tuned kernels
+(u2, and groups of 32 and 128 at every width), which run on the
+general-format decode kernel, against the oracle (same packed format:
+32/b codes per word, lowest bits first, one bf16 scale and bias per group;
+"saragossa", "Quantization formats").
+
+Bars as for the tuned formats: unpacked codes and dequantized values bit
+for bit; outputs within |err| <= 1e-2 * max(1, |ref|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import group_wise_affine_gb300 as gwa
+import gwa_synth as synth
+import oracle
+from helpers import dev_bf16, dev_qweight
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+FORMATS = [(2, 32), (2, 64), (2, 128), (4, 32), (4, 128), (8, 32), (8, 128)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gwa.build()
+    gwa.load()
+    assert torch.cuda.is_available()
+
+
+def close(got, ref, what=""):
+    ok, max_err, worst = oracle.within_tolerance(
+        got.float().cpu().numpy().astype(np.float64), ref, TOL)
+    assert ok, f"{what}: max |err| {max_err:.3g}, worst {worst:.3g}"
+
+
+@pytest.mark.parametrize("bits,group", FORMATS)
+def test_unpack_and_dequant_bit_exact(bits, group):
+    N, K = 37, 512
+    w = synth.qweight(3 + bits + group, N, K, bits, group)
+    dw = dev_qweight(w)
+    codes = gwa.debug_unpack(dw).cpu().numpy()
+    assert np.array_equal(codes, oracle.unpack(w.wq, N, K, bits))
+    wf = gwa.debug_dequant(dw).cpu().numpy().astype(np.float64)
+    ref = oracle.dequant(w.wq, w.scales, w.biases, N, K, bits, group)
+    assert np.array_equal(wf, ref.astype(np.float32).astype(np.float64))
+
+
+@pytest.mark.parametrize("bits,group", FORMATS)
+@pytest.mark.parametrize("M", [1, 3, 8, 11])
+def test_plain_projection(bits, group, M):
+    N, K = 300, 1024
+    w = synth.qweight(100 + bits + group, N, K, bits, group)
+    x = synth.activations(200 + M, M, K)
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
+    torch.cuda.synchronize()
+    close(y, oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits, group),
+          f"u{bits} g{group} M={M}")
+
+
+@pytest.mark.parametrize("bits,group", [(2, 32), (4, 128), (8, 32)])
+def test_sections_gate_up_and_rope(bits, group):
+    K, M = 512, 2
+    rng = np.random.default_rng(bits + group)
+    # sections with bias
+    sizes = [256, 64, 64]
+    w = synth.qweight(300 + group, sum(sizes), K, bits, group)
+    x = synth.activations(301, M, K)
+    bias = [synth.bf16_bits(rng.normal(0, 0.5, size=s).astype(np.float32))
+            for s in sizes]
+    dw = dev_qweight(w)
+    outs = gwa.qmv_fused_sections(dev_bf16(x), dw, sizes,
+                                  out_bias=[dev_bf16(b) for b in bias])
+    refs = oracle.fused_sections(x, w.wq, w.scales, w.biases, sizes, K, bits,
+                                 group=group, out_bias=bias)
+    for o, r in zip(outs, refs):
+        close(o, r, "sections")
+    # gate+up SwiGLU
+    g = synth.qweight(302 + group, 2 * 160, K, bits, group)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(g))
+    close(h, oracle.gate_up_silu(x, g.wq, g.scales, g.biases, 2 * 160, K, bits,
+                                 group=group), "gate+up")
+    # QKV with the rotary embedding (heads of 64), one token and three
+    for m in (1, 3):
+        xm = synth.activations(303 + m, m, K)
+        pos = np.arange(m, dtype=np.int32) + 40
+        got = gwa.qmv_qkv_rope(dev_bf16(xm), dw, 256, 64, 64, 1e4,
+                               torch.from_numpy(pos).cuda())
+        ref = oracle.qkv_rope(xm, w.wq, w.scales, w.biases, 256, 64, K, bits,
+                              64, 1e4, pos, group=group)
+        for o, r in zip(got, ref):
+            close(o, r, f"rope M={m}")
+    torch.cuda.synchronize()

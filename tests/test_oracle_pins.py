@@ -128,12 +128,13 @@ def test_dequant_closed_form_and_identity_case():
 
 
 # ---------------------------------------------------------------- qmv
-@pytest.mark.parametrize("bits", [4, 8])
-def test_qmv_matches_exact_rational_bruteforce(bits):
-    M, N, K = 2, 5, 192            # three groups; N != K catches transposes
-    w = synth.qweight(21 + bits, N, K, bits)
+@pytest.mark.parametrize("bits,group", [(4, 64), (8, 64), (2, 64), (4, 32),
+                                        (4, 128), (2, 32), (8, 128)])
+def test_qmv_matches_exact_rational_bruteforce(bits, group):
+    M, N, K = 2, 5, 384            # several groups; N != K catches transposes
+    w = synth.qweight(21 + bits + group, N, K, bits, group)
     x = synth.activations(31 + bits, M, K)
-    got = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+    got = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits, group)
     want = exact_qmv(x, w)
     for m in range(M):
         for n in range(N):
