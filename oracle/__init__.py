@@ -88,10 +88,14 @@ def _load():
                                             _u32p, _u16p, _u16p]
         lib.orc_rope.argtypes = [_f64p, _i64, _i64, _i64, ctypes.c_double,
                                  _i32p]
+        lib.orc_sdpa_dequant_v.argtypes = [_u16p, _i64, _i64, _i64, _i64, _u16p,
+                                           _i64, _i64, _u32p, _u16p, _u16p,
+                                           _int, _int, ctypes.c_double, _int,
+                                           _f64p]
         for name in ("orc_unpack", "orc_dequant", "orc_qmv",
                      "orc_gate_up_silu", "orc_moe_gate_up_silu",
                      "orc_moe_down_combine", "orc_quantize_affine",
-                     "orc_rope"):
+                     "orc_rope", "orc_sdpa_dequant_v"):
             getattr(lib, name).restype = _int
         _lib = lib
         return lib
@@ -262,6 +266,22 @@ def qkv_rope(x, wq, scales, biases, q_size: int, kv_size: int, K: int,
                              K, bits, group=group, out_bias=out_bias)
     return [rope(q, head_dim, base, positions), rope(k, head_dim, base, positions),
             v]
+
+
+def sdpa_dequant_v(q, k, vq, vs, vb, B: int, Hq: int, Lq: int, D: int,
+                   Hkv: int, T: int, bits: int = 4, group: int = 64,
+                   scale: float = None, causal: bool = True) -> np.ndarray:
+    """Softmax attention of q [B, Hq, Lq, D] over bf16 keys k [B, Hkv, T, D]
+    and affine-quantized values (codes vq [B, Hkv, T, D*bits/32], bf16 scales
+    and biases vs, vb [B, Hkv, T, D/group]); fp64 out [B, Hq, Lq, D]."""
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.empty((B, Hq, Lq, D), dtype=np.float64)
+    _check(_load().orc_sdpa_dequant_v(
+        _c(q, np.uint16), B, Hq, Lq, D, _c(k, np.uint16), Hkv, T,
+        _c(vq, np.uint32), _c(vs, np.uint16), _c(vb, np.uint16), bits, group,
+        float(scale), int(bool(causal)), out), "sdpa_dequant_v")
+    return out
 
 
 def within_tolerance(got, ref, rel: float = 1e-2):

@@ -45,6 +45,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -379,6 +380,77 @@ int orc_rope(double *y, int64_t M, int64_t width, int64_t head_dim,
             }
         }
     }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Attention with a 4-bit value cache ("Sanctum-MLX", the six-changes table,
+ * row 5 "Fused attention with inline V dequant (sdpa_dequant_v)", and the
+ * paragraph after it: Q, a materialized bf16 K and the compressed V state
+ * (indices, scales, zeros) in; SDPA with V dequantized inline, causal mask,
+ * GQA without copies; "File map": turboquant/ holds the 4-bit value cache).
+ * The pages do not print the value format; the reading here is this
+ * library's affine format along the head dimension: codes of `bits` bits
+ * packed 32/bits per word, one bf16 scale and bias ("zero") per `group`
+ * values, v = scale * q + bias.  Plain softmax attention in fp64:
+ *
+ *   score[t] = scale * sum_d q[d] k[t][d]
+ *   p[t]     = exp(score[t] - max) / sum_t' exp(score[t'] - max)
+ *   out[d]   = sum_t p[t] v[t][d]
+ *
+ * over the keys a query may see: all T, or with the causal mask t <= T - Lq
+ * + l for query l of Lq (the queries are the last Lq positions).  Layouts:
+ * q [B, Hq, Lq, D], k [B, Hkv, T, D] (bf16), v codes [B, Hkv, T, D*bits/32],
+ * v scales / biases [B, Hkv, T, D/group], out [B, Hq, Lq, D] (fp64); query
+ * head h reads KV head h / (Hq / Hkv).
+ */
+int orc_sdpa_dequant_v(const uint16_t *q, int64_t B, int64_t Hq, int64_t Lq,
+                       int64_t D, const uint16_t *k, int64_t Hkv, int64_t T,
+                       const uint32_t *vq, const uint16_t *vs,
+                       const uint16_t *vb, int bits, int group, double scale,
+                       int causal, double *out) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq < 0 || D <= 0 ||
+        T < 0 || !bits_ok(bits) || group <= 0 || D % group != 0 ||
+        D % (32 / bits) != 0 || (causal && Lq > T))
+        return ORC_BAD_ARG;
+    const int64_t rep = Hq / Hkv, wpr = D * bits / 32, gpr = D / group;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (!p) return ORC_BAD_ARG;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < Hq; ++h) {
+            const int64_t hk = h / rep;
+            const int64_t kv = (b * Hkv + hk) * T;  /* first key row */
+            for (int64_t l = 0; l < Lq; ++l) {
+                const uint16_t *qv = q + ((b * Hq + h) * Lq + l) * D;
+                double *o = out + ((b * Hq + h) * Lq + l) * D;
+                const int64_t tn = causal ? T - Lq + l + 1 : T;
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < tn; ++t) {
+                    double sdot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        sdot += orc_bf16_to_f64(qv[d]) *
+                                orc_bf16_to_f64(k[(kv + t) * D + d]);
+                    p[t] = scale * sdot;
+                    if (p[t] > mx) mx = p[t];
+                }
+                double sum = 0.0;
+                for (int64_t t = 0; t < tn; ++t) {
+                    p[t] = exp(p[t] - mx);
+                    sum += p[t];
+                }
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t t = 0; t < tn; ++t) {
+                    const int64_t row = kv + t;
+                    for (int64_t d = 0; d < D; ++d) {
+                        const double sv = orc_bf16_to_f64(vs[row * gpr + d / group]);
+                        const double bv = orc_bf16_to_f64(vb[row * gpr + d / group]);
+                        const double c = (double)code_at(vq, wpr, row, d, bits);
+                        o[d] += p[t] / sum * (sv * c + bv);
+                    }
+                }
+            }
+        }
+    free(p);
     return ORC_OK;
 }
 
