@@ -346,6 +346,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
         extras["moe"] = run_moe_extra(dev, 50, 3)
         extras["quantize"] = run_quantize_extra(dev, 20, 3)
         extras["formats"] = run_formats_extra(dev, 10, 2)
+        extras["attention"] = run_attention_extra(dev, 20, 3)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
                 h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
@@ -573,6 +574,46 @@ def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
                                      "GB/s": round(gbs, 1),
                                      "frac_of_measured_hbm": round(gbs / peak, 4)}
         del ws
+    return res
+
+
+def run_attention_extra(dev, steps, warmup, lengths=(4096, 32768), Hq=40,
+                        Hkv=8, D=128, bits=4):
+    """Decode attention over a u4 value cache (one query per head, 40 query
+    heads over 8 KV heads of 128): bytes = bf16 K + packed V + scales and
+    biases + q + out; distinct caches per launch (more bytes than L2 across
+    one pass) so they stream from HBM."""
+    import torch
+    import group_wise_affine_gb300 as gwa
+    peak, _ = measured_peak()
+    res = {}
+    for T in lengths:
+        ncache = max(2, int(512e6 // (Hkv * T * (2 * D + D * bits // 8 + 4))))
+        ncache = min(ncache, 16)
+        g = torch.Generator(device=dev).manual_seed(9000 + T)
+        q = torch.randn((1, Hq, 1, D), generator=g, device=dev).to(torch.bfloat16)
+        caches = []
+        for c in range(ncache):
+            k = torch.randn((1, Hkv, T, D), generator=g, device=dev).to(torch.bfloat16)
+            vq = torch.randint(-2**31, 2**31 - 1, (1, Hkv, T, D * bits // 32),
+                               generator=g, device=dev, dtype=torch.int32)
+            vs = (torch.rand((1, Hkv, T, D // 64), generator=g, device=dev) * 0.04
+                  + 0.01).to(torch.bfloat16)
+            vb = (-vs.float() * 7.5).to(torch.bfloat16)
+            caches.append((k, vq, vs, vb))
+        out = torch.empty((1, Hq, 1, D), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(int(gwa.load().gwa_sdpa_workspace_bytes(1, Hq, Hkv, 1, T, D)),
+                         dtype=torch.uint8, device=dev)
+        graph = capture(lambda: [gwa.sdpa_dequant_v(q, *c, bits=bits, out=out,
+                                                    workspace=ws) for c in caches])
+        total, _ = time_graphs([graph], steps, warmup)
+        us = 1e3 * total / (steps * ncache)
+        byt = Hkv * T * (2 * D + D * bits // 8 + 4) + 2 * 2 * Hq * D
+        gbs = byt / (us * 1e-6) / 1e9
+        res[f"T{T}"] = {"us_per_call": round(us, 2), "GB/s": round(gbs, 1),
+                        "frac_of_measured_hbm": round(gbs / peak, 4),
+                        "bytes_per_call": byt}
+        del caches
     return res
 
 

@@ -8,8 +8,8 @@ arithmetic runs in the library's sm_103a kernels.  There is no fallback: if
 
 Names mirror the C entry points without the ``gwa_`` prefix:
 ``qmv_affine``, ``qmv_fused_sections``, ``qmv_gate_up_silu``,
-``qmv_qkv_rope``, ``moe_qmv_gather``, ``quantize_affine``, ``workspace_bytes``,
-``last_error``,
+``qmv_qkv_rope``, ``moe_qmv_gather``, ``quantize_affine``, ``sdpa_dequant_v``,
+``workspace_bytes``, ``last_error``,
 ``debug_unpack``, ``debug_dequant``.
 
 Weights: ``wq`` int32 [N, K*bits/32] (the packed uint32 words), ``scales`` and
@@ -41,7 +41,8 @@ EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
            "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant",
            "gwa_qmv_affine_noalloc", "gwa_quantize_affine", "gwa_qmv_qkv_rope",
-           "gwa_qkv_rope_workspace_bytes")
+           "gwa_qkv_rope_workspace_bytes", "gwa_sdpa_dequant_v",
+           "gwa_sdpa_workspace_bytes")
 
 
 class GwaError(RuntimeError):
@@ -99,6 +100,12 @@ def load(path: str = LIB_PATH):
     lib.gwa_qmv_qkv_rope.restype = ctypes.c_int
     lib.gwa_qkv_rope_workspace_bytes.argtypes = [i64, i64, i32]
     lib.gwa_qkv_rope_workspace_bytes.restype = sz
+    lib.gwa_sdpa_dequant_v.argtypes = [vp, i64, i32, i32, i32, vp, i32, i64, vp,
+                                       vp, vp, i32, i32, ctypes.c_float, i32,
+                                       vp, vp, sz, vp]
+    lib.gwa_sdpa_dequant_v.restype = ctypes.c_int
+    lib.gwa_sdpa_workspace_bytes.argtypes = [i64, i32, i32, i32, i64, i32]
+    lib.gwa_sdpa_workspace_bytes.restype = sz
     lib.gwa_quantize_affine.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
     lib.gwa_debug_dequant.argtypes = [_QW, vp, vp]
@@ -434,6 +441,47 @@ def quantize_affine(w: torch.Tensor, bits: int = 4, group: int = 64,
     _check(load().gwa_quantize_affine(_ptr(w), N, K, bits, group,
                                       _ptr(out.wq), _ptr(out.scales),
                                       _ptr(out.biases), _stream(stream)))
+    return out
+
+
+def sdpa_dequant_v(q: torch.Tensor, k: torch.Tensor, vq: torch.Tensor,
+                   vs: torch.Tensor, vb: torch.Tensor, bits: int = 4,
+                   group: int = 64, scale: Optional[float] = None,
+                   causal: bool = True, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """gwa_sdpa_dequant_v: softmax attention of q [B, Hq, Lq, D] over bf16
+    keys k [B, Hkv, T, D] and quantized values (vq int32 [B, Hkv, T,
+    D*bits/32], vs / vb bfloat16 [B, Hkv, T, D/64]); returns bf16
+    [B, Hq, Lq, D]."""
+    q, k = _bf16(q, "q"), _bf16(k, "k")
+    _bf16(vs, "vs")
+    _bf16(vb, "vb")
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, T, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("k must be [B, Hkv, T, D] with q's B and D")
+    if vq.dtype != torch.int32 or tuple(vq.shape) != (B, Hkv, T, D * bits // 32):
+        raise ValueError("vq must be int32 [B, Hkv, T, D*bits/32]")
+    for name, t in (("vs", vs), ("vb", vb)):
+        if tuple(t.shape) != (B, Hkv, T, D // group):
+            raise ValueError(f"{name} must be [B, Hkv, T, D/group]")
+    for name, t in (("q", q), ("k", k), ("vq", vq), ("vs", vs), ("vb", vb)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((B, Hq, Lq, D), dtype=torch.bfloat16, device=q.device)
+    _check_out(out, B * Hq * Lq * D, "out")
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    if workspace is None:
+        n = int(load().gwa_sdpa_workspace_bytes(B, Hq, Hkv, Lq, T, D))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    wp, wn = _ws(workspace)
+    _check(load().gwa_sdpa_dequant_v(
+        _ptr(q), B, Hq, Lq, D, _ptr(k), Hkv, T, _ptr(vq), _ptr(vs), _ptr(vb),
+        bits, group, float(scale), int(bool(causal)), _ptr(out), wp, wn,
+        _stream(stream)))
     return out
 
 

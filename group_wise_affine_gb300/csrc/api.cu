@@ -617,6 +617,69 @@ int gwa_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int32_t bits,
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
 }
 
+static int check_attention(int64_t B, int32_t Hq, int32_t Lq, int32_t D,
+                           int32_t Hkv, int64_t T, int32_t bits, int32_t group,
+                           int32_t causal, const char *fn) {
+    if (D != 64 && D != 128 && D != 256)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: D=%d (64, 128 or 256)", fn, (int)D);
+    if ((bits != 4 && bits != 8) || group != 64)
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: bits=%d group=%d (values: u4 or u8, group 64)", fn,
+                    (int)bits, (int)group);
+    if (B < 0 || B > 65535 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Lq < 0 ||
+        T < 1 || T > 0x7fffffffLL || (int64_t)Hkv * ((Hq / Hkv * (int64_t)Lq + 7) / 8) > 65535)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: B=%lld Hq=%d Hkv=%d Lq=%d T=%lld", fn, (long long)B,
+                    (int)Hq, (int)Hkv, (int)Lq, (long long)T);
+    if (causal && Lq > T)
+        return fail(GWA_ERR_INVALID_ARG,
+                    "%s: causal with Lq=%d > T=%lld (every query must see a key)",
+                    fn, (int)Lq, (long long)T);
+    return GWA_OK;
+}
+
+int gwa_sdpa_dequant_v(const uint16_t *q, int64_t B, int32_t Hq, int32_t Lq,
+                       int32_t D, const uint16_t *k, int32_t Hkv, int64_t T,
+                       const uint32_t *vq, const uint16_t *vs,
+                       const uint16_t *vb, int32_t bits, int32_t group,
+                       float scale, int32_t causal, uint16_t *out,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "gwa_sdpa_dequant_v";
+    g_last_error.clear();
+    int rc = check_attention(B, Hq, Lq, D, Hkv, T, bits, group, causal, fn);
+    if (rc) return rc;
+    if (B == 0 || Lq == 0) return GWA_OK;
+    if (!q || !k || !vq || !vs || !vb || !out)
+        return fail(GWA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(vq, 8) || !aligned(vs, 2) ||
+        !aligned(vb, 2) || !aligned(out, 2))
+        return fail(GWA_ERR_MISALIGNED, "%s: alignment (q, k 4 bytes; codes 8)",
+                    fn);
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return fail(GWA_ERR_INVALID_ARG, "%s: scale", fn);
+    const size_t need = gwa_sdpa_workspace_bytes(B, Hq, Hkv, Lq, T, D);
+    if (!workspace || workspace_bytes < need)
+        return fail(GWA_ERR_WORKSPACE, "%s: needs %zu bytes of workspace (got %zu)",
+                    fn, need, workspace_bytes);
+    if (!aligned(workspace, 16))
+        return fail(GWA_ERR_MISALIGNED, "%s: workspace alignment", fn);
+    if ((rc = check_device())) return rc;
+    cudaError_t e = launch_attention(q, k, vq, vs, vb, out,
+                                     static_cast<float *>(workspace), (int)B,
+                                     Hq, Hkv, Lq, (int)T, D, bits, scale,
+                                     causal ? 1 : 0,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
+}
+
+size_t gwa_sdpa_workspace_bytes(int64_t B, int32_t Hq, int32_t Hkv, int32_t Lq,
+                                int64_t T, int32_t D) {
+    if (B < 1 || Hkv < 1 || Hq < Hkv || Lq < 1 || T < 1 || D < 1 ||
+        T > 0x7fffffffLL)
+        return 0;
+    return attention_workspace_bytes((int)B, Hq, Hkv, Lq, (int)T, D);
+}
+
 int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream) {
     const char *fn = "gwa_debug_dequant";
     g_last_error.clear();

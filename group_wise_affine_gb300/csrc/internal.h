@@ -54,6 +54,16 @@ struct DenseParams {
 cudaError_t launch_generic(int mode, const DenseParams &p, cudaStream_t st);
 int generic_max_tokens();
 
+// Attention over an affine-quantized value cache (attention.cu): partial
+// softmax per key split into `part`, then the combine.
+cudaError_t launch_attention(const uint16_t *q, const uint16_t *k,
+                             const uint32_t *vq, const uint16_t *vs,
+                             const uint16_t *vb, uint16_t *out, float *part,
+                             int B, int Hq, int Hkv, int Lq, int T, int D,
+                             int bits, float scale, int causal,
+                             cudaStream_t st);
+size_t attention_workspace_bytes(int B, int Hq, int Hkv, int Lq, int T, int D);
+
 // (cos, sin) table of the rotary embedding, cs[m * d/2 + i] (rope.cu).
 cudaError_t launch_rope_table(float2 *cs, int64_t M, int head_dim, double r,
                               const int32_t *positions, cudaStream_t st);

@@ -216,6 +216,39 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
  * heads of head_dim (0 for M < 1). */
 size_t gwa_qkv_rope_workspace_bytes(int64_t M, int64_t K, int32_t head_dim);
 
+/* gwa_sdpa_dequant_v -- softmax attention over a quantized value cache,
+ * the values dequantized inline ("Sanctum-MLX", six-changes table row 5,
+ * "Fused attention with inline V dequant (sdpa_dequant_v)", and the
+ * paragraph after it: Q, a materialized bf16 K and the compressed V state
+ * in; fp32 online softmax; causal mask; GQA without copying K or V).  The
+ * pages do not print the value format; this library's reading is its own
+ * affine format along the head dimension: codes packed 32/bits per word,
+ * lowest bits first, one bf16 scale and bias ("zero") per 64 dimensions,
+ * v = scale * code + bias.
+ *   out[b,h,l,:] = sum_t p_t v[b,h',t,:],  p = softmax_t(scale * q[b,h,l,:] .
+ *   k[b,h',t,:]) over t < T (causal: t <= T - Lq + l, the queries being the
+ *   last Lq positions), h' = h / (Hq / Hkv).
+ *   q    bf16 [B, Hq, Lq, D];  k  bf16 [B, Hkv, T, D]   (4-byte aligned)
+ *   vq   uint32 [B, Hkv, T, D*bits/32]                   (8-byte aligned)
+ *   vs, vb  bf16 [B, Hkv, T, D/64]
+ *   out  bf16 [B, Hq, Lq, D]
+ *   D 64, 128 or 256; bits 4 or 8; group 64; Hq a multiple of Hkv; T >= 1;
+ *   causal needs Lq <= T.  scale is usually 1/sqrt(D).
+ *   workspace  >= gwa_sdpa_workspace_bytes(...), 16-byte aligned (per-split
+ *              partial softmax states).
+ * Two kernels on `stream`: the keys of each (batch, KV head) split over the
+ * GPU, then a combine.  Errors: GWA_ERR_UNSUPPORTED (D, bits, group),
+ * GWA_ERR_INVALID_ARG (shapes, null pointers, causal with Lq > T),
+ * GWA_ERR_MISALIGNED, GWA_ERR_WORKSPACE; nothing is enqueued on error. */
+int gwa_sdpa_dequant_v(const uint16_t *q, int64_t B, int32_t Hq, int32_t Lq,
+                       int32_t D, const uint16_t *k, int32_t Hkv, int64_t T,
+                       const uint32_t *vq, const uint16_t *vs,
+                       const uint16_t *vb, int32_t bits, int32_t group,
+                       float scale, int32_t causal, uint16_t *out,
+                       void *workspace, size_t workspace_bytes, void *stream);
+size_t gwa_sdpa_workspace_bytes(int64_t B, int32_t Hq, int32_t Hkv, int32_t Lq,
+                                int64_t T, int32_t D);
+
 /* gwa_quantize_affine -- affine group quantization of bf16 weights into the
  * packed format every projection above reads: the requantize step of
  * "Sanctum-MLX", "The April 2026 cutover" (LoRA merge at load dequantizes,

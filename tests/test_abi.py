@@ -183,3 +183,23 @@ def test_formats_outside_the_tuned_kernels_are_refused_where_unsupported(lib):
         assert lib.gwa_qmv_affine(0x4000, 0, _qw(gwa, bits=bits, group=group),
                                   0x5000, None, 0, None) == 0
 
+
+
+@needs_nvcc
+def test_attention_arguments_are_checked(lib):
+    call = lambda **a: lib.gwa_sdpa_dequant_v(
+        a.get("q", 0x4000), a.get("B", 1), a.get("Hq", 8), a.get("Lq", 1),
+        a.get("D", 128), 0x5000, a.get("Hkv", 2), a.get("T", 16),
+        a.get("vq", 0x6000), 0x7000, 0x8000, a.get("bits", 4),
+        a.get("group", 64), 0.1, a.get("causal", 1), 0x9000, None, 0, None)
+    assert call(D=96) == 2
+    assert call(bits=2) == 2
+    assert call(group=32) == 2
+    assert call(Hq=6, Hkv=4) == 1        # Hq not a multiple of Hkv
+    assert call(T=0) == 1
+    assert call(Lq=20, T=16) == 1        # causal: a query would see no key
+    assert call(q=None) == 1
+    assert call(vq=0x6004) == 3
+    assert call() == 5                   # no workspace
+    assert call(Lq=0) == 0               # nothing to do
+    assert lib.gwa_sdpa_workspace_bytes(1, 8, 2, 1, 16, 128) > 0
