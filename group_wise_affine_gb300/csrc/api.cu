@@ -651,10 +651,10 @@ int gwa_sdpa_dequant_v(const uint16_t *q, int64_t B, int32_t Hq, int32_t Lq,
     if (B == 0 || Lq == 0) return GWA_OK;
     if (!q || !k || !vq || !vs || !vb || !out)
         return fail(GWA_ERR_INVALID_ARG, "%s: null pointer", fn);
-    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(vq, 8) || !aligned(vs, 2) ||
-        !aligned(vb, 2) || !aligned(out, 2))
-        return fail(GWA_ERR_MISALIGNED, "%s: alignment (q, k 4 bytes; codes 8)",
-                    fn);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(vq, 8) || !aligned(vs, 8) ||
+        !aligned(vb, 8) || !aligned(out, 2))
+        return fail(GWA_ERR_MISALIGNED,
+                    "%s: alignment (q, k 16 bytes; codes, scales, biases 8)", fn);
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
         return fail(GWA_ERR_INVALID_ARG, "%s: scale", fn);
     const size_t need = gwa_sdpa_workspace_bytes(B, Hq, Hkv, Lq, T, D);

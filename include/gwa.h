@@ -228,16 +228,18 @@ size_t gwa_qkv_rope_workspace_bytes(int64_t M, int64_t K, int32_t head_dim);
  *   out[b,h,l,:] = sum_t p_t v[b,h',t,:],  p = softmax_t(scale * q[b,h,l,:] .
  *   k[b,h',t,:]) over t < T (causal: t <= T - Lq + l, the queries being the
  *   last Lq positions), h' = h / (Hq / Hkv).
- *   q    bf16 [B, Hq, Lq, D];  k  bf16 [B, Hkv, T, D]   (4-byte aligned)
+ *   q    bf16 [B, Hq, Lq, D];  k  bf16 [B, Hkv, T, D]   (16-byte aligned)
  *   vq   uint32 [B, Hkv, T, D*bits/32]                   (8-byte aligned)
- *   vs, vb  bf16 [B, Hkv, T, D/64]
+ *   vs, vb  bf16 [B, Hkv, T, D/64]                       (8-byte aligned)
  *   out  bf16 [B, Hq, Lq, D]
  *   D 64, 128 or 256; bits 4 or 8; group 64; Hq a multiple of Hkv; T >= 1;
  *   causal needs Lq <= T.  scale is usually 1/sqrt(D).
  *   workspace  >= gwa_sdpa_workspace_bytes(...), 16-byte aligned (per-split
  *              partial softmax states).
  * Two kernels on `stream`: the keys of each (batch, KV head) split over the
- * GPU, then a combine.  Errors: GWA_ERR_UNSUPPORTED (D, bits, group),
+ * GPU (scores and value products on the tensor cores, bf16 operands with
+ * fp32 accumulation: the softmax weights times the value scales enter the
+ * value product rounded to bf16), then a combine.  Errors: GWA_ERR_UNSUPPORTED (D, bits, group),
  * GWA_ERR_INVALID_ARG (shapes, null pointers, causal with Lq > T),
  * GWA_ERR_MISALIGNED, GWA_ERR_WORKSPACE; nothing is enqueued on error. */
 int gwa_sdpa_dequant_v(const uint16_t *q, int64_t B, int32_t Hq, int32_t Lq,

@@ -200,6 +200,7 @@ def test_attention_arguments_are_checked(lib):
     assert call(Lq=20, T=16) == 1        # causal: a query would see no key
     assert call(q=None) == 1
     assert call(vq=0x6004) == 3
+    assert call(q=0x4008) == 3           # q and k need 16 bytes
     assert call() == 5                   # no workspace
     assert call(Lq=0) == 0               # nothing to do
     assert lib.gwa_sdpa_workspace_bytes(1, 8, 2, 1, 16, 128) > 0
