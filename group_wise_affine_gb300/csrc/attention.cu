@@ -50,6 +50,10 @@ constexpr int kAttRows = 8;    // query rows per block: the MMAs' n
 constexpr int kAttWarps = 4;
 constexpr int kAttTile = 16;   // keys per warp tile: the MMAs' m / k
 constexpr int kAttMaxSplits = 1024;
+// Floats per (query row, split) partial: D outputs, the max and the sum,
+// padded so each partial starts on 16 bytes.
+template <int D>
+constexpr int kAttPartStride = D + 4;
 
 struct AttParams {
     const uint16_t *q;    // [B, Hq, Lq, D]
@@ -58,21 +62,23 @@ struct AttParams {
     const uint16_t *vs;   // [B, Hkv, T, D/64]
     const uint16_t *vb;
     uint16_t *out;        // [B, Hq, Lq, D]
-    float *part;          // [B, Hq, Lq, nsplit, D + 2]
+    float *part;          // [B, Hq, Lq, nsplit, D + 4]
     int B, Hq, Hkv, Lq, T, nsplit, rowgroups;
     float scale;
     int causal;
 };
 
-// Whether `blocks` blocks of kAttWarps warps with `stages` stages of
-// `stage` bytes fit in an SM's 228 KB (2 KB per block for the static
-// buffers and the system's share).
-constexpr bool att_fits(int stage, int blocks, int stages) {
-    return blocks * (kAttWarps * stages * stage + 2048) <= 228 * 1024;
+// Resident blocks of kAttWarps warps with four ring stages of `stage` bytes
+// in an SM's 228 KB (2 KB per block for the static buffers and the
+// system's share), at most four.
+constexpr int att_blocks(int stage) {
+    return (228 * 1024) / (kAttWarps * 4 * stage + 2048) > 4
+               ? 4
+               : (228 * 1024) / (kAttWarps * 4 * stage + 2048);
 }
 
-// One warp's stage of the ring, in bytes.  Every item is laid out
-// [item][lane] so a warp's copies and reads of one item are consecutive.
+// One warp's stage of the ring (one tile), in bytes.  Every item is laid
+// out [item][lane] so a warp's copies and reads of one item are consecutive.
 template <int BITS, int D>
 struct AttLayout {
     static constexpr int G = D / 64;          // scale groups per key row
@@ -84,17 +90,12 @@ struct AttLayout {
     static constexpr int S_OFF = V_OFF + 4 * G * VB * kWarp;
     static constexpr int B_OFF = S_OFF + 2 * SB * kWarp;
     static constexpr int STAGE = B_OFF + 2 * SB * kWarp;
-    // stages and resident blocks: three blocks of three stages where they
-    // fit in an SM's shared memory, else two blocks of four, three or two
-    static constexpr int S = att_fits(STAGE, 3, 3)   ? 3
-                             : att_fits(STAGE, 2, 4) ? 4
-                             : att_fits(STAGE, 2, 3) ? 3
-                                                     : 2;
-    static constexpr int BLOCKS_PER_SM = att_fits(STAGE, 3, 3) ? 3 : 2;
+    static constexpr int S = 4;  // two tiles computed while two load
+    static constexpr int BLOCKS_PER_SM = att_blocks(STAGE);
     static constexpr int WARP_BYTES = STAGE * S;
     static constexpr int BYTES = WARP_BYTES * kAttWarps;
     static_assert(kAttRows * D * 4 <= WARP_BYTES, "merge buffer fits the ring");
-    static_assert(att_fits(STAGE, BLOCKS_PER_SM, S), "shared memory per SM");
+    static_assert(BLOCKS_PER_SM >= 1, "shared memory per SM");
 };
 
 template <int N>
@@ -153,11 +154,18 @@ __device__ __forceinline__ __nv_bfloat162 bits_bf2(uint32_t v) {
     return *reinterpret_cast<const __nv_bfloat162 *>(&v);
 }
 
-// The 4-bit fields at bits 0-3 and 16-19 of x as an exact bf16 pair:
-// 0x4300 | q is 128 + q, and subtracting 128 leaves q.
+// The 4-bit fields at bits 0-3 and 16-19 of x as a bf16 pair of 128 + q
+// (0x4300 | q, exact); the 128 * sum of the weights it adds is taken back
+// in the bias term.
 __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t x) {
-    return bf2_bits(__hsub2(bits_bf2((x & 0x000f000fu) | 0x43004300u),
-                            bits_bf2(0x43004300u)));
+    return (x & 0x000f000fu) | 0x43004300u;
+}
+
+// Bulk L2 prefetch of [ptr, ptr + bytes) by the copy engine (ptr and bytes
+// multiples of 16).
+__device__ __forceinline__ void prefetch_bulk_l2(const void *ptr, int bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes)
+                 : "memory");
 }
 
 template <int BITS, int D>
@@ -172,6 +180,8 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
     extern __shared__ __align__(16) unsigned char att_smem[];
     __shared__ float s_m[kAttWarps][kAttRows], s_l[kAttWarps][kAttRows];
     __shared__ float s_b[kAttWarps][kAttRows][G];
+    __shared__ float s_f[kAttWarps][kAttRows];
+    __shared__ float *s_dst[kAttRows];
 
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
     const int g = lane >> 2, t = lane & 3;  // fragment row group, column pair
@@ -185,7 +195,28 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
     const int64_t kv = ((int64_t)b * p.Hkv + hk) * p.T;  // first key row
     const int64_t rows_total = (int64_t)p.B * p.Hkv * p.T;
     unsigned char *wsm = att_smem + warp * L::WARP_BYTES;
+    const int ntile = t1 > t0 ? (t1 - t0 + kAttTile - 1) / kAttTile : 0;
+    const int nmine = ntile > warp ? (ntile - warp + kAttWarps - 1) / kAttWarps : 0;
+    const int npair = (nmine + 1) / 2;  // an odd count ends on a masked tile
     if (threadIdx.x == 0) pdl_launch_dependents();
+    // While the previous kernel finishes, pull the K and code rows of this
+    // warp's first two tiles into L2.  A prefetch moves nothing into the
+    // SM, so the copies made after the wait still see whatever that kernel
+    // writes.  (The transfer into the SMs after the wait, not the DRAM
+    // latency, dominates the first tiles, so this gains little when the
+    // previous kernel is short.)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int ts = t0 + (warp + j * kAttWarps) * kAttTile;
+        if (j < nmine) {
+            const int nk = min(kAttTile, t1 - ts);
+            const int64_t r0 = kv + ts;
+            if (lane == 0) {  // K and code rows: 16-byte aligned, whole
+                prefetch_bulk_l2(p.k + r0 * D, nk * D * 2);
+                prefetch_bulk_l2(p.vq + r0 * WPR, nk * WPR * 4);
+            }
+        }
+    }
     pdl_wait_primary();  // q, k, v may come from the previous kernel
 
     // keys [0, tm) are visible to this lane's output rows 2t and 2t + 1
@@ -213,14 +244,14 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
         for (int c = 0; c < KC; ++c) qf[c] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    const int ntile = t1 > t0 ? (t1 - t0 + kAttTile - 1) / kAttTile : 0;
-    const int nmine = ntile > warp ? (ntile - warp + kAttWarps - 1) / kAttWarps : 0;
     // Tile i of this warp: keys ts .. ts + 15.  The scores' row g is key
     // 2g and row g + 8 key 2g + 1 (the lane copies those two K rows and
     // their scales and biases); the value product's k = 2t, 2t + 1 are keys
     // 4t, 4t + 2 and k = 2t + 8, 2t + 9 keys 4t + 1, 4t + 3 (the lane copies
     // its 8 dimensions of each group of those four keys).  Keys past the
-    // split are clamped to its last key and masked.
+    // split are clamped to its last key and masked; a warp with an odd
+    // number of tiles computes one more, wholly past the split, so that
+    // tiles go in pairs.
     auto issue = [&](int i) {
         unsigned char *st = wsm + (i % S) * L::STAGE;
         const int ts = t0 + (warp + i * kAttWarps) * kAttTile;
@@ -266,57 +297,83 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) bs[gg][0] = bs[gg][1] = 0.f;
     const float sl2 = p.scale * 1.4426950408889634f;  // scores in base 2
+    const int lim[2] = {min(t1, tm[0]), min(t1, tm[1])};
+    // The running max m moves only when a score exceeds it by more than
+    // 2^kLazy (weights up to 2^8: no overflow, no loss), so most tiles need
+    // one vote instead of a max-reduction and a rescale.
+    constexpr float kLazy = 8.f;
+    // 128 * weight enters the value product with every code (once per
+    // nibble product: 1 + 16 for 8-bit codes)
+    constexpr float kCodeBias = BITS == 4 ? 128.f : 128.f * 17.f;
 
-#pragma unroll
-    for (int i = 0; i < S - 1; ++i) {
-        if (i < nmine) issue(i);
-        cp_async_commit();
+    if (npair > 0) {
+        issue(0);
+        issue(1);  // not part of the split when nmine == 1: masked
     }
-    for (int i = 0; i < nmine; ++i) {
-        if (i + S - 1 < nmine) issue(i + S - 1);
+    cp_async_commit();
+    cp_async_commit();
+    for (int it = 0; it < npair; ++it) {
+        if (it + 1 < npair) {
+            issue(2 * it + 2);
+            issue(2 * it + 3);
+        }
         cp_async_commit();
-        cp_async_wait<S - 1>();  // tile i has landed
-        const unsigned char *st = wsm + (i % S) * L::STAGE;
-        const int ts = t0 + (warp + i * kAttWarps) * kAttTile;
+        cp_async_wait<1>();  // tiles 2it and 2it + 1 (one group) have landed
+        const unsigned char *stg[2];
+        stg[0] = wsm + ((2 * it) % S) * L::STAGE;
+        stg[1] = stg[0] + L::STAGE;
+        int ts[2];
+        ts[0] = t0 + (warp + 2 * it * kAttWarps) * kAttTile;
+        ts[1] = ts[0] + kAttWarps * kAttTile;
 
-        // scores: two accumulator chains over the k-steps
-        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+        // scores: two accumulator chains per tile over the k-steps
+        float ca[2][4], cb[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ca[u][e] = cb[u][e] = 0.f;
 #pragma unroll
         for (int c = 0; c < KC; ++c) {
-            const uint4 k0 = *reinterpret_cast<const uint4 *>(
-                st + L::K_OFF + (c * kWarp + lane) * 16);
-            const uint4 k1 = *reinterpret_cast<const uint4 *>(
-                st + L::K_OFF + ((KC + c) * kWarp + lane) * 16);
-            mma_bf16(ca, k0.x, k1.x, k0.y, k1.y, qf[c].x, qf[c].y);
-            mma_bf16(cb, k0.z, k1.z, k0.w, k1.w, qf[c].z, qf[c].w);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint4 k0 = *reinterpret_cast<const uint4 *>(
+                    stg[u] + L::K_OFF + (c * kWarp + lane) * 16);
+                const uint4 k1 = *reinterpret_cast<const uint4 *>(
+                    stg[u] + L::K_OFF + ((KC + c) * kWarp + lane) * 16);
+                mma_bf16(ca[u], k0.x, k1.x, k0.y, k1.y, qf[c].x, qf[c].y);
+                mma_bf16(cb[u], k0.z, k1.z, k0.w, k1.w, qf[c].z, qf[c].w);
+            }
         }
-        // x[kk][h]: key ts + 2g + kk against row 2t + h, masked to -inf
-        float x[2][2];
+        // x[u][kk][h]: key ts[u] + 2g + kk against row 2t + h, or -inf
+        float x[2][2][2], lm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const int key = ts + 2 * g + kk;
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                x[kk][h] = key < t1 && key < tm[h]
-                               ? (ca[2 * kk + h] + cb[2 * kk + h]) * sl2
-                               : -INFINITY;
-        }
-        float cr[2], pr[2][2];
+            for (int kk = 0; kk < 2; ++kk) {
+                const int key = ts[u] + 2 * g + kk;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float mt = fmaxf(x[0][h], x[1][h]);
+                for (int h = 0; h < 2; ++h) {
+                    x[u][kk][h] = key < lim[h]
+                                      ? (ca[u][2 * kk + h] + cb[u][2 * kk + h]) * sl2
+                                      : -INFINITY;
+                    lm[h] = fmaxf(lm[h], x[u][kk][h]);
+                }
+            }
+        if (__any_sync(FULL, lm[0] > m[0] + kLazy || lm[1] > m[1] + kLazy)) {
+            float cr[2];
 #pragma unroll
-            for (int off = 4; off < kWarp; off <<= 1)
-                mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, off));
-            const float mn = fmaxf(m[h], mt);
-            cr[h] = mn == -INFINITY ? 1.f : ex2(m[h] - mn);
+            for (int h = 0; h < 2; ++h) {
+                float mt = lm[h];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-                pr[kk][h] = x[kk][h] == -INFINITY ? 0.f : ex2(x[kk][h] - mn);
-            l[h] = l[h] * cr[h] + pr[0][h] + pr[1][h];
-            m[h] = mn;
-        }
-        if (!__all_sync(FULL, cr[0] == 1.f && cr[1] == 1.f)) {
+                for (int off = 4; off < kWarp; off <<= 1)
+                    mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, off));
+                const float mn = fmaxf(m[h], mt);
+                cr[h] = mn == -INFINITY ? 1.f : ex2(m[h] - mn);
+                m[h] = mn;
+                l[h] *= cr[h];
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) bs[gg][h] *= cr[h];
+            }
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 o[j][0] *= cr[0];
@@ -325,89 +382,130 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
                 o[j][3] *= cr[1];
             }
         }
+        float pr[2][2][2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    pr[u][kk][h] = x[u][kk][h] == -INFINITY ? 0.f : ex2(x[u][kk][h] - m[h]);
+                    l[h] += pr[u][kk][h];
+                }
 
-        // scales and biases of keys 2g, 2g + 1, group gg
-        float sc[2][G], bi[2][G];
+        // scales and biases of keys 2g, 2g + 1 of each tile, group gg
+        float sc[2][2][G], bi[2][2][G];
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const unsigned char *ss = st + L::S_OFF + (kk * kWarp + lane) * SB;
-            const unsigned char *sb = st + L::B_OFF + (kk * kWarp + lane) * SB;
-            if constexpr (G == 1) {
-                const int64_t row = kv + min(ts + 2 * g + kk, t1 - 1);
-                const int sh = (int)(row & 1) * 16;
-                sc[kk][0] = bf16_bits_to_f32(
-                    (uint16_t)(*reinterpret_cast<const uint32_t *>(ss) >> sh));
-                bi[kk][0] = bf16_bits_to_f32(
-                    (uint16_t)(*reinterpret_cast<const uint32_t *>(sb) >> sh));
-            } else {
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int w = 0; w < G / 2; ++w) {
-                    const uint32_t vs = reinterpret_cast<const uint32_t *>(ss)[w];
-                    const uint32_t vb = reinterpret_cast<const uint32_t *>(sb)[w];
-                    sc[kk][2 * w] = bf16_lo(vs);
-                    sc[kk][2 * w + 1] = bf16_hi(vs);
-                    bi[kk][2 * w] = bf16_lo(vb);
-                    bi[kk][2 * w + 1] = bf16_hi(vb);
+            for (int kk = 0; kk < 2; ++kk) {
+                const unsigned char *ss = stg[u] + L::S_OFF + (kk * kWarp + lane) * SB;
+                const unsigned char *sb = stg[u] + L::B_OFF + (kk * kWarp + lane) * SB;
+                if constexpr (G == 1) {
+                    const int64_t row = kv + min(ts[u] + 2 * g + kk, t1 - 1);
+                    const int sh = (int)(row & 1) * 16;
+                    sc[u][kk][0] = bf16_bits_to_f32(
+                        (uint16_t)(*reinterpret_cast<const uint32_t *>(ss) >> sh));
+                    bi[u][kk][0] = bf16_bits_to_f32(
+                        (uint16_t)(*reinterpret_cast<const uint32_t *>(sb) >> sh));
+                } else {
+#pragma unroll
+                    for (int w = 0; w < G / 2; ++w) {
+                        const uint32_t vs = reinterpret_cast<const uint32_t *>(ss)[w];
+                        const uint32_t vb = reinterpret_cast<const uint32_t *>(sb)[w];
+                        sc[u][kk][2 * w] = bf16_lo(vs);
+                        sc[u][kk][2 * w + 1] = bf16_hi(vs);
+                        bi[u][kk][2 * w] = bf16_lo(vb);
+                        bi[u][kk][2 * w + 1] = bf16_hi(vb);
+                    }
                 }
             }
-        }
 
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
+            uint32_t pb[2][2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                bs[gg][h] = fmaf(pr[0][h], bi[0][gg],
-                                 fmaf(pr[1][h], bi[1][gg], bs[gg][h] * cr[h]));
-            // P' rows (keys 2g / 2g + 1) x columns (rows 2t, 2t + 1), then
-            // transposed into the value product's B fragments
-            const uint32_t pb0 = movmatrix_t(
-                pack_bf16(pr[0][0] * sc[0][gg], pr[0][1] * sc[0][gg]));
-            const uint32_t pb1 = movmatrix_t(
-                pack_bf16(pr[1][0] * sc[1][gg], pr[1][1] * sc[1][gg]));
-            const unsigned char *sv = st + L::V_OFF + (gg * kWarp + lane) * VB;
+            for (int u = 0; u < 2; ++u) {
+                // P' rows (keys 2g / 2g + 1) x columns (rows 2t, 2t + 1),
+                // then transposed into the value product's B fragments
+                const uint32_t x0 = pack_bf16(pr[u][0][0] * sc[u][0][gg],
+                                              pr[u][0][1] * sc[u][0][gg]);
+                const uint32_t x1 = pack_bf16(pr[u][1][0] * sc[u][1][gg],
+                                              pr[u][1][1] * sc[u][1][gg]);
+                // bias term, less the 128 * P' (as rounded) the codes carry
+                bs[gg][0] = fmaf(pr[u][0][0], bi[u][0][gg],
+                                 fmaf(pr[u][1][0], bi[u][1][gg],
+                                      fmaf(-kCodeBias, bf16_lo(x0) + bf16_lo(x1),
+                                           bs[gg][0])));
+                bs[gg][1] = fmaf(pr[u][0][1], bi[u][0][gg],
+                                 fmaf(pr[u][1][1], bi[u][1][gg],
+                                      fmaf(-kCodeBias, bf16_hi(x0) + bf16_hi(x1),
+                                           bs[gg][1])));
+                pb[u][0] = movmatrix_t(x0);
+                pb[u][1] = movmatrix_t(x1);
+            }
             constexpr int KQ = G * kWarp * VB;  // stride between the four keys
             if constexpr (BITS == 4) {
                 // keys 4t, 4t+2 (k = 2t, 2t+1) and 4t+1, 4t+3 (k = 2t+8, 2t+9)
-                const uint32_t wa = *reinterpret_cast<const uint32_t *>(sv);
-                const uint32_t wc = *reinterpret_cast<const uint32_t *>(sv + KQ);
-                const uint32_t wb = *reinterpret_cast<const uint32_t *>(sv + 2 * KQ);
-                const uint32_t wd = *reinterpret_cast<const uint32_t *>(sv + 3 * KQ);
+                uint32_t wa[2], wb[2], wc[2], wd[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const unsigned char *sv = stg[u] + L::V_OFF + (gg * kWarp + lane) * VB;
+                    wa[u] = *reinterpret_cast<const uint32_t *>(sv);
+                    wc[u] = *reinterpret_cast<const uint32_t *>(sv + KQ);
+                    wb[u] = *reinterpret_cast<const uint32_t *>(sv + 2 * KQ);
+                    wd[u] = *reinterpret_cast<const uint32_t *>(sv + 3 * KQ);
+                }
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     // byte jj of each word: dimensions 8g + 2jj (low nibble,
                     // m-row g) and 8g + 2jj + 1 (high nibble, m-row g + 8)
                     const uint32_t sel =
                         jj | (jj << 4) | ((4 + jj) << 8) | ((4 + jj) << 12);
-                    const uint32_t rab = __byte_perm(wa, wb, sel);
-                    const uint32_t rcd = __byte_perm(wc, wd, sel);
-                    mma_bf16(o[4 * gg + jj], codes_bf16x2(rab), codes_bf16x2(rab >> 4),
-                             codes_bf16x2(rcd), codes_bf16x2(rcd >> 4), pb0, pb1);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t rab = __byte_perm(wa[u], wb[u], sel);
+                        const uint32_t rcd = __byte_perm(wc[u], wd[u], sel);
+                        mma_bf16(o[4 * gg + jj], codes_bf16x2(rab), codes_bf16x2(rab >> 4),
+                                 codes_bf16x2(rcd), codes_bf16x2(rcd >> 4), pb[u][0],
+                                 pb[u][1]);
+                    }
                 }
             } else {
                 // 8-bit codes as 16 * high nibble + low nibble: two products,
                 // the high one against 16 P' (exact in bf16)
                 const __nv_bfloat162 k16 = bits_bf2(0x41804180u);  // 16.0
-                const uint32_t ph0 = bf2_bits(__hmul2(bits_bf2(pb0), k16));
-                const uint32_t ph1 = bf2_bits(__hmul2(bits_bf2(pb1), k16));
-                const uint2 wa = *reinterpret_cast<const uint2 *>(sv);
-                const uint2 wc = *reinterpret_cast<const uint2 *>(sv + KQ);
-                const uint2 wb = *reinterpret_cast<const uint2 *>(sv + 2 * KQ);
-                const uint2 wd = *reinterpret_cast<const uint2 *>(sv + 3 * KQ);
+                uint2 wa[2], wb[2], wc[2], wd[2];
+                uint32_t ph[2][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const unsigned char *sv = stg[u] + L::V_OFF + (gg * kWarp + lane) * VB;
+                    wa[u] = *reinterpret_cast<const uint2 *>(sv);
+                    wc[u] = *reinterpret_cast<const uint2 *>(sv + KQ);
+                    wb[u] = *reinterpret_cast<const uint2 *>(sv + 2 * KQ);
+                    wd[u] = *reinterpret_cast<const uint2 *>(sv + 3 * KQ);
+                    ph[u][0] = bf2_bits(__hmul2(bits_bf2(pb[u][0]), k16));
+                    ph[u][1] = bf2_bits(__hmul2(bits_bf2(pb[u][1]), k16));
+                }
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     // bytes 2jj (m-row g) and 2jj + 1 (m-row g + 8)
                     const int e = 2 * (jj & 1);
                     const uint32_t sel =
                         e | ((e + 1) << 4) | ((4 + e) << 8) | ((5 + e) << 12);
-                    const uint32_t rab =
-                        __byte_perm(jj < 2 ? wa.x : wa.y, jj < 2 ? wb.x : wb.y, sel);
-                    const uint32_t rcd =
-                        __byte_perm(jj < 2 ? wc.x : wc.y, jj < 2 ? wd.x : wd.y, sel);
-                    mma_bf16(o[4 * gg + jj], codes_bf16x2(rab), codes_bf16x2(rab >> 8),
-                             codes_bf16x2(rcd), codes_bf16x2(rcd >> 8), pb0, pb1);
-                    mma_bf16(o[4 * gg + jj], codes_bf16x2(rab >> 4),
-                             codes_bf16x2(rab >> 12), codes_bf16x2(rcd >> 4),
-                             codes_bf16x2(rcd >> 12), ph0, ph1);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t rab = __byte_perm(jj < 2 ? wa[u].x : wa[u].y,
+                                                         jj < 2 ? wb[u].x : wb[u].y, sel);
+                        const uint32_t rcd = __byte_perm(jj < 2 ? wc[u].x : wc[u].y,
+                                                         jj < 2 ? wd[u].x : wd[u].y, sel);
+                        mma_bf16(o[4 * gg + jj], codes_bf16x2(rab), codes_bf16x2(rab >> 8),
+                                 codes_bf16x2(rcd), codes_bf16x2(rcd >> 8), pb[u][0],
+                                 pb[u][1]);
+                        mma_bf16(o[4 * gg + jj], codes_bf16x2(rab >> 4),
+                                 codes_bf16x2(rab >> 12), codes_bf16x2(rcd >> 4),
+                                 codes_bf16x2(rcd >> 12), ph[u][0], ph[u][1]);
+                    }
                 }
             }
         }
@@ -426,16 +524,15 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
         }
     }
     // the warp's (unnormalized) output rows into its own ring: [row][D];
-    // m-tile 4gg + jj holds dimensions 64gg + 8g + 2jj (+1 for m-row g + 8)
+    // m-tile 4gg + jj holds dimensions 64gg + 8g + 2jj (and + 1, m-row g + 8)
     __syncwarp();
     float *so = reinterpret_cast<float *>(wsm);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int d = 64 * (j / 4) + 8 * g + 2 * (j % 4);
-        so[(2 * t) * D + d] = o[j][0];
-        so[(2 * t + 1) * D + d] = o[j][1];
-        so[(2 * t) * D + d + 1] = o[j][2];
-        so[(2 * t + 1) * D + d + 1] = o[j][3];
+        *reinterpret_cast<float2 *>(so + (2 * t) * D + d) = make_float2(o[j][0], o[j][2]);
+        *reinterpret_cast<float2 *>(so + (2 * t + 1) * D + d) =
+            make_float2(o[j][1], o[j][3]);
     }
     if (g == 0) {
 #pragma unroll
@@ -447,49 +544,74 @@ __global__ void __launch_bounds__(kAttWarps * kWarp,
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < kAttRows * (D + 2); e += blockDim.x) {
-        const int i = e / (D + 2), c = e % (D + 2);
-        if (i >= nlive) continue;
+    // per row: the warps' factors 2^(m_w - max) and the row's partial slot
+    if (threadIdx.x < nlive) {
+        const int i = threadIdx.x;
         float mx = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kAttWarps; ++w) mx = fmaxf(mx, s_m[w][i]);
-        float val = 0.f;
-        if (c == D) {
-            val = mx;
-        } else {
+        float den = 0.f;
 #pragma unroll
-            for (int w = 0; w < kAttWarps; ++w) {
-                const float f = s_m[w][i] == -INFINITY ? 0.f : ex2(s_m[w][i] - mx);
-                const float *sow =
-                    reinterpret_cast<const float *>(att_smem + w * L::WARP_BYTES);
-                val += f * (c == D + 1 ? s_l[w][i] : sow[i * D + c] + s_b[w][i][c / 64]);
-            }
+        for (int w = 0; w < kAttWarps; ++w) {
+            const float f = s_m[w][i] == -INFINITY ? 0.f : ex2(s_m[w][i] - mx);
+            s_f[w][i] = f;
+            den += f * s_l[w][i];
         }
         const int r = rg * kAttRows + i;
         const int hq = hk * rep + r / p.Lq, lq = r % p.Lq;
         float *dst = p.part + ((((int64_t)b * p.Hq + hq) * p.Lq + lq) * p.nsplit +
-                               split) * (D + 2);
-        dst[c] = val;  // [0, D): output, D: max (base 2), D + 1: sum
+                               split) * kAttPartStride<D>;
+        s_dst[i] = dst;
+        dst[D] = mx;       // max (base 2)
+        dst[D + 1] = den;  // sum
+    }
+    __syncthreads();
+    constexpr int C4 = D / 4;  // float4 columns of a row
+    for (int e = threadIdx.x; e < nlive * C4; e += blockDim.x) {
+        const int i = e / C4, c4 = e % C4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kAttWarps; ++w) {
+            const float f = s_f[w][i], bw = s_b[w][i][c4 / 16];
+            const float4 v = reinterpret_cast<const float4 *>(
+                att_smem + w * L::WARP_BYTES)[i * C4 + c4];
+            acc.x = fmaf(f, v.x + bw, acc.x);
+            acc.y = fmaf(f, v.y + bw, acc.y);
+            acc.z = fmaf(f, v.z + bw, acc.z);
+            acc.w = fmaf(f, v.w + bw, acc.w);
+        }
+        reinterpret_cast<float4 *>(s_dst[i])[c4] = acc;  // output [0, D)
     }
 }
 
 // out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits (the
-// maxima are base-2 scores).  The splits' maxima and sums are read in
-// parallel into shared memory first; each thread then adds its dimension
-// over the splits with eight loads in flight.
+// maxima are base-2 scores).  Every load of a row's partials is independent,
+// so they are all issued up front: each thread's dimension for the first
+// kCombineChunk splits into registers, and the splits' maxima and sums into
+// shared memory, before the block reduces the maxima; further chunks (more
+// than kCombineChunk splits) cost one more round trip each.
+constexpr int kCombineChunk = 64;
+
 template <int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(AttParams p) {
-    __shared__ float s_f[kAttMaxSplits];  // 2^(m_s - M), 0 for empty splits
+    __shared__ float s_f[kAttMaxSplits];  // m_s, then 2^(m_s - M) (0 if empty)
+    __shared__ float s_ls[kAttMaxSplits];
     __shared__ float s_red[D / kWarp];
     __shared__ float s_mx, s_den;
     if (threadIdx.x == 0) pdl_launch_dependents();
     pdl_wait_primary();  // the partials are the previous kernel's output
     const int64_t row = blockIdx.x;  // (b, hq, lq)
-    const float *src = p.part + row * p.nsplit * (D + 2);
+    const int ns = p.nsplit;
+    const float *src = p.part + row * ns * kAttPartStride<D>;
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
+    float ov[kCombineChunk];
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u)
+        ov[u] = u < ns ? src[(int64_t)u * kAttPartStride<D> + threadIdx.x] : 0.f;
     float mx = -INFINITY;
-    for (int sp = threadIdx.x; sp < p.nsplit; sp += D) {
-        const float ms = src[(int64_t)sp * (D + 2) + D];
+    for (int sp = threadIdx.x; sp < ns; sp += D) {
+        const float ms = src[(int64_t)sp * kAttPartStride<D> + D];
+        s_ls[sp] = src[(int64_t)sp * kAttPartStride<D> + D + 1];
         s_f[sp] = ms;
         mx = fmaxf(mx, ms);
     }
@@ -505,11 +627,11 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttParams p) {
     __syncthreads();
     const float M = s_mx;
     float den = 0.f;
-    for (int sp = threadIdx.x; sp < p.nsplit; sp += D) {
+    for (int sp = threadIdx.x; sp < ns; sp += D) {
         const float ms = s_f[sp];
         const float f = ms == -INFINITY ? 0.f : ex2(ms - M);
         s_f[sp] = f;
-        den += f * src[(int64_t)sp * (D + 2) + D + 1];
+        den += f * s_ls[sp];
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -523,16 +645,17 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttParams p) {
     }
     __syncthreads();
     float num = 0.f;
-    int sp = 0;
-    for (; sp + 8 <= p.nsplit; sp += 8) {
-        float ov[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) ov[u] = src[(int64_t)(sp + u) * (D + 2) + threadIdx.x];
+    for (int u = 0; u < kCombineChunk; ++u)
+        if (u < ns) num = fmaf(s_f[u], ov[u], num);
+    for (int c0 = kCombineChunk; c0 < ns; c0 += kCombineChunk) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) num = fmaf(s_f[sp + u], ov[u], num);
+        for (int u = 0; u < kCombineChunk; ++u)
+            ov[u] = c0 + u < ns ? src[(int64_t)(c0 + u) * kAttPartStride<D> + threadIdx.x] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kCombineChunk; ++u)
+            if (c0 + u < ns) num = fmaf(s_f[c0 + u], ov[u], num);
     }
-    for (; sp < p.nsplit; ++sp)
-        num = fmaf(s_f[sp], src[(int64_t)sp * (D + 2) + threadIdx.x], num);
     p.out[row * D + threadIdx.x] = f32_to_bf16_bits(num / s_den);
 }
 
@@ -631,7 +754,9 @@ size_t attention_workspace_bytes(int B, int Hq, int Hkv, int Lq, int T,
     const int ns = std::max(
         attn_splits(B, Hkv, rowgroups, T, attn_blocks_per_sm(4, D)),
         attn_splits(B, Hkv, rowgroups, T, attn_blocks_per_sm(8, D)));
-    return (size_t)B * Hq * Lq * ns * (D + 2) * sizeof(float);
+    const size_t stride = D == 64 ? kAttPartStride<64> : D == 128 ? kAttPartStride<128>
+                                                        : kAttPartStride<256>;
+    return (size_t)B * Hq * Lq * ns * stride * sizeof(float);
 }
 
 }  // namespace gwa
