@@ -577,12 +577,13 @@ def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
     return res
 
 
-def run_attention_extra(dev, steps, warmup, lengths=(4096, 32768), Hq=40,
-                        Hkv=8, D=128, bits=4):
+def run_attention_extra(dev, steps, warmup, lengths=(4096, 32768, 131072),
+                        Hq=40, Hkv=8, D=128, bits=4):
     """Decode attention over a u4 value cache (one query per head, 40 query
     heads over 8 KV heads of 128): bytes = bf16 K + packed V + scales and
     biases + q + out; distinct caches per launch (more bytes than L2 across
-    one pass) so they stream from HBM."""
+    one pass) so they stream from HBM.  Short caches show the per-call
+    latency (two dependent kernels), long ones the streaming rate."""
     import torch
     import group_wise_affine_gb300 as gwa
     peak, _ = measured_peak()
