@@ -54,6 +54,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the secondary workloads (M=4, M=512, MoE)")
+    ap.add_argument("--only-extra", default=None,
+                    choices=["attention", "quantize", "moe", "formats"],
+                    help="run one standalone secondary workload for --steps "
+                         "after --warmup replays, print its figures and exit "
+                         "(for profiling; not the bench line)")
+    ap.add_argument("--lengths", default=None,
+                    help="--only-extra attention: comma-separated cache lengths")
     return ap.parse_args()
 
 
@@ -729,6 +736,16 @@ METRIC = ("quantized GEMV achieved HBM GB/s (% of GB300 peak); "
 
 def main():
     args = parse()
+    if args.only_extra:
+        import torch
+        dev = torch.device("cuda")
+        fn = {"attention": run_attention_extra, "quantize": run_quantize_extra,
+              "moe": run_moe_extra, "formats": run_formats_extra}[args.only_extra]
+        kw = {}
+        if args.only_extra == "attention" and args.lengths:
+            kw["lengths"] = tuple(int(v) for v in args.lengths.split(","))
+        print(json.dumps({args.only_extra: fn(dev, args.steps, args.warmup, **kw)}))
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
