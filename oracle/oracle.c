@@ -23,16 +23,20 @@
  *       along the input axis -- and its one matmul output is split back into
  *       Q, K, V on the last axis; the gate+up fusion applies the same recipe
  *       to gate_proj and up_proj ahead of SiLU and the multiply.
- *   "saragossa", "Quantization formats": MLX affine integer weights at group
- *       size 64 with bf16 scales and biases; u4 ~4.5 bpw and u8 ~8.5 bpw,
- *       i.e. two 16-bit parameters per 64 weights.
+ *   "saragossa", "Quantization formats": MLX affine integer weights
+ *       u2/u3/u4/u6/u8 at group size 64 with bf16 scales and biases; u3
+ *       ~3.5, u4 ~4.5, u6 ~6.5 and u8 ~8.5 bpw, i.e. two 16-bit parameters
+ *       per 64 weights.
  *   "Sanctum-MLX" and "Four Candles For The Cathedral": 3-D switch_mlp expert
  *       grids with per-expert gate_proj / up_proj (MoE routed experts).
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes):
- *   - bit order inside a word: code k mod P sits at bits [b*(k mod P), +b),
- *     lowest bits first;
+ *   - bit order: a row's words form one little-endian bit stream and code k
+ *     sits at its bits [b*k, +b), lowest bits first.  For b dividing 32
+ *     (u2, u4, u8) that is field k mod P of word k / P, P = 32/b; a u3 or u6
+ *     code may straddle two words (its low bits at the top of one word, the
+ *     rest at the bottom of the next);
  *   - codes are unsigned, 0 .. 2^b-1; the affine bias carries any offset;
  *   - the dequantized weight is scale*q + bias;
  *   - gate rows come first, then up rows; SiLU(g) = g / (1 + exp(-g));
@@ -63,22 +67,28 @@ double orc_bf16_to_f64(uint16_t h) {
     return (double)f;
 }
 
-static int bits_ok(int bits) { return bits == 2 || bits == 4 || bits == 8; }
-
-/* The integer code at (row n, input k): field k mod P of word k / P. */
-static inline uint32_t code_at(const uint32_t *wq, int64_t words_per_row,
-                               int64_t n, int64_t k, int bits) {
-    int64_t per_word = 32 / bits;
-    uint32_t word = wq[n * words_per_row + k / per_word];
-    uint32_t shift = (uint32_t)(bits * (k % per_word));
-    uint32_t mask = (1u << bits) - 1u;
-    return (word >> shift) & mask;
+static int bits_ok(int bits) {
+    return bits == 2 || bits == 3 || bits == 4 || bits == 6 || bits == 8;
 }
 
+/* The integer code at (row n, input k): bits [b*k, b*k + b) of the row's
+ * bit stream, word j holding stream bits [32j, 32j + 32). */
+static inline uint32_t code_at(const uint32_t *wq, int64_t words_per_row,
+                               int64_t n, int64_t k, int bits) {
+    const uint32_t *row = wq + n * words_per_row;
+    int64_t pos = (int64_t)bits * k;      /* stream position of the low bit */
+    uint32_t shift = (uint32_t)(pos % 32);
+    uint32_t code = row[pos / 32] >> shift;
+    if (shift + (uint32_t)bits > 32u)     /* the rest in the next word */
+        code |= row[pos / 32 + 1] << (32u - shift);
+    return code & ((1u << bits) - 1u);
+}
+
+/* A row of K codes must fill whole words. */
 static int shape_ok(int64_t N, int64_t K, int bits, int group) {
     if (N < 0 || K < 0 || !bits_ok(bits) || group <= 0) return 0;
     if (K % group != 0) return 0;
-    if (K % (32 / bits) != 0) return 0;
+    if ((K * bits) % 32 != 0) return 0;
     return 1;
 }
 
@@ -297,11 +307,12 @@ static float bf16_to_f32(uint16_t h) {
     return f;
 }
 
-/* w: bf16 [N, K]; out wq [N, K*b/32], scales and biases bf16 [N, K/G]. */
+/* w: bf16 [N, K]; out wq [N, K*b/32], scales and biases bf16 [N, K/G];
+ * widths that divide 32 (u2, u4, u8). */
 int orc_quantize_affine(const uint16_t *w, int64_t N, int64_t K, int bits,
                         int group, uint32_t *wq, uint16_t *scales,
                         uint16_t *biases) {
-    if (!shape_ok(N, K, bits, group)) return ORC_BAD_ARG;
+    if (!shape_ok(N, K, bits, group) || 32 % bits != 0) return ORC_BAD_ARG;
     const int64_t gpr = K / group, wpr = K * bits / 32;
     const int per_word = 32 / bits;
     const uint32_t qmax = (1u << bits) - 1u;

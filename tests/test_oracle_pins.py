@@ -33,6 +33,23 @@ def word_of_fields(codes, bits: int) -> int:
     return int("".join(format(int(c), f"0{bits}b") for c in reversed(codes)), 2)
 
 
+def fields_of_row(words, bits: int, K: int):
+    """Codes of one packed row via the binary string of its whole bit
+    stream (word 0 holds stream bits 0..31): code k is stream bits
+    [bits*k, bits*k + bits).  Covers widths that straddle words (u3, u6)."""
+    s = "".join(format(int(w), "032b") for w in reversed(list(words)))
+    L = len(s)                                       # s[L-1] is stream bit 0
+    return [int(s[L - bits * (k + 1):L - bits * k], 2) for k in range(K)]
+
+
+def row_of_fields(codes, bits: int):
+    """Inverse of fields_of_row: the row's words, again through a string."""
+    s = "".join(format(int(c), f"0{bits}b") for c in reversed(list(codes)))
+    assert len(s) % 32 == 0
+    return [int(s[len(s) - 32 * (j + 1):len(s) - 32 * j], 2)
+            for j in range(len(s) // 32)]
+
+
 def bf16_fraction(h: int) -> Fraction:
     """Exact value of a bf16 bit pattern from its fields."""
     h = int(h)
@@ -48,12 +65,10 @@ def bf16_fraction(h: int) -> Fraction:
 def exact_qmv(x, w: synth.QWeight):
     """y[m, n] as exact rationals, from bit strings and field-decoded bf16."""
     M = x.shape[0]
-    P = 32 // w.bits
-    codes = [[c for word in w.wq[n] for c in fields_of_word(word, w.bits)]
-             for n in range(w.N)]
+    codes = [fields_of_row(w.wq[n], w.bits, w.K) for n in range(w.N)]
     y = [[Fraction(0)] * w.N for _ in range(M)]
     for n in range(w.N):
-        assert len(codes[n]) == w.K and w.wq.shape[1] * P == w.K
+        assert len(codes[n]) == w.K and w.wq.shape[1] * 32 == w.K * w.bits
         for m in range(M):
             acc = Fraction(0)
             for k in range(w.K):
@@ -127,9 +142,45 @@ def test_dequant_closed_form_and_identity_case():
     assert np.array_equal(got, codes.astype(np.float64))
 
 
+def test_unpack_straddling_codes_literal_words():
+    """u3 code 10 occupies stream bits 30..32 and u6 code 5 bits 30..35: a
+    code of all ones there sets the top two bits of word 0 and the lowest
+    one (u3) or four (u6) bits of word 1, worked by hand."""
+    for bits, k, w0, w1 in [(3, 10, 0xC0000000, 0x00000001),
+                            (6, 5, 0xC0000000, 0x0000000F)]:
+        K = 32
+        words = np.zeros((1, K * bits // 32), np.uint32)
+        words[0, 0], words[0, 1] = w0, w1
+        want = [0] * K
+        want[k] = (1 << bits) - 1
+        assert list(oracle.unpack(words, 1, K, bits)[0]) == want
+    # u3 codes 0..7 in order: 0b111_110_101_100_011_010_001_000 = 0xFAC688
+    words = np.zeros((1, 3), np.uint32)
+    words[0, 0] = 0x00FAC688
+    assert list(oracle.unpack(words, 1, 32, 3)[0][:8]) == list(range(8))
+
+
+@pytest.mark.parametrize("bits", [3, 6])
+def test_unpack_roundtrip_straddling_widths(bits):
+    """Every code value at every position of a 32-code row (3 or 6 words),
+    packed through a bit string; and random rows read back by slicing."""
+    K, levels = 32, 1 << bits
+    rows = [[(v + k) % levels for k in range(K)] for v in range(levels)]
+    words = np.array([row_of_fields(r, bits) for r in rows], np.uint32)
+    got = oracle.unpack(words, len(rows), K, bits)
+    assert np.array_equal(got, np.array(rows))
+    r = np.random.default_rng(bits).integers(0, 2**32, size=(5, 3 * 4 * bits // 4),
+                                             dtype=np.uint64).astype(np.uint32)
+    Kr = r.shape[1] * 32 // bits
+    got = oracle.unpack(r, 5, Kr, bits)
+    want = [fields_of_row(row, bits, Kr) for row in r]
+    assert np.array_equal(got, np.array(want))
+
+
 # ---------------------------------------------------------------- qmv
 @pytest.mark.parametrize("bits,group", [(4, 64), (8, 64), (2, 64), (4, 32),
-                                        (4, 128), (2, 32), (8, 128)])
+                                        (4, 128), (2, 32), (8, 128), (3, 64),
+                                        (6, 64), (3, 32), (6, 128)])
 def test_qmv_matches_exact_rational_bruteforce(bits, group):
     M, N, K = 2, 5, 384            # several groups; N != K catches transposes
     w = synth.qweight(21 + bits + group, N, K, bits, group)
@@ -352,11 +403,8 @@ def test_bits_per_weight_matches_printed_table():
     # the oracle consumes, per weight, must equal the printed bpw.
     for quant, bits, bpw in _rows("bpw_table.txt"):
         bits, bpw = int(bits), float(bpw)
-        if 32 % bits:          # u3/u6 do not tile a 32-bit word evenly
-            per_weight = bits + 2 * 16 / 64
-        else:
-            w = synth.qweight(1, 4, 256, bits)
-            per_weight = 8 * w.nbytes / (4 * 256)
+        w = synth.qweight(1, 4, 256, bits)
+        per_weight = 8 * w.nbytes / (4 * 256)
         assert per_weight == bpw, quant
 
 
