@@ -554,7 +554,7 @@ def run_rope_extra(W, dev, steps, warmup, tokens=(1, 4, 512),
 
 
 def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
-                      formats=((2, 64), (4, 32), (4, 128))):
+                      formats=((2, 64), (3, 64), (6, 64), (4, 32), (4, 128))):
     """The gate+up shape (27648 x 5120, one token, SiLU epilogue) in code
     widths and group sizes outside the tuned kernels: the general-format
     decode kernel, eight back-to-back launches over distinct weights so

@@ -208,7 +208,7 @@ def _check_weight(w: QWeight, copies: int = 1) -> None:
     """The library cannot see buffer sizes: refuse tensors whose sizes do not
     match (N, K, bits, group), so a wrong shape raises instead of reading
     past the end of a buffer.  `copies` = number of stacked experts."""
-    if w.bits not in (2, 4, 8) or w.group <= 0 or w.K % w.group:
+    if w.bits not in (2, 3, 4, 6, 8) or w.group <= 0 or w.K % w.group:
         return                                   # the C ABI reports these
     words = copies * w.N * w.K * w.bits // 32
     groups = copies * w.N * (w.K // w.group)

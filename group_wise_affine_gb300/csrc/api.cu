@@ -151,8 +151,8 @@ static bool tuned_format(int bits, int group) {
 }
 
 static int check_qweight(const gwa_qweight &w, const char *fn) {
-    if (w.bits != 2 && w.bits != 4 && w.bits != 8)
-        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 2, 4, 8)",
+    if (w.bits != 2 && w.bits != 3 && w.bits != 4 && w.bits != 6 && w.bits != 8)
+        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 2, 3, 4, 6, 8)",
                     fn, (int)w.bits);
     if (w.group != 32 && w.group != 64 && w.group != 128)
         return fail(GWA_ERR_UNSUPPORTED,

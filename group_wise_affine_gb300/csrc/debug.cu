@@ -8,37 +8,43 @@
 
 namespace gwa {
 
-__global__ void debug_unpack_kernel(const uint32_t *__restrict__ wq,
-                                    int64_t words, int bits,
+// Code k of a row: bits [b*k, b*k + b) of the row's little-endian bit
+// stream (a u3 or u6 code may take the top bits of one word and the bottom
+// bits of the next; the next word is read only then).
+__device__ __forceinline__ uint32_t row_code(const uint32_t *row, int64_t k,
+                                             int bits) {
+    const int64_t pos = (int64_t)bits * k;
+    const int sh = (int)(pos & 31);
+    const uint32_t lo = row[pos >> 5];
+    const uint32_t v = sh + bits <= 32 ? lo >> sh
+                                       : __funnelshift_r(lo, row[(pos >> 5) + 1], sh);
+    return v & ((1u << bits) - 1u);
+}
+
+// One thread per code.
+__global__ void debug_unpack_kernel(const uint32_t *__restrict__ wq, int64_t N,
+                                    int64_t K, int bits,
                                     uint8_t *__restrict__ codes) {
-    const int per = 32 / bits;
-    const uint32_t mask = (1u << bits) - 1u;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
+    const int64_t wpr = K * bits / 32;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N * K;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t w = wq[i];
-        for (int j = 0; j < per; ++j)
-            codes[i * per + j] = (uint8_t)((w >> (bits * j)) & mask);
+        const int64_t n = i / K, k = i - n * K;
+        codes[i] = (uint8_t)row_code(wq + n * wpr, k, bits);
     }
 }
 
 __global__ void debug_dequant_kernel(const uint32_t *__restrict__ wq,
                                      const uint16_t *__restrict__ sc,
-                                     const uint16_t *__restrict__ bi,
-                                     int64_t words, int64_t words_per_row,
-                                     int64_t G, int group, int bits,
+                                     const uint16_t *__restrict__ bi, int64_t N,
+                                     int64_t K, int group, int bits,
                                      float *__restrict__ wf) {
-    const int per = 32 / bits;
-    const uint32_t mask = (1u << bits) - 1u;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
+    const int64_t wpr = K * bits / 32, G = K / group;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N * K;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i / words_per_row, wi = i - n * words_per_row;
-        const uint32_t w = wq[i];
-        for (int j = 0; j < per; ++j) {
-            const int64_t k = wi * per + j;
-            const float s = bf16_bits_to_f32(sc[n * G + k / group]);
-            const float b = bf16_bits_to_f32(bi[n * G + k / group]);
-            wf[i * per + j] = fmaf(s, (float)((w >> (bits * j)) & mask), b);
-        }
+        const int64_t n = i / K, k = i - n * K;
+        const float s = bf16_bits_to_f32(sc[n * G + k / group]);
+        const float b = bf16_bits_to_f32(bi[n * G + k / group]);
+        wf[i] = fmaf(s, (float)row_code(wq + n * wpr, k, bits), b);
     }
 }
 
@@ -51,8 +57,7 @@ static unsigned grid_for(int64_t n, int threads) {
 
 cudaError_t launch_debug_unpack(const uint32_t *wq, int64_t N, int64_t K,
                                 int bits, uint8_t *codes, cudaStream_t st) {
-    const int64_t words = N * K * bits / 32;
-    debug_unpack_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, words, bits,
+    debug_unpack_kernel<<<grid_for(N * K, 256), 256, 0, st>>>(wq, N, K, bits,
                                                               codes);
     return cudaGetLastError();
 }
@@ -61,9 +66,8 @@ cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
                                  const uint16_t *bi, int64_t N, int64_t K,
                                  int bits, int group, float *wf,
                                  cudaStream_t st) {
-    const int64_t words = N * K * bits / 32;
-    debug_dequant_kernel<<<grid_for(words, 256), 256, 0, st>>>(
-        wq, sc, bi, words, K * bits / 32, K / group, group, bits, wf);
+    debug_dequant_kernel<<<grid_for(N * K, 256), 256, 0, st>>>(wq, sc, bi, N, K,
+                                                               group, bits, wf);
     return cudaGetLastError();
 }
 

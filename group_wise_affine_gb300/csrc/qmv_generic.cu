@@ -1,19 +1,24 @@
 // Decode kernel for the code widths and group sizes outside the tuned ones
-// (u4/u8 at group 64): u2, u4, u8 codes with groups of 32, 64 or 128 inputs
-// ("saragossa", "Quantization formats": MLX affine integer weights at
-// several widths; the group size is a parameter of MLX's quantized_matmul).
-// Same packed format: P = 32/b codes per word along the input axis, lowest
-// bits first; one bf16 scale and bias per group; w = scale * q + bias.
+// (u4/u8 at group 64): u2, u3, u4, u6, u8 codes with groups of 32, 64 or
+// 128 inputs ("saragossa", "Quantization formats": MLX affine integer
+// weights u2/u3/u4/u6/u8; the group size is a parameter of MLX's
+// quantized_matmul).  Same packed format: a row's words are one
+// little-endian bit stream, code k at bits [b*k, b*k + b), lowest bits
+// first (field k mod 32/b of word k*b/32 for the widths that divide 32; a
+// u3 or u6 code may straddle two words); one bf16 scale and bias per group;
+// w = scale * q + bias.
 //
 // One warp per output unit (a row, or a gate/up or rotary pair of rows):
-// the lanes stride over the row's 32-bit words (a word never spans two
-// groups, since every group is a multiple of P codes), form each weight in
-// fp32 and accumulate its products with up to four tokens, reading the
-// activations straight from global memory (a few KB, cached in L1 and L2
-// across all rows; a word's activations are one 8-32-byte read per token).
-// A warp reduction and the same epilogues as the tuned kernels (plain,
-// sections with bias, SiLU(gate) * up, rotary pairs) finish it.  It trades
-// speed for generality: about four instructions per code and token.
+// the lanes stride over the row in code units -- one word (32/b codes) for
+// the widths that divide 32, three words (96 bits: 32 u3 or 16 u6 codes)
+// for the others -- so a unit never spans two groups and starts on a code
+// boundary.  Each lane forms its unit's weights in fp32 (a straddling code
+// by a funnel shift of two words) and accumulates their products with up to
+// four tokens, reading the activations straight from global memory (a few
+// KB, cached in L1 and L2 across all rows).  A warp reduction and the same
+// epilogues as the tuned kernels (plain, sections with bias, SiLU(gate) *
+// up, rotary pairs) finish it.  It trades speed for generality: about four
+// instructions per code and token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,16 +27,32 @@ namespace gwa {
 constexpr int kGenTokens = 4;   // tokens per pass
 constexpr int kGenThreads = 256;
 
+// Words per code unit and codes per unit of a width.
+template <int BITS>
+struct GenUnit {
+    static constexpr int kWords = 32 % BITS == 0 ? 1 : 3;
+    static constexpr int kCodes = 32 * kWords / BITS;
+};
+
+// Code c of a unit held in w[0 .. kWords): stream bits [BITS*c, +BITS).
+template <int BITS>
+__device__ __forceinline__ uint32_t unit_code(const uint32_t (&w)[GenUnit<BITS>::kWords],
+                                              int c) {
+    const int pos = BITS * c, i = pos >> 5, sh = pos & 31;
+    const uint32_t v = sh + BITS <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1], sh);
+    return v & ((1u << BITS) - 1u);
+}
+
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(kGenThreads)
     qmv_generic_kernel(DenseParams p, int64_t units) {
-    constexpr int P = 32 / BITS;
-    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    constexpr int UW = GenUnit<BITS>::kWords, CU = GenUnit<BITS>::kCodes;
     constexpr bool PAIRS = MODE == 2 || MODE == 3;
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
-    const int64_t wpr = (int64_t)p.K / P;  // words per row
+    const int64_t wpr = (int64_t)p.K * BITS / 32;  // words per row
+    const int64_t upr = wpr / UW;                  // code units per row
     const int64_t I = p.N / 2;
     const int gshift = __ffs(p.group) - 1;  // groups are 32, 64 or 128
     if (threadIdx.x == 0) pdl_launch_dependents();
@@ -57,46 +78,60 @@ __global__ void __launch_bounds__(kGenThreads)
             const uint32_t *wrow = p.wq + rows[h] * wpr;
             const uint16_t *srow = p.sc + rows[h] * p.G;
             const uint16_t *brow = p.bi + rows[h] * p.G;
-            // a lane takes words wi, wi + 32, wi + 64, wi + 96 per step: four
-            // loads in flight, each a contiguous 128 bytes across the warp,
-            // and the activations of consecutive lanes stay contiguous too
-            // (rows are whole multiples of 128 words when K % 512 == 0;
-            // shorter tails are masked)
-            for (int64_t w0 = 0; w0 < wpr; w0 += 4 * kWarp) {
-                uint32_t words[4];
+            // a lane takes units ui, ui + 32, ui + 64, ui + 96 per step: four
+            // loads (of UW words) in flight, consecutive lanes on consecutive
+            // units, and the activations of consecutive lanes contiguous
+            // (shorter tails are masked)
+            for (int64_t u0 = 0; u0 < upr; u0 += 4 * kWarp) {
+                uint32_t words[4][UW];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const int64_t wi = w0 + q4 * kWarp + lane;
-                    words[q4] = wi < wpr ? wrow[wi] : 0u;
+                    const int64_t ui = u0 + q4 * kWarp + lane;
+#pragma unroll
+                    for (int j = 0; j < UW; ++j)
+                        words[q4][j] = ui < upr ? wrow[ui * UW + j] : 0u;
                 }
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const int64_t wi = w0 + q4 * kWarp + lane;
-                    if (wi >= wpr) break;
-                    const int64_t k0 = wi * P;
-                    const int g = (int)(k0 >> gshift);  // one group per word
+                    const int64_t ui = u0 + q4 * kWarp + lane;
+                    if (ui >= upr) break;
+                    const int64_t k0 = ui * CU;
+                    const int g = (int)(k0 >> gshift);  // one group per unit
                     const float s = bf16_bits_to_f32(srow[g]);
                     const float b = bf16_bits_to_f32(brow[g]);
-                    float wv[P];
+                    float wv[CU];
 #pragma unroll
-                    for (int c = 0; c < P; ++c) {
+                    for (int c = 0; c < CU; ++c) {
                         // the code as a float: 2^23 + q minus 2^23 (exact)
                         const float q = __uint_as_float(
-                            0x4b000000u | ((words[q4] >> (BITS * c)) & MASK)) -
-                                        8388608.0f;
+                            0x4b000000u | unit_code<BITS>(words[q4], c)) - 8388608.0f;
                         wv[c] = fmaf(s, q, b);
                     }
 #pragma unroll
                     for (int m = 0; m < kGenTokens; ++m) {
                         if (m >= p.M) break;
-                        // the word's P activations of token m (2P bytes)
-                        const uint32_t *xw = reinterpret_cast<const uint32_t *>(
-                            p.x + (int64_t)m * p.K + k0);
+                        // the unit's CU activations of token m (2 CU bytes)
+                        const uint16_t *xm = p.x + (int64_t)m * p.K + k0;
+                        if constexpr (CU % 8 == 0) {
 #pragma unroll
-                        for (int c2 = 0; c2 < P / 2; ++c2) {
-                            const uint32_t pr = xw[c2];
-                            acc[h][m] = fmaf(wv[2 * c2], bf16_lo(pr), acc[h][m]);
-                            acc[h][m] = fmaf(wv[2 * c2 + 1], bf16_hi(pr), acc[h][m]);
+                            for (int c8 = 0; c8 < CU / 8; ++c8) {
+                                const uint4 v = reinterpret_cast<const uint4 *>(xm)[c8];
+                                const uint32_t pr[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    acc[h][m] = fmaf(wv[8 * c8 + 2 * e], bf16_lo(pr[e]), acc[h][m]);
+                                    acc[h][m] = fmaf(wv[8 * c8 + 2 * e + 1], bf16_hi(pr[e]),
+                                                     acc[h][m]);
+                                }
+                            }
+                        } else {
+                            const uint32_t *xw = reinterpret_cast<const uint32_t *>(xm);
+#pragma unroll
+                            for (int c2 = 0; c2 < CU / 2; ++c2) {
+                                const uint32_t pr = xw[c2];
+                                acc[h][m] = fmaf(wv[2 * c2], bf16_lo(pr), acc[h][m]);
+                                acc[h][m] = fmaf(wv[2 * c2 + 1], bf16_hi(pr), acc[h][m]);
+                            }
                         }
                     }
                 }
@@ -169,9 +204,14 @@ static cudaError_t launch_generic_b(int mode, const DenseParams &p,
 // `mode` as the other decode kernels (0 plain, 1 sections, 2 gate+up, 3
 // sections with the rotary embedding from p.rope_cs).
 cudaError_t launch_generic(int mode, const DenseParams &p, cudaStream_t st) {
-    return p.bits == 2   ? launch_generic_b<2>(mode, p, st)
-           : p.bits == 4 ? launch_generic_b<4>(mode, p, st)
-                         : launch_generic_b<8>(mode, p, st);
+    switch (p.bits) {
+        case 2: return launch_generic_b<2>(mode, p, st);
+        case 3: return launch_generic_b<3>(mode, p, st);
+        case 4: return launch_generic_b<4>(mode, p, st);
+        case 6: return launch_generic_b<6>(mode, p, st);
+        case 8: return launch_generic_b<8>(mode, p, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 int generic_max_tokens() { return kGenTokens; }

@@ -3,13 +3,15 @@
  * one NVIDIA GB300 (sm_103a).
  *
  * The operation (MLX-style affine integer weights):
- *   code   q[n,k] = (Wq[n, k/P] >> (b*(k mod P))) & (2^b - 1),  P = 32/b
+ *   code   q[n,k] = bits [b*k, b*k + b) of row n's little-endian bit stream
+ *          (word j holds stream bits [32j, 32j + 32)); for b dividing 32
+ *          that is (Wq[n, k/P] >> (b*(k mod P))) & (2^b - 1),  P = 32/b
  *   weight w[n,k] = scale[n, k/64] * q[n,k] + bias[n, k/64]
  *   output y[m,n] = sum_k x[m,k] * w[n,k]   (fp32 accumulation, bf16 out)
  * Defined by: "Sanctum-MLX", server diagram and model parameter table
  * (4-bit QuantizedLinear, group_size=64); "saragossa", "Quantization
- * formats" (MLX affine u4/u8, group size 64, bf16 scales/biases, ~4.5 and
- * ~8.5 bits per weight); "The Cathedral Doubled Itself", "The two fusions"
+ * formats" (MLX affine u2/u3/u4/u6/u8, group size 64, bf16 scales/biases,
+ * u3 ~3.5, u4 ~4.5, u6 ~6.5, u8 ~8.5 bits per weight); "The Cathedral Doubled Itself", "The two fusions"
  * (packed weight [rows, hidden/8] uint32 for 4-bit codes, codes packed along
  * the input axis).  Inside a word the first code sits in the lowest bits.
  *
@@ -23,7 +25,7 @@
  *   - All matrices are row-major and contiguous.  x is [M, K].
  *   - Wq, x and the workspace must be 16-byte aligned; scales, biases and
  *     outputs 2-byte aligned.  K must be a multiple of 64.
- *   - bits is 4 or 8; group must be 64.
+ *   - bits is 2, 3, 4, 6 or 8; group 32, 64 or 128 (see gwa_qweight).
  *   - M <= 8 runs the decode (GEMV) kernels on the CUDA cores and needs no
  *     workspace (pass NULL, 0).  M > 8 needs `gwa_workspace_bytes(M, K)`
  *     bytes of device workspace, which the call overwrites; calls sharing one
@@ -50,7 +52,7 @@ extern "C" {
 enum {
     GWA_OK = 0,
     GWA_ERR_INVALID_ARG = 1, /* null pointer, bad size, sizes not adding up */
-    GWA_ERR_UNSUPPORTED = 2, /* bits not in {2,4,8}, group not in
+    GWA_ERR_UNSUPPORTED = 2, /* bits not in {2,3,4,6,8}, group not in
                                 {32,64,128}; or a format an entry point does
                                 not take (experts, quantization: u4/u8 at
                                 group 64)                                  */
@@ -61,12 +63,14 @@ enum {
 
 /* One packed weight of N output rows and K inputs (K a multiple of 64 and
  * of the group).
- *   wq:     uint32 [N, K*bits/32]: 32/bits codes per word along the input
- *           axis, lowest bits first
+ *   wq:     uint32 [N, K*bits/32]: the row's codes along the input axis as
+ *           one little-endian bit stream, lowest bits first (32/bits per
+ *           word for u2/u4/u8; u3 and u6 codes may straddle two words)
  *   scales: bf16   [N, K/group]
  *   biases: bf16   [N, K/group]
- * bits 4 or 8 with group 64 run the tuned kernels; bits 2, 4, 8 with groups
- * of 32 or 128 (and u2 at 64) run a general decode kernel for the dense
+ * bits 4 or 8 with group 64 run the tuned kernels; every other width and
+ * group (u2, u3, u6 at any group; u4, u8 at 32 or 128) runs a general decode
+ * kernel for the dense
  * projections (all of gwa_qmv_affine, gwa_qmv_fused_sections,
  * gwa_qmv_gate_up_silu, gwa_qmv_qkv_rope, the debug exports); the experts
  * and the quantization take u4/u8 at group 64 only.                      */

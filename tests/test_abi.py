@@ -52,7 +52,7 @@ def _qw(gwa, bits=4, group=64, N=16, K=128, wq=0x1000, sc=0x2000, bi=0x3000):
 
 @needs_nvcc
 @pytest.mark.parametrize("kw,code", [
-    (dict(bits=3), 2), (dict(bits=6), 2), (dict(group=48), 2),
+    (dict(bits=5), 2), (dict(bits=7), 2), (dict(group=48), 2),
     (dict(group=256), 2),
     (dict(K=100), 1), (dict(K=0), 1), (dict(N=-1), 1),
     (dict(wq=0x1004), 3), (dict(sc=0x2001), 3),

@@ -208,7 +208,7 @@ def test_empty_inputs_are_no_ops():
 def test_bad_arguments_raise_status_not_fault():
     w = dev_qweight(synth.qweight(601, 16, 128, 4))
     x = dev_bf16(synth.activations(602, 1, 128))
-    bad = gwa.QWeight(w.wq, w.scales, w.biases, 16, 128, 3, 64)
+    bad = gwa.QWeight(w.wq, w.scales, w.biases, 16, 128, 5, 64)
     with pytest.raises(gwa.GwaError) as e:
         gwa.qmv_affine(x, bad)
     assert e.value.code == gwa.GWA_ERR_UNSUPPORTED

@@ -1,8 +1,9 @@
 """GPU parity of the code widths and group sizes outside the tuned kernels
-(u2, and groups of 32 and 128 at every width), which run on the
-general-format decode kernel, against the oracle (same packed format:
-32/b codes per word, lowest bits first, one bf16 scale and bias per group;
-"saragossa", "Quantization formats").
+(u2, u3, u6, and groups of 32 and 128 at every width), which run on the
+general-format decode kernel, against the oracle (same packed format: a
+row's words are one little-endian bit stream, code k at bits [b*k, +b),
+lowest bits first, so u3 and u6 codes straddle words; one bf16 scale and
+bias per group; "saragossa", "Quantization formats").
 
 Bars as for the tuned formats: unpacked codes and dequantized values bit
 for bit; outputs within |err| <= 1e-2 * max(1, |ref|).
@@ -18,7 +19,8 @@ from helpers import dev_bf16, dev_qweight
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
-FORMATS = [(2, 32), (2, 64), (2, 128), (4, 32), (4, 128), (8, 32), (8, 128)]
+FORMATS = [(2, 32), (2, 64), (2, 128), (4, 32), (4, 128), (8, 32), (8, 128),
+           (3, 32), (3, 64), (3, 128), (6, 32), (6, 64), (6, 128)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,7 +61,8 @@ def test_plain_projection(bits, group, M):
           f"u{bits} g{group} M={M}")
 
 
-@pytest.mark.parametrize("bits,group", [(2, 32), (4, 128), (8, 32)])
+@pytest.mark.parametrize("bits,group", [(2, 32), (4, 128), (8, 32), (3, 64),
+                                        (6, 64)])
 def test_sections_gate_up_and_rope(bits, group):
     K, M = 512, 2
     rng = np.random.default_rng(bits + group)
