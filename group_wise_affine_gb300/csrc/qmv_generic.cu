@@ -43,6 +43,61 @@ __device__ __forceinline__ uint32_t unit_code(const uint32_t (&w)[GenUnit<BITS>:
     return v & ((1u << BITS) - 1u);
 }
 
+// Warp reduction of the per-lane sums and the epilogue of one output unit:
+// plain, sections with bias, SiLU(gate) * up, or sections with the rotary
+// embedding from p.rope_cs; lane m writes token m.
+template <int MODE>
+__device__ __forceinline__ void gen_finish(const DenseParams &p, int64_t u,
+                                           const int64_t (&rows)[2],
+                                           float (&acc)[2][kGenTokens], int lane) {
+    const int64_t I = p.N / 2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int m = 0; m < kGenTokens; ++m)
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                acc[h][m] += __shfl_xor_sync(0xffffffffu, acc[h][m], o);
+    if (lane >= kGenTokens || lane >= p.M) return;
+    // lane m writes token m (a compile-time index below)
+#pragma unroll
+    for (int m = 0; m < kGenTokens; ++m) {
+        if (m != lane) continue;
+        if constexpr (MODE == 0) {
+            p.y[(int64_t)m * p.N + u] = f32_to_bf16_bits(acc[0][m]);
+        } else if constexpr (MODE == 2) {
+            const float gv = acc[0][m], uv = acc[1][m];
+            p.y[(int64_t)m * I + u] =
+                f32_to_bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+        } else {
+            const int64_t r0 = rows[0];
+            int s = 0;
+            while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
+            const int64_t j = r0 - p.sec_start[s];
+            const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+            float a = acc[0][m];
+            if (p.sec_bias[s]) a += bf16_bits_to_f32(p.sec_bias[s][j]);
+            if constexpr (MODE == 1) {
+                p.sec_out[s][(int64_t)m * size + j] = f32_to_bf16_bits(a);
+            } else {
+                const int half = p.rope_hd / 2;
+                float c = acc[1][m];
+                if (p.sec_bias[s]) c += bf16_bits_to_f32(p.sec_bias[s][j + half]);
+                if (r0 < p.rope_end) {
+                    const float2 t =
+                        p.rope_cs[(int64_t)m * half + (int)(u % half)];
+                    const float a2 = a * t.x - c * t.y;
+                    c = c * t.x + a * t.y;
+                    a = a2;
+                }
+                uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
+                o[0] = f32_to_bf16_bits(a);
+                o[half] = f32_to_bf16_bits(c);
+            }
+        }
+    }
+}
+
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(kGenThreads)
     qmv_generic_kernel(DenseParams p, int64_t units) {
@@ -137,52 +192,214 @@ __global__ void __launch_bounds__(kGenThreads)
                 }
             }
         }
+        gen_finish<MODE>(p, u, rows, acc, lane);
+    }
+}
+
+// ------------------------------------------------------------ integer dot
+// The same outputs by an exact integer dot, as in the tuned kernels: each
+// block first encodes the pass's activations into shared memory as int16
+// with a power-of-two scale per weight group (the group's largest magnitude
+// maps into [2^14, 2^15)), together with each code unit's plain sum for
+// the bias term; a lane then spreads its unit's codes into bytes and forms
+// sum_k q_k xi_k with dp2a (two 16x8-bit products per instruction), so per
+// unit and token
+//   y += (scale * 2^E) * D + bias * sum_k x_k.
+// Spreading: widths dividing 8 take byte planes of a word (plane i, the
+// word shifted by b*i and masked, holds codes (8/b) j + i in byte j: the
+// activations are stored in that order); u3 and u6 spread each chunk of
+// four codes (12 or 24 bits) into the four bytes of a word with shifts
+// and masks, keeping the natural order.  Eight one-word units (or four
+// three-word units) per lane and step keep 32-48 bytes of codes per lane
+// in flight.
+constexpr int kGdThreads = 512;
+
+template <int BITS>
+struct GdFmt {
+    static constexpr bool kAligned = 32 % BITS == 0;  // u2, u4, u8
+    static constexpr int UW = kAligned ? 1 : 3;       // words per unit
+    static constexpr int CU = 32 * UW / BITS;         // codes per unit
+    static constexpr int SW = CU / 4;                 // byte words per unit
+    static constexpr int US = kAligned ? 8 : 4;       // units per lane, step
+};
+
+// Position of code c of a unit among its activations (dp2a order).
+template <int BITS>
+__device__ __forceinline__ int gd_pos(int c) {
+    return BITS == 2 || BITS == 4 ? 4 * (c % (8 / BITS)) + c / (8 / BITS) : c;
+}
+
+// A unit's codes as SW words of four unsigned bytes, in dp2a order.
+template <int BITS>
+__device__ __forceinline__ void gd_spread(const uint32_t (&w)[GdFmt<BITS>::UW],
+                                          uint32_t (&b)[GdFmt<BITS>::SW]) {
+    constexpr int UW = GdFmt<BITS>::UW, SW = GdFmt<BITS>::SW;
+    if constexpr (BITS == 8) {
+        b[0] = w[0];
+    } else if constexpr (BITS == 4 || BITS == 2) {
+        constexpr uint32_t M = BITS == 4 ? 0x0f0f0f0fu : 0x03030303u;
+#pragma unroll
+        for (int i = 0; i < SW; ++i) b[i] = (w[0] >> (BITS * i)) & M;
+    } else {
+        constexpr int CB = 4 * BITS;  // bits of a chunk of four codes
+#pragma unroll
+        for (int i = 0; i < SW; ++i) {
+            const int pos = CB * i, j = pos >> 5, sh = pos & 31;
+            const uint32_t v = sh + CB <= 32
+                                   ? w[j] >> sh
+                                   : __funnelshift_r(w[j], w[j + 1 < UW ? j + 1 : j], sh);
+            if constexpr (BITS == 6)
+                b[i] = (v & 0x3fu) | ((v << 2) & 0x3f00u) | ((v << 4) & 0x3f0000u) |
+                       ((v << 6) & 0x3f000000u);
+            else
+                b[i] = (v & 0x7u) | ((v << 5) & 0x700u) | ((v << 10) & 0x70000u) |
+                       ((v << 15) & 0x7000000u);
+        }
+    }
+}
+
+// Shared bytes of one pass's encoded activations.
+template <int BITS>
+static size_t gd_smem_bytes(int M, int64_t K, int group) {
+    const int64_t units = K / GdFmt<BITS>::CU;
+    return (size_t)M * (K * 2 + (K / group) * 4 + units * 4);
+}
+
+template <int BITS, int MODE>
+__global__ void __launch_bounds__(kGdThreads, 2)
+    qmv_gdot_kernel(DenseParams p, int64_t units) {
+    using F = GdFmt<BITS>;
+    constexpr int UW = F::UW, CU = F::CU, SW = F::SW, US = F::US;
+    constexpr bool PAIRS = MODE == 2 || MODE == 3;
+    extern __shared__ __align__(16) unsigned char gd_smem[];
+    const int K = p.K, G = p.G, M = p.M, GS = p.group;
+    const int64_t upr = (int64_t)K / CU;  // code units per row
+    int16_t *xe = reinterpret_cast<int16_t *>(gd_smem);          // [M][K]
+    float *xf = reinterpret_cast<float *>(gd_smem + (size_t)M * K * 2);  // [M][G]
+    float *xu = xf + (size_t)M * G;                               // [M][upr]
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
+    constexpr int kWarps = kGdThreads / kWarp;
+    const int gshift = __ffs(GS) - 1;  // groups are 32, 64 or 128
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    pdl_wait_primary();  // x may be the previous kernel's output
+
+    // encode: one warp per (token, group); lane takes inputs lane + 32r
+    for (int task = warp; task < M * G; task += kWarps) {
+        const int m = task / G, g = task - m * G;
+        const uint16_t *xg = p.x + (int64_t)m * K + (int64_t)g * GS;
+        float v[4];
+        int ef = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            v[r] = r * kWarp < GS ? bf16_bits_to_f32(xg[r * kWarp + lane]) : 0.f;
+            ef = max(ef, f32_exp_field(v[r]));
+        }
+        ef = __reduce_max_sync(0xffffffffu, ef);
+        float f, finv;
+        group_scale(ef, f, finv);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if (r * kWarp >= GS) break;
+            const int k = g * GS + r * kWarp + lane;
+            const int ui = k / CU, c = k - ui * CU;
+            xe[(int64_t)m * K + ui * CU + gd_pos<BITS>(c)] =
+                (int16_t)__float2int_rn(v[r] * finv);
+            float sum = v[r];  // the unit's plain sum: CU consecutive lanes
+#pragma unroll
+            for (int o = 1; o < CU; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if ((lane & (CU - 1)) == 0) xu[(int64_t)m * upr + ui] = sum;
+        }
+        if (lane == 0) xf[(int64_t)m * G + g] = f;
+    }
+    __syncthreads();
+
+    const int64_t I = p.N / 2;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    const int64_t nw = (int64_t)gridDim.x * blockDim.x / kWarp;
+    const int64_t wpr = (int64_t)K * BITS / 32;
+    for (int64_t u = gw; u < units; u += nw) {
+        int64_t rows[2];
+        if (MODE == 2) {
+            rows[0] = u;
+            rows[1] = I + u;
+        } else if (MODE == 3) {
+            rows[0] = rope_pair_row(u, 0, p.rope_hd);
+            rows[1] = rope_pair_row(u, 1, p.rope_hd);
+        } else {
+            rows[0] = rows[1] = u;
+        }
+        float acc[2][kGenTokens];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int m = 0; m < kGenTokens; ++m)
+            for (int m = 0; m < kGenTokens; ++m) acc[h][m] = 0.f;
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1)
-                    acc[h][m] += __shfl_xor_sync(0xffffffffu, acc[h][m], o);
-        if (lane >= kGenTokens || lane >= p.M) continue;
-        // lane m writes token m (a compile-time index below)
+        for (int h = 0; h < (PAIRS ? 2 : 1); ++h) {
+            const uint32_t *wrow = p.wq + rows[h] * wpr;
+            const uint16_t *srow = p.sc + rows[h] * G;
+            const uint16_t *brow = p.bi + rows[h] * G;
+            for (int64_t u0 = 0; u0 < upr; u0 += US * kWarp) {
+                uint32_t words[US][UW];
 #pragma unroll
-        for (int m = 0; m < kGenTokens; ++m) {
-            if (m != lane) continue;
-            if constexpr (MODE == 0) {
-                p.y[(int64_t)m * p.N + u] = f32_to_bf16_bits(acc[0][m]);
-            } else if constexpr (MODE == 2) {
-                const float gv = acc[0][m], uv = acc[1][m];
-                p.y[(int64_t)m * I + u] =
-                    f32_to_bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
-            } else {
-                const int64_t r0 = rows[0];
-                int s = 0;
-                while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
-                const int64_t j = r0 - p.sec_start[s];
-                const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
-                float a = acc[0][m];
-                if (p.sec_bias[s]) a += bf16_bits_to_f32(p.sec_bias[s][j]);
-                if constexpr (MODE == 1) {
-                    p.sec_out[s][(int64_t)m * size + j] = f32_to_bf16_bits(a);
-                } else {
-                    const int half = p.rope_hd / 2;
-                    float c = acc[1][m];
-                    if (p.sec_bias[s]) c += bf16_bits_to_f32(p.sec_bias[s][j + half]);
-                    if (r0 < p.rope_end) {
-                        const float2 t =
-                            p.rope_cs[(int64_t)m * half + (int)(u % half)];
-                        const float a2 = a * t.x - c * t.y;
-                        c = c * t.x + a * t.y;
-                        a = a2;
+                for (int q = 0; q < US; ++q) {
+                    const int64_t ui = u0 + q * kWarp + lane;
+#pragma unroll
+                    for (int j = 0; j < UW; ++j)
+                        words[q][j] = ui < upr ? wrow[ui * UW + j] : 0u;
+                }
+#pragma unroll
+                for (int q = 0; q < US; ++q) {
+                    const int64_t ui = u0 + q * kWarp + lane;
+                    if (ui >= upr) break;
+                    const int k0 = (int)ui * CU;
+                    const int g = k0 >> gshift;  // one group per unit
+                    const float sc = bf16_bits_to_f32(srow[g]);
+                    const float bi = bf16_bits_to_f32(brow[g]);
+                    uint32_t bw[SW];
+                    gd_spread<BITS>(words[q], bw);
+#pragma unroll
+                    for (int m = 0; m < kGenTokens; ++m) {
+                        if (m >= M) break;
+                        const int16_t *xm = xe + (int64_t)m * K + k0;
+                        int d = 0;
+                        if constexpr (SW == 1) {
+                            const uint2 xp = *reinterpret_cast<const uint2 *>(xm);
+                            d = dp2a_hi(xp.y, bw[0], dp2a_lo(xp.x, bw[0], d));
+                        } else {
+#pragma unroll
+                            for (int s2 = 0; s2 < SW; s2 += 2) {
+                                const uint4 xp =
+                                    *reinterpret_cast<const uint4 *>(xm + 4 * s2);
+                                d = dp2a_hi(xp.y, bw[s2], dp2a_lo(xp.x, bw[s2], d));
+                                d = dp2a_hi(xp.w, bw[s2 + 1], dp2a_lo(xp.z, bw[s2 + 1], d));
+                            }
+                        }
+                        acc[h][m] = fmaf(sc * xf[(int64_t)m * G + g], (float)d,
+                                         fmaf(bi, xu[(int64_t)m * upr + ui], acc[h][m]));
                     }
-                    uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
-                    o[0] = f32_to_bf16_bits(a);
-                    o[half] = f32_to_bf16_bits(c);
                 }
             }
         }
+        gen_finish<MODE>(p, u, rows, acc, lane);
     }
+}
+
+template <int BITS>
+static cudaError_t launch_gdot_b(int mode, const DenseParams &p,
+                                 cudaStream_t st) {
+    const int64_t units = mode == 2 || mode == 3 ? p.N / 2 : p.N;
+    if (units <= 0) return cudaSuccess;
+    const void *k = mode == 0   ? reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 0>)
+                    : mode == 1 ? reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 1>)
+                    : mode == 2 ? reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 2>)
+                                : reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 3>);
+    const size_t smem = gd_smem_bytes<BITS>(p.M, p.K, p.group);
+    int grid = 0;
+    cudaError_t e = occupancy_grid(k, kGdThreads, smem, &grid);
+    if (e != cudaSuccess) return e;
+    const int64_t need = (units + kGdThreads / kWarp - 1) / (kGdThreads / kWarp);
+    if (grid > need) grid = (int)need;
+    return launch_pdl(k, (unsigned)grid, (unsigned)kGdThreads, smem, st, p, units);
 }
 
 template <int BITS>
@@ -203,13 +420,25 @@ static cudaError_t launch_generic_b(int mode, const DenseParams &p,
 // Runs the general-format kernel over passes of up to kGenTokens tokens;
 // `mode` as the other decode kernels (0 plain, 1 sections, 2 gate+up, 3
 // sections with the rotary embedding from p.rope_cs).
+// The integer-dot kernel when the pass's encoded activations fit in shared
+// memory (K up to ~16K inputs at four tokens), else the fp32 kernel.
+constexpr size_t kGdMaxSmem = 200 * 1024;
+
+template <int BITS>
+static cudaError_t launch_generic_w(int mode, const DenseParams &p,
+                                    cudaStream_t st) {
+    if (gd_smem_bytes<BITS>(p.M, p.K, p.group) <= kGdMaxSmem)
+        return launch_gdot_b<BITS>(mode, p, st);
+    return launch_generic_b<BITS>(mode, p, st);
+}
+
 cudaError_t launch_generic(int mode, const DenseParams &p, cudaStream_t st) {
     switch (p.bits) {
-        case 2: return launch_generic_b<2>(mode, p, st);
-        case 3: return launch_generic_b<3>(mode, p, st);
-        case 4: return launch_generic_b<4>(mode, p, st);
-        case 6: return launch_generic_b<6>(mode, p, st);
-        case 8: return launch_generic_b<8>(mode, p, st);
+        case 2: return launch_generic_w<2>(mode, p, st);
+        case 3: return launch_generic_w<3>(mode, p, st);
+        case 4: return launch_generic_w<4>(mode, p, st);
+        case 6: return launch_generic_w<6>(mode, p, st);
+        case 8: return launch_generic_w<8>(mode, p, st);
         default: return cudaErrorInvalidValue;
     }
 }
