@@ -200,54 +200,64 @@ __global__ void __launch_bounds__(kGenThreads)
 // The same outputs by an exact integer dot, as in the tuned kernels: each
 // block first encodes the pass's activations into shared memory as int16
 // with a power-of-two scale per weight group (the group's largest magnitude
-// maps into [2^14, 2^15)), together with each code unit's plain sum for
-// the bias term; a lane then spreads its unit's codes into bytes and forms
-// sum_k q_k xi_k with dp2a (two 16x8-bit products per instruction), so per
-// unit and token
+// maps into [2^14, 2^15)), together with the plain sum of every 32
+// activations for the bias term.  A lane takes chunks of 32 codes (a chunk
+// never spans two groups: groups are 32, 64 or 128), spreads the chunk's
+// codes into eight words of four unsigned bytes and forms sum_k q_k xi_k
+// with dp2a (two 16x8-bit products per instruction), so per chunk and token
 //   y += (scale * 2^E) * D + bias * sum_k x_k.
 // Spreading: widths dividing 8 take byte planes of a word (plane i, the
 // word shifted by b*i and masked, holds codes (8/b) j + i in byte j: the
-// activations are stored in that order); u3 and u6 spread each chunk of
-// four codes (12 or 24 bits) into the four bytes of a word with shifts
-// and masks, keeping the natural order.  Eight one-word units (or four
-// three-word units) per lane and step keep 32-48 bytes of codes per lane
-// in flight.
+// activations are stored in that order); u3 and u6 spread each run of four
+// codes (12 or 24 bits) into the four bytes of a word with shifts and
+// masks, keeping the natural order.  Each lane loads 32-64 bytes of codes
+// (and the chunks' scales and biases) per step before using any of them.
 constexpr int kGdThreads = 512;
+constexpr int kGdChunk = 32;  // codes per chunk
 
 template <int BITS>
 struct GdFmt {
-    static constexpr bool kAligned = 32 % BITS == 0;  // u2, u4, u8
-    static constexpr int UW = kAligned ? 1 : 3;       // words per unit
-    static constexpr int CU = 32 * UW / BITS;         // codes per unit
-    static constexpr int SW = CU / 4;                 // byte words per unit
-    static constexpr int US = kAligned ? 8 : 4;       // units per lane, step
+    static constexpr int CW = kGdChunk * BITS / 32;  // words per chunk
+    // chunks per lane and step: 32-64 bytes of codes in flight
+    static constexpr int NQ = BITS == 8 || BITS == 6 ? 2 : 4;
 };
 
-// Position of code c of a unit among its activations (dp2a order).
+// Position of code c of a chunk among its activations (dp2a order): within
+// each word, byte plane by byte plane for u2 and u4; natural otherwise.
 template <int BITS>
 __device__ __forceinline__ int gd_pos(int c) {
-    return BITS == 2 || BITS == 4 ? 4 * (c % (8 / BITS)) + c / (8 / BITS) : c;
+    if constexpr (BITS == 2 || BITS == 4) {
+        constexpr int CPW = 32 / BITS, NP = 8 / BITS;
+        const int w = c / CPW, r = c % CPW;
+        return w * CPW + 4 * (r % NP) + r / NP;
+    } else {
+        return c;
+    }
 }
 
-// A unit's codes as SW words of four unsigned bytes, in dp2a order.
+// A chunk's 32 codes as eight words of four unsigned bytes, in dp2a order.
 template <int BITS>
-__device__ __forceinline__ void gd_spread(const uint32_t (&w)[GdFmt<BITS>::UW],
-                                          uint32_t (&b)[GdFmt<BITS>::SW]) {
-    constexpr int UW = GdFmt<BITS>::UW, SW = GdFmt<BITS>::SW;
+__device__ __forceinline__ void gd_spread(const uint32_t (&w)[GdFmt<BITS>::CW],
+                                          uint32_t (&b)[8]) {
+    constexpr int CW = GdFmt<BITS>::CW;
     if constexpr (BITS == 8) {
-        b[0] = w[0];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = w[i];
     } else if constexpr (BITS == 4 || BITS == 2) {
         constexpr uint32_t M = BITS == 4 ? 0x0f0f0f0fu : 0x03030303u;
+        constexpr int NP = 8 / BITS;
 #pragma unroll
-        for (int i = 0; i < SW; ++i) b[i] = (w[0] >> (BITS * i)) & M;
+        for (int j = 0; j < CW; ++j)
+#pragma unroll
+            for (int i = 0; i < NP; ++i) b[j * NP + i] = (w[j] >> (BITS * i)) & M;
     } else {
-        constexpr int CB = 4 * BITS;  // bits of a chunk of four codes
+        constexpr int CB = 4 * BITS;  // bits of a run of four codes
 #pragma unroll
-        for (int i = 0; i < SW; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const int pos = CB * i, j = pos >> 5, sh = pos & 31;
-            const uint32_t v = sh + CB <= 32
-                                   ? w[j] >> sh
-                                   : __funnelshift_r(w[j], w[j + 1 < UW ? j + 1 : j], sh);
+            const uint32_t v =
+                sh + CB <= 32 ? w[j] >> sh
+                              : __funnelshift_r(w[j], w[j + 1 < CW ? j + 1 : j], sh);
             if constexpr (BITS == 6)
                 b[i] = (v & 0x3fu) | ((v << 2) & 0x3f00u) | ((v << 4) & 0x3f0000u) |
                        ((v << 6) & 0x3f000000u);
@@ -258,65 +268,103 @@ __device__ __forceinline__ void gd_spread(const uint32_t (&w)[GdFmt<BITS>::UW],
     }
 }
 
-// Shared bytes of one pass's encoded activations.
-template <int BITS>
+// Loads a chunk's CW words (byte offset a multiple of 4 * CW) with the
+// widest aligned vectors.
+template <int CW>
+__device__ __forceinline__ void gd_load(const uint32_t *p, uint32_t (&w)[CW]) {
+    if constexpr (CW % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < CW / 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+    } else if constexpr (CW % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < CW / 2; ++i) {
+            const uint2 v = reinterpret_cast<const uint2 *>(p)[i];
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) w[i] = p[i];
+    }
+}
+
+// Shared bytes of one pass's encoded activations: int16 [M][K], the group
+// scales [M][K/group] and the chunk sums [M][K/32].
 static size_t gd_smem_bytes(int M, int64_t K, int group) {
-    const int64_t units = K / GdFmt<BITS>::CU;
-    return (size_t)M * (K * 2 + (K / group) * 4 + units * 4);
+    return (size_t)M * (K * 2 + (K / group) * 4 + (K / kGdChunk) * 4);
 }
 
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(kGdThreads, 2)
     qmv_gdot_kernel(DenseParams p, int64_t units) {
     using F = GdFmt<BITS>;
-    constexpr int UW = F::UW, CU = F::CU, SW = F::SW, US = F::US;
+    constexpr int CW = F::CW, NQ = F::NQ;
     constexpr bool PAIRS = MODE == 2 || MODE == 3;
+    constexpr int kWarps = kGdThreads / kWarp;
+    constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char gd_smem[];
     const int K = p.K, G = p.G, M = p.M, GS = p.group;
-    const int64_t upr = (int64_t)K / CU;  // code units per row
-    int16_t *xe = reinterpret_cast<int16_t *>(gd_smem);          // [M][K]
+    const int nch = K / kGdChunk;  // chunks per row
+    // xe [M][4][nch][8]: the eight activations (dp2a order) of piece s of
+    // chunk c at (s * nch + c) * 8, so lanes on consecutive chunks read
+    // consecutive 16-byte pieces (no bank conflicts)
+    int16_t *xe = reinterpret_cast<int16_t *>(gd_smem);
     float *xf = reinterpret_cast<float *>(gd_smem + (size_t)M * K * 2);  // [M][G]
-    float *xu = xf + (size_t)M * G;                               // [M][upr]
+    float *xu = xf + M * G;                                              // [M][nch]
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
-    constexpr int kWarps = kGdThreads / kWarp;
     const int gshift = __ffs(GS) - 1;  // groups are 32, 64 or 128
     if (threadIdx.x == 0) pdl_launch_dependents();
     pdl_wait_primary();  // x may be the previous kernel's output
 
-    // encode: one warp per (token, group); lane takes inputs lane + 32r
-    for (int task = warp; task < M * G; task += kWarps) {
-        const int m = task / G, g = task - m * G;
-        const uint16_t *xg = p.x + (int64_t)m * K + (int64_t)g * GS;
-        float v[4];
-        int ef = 0;
+    // encode: one warp per (token, group), four groups' loads in flight; the
+    // lane takes inputs lane + 32r of its group, so each r is one chunk
+    const int ntask = M * G, rmax = GS / kWarp;
+    for (int t0 = warp; t0 < ntask; t0 += 4 * kWarps) {
+        float v[4][4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            v[r] = r * kWarp < GS ? bf16_bits_to_f32(xg[r * kWarp + lane]) : 0.f;
-            ef = max(ef, f32_exp_field(v[r]));
+        for (int b = 0; b < 4; ++b) {
+            const int task = t0 + b * kWarps;
+            const int m = task / G, g = task - m * G;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                v[b][r] = task < ntask && r < rmax
+                              ? bf16_bits_to_f32(p.x[m * K + g * GS + r * kWarp + lane])
+                              : 0.f;
         }
-        ef = __reduce_max_sync(0xffffffffu, ef);
-        float f, finv;
-        group_scale(ef, f, finv);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            if (r * kWarp >= GS) break;
-            const int k = g * GS + r * kWarp + lane;
-            const int ui = k / CU, c = k - ui * CU;
-            xe[(int64_t)m * K + ui * CU + gd_pos<BITS>(c)] =
-                (int16_t)__float2int_rn(v[r] * finv);
-            float sum = v[r];  // the unit's plain sum: CU consecutive lanes
+        for (int b = 0; b < 4; ++b) {
+            const int task = t0 + b * kWarps;
+            if (task >= ntask) break;  // the same for every lane
+            const int m = task / G, g = task - m * G;
+            int ef = 0;
 #pragma unroll
-            for (int o = 1; o < CU; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if ((lane & (CU - 1)) == 0) xu[(int64_t)m * upr + ui] = sum;
+            for (int r = 0; r < 4; ++r) ef = max(ef, f32_exp_field(v[b][r]));
+            ef = __reduce_max_sync(FULL, ef);
+            float f, finv;
+            group_scale(ef, f, finv);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r >= rmax) break;
+                const int k0 = g * GS + r * kWarp;  // this r's chunk
+                const int pos = gd_pos<BITS>(lane);
+                xe[m * K + ((pos >> 3) * nch + k0 / kGdChunk) * 8 + (pos & 7)] =
+                    (int16_t)__float2int_rn(v[b][r] * finv);
+                float sum = v[b][r];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+                if (lane == 0) xu[m * nch + k0 / kGdChunk] = sum;
+            }
+            if (lane == 0) xf[m * G + g] = f;
         }
-        if (lane == 0) xf[(int64_t)m * G + g] = f;
     }
     __syncthreads();
 
     const int64_t I = p.N / 2;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nw = (int64_t)gridDim.x * blockDim.x / kWarp;
-    const int64_t wpr = (int64_t)K * BITS / 32;
+    const int wpr = K * BITS / 32;  // words per row
     for (int64_t u = gw; u < units; u += nw) {
         int64_t rows[2];
         if (MODE == 2) {
@@ -338,44 +386,45 @@ __global__ void __launch_bounds__(kGdThreads, 2)
             const uint32_t *wrow = p.wq + rows[h] * wpr;
             const uint16_t *srow = p.sc + rows[h] * G;
             const uint16_t *brow = p.bi + rows[h] * G;
-            for (int64_t u0 = 0; u0 < upr; u0 += US * kWarp) {
-                uint32_t words[US][UW];
+            for (int c0 = 0; c0 < nch; c0 += NQ * kWarp) {
+                // the step's codes, scales and biases (scale | bias << 16),
+                // every load issued before any is used
+                uint32_t words[NQ][CW], sb[NQ];
 #pragma unroll
-                for (int q = 0; q < US; ++q) {
-                    const int64_t ui = u0 + q * kWarp + lane;
+                for (int q = 0; q < NQ; ++q) {
+                    const int ci = c0 + q * kWarp + lane;
+                    if (ci < nch) {
+                        gd_load<CW>(wrow + ci * CW, words[q]);
+                        const int g = (ci * kGdChunk) >> gshift;
+                        sb[q] = (uint32_t)srow[g] | ((uint32_t)brow[g] << 16);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < UW; ++j)
-                        words[q][j] = ui < upr ? wrow[ui * UW + j] : 0u;
+                        for (int j = 0; j < CW; ++j) words[q][j] = 0u;
+                        sb[q] = 0u;
+                    }
                 }
 #pragma unroll
-                for (int q = 0; q < US; ++q) {
-                    const int64_t ui = u0 + q * kWarp + lane;
-                    if (ui >= upr) break;
-                    const int k0 = (int)ui * CU;
-                    const int g = k0 >> gshift;  // one group per unit
-                    const float sc = bf16_bits_to_f32(srow[g]);
-                    const float bi = bf16_bits_to_f32(brow[g]);
-                    uint32_t bw[SW];
+                for (int q = 0; q < NQ; ++q) {
+                    const int ci = c0 + q * kWarp + lane;
+                    if (ci >= nch) break;
+                    const int g = (ci * kGdChunk) >> gshift;
+                    const float sc = bf16_lo(sb[q]), bi = bf16_hi(sb[q]);
+                    uint32_t bw[8];
                     gd_spread<BITS>(words[q], bw);
 #pragma unroll
                     for (int m = 0; m < kGenTokens; ++m) {
                         if (m >= M) break;
-                        const int16_t *xm = xe + (int64_t)m * K + k0;
+                        const uint4 *xp = reinterpret_cast<const uint4 *>(xe + m * K);
                         int d = 0;
-                        if constexpr (SW == 1) {
-                            const uint2 xp = *reinterpret_cast<const uint2 *>(xm);
-                            d = dp2a_hi(xp.y, bw[0], dp2a_lo(xp.x, bw[0], d));
-                        } else {
 #pragma unroll
-                            for (int s2 = 0; s2 < SW; s2 += 2) {
-                                const uint4 xp =
-                                    *reinterpret_cast<const uint4 *>(xm + 4 * s2);
-                                d = dp2a_hi(xp.y, bw[s2], dp2a_lo(xp.x, bw[s2], d));
-                                d = dp2a_hi(xp.w, bw[s2 + 1], dp2a_lo(xp.z, bw[s2 + 1], d));
-                            }
+                        for (int s4 = 0; s4 < 4; ++s4) {
+                            const uint4 x4 = xp[s4 * nch + ci];
+                            d = dp2a_hi(x4.y, bw[2 * s4], dp2a_lo(x4.x, bw[2 * s4], d));
+                            d = dp2a_hi(x4.w, bw[2 * s4 + 1],
+                                        dp2a_lo(x4.z, bw[2 * s4 + 1], d));
                         }
-                        acc[h][m] = fmaf(sc * xf[(int64_t)m * G + g], (float)d,
-                                         fmaf(bi, xu[(int64_t)m * upr + ui], acc[h][m]));
+                        acc[h][m] = fmaf(sc * xf[m * G + g], (float)d,
+                                         fmaf(bi, xu[m * nch + ci], acc[h][m]));
                     }
                 }
             }
@@ -393,7 +442,7 @@ static cudaError_t launch_gdot_b(int mode, const DenseParams &p,
                     : mode == 1 ? reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 1>)
                     : mode == 2 ? reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 2>)
                                 : reinterpret_cast<const void *>(qmv_gdot_kernel<BITS, 3>);
-    const size_t smem = gd_smem_bytes<BITS>(p.M, p.K, p.group);
+    const size_t smem = gd_smem_bytes(p.M, p.K, p.group);
     int grid = 0;
     cudaError_t e = occupancy_grid(k, kGdThreads, smem, &grid);
     if (e != cudaSuccess) return e;
@@ -427,7 +476,7 @@ constexpr size_t kGdMaxSmem = 200 * 1024;
 template <int BITS>
 static cudaError_t launch_generic_w(int mode, const DenseParams &p,
                                     cudaStream_t st) {
-    if (gd_smem_bytes<BITS>(p.M, p.K, p.group) <= kGdMaxSmem)
+    if (gd_smem_bytes(p.M, p.K, p.group) <= kGdMaxSmem)
         return launch_gdot_b<BITS>(mode, p, st);
     return launch_generic_b<BITS>(mode, p, st);
 }
