@@ -67,32 +67,37 @@ __global__ void __launch_bounds__(256)
         // product with the correctly rounded reciprocal is within
         // 1.5 * 2^-23 * d/s (<= 4.6e-5, d/s <= ~257) of that quotient, so its
         // rounding can differ only when it lies within that distance of a
-        // half-integer; those (about one input in 10^4) take the division.
-        // Subnormal scales (a reciprocal that may overflow) always divide.
+        // half-integer (about one input in 10^4); a lane holding such an
+        // input redoes its eight codes by the division, which gives the same
+        // codes for the others.  Subnormal scales (a reciprocal that may
+        // overflow) always divide.
         const bool fast = s >= 1.17549435e-38f;
         const float r = fast ? __frcp_rn(s) : 0.0f;
         uint32_t q[8];
+        float emax = 0.0f;  // the largest distance of a product from an integer
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float d = v[i] - lo;  // >= 0, as in the reading
-            uint32_t c = 0u;
-            if (fast) {
-                const float t = d * r;
-                // t + 1.5 * 2^23 rounds t to an integer, ties to even, into
-                // the low mantissa bits (0 <= t < 2^22)
-                const float tt = t + 12582912.0f;
-                const float e = t - (tt - 12582912.0f);
-                c = __float_as_uint(tt) - 0x4b400000u;
-                if (fabsf(e) > 0.5f - 0x1p-12f) {
+            const float t = d * r;
+            // t + 1.5 * 2^23 rounds t to an integer, ties to even, into
+            // the low mantissa bits (0 <= t < 2^22)
+            const float tt = t + 12582912.0f;
+            emax = fmaxf(emax, fabsf(t - (tt - 12582912.0f)));
+            q[i] = min(__float_as_uint(tt) - 0x4b400000u, QMAX);
+        }
+        // a product within reach of a half-integer, or no usable reciprocal:
+        // all eight codes again by the division (rare; uniform per lane)
+        if (!fast || emax > 0.5f - 0x1p-12f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float d = v[i] - lo;
+                uint32_t c = 0u;
+                if (s != 0.0f) {
                     const float tx = rintf(__fdiv_rn(d, s));
                     c = tx <= 0.0f ? 0u : tx >= (float)QMAX ? QMAX : (uint32_t)tx;
                 }
-                c = min(c, QMAX);
-            } else if (s != 0.0f) {
-                const float tx = rintf(__fdiv_rn(d, s));
-                c = tx <= 0.0f ? 0u : tx >= (float)QMAX ? QMAX : (uint32_t)tx;
+                q[i] = c;
             }
-            q[i] = c;
         }
         if (!live) continue;
         if constexpr (BITS == 4) {
