@@ -95,3 +95,23 @@ def test_sections_gate_up_and_rope(bits, group):
         for o, r in zip(got, ref):
             close(o, r, f"rope M={m}")
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bits,group,K", [(3, 64, 13824), (6, 128, 13824),
+                                          (2, 32, 32768), (3, 64, 32768),
+                                          (6, 64, 32768)])
+def test_long_rows(bits, group, K):
+    """K = 13824 at four tokens keeps the integer-dot kernel with ~120 KB of
+    encoded activations per block; K = 32768 at four tokens exceeds its
+    shared memory and runs the fp32 kernel.  Plain and gate+up."""
+    M, N = 4, 40
+    w = synth.qweight(700 + bits + group, N, K, bits, group)
+    x = synth.activations(701, M, K)
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w), workspace=ws)
+    torch.cuda.synchronize()
+    close(y, oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits, group),
+          f"u{bits} g{group} K={K}")
+    close(h, oracle.gate_up_silu(x, w.wq, w.scales, w.biases, N, K, bits,
+                                 group=group), f"gate+up u{bits} K={K}")
