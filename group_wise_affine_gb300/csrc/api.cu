@@ -216,6 +216,17 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         probe.M = 1;
         if (stream_eligible(probe)) mt = mt < 4 ? mt : 4;
     }
+    // 5..8 tokens: the tensor-core decode kernel in one pass when the shape
+    // allows it (the streaming kernel would stream the weights twice; at 2..4
+    // tokens the two run level, and the streaming kernel stays)
+    if (!generic && M >= 5 && M <= 8) {
+        DenseParams q = p;
+        q.M = (int)M;
+        bool used = false;
+        cudaError_t e = launch_mma(mode, q, st, &used);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        if (used) return GWA_OK;
+    }
     for (int64_t t0 = 0; t0 < M; t0 += mt) {
         DenseParams q = p;
         q.M = (int)((M - t0) < mt ? (M - t0) : mt);
@@ -279,7 +290,8 @@ int gwa_pipeline_status(uint32_t *timeouts, int32_t reset) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "gwa_pipeline_status");
     *timeouts = group_timeouts(reset != 0) + stream_timeouts(reset != 0) +
-                moe_stream_timeouts(reset != 0) + qmm_timeouts(reset != 0);
+                moe_stream_timeouts(reset != 0) + qmm_timeouts(reset != 0) +
+                mma_timeouts(reset != 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? GWA_OK : cuda_fail(e, "gwa_pipeline_status");
 }

@@ -123,6 +123,11 @@ cudaError_t launch_dense(int mode, const DenseParams &p, cudaStream_t st);
 cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
                           bool *used);
 unsigned int stream_timeouts(bool reset);
+// Tensor-core decode kernel, up to 8 tokens in one pass (qmv_mma.cu; used for
+// 5..8 tokens); *used tells the caller whether the shape allowed it.
+cudaError_t launch_mma(int mode, const DenseParams &p, cudaStream_t st,
+                       bool *used);
+unsigned int mma_timeouts(bool reset);
 // One-token kernel with one quantization group per lane (qmv_group.cu).
 // mode: 0 plain, 1 sections, 2 gate+up SiLU, 3 QKV sections with the
 // rotary embedding of rows [0, p.rope_end)

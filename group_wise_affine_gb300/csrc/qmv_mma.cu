@@ -1,0 +1,434 @@
+// Decode kernel for 5..8 tokens on the tensor cores (u4/u8 codes, groups of
+// 64; rows of 512..5120 inputs): the same weight stream as the streaming
+// decode kernel (a producer thread copies the rows of a CTA's units into a
+// shared-memory ring with the bulk-copy engine), but the consumers form the
+// products with warp-level bf16 MMAs (m16n8k16, fp32 accumulation):
+//
+//   C = X W^T     m = the tokens (8 of the 16 used), n = 8 weight rows,
+//                 k = 16 inputs,
+//
+// per group of 64 inputs, then y += scale * (C - 128 X_g) + bias * X_g in
+// fp32, X_g the group's activation sum.  Codes enter as the exact bf16
+// 128 + q (0x4300 | q); u8 codes as their two nibbles in two products (the
+// high one counted 16 times), each made exact by subtracting 128 in bf16.
+// Activations are exact in bf16, so every product is exact and only the
+// accumulation rounds.
+//
+// Work layout: a stage holds 8 units (rows, or gate/up or rotary pairs) of
+// whole rows.  Consumer warp w owns inputs [512 w, 512 w + 512) of every
+// row: eight groups, whose activation fragments (the 16 of each group its
+// lane's k slice needs, for the lane's token) it keeps in registers for the
+// whole kernel.  Per stage and group it reads its lane's 8 (u4) or 16 (u8)
+// code bytes of weight row g, forms the B fragments, runs four (eight) MMAs
+// into a fresh accumulator and folds it into the per-row totals with the
+// row's scale and bias; the warps' totals go to per-warp slots that the
+// epilogue adds in a fixed order (plain, sections with bias, SiLU(gate)*up,
+// or the rotary embedding from p.rope_cs).
+//
+// Measured on the 27648 x 5120 gate+up weight: 36.9 us for 8 tokens in one
+// pass (the streaming kernel streams the weights twice: ~72 us), but only
+// level with the streaming kernel at 4 tokens (35.1 against 36.3 us): the
+// B-fragment reads of eight rows whose shared-memory stride is a multiple
+// of 128 bytes conflict eight ways, so it serves 5..8 tokens.
+//
+// k order: within a group, lane t's k-slice of k-step s (logical k 2t, 2t+1,
+// 2t+8, 2t+9) is the nibbles (j, j+4) and (j+1, j+5), j = 2 (s & 1), of word
+// 2t + s/2 (u4), or the low/high nibbles of bytes (0, 2) and (1, 3) of word
+// 4t + s (u8), so both operands come from 16 contiguous inputs per lane.
+// Formulas and sources as in qmv.cu ("Sanctum-MLX"; "The Cathedral Doubled
+// Itself", "The two fusions"; "saragossa", "Quantization formats").
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gwa {
+
+static __device__ unsigned int g_mma_timeouts;
+
+constexpr int kMmaUnits = 8;          // units per stage: the MMAs' n
+constexpr int kMmaGroupsPerWarp = 8;  // 512 inputs per consumer warp
+constexpr int kMmaMaxWarps = 10;      // K <= 5120
+constexpr int kMmaTokens = 8;
+constexpr size_t kMmaRingTarget = 160 * 1024;
+
+enum MmaMode { kMPlain = 0, kMSections = 1, kMGateUp = 2, kMRope = 3 };
+
+// d += a b, bf16 m16n8k16 with the A rows 8..15 zero.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// The 4-bit fields at bits 0-3 and 16-19 of v as the bf16 pair 128 + q.
+__device__ __forceinline__ uint32_t nib_pair(uint32_t v) {
+    return (v & 0x000f000fu) | 0x43004300u;
+}
+// The same minus 128: the exact bf16 pair q.
+__device__ __forceinline__ uint32_t nib_pair_exact(uint32_t v) {
+    const uint32_t a = nib_pair(v);
+    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                     __floats2bfloat162_rn(128.f, 128.f));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// Per-lane activation state: the A fragments (a0, a2) of the lane's token
+// for every k-step of the warp's eight groups, and the groups' sums.
+struct MmaX {
+    uint32_t a[kMmaGroupsPerWarp][4][2];
+    float xs[kMmaGroupsPerWarp];
+};
+
+// Loads the 16 inputs [16 t, 16 t + 16) of each of the warp's groups for
+// token g (zeros for g >= M) and arranges them in the k order above.
+template <int BITS>
+__device__ __forceinline__ void mma_load_x(const uint16_t *__restrict__ x, int M,
+                                           int K, int warp, int g, int t,
+                                           MmaX &xr) {
+#pragma unroll
+    for (int gi = 0; gi < kMmaGroupsPerWarp; ++gi) {
+        uint32_t w[8];
+        if (g < M) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                x + (int64_t)g * K + (int64_t)(warp * kMmaGroupsPerWarp + gi) * kGroup +
+                16 * t);
+            const uint4 u0 = src[0], u1 = src[1];
+            w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+            w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0u;
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s += bf16_lo(w[i]) + bf16_hi(w[i]);
+        // the group's sum: the four lanes t of token g
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        xr.xs[gi] = s;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t lo, hi;  // local indices of the pairs (l, l + d)
+            if constexpr (BITS == 4) {
+                // inputs 8 (ks/2) + j + {0, 4} and + {1, 5}, j = 2 (ks & 1)
+                const int l = 8 * (ks >> 1) + 2 * (ks & 1);
+                lo = __byte_perm(w[l / 2], w[l / 2 + 2], 0x5410);
+                hi = __byte_perm(w[l / 2], w[l / 2 + 2], 0x7632);
+            } else {
+                // inputs 4 ks + {0, 2} and + {1, 3}
+                lo = __byte_perm(w[2 * ks], w[2 * ks + 1], 0x5410);
+                hi = __byte_perm(w[2 * ks], w[2 * ks + 1], 0x7632);
+            }
+            xr.a[gi][ks][0] = lo;
+            xr.a[gi][ks][1] = hi;
+        }
+        // one group's loads at a time (registers)
+        asm volatile("" ::: "memory");
+    }
+}
+
+// 168 registers: up to 11 warps (10 consumers and the producer) per CTA.
+template <int BITS, int MODE>
+__global__ void __maxnreg__(168)
+    qmv_mma_kernel(DenseParams p, int stages, int64_t units, int nw) {
+    constexpr int HALVES = (MODE == kMGateUp || MODE == kMRope) ? 2 : 1;
+    constexpr int GB = BITS * 8;  // code bytes per row and group
+    constexpr int ups = kMmaUnits;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int ncons = nw * kWarp;
+    const int lane = tid & (kWarp - 1), warp = tid / kWarp;
+    const int M = p.M;
+    const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
+    const uint32_t sbrow = (uint32_t)p.G * 2;
+    const uint32_t rows_stage = (uint32_t)(HALVES * ups);
+    const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
+    uint64_t *empty = full + stages;
+    float *red = reinterpret_cast<float *>(empty + stages);
+    __shared__ int s_issued, s_consumed;
+
+    // rope: whole stages per CTA (8 divides d/2), so no stage crosses a head
+    const int64_t ualign = MODE == kMRope ? ups : 1;
+    const int64_t u0 = units / ualign * blockIdx.x / gridDim.x * ualign;
+    const int64_t u1 = units / ualign * (blockIdx.x + 1) / gridDim.x * ualign;
+    const int nu = (int)(u1 - u0);
+    const int nst = (nu + ups - 1) / ups;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nw);
+        }
+        fence_mbar_init();
+        s_issued = 0;
+        s_consumed = nst;
+        pdl_launch_dependents();
+    }
+    __syncthreads();
+
+    if (tid >= ncons) {
+        // ------------------------------------------------ producer
+        if (tid == ncons) {
+            const unsigned char *wq = reinterpret_cast<const unsigned char *>(p.wq);
+            const unsigned char *sc = reinterpret_cast<const unsigned char *>(p.sc);
+            const unsigned char *bi = reinterpret_cast<const unsigned char *>(p.bi);
+            for (int st = 0; st < nst; ++st) {
+                const int s = st % stages;
+                // weights are never written by this library's kernels: the
+                // first `stages` stages are fetched before the wait
+                if (st == stages) pdl_wait_primary();
+                if (st >= stages && !mbar_wait(&empty[s], ((st / stages) & 1) ^ 1)) {
+                    atomicAdd(&g_mma_timeouts, 1u);
+                    break;
+                }
+                const int64_t ua = u0 + (int64_t)st * ups;
+                const int n = (int)min((int64_t)ups, u1 - ua);
+                unsigned char *base = smem + (size_t)s * stage_bytes;
+                unsigned char *dsc = base + rows_stage * rowbytes;
+                unsigned char *dbi = dsc + rows_stage * sbrow;
+                mbar_expect_tx(&full[s], (uint32_t)(HALVES * n) * (rowbytes + 2 * sbrow));
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    const int64_t r = MODE == kMRope ? rope_pair_row(ua, h, p.rope_hd)
+                                                     : ua + (h ? p.I : 0);
+                    bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes, n * rowbytes,
+                             &full[s]);
+                    bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow, &full[s]);
+                    bulk_g2s(dbi + h * ups * sbrow, bi + r * sbrow, n * sbrow, &full[s]);
+                }
+                s_issued = st + 1;
+            }
+        }
+    } else {
+        // ------------------------------------------------ consumers
+        const int g = lane >> 2, t = lane & 3;  // token / weight row, k slice
+        const int gbase = warp * kMmaGroupsPerWarp;
+        MmaX xr;
+        pdl_wait_primary();  // x may be the previous kernel's output
+        mma_load_x<BITS>(p.x, M, p.K, warp, g, t, xr);
+        for (int st = 0; st < nst; ++st) {
+            const int s = st % stages;
+            if (!mbar_wait(&full[s], (st / stages) & 1)) {
+                atomicAdd(&g_mma_timeouts, 1u);
+                atomicMin(&s_consumed, st);
+                break;
+            }
+            const int64_t ua = u0 + (int64_t)st * ups;
+            const int n = (int)min((int64_t)ups, u1 - ua);
+            const unsigned char *base = smem + (uint32_t)s * stage_bytes;
+            const unsigned char *scb = base + rows_stage * rowbytes;
+            const unsigned char *bib = scb + rows_stage * sbrow;
+            // rows past the stage's end hold stale data: their columns of
+            // the products are dropped below
+            float acc[HALVES][2];
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) acc[h][0] = acc[h][1] = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < kMmaGroupsPerWarp; ++gi) {
+                const int gg = gbase + gi;
+                const float xs = xr.xs[gi];
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    // lane (g, t) supplies weight row g's k slice t ...
+                    const unsigned char *wr = base + (uint32_t)(h * ups + g) * rowbytes +
+                                              (uint32_t)gg * GB + (uint32_t)t * (GB / 4);
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (BITS == 4) {
+                        const uint2 wv = *reinterpret_cast<const uint2 *>(wr);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t word = ks < 2 ? wv.x : wv.y;
+                            const int j = 2 * (ks & 1);
+                            mma16816(c, xr.a[gi][ks][0], xr.a[gi][ks][1],
+                                     nib_pair(word >> (4 * j)), nib_pair(word >> (4 * j + 4)));
+                        }
+                    } else {
+                        const uint4 wv = *reinterpret_cast<const uint4 *>(wr);
+                        float ch[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t word = ks == 0   ? wv.x
+                                                  : ks == 1 ? wv.y
+                                                  : ks == 2 ? wv.z
+                                                            : wv.w;
+                            mma16816(c, xr.a[gi][ks][0], xr.a[gi][ks][1],
+                                     nib_pair_exact(word), nib_pair_exact(word >> 8));
+                            mma16816(ch, xr.a[gi][ks][0], xr.a[gi][ks][1],
+                                     nib_pair_exact(word >> 4), nib_pair_exact(word >> 12));
+                        }
+                        c[0] = fmaf(16.f, ch[0], c[0]);
+                        c[1] = fmaf(16.f, ch[1], c[1]);
+                    }
+                    // ... and gets the products of token g with rows 2t, 2t + 1
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const uint32_t so = ((uint32_t)(h * ups + 2 * t + v) * p.G + gg) * 2u;
+                        const float sv =
+                            bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(scb + so));
+                        const float bv =
+                            bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(bib + so));
+                        const float cv = BITS == 4 ? fmaf(-128.f, xs, c[v]) : c[v];
+                        acc[h][v] = fmaf(sv, cv, fmaf(bv, xs, acc[h][v]));
+                    }
+                    // keep the next half's and group's loads after this
+                    // one (registers)
+                    asm volatile("" ::: "memory");
+                }
+            }
+            // every lane's reads of this stage are done: release the slot
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (g < M) {
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const int u = 2 * t + v;
+                        if (u < n)
+                            red[(((st * ups + u) * HALVES + h) * M + g) * nw + warp] =
+                                acc[h][v];
+                    }
+            }
+        }
+    }
+    __syncthreads();
+    pdl_wait_primary();  // outputs may alias the previous kernel's inputs
+    // A timed-out pipeline must not leave bulk copies landing in shared
+    // memory after the CTA exits: wait (again bounded) for every stage that
+    // was issued but not consumed.
+    if (tid == ncons && s_consumed < s_issued) {
+        for (int st = s_consumed; st < s_issued; ++st)
+            if (!mbar_wait(&full[st % stages], (st / stages) & 1)) break;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------- epilogue
+    // the warps' slots of an output, added in a fixed order
+    auto total = [&](int idx) {
+        float v = 0.f;
+        for (int w = 0; w < nw; ++w) v += red[idx * nw + w];
+        return v;
+    };
+    for (int i = tid; i < nu * M; i += blockDim.x) {
+        const int lu = i / M, m = i % M;
+        const int64_t n = u0 + lu;
+        if constexpr (MODE == kMGateUp) {
+            const float gv = total((lu * 2 + 0) * M + m);
+            const float uv = total((lu * 2 + 1) * M + m);
+            p.y[(int64_t)m * p.I + n] = f32_to_bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+        } else if constexpr (MODE == kMRope) {
+            const int half = p.rope_hd / 2;
+            float a = total((lu * 2 + 0) * M + m);
+            float b = total((lu * 2 + 1) * M + m);
+            const int64_t r0 = rope_pair_row(n, 0, p.rope_hd);
+            int s = 0;
+            while (s + 1 < p.nsec && r0 >= p.sec_start[s + 1]) ++s;
+            const int64_t j = r0 - p.sec_start[s];
+            const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+            if (p.sec_bias[s]) {
+                a += bf16_bits_to_f32(p.sec_bias[s][j]);
+                b += bf16_bits_to_f32(p.sec_bias[s][j + half]);
+            }
+            if (r0 < p.rope_end) {
+                const float2 cs = p.rope_cs[(int64_t)m * half + (int)(n % half)];
+                const float a2 = a * cs.x - b * cs.y;
+                b = b * cs.x + a * cs.y;
+                a = a2;
+            }
+            uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
+            o[0] = f32_to_bf16_bits(a);
+            o[half] = f32_to_bf16_bits(b);
+        } else if constexpr (MODE == kMPlain) {
+            p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(total(lu * M + m));
+        } else {
+            int s = 0;
+            while (s + 1 < p.nsec && n >= p.sec_start[s + 1]) ++s;
+            const int64_t j = n - p.sec_start[s];
+            const int64_t size = p.sec_start[s + 1] - p.sec_start[s];
+            float val = total(lu * M + m);
+            if (p.sec_bias[s]) val += bf16_bits_to_f32(p.sec_bias[s][j]);
+            p.sec_out[s][(int64_t)m * size + j] = f32_to_bf16_bits(val);
+        }
+    }
+}
+
+// ------------------------------------------------------------ host side
+template <int BITS, int MODE>
+static cudaError_t launch_mma_t(const DenseParams &p, cudaStream_t st, bool *used) {
+    constexpr int HALVES = (MODE == kMGateUp || MODE == kMRope) ? 2 : 1;
+    const int64_t units = MODE == kMGateUp ? p.I : MODE == kMRope ? p.N / 2 : p.N;
+    if (units <= 0) return cudaSuccess;
+    if (MODE == kMRope && (p.rope_hd / 2) % kMmaUnits != 0)
+        return cudaSuccess;  // not used: stages would cross heads
+    const int nw = p.K / (kGroup * kMmaGroupsPerWarp);
+    const int threads = (nw + 1) * kWarp;
+    const size_t rowbytes = (size_t)p.K * BITS / 8;
+    const size_t sbrow = (size_t)p.G * 2;
+    const size_t stage_bytes = (size_t)HALVES * kMmaUnits * (rowbytes + 2 * sbrow);
+    int grid = num_sms();
+    const int64_t ualign = MODE == kMRope ? kMmaUnits : 1;
+    if ((int64_t)grid > units / ualign) grid = (int)(units / ualign);
+    if (grid < 1) return cudaSuccess;
+    const int64_t umax = (units / ualign + grid - 1) / grid * ualign;
+    const size_t red_bytes = (size_t)umax * HALVES * p.M * nw * 4;
+    if (red_bytes + 2 * (stage_bytes + 16) > kMaxDynSmem) return cudaSuccess;
+    int stages = (int)((kMaxDynSmem - red_bytes) / (stage_bytes + 16));
+    const int cap = (int)(kMmaRingTarget / stage_bytes);
+    if (stages > cap) stages = cap;
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    const size_t smem = stages * (stage_bytes + 16) + red_bytes;
+    auto kern = qmv_mma_kernel<BITS, MODE>;
+    int dummy = 0;
+    cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern), threads, smem,
+                                   &dummy);
+    if (e != cudaSuccess) return e;
+    *used = true;
+    return launch_pdl(reinterpret_cast<const void *>(kern), (unsigned)grid,
+                      (unsigned)threads, smem, st, p, stages, units, nw);
+}
+
+static bool mma_aligned16(const void *q) {
+    return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
+}
+
+// Runs the tensor-core decode kernel for up to 8 tokens in one pass when the
+// shape allows it (u4/u8 at group 64, K a multiple of 512 up to 5120, so a
+// row's scales are whole 16-byte units for the bulk copies; 16-byte aligned
+// weights); *used tells the caller whether it ran.
+cudaError_t launch_mma(int mode, const DenseParams &p, cudaStream_t st, bool *used) {
+    *used = false;
+    if (p.M < 2 || p.M > kMmaTokens || (p.bits != 4 && p.bits != 8) ||
+        p.group != kGroup || p.K % 512 != 0 ||
+        p.K > kGroup * kMmaGroupsPerWarp * kMmaMaxWarps || !mma_aligned16(p.wq) ||
+        !mma_aligned16(p.sc) || !mma_aligned16(p.bi))
+        return cudaSuccess;
+#define GWA_MMA_CASE(B)                                                         \
+    if (p.bits == B) {                                                          \
+        if (mode == kMPlain) return launch_mma_t<B, kMPlain>(p, st, used);      \
+        if (mode == kMSections) return launch_mma_t<B, kMSections>(p, st, used); \
+        if (mode == kMRope) return launch_mma_t<B, kMRope>(p, st, used);        \
+        return launch_mma_t<B, kMGateUp>(p, st, used);                          \
+    }
+    GWA_MMA_CASE(4)
+    GWA_MMA_CASE(8)
+#undef GWA_MMA_CASE
+    return cudaSuccess;
+}
+
+unsigned int mma_timeouts(bool reset) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_mma_timeouts, sizeof v);
+    if (reset) {
+        const unsigned int z = 0;
+        cudaMemcpyToSymbol(g_mma_timeouts, &z, sizeof z);
+    }
+    return v;
+}
+
+}  // namespace gwa

@@ -221,10 +221,11 @@ def test_bad_arguments_raise_status_not_fault():
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 5, 8])
 def test_sections_bias_streaming_kernels(bits, M):
-    # K = 1024: the one-token lane-per-group kernel (M = 1) and the chunk
-    # streaming kernel (M = 3), ragged section sizes, optional biases
+    # K = 1024: the one-token lane-per-group kernel (M = 1), the chunk
+    # streaming kernel (M = 3) and the tensor-core kernel (M = 5, 8; ragged
+    # last stage), ragged section sizes, optional biases
     K, secs = 1024, (200, 56, 56, 9)
     parts = [synth.qweight(440 + i + bits, n, K, bits)
              for i, n in enumerate(secs)]
