@@ -341,6 +341,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     extras = {}
     if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
         extras["stack_M4"] = run_stack_extra(W, 4, dev, 50, 3)
+        extras["stack_M8"] = run_stack_extra(W, 8, dev, 30, 3)
         extras["qkv_rope"] = run_rope_extra(W, dev, 20, 3)
         extras["prefill_stack_M512"] = run_stack_extra(W, 512, dev, 5, 2)
         # the same stack with u8 codes (its own 14 GB of weights)
