@@ -74,3 +74,8 @@ def test_u8_values_and_batches():
 
 def test_not_causal_and_sharp_scores():
     run(1, 4, 1, 3, 200, 128, causal=False, seed=6, qscale=4.0)
+
+
+def test_decode_full_cache():
+    # the bench's 32768-key decode over 8 KV heads of 128 (40 query heads)
+    run(1, 40, 8, 1, 32768, 128, seed=32768)

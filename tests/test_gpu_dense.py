@@ -185,8 +185,10 @@ def test_gate_up_silu_small(bits, M):
     assert_close(bf16_to_f64(h), ref, f"gate_up M={M} u{bits}")
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_gate_up_silu_config_full(M):
+    # M = 1: lane-per-group kernel; 4: streaming kernel; 8: tensor-core
+    # kernel, one pass
     K, I = 5120, 13824
     w = synth.stack_rows([synth.qweight(synth.seed_for(2, 0, 0), I, K, 4),
                           synth.qweight(synth.seed_for(2, 0, 1), I, K, 4)])

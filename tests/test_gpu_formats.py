@@ -115,3 +115,18 @@ def test_long_rows(bits, group, K):
           f"u{bits} g{group} K={K}")
     close(h, oracle.gate_up_silu(x, w.wq, w.scales, w.biases, N, K, bits,
                                  group=group), f"gate+up u{bits} K={K}")
+
+
+@pytest.mark.parametrize("bits", [3, 6])
+def test_gate_up_full_shape_sampled(bits):
+    """The 27648 x 5120 gate+up weight at one token, the launch the formats
+    bench times: 512 sampled outputs against the oracle."""
+    K, I = 5120, 13824
+    w = synth.qweight(900 + bits, 2 * I, K, bits, 64)
+    x = synth.activations(901, 1, K)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(bits).choice(I, size=512, replace=False)
+    ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits,
+                              group=64, cols=cols)
+    close(h[:, torch.from_numpy(cols).cuda()], ref, f"u{bits} full shape")
