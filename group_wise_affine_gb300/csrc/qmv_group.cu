@@ -52,7 +52,8 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
 template <int BITS, int MT, int MODE, int RPH>
 __global__ void __maxnreg__(88)
     qmv_group_kernel(DenseParams p, int stages, int64_t units, int rs,
-                     int slices, uint32_t xenc_off, uint32_t rope_off) {
+                     int slices, uint32_t ring_bytes, uint32_t xenc_off,
+                     uint32_t rope_off) {
     constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;
     constexpr int V = RPH * MT;
@@ -67,7 +68,11 @@ __global__ void __maxnreg__(88)
     const uint32_t sbrow = (uint32_t)p.G * 2;
     const uint32_t rows_stage = (uint32_t)(HALVES * ups);
     const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
+    // A stage holds its rows' scales, then their biases, then their codes,
+    // so a stage of fewer units needs only a prefix of the slot: the last
+    // slot of the ring may be such a short one (see the host side).
+    const uint32_t codes_off = 2 * rows_stage * sbrow;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes);
     uint64_t *empty = full + stages;
     float *red = reinterpret_cast<float *>(empty + stages);
     __shared__ int s_issued, s_consumed;
@@ -116,15 +121,16 @@ __global__ void __maxnreg__(88)
                 const int64_t ua = u0 + (int64_t)st * ups;
                 const int n = (int)min((int64_t)ups, u1 - ua);
                 unsigned char *base = smem + (size_t)s * stage_bytes;
-                unsigned char *dsc = base + rows_stage * rowbytes;
+                unsigned char *dsc = base;
                 unsigned char *dbi = dsc + rows_stage * sbrow;
+                unsigned char *dwq = base + codes_off;
                 mbar_expect_tx(&full[s], (uint32_t)(HALVES * n) *
                                              (rowbytes + 2 * sbrow));
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
                     const int64_t r = MODE == kGRope ? rope_pair_row(ua, h, p.rope_hd)
                                                      : ua + (h ? p.I : 0);
-                    bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
+                    bulk_g2s(dwq + h * ups * rowbytes, wq + r * rowbytes,
                              n * rowbytes, &full[s]);
                     bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
                              &full[s]);
@@ -177,9 +183,14 @@ __global__ void __maxnreg__(88)
         for (int j = 0; j < RPH; ++j) {
             const uint32_t srow =
                 (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
-            offw[j] = srow * rowbytes + (uint32_t)gg * GB;
-            offs[j] = rows_stage * rowbytes + (srow * (uint32_t)p.G + gg) * 2u;
+            offw[j] = codes_off + srow * rowbytes + (uint32_t)gg * GB;
+            offs[j] = (srow * (uint32_t)p.G + gg) * 2u;
         }
+        // rows past the end of a stage of fewer units read the stage's first
+        // row instead (their values are never stored), so that no read
+        // leaves a short slot
+        const uint32_t offw0 = codes_off + (uint32_t)gg * GB;
+        const uint32_t offs0 = (uint32_t)gg * 2u;
         // this lane's slot of the partial sums: value index idx = j*MT + m
         // of unit u (stage-relative), half h
         constexpr int SPREAD = kSlice / V;
@@ -202,16 +213,19 @@ __global__ void __maxnreg__(88)
                 break;
             }
             const unsigned char *base = smem + (uint32_t)s * stage_bytes;
+            const int left = nu - st * ups;  // units in this stage: min(ups, left)
             float v[V];
 #pragma unroll
             for (int j = 0; j < RPH; ++j) {
+                const bool in = hg * UPT + (j % UPT) < left;
+                const uint32_t ow = in ? offw[j] : offw0;
+                const uint32_t os = in ? offs[j] : offs0;
                 uint4 w[BITS / 2];
-                lds_group<BITS>(base + offw[j], rot, w);
+                lds_group<BITS>(base + ow, rot, w);
                 const float sv = bf16_bits_to_f32(
-                    *reinterpret_cast<const uint16_t *>(base + offs[j]));
+                    *reinterpret_cast<const uint16_t *>(base + os));
                 const float bv = bf16_bits_to_f32(
-                    *reinterpret_cast<const uint16_t *>(base + offs[j] +
-                                                        sb_delta));
+                    *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
                 int d[MT];
                 group_dot<BITS, MT>(w, gx, d);
 #pragma unroll
@@ -331,8 +345,23 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     int stages = (int)((kGroupSmemCap - fixed) / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) return cudaSuccess;  // rows too long for the ring
-    const size_t rope_off =
-        stages * stage_bytes + 16 * stages + ((red_bytes + 15) / 16) * 16;
+    size_t ring = (size_t)stages * stage_bytes;
+    // When every CTA's share is at most one stage more than the ring holds,
+    // a short last slot (a prefix of a stage: scales, biases, then the codes
+    // of the units it carries) can take that stage, so the whole share is
+    // fetched before the previous kernel finishes and no fetch is left for
+    // after the activations arrive.
+    const int64_t ups = (int64_t)rs * UPT;
+    if (stages < 8 && umax > stages * ups && umax <= (stages + 1) * ups) {
+        const int64_t tail = umax - stages * ups;
+        const size_t foot = (size_t)2 * HALVES * ups * sbrow +
+                            (size_t)((HALVES - 1) * ups + tail) * rowbytes;
+        if (fixed + ring + foot <= kGroupSmemCap) {
+            ++stages;
+            ring += foot;
+        }
+    }
+    const size_t rope_off = ring + 16 * stages + ((red_bytes + 15) / 16) * 16;
     const size_t xenc_off = rope_off + rope_bytes;
     const size_t smem = xenc_off + ximg_bytes(MT, p.G);
     auto kern = qmv_group_kernel<BITS, MT, MODE, RPH>;
@@ -342,7 +371,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     if (e != cudaSuccess) return e;
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,
-                      smem, st, p, stages, units, rs, slices,
+                      smem, st, p, stages, units, rs, slices, (uint32_t)ring,
                       (uint32_t)xenc_off, (uint32_t)rope_off);
 }
 

@@ -254,3 +254,31 @@ def test_gate_up_lane_per_group_kernel(bits):
     h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
     ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits)
     assert_close(bf16_to_f64(h), ref, f"gate_up lane-per-group u{bits}")
+
+
+# One-token shares one stage longer than the shared-memory ring: 152 CTAs
+# of 33 or 34 rows (u4, K = 5120: four stages of eight rows plus a short
+# slot) or of 17 or 18 rows (u8: two stages plus a short slot).  Rows past
+# the end of the short stage must neither be stored nor read out of it.
+@pytest.mark.parametrize("bits,N", [(4, 5000), (4, 5120), (8, 2600)])
+def test_one_token_short_last_slot(bits, N):
+    K = 5120
+    w = synth.qweight(600 + N + bits, N, K, bits)
+    x = synth.activations(610 + bits, 1, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w))
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+    assert_close(bf16_to_f64(y), ref, f"short slot N={N} u{bits}")
+
+
+def test_one_token_short_last_slot_sections():
+    K, secs = 5120, (4096, 512, 512)
+    parts = [synth.qweight(620 + i, n, K, 4) for i, n in enumerate(secs)]
+    fused = synth.stack_rows(parts)
+    bias = [synth.activations(630 + i, 1, n)[0] for i, n in enumerate(secs)]
+    x = synth.activations(640, 1, K)
+    outs = gwa.qmv_fused_sections(dev_bf16(x), dev_qweight(fused), secs,
+                                  out_bias=[dev_bf16(b) for b in bias])
+    refs = oracle.fused_sections(x, fused.wq, fused.scales, fused.biases, secs,
+                                 K, 4, out_bias=bias)
+    for o, r in zip(outs, refs):
+        assert_close(bf16_to_f64(o), r, "short slot sections")
