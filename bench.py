@@ -557,9 +557,10 @@ def run_rope_extra(W, dev, steps, warmup, tokens=(1, 4, 512),
 def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
                       formats=((2, 64), (3, 64), (6, 64), (4, 32), (4, 128))):
     """The gate+up shape (27648 x 5120, one token, SiLU epilogue) in code
-    widths and group sizes outside the tuned kernels: the general-format
-    decode kernel, eight back-to-back launches over distinct weights so
-    the timed bytes stream from HBM."""
+    widths and group sizes outside group 64: u2, u3 and u6 on the
+    general-format decode kernel, u4 in groups of 32 and 128 on the
+    one-token chunk kernel; eight back-to-back launches over distinct
+    weights so the timed bytes stream from HBM."""
     import torch
     import group_wise_affine_gb300 as gwa
     import gwa_synth as synth

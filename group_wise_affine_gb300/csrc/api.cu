@@ -244,7 +244,10 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         }
         bool used = false;
         if (generic) {
-            cudaError_t e = launch_generic(mode, q, st);
+            // one token of u4 / u8 codes in groups of 32 or 128: the
+            // chunk-per-lane kernel when the shape allows it
+            cudaError_t e = launch_group(mode, q, st, &used);
+            if (e == cudaSuccess && !used) e = launch_generic(mode, q, st);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             continue;
         }
@@ -440,7 +443,8 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
     r.rope_end = q_size + kv_size;
     r.rope_pos = positions;
     r.rope_r = pow(rope_base, -2.0 / (double)head_dim);
-    if (M == 1 && tuned_format(w.bits, w.group)) {
+    if (M == 1 && (w.bits == 4 || w.bits == 8) &&
+        (w.group == 32 || w.group == 64 || w.group == 128)) {
         // the one-token kernel forms its own (cos, sin) and rotates Q and K
         // in its epilogue
         bool used = false;

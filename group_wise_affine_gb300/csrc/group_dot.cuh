@@ -1,12 +1,16 @@
 // Group-per-lane integer dot shared by the one-token decode kernel
 // (qmv_group.cu) and the streaming MoE kernels (moe_stream.cu).
 //
-// A lane owns one group of 64 inputs.  The activations of that group are
+// A lane owns one chunk of 64 inputs (one quantization group of 64, half a
+// group of 128, or two groups of 32).  The activations of that chunk are
 // encoded once per CTA into a shared-memory image (int16 pairs with one
-// power-of-two scale per group, see common.cuh) and then held in 32
+// power-of-two scale per chunk, see common.cuh) and then held in 32
 // registers per activation row; per weight row the lane forms the exact
-// integer dot of its group with dp2a and applies the affine map once:
-//   y += (s * 2^E) * D + b * sum_k x_k,   D = sum_k q_k * xi_k.
+// integer dot of its chunk with dp2a and applies the affine map once per
+// group it covers:
+//   y += (s * 2^E) * D + b * sum_k x_k,   D = sum_k q_k * xi_k,
+// with D and sum_k x_k taken over the chunk, or over each half of it for
+// groups of 32 ("split" images carry the two half sums).
 // Packed format: "saragossa", "Quantization formats" (MLX affine, codes
 // lowest bits first, one bf16 scale and bias per 64 inputs).
 #pragma once
@@ -15,12 +19,14 @@
 
 namespace gwa {
 
-// Activations of one group for MT activation rows, encoded for the dot.
+// Activations of one chunk for MT activation rows, encoded for the dot.
 template <int MT>
 struct GroupX {
     uint32_t pr[MT][32];  // int16 pairs in dp2a order
     float f[MT];          // 2^E (u4: 2^E / 16, see encode_quarter)
-    float xs[MT];         // plain fp32 sum of the group's activations
+    float xs[MT];         // plain fp32 sum of the chunk's activations
+                          // (split: of its first 32)
+    float xs2[MT];        // split: plain fp32 sum of its last 32
 };
 
 // int16 of v * finv, rounded to nearest even: adding 1.5 * 2^23 puts the
@@ -34,12 +40,14 @@ __device__ __forceinline__ uint32_t i16_pair_fast(float a, float b,
     return __byte_perm(i16_bits(a, finv), i16_bits(b, finv), 0x5410);
 }
 
-// Shared-memory image of R encoded activation rows, chunk-major so that the
-// lanes of a warp (consecutive groups) read consecutive 16-byte chunks:
-//   pairs[r][c][g] (uint4: pairs 4c..4c+3 of group g), then f[r][g],
-//   xs[r][g].
-__host__ __device__ constexpr size_t ximg_bytes(int R, int G) {
-    return (size_t)R * G * (8 * 16 + 8);
+// Shared-memory image of R encoded activation rows of G chunks, chunk-major
+// so that the lanes of a warp (consecutive chunks) read consecutive 16-byte
+// pieces:
+//   pairs[r][c][g] (uint4: pairs 4c..4c+3 of chunk g), then f[r][g],
+//   xs[r][g], and for split images xs2[r][g].
+__host__ __device__ constexpr size_t ximg_bytes(int R, int G,
+                                                bool split = false) {
+    return (size_t)R * G * (8 * 16 + 8 + (split ? 4 : 0));
 }
 
 // Quarter `q` (16 inputs) of group g of image row r, from its 8 packed bf16
@@ -47,7 +55,7 @@ __host__ __device__ constexpr size_t ximg_bytes(int R, int G) {
 // on the group's exponent and sum through shuffles, so every lane of the
 // warp must call this.  u4: the high-nibble products of the dot come out
 // 16x too large and exact, so f is stored as 2^E / 16.
-template <int BITS>
+template <int BITS, bool SPLIT = false>
 __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
                                                bool store, int r, int g, int q,
                                                int R, int G,
@@ -71,8 +79,8 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
 #pragma unroll
     for (int i = 0; i < 4; ++i) t[i] = (v[i] + v[i + 4]) + (v[i + 8] + v[i + 12]);
     float sum = (t[0] + t[1]) + (t[2] + t[3]);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);  // quarters 0+1, 2+3
+    if constexpr (!SPLIT) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     float f, finv;
     group_scale((int)((m16 >> 7) & 0xffu), f, finv);
     uint32_t pr[8];
@@ -103,6 +111,7 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
             xf[(size_t)r * G + g] = BITS == 4 ? f * 0.0625f : f;
             xsm[(size_t)r * G + g] = sum;
         }
+        if (SPLIT && q == 2) xsm[(size_t)R * G + (size_t)r * G + g] = sum;
     }
 }
 
@@ -113,7 +122,7 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
 // costs about one memory round trip.
 constexpr int kXBatch = 4;
 
-template <int BITS>
+template <int BITS, bool SPLIT = false>
 __device__ __forceinline__ void encode_rows_shared(
     const uint16_t *__restrict__ x, int Rv, int R, int K, int G, int tid,
     int ncons, unsigned char *img, const int *rowsrc = nullptr) {
@@ -144,8 +153,8 @@ __device__ __forceinline__ void encode_rows_shared(
             if (b0 + j >= iters) break;  // uniform: the shuffles need every lane
             const int it = (b0 + j) * ncons + tid;
             const int r = it / (4 * G), rem = it - r * 4 * G;
-            encode_quarter<BITS>(u[j], it < items, r, rem >> 2, rem & 3, R, G,
-                                 img);
+            encode_quarter<BITS, SPLIT>(u[j], it < items, r, rem >> 2, rem & 3,
+                                        R, G, img);
         }
     }
 }
@@ -174,7 +183,7 @@ __device__ __forceinline__ void lds_group(const unsigned char *src, int rot,
 
 // Image rows r0 .. r0+MT-1 of group g into registers (zeros when !active),
 // image chunks rotated by `shift` (see chunk_rot).
-template <int MT>
+template <int MT, bool SPLIT = false>
 __device__ __forceinline__ void load_group_rows(const unsigned char *img,
                                                 int R, int G, int r0, int g,
                                                 bool active, GroupX<MT> &gx,
@@ -195,6 +204,7 @@ __device__ __forceinline__ void load_group_rows(const unsigned char *img,
         }
         gx.f[m] = active ? xf[(size_t)r * G + g] : 0.f;
         gx.xs[m] = active ? xsm[(size_t)r * G + g] : 0.f;
+        gx.xs2[m] = SPLIT && active ? xsm[(size_t)R * G + (size_t)r * G + g] : 0.f;
     }
 }
 
@@ -242,6 +252,64 @@ __device__ __forceinline__ void group_dot(const uint4 (&w)[BITS / 2],
             d[m] = 16 * (a[m][0] + a[m][2]) + (a[m][1] + a[m][3]);
         else
             d[m] = (a[m][0] + a[m][1]) + (a[m][2] + a[m][3]);
+    }
+}
+
+// The same dot split over the chunk's two halves (groups of 32): dl over
+// inputs [0, 32), dh over [32, 64), each scaled like group_dot's result.
+// Register piece v of w holds code piece (v + rot) & (NV - 1) (lds_group
+// with rotation rot), so which half a piece falls in is known only at run
+// time: each piece keeps its own sums and they are assigned at the end.
+template <int BITS, int MT>
+__device__ __forceinline__ void group_dot_split(const uint4 (&w)[BITS / 2],
+                                                const GroupX<MT> &gx, int rot,
+                                                int (&dl)[MT], int (&dh)[MT]) {
+    constexpr int NV = BITS / 2;
+    int a[NV][MT][2];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) a[v][m][0] = a[v][m][1] = 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wd = 4 * v + c;
+            const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
+                                  : c == 2 ? w[v].z : w[v].w;
+            if constexpr (BITS == 4) {
+                const uint32_t lo = word & 0x0f0f0f0fu;
+                const uint32_t hi = word & 0xf0f0f0f0u;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = gx.pr[m] + 4 * wd;
+                    a[v][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, a[v][m][0]));
+                    a[v][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, a[v][m][1]));
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = gx.pr[m] + 2 * wd;
+                    a[v][m][c & 1] =
+                        dp2a_hi(pr[1], word, dp2a_lo(pr[0], word, a[v][m][c & 1]));
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        int lo = 0, hi = 0;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int dv = BITS == 4 ? 16 * a[v][m][0] + a[v][m][1]
+                                     : a[v][m][0] + a[v][m][1];
+            if (((v + rot) & (NV - 1)) < NV / 2)
+                lo += dv;
+            else
+                hi += dv;
+        }
+        dl[m] = lo;
+        dh[m] = hi;
     }
 }
 

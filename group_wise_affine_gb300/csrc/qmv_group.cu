@@ -1,20 +1,22 @@
-// Streaming decode kernel for one or two tokens, one quantization group per
-// lane.  Same pipeline as qmv_stream.cu (a producer thread fills a
-// shared-memory ring with whole packed rows and their scales and biases by
-// bulk copy, consumer threads form exact integer dots), but each consumer
-// lane owns a whole group of 64 inputs instead of a 16-byte chunk:
-//  * the lane's activations of that group sit in 32 registers per token
-//    (int16 pairs, one power-of-two scale per group, see common.cuh), so no
+// Streaming decode kernel for one token, one 64-input chunk per lane.  Same
+// pipeline as qmv_stream.cu (a producer thread fills a shared-memory ring
+// with whole packed rows and their scales and biases by bulk copy, consumer
+// threads form exact integer dots), but each consumer lane owns a chunk of
+// 64 inputs (a group of 64, half a group of 128 or two groups of 32)
+// instead of a 16-byte piece:
+//  * the lane's activations of that chunk sit in 32 registers per token
+//    (int16 pairs, one power-of-two scale per chunk, see common.cuh), so no
 //    lane needs another lane's exponent;
-//  * per row and group the lane reads 32 (u4) or 64 (u8) bytes of codes, one
-//    scale and one bias, and applies the affine map once per group:
+//  * per row and chunk the lane reads 32 (u4) or 64 (u8) bytes of codes and
+//    the scale and bias of each group the chunk covers, and applies the
+//    affine map once per group:
 //      y += (s * 2^E) * D + b * sum_k x_k,   D = sum_k q_k * xi_k (exact);
-//  * a row's groups are spread over 16-lane slices (ceil(G/16) slices per
-//    row); each slice reduces its values with a 16-lane transpose reduction
-//    and stores one partial per (row, token) in its own slot, and the
-//    epilogue adds a row's slots in slice order (deterministic).
-// Per 64 codes this costs one scale application and one reduction share
-// instead of two, which is most of the non-dot work of the chunk layout.
+//  * a row's chunks are spread over 16-lane slices (ceil(K/64/16) slices
+//    per row); each slice reduces its values with a 16-lane transpose
+//    reduction and stores one partial per (row, token) in its own slot, and
+//    the epilogue adds a row's slots in slice order (deterministic).
+// Per 64 codes this costs one or two scale applications and one reduction
+// share, against two of each in the 16-byte-piece layout.
 // Sources: "Sanctum-MLX" (decode is a bandwidth-bound quantized GEMV); the
 // packed format of "saragossa", "Quantization formats"; the fused QKV and
 // gate+up epilogues of "The Cathedral Doubled Itself", "The two fusions".
@@ -49,7 +51,7 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
 // [16 * (h % slices), +16) of that row group's RPH rows.  Half-warps past
 // RS * slices (an odd count rounded up to whole warps) only take part in
 // the shuffles.
-template <int BITS, int MT, int MODE, int RPH>
+template <int BITS, int MT, int MODE, int RPH, int GS>
 __global__ void __maxnreg__(88)
     qmv_group_kernel(DenseParams p, int stages, int64_t units, int rs,
                      int slices, uint32_t ring_bytes, uint32_t xenc_off,
@@ -57,7 +59,8 @@ __global__ void __maxnreg__(88)
     constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;
     constexpr int V = RPH * MT;
-    constexpr int GB = BITS * 8;  // bytes of codes per row and group
+    constexpr int GB = BITS * 8;  // bytes of codes per row and chunk
+    constexpr bool SPLIT = GS == 32;  // a chunk covers two groups
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -150,11 +153,14 @@ __global__ void __maxnreg__(88)
         const bool in_group = hw < rs * slices;
         const int hg = in_group ? hw / slices : 0;  // row group
         const int sl = in_group ? hw - hg * slices : 0;
-        const int g = sl * kSlice + (tid & (kSlice - 1));
-        const bool active = in_group && g < p.G;
-        // lanes without a group read group 0 (finite weights) with zero
+        const int nchunk = p.K / 64;
+        const int g = sl * kSlice + (tid & (kSlice - 1));  // chunk
+        const bool active = in_group && g < nchunk;
+        // lanes without a chunk read chunk 0 (finite weights) with zero
         // activations, so their values are exact zeros
         const int gg = active ? g : 0;
+        // first weight group of the chunk
+        const int sg = GS == 64 ? gg : GS == 128 ? gg >> 1 : 2 * gg;
         unsigned char *xenc = smem + xenc_off;
         if constexpr (MODE == kGRope) {
             // the CTA's (cos, sin) table, while the previous kernel drains
@@ -170,13 +176,14 @@ __global__ void __maxnreg__(88)
             }
         }
         pdl_wait_primary();  // x may be the previous kernel's output
-        encode_rows_shared<BITS>(p.x, p.M, MT, p.K, p.G, tid, ncons, xenc);
+        encode_rows_shared<BITS, SPLIT>(p.x, p.M, MT, p.K, nchunk, tid, ncons,
+                                        xenc);
         // the consumer warps only (the producer is in its copy loop)
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
         GroupX<MT> gx;
         const int rot = chunk_rot<BITS>(gg);
-        load_group_rows<MT>(xenc, MT, p.G, 0, gg, active, gx,
-                            image_shift<BITS>(gg));
+        load_group_rows<MT, SPLIT>(xenc, MT, nchunk, 0, gg, active, gx,
+                                   image_shift<BITS>(gg));
         uint32_t offw[RPH], offs[RPH];
         const uint32_t sb_delta = rows_stage * (uint32_t)p.G * 2u;
 #pragma unroll
@@ -184,13 +191,13 @@ __global__ void __maxnreg__(88)
             const uint32_t srow =
                 (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
             offw[j] = codes_off + srow * rowbytes + (uint32_t)gg * GB;
-            offs[j] = (srow * (uint32_t)p.G + gg) * 2u;
+            offs[j] = (srow * (uint32_t)p.G + sg) * 2u;
         }
         // rows past the end of a stage of fewer units read the stage's first
         // row instead (their values are never stored), so that no read
         // leaves a short slot
         const uint32_t offw0 = codes_off + (uint32_t)gg * GB;
-        const uint32_t offs0 = (uint32_t)gg * 2u;
+        const uint32_t offs0 = (uint32_t)sg * 2u;
         // this lane's slot of the partial sums: value index idx = j*MT + m
         // of unit u (stage-relative), half h
         constexpr int SPREAD = kSlice / V;
@@ -222,16 +229,33 @@ __global__ void __maxnreg__(88)
                 const uint32_t os = in ? offs[j] : offs0;
                 uint4 w[BITS / 2];
                 lds_group<BITS>(base + ow, rot, w);
-                const float sv = bf16_bits_to_f32(
-                    *reinterpret_cast<const uint16_t *>(base + os));
-                const float bv = bf16_bits_to_f32(
-                    *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
-                int d[MT];
-                group_dot<BITS, MT>(w, gx, d);
+                if constexpr (SPLIT) {
+                    // the scales and biases of the chunk's two groups
+                    const uint32_t s2 =
+                        *reinterpret_cast<const uint32_t *>(base + os);
+                    const uint32_t b2 =
+                        *reinterpret_cast<const uint32_t *>(base + os + sb_delta);
+                    int dl[MT], dh[MT];
+                    group_dot_split<BITS, MT>(w, gx, rot, dl, dh);
 #pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    v[j * MT + m] =
-                        fmaf(sv * gx.f[m], (float)d[m], bv * gx.xs[m]);
+                    for (int m = 0; m < MT; ++m)
+                        v[j * MT + m] = fmaf(
+                            bf16_lo(s2) * gx.f[m], (float)dl[m],
+                            fmaf(bf16_hi(s2) * gx.f[m], (float)dh[m],
+                                 fmaf(bf16_lo(b2), gx.xs[m],
+                                      bf16_hi(b2) * gx.xs2[m])));
+                } else {
+                    const float sv = bf16_bits_to_f32(
+                        *reinterpret_cast<const uint16_t *>(base + os));
+                    const float bv = bf16_bits_to_f32(
+                        *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
+                    int d[MT];
+                    group_dot<BITS, MT>(w, gx, d);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        v[j * MT + m] =
+                            fmaf(sv * gx.f[m], (float)d[m], bv * gx.xs[m]);
+                }
             }
             // every lane's reads of this stage are done: release the slot
             __syncwarp();
@@ -307,7 +331,7 @@ __global__ void __maxnreg__(88)
 }
 
 // ------------------------------------------------------------ host side
-template <int BITS, int MT, int MODE, int RPH>
+template <int BITS, int MT, int MODE, int RPH, int GS>
 static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
                                   bool *used) {
     constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
@@ -316,7 +340,8 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
         MODE == kGGateUp ? p.I : MODE == kGRope ? p.N / 2 : p.N;
     const size_t rowbytes = (size_t)p.K * BITS / 8;
     const size_t sbrow = (size_t)p.G * 2;
-    const int slices = (p.G + kSlice - 1) / kSlice;
+    const int nchunk = p.K / 64;
+    const int slices = (nchunk + kSlice - 1) / kSlice;
     // row groups: as many as fit the thread limit with the producer warp
     int rs = 1;
     while (rs < 8 && 2 * rs * slices * kSlice <= kGroupMaxThreads - kWarp)
@@ -340,7 +365,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     const size_t rope_bytes =
         MODE == kGRope ? ((size_t)umax * MT * 8 + 15) / 16 * 16 : 0;
     const size_t fixed = 16 * 8 + ((red_bytes + 15) / 16) * 16 + rope_bytes +
-                         ximg_bytes(MT, p.G);
+                         ximg_bytes(MT, nchunk, GS == 32);
     if (fixed >= kGroupSmemCap) return cudaSuccess;
     int stages = (int)((kGroupSmemCap - fixed) / stage_bytes);
     if (stages > 8) stages = 8;
@@ -363,8 +388,8 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     }
     const size_t rope_off = ring + 16 * stages + ((red_bytes + 15) / 16) * 16;
     const size_t xenc_off = rope_off + rope_bytes;
-    const size_t smem = xenc_off + ximg_bytes(MT, p.G);
-    auto kern = qmv_group_kernel<BITS, MT, MODE, RPH>;
+    const size_t smem = xenc_off + ximg_bytes(MT, nchunk, GS == 32);
+    auto kern = qmv_group_kernel<BITS, MT, MODE, RPH, GS>;
     int dummy = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),
                                    threads, smem, &dummy);
@@ -379,28 +404,42 @@ static bool aligned16g(const void *q) {
     return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
 }
 
-// Launches the group-per-lane kernel when the shape allows it (one token,
-// row strides of scales multiple of 16 bytes, 16-byte aligned bases);
-// *used tells the caller whether it ran.
+template <int GS>
+static cudaError_t launch_group_gs(int mode, const DenseParams &p,
+                                   cudaStream_t st, bool *used) {
+    if (mode == kGRope)
+        return p.bits == 4 ? launch_group_r<4, 1, kGRope, 2, GS>(p, st, used)
+                           : launch_group_r<8, 1, kGRope, 2, GS>(p, st, used);
+    if (p.bits == 4) {
+        if (mode == kGPlain)
+            return launch_group_r<4, 1, kGPlain, 2, GS>(p, st, used);
+        if (mode == kGSections)
+            return launch_group_r<4, 1, kGSections, 2, GS>(p, st, used);
+        return launch_group_r<4, 1, kGGateUp, 2, GS>(p, st, used);
+    }
+    if (mode == kGPlain) return launch_group_r<8, 1, kGPlain, 2, GS>(p, st, used);
+    if (mode == kGSections)
+        return launch_group_r<8, 1, kGSections, 2, GS>(p, st, used);
+    return launch_group_r<8, 1, kGGateUp, 2, GS>(p, st, used);
+}
+
+// Launches the chunk-per-lane kernel when the shape allows it (one token,
+// u4 or u8 codes in groups of 32, 64 or 128, whole 64-input chunks, row
+// strides of scales multiple of 16 bytes, 16-byte aligned bases); *used
+// tells the caller whether it ran.
 cudaError_t launch_group(int mode, const DenseParams &p, cudaStream_t st,
                          bool *used) {
     *used = false;
-    if (p.M != 1 || (p.G % 8) != 0 || !aligned16g(p.sc) ||
-        !aligned16g(p.bi) || !aligned16g(p.wq))
+    if (p.M != 1 || (p.bits != 4 && p.bits != 8) || (p.K % 64) != 0 ||
+        (p.G % 8) != 0 || !aligned16g(p.sc) || !aligned16g(p.bi) ||
+        !aligned16g(p.wq))
         return cudaSuccess;
-    if (mode == kGRope)
-        return p.bits == 4 ? launch_group_r<4, 1, kGRope, 2>(p, st, used)
-                           : launch_group_r<8, 1, kGRope, 2>(p, st, used);
-    if (p.bits == 4) {
-        if (mode == kGPlain) return launch_group_r<4, 1, kGPlain, 2>(p, st, used);
-        if (mode == kGSections)
-            return launch_group_r<4, 1, kGSections, 2>(p, st, used);
-        return launch_group_r<4, 1, kGGateUp, 2>(p, st, used);
+    switch (p.group) {
+        case 64: return launch_group_gs<64>(mode, p, st, used);
+        case 32: return launch_group_gs<32>(mode, p, st, used);
+        case 128: return launch_group_gs<128>(mode, p, st, used);
+        default: return cudaSuccess;
     }
-    if (mode == kGPlain) return launch_group_r<8, 1, kGPlain, 2>(p, st, used);
-    if (mode == kGSections)
-        return launch_group_r<8, 1, kGSections, 2>(p, st, used);
-    return launch_group_r<8, 1, kGGateUp, 2>(p, st, used);
 }
 
 unsigned int group_timeouts(bool reset) {

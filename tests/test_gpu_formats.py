@@ -1,6 +1,7 @@
 """GPU parity of the code widths and group sizes outside the tuned kernels
 (u2, u3, u6, and groups of 32 and 128 at every width), which run on the
-general-format decode kernel, against the oracle (same packed format: a
+general-format decode kernel (one token of u4 / u8 in groups of 32 or 128:
+on the one-token chunk kernel), against the oracle (same packed format: a
 row's words are one little-endian bit stream, code k at bits [b*k, +b),
 lowest bits first, so u3 and u6 codes straddle words; one bf16 scale and
 bias per group; "saragossa", "Quantization formats").
@@ -130,3 +131,68 @@ def test_gate_up_full_shape_sampled(bits):
     ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits,
                               group=64, cols=cols)
     close(h[:, torch.from_numpy(cols).cuda()], ref, f"u{bits} full shape")
+
+
+# One token of u4 / u8 codes in groups of 32 or 128: the chunk-per-lane
+# kernel (a lane owns 64 inputs: half a group of 128, or two groups of 32
+# with a dot per half) wherever the scale rows are whole 16-byte units;
+# K = 13824 at groups of 128 (108 groups a row) takes the general kernel.
+ONE_TOKEN = [(4, 32), (4, 128), (8, 32), (8, 128)]
+
+
+@pytest.mark.parametrize("bits,group", ONE_TOKEN)
+@pytest.mark.parametrize("N,K", [(777, 2048), (5120, 5120), (45, 13824)])
+def test_one_token_chunk_kernel(bits, group, N, K):
+    w = synth.qweight(800 + bits + group + N, N, K, bits, group)
+    x = synth.activations(801 + K, 1, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w))
+    torch.cuda.synchronize()
+    close(y, oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits, group),
+          f"u{bits} g{group} N={N} K={K}")
+
+
+@pytest.mark.parametrize("bits,group", ONE_TOKEN)
+def test_one_token_chunk_kernel_fused(bits, group):
+    """Sections with biases, gate+up SiLU and QKV with the rotary embedding
+    (heads of 64) at one token."""
+    K = 2048
+    rng = np.random.default_rng(810 + bits + group)
+    sizes = [512, 128, 128]
+    w = synth.qweight(811 + group, sum(sizes), K, bits, group)
+    x = synth.activations(812, 1, K)
+    bias = [synth.bf16_bits(rng.normal(0, 0.5, size=s).astype(np.float32))
+            for s in sizes]
+    dw = dev_qweight(w)
+    outs = gwa.qmv_fused_sections(dev_bf16(x), dw, sizes,
+                                  out_bias=[dev_bf16(b) for b in bias])
+    refs = oracle.fused_sections(x, w.wq, w.scales, w.biases, sizes, K, bits,
+                                 group=group, out_bias=bias)
+    for o, r in zip(outs, refs):
+        close(o, r, "sections")
+    g = synth.qweight(813 + group, 2 * 333, K, bits, group)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(g))
+    close(h, oracle.gate_up_silu(x, g.wq, g.scales, g.biases, 2 * 333, K, bits,
+                                 group=group), "gate+up")
+    pos = np.array([77], dtype=np.int32)
+    got = gwa.qmv_qkv_rope(dev_bf16(x), dw, 512, 128, 64, 1e4,
+                           torch.from_numpy(pos).cuda())
+    ref = oracle.qkv_rope(x, w.wq, w.scales, w.biases, 512, 128, K, bits, 64,
+                          1e4, pos, group=group)
+    for o, r in zip(got, ref):
+        close(o, r, "rope")
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bits,group", [(4, 32), (4, 128)])
+def test_one_token_chunk_kernel_full_shape_sampled(bits, group):
+    """The 27648 x 5120 gate+up weight at one token, the launch the formats
+    bench times: 512 sampled outputs against the oracle."""
+    K, I = 5120, 13824
+    w = synth.qweight(820 + group, 2 * I, K, bits, group)
+    x = synth.activations(821, 1, K)
+    h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(group).choice(I, size=512, replace=False)
+    ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits,
+                              group=group, cols=cols)
+    close(h[:, torch.from_numpy(cols).cuda()], ref, f"u{bits} g{group} full")
