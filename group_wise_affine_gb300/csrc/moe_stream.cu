@@ -173,29 +173,6 @@ struct MsTasks {
     }
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile(
-        "barrier.cluster.arrive.release;\n"
-        "barrier.cluster.wait.acquire;" ::
-            : "memory");
-}
-// fp32 at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster_f32(const float *local,
-                                                uint32_t rank) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(a)
-                 : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-
 template <int BITS, int MODE, int W>
 __global__ void __maxnreg__(128)
     moe_stream_kernel(MoeParams p, int stages, int rs, int ups, int cl,

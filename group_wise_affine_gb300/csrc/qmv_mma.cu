@@ -39,6 +39,10 @@
 // Itself", "The two fusions"; "saragossa", "Quantization formats").
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -131,7 +135,12 @@ __device__ __forceinline__ void mma_load_x(const uint16_t *__restrict__ x, int M
 }
 
 // 168 registers: up to 11 warps (10 consumers and the producer) per CTA.
-template <int BITS, int MODE>
+// KS > 1: rows longer than 5120 inputs, cut along K over a cluster of KS
+// CTAs.  Rank r streams inputs [r K/KS, (r+1) K/KS) of the cluster's rows
+// (one bulk copy per row segment) and keeps those activations; the ranks'
+// partial sums meet in rank 0 over distributed shared memory, added in rank
+// order, and rank 0 runs the epilogue.
+template <int BITS, int MODE, int KS>
 __global__ void __maxnreg__(168)
     qmv_mma_kernel(DenseParams p, int stages, int64_t units, int nw) {
     constexpr int HALVES = (MODE == kMGateUp || MODE == kMRope) ? 2 : 1;
@@ -143,8 +152,15 @@ __global__ void __maxnreg__(168)
     const int ncons = nw * kWarp;
     const int lane = tid & (kWarp - 1), warp = tid / kWarp;
     const int M = p.M;
-    const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
-    const uint32_t sbrow = (uint32_t)p.G * 2;
+    const int rank = KS > 1 ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / KS, ncl = gridDim.x / KS;
+    const int Ks = p.K / KS;      // inputs of a row this CTA covers
+    const int Gs = Ks / kGroup;   // their groups
+    // a row's share in a stage; whole rows in memory
+    const uint32_t rowbytes = (uint32_t)Ks * BITS / 8;
+    const uint32_t sbrow = (uint32_t)Gs * 2;
+    const uint32_t growbytes = (uint32_t)p.K * BITS / 8;
+    const uint32_t gsbrow = (uint32_t)p.G * 2;
     const uint32_t rows_stage = (uint32_t)(HALVES * ups);
     const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
@@ -154,8 +170,8 @@ __global__ void __maxnreg__(168)
 
     // rope: whole stages per CTA (8 divides d/2), so no stage crosses a head
     const int64_t ualign = MODE == kMRope ? ups : 1;
-    const int64_t u0 = units / ualign * blockIdx.x / gridDim.x * ualign;
-    const int64_t u1 = units / ualign * (blockIdx.x + 1) / gridDim.x * ualign;
+    const int64_t u0 = units / ualign * cid / ncl * ualign;
+    const int64_t u1 = units / ualign * (cid + 1) / ncl * ualign;
     const int nu = (int)(u1 - u0);
     const int nst = (nu + ups - 1) / ups;
 
@@ -196,10 +212,29 @@ __global__ void __maxnreg__(168)
                 for (int h = 0; h < HALVES; ++h) {
                     const int64_t r = MODE == kMRope ? rope_pair_row(ua, h, p.rope_hd)
                                                      : ua + (h ? p.I : 0);
-                    bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes, n * rowbytes,
-                             &full[s]);
-                    bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow, &full[s]);
-                    bulk_g2s(dbi + h * ups * sbrow, bi + r * sbrow, n * sbrow, &full[s]);
+                    if constexpr (KS == 1) {
+                        bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
+                                 n * rowbytes, &full[s]);
+                        bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
+                                 &full[s]);
+                        bulk_g2s(dbi + h * ups * sbrow, bi + r * sbrow, n * sbrow,
+                                 &full[s]);
+                    } else {
+                        // this rank's segment of each row
+                        for (int i = 0; i < n; ++i) {
+                            const int64_t ri = r + i;
+                            const uint32_t d = (uint32_t)(h * ups + i);
+                            bulk_g2s(base + d * rowbytes,
+                                     wq + ri * growbytes + (uint32_t)rank * rowbytes,
+                                     rowbytes, &full[s]);
+                            bulk_g2s(dsc + d * sbrow,
+                                     sc + ri * gsbrow + (uint32_t)rank * sbrow, sbrow,
+                                     &full[s]);
+                            bulk_g2s(dbi + d * sbrow,
+                                     bi + ri * gsbrow + (uint32_t)rank * sbrow, sbrow,
+                                     &full[s]);
+                        }
+                    }
                 }
                 s_issued = st + 1;
             }
@@ -210,7 +245,7 @@ __global__ void __maxnreg__(168)
         const int gbase = warp * kMmaGroupsPerWarp;
         MmaX xr;
         pdl_wait_primary();  // x may be the previous kernel's output
-        mma_load_x<BITS>(p.x, M, p.K, warp, g, t, xr);
+        mma_load_x<BITS>(p.x + (int64_t)rank * Ks, M, p.K, warp, g, t, xr);
         for (int st = 0; st < nst; ++st) {
             const int s = st % stages;
             if (!mbar_wait(&full[s], (st / stages) & 1)) {
@@ -267,7 +302,7 @@ __global__ void __maxnreg__(168)
                     // ... and gets the products of token g with rows 2t, 2t + 1
 #pragma unroll
                     for (int v = 0; v < 2; ++v) {
-                        const uint32_t so = ((uint32_t)(h * ups + 2 * t + v) * p.G + gg) * 2u;
+                        const uint32_t so = ((uint32_t)(h * ups + 2 * t + v) * Gs + gg) * 2u;
                         const float sv =
                             bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(scb + so));
                         const float bv =
@@ -308,13 +343,31 @@ __global__ void __maxnreg__(168)
     __syncthreads();
 
     // ---------------------------------------------------- epilogue
-    // the warps' slots of an output, added in a fixed order
+    if constexpr (KS > 1) {
+        // this CTA's sum over its warps, in place of the first warp's slot
+        for (int i = tid; i < nu * HALVES * M; i += blockDim.x) {
+            float v = 0.f;
+            for (int w = 0; w < nw; ++w) v += red[i * nw + w];
+            red[i * nw] = v;
+        }
+        cluster_sync_all();
+    }
+    // the warps' slots of an output (the ranks' sums), added in a fixed order
     auto total = [&](int idx) {
         float v = 0.f;
-        for (int w = 0; w < nw; ++w) v += red[idx * nw + w];
+        if constexpr (KS > 1) {
+            float part[KS];  // all ranks' loads in flight at once
+#pragma unroll
+            for (int q = 0; q < KS; ++q)
+                part[q] = ld_cluster_f32(red + idx * nw, (uint32_t)q);
+#pragma unroll
+            for (int q = 0; q < KS; ++q) v += part[q];
+        } else {
+            for (int w = 0; w < nw; ++w) v += red[idx * nw + w];
+        }
         return v;
     };
-    for (int i = tid; i < nu * M; i += blockDim.x) {
+    for (int i = tid; i < (rank == 0 ? nu * M : 0); i += blockDim.x) {
         const int lu = i / M, m = i % M;
         const int64_t n = u0 + lu;
         if constexpr (MODE == kMGateUp) {
@@ -355,41 +408,103 @@ __global__ void __maxnreg__(168)
             p.sec_out[s][(int64_t)m * size + j] = f32_to_bf16_bits(val);
         }
     }
+    // no CTA leaves while rank 0 still reads its sums
+    if constexpr (KS > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------ host side
-template <int BITS, int MODE>
+// Clusters of `cl` CTAs of `kern` the GPU can keep resident at once
+// (cached per device, kernel, cluster size, block and shared memory).
+static int mma_resident_clusters(const void *kern, int cl, int threads,
+                                 size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, kern, cl, threads, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+template <int BITS, int MODE, int KS>
 static cudaError_t launch_mma_t(const DenseParams &p, cudaStream_t st, bool *used) {
     constexpr int HALVES = (MODE == kMGateUp || MODE == kMRope) ? 2 : 1;
     const int64_t units = MODE == kMGateUp ? p.I : MODE == kMRope ? p.N / 2 : p.N;
     if (units <= 0) return cudaSuccess;
     if (MODE == kMRope && (p.rope_hd / 2) % kMmaUnits != 0)
         return cudaSuccess;  // not used: stages would cross heads
-    const int nw = p.K / (kGroup * kMmaGroupsPerWarp);
+    const int Ks = p.K / KS;
+    const int nw = Ks / (kGroup * kMmaGroupsPerWarp);
     const int threads = (nw + 1) * kWarp;
-    const size_t rowbytes = (size_t)p.K * BITS / 8;
-    const size_t sbrow = (size_t)p.G * 2;
+    const size_t rowbytes = (size_t)Ks * BITS / 8;
+    const size_t sbrow = (size_t)(Ks / kGroup) * 2;
     const size_t stage_bytes = (size_t)HALVES * kMmaUnits * (rowbytes + 2 * sbrow);
-    int grid = num_sms();
     const int64_t ualign = MODE == kMRope ? kMmaUnits : 1;
-    if ((int64_t)grid > units / ualign) grid = (int)(units / ualign);
-    if (grid < 1) return cudaSuccess;
-    const int64_t umax = (units / ualign + grid - 1) / grid * ualign;
-    const size_t red_bytes = (size_t)umax * HALVES * p.M * nw * 4;
-    if (red_bytes + 2 * (stage_bytes + 16) > kMaxDynSmem) return cudaSuccess;
-    int stages = (int)((kMaxDynSmem - red_bytes) / (stage_bytes + 16));
-    const int cap = (int)(kMmaRingTarget / stage_bytes);
-    if (stages > cap) stages = cap;
-    if (stages > 8) stages = 8;
-    if (stages < 2) stages = 2;
-    const size_t smem = stages * (stage_bytes + 16) + red_bytes;
-    auto kern = qmv_mma_kernel<BITS, MODE>;
+    int ncl = num_sms() / KS;  // clusters (CTAs when KS = 1)
+    if ((int64_t)ncl > units / ualign) ncl = (int)(units / ualign);
+    if (ncl < 1) return cudaSuccess;
+    int stages = 0;
+    size_t smem = 0;
+    // ring stages and shared memory for ncl clusters (false: does not fit)
+    auto plan = [&](int n) {
+        const int64_t umax = (units / ualign + n - 1) / n * ualign;
+        const size_t red_bytes = (size_t)umax * HALVES * p.M * nw * 4;
+        if (red_bytes + 2 * (stage_bytes + 16) > kMaxDynSmem) return false;
+        stages = (int)((kMaxDynSmem - red_bytes) / (stage_bytes + 16));
+        const int cap = (int)(kMmaRingTarget / stage_bytes);
+        if (stages > cap) stages = cap;
+        if (stages > 8) stages = 8;
+        if (stages < 2) stages = 2;
+        smem = stages * (stage_bytes + 16) + red_bytes;
+        return true;
+    };
+    if (!plan(ncl)) return cudaSuccess;
+    auto kern = qmv_mma_kernel<BITS, MODE, KS>;
     int dummy = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern), threads, smem,
                                    &dummy);
     if (e != cudaSuccess) return e;
+    if constexpr (KS > 1) {
+        // one wave: no more clusters than the GPU keeps resident
+        const int res = mma_resident_clusters(reinterpret_cast<const void *>(kern), KS,
+                                              threads, smem);
+        if (res < 1) return cudaSuccess;
+        if (res < ncl) {
+            ncl = res;
+            if (!plan(ncl)) return cudaSuccess;
+            e = occupancy_grid(reinterpret_cast<const void *>(kern), threads, smem,
+                               &dummy);
+            if (e != cudaSuccess) return e;
+        }
+        *used = true;
+        return launch_pdl_cluster(reinterpret_cast<const void *>(kern),
+                                  (unsigned)(ncl * KS), (unsigned)KS, (unsigned)threads,
+                                  smem, st, p, stages, units, nw);
+    }
     *used = true;
-    return launch_pdl(reinterpret_cast<const void *>(kern), (unsigned)grid,
+    return launch_pdl(reinterpret_cast<const void *>(kern), (unsigned)ncl,
                       (unsigned)threads, smem, st, p, stages, units, nw);
 }
 
@@ -397,23 +512,44 @@ static bool mma_aligned16(const void *q) {
     return (reinterpret_cast<uintptr_t>(q) & 15) == 0;
 }
 
+constexpr int kMmaMaxSplit = 4;  // CTAs per cluster along K
+
 // Runs the tensor-core decode kernel for up to 8 tokens in one pass when the
-// shape allows it (u4/u8 at group 64, K a multiple of 512 up to 5120, so a
-// row's scales are whole 16-byte units for the bulk copies; 16-byte aligned
-// weights); *used tells the caller whether it ran.
+// shape allows it (u4/u8 at group 64, K a multiple of 512, so a row's scales
+// are whole 16-byte units for the bulk copies; 16-byte aligned weights).
+// Rows of up to 5120 inputs run on one CTA each; longer rows of a plain
+// projection on a cluster of KS CTAs along K, the smallest KS for which
+// K / KS is a multiple of 512 and at most 5120.  *used tells the caller
+// whether it ran.
 cudaError_t launch_mma(int mode, const DenseParams &p, cudaStream_t st, bool *used) {
     *used = false;
     if (p.M < 2 || p.M > kMmaTokens || (p.bits != 4 && p.bits != 8) ||
-        p.group != kGroup || p.K % 512 != 0 ||
-        p.K > kGroup * kMmaGroupsPerWarp * kMmaMaxWarps || !mma_aligned16(p.wq) ||
+        p.group != kGroup || p.K % 512 != 0 || !mma_aligned16(p.wq) ||
         !mma_aligned16(p.sc) || !mma_aligned16(p.bi))
         return cudaSuccess;
-#define GWA_MMA_CASE(B)                                                         \
+    constexpr int kMaxK = kGroup * kMmaGroupsPerWarp * kMmaMaxWarps;
+    if (p.K > kMaxK) {
+        if (mode != kMPlain) return cudaSuccess;
+        int ks = 2;
+        while (ks <= kMmaMaxSplit && (p.K % (512 * ks) != 0 || p.K / ks > kMaxK)) ++ks;
+        if (ks > kMmaMaxSplit) return cudaSuccess;
+#define GWA_MMA_SPLIT(B)                                                        \
     if (p.bits == B) {                                                          \
-        if (mode == kMPlain) return launch_mma_t<B, kMPlain>(p, st, used);      \
-        if (mode == kMSections) return launch_mma_t<B, kMSections>(p, st, used); \
-        if (mode == kMRope) return launch_mma_t<B, kMRope>(p, st, used);        \
-        return launch_mma_t<B, kMGateUp>(p, st, used);                          \
+        if (ks == 2) return launch_mma_t<B, kMPlain, 2>(p, st, used);           \
+        if (ks == 3) return launch_mma_t<B, kMPlain, 3>(p, st, used);           \
+        return launch_mma_t<B, kMPlain, 4>(p, st, used);                        \
+    }
+        GWA_MMA_SPLIT(4)
+        GWA_MMA_SPLIT(8)
+#undef GWA_MMA_SPLIT
+        return cudaSuccess;
+    }
+#define GWA_MMA_CASE(B)                                                            \
+    if (p.bits == B) {                                                             \
+        if (mode == kMPlain) return launch_mma_t<B, kMPlain, 1>(p, st, used);      \
+        if (mode == kMSections) return launch_mma_t<B, kMSections, 1>(p, st, used); \
+        if (mode == kMRope) return launch_mma_t<B, kMRope, 1>(p, st, used);        \
+        return launch_mma_t<B, kMGateUp, 1>(p, st, used);                          \
     }
     GWA_MMA_CASE(4)
     GWA_MMA_CASE(8)

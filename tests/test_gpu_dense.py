@@ -199,6 +199,44 @@ def test_gate_up_silu_config_full(M):
     assert_close(bf16_to_f64(h), ref, f"gate_up config M={M}")
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [5, 8])
+@pytest.mark.parametrize("N,K", [(301, 6144), (1000, 13824), (19, 20480),
+                                 (8, 7680)])
+def test_rows_split_over_a_cluster(bits, M, N, K):
+    # 5..8 tokens on rows longer than 5120 inputs: the tensor-core decode
+    # kernel on clusters of 2 (K = 6144), 3 (7680, 13824) or 4 (20480) CTAs
+    # along K; N ragged against the 8-row stages and the cluster count.  The
+    # output sits between guard bands: only rank 0 of a cluster writes.
+    w = synth.qweight(400 + N + bits, N, K, bits)
+    x = synth.activations(410 + M, M, K)
+    buf, y, pad = _guarded(M, N)
+    gwa.qmv_affine(dev_bf16(x), dev_qweight(w), y=y)
+    torch.cuda.synchronize()
+    _check_guards(buf, pad)
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+    assert_close(bf16_to_f64(y), ref, f"M={M} N={N} K={K} u{bits}")
+    # deterministic: the ranks' sums are added in a fixed order
+    y2 = gwa.qmv_affine(dev_bf16(x), dev_qweight(w))
+    assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_down_config_full_eight_tokens(bits):
+    # the stack's down projection (13824 -> 5120) at 8 tokens in one pass on
+    # clusters of three CTAs, against the oracle and two 4-token calls
+    N, K = 5120, 13824
+    w = synth.qweight(synth.seed_for(3, 0, 3) + bits, N, K, bits)
+    xh = synth.activations(synth.seed_for(3, 0, 9), 8, K)
+    dw, x = dev_qweight(w), dev_bf16(xh)
+    y8 = gwa.qmv_affine(x, dw)
+    y4 = torch.cat([gwa.qmv_affine(x[i:i + 4], dw) for i in (0, 4)])
+    torch.cuda.synchronize()
+    ref = oracle.qmv(xh, w.wq, w.scales, w.biases, N, K, bits)
+    assert_close(bf16_to_f64(y8), ref, f"down M=8 u{bits}")
+    assert_close(bf16_to_f64(y4), ref, f"down 2x4 tokens u{bits}")
+
+
 # ---------------------------------------------------------------- edges
 def test_empty_inputs_are_no_ops():
     w = dev_qweight(synth.qweight(600, 16, 128, 4))
