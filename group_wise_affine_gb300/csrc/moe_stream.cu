@@ -39,6 +39,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "cluster.cuh"
 #include "group_dot.cuh"
 #include "internal.h"
 

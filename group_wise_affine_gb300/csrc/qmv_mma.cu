@@ -43,6 +43,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
