@@ -1,5 +1,6 @@
 // Decode kernel for 5..8 tokens on the tensor cores (u4/u8 codes, groups of
-// 64; rows of 512..5120 inputs): the same weight stream as the streaming
+// 64; rows of 512..5120 inputs on one CTA, longer rows of a plain projection
+// cut along K over a thread-block cluster): the same weight stream as the streaming
 // decode kernel (a producer thread copies the rows of a CTA's units into a
 // shared-memory ring with the bulk-copy engine), but the consumers form the
 // products with warp-level bf16 MMAs (m16n8k16, fp32 accumulation):
