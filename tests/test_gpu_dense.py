@@ -204,10 +204,11 @@ def test_gate_up_silu_config_full(M):
 @pytest.mark.parametrize("N,K", [(301, 6144), (1000, 13824), (19, 20480),
                                  (8, 7680)])
 def test_rows_split_over_a_cluster(bits, M, N, K):
-    # 5..8 tokens on rows longer than 5120 inputs: the tensor-core decode
-    # kernel on clusters of 2 (K = 6144), 3 (7680, 13824) or 4 (20480) CTAs
-    # along K; N ragged against the 8-row stages and the cluster count.  The
-    # output sits between guard bands: only rank 0 of a cluster writes.
+    # 5..8 tokens on rows longer than 5120 inputs: for u8 the tensor-core
+    # decode kernel on clusters of 2 (K = 6144), 3 (7680, 13824) or 4 (20480)
+    # CTAs along K, for u4 the streaming kernel in two passes; N ragged
+    # against the 8-row stages and the cluster count.  The output sits
+    # between guard bands: only rank 0 of a cluster writes.
     w = synth.qweight(400 + N + bits, N, K, bits)
     x = synth.activations(410 + M, M, K)
     buf, y, pad = _guarded(M, N)
@@ -223,8 +224,8 @@ def test_rows_split_over_a_cluster(bits, M, N, K):
 
 @pytest.mark.parametrize("bits", [4, 8])
 def test_down_config_full_eight_tokens(bits):
-    # the stack's down projection (13824 -> 5120) at 8 tokens in one pass on
-    # clusters of three CTAs, against the oracle and two 4-token calls
+    # the stack's down projection (13824 -> 5120) at 8 tokens (u8: one pass
+    # on clusters of three CTAs), against the oracle and two 4-token calls
     N, K = 5120, 13824
     w = synth.qweight(synth.seed_for(3, 0, 3) + bits, N, K, bits)
     xh = synth.activations(synth.seed_for(3, 0, 9), 8, K)
