@@ -348,6 +348,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
         W8 = stack_weights(8, L, dev)
         extras["stack_u8_M1"] = run_stack_extra(W8, 1, dev, 50, 3)
         extras["stack_u8_M4"] = run_stack_extra(W8, 4, dev, 30, 3)
+        extras["stack_u8_M8"] = run_stack_extra(W8, 8, dev, 30, 3)
         extras["prefill_stack_u8_M512"] = run_stack_extra(W8, 512, dev, 5, 2)
         del W8
         torch.cuda.empty_cache()
