@@ -276,6 +276,10 @@ static int run_prefill(const QmmArgs &a, int mode, const DenseParams &p,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
         return fail(GWA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned",
                     fn);
+    // the decode kernels raise no status: the word reads 0 after the call,
+    // as after a tensor-core call that met no problem
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     return run_dense(mode, p, a.M, out_stride, sec_sizes, st, fn);
 }
 
@@ -470,6 +474,10 @@ int gwa_qmv_qkv_rope(const uint16_t *x, int64_t M, gwa_qweight w,
     if (e != cudaSuccess) return cuda_fail(e, fn);
     r.rope_cs = cs;
     if (M > 8) {
+        // the status word reads 0 after a call that met no problem, on the
+        // decode kernels as on the tensor cores
+        e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
         // tensor cores when the shape allows it and each head and section
         // is whole inside the 128-row tiles
         QmmArgs a{};

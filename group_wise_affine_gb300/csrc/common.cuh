@@ -9,6 +9,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,7 +76,8 @@ namespace gwa {
 // largest magnitude maps into [2^14, 2^15)).  A bf16 value carries 8
 // significant bits, so every value within 2^7 of the group's largest
 // exponent is represented exactly; smaller ones round to the group's quantum
-// (at most 2^-15 of the largest magnitude).  Codes stay unsigned bytes, and
+// (at most 2^-15 of the largest magnitude; groups where that matters take
+// an fp32 path, see "marked groups" below).  Codes stay unsigned bytes, and
 // dp2a forms two 16x8-bit products per instruction into an int32 (at most
 // 64 * 255 * 32640 < 2^31 per group).  Per group:
 //   y += (scale * 2^E) * D + bias * sum_k x_k,   D = sum_k q_k * xi_k.
@@ -87,6 +89,13 @@ __device__ __forceinline__ int dp2a_lo(uint32_t a16, uint32_t b8, int c) {
 __device__ __forceinline__ int dp2a_hi(uint32_t a16, uint32_t b8, int c) {
     int d;
     asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a16), "r"(b8), "r"(c));
+    return d;
+}
+// Four unsigned code bytes times four signed bytes (a residual plane, see
+// "marked groups"), added to c.
+__device__ __forceinline__ int dp4a_us(uint32_t a8, uint32_t b8, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a8), "r"(b8), "r"(c));
     return d;
 }
 
@@ -153,6 +162,138 @@ __device__ __forceinline__ int dot_total(const int (&acc)[2]) {
     return BITS == 4 ? acc[0] + (acc[1] >> 4) : acc[0] + acc[1];
 }
 
+// ------------------------------------------------------- marked groups
+// The one-plane encoding above is exact when a group's values lie within
+// 2^7 of its largest one; smaller values round to the group's quantum f.
+// One large activation among ordinary ones (an outlier channel), or values
+// spread over many binades (a gated product such as SiLU(g) * u), then
+// round many values of the group, and an output whose products cancel loses
+// more than the fp32 sum it stands for.  So every encoder also forms, per
+// group and in units of f,
+//   R = sum_k |x_k / f - xi_k|   (the rounding error, exact term by term)
+//   A = sum_k |x_k| / f,
+// and marks the group when R > 2^-16 * A (an unmarked group thus has
+// sum_k |x_k - f * xi_k| <= 2^-16 * sum_k |x_k|, 128 times less than
+// rounding its activations to bf16 once more).  Measured on 20000 groups:
+// N(0,1) activations reach R / A = 2^-16.9 at most (none marked), Laplace
+// ones mark 0.09% of groups, SiLU(g) * u with g, u ~ N(0,1) 18%, and one
+// value 30 times the rest of its group, or magnitudes spread over 2^20,
+// mark it.  A marked group is finished one of two ways:
+//  * two planes (the one- and few-token decode kernels): the int16 image
+//    stays, and the lane adds a second dot with the int8 residual plane
+//    lo_k = rint(2^7 * (x_k / f - xi_k)) (dp4a, four products per
+//    instruction): the rounding error drops below 2^-8 f per value, so
+//    R <= 0.25 and, as A >= 2^14 always, R <= 2^-16 * A for every input;
+//  * fp32 (the other kernels): the group keeps its raw bf16 activations in
+//    the slots of its int16 pairs (same size, same pair order), its stored
+//    scale is negative, and its dots are taken by the fp32 counterparts of
+//    dp2a below (codes and activations exact, every product exact, fp32
+//    sums).
+// The kernels decide per warp (or per CTA), before their main loop, whether
+// any lane holds a marked group, and run a copy of the loop without the
+// marked path otherwise.
+__device__ __forceinline__ bool group_marked(float r, float a) {
+    return r * 65536.0f > a;
+}
+
+// |v * finv - rint(v * finv)|, exact: v is a bf16 value and finv a power of
+// two, so v * finv is exact; adding 1.5 * 2^23 rounds it to the integer the
+// encoders store (half to even), and the difference has no more bits than v.
+__device__ __forceinline__ float i16_resid(float v, float finv) {
+    const float t = fmaf(v, finv, 12582912.0f) - 12582912.0f;
+    return fabsf(fmaf(v, finv, -t));
+}
+
+// Signed 2^7 * (v * finv - rint(v * finv)) rounded to an integer in
+// [-64, 64], as the low byte of the result (two's complement): one entry
+// of a residual plane.  Both roundings are half to even.
+__device__ __forceinline__ uint32_t i8_resid(float v, float finv) {
+    const float t = fmaf(v, finv, 12582912.0f) - 12582912.0f;
+    const float r = fmaf(v, finv, -t);  // exact, in [-0.5, 0.5]
+    return __float_as_uint(fmaf(r, 128.0f, 12582912.0f)) & 0xffu;
+}
+
+// The raw bf16 pair (lo = a, hi = b) of two values widened from bf16.
+__device__ __forceinline__ uint32_t raw_pair(float a, float b) {
+    return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
+}
+
+// Byte I of b as an exact fp32 value: the permute builds 2^23 + byte, and
+// subtracting 2^23 is exact.
+template <int I>
+__device__ __forceinline__ float byte_f32(uint32_t b) {
+    return __uint_as_float(__byte_perm(b, 0x4b000000u, 0x7440 | I)) - 8388608.0f;
+}
+
+// fp32 counterparts of dp2a_lo / dp2a_hi for a marked group: a holds two raw
+// bf16 activations, b the code bytes; every product is exact (8 by 8
+// significant bits), the sums round in fp32.
+__device__ __forceinline__ float fdp2a_lo(uint32_t a, uint32_t b, float c) {
+    return fmaf(bf16_hi(a), byte_f32<1>(b), fmaf(bf16_lo(a), byte_f32<0>(b), c));
+}
+__device__ __forceinline__ float fdp2a_hi(uint32_t a, uint32_t b, float c) {
+    return fmaf(bf16_hi(a), byte_f32<3>(b), fmaf(bf16_lo(a), byte_f32<2>(b), c));
+}
+
+// word_dot_u4 / word_dot_u8 and dot_total in fp32 (one chunk word at a
+// time): the true sum of q_k * x_k, the u4 high nibbles' 16x divided out.
+__device__ __forceinline__ void fword_dot_u4(uint32_t w, const uint32_t *pr,
+                                             float (&acc)[2]) {
+    const uint32_t lo = w & 0x0f0f0f0fu;
+    const uint32_t hi = w & 0xf0f0f0f0u;
+    acc[0] = fdp2a_hi(pr[1], lo, fdp2a_lo(pr[0], lo, acc[0]));
+    acc[1] = fdp2a_hi(pr[3], hi, fdp2a_lo(pr[2], hi, acc[1]));
+}
+__device__ __forceinline__ void fword_dot_u8(uint32_t w, const uint32_t *pr,
+                                             float (&acc)[2]) {
+    acc[0] = fdp2a_lo(pr[0], w, acc[0]);
+    acc[1] = fdp2a_hi(pr[1], w, acc[1]);
+}
+template <int BITS>
+__device__ __forceinline__ float fdot_total(const float (&acc)[2]) {
+    return BITS == 4 ? fmaf(acc[1], 0.0625f, acc[0]) : acc[0] + acc[1];
+}
+
+// Element i (a run-time index) of a register array, by a chain of selects
+// (no local-memory indexing); used by the marked paths, which run one row at
+// a time so that their registers stay few.
+template <typename T, int N>
+__device__ __forceinline__ T pick(const T (&a)[N], int i) {
+    T v = a[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k)
+        if (i == k) v = a[k];
+    return v;
+}
+
+// sum_k q_k * x_k of one 16-byte chunk word by word (fword_dot_*), w the
+// chunk's four code words and pr its activation pairs (4 per word for u4, 2
+// for u8) as raw bf16: a marked chunk's dot in fp32.  One word per loop
+// step, so that only that word's products are in flight.
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_f32(const uint4 &w,
+                                               const uint32_t (&pr)[BITS == 4 ? 16 : 8]) {
+    constexpr int P = BITS == 4 ? 4 : 2;
+    float a[2] = {0.f, 0.f};
+#pragma unroll 1
+    for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t word = wd == 0 ? w.x : wd == 1 ? w.y : wd == 2 ? w.z : w.w;
+        uint32_t p[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            p[i] = pr[i];
+#pragma unroll
+            for (int k = 1; k < 4; ++k)
+                if (wd == k) p[i] = pr[k * P + i];
+        }
+        if constexpr (BITS == 4)
+            fword_dot_u4(word, p, a);
+        else
+            fword_dot_u8(word, p, a);
+    }
+    return fdot_total<BITS>(a);
+}
+
 }  // namespace gwa
 
 // ---------------------------------------------------------------- async copy
@@ -171,6 +312,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Named barrier `id` over `nthreads` threads (whole warps) that also ORs a
+// predicate across them.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((int)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -27,6 +27,8 @@ struct GroupX {
     float xs[MT];         // plain fp32 sum of the chunk's activations
                           // (split: of its first 32)
     float xs2[MT];        // split: plain fp32 sum of its last 32
+    bool mk[MT];          // marked chunk (common.cuh, "marked groups")
+    uint32_t lo[MT][16];  // two-plane path: its int8 residual plane
 };
 
 // int16 of v * finv, rounded to nearest even: adding 1.5 * 2^23 puts the
@@ -44,22 +46,38 @@ __device__ __forceinline__ uint32_t i16_pair_fast(float a, float b,
 // so that the lanes of a warp (consecutive chunks) read consecutive 16-byte
 // pieces:
 //   pairs[r][c][g] (uint4: pairs 4c..4c+3 of chunk g), then f[r][g],
-//   xs[r][g], and for split images xs2[r][g].
+//   xs[r][g], for split images xs2[r][g], and for images with deferred
+//   marks (two-plane kernels) mq[r][g][4]: per quarter of the chunk
+//   R_q - 2^-16 A_q in fp16 (common.cuh, "marked groups"; the criterion is
+//   linear, so the chunk is marked when the four add up above zero).
 __host__ __device__ constexpr size_t ximg_bytes(int R, int G,
-                                                bool split = false) {
-    return (size_t)R * G * (8 * 16 + 8 + (split ? 4 : 0));
+                                                bool split = false,
+                                                bool marks = false) {
+    return (size_t)R * G * (8 * 16 + 8 + (split ? 4 : 0) + (marks ? 8 : 0));
 }
+
+// How an encoder settles a chunk's mark: RAW agrees on it through shuffles
+// and stores a marked chunk's raw bf16 pairs (fp32 path); DEFER stores each
+// quarter's part of the criterion and leaves the int16 pairs (two-plane
+// path): no shuffle is added to the encode.
+enum MarkMode { kMarkRaw = 0, kMarkDefer = 1 };
 
 // Quarter `q` (16 inputs) of group g of image row r, from its 8 packed bf16
 // words.  The four quarters of a group sit in four adjacent lanes and agree
-// on the group's exponent and sum through shuffles, so every lane of the
-// warp must call this.  u4: the high-nibble products of the dot come out
-// 16x too large and exact, so f is stored as 2^E / 16.
-template <int BITS, bool SPLIT = false>
+// on the group's exponent, sum and mark through shuffles, so every lane of
+// the warp must call this.  u4: the high-nibble products of the dot come
+// out 16x too large and exact, so f is stored as 2^E / 16.  Marks (common.cuh,
+// "marked groups"): with kMarkRaw a marked chunk sets *mkflag (when given)
+// to 1 and stores its raw bf16 pairs in the same order and f = -1/16 (u4)
+// or -1 (u8), the unit of the fp32 dot; with kMarkDefer every quarter
+// stores its part of the criterion (see ximg_bytes) and the pairs and f are
+// the usual ones.
+template <int BITS, bool SPLIT = false, int MK = kMarkRaw>
 __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
                                                bool store, int r, int g, int q,
                                                int R, int G,
-                                               unsigned char *img) {
+                                               unsigned char *img,
+                                               int *mkflag = nullptr) {
     uint4 *pairs = reinterpret_cast<uint4 *>(img);
     float *xf = reinterpret_cast<float *>(pairs + (size_t)R * 8 * G);
     float *xsm = xf + (size_t)R * G;
@@ -83,23 +101,41 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
     if constexpr (!SPLIT) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     float f, finv;
     group_scale((int)((m16 >> 7) & 0xffu), f, finv);
+    // rounding error and magnitude of the chunk in units of f
+    float re = 0.f, ab = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        re += i16_resid(v[i], finv);
+        ab += fabsf(v[i]);
+    }
+    bool marked = false;
+    if constexpr (MK == kMarkRaw) {
+        re += __shfl_xor_sync(0xffffffffu, re, 1);
+        re += __shfl_xor_sync(0xffffffffu, re, 2);
+        ab += __shfl_xor_sync(0xffffffffu, ab, 1);
+        ab += __shfl_xor_sync(0xffffffffu, ab, 2);
+        marked = group_marked(re, ab * finv);
+    }
+    auto pair = [&](float a, float b) {
+        return marked ? raw_pair(a, b) : i16_pair_fast(a, b, finv);
+    };
     uint32_t pr[8];
     if constexpr (BITS == 4) {
         // words 2q, 2q+1: (x0,x2) (x4,x6) (x1,x3) (x5,x7) each
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
             const float *vw = v + 8 * w;
-            pr[4 * w + 0] = i16_pair_fast(vw[0], vw[2], finv);
-            pr[4 * w + 1] = i16_pair_fast(vw[4], vw[6], finv);
-            pr[4 * w + 2] = i16_pair_fast(vw[1], vw[3], finv);
-            pr[4 * w + 3] = i16_pair_fast(vw[5], vw[7], finv);
+            pr[4 * w + 0] = pair(vw[0], vw[2]);
+            pr[4 * w + 1] = pair(vw[4], vw[6]);
+            pr[4 * w + 2] = pair(vw[1], vw[3]);
+            pr[4 * w + 3] = pair(vw[5], vw[7]);
         }
     } else {
         // words 4q..4q+3: (x0,x1) (x2,x3) each
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            pr[2 * w] = i16_pair_fast(v[4 * w], v[4 * w + 1], finv);
-            pr[2 * w + 1] = i16_pair_fast(v[4 * w + 2], v[4 * w + 3], finv);
+            pr[2 * w] = pair(v[4 * w], v[4 * w + 1]);
+            pr[2 * w + 1] = pair(v[4 * w + 2], v[4 * w + 3]);
         }
     }
     if (store) {
@@ -108,24 +144,34 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
         pairs[((size_t)r * 8 + 2 * q + 1) * G + g] =
             make_uint4(pr[4], pr[5], pr[6], pr[7]);
         if (q == 0) {
-            xf[(size_t)r * G + g] = BITS == 4 ? f * 0.0625f : f;
+            const float unit = BITS == 4 ? 0.0625f : 1.f;
+            xf[(size_t)r * G + g] = marked ? -unit : f * unit;
+            if (marked && mkflag) *mkflag = 1;
             xsm[(size_t)r * G + g] = sum;
         }
         if (SPLIT && q == 2) xsm[(size_t)R * G + (size_t)r * G + g] = sum;
+        if constexpr (MK == kMarkDefer) {
+            __half *mq = reinterpret_cast<__half *>(xsm + (SPLIT ? 2 : 1) *
+                                                              (size_t)R * G);
+            mq[((size_t)r * G + g) * 4 + q] =
+                __float2half_rn(fmaf(ab * finv, -1.0f / 65536.0f, re));
+        }
     }
 }
 
 // All `ncons` threads (whole warps) encode R rows of K activations into the
 // image: row r from x + src(r) * K, src(r) = rowsrc ? rowsrc[r] : r (rows
-// >= Rv encode as zeros).  A thread issues
+// >= Rv encode as zeros); *mkflag, when given, is set to 1 if any group
+// is marked (the caller clears it first).  A thread issues
 // the loads of up to kXBatch quarters before encoding any, so a long image
 // costs about one memory round trip.
 constexpr int kXBatch = 4;
 
-template <int BITS, bool SPLIT = false>
+template <int BITS, bool SPLIT = false, int MK = kMarkRaw>
 __device__ __forceinline__ void encode_rows_shared(
     const uint16_t *__restrict__ x, int Rv, int R, int K, int G, int tid,
-    int ncons, unsigned char *img, const int *rowsrc = nullptr) {
+    int ncons, unsigned char *img, const int *rowsrc = nullptr,
+    int *mkflag = nullptr) {
     const int items = R * G * 4;
     const int iters = (items + ncons - 1) / ncons;  // same for every thread
     for (int b0 = 0; b0 < iters; b0 += kXBatch) {
@@ -153,10 +199,29 @@ __device__ __forceinline__ void encode_rows_shared(
             if (b0 + j >= iters) break;  // uniform: the shuffles need every lane
             const int it = (b0 + j) * ncons + tid;
             const int r = it / (4 * G), rem = it - r * 4 * G;
-            encode_quarter<BITS, SPLIT>(u[j], it < items, r, rem >> 2, rem & 3,
-                                        R, G, img);
+            encode_quarter<BITS, SPLIT, MK>(u[j], it < items, r, rem >> 2,
+                                            rem & 3, R, G, img, mkflag);
         }
     }
+}
+
+// Whether chunk g of an image with deferred marks (kMarkDefer) is marked,
+// in any of its R rows (common.cuh, "marked groups").
+template <int R, bool SPLIT>
+__device__ __forceinline__ bool chunk_marked(const unsigned char *img, int G,
+                                             int g) {
+    const float *xsm = reinterpret_cast<const float *>(
+        reinterpret_cast<const uint4 *>(img) + (size_t)R * 8 * G) + (size_t)R * G;
+    const __half2 *mq = reinterpret_cast<const __half2 *>(xsm + (SPLIT ? 2 : 1) *
+                                                                    (size_t)R * G);
+    bool mk = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float2 a = __half22float2(mq[((size_t)r * G + g) * 2]);
+        const float2 b = __half22float2(mq[((size_t)r * G + g) * 2 + 1]);
+        mk |= (a.x + a.y) + (b.x + b.y) > 0.f;
+    }
+    return mk;
 }
 
 // Bank-conflict-free reads of a row's group.  Lane g reads its group's
@@ -183,7 +248,7 @@ __device__ __forceinline__ void lds_group(const unsigned char *src, int rot,
 
 // Image rows r0 .. r0+MT-1 of group g into registers (zeros when !active),
 // image chunks rotated by `shift` (see chunk_rot).
-template <int MT, bool SPLIT = false>
+template <int MT, bool SPLIT = false, int MK = kMarkRaw>
 __device__ __forceinline__ void load_group_rows(const unsigned char *img,
                                                 int R, int G, int r0, int g,
                                                 bool active, GroupX<MT> &gx,
@@ -202,7 +267,17 @@ __device__ __forceinline__ void load_group_rows(const unsigned char *img,
             gx.pr[m][4 * c + 2] = t.z;
             gx.pr[m][4 * c + 3] = t.w;
         }
-        gx.f[m] = active ? xf[(size_t)r * G + g] : 0.f;
+        const float fm = active ? xf[(size_t)r * G + g] : 0.f;
+        if constexpr (MK == kMarkDefer) {
+            const __half2 *mq = reinterpret_cast<const __half2 *>(
+                xsm + (SPLIT ? 2 : 1) * (size_t)R * G);
+            const float2 a = __half22float2(mq[((size_t)r * G + g) * 2]);
+            const float2 b = __half22float2(mq[((size_t)r * G + g) * 2 + 1]);
+            gx.mk[m] = active && (a.x + a.y) + (b.x + b.y) > 0.f;
+        } else {
+            gx.mk[m] = fm < 0.f;
+        }
+        gx.f[m] = fabsf(fm);
         gx.xs[m] = active ? xsm[(size_t)r * G + g] : 0.f;
         gx.xs2[m] = SPLIT && active ? xsm[(size_t)R * G + (size_t)r * G + g] : 0.f;
     }
@@ -253,6 +328,172 @@ __device__ __forceinline__ void group_dot(const uint4 (&w)[BITS / 2],
         else
             d[m] = (a[m][0] + a[m][1]) + (a[m][2] + a[m][3]);
     }
+}
+
+// The int8 residual plane of a marked chunk (two-plane path, common.cuh
+// "marked groups"), formed by the lane that owns the chunk from its 64 raw
+// bf16 activations x (16-byte aligned) and its scale f as stored in GroupX
+// (u4: 2^E / 16).  Register v * P + j holds the entries of code piece
+// (v + rot) & (NV - 1) (the order lds_group loads the codes in), P = 16 / NV
+// registers per piece, in dp4a order: per u4 word the entries of its low
+// nibbles' inputs (x0 x2 x4 x6), then of its high nibbles' (x1 x3 x5 x7);
+// per u8 word x0..x3.
+template <int BITS>
+__device__ __forceinline__ void group_lo_plane(const uint16_t *x, float f,
+                                               int rot, uint32_t (&lo)[16]) {
+    constexpr int NV = BITS / 2;
+    constexpr int P = 16 / NV;
+    const float finv = 1.0f / (BITS == 4 ? 16.0f * f : f);  // exact: 2^-E
+    uint32_t raw[16];
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // activations 8i .. 8i + 7
+        const uint4 u = xv[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t e[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            e[2 * k] = i8_resid(bf16_lo(w[k]), finv);
+            e[2 * k + 1] = i8_resid(bf16_hi(w[k]), finv);
+        }
+        if constexpr (BITS == 4) {  // one u4 word: even, then odd entries
+            raw[2 * i] = e[0] | (e[2] << 8) | (e[4] << 16) | (e[6] << 24);
+            raw[2 * i + 1] = e[1] | (e[3] << 8) | (e[5] << 16) | (e[7] << 24);
+        } else {  // two u8 words
+            raw[2 * i] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
+            raw[2 * i + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            uint32_t t = raw[v * P + j];
+#pragma unroll
+            for (int r = 1; r < NV; ++r)
+                if (rot == r) t = raw[((v + r) & (NV - 1)) * P + j];
+            lo[v * P + j] = t;
+        }
+}
+
+// group_dot and the residual-plane dot of the two-plane path in one pass
+// (the code bytes split once): dh as group_dot's d, dl the same dot with
+// gx.lo (its scale 2^-7 of dh's).
+template <int BITS, int MT>
+__device__ __forceinline__ void group_dot2(const uint4 (&w)[BITS / 2],
+                                           const GroupX<MT> &gx, int (&dh)[MT],
+                                           int (&dl)[MT]) {
+    int a[MT][4], b[MT][2];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        a[m][0] = a[m][1] = a[m][2] = a[m][3] = 0;
+        b[m][0] = b[m][1] = 0;
+    }
+#pragma unroll
+    for (int v = 0; v < BITS / 2; ++v) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wd = 4 * v + c;
+            const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
+                                  : c == 2 ? w[v].z : w[v].w;
+            if constexpr (BITS == 4) {
+                const uint32_t lo = word & 0x0f0f0f0fu;
+                const uint32_t hi = word & 0xf0f0f0f0u;
+                const int p = (wd & 1) * 2;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = gx.pr[m] + 4 * wd;
+                    a[m][p] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, a[m][p]));
+                    a[m][p + 1] =
+                        dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, a[m][p + 1]));
+                    b[m][0] = dp4a_us(lo, gx.lo[m][2 * wd], b[m][0]);
+                    b[m][1] = dp4a_us(hi, gx.lo[m][2 * wd + 1], b[m][1]);
+                }
+            } else {
+                const int p = wd & 3;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = gx.pr[m] + 2 * wd;
+                    a[m][p] = dp2a_hi(pr[1], word, dp2a_lo(pr[0], word, a[m][p]));
+                    b[m][wd & 1] = dp4a_us(word, gx.lo[m][wd], b[m][wd & 1]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if constexpr (BITS == 4) {
+            dh[m] = 16 * (a[m][0] + a[m][2]) + (a[m][1] + a[m][3]);
+            dl[m] = 16 * b[m][0] + b[m][1];
+        } else {
+            dh[m] = (a[m][0] + a[m][1]) + (a[m][2] + a[m][3]);
+            dl[m] = b[m][0] + b[m][1];
+        }
+    }
+}
+
+// The residual-plane dot of group_dot_split's halves (dl over inputs
+// [0, 32), dh over [32, 64), each scaled like group_dot2's dl).
+template <int BITS, int MT>
+__device__ __forceinline__ void group_dot_lo_split(const uint4 (&w)[BITS / 2],
+                                                   const GroupX<MT> &gx, int rot,
+                                                   int (&dl)[MT], int (&dh)[MT]) {
+    constexpr int NV = BITS / 2;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) dl[m] = dh[m] = 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        int b[MT][2];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) b[m][0] = b[m][1] = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wd = 4 * v + c;
+            const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
+                                  : c == 2 ? w[v].z : w[v].w;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if constexpr (BITS == 4) {
+                    b[m][0] = dp4a_us(word & 0x0f0f0f0fu, gx.lo[m][2 * wd], b[m][0]);
+                    b[m][1] = dp4a_us(word & 0xf0f0f0f0u, gx.lo[m][2 * wd + 1],
+                                      b[m][1]);
+                } else {
+                    b[m][0] = dp4a_us(word, gx.lo[m][wd], b[m][0]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int dv = BITS == 4 ? 16 * b[m][0] + b[m][1] : b[m][0];
+            if (((v + rot) & (NV - 1)) < NV / 2)
+                dl[m] += dv;
+            else
+                dh[m] += dv;
+        }
+    }
+}
+
+// group_dot of token m of a marked chunk, in fp32 (common.cuh): the same
+// pairs hold raw bf16 activations and the same code bytes multiply them, so
+// the result has group_dot's scale (u4: 16 times the true sum).
+template <int BITS, int MT>
+__device__ __forceinline__ float group_dot_f32(const uint4 (&w)[BITS / 2],
+                                               const GroupX<MT> &gx, int m) {
+    float a[2] = {0.f, 0.f};
+#pragma unroll
+    for (int v = 0; v < BITS / 2; ++v) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wd = 4 * v + c;
+            const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
+                                  : c == 2 ? w[v].z : w[v].w;
+            if constexpr (BITS == 4)
+                fword_dot_u4(word, gx.pr[m] + 4 * wd, a);
+            else
+                fword_dot_u8(word, gx.pr[m] + 2 * wd, a);
+        }
+    }
+    return BITS == 4 ? fmaf(a[0], 16.f, a[1]) : a[0] + a[1];
 }
 
 // The same dot split over the chunk's two halves (groups of 32): dl over

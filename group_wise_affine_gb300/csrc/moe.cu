@@ -32,7 +32,8 @@ __device__ __forceinline__ void moe_gate_up_body(const MoeParams &p,
                                                  const WView &v,
                                                  const int *list, int mt,
                                                  int64_t i0,
-                                                 const unsigned char *xs) {
+                                                 const unsigned char *xs,
+                                                 bool mk) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t I = p.N / 2;
     constexpr int R = 2 * kMoeRP;
@@ -47,7 +48,10 @@ __device__ __forceinline__ void moe_gate_up_body(const MoeParams &p,
 #pragma unroll
     for (int m = 0; m < MT; ++m) midx[m] = m;
     float acc[R][MT];
-    rows_dot<BITS, MT, R>(v, rows, midx, MT, xs, lane, acc);
+    if (mk)
+        rows_dot<BITS, MT, R, true>(v, rows, midx, MT, xs, lane, acc);
+    else
+        rows_dot<BITS, MT, R, false>(v, rows, midx, MT, xs, lane, acc);
     warp_reduce<R, MT>(acc);
 #pragma unroll
     for (int r = 0; r < kMoeRP; ++r)
@@ -67,6 +71,7 @@ __global__ void __launch_bounds__(kMoeThreads)
     __shared__ int list[kMoeMaxSlots];
     __shared__ int tok[8];
     __shared__ int s_cnt, s_state;
+    __shared__ int s_mk;  // some staged group of the pass is marked
     const int S = p.M * p.topk;
     const int slot = blockIdx.y;
     const int64_t I = p.N / 2;
@@ -111,16 +116,18 @@ __global__ void __launch_bounds__(kMoeThreads)
         if (threadIdx.x < 8)
             tok[threadIdx.x] =
                 threadIdx.x < mt ? list[base + threadIdx.x] / p.topk : -1;
+        if (threadIdx.x == 0) s_mk = 0;
         __syncthreads();
-        stage_x<BITS>(p.x, p.K, tok, mtb, p.nch, smem);
+        stage_x<BITS>(p.x, p.K, tok, mtb, p.nch, smem, &s_mk);
         __syncthreads();
+        const bool mk = s_mk != 0;
         const int *l = list + base;
         if (mtb == 1)
-            moe_gate_up_body<BITS, 1>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 1>(p, v, l, mt, i0, smem, mk);
         else if (mtb == 2)
-            moe_gate_up_body<BITS, 2>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 2>(p, v, l, mt, i0, smem, mk);
         else
-            moe_gate_up_body<BITS, 4>(p, v, l, mt, i0, smem);
+            moe_gate_up_body<BITS, 4>(p, v, l, mt, i0, smem, mk);
         __syncthreads();
     }
 }
@@ -138,9 +145,11 @@ __global__ void __launch_bounds__(kMoeDownThreads)
     __shared__ int s_order[kMoeMaxSlots];
     __shared__ float s_rw[kMoeMaxSlots];
     __shared__ int s_ng;
+    __shared__ int s_mk;  // some staged group is marked (common.cuh)
     const int S = p.M * p.topk;
     const int t = threadIdx.x;
 
+    if (t == 0) s_mk = 0;
     // 1. earliest slot naming the same (valid) expert
     if (t < S) {
         const int e = p.ids[t];
@@ -188,8 +197,9 @@ __global__ void __launch_bounds__(kMoeDownThreads)
         for (int s = f; s < t; ++s) rank += (s_first[s] == f);
         s_order[s_gstart[s_gidx[f]] + rank] = t;
     }
-    stage_x<BITS>(p.x, p.K, s_tok, S, p.nch, smem);
+    stage_x<BITS>(p.x, p.K, s_tok, S, p.nch, smem, &s_mk);
     __syncthreads();
+    const bool mk = s_mk != 0;
 
     const int lane = t & 31, warp = t >> 5;
     const int lg = lane / L, sub = lane % L;
@@ -234,8 +244,12 @@ __global__ void __launch_bounds__(kMoeDownThreads)
                     const int s = s_order[q];
                     const int midx[1] = {s};
                     float part[1][1] = {{0.f}};
-                    chunk_fma<BITS, 1, 1>(ring[k], c, p.nch, midx, aux, smem,
-                                          part);
+                    if (mk)
+                        chunk_fma<BITS, 1, 1, true>(ring[k], c, p.nch, midx, aux,
+                                                    smem, part);
+                    else
+                        chunk_fma<BITS, 1, 1, false>(ring[k], c, p.nch, midx, aux,
+                                                     smem, part);
                     const int tk = s / p.topk;
                     const float v = s_rw[s] * part[0][0];
 #pragma unroll

@@ -188,6 +188,7 @@ __global__ void __maxnreg__(128)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ MsTables tb;
     __shared__ int s_issued, s_consumed;
+    __shared__ int s_marked;  // some image group is marked (group_dot.cuh)
     // down: accumulators [row of the cluster block][token]
     float *acc = reinterpret_cast<float *>(smem + acc_off);
 
@@ -263,6 +264,7 @@ __global__ void __maxnreg__(128)
         tb.gstart[ng] = valid;
         s_issued = 0;
         s_consumed = 1 << 30;
+        s_marked = 0;
     }
     __syncthreads();
     for (int s = tid; s < S; s += blockDim.x) {
@@ -361,85 +363,99 @@ __global__ void __maxnreg__(128)
 
         pdl_wait_primary();  // x / h may be the previous kernel's output
         encode_rows_shared<BITS>(p.x, tb.nimg, tb.nimg, p.K, p.G, tid, ncons,
-                                 img, MODE == 1 ? tb.imgsrc : nullptr);
+                                 img, MODE == 1 ? tb.imgsrc : nullptr, &s_marked);
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
+        const bool img_marked = s_marked != 0;
 
         GroupX<1> gx;
         int cached = -1;
         int s = -1;       // ring slot of the current stage
         uint32_t ph = 1;  // its use count parity
-        MsTask t;
-        while (tasks.next(t)) {
-            if (t.sb == 0) {
-                if (++s == stages) s = 0;
-                if (s == 0) ph ^= 1;
-                if (!mbar_wait(&full[s], ph)) {
-                    atomicAdd(&g_moe_timeouts, 1u);
-                    atomicMin(&s_consumed, t.k);
-                    break;
-                }
-            }
-            const unsigned char *base = smem + (size_t)s * stage_bytes;
-            const int pos = t.sb + hgc * UPT;
-            const int q1 = tb.gstart[t.sg.gi + 1];
-            for (int qi = tb.gstart[t.sg.gi]; qi < q1; ++qi) {
-                const int2 sr = tb.slotrow[qi];
-                const int slot = sr.x, row = sr.y;
-                if (row != cached) {
-                    load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx,
-                                       image_shift<BITS>(gg));
-                    cached = row;
-                }
-                float v[RPH];
-#pragma unroll
-                for (int j = 0; j < RPH; ++j) {
-                    // stage row of value j (rows past the stage's end read
-                    // its last row, finite, and are not stored)
-                    const uint32_t roj = (uint32_t)((j / UPT) * ups +
-                                                    min(pos + (j % UPT), t.sg.n - 1));
-                    uint4 wv[BITS / 2];
-                    lds_group<BITS>(base + roj * rowbytes + (uint32_t)gg * GB,
-                                    rot, wv);
-                    const uint32_t so = (roj * (uint32_t)p.G + gg) * 2u;
-                    const float sv = bf16_bits_to_f32(
-                        *reinterpret_cast<const uint16_t *>(base + sc_off + so));
-                    const float bv = bf16_bits_to_f32(
-                        *reinterpret_cast<const uint16_t *>(base + bi_off + so));
-                    int d[1];
-                    group_dot<BITS, 1>(wv, gx, d);
-                    v[j] = fmaf(sv * gx.f[0], (float)d[0], bv * gx.xs[0]);
-                    // keep the next row's loads after this dot (registers)
-                    asm volatile("" ::: "memory");
-                }
-                // value j ends in slice lane j * (W / RPH); the second half's
-                // values (up rows, or down's odd rows) sit W/2 lanes up
-                const float tot = sub_reduce<W, RPH>(v, lane);
-                const float tot1 = __shfl_down_sync(0xffffffffu, tot, W / 2);
-                constexpr int SPREAD = W / RPH;
-                const int j = g / SPREAD;  // value index of this lane
-                if (in_group && g % SPREAD == 0 && g < W / 2) {
-                    if (MODE == 0) {
-                        // pair pos + j: gate value j, up value UPT + j
-                        if (pos + j < t.sg.n)
-                            p.out[(int64_t)slot * I + t.sg.u + pos + j] =
-                                f32_to_bf16_bits(tot / (1.0f + __expf(-tot)) *
-                                                 tot1);
-                    } else if (j == 0 && pos < t.sg.n) {
-                        // rows pos (value 0) and pos + 1 (value 1)
-                        const int tk = slot / p.topk;
-                        const float r = tb.rw[slot];
-                        float *a = acc + (size_t)(t.sg.u - blk0 + pos) * p.M + tk;
-                        a[0] += r * tot;
-                        if (pos + 1 < t.sg.n) a[p.M] += r * tot1;
+        // The task loop, once with the marked-group path (EX) and once
+        // without it (see qmv_group.cu); the image rows a lane reads change
+        // over the loop, so the choice is made from every row of the image.
+        auto task_loop = [&](auto ex) {
+            constexpr bool EX = decltype(ex)::value;
+            MsTask t;
+            while (tasks.next(t)) {
+                if (t.sb == 0) {
+                    if (++s == stages) s = 0;
+                    if (s == 0) ph ^= 1;
+                    if (!mbar_wait(&full[s], ph)) {
+                        atomicAdd(&g_moe_timeouts, 1u);
+                        atomicMin(&s_consumed, t.k);
+                        break;
                     }
                 }
+                const unsigned char *base = smem + (size_t)s * stage_bytes;
+                const int pos = t.sb + hgc * UPT;
+                const int q1 = tb.gstart[t.sg.gi + 1];
+                for (int qi = tb.gstart[t.sg.gi]; qi < q1; ++qi) {
+                    const int2 sr = tb.slotrow[qi];
+                    const int slot = sr.x, row = sr.y;
+                    if (row != cached) {
+                        load_group_rows<1>(img, tb.nimg, p.G, row, gg, active, gx,
+                                           image_shift<BITS>(gg));
+                        cached = row;
+                    }
+                    float v[RPH];
+#pragma unroll
+                    for (int j = 0; j < RPH; ++j) {
+                        // stage row of value j (rows past the stage's end read
+                        // its last row, finite, and are not stored)
+                        const uint32_t roj = (uint32_t)((j / UPT) * ups +
+                                                        min(pos + (j % UPT), t.sg.n - 1));
+                        uint4 wv[BITS / 2];
+                        lds_group<BITS>(base + roj * rowbytes + (uint32_t)gg * GB,
+                                        rot, wv);
+                        const uint32_t so = (roj * (uint32_t)p.G + gg) * 2u;
+                        const float sv = bf16_bits_to_f32(
+                            *reinterpret_cast<const uint16_t *>(base + sc_off + so));
+                        const float bv = bf16_bits_to_f32(
+                            *reinterpret_cast<const uint16_t *>(base + bi_off + so));
+                        int d[1];
+                        group_dot<BITS, 1>(wv, gx, d);
+                        float df = (float)d[0];
+                        if (EX && gx.mk[0])  // marked group: fp32 dot of raw x
+                            df = group_dot_f32<BITS, 1>(wv, gx, 0);
+                        v[j] = fmaf(sv * gx.f[0], df, bv * gx.xs[0]);
+                        // keep the next row's loads after this dot (registers)
+                        asm volatile("" ::: "memory");
+                    }
+                    // value j ends in slice lane j * (W / RPH); the second half's
+                    // values (up rows, or down's odd rows) sit W/2 lanes up
+                    const float tot = sub_reduce<W, RPH>(v, lane);
+                    const float tot1 = __shfl_down_sync(0xffffffffu, tot, W / 2);
+                    constexpr int SPREAD = W / RPH;
+                    const int j = g / SPREAD;  // value index of this lane
+                    if (in_group && g % SPREAD == 0 && g < W / 2) {
+                        if (MODE == 0) {
+                            // pair pos + j: gate value j, up value UPT + j
+                            if (pos + j < t.sg.n)
+                                p.out[(int64_t)slot * I + t.sg.u + pos + j] =
+                                    f32_to_bf16_bits(tot / (1.0f + __expf(-tot)) *
+                                                     tot1);
+                        } else if (j == 0 && pos < t.sg.n) {
+                            // rows pos (value 0) and pos + 1 (value 1)
+                            const int tk = slot / p.topk;
+                            const float r = tb.rw[slot];
+                            float *a = acc + (size_t)(t.sg.u - blk0 + pos) * p.M + tk;
+                            a[0] += r * tot;
+                            if (pos + 1 < t.sg.n) a[p.M] += r * tot1;
+                        }
+                    }
+                }
+                if (t.last) {
+                    // every lane's reads of this stage are done: release it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
             }
-            if (t.last) {
-                // every lane's reads of this stage are done: release it
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-        }
+        };
+        if (img_marked)
+            task_loop(std::true_type{});
+        else
+            task_loop(std::false_type{});
     }
     __syncthreads();
     // Outputs are written by consumer threads only: they passed the

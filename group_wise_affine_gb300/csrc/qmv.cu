@@ -30,11 +30,14 @@ __global__ void __launch_bounds__(kDenseThreads)
     qmv_dense_kernel(DenseParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int tok[8];
+    __shared__ int s_mk;  // some staged group is marked (common.cuh)
     if (threadIdx.x < 8)
         tok[threadIdx.x] = (int)threadIdx.x < p.M ? (int)threadIdx.x : -1;
+    if (threadIdx.x == 0) s_mk = 0;
     __syncthreads();
-    stage_x<BITS>(p.x, p.K, tok, MT, p.nch, smem);
+    stage_x<BITS>(p.x, p.K, tok, MT, p.nch, smem, &s_mk);
     __syncthreads();
+    const bool mk = s_mk != 0;
 
     const int lane = threadIdx.x & (kWarp - 1);
     const int warp = threadIdx.x / kWarp;
@@ -63,7 +66,10 @@ __global__ void __launch_bounds__(kDenseThreads)
 #pragma unroll
         for (int m = 0; m < MT; ++m) midx[m] = m;
         float acc[R][MT];
-        rows_dot<BITS, MT, R>(v, rows, midx, MT, smem, lane, acc);
+        if (mk)
+            rows_dot<BITS, MT, R, true>(v, rows, midx, MT, smem, lane, acc);
+        else
+            rows_dot<BITS, MT, R, false>(v, rows, midx, MT, smem, lane, acc);
         warp_reduce<R, MT>(acc);
 
 #pragma unroll

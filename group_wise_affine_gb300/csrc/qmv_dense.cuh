@@ -23,6 +23,8 @@ namespace gwa {
 // that the 32 lanes of a warp read 32 consecutive 16-byte slots:
 //   uint4 q[m][e][c], e < kChunkCodes/8
 // followed by float2 aux[m][c] = (group scale 2^E, sum of the chunk's x).
+// A marked group (common.cuh, "marked groups") holds raw bf16 pairs in the
+// same order and a scale of -1.
 template <int BITS>
 struct XStage {
     static constexpr int kQuads = Fmt<BITS>::kChunkCodes / 8;
@@ -33,12 +35,14 @@ struct XStage {
 
 // Stage tokens `tok[0..mt)` (rows of x, K = nch * chunk codes) into shared
 // memory; token slots with tok[m] < 0 are zero-filled.  One item per
-// (token, group of 64).  Called by the whole CTA; the caller synchronizes.
+// (token, group of 64).  *mkflag is set to 1 if any group is marked (the
+// caller clears it first).  Called by the whole CTA; the caller
+// synchronizes.
 template <int BITS>
 __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
                                         int64_t x_row_stride,
                                         const int *tok, int mt, int nch,
-                                        unsigned char *smem) {
+                                        unsigned char *smem, int *mkflag) {
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
     constexpr int CPG = kGroup / CODES;  // chunks per group
     constexpr int Q = XStage<BITS>::kQuads;
@@ -73,6 +77,14 @@ __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
         for (int i = 0; i < kGroup; ++i) ef = max(ef, f32_exp_field(v[i]));
         float f, finv;
         group_scale(ef, f, finv);
+        float re = 0.f, ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+            re += i16_resid(v[i], finv);
+            ab += fabsf(v[i]);
+        }
+        const bool marked = group_marked(re, ab * finv);
+        if (marked) *mkflag = 1;
 #pragma unroll
         for (int cg = 0; cg < CPG; ++cg) {
             const int c = g * CPG + cg;
@@ -82,13 +94,25 @@ __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
 #pragma unroll
             for (int wd = 0; wd < 4; ++wd) {
                 if constexpr (BITS == 4) {
+                    const float *vw = vc + 8 * wd;
                     uint32_t t[4];
-                    u4_pairs(vc + 8 * wd, finv, t);
+                    u4_pairs(vw, finv, t);
+                    if (marked) {  // raw bf16 in the same dp2a order
+                        t[0] = raw_pair(vw[0], vw[2]);
+                        t[1] = raw_pair(vw[4], vw[6]);
+                        t[2] = raw_pair(vw[1], vw[3]);
+                        t[3] = raw_pair(vw[5], vw[7]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) pr[4 * wd + i] = t[i];
                 } else {
+                    const float *vw = vc + 4 * wd;
                     uint32_t t[2];
-                    u8_pairs(vc + 4 * wd, finv, t);
+                    u8_pairs(vw, finv, t);
+                    if (marked) {
+                        t[0] = raw_pair(vw[0], vw[1]);
+                        t[1] = raw_pair(vw[2], vw[3]);
+                    }
                     pr[2 * wd] = t[0];
                     pr[2 * wd + 1] = t[1];
                 }
@@ -100,7 +124,7 @@ __device__ __forceinline__ void stage_x(const uint16_t *__restrict__ x,
                 q[((size_t)m * Q + e) * nch + c] =
                     make_uint4(pr[4 * e], pr[4 * e + 1], pr[4 * e + 2],
                                pr[4 * e + 3]);
-            aux[(size_t)m * nch + c] = make_float2(f, xs);
+            aux[(size_t)m * nch + c] = make_float2(marked ? -1.f : f, xs);
         }
     }
 }
@@ -170,14 +194,41 @@ __device__ __forceinline__ void load_chunk(const WView &v,
 }
 
 // One 16-byte chunk of R rows against MT staged tokens (stage slots
-// midx[m]); adds the scaled, bias-corrected chunk dot into acc.
-template <int BITS, int MT, int R>
+// midx[m]); adds the scaled, bias-corrected chunk dot into acc.  With EX
+// (some staged group is marked), a marked token's chunk (raw bf16 pairs,
+// scale -1) takes the same dot in fp32.
+template <int BITS, int MT, int R, bool EX>
 __device__ __forceinline__ void chunk_fma(const ChunkRegs<R> &cr, int c,
                                           int nch, const int (&midx)[MT],
                                           const float2 *aux,
                                           const unsigned char *xs,
                                           float (&acc)[R][MT]) {
     constexpr int PAIRS = BITS == 4 ? 4 : 2;
+    float2 fa[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) fa[m] = aux[(size_t)midx[m] * nch + c];
+    // marked tokens first (raw bf16 pairs, scale -1: fp32 dot one row at a
+    // time), so that the integer accumulators below are not live meanwhile
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (!EX || fa[m].x >= 0.f) continue;
+        uint32_t xp[4 * PAIRS];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+            uint32_t t[PAIRS];
+            x_pairs<BITS>(xs, midx[m], nch, c, wd, t);
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) xp[wd * PAIRS + i] = t[i];
+        }
+#pragma unroll 1
+        for (int r = 0; r < R; ++r) {
+            const float v = chunk_dot_f32<BITS>(pick(cr.w, r), xp);
+            const float sr = pick(cr.s, r), br = pick(cr.b, r);
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+                if (k == r) acc[k][m] = fmaf(sr, v, fmaf(br, fa[m].y, acc[k][m]));
+        }
+    }
     int d[R][MT][2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -206,17 +257,17 @@ __device__ __forceinline__ void chunk_fma(const ChunkRegs<R> &cr, int c,
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const float2 fa = aux[(size_t)midx[m] * nch + c];
+        if (EX && fa[m].x < 0.f) continue;
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            acc[r][m] = fmaf(cr.s[r] * fa.x, (float)dot_total<BITS>(d[r][m]),
-                             fmaf(cr.b[r], fa.y, acc[r][m]));
+            acc[r][m] = fmaf(cr.s[r] * fa[m].x, (float)dot_total<BITS>(d[r][m]),
+                             fmaf(cr.b[r], fa[m].y, acc[r][m]));
     }
 }
 
 // Partial sums of this lane for R rows and MT staged tokens (not reduced).
 // L lanes share a row: the lane walks chunks (lane % L), +L, ...
-template <int BITS, int MT, int R, int L = kWarp>
+template <int BITS, int MT, int R, bool EX, int L = kWarp>
 __device__ __forceinline__ void rows_dot(const WView &v,
                                          const int64_t (&rows)[R],
                                          const int (&midx)[MT], int mt_stage,
@@ -236,7 +287,7 @@ __device__ __forceinline__ void rows_dot(const WView &v,
         const bool more = cn < v.nch;
         ChunkRegs<R> nxt;
         if (more) load_chunk<BITS, R>(v, rows, cn, nxt);
-        chunk_fma<BITS, MT, R>(cur, c, v.nch, midx, aux, xs, acc);
+        chunk_fma<BITS, MT, R, EX>(cur, c, v.nch, midx, aux, xs, acc);
         if (!more) break;
         c = cn;
         cur = nxt;

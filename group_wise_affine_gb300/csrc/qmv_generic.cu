@@ -19,6 +19,8 @@
 // epilogues as the tuned kernels (plain, sections with bias, SiLU(gate) *
 // up, rotary pairs) finish it.  It trades speed for generality: about four
 // instructions per code and token.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -315,7 +317,12 @@ __global__ void __launch_bounds__(kGdThreads, 2)
     float *xu = xf + M * G;                                              // [M][nch]
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
     const int gshift = __ffs(GS) - 1;  // groups are 32, 64 or 128
-    if (threadIdx.x == 0) pdl_launch_dependents();
+    __shared__ int s_mk;  // some group is marked (common.cuh)
+    if (threadIdx.x == 0) {
+        pdl_launch_dependents();
+        s_mk = 0;
+    }
+    __syncthreads();
     pdl_wait_primary();  // x may be the previous kernel's output
 
     // encode: one warp per (token, group), four groups' loads in flight; the
@@ -344,19 +351,35 @@ __global__ void __launch_bounds__(kGdThreads, 2)
             ef = __reduce_max_sync(FULL, ef);
             float f, finv;
             group_scale(ef, f, finv);
+            // the group's rounding error and magnitude in units of f; a
+            // marked group (common.cuh) keeps raw bf16 in its int16 slots
+            float re = 0.f, ab = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                re += i16_resid(v[b][r], finv);
+                ab += fabsf(v[b][r]);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                re += __shfl_xor_sync(FULL, re, o);
+                ab += __shfl_xor_sync(FULL, ab, o);
+            }
+            const bool marked = group_marked(re, ab * finv);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 if (r >= rmax) break;
                 const int k0 = g * GS + r * kWarp;  // this r's chunk
                 const int pos = gd_pos<BITS>(lane);
                 xe[m * K + ((pos >> 3) * nch + k0 / kGdChunk) * 8 + (pos & 7)] =
-                    (int16_t)__float2int_rn(v[b][r] * finv);
+                    marked ? (int16_t)(__float_as_uint(v[b][r]) >> 16)
+                           : (int16_t)__float2int_rn(v[b][r] * finv);
                 float sum = v[b][r];
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
                 if (lane == 0) xu[m * nch + k0 / kGdChunk] = sum;
             }
-            if (lane == 0) xf[m * G + g] = f;
+            if (lane == 0) xf[m * G + g] = marked ? -1.f : f;
+            if (marked && lane == 0) s_mk = 1;
         }
     }
     __syncthreads();
@@ -365,72 +388,93 @@ __global__ void __launch_bounds__(kGdThreads, 2)
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nw = (int64_t)gridDim.x * blockDim.x / kWarp;
     const int wpr = K * BITS / 32;  // words per row
-    for (int64_t u = gw; u < units; u += nw) {
-        int64_t rows[2];
-        if (MODE == 2) {
-            rows[0] = u;
-            rows[1] = I + u;
-        } else if (MODE == 3) {
-            rows[0] = rope_pair_row(u, 0, p.rope_hd);
-            rows[1] = rope_pair_row(u, 1, p.rope_hd);
-        } else {
-            rows[0] = rows[1] = u;
-        }
-        float acc[2][kGenTokens];
+    // the unit loop, once with the marked-group path (EX) and once without
+    auto unit_loop = [&](auto ex) {
+        constexpr bool EX = decltype(ex)::value;
+        for (int64_t u = gw; u < units; u += nw) {
+            int64_t rows[2];
+            if (MODE == 2) {
+                rows[0] = u;
+                rows[1] = I + u;
+            } else if (MODE == 3) {
+                rows[0] = rope_pair_row(u, 0, p.rope_hd);
+                rows[1] = rope_pair_row(u, 1, p.rope_hd);
+            } else {
+                rows[0] = rows[1] = u;
+            }
+            float acc[2][kGenTokens];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int m = 0; m < kGenTokens; ++m) acc[h][m] = 0.f;
+                for (int m = 0; m < kGenTokens; ++m) acc[h][m] = 0.f;
 #pragma unroll
-        for (int h = 0; h < (PAIRS ? 2 : 1); ++h) {
-            const uint32_t *wrow = p.wq + rows[h] * wpr;
-            const uint16_t *srow = p.sc + rows[h] * G;
-            const uint16_t *brow = p.bi + rows[h] * G;
-            for (int c0 = 0; c0 < nch; c0 += NQ * kWarp) {
-                // the step's codes, scales and biases (scale | bias << 16),
-                // every load issued before any is used
-                uint32_t words[NQ][CW], sb[NQ];
+            for (int h = 0; h < (PAIRS ? 2 : 1); ++h) {
+                const uint32_t *wrow = p.wq + rows[h] * wpr;
+                const uint16_t *srow = p.sc + rows[h] * G;
+                const uint16_t *brow = p.bi + rows[h] * G;
+                for (int c0 = 0; c0 < nch; c0 += NQ * kWarp) {
+                    // the step's codes, scales and biases (scale | bias << 16),
+                    // every load issued before any is used
+                    uint32_t words[NQ][CW], sb[NQ];
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const int ci = c0 + q * kWarp + lane;
-                    if (ci < nch) {
-                        gd_load<CW>(wrow + ci * CW, words[q]);
-                        const int g = (ci * kGdChunk) >> gshift;
-                        sb[q] = (uint32_t)srow[g] | ((uint32_t)brow[g] << 16);
-                    } else {
+                    for (int q = 0; q < NQ; ++q) {
+                        const int ci = c0 + q * kWarp + lane;
+                        if (ci < nch) {
+                            gd_load<CW>(wrow + ci * CW, words[q]);
+                            const int g = (ci * kGdChunk) >> gshift;
+                            sb[q] = (uint32_t)srow[g] | ((uint32_t)brow[g] << 16);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < CW; ++j) words[q][j] = 0u;
-                        sb[q] = 0u;
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const int ci = c0 + q * kWarp + lane;
-                    if (ci >= nch) break;
-                    const int g = (ci * kGdChunk) >> gshift;
-                    const float sc = bf16_lo(sb[q]), bi = bf16_hi(sb[q]);
-                    uint32_t bw[8];
-                    gd_spread<BITS>(words[q], bw);
-#pragma unroll
-                    for (int m = 0; m < kGenTokens; ++m) {
-                        if (m >= M) break;
-                        const uint4 *xp = reinterpret_cast<const uint4 *>(xe + m * K);
-                        int d = 0;
-#pragma unroll
-                        for (int s4 = 0; s4 < 4; ++s4) {
-                            const uint4 x4 = xp[s4 * nch + ci];
-                            d = dp2a_hi(x4.y, bw[2 * s4], dp2a_lo(x4.x, bw[2 * s4], d));
-                            d = dp2a_hi(x4.w, bw[2 * s4 + 1],
-                                        dp2a_lo(x4.z, bw[2 * s4 + 1], d));
+                            for (int j = 0; j < CW; ++j) words[q][j] = 0u;
+                            sb[q] = 0u;
                         }
-                        acc[h][m] = fmaf(sc * xf[m * G + g], (float)d,
-                                         fmaf(bi, xu[m * nch + ci], acc[h][m]));
+                    }
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        const int ci = c0 + q * kWarp + lane;
+                        if (ci >= nch) break;
+                        const int g = (ci * kGdChunk) >> gshift;
+                        const float sc = bf16_lo(sb[q]), bi = bf16_hi(sb[q]);
+                        uint32_t bw[8];
+                        gd_spread<BITS>(words[q], bw);
+#pragma unroll
+                        for (int m = 0; m < kGenTokens; ++m) {
+                            if (m >= M) break;
+                            const uint4 *xp = reinterpret_cast<const uint4 *>(xe + m * K);
+                            const float fg = xf[m * G + g];
+                            float dq;
+                            if (!EX || fg >= 0.f) {
+                                int d = 0;
+#pragma unroll
+                                for (int s4 = 0; s4 < 4; ++s4) {
+                                    const uint4 x4 = xp[s4 * nch + ci];
+                                    d = dp2a_hi(x4.y, bw[2 * s4], dp2a_lo(x4.x, bw[2 * s4], d));
+                                    d = dp2a_hi(x4.w, bw[2 * s4 + 1],
+                                                dp2a_lo(x4.z, bw[2 * s4 + 1], d));
+                                }
+                                dq = fg * (float)d;
+                            } else {  // marked group: fp32 dot of the raw activations
+                                dq = 0.f;
+#pragma unroll
+                                for (int s4 = 0; s4 < 4; ++s4) {
+                                    const uint4 x4 = xp[s4 * nch + ci];
+                                    dq = fdp2a_hi(x4.y, bw[2 * s4], fdp2a_lo(x4.x, bw[2 * s4], dq));
+                                    dq = fdp2a_hi(x4.w, bw[2 * s4 + 1],
+                                                  fdp2a_lo(x4.z, bw[2 * s4 + 1], dq));
+                                }
+                            }
+                            acc[h][m] = fmaf(sc, dq, fmaf(bi, xu[m * nch + ci], acc[h][m]));
+                        }
                     }
                 }
             }
+            gen_finish<MODE>(p, u, rows, acc, lane);
         }
-        gen_finish<MODE>(p, u, rows, acc, lane);
-    }
+    };
+    if (s_mk)
+        unit_loop(std::true_type{});
+    else
+        unit_loop(std::false_type{});
 }
 
 template <int BITS>

@@ -34,7 +34,12 @@ enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2, kGRope = 3 };
 // within one head.
 
 constexpr int kSlice = 16;  // lanes per reduction slice
-// Two CTAs per SM (this one and the next kernel's) must fit in registers.
+// Two CTAs per SM (this one and the next kernel's) must fit in registers:
+// an SM's warps are spread over its four schedulers, each with a quarter of
+// the register file (16K), so two CTAs of 11 warps put 6 warps on some
+// scheduler and can use 80 registers a thread at most (88 would need 16896).
+// The u4 loops fit in 80; the u8 ones keep 88 (one CTA of 11 warps per SM
+// with 88, against spills in the loop at 80).
 constexpr int kGroupMaxThreads = 352;
 // Shared memory per CTA: two CTAs (228 KB per SM, 1 KB reserved each).
 constexpr size_t kGroupSmemCap = 110 * 1024;
@@ -46,13 +51,174 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
     return t;
 }
 
+// The consumer side of the stage loop (see qmv_group_kernel), for a lane
+// whose image is ready.  EX (two-plane path, common.cuh "marked groups"):
+// the lane of a marked chunk forms its int8 residual plane in registers
+// from the raw activations, every lane (zero planes for unmarked chunks)
+// takes both planes' dots in one pass over the code bytes.
+template <int BITS, int MT, int MODE, int RPH, int GS, bool EX>
+__device__ __forceinline__ void group_loop(
+    const uint16_t *x, int K, int G, unsigned char *smem, uint64_t *full,
+    uint64_t *empty, float *red, int *s_consumed, int stages, int nst, int nu,
+    int ups, int slices, uint32_t stage_bytes, uint32_t codes_off,
+    uint32_t rows_stage, uint32_t rowbytes, int ncons, int tid,
+    uint32_t xenc_off) {
+    constexpr int HALVES = (MODE == kGGateUp || MODE == kGRope) ? 2 : 1;
+    constexpr int UPT = RPH / HALVES;
+    constexpr int V = RPH * MT;
+    constexpr int GB = BITS * 8;  // bytes of codes per row and chunk
+    constexpr bool SPLIT = GS == 32;
+    const int lane = tid & (kWarp - 1);
+    const int hw = tid / kSlice;  // half-warp
+    const bool in_group = hw < ups / UPT * slices;  // row groups x slices
+    const int hg = in_group ? hw / slices : 0;  // row group
+    const int sl = in_group ? hw - hg * slices : 0;
+    const int nchunk = K / 64;
+    const int g = sl * kSlice + (tid & (kSlice - 1));  // chunk
+    const bool active = in_group && g < nchunk;
+    // lanes without a chunk read chunk 0 (finite weights) with zero
+    // activations, so their values are exact zeros
+    const int gg = active ? g : 0;
+    // first weight group of the chunk
+    const int sg = GS == 64 ? gg : GS == 128 ? gg >> 1 : 2 * gg;
+    unsigned char *xenc = smem + xenc_off;
+    GroupX<MT> gx;
+    const int rot = chunk_rot<BITS>(gg);
+    load_group_rows<MT, SPLIT, EX ? kMarkDefer : kMarkRaw>(
+        xenc, MT, nchunk, 0, gg, active, gx, image_shift<BITS>(gg));
+    if constexpr (EX) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (gx.mk[m])
+                group_lo_plane<BITS>(x + (int64_t)m * K + gg * 64, gx.f[m], rot,
+                                     gx.lo[m]);
+            else
+#pragma unroll
+                for (int i = 0; i < 16; ++i) gx.lo[m][i] = 0u;
+        }
+    }
+    uint32_t offw[RPH], offs[RPH];
+    const uint32_t sb_delta = rows_stage * (uint32_t)G * 2u;
+#pragma unroll
+    for (int j = 0; j < RPH; ++j) {
+        const uint32_t srow =
+            (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
+        offw[j] = codes_off + srow * rowbytes + (uint32_t)gg * GB;
+        offs[j] = (srow * (uint32_t)G + sg) * 2u;
+    }
+    // rows past the end of a stage of fewer units read the stage's first
+    // row instead (their values are never stored), so that no read
+    // leaves a short slot
+    const uint32_t offw0 = codes_off + (uint32_t)gg * GB;
+    const uint32_t offs0 = (uint32_t)sg * 2u;
+    // this lane's slot of the partial sums: value index idx = j*MT + m
+    // of unit u (stage-relative), half h
+    constexpr int SPREAD = kSlice / V;
+    const bool stores = in_group && (lane & (SPREAD - 1)) == 0;
+    int lu, roff;
+    {
+        const int idx = (lane & (kSlice - 1)) / SPREAD;
+        const int j = idx / MT, m = idx % MT;
+        const int u = hg * UPT + (j % UPT), h = j / UPT;
+        lu = u;
+        roff = ((u * HALVES + h) * MT + m) * slices + sl;
+    }
+    const int rstep = ups * HALVES * MT * slices;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int st = 0; st < nst; ++st) {
+        if (!mbar_wait(&full[s], ph)) {
+            atomicAdd(&g_group_timeouts, 1u);
+            atomicMin(s_consumed, st);
+            break;
+        }
+        const unsigned char *base = smem + (uint32_t)s * stage_bytes;
+        const int left = nu - st * ups;  // units in this stage: min(ups, left)
+        float v[V];
+#pragma unroll
+        for (int j = 0; j < RPH; ++j) {
+            const bool in = hg * UPT + (j % UPT) < left;
+            const uint32_t ow = in ? offw[j] : offw0;
+            const uint32_t os = in ? offs[j] : offs0;
+            uint4 w[BITS / 2];
+            lds_group<BITS>(base + ow, rot, w);
+            if constexpr (SPLIT) {
+                // the scales and biases of the chunk's two groups
+                const uint32_t s2 =
+                    *reinterpret_cast<const uint32_t *>(base + os);
+                const uint32_t b2 =
+                    *reinterpret_cast<const uint32_t *>(base + os + sb_delta);
+                int dl[MT], dh[MT], ll[MT], lh[MT];
+                group_dot_split<BITS, MT>(w, gx, rot, dl, dh);
+                if constexpr (EX)
+                    group_dot_lo_split<BITS, MT>(w, gx, rot, ll, lh);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float fl = bf16_lo(s2) * gx.f[m];
+                    const float fh = bf16_hi(s2) * gx.f[m];
+                    float t = fmaf(bf16_lo(b2), gx.xs[m],
+                                   bf16_hi(b2) * gx.xs2[m]);
+                    if constexpr (EX)  // the residual plane, 2^-7 of the scale
+                        t = fmaf(fl * 0.0078125f, (float)ll[m],
+                                 fmaf(fh * 0.0078125f, (float)lh[m], t));
+                    v[j * MT + m] =
+                        fmaf(fl, (float)dl[m], fmaf(fh, (float)dh[m], t));
+                }
+            } else {
+                const float sv = bf16_bits_to_f32(
+                    *reinterpret_cast<const uint16_t *>(base + os));
+                const float bv = bf16_bits_to_f32(
+                    *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
+                int d[MT], dlo[MT];
+                if constexpr (EX)
+                    group_dot2<BITS, MT>(w, gx, d, dlo);
+                else
+                    group_dot<BITS, MT>(w, gx, d);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float sf = sv * gx.f[m];
+                    float t = bv * gx.xs[m];
+                    if constexpr (EX)  // the residual plane, 2^-7 of the scale
+                        t = fmaf(sf * 0.0078125f, (float)dlo[m], t);
+                    v[j * MT + m] = fmaf(sf, (float)d[m], t);
+                }
+            }
+        }
+        // every lane's reads of this stage are done: release the slot
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        const float tot = sub_reduce<kSlice, V>(v, lane);
+        if (stores && lu < nu) red[roff] = tot;
+        lu += ups;
+        roff += rstep;
+        if (++s == stages) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+}
+
+// The marked instance of group_loop, out of line.
+template <int BITS, int MT, int MODE, int RPH, int GS>
+__device__ __noinline__ void group_loop_marked(
+    const uint16_t *x, int K, int G, unsigned char *smem, uint64_t *full,
+    uint64_t *empty, float *red, int *s_consumed, int stages, int nst, int nu,
+    int ups, int slices, uint32_t stage_bytes, uint32_t codes_off,
+    uint32_t rows_stage, uint32_t rowbytes, int ncons, int tid,
+    uint32_t xenc_off) {
+    group_loop<BITS, MT, MODE, RPH, GS, true>(
+        x, K, G, smem, full, empty, red, s_consumed, stages, nst, nu, ups,
+        slices, stage_bytes, codes_off, rows_stage, rowbytes, ncons, tid,
+        xenc_off);
+}
+
 // A stage holds UPS = RS * UPT units (rows, or gate/up row pairs).  Consumer
 // half-warp h belongs to row group h / slices and covers groups
 // [16 * (h % slices), +16) of that row group's RPH rows.  Half-warps past
 // RS * slices (an odd count rounded up to whole warps) only take part in
 // the shuffles.
 template <int BITS, int MT, int MODE, int RPH, int GS>
-__global__ void __maxnreg__(88)
+__global__ void __maxnreg__(BITS == 4 ? 80 : 88)
     qmv_group_kernel(DenseParams p, int stages, int64_t units, int rs,
                      int slices, uint32_t ring_bytes, uint32_t xenc_off,
                      uint32_t rope_off) {
@@ -149,6 +315,7 @@ __global__ void __maxnreg__(88)
         }
     } else {
         // ------------------------------------------------ consumers
+        // (the lane layout is group_loop's: chunk g of row group hg)
         const int hw = tid / kSlice;              // half-warp
         const bool in_group = hw < rs * slices;
         const int hg = in_group ? hw / slices : 0;  // row group
@@ -156,11 +323,7 @@ __global__ void __maxnreg__(88)
         const int nchunk = p.K / 64;
         const int g = sl * kSlice + (tid & (kSlice - 1));  // chunk
         const bool active = in_group && g < nchunk;
-        // lanes without a chunk read chunk 0 (finite weights) with zero
-        // activations, so their values are exact zeros
         const int gg = active ? g : 0;
-        // first weight group of the chunk
-        const int sg = GS == 64 ? gg : GS == 128 ? gg >> 1 : 2 * gg;
         unsigned char *xenc = smem + xenc_off;
         if constexpr (MODE == kGRope) {
             // the CTA's (cos, sin) table, while the previous kernel drains
@@ -176,99 +339,24 @@ __global__ void __maxnreg__(88)
             }
         }
         pdl_wait_primary();  // x may be the previous kernel's output
-        encode_rows_shared<BITS, SPLIT>(p.x, p.M, MT, p.K, nchunk, tid, ncons,
-                                        xenc);
+        encode_rows_shared<BITS, SPLIT, kMarkDefer>(p.x, p.M, MT, p.K, nchunk,
+                                                    tid, ncons, xenc);
         // the consumer warps only (the producer is in its copy loop)
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
-        GroupX<MT> gx;
-        const int rot = chunk_rot<BITS>(gg);
-        load_group_rows<MT, SPLIT>(xenc, MT, nchunk, 0, gg, active, gx,
-                                   image_shift<BITS>(gg));
-        uint32_t offw[RPH], offs[RPH];
-        const uint32_t sb_delta = rows_stage * (uint32_t)p.G * 2u;
-#pragma unroll
-        for (int j = 0; j < RPH; ++j) {
-            const uint32_t srow =
-                (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
-            offw[j] = codes_off + srow * rowbytes + (uint32_t)gg * GB;
-            offs[j] = (srow * (uint32_t)p.G + sg) * 2u;
-        }
-        // rows past the end of a stage of fewer units read the stage's first
-        // row instead (their values are never stored), so that no read
-        // leaves a short slot
-        const uint32_t offw0 = codes_off + (uint32_t)gg * GB;
-        const uint32_t offs0 = (uint32_t)sg * 2u;
-        // this lane's slot of the partial sums: value index idx = j*MT + m
-        // of unit u (stage-relative), half h
-        constexpr int SPREAD = kSlice / V;
-        const bool stores = in_group && (lane & (SPREAD - 1)) == 0;
-        int lu, roff;
-        {
-            const int idx = (lane & (kSlice - 1)) / SPREAD;
-            const int j = idx / MT, m = idx % MT;
-            const int u = hg * UPT + (j % UPT), h = j / UPT;
-            lu = u;
-            roff = ((u * HALVES + h) * MT + m) * slices + sl;
-        }
-        const int rstep = ups * HALVES * MT * slices;
-        int s = 0;
-        uint32_t ph = 0;
-        for (int st = 0; st < nst; ++st) {
-            if (!mbar_wait(&full[s], ph)) {
-                atomicAdd(&g_group_timeouts, 1u);
-                atomicMin(&s_consumed, st);
-                break;
-            }
-            const unsigned char *base = smem + (uint32_t)s * stage_bytes;
-            const int left = nu - st * ups;  // units in this stage: min(ups, left)
-            float v[V];
-#pragma unroll
-            for (int j = 0; j < RPH; ++j) {
-                const bool in = hg * UPT + (j % UPT) < left;
-                const uint32_t ow = in ? offw[j] : offw0;
-                const uint32_t os = in ? offs[j] : offs0;
-                uint4 w[BITS / 2];
-                lds_group<BITS>(base + ow, rot, w);
-                if constexpr (SPLIT) {
-                    // the scales and biases of the chunk's two groups
-                    const uint32_t s2 =
-                        *reinterpret_cast<const uint32_t *>(base + os);
-                    const uint32_t b2 =
-                        *reinterpret_cast<const uint32_t *>(base + os + sb_delta);
-                    int dl[MT], dh[MT];
-                    group_dot_split<BITS, MT>(w, gx, rot, dl, dh);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-                        v[j * MT + m] = fmaf(
-                            bf16_lo(s2) * gx.f[m], (float)dl[m],
-                            fmaf(bf16_hi(s2) * gx.f[m], (float)dh[m],
-                                 fmaf(bf16_lo(b2), gx.xs[m],
-                                      bf16_hi(b2) * gx.xs2[m])));
-                } else {
-                    const float sv = bf16_bits_to_f32(
-                        *reinterpret_cast<const uint16_t *>(base + os));
-                    const float bv = bf16_bits_to_f32(
-                        *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
-                    int d[MT];
-                    group_dot<BITS, MT>(w, gx, d);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-                        v[j * MT + m] =
-                            fmaf(sv * gx.f[m], (float)d[m], bv * gx.xs[m]);
-                }
-            }
-            // every lane's reads of this stage are done: release the slot
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            const float tot = sub_reduce<kSlice, V>(v, lane);
-            if (stores && lu < nu) red[roff] = tot;
-            lu += ups;
-            roff += rstep;
-            if (++s == stages) {
-                s = 0;
-                ph ^= 1;
-            }
-        }
+        // Marked chunks (common.cuh, "marked groups"): if any consumer lane
+        // holds one, the CTA runs the two-plane loop, kept out of line so
+        // that the plain loop below keeps its code and registers.
+        const bool mk = active && chunk_marked<MT, SPLIT>(xenc, nchunk, gg);
+        if (bar_red_or(1, ncons, mk))
+            group_loop_marked<BITS, MT, MODE, RPH, GS>(
+                p.x, p.K, p.G, smem, full, empty, red, &s_consumed, stages, nst,
+                nu, ups, slices, stage_bytes, codes_off, rows_stage, rowbytes,
+                ncons, tid, xenc_off);
+        else
+            group_loop<BITS, MT, MODE, RPH, GS, false>(
+                p.x, p.K, p.G, smem, full, empty, red, &s_consumed, stages, nst,
+                nu, ups, slices, stage_bytes, codes_off, rows_stage, rowbytes,
+                ncons, tid, xenc_off);
     }
     __syncthreads();
     pdl_wait_primary();  // outputs may alias the previous kernel's inputs
@@ -365,7 +453,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     const size_t rope_bytes =
         MODE == kGRope ? ((size_t)umax * MT * 8 + 15) / 16 * 16 : 0;
     const size_t fixed = 16 * 8 + ((red_bytes + 15) / 16) * 16 + rope_bytes +
-                         ximg_bytes(MT, nchunk, GS == 32);
+                         ximg_bytes(MT, nchunk, GS == 32, true);
     if (fixed >= kGroupSmemCap) return cudaSuccess;
     int stages = (int)((kGroupSmemCap - fixed) / stage_bytes);
     if (stages > 8) stages = 8;
@@ -388,7 +476,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     }
     const size_t rope_off = ring + 16 * stages + ((red_bytes + 15) / 16) * 16;
     const size_t xenc_off = rope_off + rope_bytes;
-    const size_t smem = xenc_off + ximg_bytes(MT, nchunk, GS == 32);
+    const size_t smem = xenc_off + ximg_bytes(MT, nchunk, GS == 32, true);
     auto kern = qmv_group_kernel<BITS, MT, MODE, RPH, GS>;
     int dummy = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),

@@ -21,6 +21,8 @@
 //    buffers, or SiLU(gate)*up.
 // Formulas and sources as in qmv.cu ("Sanctum-MLX"; "The Cathedral Doubled
 // Itself", "The two fusions"; "saragossa", "Quantization formats").
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,11 +45,13 @@ struct XRegs {
     uint32_t pr[MT][CODES / 2];
     float f[MT];
     float xs[MT];
+    bool mk[MT];                 // marked group (common.cuh, "marked groups")
+    uint32_t lo[MT][CODES / 4];  // its int8 residual plane, in dp4a order
 };
 
 // Loads and encodes chunk c of each token.  Every lane of the warp must
-// call this (the lanes of one group agree on its scale through shuffles);
-// inactive lanes encode zeros.
+// call this (the lanes of one group agree on its scale and mark through
+// shuffles); inactive lanes encode zeros.
 template <int BITS, int MT>
 __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
                                             int M, int K, int c, bool active,
@@ -87,6 +91,19 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
         float xs = 0.f;
 #pragma unroll
         for (int i = 0; i < CODES; ++i) xs += v[i];
+        // the group's rounding error and magnitude in units of f
+        float re = 0.f, ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < CODES; ++i) {
+            re += i16_resid(v[i], finv);
+            ab += fabsf(v[i]);
+        }
+#pragma unroll
+        for (int o = 1; o < CPG; o <<= 1) {
+            re += __shfl_xor_sync(0xffffffffu, re, o);
+            ab += __shfl_xor_sync(0xffffffffu, ab, o);
+        }
+        const bool marked = group_marked(re, ab * finv);
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
             if constexpr (BITS == 4) {
@@ -101,7 +118,23 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
                 xr.pr[m][2 * wd + 1] = t[1];
             }
         }
+        // the residual plane (zero unless marked): per u4 word the entries
+        // of its low nibbles' inputs (x0 x2 x4 x6), then of its high ones;
+        // per u8 word x0..x3
+#pragma unroll
+        for (int i = 0; i < CODES / 4; ++i) {
+            uint32_t q = 0u;
+            if (marked) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = BITS == 4 ? 8 * (i >> 1) + 2 * k + (i & 1) : 4 * i + k;
+                    q |= i8_resid(v[e], finv) << (8 * k);
+                }
+            }
+            xr.lo[m][i] = q;
+        }
         xr.f[m] = f;
+        xr.mk[m] = marked;
         xr.xs[m] = xs;
     }
 }
@@ -109,56 +142,96 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
 // Chunk dots of R rows against MT tokens: exact integer sums per chunk,
 // then (s * 2^E) * D + b * sum(x) in fp32.  The word loop is outside the row
 // loop so the rows' dp2a chains interleave; a word's code bytes are split
-// once and reused for every token.
-template <int BITS, int MT, int R>
+// once and reused for every token.  With EX, the same words also meet the
+// tokens' int8 residual planes (common.cuh, "marked groups"; zero for
+// unmarked groups).
+template <int BITS, int MT, int R, bool EX>
 __device__ __forceinline__ void batch_dot(const uint4 (&w)[R],
                                           const float (&s)[R],
                                           const float (&b)[R],
                                           const XRegs<BITS, MT> &xr,
                                           float (&out)[R][MT]) {
-    int d[R][MT][2];
+    {
+        int d[R][MT][2];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) d[r][m][0] = d[r][m][1] = 0;
+            for (int m = 0; m < MT; ++m) d[r][m][0] = d[r][m][1] = 0;
 #pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
+        for (int wd = 0; wd < 4; ++wd) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t word = wd == 0   ? w[r].x
-                                  : wd == 1 ? w[r].y
-                                  : wd == 2 ? w[r].z
-                                            : w[r].w;
-            if constexpr (BITS == 4) {
-                // high nibbles stay in place (16 * q) and are summed apart
-                const uint32_t lo = word & 0x0f0f0f0fu;
-                const uint32_t hi = word & 0xf0f0f0f0u;
+            for (int r = 0; r < R; ++r) {
+                const uint32_t word = wd == 0   ? w[r].x
+                                      : wd == 1 ? w[r].y
+                                      : wd == 2 ? w[r].z
+                                                : w[r].w;
+                if constexpr (BITS == 4) {
+                    // high nibbles stay in place (16 * q) and are summed apart
+                    const uint32_t lo = word & 0x0f0f0f0fu;
+                    const uint32_t hi = word & 0xf0f0f0f0u;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const uint32_t *pr = xr.pr[m] + 4 * wd;
-                    d[r][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, d[r][m][0]));
-                    d[r][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, d[r][m][1]));
-                }
-            } else {
+                    for (int m = 0; m < MT; ++m) {
+                        const uint32_t *pr = xr.pr[m] + 4 * wd;
+                        d[r][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, d[r][m][0]));
+                        d[r][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, d[r][m][1]));
+                    }
+                } else {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const uint32_t *pr = xr.pr[m] + 2 * wd;
-                    int a = d[r][m][wd & 1];
-                    a = dp2a_lo(pr[0], word, a);
-                    d[r][m][wd & 1] = dp2a_hi(pr[1], word, a);
+                    for (int m = 0; m < MT; ++m) {
+                        const uint32_t *pr = xr.pr[m] + 2 * wd;
+                        int a = d[r][m][wd & 1];
+                        a = dp2a_lo(pr[0], word, a);
+                        d[r][m][wd & 1] = dp2a_hi(pr[1], word, a);
+                    }
                 }
             }
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                // u4: the high-nibble sum is 16x the true sum, exactly
+                const int dsum = BITS == 4 ? d[r][m][0] + (d[r][m][1] >> 4)
+                                           : d[r][m][0] + d[r][m][1];
+                out[r][m] = fmaf(s[r] * xr.f[m], (float)dsum, b[r] * xr.xs[m]);
+            }
     }
+    if constexpr (EX) {
+        // the residual planes, 2^-7 of the scale, after the first dot so
+        // that the two sets of accumulators are never live together
+        int e[R][MT];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            // u4: the high-nibble sum is 16x the true sum, exactly
-            const int dsum = BITS == 4 ? d[r][m][0] + (d[r][m][1] >> 4)
-                                       : d[r][m][0] + d[r][m][1];
-            out[r][m] = fmaf(s[r] * xr.f[m], (float)dsum, b[r] * xr.xs[m]);
+            for (int m = 0; m < MT; ++m) e[r][m] = 0;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t word = wd == 0   ? w[r].x
+                                      : wd == 1 ? w[r].y
+                                      : wd == 2 ? w[r].z
+                                                : w[r].w;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if constexpr (BITS == 4) {
+                        // the high nibbles' products in place (16x), then
+                        // the low ones' scaled to match
+                        const int t = dp4a_us(word & 0xf0f0f0f0u, xr.lo[m][2 * wd + 1], 0);
+                        e[r][m] = dp4a_us(word & 0x0f0f0f0fu, xr.lo[m][2 * wd],
+                                          e[r][m] + (t >> 4));
+                    } else {
+                        e[r][m] = dp4a_us(word, xr.lo[m][wd], e[r][m]);
+                    }
+                }
+            }
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                out[r][m] = fmaf(s[r] * xr.f[m] * 0.0078125f, (float)e[r][m], out[r][m]);
+    }
 }
 
 // Sum of the per-warp slots of one output, in a fixed order.
@@ -177,8 +250,12 @@ __device__ __forceinline__ float red_total(const float *red, int idx, int nwh) {
 // and were slower on the 48-layer stack).
 constexpr int kRowsPerThread = 4;
 
+// Registers: up to two tokens, 80 per thread, so that two CTAs of 352 threads
+// (rows of 5120 inputs: this kernel and the next one in the stream) share an
+// SM (each scheduler's quarter of the register file holds 6 warps of 80);
+// four tokens need more and run one CTA per SM.
 template <int BITS, int MT, int MODE, int RPH>
-__global__ void __launch_bounds__(kStreamMaxThreads)
+__global__ void __maxnreg__(MT == 4 ? 128 : 80)
     qmv_stream_kernel(DenseParams p, int stages, int64_t units, int rs) {
     constexpr int HALVES = (MODE == kSGateUp || MODE == kSRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;     // units per thread per stage
@@ -290,48 +367,61 @@ __global__ void __launch_bounds__(kStreamMaxThreads)
             offw[j] = srow * rowbytes + (uint32_t)cc * 16u;
             offs[j] = rows_stage * rowbytes + (srow * (uint32_t)p.G + g) * 2u;
         }
-        for (int st = 0; st < nst; ++st) {
-            const int s = st % stages;
-            if (!mbar_wait(&full[s], (st / stages) & 1)) {
-                atomicAdd(&g_stream_timeouts, 1u);
-                atomicMin(&s_consumed, st);
-                break;
-            }
-            const int64_t ua = u0 + (int64_t)st * ups;
-            const int n = (int)min((int64_t)ups, u1 - ua);
-            const unsigned char *base = smem + (uint32_t)s * stage_bytes;
-            uint4 w[RPH];
-            float sv[RPH], bv[RPH];
+        // The stage loop, once with the residual-plane dot (EX) and once
+        // without it: a warp none of whose lanes holds a marked group runs
+        // the one-plane copy.
+        auto stage_loop = [&](auto ex) {
+            constexpr bool EX = decltype(ex)::value;
+            for (int st = 0; st < nst; ++st) {
+                const int s = st % stages;
+                if (!mbar_wait(&full[s], (st / stages) & 1)) {
+                    atomicAdd(&g_stream_timeouts, 1u);
+                    atomicMin(&s_consumed, st);
+                    break;
+                }
+                const int64_t ua = u0 + (int64_t)st * ups;
+                const int n = (int)min((int64_t)ups, u1 - ua);
+                const unsigned char *base = smem + (uint32_t)s * stage_bytes;
+                uint4 w[RPH];
+                float sv[RPH], bv[RPH];
 #pragma unroll
-            for (int j = 0; j < RPH; ++j) {
-                w[j] = *reinterpret_cast<const uint4 *>(base + offw[j]);
-                sv[j] = bf16_bits_to_f32(
-                    *reinterpret_cast<const uint16_t *>(base + offs[j]));
-                bv[j] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(
-                    base + offs[j] + sb_delta));
-            }
-            float o[RPH][MT];
-            batch_dot<BITS, MT, RPH>(w, sv, bv, xr, o);
-            float v[V];
+                for (int j = 0; j < RPH; ++j) {
+                    w[j] = *reinterpret_cast<const uint4 *>(base + offw[j]);
+                    sv[j] = bf16_bits_to_f32(
+                        *reinterpret_cast<const uint16_t *>(base + offs[j]));
+                    bv[j] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(
+                        base + offs[j] + sb_delta));
+                }
+                float o[RPH][MT];
+                batch_dot<BITS, MT, RPH, EX>(w, sv, bv, xr, o);
+                float v[V];
 #pragma unroll
-            for (int j = 0; j < RPH; ++j)
+                for (int j = 0; j < RPH; ++j)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) v[j * MT + m] = o[j][m];
-            // every lane's reads of this stage are done: release the slot
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            const float tot = transpose_reduce<V>(v, lane);
-            constexpr int SPREAD = kWarp / V;
-            if ((lane & (SPREAD - 1)) == 0) {
-                const int idx = lane / SPREAD;  // j * MT + m
-                const int j = idx / MT, m = idx % MT;
-                const int u = hg * UPT + (j % UPT), h = j / UPT;
-                // per-warp slot: the epilogue adds the warps in a fixed order
-                if (u < n)
-                    red[((((st * ups + u) * HALVES + h) * MT + m) * nwh) + wh] =
-                        tot;
+                    for (int m = 0; m < MT; ++m) v[j * MT + m] = o[j][m];
+                // every lane's reads of this stage are done: release the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                const float tot = transpose_reduce<V>(v, lane);
+                constexpr int SPREAD = kWarp / V;
+                if ((lane & (SPREAD - 1)) == 0) {
+                    const int idx = lane / SPREAD;  // j * MT + m
+                    const int j = idx / MT, m = idx % MT;
+                    const int u = hg * UPT + (j % UPT), h = j / UPT;
+                    // per-warp slot: the epilogue adds the warps in a fixed order
+                    if (u < n)
+                        red[((((st * ups + u) * HALVES + h) * MT + m) * nwh) + wh] =
+                            tot;
+                }
             }
-        }
+        };
+        bool anymk = false;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) anymk |= xr.mk[m];
+        if (__any_sync(0xffffffffu, anymk))
+            stage_loop(std::true_type{});
+        else
+            stage_loop(std::false_type{});
     }
     __syncthreads();
     pdl_wait_primary();  // outputs may alias the previous kernel's inputs

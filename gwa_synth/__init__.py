@@ -6,7 +6,9 @@ distributions of the workloads below, and hands the same arrays to both the
 CUDA library and the CPU oracle.
 
 Recipe (every draw from numpy's PCG64 with an explicit seed):
-  * activations x: bf16(N(0, 1));
+  * activations x: bf16(N(0, 1)); for the edge-case tests also N(0, 1)
+    with outlier channels (1e2 .. 1e4), N(0, 1) scaled by 2^U{-14..8} per
+    element, and groups of zeros and bf16 subnormals;
   * packed weights: uniform random uint32 words, so every b-bit field of every
     word is an independent uniform code in 0 .. 2^b - 1;
   * scales: bf16(U(0.005, 0.02)), one per row per group of 64 inputs;
@@ -76,6 +78,57 @@ def activations(seed: int, M: int, K: int) -> np.ndarray:
     """x bf16 [M, K] ~ N(0, 1)."""
     r = rng_for(seed)
     return bf16_bits(r.standard_normal((M, K), dtype=np.float32))
+
+
+def activations_outliers(seed: int, M: int, K: int, values=(1e3,),
+                         count: int = 3) -> np.ndarray:
+    """x bf16 [M, K] ~ N(0, 1) with `count` entries of each row set to
+    +-v for v cycling over `values` (outlier channels), at positions drawn
+    without replacement."""
+    r = rng_for(seed)
+    x = r.standard_normal((M, K), dtype=np.float32)
+    for m in range(M):
+        pos = r.choice(K, size=count, replace=False)
+        sign = np.where(r.random(count) < 0.5, -1.0, 1.0)
+        for i, k in enumerate(pos):
+            x[m, k] = sign[i] * values[i % len(values)]
+    return bf16_bits(x)
+
+
+def activations_wide(seed: int, M: int, K: int, lo: int = -14,
+                     hi: int = 8) -> np.ndarray:
+    """x bf16 [M, K]: N(0, 1) times 2^e, e uniform on lo..hi per element, so
+    every group of 64 spans far more than 2^8 in magnitude."""
+    r = rng_for(seed)
+    x = r.standard_normal((M, K), dtype=np.float32)
+    e = r.integers(lo, hi + 1, size=(M, K))
+    return bf16_bits(np.ldexp(x, e).astype(np.float32))
+
+
+def activations_edge(seed: int, M: int, K: int) -> np.ndarray:
+    """x bf16 [M, K] of edge values, cycling over the groups of 64: a group
+    of zeros (both signs), a group of bf16 subnormals, normal values with a
+    few subnormals and zeros among them, and plain N(0, 1)."""
+    r = rng_for(seed)
+    h = bf16_bits(r.standard_normal((M, K), dtype=np.float32))
+    G = K // GROUP
+    for m in range(M):
+        for g in range(G):
+            sl = slice(g * GROUP, (g + 1) * GROUP)
+            kind = (g + m) % 4
+            if kind == 0:
+                h[m, sl] = np.where(r.random(GROUP) < 0.5, 0x0000, 0x8000)
+            elif kind == 1:
+                sub = r.integers(1, 0x80, size=GROUP).astype(np.uint16)
+                h[m, sl] = sub | np.where(r.random(GROUP) < 0.5, 0, 0x8000
+                                          ).astype(np.uint16)
+            elif kind == 2:
+                idx = r.choice(GROUP, size=12, replace=False)
+                seg = h[m, sl].copy()
+                seg[idx[:6]] = r.integers(1, 0x80, size=6).astype(np.uint16)
+                seg[idx[6:]] = 0
+                h[m, sl] = seg
+    return h
 
 
 def packed_words(rng: np.random.Generator, N: int, K: int,
