@@ -665,27 +665,30 @@ def oracle_layer_prep(bits: int, M: int):
     return shapes, ws, xs
 
 
-def oracle_layer_pass(prep, bits: int):
+def oracle_layer_pass(prep, bits: int, nthreads: int = 0):
     import oracle
     shapes, ws, xs = prep
     for (name, rows, K), w in zip(shapes, ws):
         if name == "gate_up":
-            oracle.gate_up_silu(xs[K], w.wq, w.scales, w.biases, rows, K, bits)
+            oracle.gate_up_silu(xs[K], w.wq, w.scales, w.biases, rows, K, bits,
+                                nthreads=nthreads)
         else:
-            oracle.qmv(xs[K], w.wq, w.scales, w.biases, rows, K, bits)
+            oracle.qmv(xs[K], w.wq, w.scales, w.biases, rows, K, bits,
+                       nthreads=nthreads)
 
 
 def oracle_layer_sample(bits: int, M: int, seconds: float, max_reps: int,
-                        prep=None):
+                        prep=None, nthreads: int = 0):
     """Times the oracle on layer 0's four projections, repeated until
-    `seconds` have passed or `max_reps` passes ran."""
+    `seconds` have passed or `max_reps` passes ran (`nthreads` 0: all of
+    the oracle's OpenMP threads)."""
     import oracle
     oracle.build()
     prep = prep or oracle_layer_prep(bits, M)
-    nthreads = oracle.max_threads()
+    nthreads = nthreads or oracle.max_threads()
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_layer_pass(prep, bits)
+        oracle_layer_pass(prep, bits, nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= max_reps:
@@ -694,14 +697,22 @@ def oracle_layer_sample(bits: int, M: int, seconds: float, max_reps: int,
 
 
 def cpu_baseline(args):
-    reps, el, nthreads = oracle_layer_sample(args.bits, args.tokens, 10.0, 48)
+    prep = oracle_layer_prep(args.bits, args.tokens)
+    reps, el, nthreads = oracle_layer_sample(args.bits, args.tokens, 10.0, 48,
+                                             prep)
+    reps1, el1, _ = oracle_layer_sample(args.bits, args.tokens, 4.0, 16, prep,
+                                        nthreads=1)
     lb = sum(layer_bytes(args.bits, args.tokens).values())
     return {"value": round(reps * lb / el / 1e9, 4), "unit": "GB/s",
             "cores": nthreads, "kind": "oracle",
             "steps_per_s": round(reps / el / args.layers, 6),
+            "one_thread": {"value": round(reps1 * lb / el1 / 1e9, 4),
+                           "unit": "GB/s", "cores": 1,
+                           "sample": f"{reps1} pass(es), {el1:.1f} s"},
             "sample": (f"{reps} pass(es) of layer 0's four projections "
                        f"(fp64 C oracle, {nthreads} OpenMP threads), "
-                       f"{el:.1f} s; GB/s of the same algorithmic bytes")}
+                       f"{el:.1f} s; GB/s of the same algorithmic bytes; "
+                       f"one_thread: the same on one thread")}
 
 
 def run_reference(args, rank: int):
@@ -821,6 +832,11 @@ def main():
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": recorded_traffic(dom),
+                     "traffic_source": "dram__bytes_read.sum + "
+                     "dram__bytes_write.sum per launch from the ncu capture "
+                     "recorded in profiles/qmv_group_gate_up_27648x5120_m1.md "
+                     "(not measured by this run); null when absent or when "
+                     "the kernel's sources changed since the capture",
                      "algorithmic_bytes": lb[dom]},
         "kernels": kernels,
         "kernels_timing": "per projection type: one graph of its 48 launches "

@@ -189,9 +189,10 @@ __device__ __forceinline__ int dot_total(const int (&acc)[2]) {
 //    scale is negative, and its dots are taken by the fp32 counterparts of
 //    dp2a below (codes and activations exact, every product exact, fp32
 //    sums).
-// The kernels decide per warp (or per CTA), before their main loop, whether
-// any lane holds a marked group, and run a copy of the loop without the
-// marked path otherwise.
+// The kernels decide before their main loop, per CTA (one-token, staged,
+// general and MoE kernels) or per warp (streaming kernel), whether any
+// group is marked, and otherwise run a copy of the loop without the marked
+// path.
 __device__ __forceinline__ bool group_marked(float r, float a) {
     return r * 65536.0f > a;
 }

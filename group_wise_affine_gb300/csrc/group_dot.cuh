@@ -28,7 +28,6 @@ struct GroupX {
                           // (split: of its first 32)
     float xs2[MT];        // split: plain fp32 sum of its last 32
     bool mk[MT];          // marked chunk (common.cuh, "marked groups")
-    uint32_t lo[MT][16];  // two-plane path: its int8 residual plane
 };
 
 // int16 of v * finv, rounded to nearest even: adding 1.5 * 2^23 puts the
@@ -157,7 +156,18 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
                 __float2half_rn(fmaf(ab * finv, -1.0f / 65536.0f, re));
         }
     }
+
 }
+
+// Slot (16-byte piece of the chunk's pairs in the image) that holds quarter
+// q's residual plane in the two-plane path: the pieces follow the order in
+// which lds_group loads the chunk's codes (rotation rot = chunk_rot(g)), so
+// register piece v of the codes meets plane slots 2v, 2v + 1 (u4) or v (u8).
+template <int BITS>
+__device__ __forceinline__ int group_lo_slot(int q, int rot) {
+    return BITS == 4 ? 2 * (((q >> 1) - rot) & 1) + (q & 1) : (q - rot) & 3;
+}
+
 
 // All `ncons` threads (whole warps) encode R rows of K activations into the
 // image: row r from x + src(r) * K, src(r) = rowsrc ? rowsrc[r] : r (rows
@@ -330,146 +340,137 @@ __device__ __forceinline__ void group_dot(const uint4 (&w)[BITS / 2],
     }
 }
 
-// The int8 residual plane of a marked chunk (two-plane path, common.cuh
-// "marked groups"), formed by the lane that owns the chunk from its 64 raw
-// bf16 activations x (16-byte aligned) and its scale f as stored in GroupX
-// (u4: 2^E / 16).  Register v * P + j holds the entries of code piece
-// (v + rot) & (NV - 1) (the order lds_group loads the codes in), P = 16 / NV
-// registers per piece, in dp4a order: per u4 word the entries of its low
-// nibbles' inputs (x0 x2 x4 x6), then of its high nibbles' (x1 x3 x5 x7);
-// per u8 word x0..x3.
+// The int8 residual plane of a chunk (two-plane path, common.cuh "marked
+// groups") written over its pairs in the image (dead by then: every lane
+// holds its pairs in registers) at dst[slot * stride], slots as
+// group_lo_slot for rotation rot: zeros unless `marked`, else formed from
+// its 64 raw bf16 activations x (16-byte aligned) and its scale f as stored
+// in GroupX (u4: 2^E / 16).  Quarter q (inputs 16q .. 16q + 15) in dp4a
+// order: per u4 word the entries of its low nibbles' inputs (x0 x2 x4 x6),
+// then of its high nibbles' (x1 x3 x5 x7); per u8 word x0..x3.  A loop, not
+// unrolled: it runs once per chunk.
 template <int BITS>
-__device__ __forceinline__ void group_lo_plane(const uint16_t *x, float f,
-                                               int rot, uint32_t (&lo)[16]) {
-    constexpr int NV = BITS / 2;
-    constexpr int P = 16 / NV;
-    const float finv = 1.0f / (BITS == 4 ? 16.0f * f : f);  // exact: 2^-E
-    uint32_t raw[16];
+__device__ __forceinline__ void group_lo_store(bool marked, const uint16_t *x,
+                                               float f, int rot, uint4 *dst,
+                                               int stride) {
+    const float finv = marked ? 1.0f / (BITS == 4 ? 16.0f * f : f) : 0.f;
     const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+        if (marked) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {  // activations 8i .. 8i + 7
-        const uint4 u = xv[i];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint32_t e[8];
+            for (int h = 0; h < 2; ++h) {
+                const uint4 u = xv[2 * q + h];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                uint32_t e[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            e[2 * k] = i8_resid(bf16_lo(w[k]), finv);
-            e[2 * k + 1] = i8_resid(bf16_hi(w[k]), finv);
+                for (int k = 0; k < 4; ++k) {
+                    e[2 * k] = i8_resid(bf16_lo(w[k]), finv);
+                    e[2 * k + 1] = i8_resid(bf16_hi(w[k]), finv);
+                }
+                if constexpr (BITS == 4) {  // one u4 word: even, then odd
+                    w4[2 * h] = e[0] | (e[2] << 8) | (e[4] << 16) | (e[6] << 24);
+                    w4[2 * h + 1] = e[1] | (e[3] << 8) | (e[5] << 16) | (e[7] << 24);
+                } else {  // two u8 words
+                    w4[2 * h] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
+                    w4[2 * h + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
+                }
+            }
         }
-        if constexpr (BITS == 4) {  // one u4 word: even, then odd entries
-            raw[2 * i] = e[0] | (e[2] << 8) | (e[4] << 16) | (e[6] << 24);
-            raw[2 * i + 1] = e[1] | (e[3] << 8) | (e[5] << 16) | (e[7] << 24);
-        } else {  // two u8 words
-            raw[2 * i] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
-            raw[2 * i + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
-        }
+        dst[(size_t)group_lo_slot<BITS>(q, rot) * stride] =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
     }
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            uint32_t t = raw[v * P + j];
-#pragma unroll
-            for (int r = 1; r < NV; ++r)
-                if (rot == r) t = raw[((v + r) & (NV - 1)) * P + j];
-            lo[v * P + j] = t;
-        }
 }
 
 // group_dot and the residual-plane dot of the two-plane path in one pass
-// (the code bytes split once): dh as group_dot's d, dl the same dot with
-// gx.lo (its scale 2^-7 of dh's).
+// over the code bytes: dh as group_dot's d; dl the same dot with the plane
+// at lo[0], lo[stride], ... (slots as group_lo_slot), read word by word,
+// its scale 2^-7 of dh's.  w as lds_group loaded it.
 template <int BITS, int MT>
 __device__ __forceinline__ void group_dot2(const uint4 (&w)[BITS / 2],
-                                           const GroupX<MT> &gx, int (&dh)[MT],
-                                           int (&dl)[MT]) {
-    int a[MT][4], b[MT][2];
+                                           const GroupX<MT> &gx, const uint4 *lo,
+                                           int stride, int (&dh)[MT], int &dl) {
+    constexpr int NV = BITS / 2;
+    int a[MT][4], b[2] = {0, 0};
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        a[m][0] = a[m][1] = a[m][2] = a[m][3] = 0;
-        b[m][0] = b[m][1] = 0;
-    }
+    for (int m = 0; m < MT; ++m) a[m][0] = a[m][1] = a[m][2] = a[m][3] = 0;
 #pragma unroll
-    for (int v = 0; v < BITS / 2; ++v) {
+    for (int v = 0; v < NV; ++v) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int wd = 4 * v + c;
             const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
                                   : c == 2 ? w[v].z : w[v].w;
             if constexpr (BITS == 4) {
-                const uint32_t lo = word & 0x0f0f0f0fu;
-                const uint32_t hi = word & 0xf0f0f0f0u;
+                // plane entries of this word: slot 2v + c/2, words
+                // 2(c%2), 2(c%2) + 1
+                const uint2 e = reinterpret_cast<const uint2 *>(
+                    lo + (size_t)(2 * v + (c >> 1)) * stride)[c & 1];
+                const uint32_t l = word & 0x0f0f0f0fu;
+                const uint32_t h = word & 0xf0f0f0f0u;
                 const int p = (wd & 1) * 2;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     const uint32_t *pr = gx.pr[m] + 4 * wd;
-                    a[m][p] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, a[m][p]));
-                    a[m][p + 1] =
-                        dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, a[m][p + 1]));
-                    b[m][0] = dp4a_us(lo, gx.lo[m][2 * wd], b[m][0]);
-                    b[m][1] = dp4a_us(hi, gx.lo[m][2 * wd + 1], b[m][1]);
+                    a[m][p] = dp2a_hi(pr[1], l, dp2a_lo(pr[0], l, a[m][p]));
+                    a[m][p + 1] = dp2a_hi(pr[3], h, dp2a_lo(pr[2], h, a[m][p + 1]));
                 }
+                b[0] = dp4a_us(l, e.x, b[0]);
+                b[1] = dp4a_us(h, e.y, b[1]);
             } else {
+                const uint32_t e = reinterpret_cast<const uint32_t *>(
+                    lo + (size_t)v * stride)[c];
                 const int p = wd & 3;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     const uint32_t *pr = gx.pr[m] + 2 * wd;
                     a[m][p] = dp2a_hi(pr[1], word, dp2a_lo(pr[0], word, a[m][p]));
-                    b[m][wd & 1] = dp4a_us(word, gx.lo[m][wd], b[m][wd & 1]);
                 }
+                b[wd & 1] = dp4a_us(word, e, b[wd & 1]);
             }
         }
     }
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        if constexpr (BITS == 4) {
-            dh[m] = 16 * (a[m][0] + a[m][2]) + (a[m][1] + a[m][3]);
-            dl[m] = 16 * b[m][0] + b[m][1];
-        } else {
-            dh[m] = (a[m][0] + a[m][1]) + (a[m][2] + a[m][3]);
-            dl[m] = b[m][0] + b[m][1];
-        }
-    }
+    for (int m = 0; m < MT; ++m)
+        dh[m] = BITS == 4 ? 16 * (a[m][0] + a[m][2]) + (a[m][1] + a[m][3])
+                          : (a[m][0] + a[m][1]) + (a[m][2] + a[m][3]);
+    dl = BITS == 4 ? 16 * b[0] + b[1] : b[0] + b[1];
 }
 
-// The residual-plane dot of group_dot_split's halves (dl over inputs
-// [0, 32), dh over [32, 64), each scaled like group_dot2's dl).
-template <int BITS, int MT>
+// The residual-plane dot of group_dot_split's halves: dl over inputs
+// [0, 32), dh over [32, 64), scaled like group_dot2's dl (slots as
+// group_lo_slot; rot decides which half a register piece falls in).
+template <int BITS>
 __device__ __forceinline__ void group_dot_lo_split(const uint4 (&w)[BITS / 2],
-                                                   const GroupX<MT> &gx, int rot,
-                                                   int (&dl)[MT], int (&dh)[MT]) {
+                                                   const uint4 *lo, int stride,
+                                                   int rot, int &dl, int &dh) {
     constexpr int NV = BITS / 2;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) dl[m] = dh[m] = 0;
+    dl = dh = 0;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        int b[MT][2];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) b[m][0] = b[m][1] = 0;
+        const int pc = (v + rot) & (NV - 1);
+        int b0 = 0, b1 = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int wd = 4 * v + c;
             const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
                                   : c == 2 ? w[v].z : w[v].w;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if constexpr (BITS == 4) {
-                    b[m][0] = dp4a_us(word & 0x0f0f0f0fu, gx.lo[m][2 * wd], b[m][0]);
-                    b[m][1] = dp4a_us(word & 0xf0f0f0f0u, gx.lo[m][2 * wd + 1],
-                                      b[m][1]);
-                } else {
-                    b[m][0] = dp4a_us(word, gx.lo[m][wd], b[m][0]);
-                }
+            if constexpr (BITS == 4) {
+                const uint2 e = reinterpret_cast<const uint2 *>(
+                    lo + (size_t)(2 * v + (c >> 1)) * stride)[c & 1];
+                b0 = dp4a_us(word & 0x0f0f0f0fu, e.x, b0);
+                b1 = dp4a_us(word & 0xf0f0f0f0u, e.y, b1);
+            } else {
+                const uint32_t e = reinterpret_cast<const uint32_t *>(
+                    lo + (size_t)v * stride)[c];
+                b0 = dp4a_us(word, e, b0);
             }
         }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const int dv = BITS == 4 ? 16 * b[m][0] + b[m][1] : b[m][0];
-            if (((v + rot) & (NV - 1)) < NV / 2)
-                dl[m] += dv;
-            else
-                dh[m] += dv;
-        }
+        const int dv = BITS == 4 ? 16 * b0 + b1 : b0;
+        if (pc < NV / 2)
+            dl += dv;
+        else
+            dh += dv;
     }
 }
 

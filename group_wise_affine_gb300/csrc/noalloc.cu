@@ -8,11 +8,11 @@
 // a fixed scratch buffer that lives in the library itself.
 //
 // The scratch is a file-scope device array.  In host code its name is only a
-// host-side stand-in, not a device address, so the device address is looked
-// up once per device with cudaGetSymbolAddress, with that device current,
-// and handed to the kernels as their workspace.
-#include <mutex>
-
+// host-side stand-in, not a device address, so every call looks up the
+// device address on the current device with cudaGetSymbolAddress (no
+// allocation, no synchronization) and hands it to the kernels as their
+// workspace.  Looking it up per call rather than caching it keeps the address
+// right after the device's context is torn down and made again.
 #include "../../include/gwa.h"
 #include "qmm.h"
 
@@ -22,29 +22,15 @@ namespace gwa {
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[GWA_NOALLOC_SCRATCH_BYTES];
 
-static std::mutex g_noalloc_mu;
-static void *g_noalloc_ptr[256];  // per device ordinal; filled on first use
-
-// Device address of the scratch on the current device (set-up on first use).
+// Device address of the scratch on the current device.
 static int noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return set_error(GWA_ERR_CUDA, "gwa_qmv_affine_noalloc: %s",
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+        return set_error(GWA_ERR_CUDA,
+                         "gwa_qmv_affine_noalloc: scratch lookup failed: %s",
                          cudaGetErrorString(e));
-    if (dev < 0 || dev >= 256)
-        return set_error(GWA_ERR_CUDA, "gwa_qmv_affine_noalloc: device %d", dev);
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p)
-            return set_error(GWA_ERR_CUDA,
-                             "gwa_qmv_affine_noalloc: scratch lookup failed: %s",
-                             cudaGetErrorString(e));
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return GWA_OK;
 }
 

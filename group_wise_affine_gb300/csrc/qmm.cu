@@ -12,8 +12,19 @@
 //   y[m,n] = sum_k x[m,k] w'[n,k] + sum_g b'[n,g] X[m,g],  X = per-group sum.
 // b' and X are split into fp16 hi + lo parts and the bias term is carried by
 // three extra columns per group (b'hi*Xhi + b'hi*Xlo + b'lo*Xhi).  Activations
-// are converted to fp16 once per call by a pre-pass (exact for |x| in fp16's
-// normal range); products are exact and accumulate in fp32 in tensor memory.
+// are converted to fp16 once per call by a pre-pass; products are exact and
+// accumulate in fp32 in tensor memory.
+//
+// Range.  fp16 covers 2^-14 .. 65504, bf16 2^-133 .. 3.4e38.  So every token
+// and every weight row is scaled by a power of two before the conversion:
+// token m by 2^e_m, which brings the largest of its |x| and of its group
+// sums |X| into [2^14, 2^15) (pre-pass); row n by 2^f_n, which brings the
+// largest of its |s| * 8 (u4; 128 for u8, the largest |16 s (qh-8)|) and
+// |b'| there (dequantizers, once per tile).  The fp32 epilogue multiplies by
+// 2^-f_n and 2^-e_m, both exact.  Values then stay exact wherever they lie
+// within 2^24 of the largest of their token or row; smaller ones fall into
+// fp16's subnormals and keep an error below 2^-25 of that largest, which is
+// below the fp32 rounding of a sum that holds it.
 //
 // Kernel shape.  A CTA computes one 128-row weight tile (for gate+up: 64 gate
 // rows and the matching 64 up rows) against NT = 128 or 256 tokens, one MMA
@@ -48,9 +59,8 @@ constexpr int kQmmRows = 128;        // weight rows per CTA (MMA M)
 constexpr int kQmmSStages = 2;       // scale/bias-tile ring (8 K blocks each)
 constexpr int kStatusBytes = 256;
 
-// status word bits
+// status word bit: a pipeline wait ran out
 constexpr unsigned kStTimeout = 1u;
-constexpr unsigned kStFp16Range = 2u;
 
 static __device__ unsigned int g_qmm_timeouts;
 
@@ -59,9 +69,24 @@ static int64_t qmm_kext(int64_t K) {
     return K + ((3 * G + 63) / 64) * 64;
 }
 
+// Workspace: status word (256 bytes), the fp16 activations with their bias
+// columns [M, kext], then each token's factor 2^-e_m [M] (fp32).
+static size_t qmm_xe_bytes(int64_t M, int64_t K) {
+    return (((size_t)M * (size_t)qmm_kext(K) * 2 + 255) / 256) * 256;
+}
+
 size_t qmm_workspace_bytes(int64_t M, int64_t K) {
-    const size_t x = (size_t)M * (size_t)qmm_kext(K) * 2;
-    return kStatusBytes + ((x + 255) / 256) * 256;
+    return kStatusBytes + qmm_xe_bytes(M, K) + (((size_t)M * 4 + 255) / 256) * 256;
+}
+
+// 2^p and 2^-p for the power p that brings t (> 0, finite) into
+// [2^14, 2^15), with p clamped so that both stay normal fp32 numbers.
+__device__ __forceinline__ void range_scale(float t, float &up, float &down) {
+    int p = 0;
+    if (t > 0.f && t < 3.0e38f) p = 141 - f32_exp_field(t);
+    p = p < -125 ? -125 : p > 125 ? 125 : p;
+    up = __uint_as_float((uint32_t)(127 + p) << 23);
+    down = __uint_as_float((uint32_t)(127 - p) << 23);
 }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -183,73 +208,93 @@ __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------ pre-pass
-// x_ext[m, :] = fp16 activations of token m in the dequantizers' k order,
-// then per group g three bias columns (Xhi, Xlo, Xhi), then zero padding.
-// u4 order inside each 8-block: 0 4 1 5 2 6 3 7; u8 inside each 4-block:
-// 0 2 1 3.  One thread per (token, group).
+// x_ext[m, :] = fp16 activations of token m times 2^e_m (range_scale of the
+// largest |x| and |group sum| of the token) in the dequantizers' k order,
+// then per group g three bias columns (Xhi, Xlo, Xhi) of its scaled sum,
+// then zero padding; tscale[m] = 2^-e_m.  u4 order inside each 8-block:
+// 0 4 1 5 2 6 3 7; u8 inside each 4-block: 0 2 1 3.  One warp per token: a
+// pass for the scale, a pass (the loads hit the cache) for the conversion.
+__device__ __forceinline__ void load_group64(const uint16_t *src, float (&v)[64]) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 u = s4[i];
+        v[8 * i + 0] = bf16_lo(u.x);
+        v[8 * i + 1] = bf16_hi(u.x);
+        v[8 * i + 2] = bf16_lo(u.y);
+        v[8 * i + 3] = bf16_hi(u.y);
+        v[8 * i + 4] = bf16_lo(u.z);
+        v[8 * i + 5] = bf16_hi(u.z);
+        v[8 * i + 6] = bf16_lo(u.w);
+        v[8 * i + 7] = bf16_hi(u.w);
+    }
+}
+
 template <int BITS>
 __global__ void qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M,
                                    int K, int64_t kext, __half *xe,
-                                   unsigned int *status) {
+                                   float *tscale) {
     const int G = K / 64;
-    const int64_t items = M * G;
-    for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-         it < items; it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t m = it / G;
-        const int g = (int)(it - m * G);
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + m * K + g * 64);
-        __half *dst = xe + m * kext + g * 64;
-        float v[64];
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int64_t nw = (int64_t)gridDim.x * blockDim.x / 32;
+    for (int64_t m = w0; m < M; m += nw) {
+        const uint16_t *xr = x + m * K;
+        float t = 0.f;
+        for (int g = lane; g < G; g += 32) {
+            float v[64];
+            load_group64(xr + g * 64, v);
+            float X = 0.f, mx = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 u = src[i];
-            v[8 * i + 0] = bf16_lo(u.x);
-            v[8 * i + 1] = bf16_hi(u.x);
-            v[8 * i + 2] = bf16_lo(u.y);
-            v[8 * i + 3] = bf16_hi(u.y);
-            v[8 * i + 4] = bf16_lo(u.z);
-            v[8 * i + 5] = bf16_hi(u.z);
-            v[8 * i + 6] = bf16_lo(u.w);
-            v[8 * i + 7] = bf16_hi(u.w);
-        }
-        float X = 0.f;
-        bool over = false;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            X += v[i];
-            over |= fabsf(v[i]) > 65504.f;
-        }
-        uint32_t o[32];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const float *vb = v + 8 * b;
-            if constexpr (BITS == 4) {
-                o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0], vb[4]));
-                o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1], vb[5]));
-                o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[2], vb[6]));
-                o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[3], vb[7]));
-            } else {
-                o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0], vb[2]));
-                o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1], vb[3]));
-                o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[4], vb[6]));
-                o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[5], vb[7]));
+            for (int i = 0; i < 64; ++i) {
+                X += v[i];
+                mx = fmaxf(mx, fabsf(v[i]));
             }
+            t = fmaxf(t, fmaxf(mx, fabsf(X)));
         }
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        const __half xh = __float2half_rn(X);
-        const __half xl = __float2half_rn(X - __half2float(xh));
-        __half *bc = xe + m * kext + K + 3 * g;
-        bc[0] = xh;
-        bc[1] = xl;
-        bc[2] = xh;
-        over |= fabsf(X) > 65504.f;
-        if (over) atomicOr(status, kStFp16Range);
-        if (g == 0)
-            for (int64_t c = K + 3 * G; c < kext; ++c)
-                xe[m * kext + c] = __float2half_rn(0.f);
+        for (int o = 16; o > 0; o >>= 1)
+            t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+        float up, down;
+        range_scale(t, up, down);
+        if (lane == 0) tscale[m] = down;
+        __half *row = xe + m * kext;
+        for (int g = lane; g < G; g += 32) {
+            float v[64];
+            load_group64(xr + g * 64, v);
+            float X = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) X += v[i];
+            uint32_t o[32];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const float *vb = v + 8 * b;
+                if constexpr (BITS == 4) {
+                    o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0] * up, vb[4] * up));
+                    o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1] * up, vb[5] * up));
+                    o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[2] * up, vb[6] * up));
+                    o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[3] * up, vb[7] * up));
+                } else {
+                    o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0] * up, vb[2] * up));
+                    o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1] * up, vb[3] * up));
+                    o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[4] * up, vb[6] * up));
+                    o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[5] * up, vb[7] * up));
+                }
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(row + g * 64);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            const float Xs = X * up;
+            const __half xh = __float2half_rn(Xs);
+            const __half xl = __float2half_rn(Xs - __half2float(xh));
+            __half *bc = row + K + 3 * g;
+            bc[0] = xh;
+            bc[1] = xl;
+            bc[2] = xh;
+        }
+        for (int64_t c = K + 3 * G + lane; c < kext; c += 32)
+            row[c] = __float2half_rn(0.f);
     }
 }
 
@@ -272,6 +317,7 @@ struct QmmParams {
     int rope_hd;
     int64_t rope_end;
     const float2 *rope_cs;
+    const float *tscale;  // [M]: 2^-e_m of each token (pre-pass)
     unsigned int *status;
 };
 
@@ -337,10 +383,10 @@ __device__ __forceinline__ void dequant_row(const uint32_t *w, float s,
 
 // Bias block (K block kb >= G) for row n: column pair c holds bias columns
 // 2c, 2c+1 of the block; bias column j belongs to group j/3 (hi, hi, lo of
-// b' = b + 8s or b + 136s).
+// 2^f_n b', b' = b + 8s or b + 136s; up = 2^f_n).
 template <int BITS>
 __device__ __forceinline__ void bias_row(const QmmParams &p, int64_t n, int kb,
-                                         uint32_t *a, unsigned &flags) {
+                                         float up, uint32_t *a) {
     const int base = (kb - p.G) * 64;
     const float k8 = BITS == 4 ? 8.f : 136.f;
 #pragma unroll
@@ -354,10 +400,9 @@ __device__ __forceinline__ void bias_row(const QmmParams &p, int64_t n, int kb,
             if (n >= 0 && g < p.G) {
                 const float s = bf16_bits_to_f32(ld_u16(p.sc + n * p.G + g));
                 const float b = bf16_bits_to_f32(ld_u16(p.bi + n * p.G + g));
-                const float bp = fmaf(k8, s, b);
+                const float bp = fmaf(k8, s, b) * up;
                 const float hi = __half2float(__float2half_rn(bp));
                 val = which < 2 ? hi : bp - hi;
-                if (fabsf(bp) > 65504.f) flags |= kStFp16Range;
             }
             e[hh] = val;
         }
@@ -380,6 +425,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     __shared__ uint64_t sfull[SS], sempty[SS], afull[SA], aempty[SA], dfull;
     __shared__ uint32_t s_tmem;
     __shared__ int s_xn, s_wn, s_sn;  // TMA loads issued per ring
+    __shared__ float s_rowt[4][kQmmRows];  // per phase: part of a row's range
+    __shared__ float s_tok[NT];            // the tile's tokens' 2^-e_m
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.y * NT;
@@ -508,7 +555,39 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             n = r0 + r < p.N ? r0 + r : -1;
         }
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        unsigned flags = 0;
+        // The row's range (see the file comment): the largest |s| * 8 (u4)
+        // or 128 (u8) and |b'| over its groups, the four phases' threads of
+        // a row taking every fourth 8-group piece of its scales and biases.
+        {
+            const float qf = BITS == 4 ? 8.f : 128.f;
+            const float k8 = BITS == 4 ? 8.f : 136.f;
+            float t = 0.f;
+            if (n >= 0)
+                for (int c = ph; c < G / 8; c += 4) {
+                    const uint4 sv = reinterpret_cast<const uint4 *>(p.sc + n * G)[c];
+                    const uint4 bv = reinterpret_cast<const uint4 *>(p.bi + n * G)[c];
+                    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+                    const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float s0 = bf16_lo(sw[i]), s1 = bf16_hi(sw[i]);
+                        const float b0 = bf16_lo(bw[i]), b1 = bf16_hi(bw[i]);
+                        t = fmaxf(t, fmaxf(fabsf(s0) * qf, fabsf(s1) * qf));
+                        t = fmaxf(t, fmaxf(fabsf(fmaf(k8, s0, b0)),
+                                           fabsf(fmaf(k8, s1, b1))));
+                    }
+                }
+            s_rowt[ph][r] = t;
+            // and the tile's token factors
+            const int tix = threadIdx.x - 2 * kWarp;
+            for (int i = tix; i < NT; i += kQmmDeqWarps * kWarp)
+                s_tok[i] = m0 + i < p.M ? p.tscale[m0 + i] : 0.f;
+        }
+        asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
+        float rup, rdown;  // 2^f_n, 2^-f_n
+        range_scale(fmaxf(fmaxf(s_rowt[0][r], s_rowt[1][r]),
+                          fmaxf(s_rowt[2][r], s_rowt[3][r])),
+                    rup, rdown);
         for (int kb = ph; kb < p.nkb; kb += 4) {
             const int sa = kb % SA;
             uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
@@ -543,19 +622,16 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 }
                 const uint16_t *st = reinterpret_cast<const uint16_t *>(
                     smem + L::SOFF + (size_t)ss * L::SBYTES);
-                const float s = bf16_bits_to_f32(st[r * 8 + (kb & 7)]);
+                const float s = bf16_bits_to_f32(st[r * 8 + (kb & 7)]) * rup;
                 // the codes and scale of this block are in registers
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&wempty[sw]);
                     if ((kb & 7) == 4 + ph || kb == G - 1) mbar_arrive(&sempty[ss]);
                 }
-                if (n >= 0 &&
-                    (!(fabsf(s) <= 511.f) || (s != 0.f && fabsf(s) < 6.103515625e-05f)))
-                    flags |= kStFp16Range;
                 dequant_row<BITS>(w, s, hi, lo);
             } else {
-                bias_row<BITS>(p, n, kb, hi, flags);
+                bias_row<BITS>(p, n, kb, rup, hi);
                 if constexpr (BITS == 8)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) lo[i] = 0u;
@@ -573,9 +649,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[sa]);
         }
-        if (flags) atomicOr(p.status, flags);
-
         // -------------------------------------------- epilogue
+        // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
         const bool done = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
         if (done) tc_fence_after();
         const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
@@ -589,7 +664,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     float g[32];
                     tc_ld32(tmem_d + lane_off + c0, g);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) gbuf[r * GS + c0 + j] = g[j];
+                    for (int j = 0; j < 32; ++j)
+                        gbuf[r * GS + c0 + j] = g[j] * rdown * s_tok[c0 + j];
                 }
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
@@ -604,8 +680,9 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                         const int64_t m = m0 + c0 + j;
                         if (m >= p.M) break;
                         const float g = gbuf[pr * GS + c0 + j];
+                        const float uv = u[j] * rdown * s_tok[c0 + j];
                         p.y[m * p.I + i] =
-                            f32_to_bf16_bits(g / (1.0f + __expf(-g)) * u[j]);
+                            f32_to_bf16_bits(g / (1.0f + __expf(-g)) * uv);
                     }
                 }
             }
@@ -630,7 +707,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     float d[32];
                     tc_ld32(tmem_d + lane_off + c0, d);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) buf[r * GS + c0 + j] = d[j] + bias;
+                    for (int j = 0; j < 32; ++j)
+                        buf[r * GS + c0 + j] = d[j] * rdown * s_tok[c0 + j] + bias;
                 }
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
@@ -676,13 +754,14 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 for (int j = 0; j < 32; ++j) {
                     const int64_t m = m0 + c0 + j;
                     if (m >= p.M) break;
+                    const float dv = d[j] * rdown * s_tok[c0 + j];
                     if (p.mode == 0) {
-                        p.y[m * p.N + n] = f32_to_bf16_bits(d[j]);
+                        p.y[m * p.N + n] = f32_to_bf16_bits(dv);
                     } else {
                         const int64_t jj = n - p.sec_start[sidx];
                         const int64_t size =
                             p.sec_start[sidx + 1] - p.sec_start[sidx];
-                        float val = d[j];
+                        float val = dv;
                         if (p.sec_bias[sidx])
                             val += bf16_bits_to_f32(p.sec_bias[sidx][jj]);
                         p.sec_out[sidx][m * size + jj] = f32_to_bf16_bits(val);
@@ -756,17 +835,17 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     const int64_t kext = qmm_kext(K);
     unsigned int *status = reinterpret_cast<unsigned int *>(ws);
     __half *xe = reinterpret_cast<__half *>(ws + kStatusBytes);
+    float *tscale = reinterpret_cast<float *>(ws + kStatusBytes + qmm_xe_bytes(M, K));
 
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned int), st);
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm status reset: %s",
                          cudaGetErrorString(e));
-    const int64_t items = M * G;
-    const int pthreads = 128;
-    int64_t pblocks = (items + pthreads - 1) / pthreads;
+    const int pthreads = 128;  // a warp per token
+    int64_t pblocks = (M * 32 + pthreads - 1) / pthreads;
     if (pblocks > (int64_t)num_sms() * 16) pblocks = (int64_t)num_sms() * 16;
     qmm_prepass_kernel<BITS><<<(unsigned)pblocks, pthreads, 0, st>>>(
-        a.x, M, (int)K, kext, xe, status);
+        a.x, M, (int)K, kext, xe, tscale);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm pre-pass: %s", cudaGetErrorString(e));
@@ -807,6 +886,7 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     p.rope_hd = a.rope_hd;
     p.rope_end = a.rope_end;
     p.rope_cs = a.rope_cs;
+    p.tscale = tscale;
     p.status = status;
 
     auto kern = qmm_tc_kernel<BITS, NT>;

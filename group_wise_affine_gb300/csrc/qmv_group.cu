@@ -17,6 +17,14 @@
 //    the epilogue adds a row's slots in slice order (deterministic).
 // Per 64 codes this costs one or two scale applications and one reduction
 // share, against two of each in the 16-byte-piece layout.
+//  * activations the int16 encoding would round by more than 2^-16 of a
+//    group's magnitude (common.cuh, "marked groups") switch the whole CTA
+//    (every CTA encodes the same activations) to a copy of the loop that
+//    adds an int8 residual plane per chunk: about 40% more instructions per
+//    row, taken only for such inputs.
+//  * plain projections run as one-section calls of the sections kernel, so
+//    a decoder layer's calls share two kernels' code in the SM's
+//    instruction cache instead of three.
 // Sources: "Sanctum-MLX" (decode is a bandwidth-bound quantized GEMV); the
 // packed format of "saragossa", "Quantization formats"; the fused QKV and
 // gate+up epilogues of "The Cathedral Doubled Itself", "The two fusions".
@@ -27,6 +35,7 @@ namespace gwa {
 
 static __device__ unsigned int g_group_timeouts;
 
+// Modes as the host passes them; a plain projection runs as one section.
 enum GroupMode { kGPlain = 0, kGSections = 1, kGGateUp = 2, kGRope = 3 };
 
 // QKV with the rotary embedding (kGRope): a unit is the pair of rows
@@ -53,9 +62,12 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
 
 // The consumer side of the stage loop (see qmv_group_kernel), for a lane
 // whose image is ready.  EX (two-plane path, common.cuh "marked groups"):
-// the lane of a marked chunk forms its int8 residual plane in registers
-// from the raw activations, every lane (zero planes for unmarked chunks)
-// takes both planes' dots in one pass over the code bytes.
+// once every lane holds its int16 pairs in registers, the image's pairs are
+// dead, and the lanes of the first row group write each chunk's int8
+// residual plane (zeros unless marked) over them; every row then takes both
+// planes' dots in one pass over its code bytes.  The kernel has no local memory and no
+// calls: a stack frame costs the SM the shared-memory carveout that lets
+// two of these CTAs share it.
 template <int BITS, int MT, int MODE, int RPH, int GS, bool EX>
 __device__ __forceinline__ void group_loop(
     const uint16_t *x, int K, int G, unsigned char *smem, uint64_t *full,
@@ -86,16 +98,14 @@ __device__ __forceinline__ void group_loop(
     const int rot = chunk_rot<BITS>(gg);
     load_group_rows<MT, SPLIT, EX ? kMarkDefer : kMarkRaw>(
         xenc, MT, nchunk, 0, gg, active, gx, image_shift<BITS>(gg));
+    const uint4 *const plane = reinterpret_cast<const uint4 *>(xenc) + gg;  // row 0
+    static_assert(!EX || MT == 1, "two-plane path: one token");
     if constexpr (EX) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (gx.mk[m])
-                group_lo_plane<BITS>(x + (int64_t)m * K + gg * 64, gx.f[m], rot,
-                                     gx.lo[m]);
-            else
-#pragma unroll
-                for (int i = 0; i < 16; ++i) gx.lo[m][i] = 0u;
-        }
+        asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
+        if (hg == 0 && in_group)
+            group_lo_store<BITS>(gx.mk[0], x + gg * 64, gx.f[0], rot,
+                                 reinterpret_cast<uint4 *>(xenc) + gg, nchunk);
+        asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
     }
     uint32_t offw[RPH], offs[RPH];
     const uint32_t sb_delta = rows_stage * (uint32_t)G * 2u;
@@ -148,10 +158,10 @@ __device__ __forceinline__ void group_loop(
                     *reinterpret_cast<const uint32_t *>(base + os);
                 const uint32_t b2 =
                     *reinterpret_cast<const uint32_t *>(base + os + sb_delta);
-                int dl[MT], dh[MT], ll[MT], lh[MT];
+                int dl[MT], dh[MT], ll = 0, lh = 0;
                 group_dot_split<BITS, MT>(w, gx, rot, dl, dh);
                 if constexpr (EX)
-                    group_dot_lo_split<BITS, MT>(w, gx, rot, ll, lh);
+                    group_dot_lo_split<BITS>(w, plane, nchunk, rot, ll, lh);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     const float fl = bf16_lo(s2) * gx.f[m];
@@ -159,8 +169,8 @@ __device__ __forceinline__ void group_loop(
                     float t = fmaf(bf16_lo(b2), gx.xs[m],
                                    bf16_hi(b2) * gx.xs2[m]);
                     if constexpr (EX)  // the residual plane, 2^-7 of the scale
-                        t = fmaf(fl * 0.0078125f, (float)ll[m],
-                                 fmaf(fh * 0.0078125f, (float)lh[m], t));
+                        t = fmaf(fl * 0.0078125f, (float)ll,
+                                 fmaf(fh * 0.0078125f, (float)lh, t));
                     v[j * MT + m] =
                         fmaf(fl, (float)dl[m], fmaf(fh, (float)dh[m], t));
                 }
@@ -169,9 +179,9 @@ __device__ __forceinline__ void group_loop(
                     *reinterpret_cast<const uint16_t *>(base + os));
                 const float bv = bf16_bits_to_f32(
                     *reinterpret_cast<const uint16_t *>(base + os + sb_delta));
-                int d[MT], dlo[MT];
+                int d[MT], dlo = 0;
                 if constexpr (EX)
-                    group_dot2<BITS, MT>(w, gx, d, dlo);
+                    group_dot2<BITS, MT>(w, gx, plane, nchunk, d, dlo);
                 else
                     group_dot<BITS, MT>(w, gx, d);
 #pragma unroll
@@ -179,7 +189,7 @@ __device__ __forceinline__ void group_loop(
                     const float sf = sv * gx.f[m];
                     float t = bv * gx.xs[m];
                     if constexpr (EX)  // the residual plane, 2^-7 of the scale
-                        t = fmaf(sf * 0.0078125f, (float)dlo[m], t);
+                        t = fmaf(sf * 0.0078125f, (float)dlo, t);
                     v[j * MT + m] = fmaf(sf, (float)d[m], t);
                 }
             }
@@ -196,20 +206,6 @@ __device__ __forceinline__ void group_loop(
             ph ^= 1;
         }
     }
-}
-
-// The marked instance of group_loop, out of line.
-template <int BITS, int MT, int MODE, int RPH, int GS>
-__device__ __noinline__ void group_loop_marked(
-    const uint16_t *x, int K, int G, unsigned char *smem, uint64_t *full,
-    uint64_t *empty, float *red, int *s_consumed, int stages, int nst, int nu,
-    int ups, int slices, uint32_t stage_bytes, uint32_t codes_off,
-    uint32_t rows_stage, uint32_t rowbytes, int ncons, int tid,
-    uint32_t xenc_off) {
-    group_loop<BITS, MT, MODE, RPH, GS, true>(
-        x, K, G, smem, full, empty, red, s_consumed, stages, nst, nu, ups,
-        slices, stage_bytes, codes_off, rows_stage, rowbytes, ncons, tid,
-        xenc_off);
 }
 
 // A stage holds UPS = RS * UPT units (rows, or gate/up row pairs).  Consumer
@@ -344,11 +340,11 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
         // the consumer warps only (the producer is in its copy loop)
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
         // Marked chunks (common.cuh, "marked groups"): if any consumer lane
-        // holds one, the CTA runs the two-plane loop, kept out of line so
-        // that the plain loop below keeps its code and registers.
+        // holds one, the CTA runs the two-plane loop (every CTA encodes the
+        // same activations, so all decide alike).
         const bool mk = active && chunk_marked<MT, SPLIT>(xenc, nchunk, gg);
         if (bar_red_or(1, ncons, mk))
-            group_loop_marked<BITS, MT, MODE, RPH, GS>(
+            group_loop<BITS, MT, MODE, RPH, GS, true>(
                 p.x, p.K, p.G, smem, full, empty, red, &s_consumed, stages, nst,
                 nu, ups, slices, stage_bytes, codes_off, rows_stage, rowbytes,
                 ncons, tid, xenc_off);
@@ -403,9 +399,6 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
             uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
             o[0] = f32_to_bf16_bits(a);
             o[half] = f32_to_bf16_bits(b);
-        } else if constexpr (MODE == kGPlain) {
-            p.y[(int64_t)m * p.N + n] =
-                f32_to_bf16_bits(slot_total(red, lu * MT + m, slices));
         } else {
             int s = 0;
             while (s + 1 < p.nsec && n >= p.sec_start[s + 1]) ++s;
@@ -498,17 +491,26 @@ static cudaError_t launch_group_gs(int mode, const DenseParams &p,
     if (mode == kGRope)
         return p.bits == 4 ? launch_group_r<4, 1, kGRope, 2, GS>(p, st, used)
                            : launch_group_r<8, 1, kGRope, 2, GS>(p, st, used);
-    if (p.bits == 4) {
-        if (mode == kGPlain)
-            return launch_group_r<4, 1, kGPlain, 2, GS>(p, st, used);
-        if (mode == kGSections)
-            return launch_group_r<4, 1, kGSections, 2, GS>(p, st, used);
-        return launch_group_r<4, 1, kGGateUp, 2, GS>(p, st, used);
+    // A plain projection runs as one section: the same kernel as the fused
+    // QKV projection, so that a layer's calls share their code (the SM's
+    // instruction cache holds two of these kernels, not three).
+    DenseParams q = p;
+    if (mode == kGPlain) {
+        q.nsec = 1;
+        q.sec_start[0] = 0;
+        q.sec_start[1] = p.N;
+        q.sec_out[0] = p.y;
+        q.sec_bias[0] = nullptr;
+        mode = kGSections;
     }
-    if (mode == kGPlain) return launch_group_r<8, 1, kGPlain, 2, GS>(p, st, used);
+    if (p.bits == 4) {
+        if (mode == kGSections)
+            return launch_group_r<4, 1, kGSections, 2, GS>(q, st, used);
+        return launch_group_r<4, 1, kGGateUp, 2, GS>(q, st, used);
+    }
     if (mode == kGSections)
-        return launch_group_r<8, 1, kGSections, 2, GS>(p, st, used);
-    return launch_group_r<8, 1, kGGateUp, 2, GS>(p, st, used);
+        return launch_group_r<8, 1, kGSections, 2, GS>(q, st, used);
+    return launch_group_r<8, 1, kGGateUp, 2, GS>(q, st, used);
 }
 
 // Launches the chunk-per-lane kernel when the shape allows it (one token,

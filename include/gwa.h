@@ -20,7 +20,9 @@
  *     pointers (section outputs/biases) and section sizes are HOST arrays.
  *     The library allocates nothing, keeps no pointer after the call returns,
  *     and never synchronizes: work is enqueued on `stream` (a cudaStream_t;
- *     NULL = the legacy default stream) and the call returns at once.
+ *     NULL = the legacy default stream) and the call returns at once.  (One
+ *     exception: gwa_qmv_affine_noalloc runs in a fixed scratch buffer that
+ *     the library holds in device memory for the life of the process.)
  *   - bf16 values are passed as their 16-bit patterns (uint16_t).
  *   - All matrices are row-major and contiguous.  x is [M, K].
  *   - Wq, x and the workspace must be 16-byte aligned; scales, biases and
@@ -32,8 +34,11 @@
  *     workspace must not overlap on the GPU.  It runs the tensor-core
  *     (tcgen05) kernels when K is a multiple of 512 and Wq, scales and
  *     biases are 16-byte aligned (the workspace's first word then holds the
- *     call's status: 1 = a pipeline wait ran out, 2 = a value outside fp16's
- *     range), and otherwise the decode kernels in passes of up to 8 tokens.
+ *     call's status: 0, or 1 when a pipeline wait ran out, which
+ *     gwa_pipeline_status also counts), and otherwise the decode kernels in
+ *     passes of up to 8 tokens.  Every finite bf16 input is in range: each
+ *     token and each weight row is scaled by a power of two before the
+ *     tensor cores' fp16 operands are formed.
  *   - Return value: GWA_OK or an error code; nothing aborts, traps or exits.
  *     On error nothing was enqueued and gwa_last_error() (thread-local) holds
  *     one line of text.  Errors raised by the GPU while the work runs surface
@@ -162,14 +167,21 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
  *   workspace.  M <= 8 needs no scratch; for M > 8 the problem must fit:
  *   gwa_workspace_bytes(M, K) <= GWA_NOALLOC_SCRATCH_BYTES, otherwise the
  *   call returns GWA_ERR_WORKSPACE and enqueues nothing.
- *   The first call on each device looks up the scratch's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   Each call looks up the scratch's device address on the current device
+ *   (cudaGetSymbolAddress) and keeps nothing between calls.
  *   Every call on a device shares the one scratch buffer and leaves its
  *   contents behind (the status word is cleared at the start of each call):
  *   calls that can overlap on the GPU -- on different streams, or from
  *   different host threads -- race on it and must be serialized by the
- *   caller. */
+ *   caller.
+ *   Status: the only condition the scratch's status word can record is a
+ *   pipeline wait that ran out, and every such wait is also counted on the
+ *   device, so gwa_pipeline_status reports it; the caller needs no access to
+ *   the scratch.
+ *   Size: gwa_workspace_bytes(M, K) is about 2.1 K bytes per token, so the
+ *   scratch fits M <= 1925 at K = 2048, M <= 779 at K = 5120 and M <= 288
+ *   at K = 13824 (a down projection); larger problems need gwa_qmv_affine
+ *   with a workspace. */
 #define GWA_NOALLOC_SCRATCH_BYTES (8u << 20)
 int gwa_qmv_affine_noalloc(const uint16_t *x, int64_t M, gwa_qweight w,
                            uint16_t *y, void *stream);

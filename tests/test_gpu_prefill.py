@@ -119,14 +119,95 @@ def test_missing_workspace_is_an_error_not_a_fault():
     torch.cuda.synchronize()
 
 
-def test_fp16_range_is_flagged():
-    # an activation beyond fp16's range sets the status bit; nothing faults
-    # (K = 512: the tensor-core kernel, which writes the status word)
-    w = dev_qweight(synth.qweight(1910, 128, 512, 4))
-    xh = synth.activations(1911, 32, 512)
-    xh[3, 5] = synth.bf16_bits(np.array([1.0e6], np.float32))[0]
-    ws = gwa.make_workspace(32, 512)
-    gwa.qmv_affine(dev_bf16(xh), w, workspace=ws)
+def scaled_weight(seed, N, K, bits, scale, bias_abs):
+    """Codes as drawn; bf16 scales scale * U(1, 2), biases +-bias_abs * U(1, 2)
+    (or the recipe's -8 scale + N(0, 1e-3) scaled with the scale when
+    bias_abs is None)."""
+    w = synth.qweight(seed, N, K, bits)
+    rng = synth.rng_for(seed + 1)
+    G = K // 64
+    s = synth.bf16_bits((scale * rng.uniform(1, 2, (N, G))).astype(np.float32))
+    if bias_abs is None:
+        b = synth.bf16_bits((-8.0 * synth.bf16_values(s)
+                             + scale * 0.1 * rng.standard_normal((N, G))).astype(np.float32))
+    else:
+        sign = np.where(rng.random((N, G)) < 0.5, -1.0, 1.0)
+        b = synth.bf16_bits((sign * bias_abs * rng.uniform(1, 2, (N, G))).astype(np.float32))
+    return synth.QWeight(w.wq, s, b, N, K, bits)
+
+
+def assert_close_acc(got, ref, x, w, rows, what=""):
+    """The output bar plus the fp32 accumulation's own rounding.
+
+    Operands reach the tensor cores exactly, but the products are summed in
+    fp32: each of the MMA's K steps (kext/16, twice for u8's two code halves)
+    rounds at most 2^-23 of the magnitude of what it adds up.  The terms
+    summed are x * s(q - c) per input and b' X per group (b' = b + c s, c = 8
+    or 136, X a group sum), all bounded by |x| (|b| + 2 c |s|) per input.
+    Where an output cancels to far below those terms (a large common weight
+    offset, as with u8 biases of -8 s), that rounding is above 1e-2 |y|."""
+    K = w.K
+    G = K // 64
+    c = 8.0 if w.bits == 4 else 136.0
+    s = np.abs(synth.bf16_values(w.scales[rows]).astype(np.float64))
+    b = np.abs(synth.bf16_values(w.biases[rows]).astype(np.float64))
+    per_group = b + 2.0 * c * s                       # [rows, G]
+    per_input = np.repeat(per_group, 64, axis=1)      # [rows, K]
+    xa = np.abs(synth.bf16_values(x).astype(np.float64))
+    mag = xa @ per_input.T
+    kext = K + ((3 * G + 63) // 64) * 64
+    steps = (kext // 16) * (2 if w.bits == 8 else 1)
+    bar = TOL * np.maximum(1.0, np.abs(ref)) + steps * 2.0**-23 * mag
+    err = np.abs(got - ref)
+    worst = float((err / bar).max())
+    assert worst <= 1.0, f"{what}: max |err| {err.max():.3g}, worst err/bar {worst:.3g}"
+
+
+# Values far outside fp16's range (2^-14 .. 65504): every token and weight
+# row is scaled by a power of two before the fp16 conversion, so these are as
+# exact as ordinary ones.  K = 1024: the tensor-core kernel.
+@pytest.mark.parametrize("M", [16, 512])
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("scale,bias_abs,xmul", [
+    (1e-6, None, 1.0),     # scales below fp16's normal range
+    (1e3, None, 1.0),      # s * (q - 8) beyond 65504
+    (0.01, 1e5, 1.0),      # |bias| far beyond 65504
+    (0.01, None, 1e6),     # |x| = 1e6 scale
+    (1e-6, 1e-3, 1e-30),   # tiny everything
+    (1e3, 1e5, 1e6),       # large everything
+])
+def test_qmm_exact_outside_fp16_range(M, bits, scale, bias_abs, xmul):
+    N, K = 256, 1024
+    w = scaled_weight(1910 + bits, N, K, bits, scale, bias_abs)
+    xv = synth.bf16_values(synth.activations(1911 + M, M, K)).astype(np.float32)
+    x = synth.bf16_bits(xv * np.float32(xmul))
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
     torch.cuda.synchronize()
-    assert status_of(ws) & 2
+    assert status_of(ws) == 0
+    sample = list(range(0, N, 7)) + [N - 1]
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits, rows=sample)
+    assert_close_acc(bf16_to_f64(y)[:, sample], ref, x, w, sample,
+                     f"M={M} u{bits} scale={scale} bias={bias_abs} x*{xmul}")
+
+
+def test_qmm_exact_outliers_and_mixed_rows():
+    # one token with a 1e6 outlier, rows whose scales differ by 1e9
+    M, N, K = 32, 256, 2048
+    w = synth.qweight(1930, N, K, 4)
+    s = synth.bf16_values(w.scales).copy()
+    s[::2] *= np.float32(1e-5)
+    s[1::4] *= np.float32(1e4)
+    sb = synth.bf16_bits(s)
+    bb = synth.bf16_bits(-8.0 * synth.bf16_values(sb))
+    w = synth.QWeight(w.wq, sb, bb, N, K, 4)
+    x = synth.activations(1931, M, K)
+    x[3, 5] = synth.bf16_bits(np.array([1.0e6], np.float32))[0]
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
+    torch.cuda.synchronize()
+    assert status_of(ws) == 0
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, 4)
+    assert_close_acc(bf16_to_f64(y), ref, x, w, list(range(N)),
+                     "outliers and mixed rows")
     assert gwa.pipeline_status() == 0
