@@ -51,6 +51,11 @@ def parse():
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--inputs", default="normal", choices=["chain", "normal"],
+                    help="normal: every projection reads its own fixed "
+                         "N(0,1) activations (the workload's x ~ N(0,1)); "
+                         "chain: each projection reads the previous one's "
+                         "output (q -> o -> gate+up -> down)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the secondary workloads (M=4, M=512, MoE)")
@@ -93,6 +98,9 @@ def workload_config(args) -> dict:
               f"{sum(layer_bytes(args.bits, args.tokens).values()) * args.layers / 1e9:.2f}"
               " GB of distinct weights (L2 is 129 MB)",
         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single",
+        "inputs": ("chained: o reads q, gate+up reads o, down reads h = "
+                   "SiLU(gate) * up" if args.inputs == "chain"
+                   else "each projection reads fixed N(0,1) activations"),
     }
 
 
@@ -236,6 +244,15 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
             h=torch.empty((M, INTER), dtype=torch.bfloat16, device=dev),
             y=torch.empty((M, HIDDEN), dtype=torch.bfloat16, device=dev)))
     ws = gwa.make_workspace(M, INTER, dev)   # None at decode sizes
+    fixed = None
+    if args.inputs == "normal":
+        fixed = {k: torch.randn((M, n), generator=g, device=dev).to(torch.bfloat16)
+                 for k, n in (("o", QOUT), ("gate_up", HIDDEN), ("down", INTER))}
+
+    def src(kind, b):
+        if fixed is not None:
+            return fixed[kind]
+        return {"o": b["q"], "gate_up": b["o"], "down": b["h"]}[kind]
 
     def call(kind, l, stream=None):
         w, b = W[l], bufs[l]
@@ -244,13 +261,13 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
                                    outs=[b["q"], b["k"], b["v"]],
                                    workspace=ws, stream=stream)
         elif kind == "o":
-            gwa.qmv_affine(b["q"], w["o"], y=b["o"], workspace=ws,
+            gwa.qmv_affine(src("o", b), w["o"], y=b["o"], workspace=ws,
                            stream=stream)
         elif kind == "gate_up":
-            gwa.qmv_gate_up_silu(b["o"], w["gate_up"], h=b["h"], workspace=ws,
-                                 stream=stream)
+            gwa.qmv_gate_up_silu(src("gate_up", b), w["gate_up"], h=b["h"],
+                                 workspace=ws, stream=stream)
         else:
-            gwa.qmv_affine(b["h"], w["down"], y=b["y"], workspace=ws,
+            gwa.qmv_affine(src("down", b), w["down"], y=b["y"], workspace=ws,
                            stream=stream)
 
     kinds = ["qkv", "o", "gate_up", "down"]
@@ -340,6 +357,10 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     e2e_ms = e0.elapsed_time(e1) / KE
     extras = {}
     if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
+        # chained activations: down reads h = SiLU(gate) * up, whose spread
+        # marks most of its groups (the exact two-plane path)
+        extras["stack_M1_chained"] = run_stack_extra(W, 1, dev, 50, 3, "chain")
+        extras["stack_M2"] = run_stack_extra(W, 2, dev, 50, 3)
         extras["stack_M4"] = run_stack_extra(W, 4, dev, 50, 3)
         extras["stack_M8"] = run_stack_extra(W, 8, dev, 30, 3)
         extras["qkv_rope"] = run_rope_extra(W, dev, 20, 3)
@@ -410,8 +431,9 @@ def stack_weights(bits: int, L: int, dev):
     return W
 
 
-def run_stack_extra(W, M, dev, steps, warmup):
-    """The same 48-layer stack (same weights) at M tokens per call."""
+def run_stack_extra(W, M, dev, steps, warmup, inputs="normal"):
+    """The same 48-layer stack (same weights) at M tokens per call; inputs
+    as the --inputs option."""
     import torch
     import group_wise_affine_gb300 as gwa
     L = len(W)
@@ -422,6 +444,15 @@ def run_stack_extra(W, M, dev, steps, warmup):
     bufs = [dict(q=mk(QOUT), k=mk(KVOUT), v=mk(KVOUT), o=mk(HIDDEN),
                  h=mk(INTER), y=mk(HIDDEN)) for _ in range(L)]
     ws = gwa.make_workspace(M, INTER, dev)
+    fixed = None
+    if inputs == "normal":
+        fixed = {k: torch.randn((M, n), generator=g, device=dev).to(torch.bfloat16)
+                 for k, n in (("o", QOUT), ("gate_up", HIDDEN), ("down", INTER))}
+
+    def src(kind, b):
+        if fixed is not None:
+            return fixed[kind]
+        return {"o": b["q"], "gate_up": b["o"], "down": b["h"]}[kind]
 
     def call(kind, l):
         w, b = W[l], bufs[l]
@@ -429,11 +460,12 @@ def run_stack_extra(W, M, dev, steps, warmup):
             gwa.qmv_fused_sections(x, w["qkv"], (QOUT, KVOUT, KVOUT),
                                    outs=[b["q"], b["k"], b["v"]], workspace=ws)
         elif kind == "o":
-            gwa.qmv_affine(b["q"], w["o"], y=b["o"], workspace=ws)
+            gwa.qmv_affine(src("o", b), w["o"], y=b["o"], workspace=ws)
         elif kind == "gate_up":
-            gwa.qmv_gate_up_silu(b["o"], w["gate_up"], h=b["h"], workspace=ws)
+            gwa.qmv_gate_up_silu(src("gate_up", b), w["gate_up"], h=b["h"],
+                                 workspace=ws)
         else:
-            gwa.qmv_affine(b["h"], w["down"], y=b["y"], workspace=ws)
+            gwa.qmv_affine(src("down", b), w["down"], y=b["y"], workspace=ws)
 
     kinds = ["qkv", "o", "gate_up", "down"]
     for k in kinds:
@@ -443,7 +475,7 @@ def run_stack_extra(W, M, dev, steps, warmup):
     total, per = time_graphs(graphs, steps, warmup)
     ms = total / steps
     shapes = {n: (r, k) for n, r, k in layer_shapes()}
-    out = {"M": M, "ms_per_step": round(ms, 4),
+    out = {"M": M, "inputs": inputs, "ms_per_step": round(ms, 4),
            "steps_per_s": round(1e3 / ms, 2), "kernels": {}}
     flops = 0
     bytes_ = 0

@@ -315,21 +315,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Named barrier `id` over `nthreads` threads (whole warps) that also ORs a
-// predicate across them.
-__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
-    int r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.s32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.s32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((int)v), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(count));

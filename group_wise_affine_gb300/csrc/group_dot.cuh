@@ -45,20 +45,50 @@ __device__ __forceinline__ uint32_t i16_pair_fast(float a, float b,
 // so that the lanes of a warp (consecutive chunks) read consecutive 16-byte
 // pieces:
 //   pairs[r][c][g] (uint4: pairs 4c..4c+3 of chunk g), then f[r][g],
-//   xs[r][g], for split images xs2[r][g], and for images with deferred
-//   marks (two-plane kernels) mq[r][g][4]: per quarter of the chunk
-//   R_q - 2^-16 A_q in fp16 (common.cuh, "marked groups"; the criterion is
-//   linear, so the chunk is marked when the four add up above zero).
+//   xs[r][g], and for split images xs2[r][g].  The two-plane path later
+//   writes each chunk's int8 residual plane over the first half of the
+//   pairs (group_plane_store), once every lane holds its pairs in
+//   registers.
 __host__ __device__ constexpr size_t ximg_bytes(int R, int G,
-                                                bool split = false,
-                                                bool marks = false) {
-    return (size_t)R * G * (8 * 16 + 8 + (split ? 4 : 0) + (marks ? 8 : 0));
+                                                bool split = false) {
+    return (size_t)R * G * (8 * 16 + 8 + (split ? 4 : 0));
+}
+
+// Bank-conflict-free reads of a row's group.  Lane g reads its group's
+// 16-byte code chunks starting at chunk rot(g), so the lanes whose groups
+// lie 128 bytes apart (4 apart for u4, 2 apart for u8) read different banks
+// in the same instruction.  Its activation pairs are loaded in the same
+// rotated order (image chunk shift), so the dot is unchanged.
+template <int BITS>
+__device__ __forceinline__ int chunk_rot(int g) {
+    return BITS == 4 ? (g >> 2) & 1 : (g >> 1) & 3;
+}
+template <int BITS>
+__device__ __forceinline__ int image_shift(int g) {
+    return (BITS == 4 ? 4 : 2) * chunk_rot<BITS>(g);
+}
+
+// Slot (16-byte piece of a chunk's residual plane) that holds quarter q's
+// entries in the two-plane path: the pieces follow the order in which
+// lds_group loads the chunk's codes (rotation rot = chunk_rot(g)), so
+// register piece v of the codes meets plane slots 2v, 2v + 1 (u4) or v (u8).
+template <int BITS>
+__device__ __forceinline__ int group_lo_slot(int q, int rot) {
+    return BITS == 4 ? 2 * (((q >> 1) - rot) & 1) + (q & 1) : (q - rot) & 3;
+}
+
+// Four bytes (the low byte of each word) packed into one word, a first.
+__device__ __forceinline__ uint32_t pack_bytes(uint32_t a, uint32_t b,
+                                               uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040),
+                       0x5410);
 }
 
 // How an encoder settles a chunk's mark: RAW agrees on it through shuffles
-// and stores a marked chunk's raw bf16 pairs (fp32 path); DEFER stores each
-// quarter's part of the criterion and leaves the int16 pairs (two-plane
-// path): no shuffle is added to the encode.
+// before forming the pairs and stores a marked chunk's raw bf16 pairs (fp32
+// path); DEFER always stores the int16 pairs and adds up the chunk's
+// criterion afterwards, off the pairs' path (two-plane path: a marked chunk
+// only sets the flag).
 enum MarkMode { kMarkRaw = 0, kMarkDefer = 1 };
 
 // Quarter `q` (16 inputs) of group g of image row r, from its 8 packed bf16
@@ -68,9 +98,10 @@ enum MarkMode { kMarkRaw = 0, kMarkDefer = 1 };
 // out 16x too large and exact, so f is stored as 2^E / 16.  Marks (common.cuh,
 // "marked groups"): with kMarkRaw a marked chunk sets *mkflag (when given)
 // to 1 and stores its raw bf16 pairs in the same order and f = -1/16 (u4)
-// or -1 (u8), the unit of the fp32 dot; with kMarkDefer every quarter
-// stores its part of the criterion (see ximg_bytes) and the pairs and f are
-// the usual ones.
+// or -1 (u8), the unit of the fp32 dot; with kMarkDefer the pairs and f are
+// always the usual ones and a marked chunk sets *mkflag.  The criterion is
+// linear in the quarters' residuals and magnitudes, so each quarter's part
+// R_q - 2^-16 A_q is formed alone and the four are added by two shuffles.
 template <int BITS, bool SPLIT = false, int MK = kMarkRaw>
 __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
                                                bool store, int r, int g, int q,
@@ -149,23 +180,13 @@ __device__ __forceinline__ void encode_quarter(const uint32_t (&u)[8],
             xsm[(size_t)r * G + g] = sum;
         }
         if (SPLIT && q == 2) xsm[(size_t)R * G + (size_t)r * G + g] = sum;
-        if constexpr (MK == kMarkDefer) {
-            __half *mq = reinterpret_cast<__half *>(xsm + (SPLIT ? 2 : 1) *
-                                                              (size_t)R * G);
-            mq[((size_t)r * G + g) * 4 + q] =
-                __float2half_rn(fmaf(ab * finv, -1.0f / 65536.0f, re));
-        }
     }
-
-}
-
-// Slot (16-byte piece of the chunk's pairs in the image) that holds quarter
-// q's residual plane in the two-plane path: the pieces follow the order in
-// which lds_group loads the chunk's codes (rotation rot = chunk_rot(g)), so
-// register piece v of the codes meets plane slots 2v, 2v + 1 (u4) or v (u8).
-template <int BITS>
-__device__ __forceinline__ int group_lo_slot(int q, int rot) {
-    return BITS == 4 ? 2 * (((q >> 1) - rot) & 1) + (q & 1) : (q - rot) & 3;
+    if constexpr (MK == kMarkDefer) {
+        float d = fmaf(ab * finv, -1.0f / 65536.0f, re);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        if (store && q == 0 && d > 0.f && mkflag) *mkflag = 1;
+    }
 }
 
 
@@ -215,38 +236,70 @@ __device__ __forceinline__ void encode_rows_shared(
     }
 }
 
-// Whether chunk g of an image with deferred marks (kMarkDefer) is marked,
-// in any of its R rows (common.cuh, "marked groups").
-template <int R, bool SPLIT>
-__device__ __forceinline__ bool chunk_marked(const unsigned char *img, int G,
-                                             int g) {
-    const float *xsm = reinterpret_cast<const float *>(
-        reinterpret_cast<const uint4 *>(img) + (size_t)R * 8 * G) + (size_t)R * G;
-    const __half2 *mq = reinterpret_cast<const __half2 *>(xsm + (SPLIT ? 2 : 1) *
-                                                                    (size_t)R * G);
-    bool mk = false;
+// The int8 residual planes of the two-plane path (common.cuh, "marked
+// groups") for an image of one row: all `ncons` threads take the (chunk,
+// quarter) items in turn, read the quarter's 16 raw bf16 activations from x
+// again (the encoder's pairs kept only their rounded values), and write its
+// residual entries, exact for every chunk, over the first half of the
+// image's pairs: slot group_lo_slot(q, chunk_rot(g)) of chunk g at
+// img + (slot * G + g) * 16.  Entries in dp4a order: per u4 word those of
+// its low nibbles' inputs (x0 x2 x4 x6), then of its high nibbles' (x1 x3
+// x5 x7); per u8 word x0..x3.  The caller brackets this with barriers: the
+// pairs must be in every lane's registers before, and the planes complete
+// after.  Each thread issues the loads of two items before using either
+// (the callers' pairs occupy 32 registers meanwhile).
+template <int BITS>
+__device__ __forceinline__ void group_plane_store(const uint16_t *__restrict__ x,
+                                                  int G, int tid, int ncons,
+                                                  unsigned char *img) {
+    const float *xf = reinterpret_cast<const float *>(
+        reinterpret_cast<const uint4 *>(img) + (size_t)8 * G);
+    uint4 *lo = reinterpret_cast<uint4 *>(img);
+    const int items = 4 * G;
+    constexpr int B = 2;
+    for (int b0 = tid; b0 < items; b0 += B * ncons) {
+        uint4 u[B][2];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const float2 a = __half22float2(mq[((size_t)r * G + g) * 2]);
-        const float2 b = __half22float2(mq[((size_t)r * G + g) * 2 + 1]);
-        mk |= (a.x + a.y) + (b.x + b.y) > 0.f;
+        for (int j = 0; j < B; ++j) {
+            const int it = b0 + j * ncons;
+            if (it < items) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(x) + 2 * it;
+                u[j][0] = src[0];
+                u[j][1] = src[1];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int it = b0 + j * ncons;
+            if (it >= items) break;
+            const int g = it >> 2, q = it & 3;
+            // the pairs' unit: f as stored (u4: 2^E / 16), so 2^-E is
+            const float finv = 1.0f / (BITS == 4 ? 16.0f * xf[g] : xf[g]);
+            uint32_t w4[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t wv[4] = {u[j][h].x, u[j][h].y, u[j][h].z, u[j][h].w};
+                uint32_t e[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    e[2 * k] = i8_resid(bf16_lo(wv[k]), finv);
+                    e[2 * k + 1] = i8_resid(bf16_hi(wv[k]), finv);
+                }
+                if constexpr (BITS == 4) {  // one u4 word: even, then odd
+                    w4[2 * h] = pack_bytes(e[0], e[2], e[4], e[6]);
+                    w4[2 * h + 1] = pack_bytes(e[1], e[3], e[5], e[7]);
+                } else {  // two u8 words
+                    w4[2 * h] = pack_bytes(e[0], e[1], e[2], e[3]);
+                    w4[2 * h + 1] = pack_bytes(e[4], e[5], e[6], e[7]);
+                }
+            }
+            lo[(size_t)group_lo_slot<BITS>(q, chunk_rot<BITS>(g)) * G + g] =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
     }
-    return mk;
 }
 
-// Bank-conflict-free reads of a row's group.  Lane g reads its group's
-// 16-byte code chunks starting at chunk rot(g), so the lanes whose groups
-// lie 128 bytes apart (4 apart for u4, 2 apart for u8) read different banks
-// in the same instruction.  Its activation pairs are loaded in the same
-// rotated order (image chunk shift), so the dot is unchanged.
-template <int BITS>
-__device__ __forceinline__ int chunk_rot(int g) {
-    return BITS == 4 ? (g >> 2) & 1 : (g >> 1) & 3;
-}
-template <int BITS>
-__device__ __forceinline__ int image_shift(int g) {
-    return (BITS == 4 ? 4 : 2) * chunk_rot<BITS>(g);
-}
+// A row's group of codes, in chunk_rot order.
 template <int BITS>
 __device__ __forceinline__ void lds_group(const unsigned char *src, int rot,
                                           uint4 (&w)[BITS / 2]) {
@@ -258,7 +311,7 @@ __device__ __forceinline__ void lds_group(const unsigned char *src, int rot,
 
 // Image rows r0 .. r0+MT-1 of group g into registers (zeros when !active),
 // image chunks rotated by `shift` (see chunk_rot).
-template <int MT, bool SPLIT = false, int MK = kMarkRaw>
+template <int MT, bool SPLIT = false>
 __device__ __forceinline__ void load_group_rows(const unsigned char *img,
                                                 int R, int G, int r0, int g,
                                                 bool active, GroupX<MT> &gx,
@@ -278,15 +331,7 @@ __device__ __forceinline__ void load_group_rows(const unsigned char *img,
             gx.pr[m][4 * c + 3] = t.w;
         }
         const float fm = active ? xf[(size_t)r * G + g] : 0.f;
-        if constexpr (MK == kMarkDefer) {
-            const __half2 *mq = reinterpret_cast<const __half2 *>(
-                xsm + (SPLIT ? 2 : 1) * (size_t)R * G);
-            const float2 a = __half22float2(mq[((size_t)r * G + g) * 2]);
-            const float2 b = __half22float2(mq[((size_t)r * G + g) * 2 + 1]);
-            gx.mk[m] = active && (a.x + a.y) + (b.x + b.y) > 0.f;
-        } else {
-            gx.mk[m] = fm < 0.f;
-        }
+        gx.mk[m] = fm < 0.f;  // raw-marked images (kMarkRaw)
         gx.f[m] = fabsf(fm);
         gx.xs[m] = active ? xsm[(size_t)r * G + g] : 0.f;
         gx.xs2[m] = SPLIT && active ? xsm[(size_t)R * G + (size_t)r * G + g] : 0.f;
@@ -340,53 +385,25 @@ __device__ __forceinline__ void group_dot(const uint4 (&w)[BITS / 2],
     }
 }
 
-// The int8 residual plane of a chunk (two-plane path, common.cuh "marked
-// groups") written over its pairs in the image (dead by then: every lane
-// holds its pairs in registers) at dst[slot * stride], slots as
-// group_lo_slot for rotation rot: zeros unless `marked`, else formed from
-// its 64 raw bf16 activations x (16-byte aligned) and its scale f as stored
-// in GroupX (u4: 2^E / 16).  Quarter q (inputs 16q .. 16q + 15) in dp4a
-// order: per u4 word the entries of its low nibbles' inputs (x0 x2 x4 x6),
-// then of its high nibbles' (x1 x3 x5 x7); per u8 word x0..x3.  A loop, not
-// unrolled: it runs once per chunk.
+// Plane entries of word c of register piece v (two words per u4 word, one
+// per u8 word), from the piece's plane slots as loaded: u4 slots 2v, 2v + 1
+// in e0, e1 (word c in e[c / 2], halves c % 2); u8 slot v in e0.
 template <int BITS>
-__device__ __forceinline__ void group_lo_store(bool marked, const uint16_t *x,
-                                               float f, int rot, uint4 *dst,
-                                               int stride) {
-    const float finv = marked ? 1.0f / (BITS == 4 ? 16.0f * f : f) : 0.f;
-    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-        if (marked) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint4 u = xv[2 * q + h];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                uint32_t e[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    e[2 * k] = i8_resid(bf16_lo(w[k]), finv);
-                    e[2 * k + 1] = i8_resid(bf16_hi(w[k]), finv);
-                }
-                if constexpr (BITS == 4) {  // one u4 word: even, then odd
-                    w4[2 * h] = e[0] | (e[2] << 8) | (e[4] << 16) | (e[6] << 24);
-                    w4[2 * h + 1] = e[1] | (e[3] << 8) | (e[5] << 16) | (e[7] << 24);
-                } else {  // two u8 words
-                    w4[2 * h] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
-                    w4[2 * h + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
-                }
-            }
-        }
-        dst[(size_t)group_lo_slot<BITS>(q, rot) * stride] =
-            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+__device__ __forceinline__ uint2 plane_words(const uint4 &e0, const uint4 &e1,
+                                             int c) {
+    if constexpr (BITS == 4) {
+        const uint4 &e = c < 2 ? e0 : e1;
+        return (c & 1) ? make_uint2(e.z, e.w) : make_uint2(e.x, e.y);
+    } else {
+        return make_uint2(c == 0 ? e0.x : c == 1 ? e0.y : c == 2 ? e0.z : e0.w,
+                          0u);
     }
 }
 
 // group_dot and the residual-plane dot of the two-plane path in one pass
 // over the code bytes: dh as group_dot's d; dl the same dot with the plane
-// at lo[0], lo[stride], ... (slots as group_lo_slot), read word by word,
-// its scale 2^-7 of dh's.  w as lds_group loaded it.
+// at lo[0], lo[stride], ... (slots as group_lo_slot), read a 16-byte slot
+// at a time, its scale 2^-7 of dh's.  w as lds_group loaded it.
 template <int BITS, int MT>
 __device__ __forceinline__ void group_dot2(const uint4 (&w)[BITS / 2],
                                            const GroupX<MT> &gx, const uint4 *lo,
@@ -397,16 +414,15 @@ __device__ __forceinline__ void group_dot2(const uint4 (&w)[BITS / 2],
     for (int m = 0; m < MT; ++m) a[m][0] = a[m][1] = a[m][2] = a[m][3] = 0;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
+        const uint4 e0 = lo[(size_t)(BITS == 4 ? 2 * v : v) * stride];
+        const uint4 e1 = BITS == 4 ? lo[(size_t)(2 * v + 1) * stride] : e0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int wd = 4 * v + c;
             const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
                                   : c == 2 ? w[v].z : w[v].w;
+            const uint2 e = plane_words<BITS>(e0, e1, c);
             if constexpr (BITS == 4) {
-                // plane entries of this word: slot 2v + c/2, words
-                // 2(c%2), 2(c%2) + 1
-                const uint2 e = reinterpret_cast<const uint2 *>(
-                    lo + (size_t)(2 * v + (c >> 1)) * stride)[c & 1];
                 const uint32_t l = word & 0x0f0f0f0fu;
                 const uint32_t h = word & 0xf0f0f0f0u;
                 const int p = (wd & 1) * 2;
@@ -419,15 +435,13 @@ __device__ __forceinline__ void group_dot2(const uint4 (&w)[BITS / 2],
                 b[0] = dp4a_us(l, e.x, b[0]);
                 b[1] = dp4a_us(h, e.y, b[1]);
             } else {
-                const uint32_t e = reinterpret_cast<const uint32_t *>(
-                    lo + (size_t)v * stride)[c];
                 const int p = wd & 3;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     const uint32_t *pr = gx.pr[m] + 2 * wd;
                     a[m][p] = dp2a_hi(pr[1], word, dp2a_lo(pr[0], word, a[m][p]));
                 }
-                b[wd & 1] = dp4a_us(word, e, b[wd & 1]);
+                b[wd & 1] = dp4a_us(word, e.x, b[wd & 1]);
             }
         }
     }
@@ -450,20 +464,19 @@ __device__ __forceinline__ void group_dot_lo_split(const uint4 (&w)[BITS / 2],
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int pc = (v + rot) & (NV - 1);
+        const uint4 e0 = lo[(size_t)(BITS == 4 ? 2 * v : v) * stride];
+        const uint4 e1 = BITS == 4 ? lo[(size_t)(2 * v + 1) * stride] : e0;
         int b0 = 0, b1 = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
                                   : c == 2 ? w[v].z : w[v].w;
+            const uint2 e = plane_words<BITS>(e0, e1, c);
             if constexpr (BITS == 4) {
-                const uint2 e = reinterpret_cast<const uint2 *>(
-                    lo + (size_t)(2 * v + (c >> 1)) * stride)[c & 1];
                 b0 = dp4a_us(word & 0x0f0f0f0fu, e.x, b0);
                 b1 = dp4a_us(word & 0xf0f0f0f0u, e.y, b1);
             } else {
-                const uint32_t e = reinterpret_cast<const uint32_t *>(
-                    lo + (size_t)v * stride)[c];
-                b0 = dp4a_us(word, e, b0);
+                b0 = dp4a_us(word, e.x, b0);
             }
         }
         const int dv = BITS == 4 ? 16 * b0 + b1 : b0;

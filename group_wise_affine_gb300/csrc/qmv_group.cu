@@ -63,9 +63,9 @@ __device__ __forceinline__ float slot_total(const float *red, int idx,
 // The consumer side of the stage loop (see qmv_group_kernel), for a lane
 // whose image is ready.  EX (two-plane path, common.cuh "marked groups"):
 // once every lane holds its int16 pairs in registers, the image's pairs are
-// dead, and the lanes of the first row group write each chunk's int8
-// residual plane (zeros unless marked) over them; every row then takes both
-// planes' dots in one pass over its code bytes.  The kernel has no local memory and no
+// dead, and all consumer threads write the chunks' int8 residual planes
+// over them (group_plane_store); every row then takes both planes' dots in
+// one pass over its code bytes.  The kernel has no local memory and no
 // calls: a stack frame costs the SM the shared-memory carveout that lets
 // two of these CTAs share it.
 template <int BITS, int MT, int MODE, int RPH, int GS, bool EX>
@@ -96,31 +96,33 @@ __device__ __forceinline__ void group_loop(
     unsigned char *xenc = smem + xenc_off;
     GroupX<MT> gx;
     const int rot = chunk_rot<BITS>(gg);
-    load_group_rows<MT, SPLIT, EX ? kMarkDefer : kMarkRaw>(
-        xenc, MT, nchunk, 0, gg, active, gx, image_shift<BITS>(gg));
-    const uint4 *const plane = reinterpret_cast<const uint4 *>(xenc) + gg;  // row 0
+    load_group_rows<MT, SPLIT>(xenc, MT, nchunk, 0, gg, active, gx,
+                               image_shift<BITS>(gg));
+    const uint4 *const plane = reinterpret_cast<const uint4 *>(xenc) + gg;
     static_assert(!EX || MT == 1, "two-plane path: one token");
     if constexpr (EX) {
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
-        if (hg == 0 && in_group)
-            group_lo_store<BITS>(gx.mk[0], x + gg * 64, gx.f[0], rot,
-                                 reinterpret_cast<uint4 *>(xenc) + gg, nchunk);
+        group_plane_store<BITS>(x, nchunk, tid, ncons, xenc);
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
     }
-    uint32_t offw[RPH], offs[RPH];
+    // the lane's reads of stage row srow(j) = (j / UPT) ups + hg UPT + j % UPT
+    // (row j of its row group): codes at offw + srow(j) rowbytes, scale at
+    // offs + 2 srow(j) G; rows past the end of a stage of fewer units read
+    // the stage's first row instead (their values are never stored), so
+    // that no read leaves a short slot
+    // (the one-plane copy keeps each row's two offsets in registers; the
+    // two-plane copy, short of registers, forms them per stage)
     const uint32_t sb_delta = rows_stage * (uint32_t)G * 2u;
+    const uint32_t offw = codes_off + (uint32_t)gg * GB;
+    const uint32_t offs = (uint32_t)sg * 2u;
+    constexpr int NO = EX ? 1 : RPH;
+    uint32_t offw_j[NO], offs_j[NO];
 #pragma unroll
-    for (int j = 0; j < RPH; ++j) {
-        const uint32_t srow =
-            (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
-        offw[j] = codes_off + srow * rowbytes + (uint32_t)gg * GB;
-        offs[j] = (srow * (uint32_t)G + sg) * 2u;
+    for (int j = 0; j < NO; ++j) {
+        const uint32_t srow = (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT));
+        offw_j[j] = offw + srow * rowbytes;
+        offs_j[j] = offs + srow * (uint32_t)G * 2u;
     }
-    // rows past the end of a stage of fewer units read the stage's first
-    // row instead (their values are never stored), so that no read
-    // leaves a short slot
-    const uint32_t offw0 = codes_off + (uint32_t)gg * GB;
-    const uint32_t offs0 = (uint32_t)sg * 2u;
     // this lane's slot of the partial sums: value index idx = j*MT + m
     // of unit u (stage-relative), half h
     constexpr int SPREAD = kSlice / V;
@@ -148,8 +150,16 @@ __device__ __forceinline__ void group_loop(
 #pragma unroll
         for (int j = 0; j < RPH; ++j) {
             const bool in = hg * UPT + (j % UPT) < left;
-            const uint32_t ow = in ? offw[j] : offw0;
-            const uint32_t os = in ? offs[j] : offs0;
+            uint32_t ow, os;
+            if constexpr (EX) {
+                const uint32_t srow =
+                    in ? (uint32_t)((j / UPT) * ups + hg * UPT + (j % UPT)) : 0u;
+                ow = offw + srow * rowbytes;
+                os = offs + srow * (uint32_t)G * 2u;
+            } else {
+                ow = in ? offw_j[j] : offw;
+                os = in ? offs_j[j] : offs;
+            }
             uint4 w[BITS / 2];
             lds_group<BITS>(base + ow, rot, w);
             if constexpr (SPLIT) {
@@ -241,6 +251,7 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
     uint64_t *empty = full + stages;
     float *red = reinterpret_cast<float *>(empty + stages);
     __shared__ int s_issued, s_consumed;
+    __shared__ int s_marked;  // the encode met a marked chunk
 
     // rope: whole stages per CTA (ups divides d/2), so no stage crosses a head
     const int64_t ualign = MODE == kGRope ? rs * UPT : 1;
@@ -257,6 +268,7 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
         fence_mbar_init();
         s_issued = 0;
         s_consumed = nst;
+        s_marked = 0;
         // let the next kernel in the stream start its own weight prefetch
         pdl_launch_dependents();
     }
@@ -336,14 +348,14 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
         }
         pdl_wait_primary();  // x may be the previous kernel's output
         encode_rows_shared<BITS, SPLIT, kMarkDefer>(p.x, p.M, MT, p.K, nchunk,
-                                                    tid, ncons, xenc);
+                                                    tid, ncons, xenc, nullptr,
+                                                    &s_marked);
         // the consumer warps only (the producer is in its copy loop)
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
-        // Marked chunks (common.cuh, "marked groups"): if any consumer lane
-        // holds one, the CTA runs the two-plane loop (every CTA encodes the
-        // same activations, so all decide alike).
-        const bool mk = active && chunk_marked<MT, SPLIT>(xenc, nchunk, gg);
-        if (bar_red_or(1, ncons, mk))
+        // Marked chunks (common.cuh, "marked groups"): if the encode flagged
+        // one, the CTA runs the two-plane loop (every CTA encodes the same
+        // activations, so all decide alike).
+        if (s_marked)
             group_loop<BITS, MT, MODE, RPH, GS, true>(
                 p.x, p.K, p.G, smem, full, empty, red, &s_consumed, stages, nst,
                 nu, ups, slices, stage_bytes, codes_off, rows_stage, rowbytes,
@@ -399,6 +411,11 @@ __global__ void __maxnreg__(BITS == 4 ? 80 : 88)
             uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
             o[0] = f32_to_bf16_bits(a);
             o[half] = f32_to_bf16_bits(b);
+        } else if (p.nsec == 1) {
+            // a plain projection: no section lookup
+            const float val = slot_total(red, lu * MT + m, slices);
+            p.sec_out[0][(int64_t)m * p.N + n] = f32_to_bf16_bits(
+                p.sec_bias[0] ? val + bf16_bits_to_f32(p.sec_bias[0][n]) : val);
         } else {
             int s = 0;
             while (s + 1 < p.nsec && n >= p.sec_start[s + 1]) ++s;
@@ -446,7 +463,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     const size_t rope_bytes =
         MODE == kGRope ? ((size_t)umax * MT * 8 + 15) / 16 * 16 : 0;
     const size_t fixed = 16 * 8 + ((red_bytes + 15) / 16) * 16 + rope_bytes +
-                         ximg_bytes(MT, nchunk, GS == 32, true);
+                         ximg_bytes(MT, nchunk, GS == 32);
     if (fixed >= kGroupSmemCap) return cudaSuccess;
     int stages = (int)((kGroupSmemCap - fixed) / stage_bytes);
     if (stages > 8) stages = 8;
@@ -469,7 +486,7 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     }
     const size_t rope_off = ring + 16 * stages + ((red_bytes + 15) / 16) * 16;
     const size_t xenc_off = rope_off + rope_bytes;
-    const size_t smem = xenc_off + ximg_bytes(MT, nchunk, GS == 32, true);
+    const size_t smem = xenc_off + ximg_bytes(MT, nchunk, GS == 32);
     auto kern = qmv_group_kernel<BITS, MT, MODE, RPH, GS>;
     int dummy = 0;
     cudaError_t e = occupancy_grid(reinterpret_cast<const void *>(kern),

@@ -30,6 +30,7 @@ namespace gwa {
 
 static __device__ unsigned int g_stream_timeouts;
 
+// Modes as the host passes them (a plain projection runs as one section).
 // kSRope: QKV sections with the rotary embedding, pairs of rows
 // (i, i + d/2) of a head (rope_pair_row) laid out like gate/up pairs, in
 // stages of whole pairs within one head; the epilogue rotates with the
@@ -38,7 +39,9 @@ enum StreamMode { kSPlain = 0, kSSections = 1, kSGateUp = 2, kSRope = 3 };
 
 // A thread's activations for its chunk, encoded for the integer dot (see
 // common.cuh): int16 pairs in dp2a order, the group scale 2^E and the plain
-// fp32 sum of the chunk's activations.
+// fp32 sum of the chunk's activations.  The chunk's int8 residual planes
+// (two-plane path) stay in shared memory, read only by a warp that needs
+// them, so that the one-plane loop keeps its registers.
 template <int BITS, int MT>
 struct XRegs {
     static constexpr int CODES = Fmt<BITS>::kChunkCodes;
@@ -46,16 +49,34 @@ struct XRegs {
     float f[MT];
     float xs[MT];
     bool mk[MT];                 // marked group (common.cuh, "marked groups")
-    uint32_t lo[MT][CODES / 4];  // its int8 residual plane, in dp4a order
 };
 
-// Loads and encodes chunk c of each token.  Every lane of the warp must
-// call this (the lanes of one group agree on its scale and mark through
-// shuffles); inactive lanes encode zeros.
+// Residual plane words of a thread per token and code word: two for u4
+// (the entries of the word's low nibbles' inputs, then of its high ones'),
+// one for u8.  Layout in shared memory: [token][code word][thread], so the
+// threads of a warp read consecutive words.
+template <int BITS>
+constexpr int kPlaneWords = BITS == 4 ? 2 : 1;
+template <int BITS>
+__device__ __forceinline__ uint2 plane_load(const uint32_t *plane, int pstride,
+                                            int m, int wd, int t) {
+    const int i = (m * 4 + wd) * pstride + t;
+    if constexpr (BITS == 4)
+        return reinterpret_cast<const uint2 *>(plane)[i];
+    else
+        return make_uint2(plane[i], 0u);
+}
+
+// Loads and encodes chunk c of each token, and writes the chunk's residual
+// planes for thread t (zero unless marked) to `plane`.  Every lane of the
+// warp must call this (the lanes of one group agree on its scale and mark
+// through shuffles); inactive lanes encode zeros.
 template <int BITS, int MT>
 __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
                                             int M, int K, int c, bool active,
-                                            XRegs<BITS, MT> &xr) {
+                                            XRegs<BITS, MT> &xr,
+                                            uint32_t *plane, int pstride,
+                                            int t) {
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
     constexpr int CPG = kGroup / CODES;  // lanes sharing a group
 #pragma unroll
@@ -118,119 +139,159 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
                 xr.pr[m][2 * wd + 1] = t[1];
             }
         }
-        // the residual plane (zero unless marked): per u4 word the entries
-        // of its low nibbles' inputs (x0 x2 x4 x6), then of its high ones;
-        // per u8 word x0..x3
-#pragma unroll
-        for (int i = 0; i < CODES / 4; ++i) {
-            uint32_t q = 0u;
-            if (marked) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = BITS == 4 ? 8 * (i >> 1) + 2 * k + (i & 1) : 4 * i + k;
-                    q |= i8_resid(v[e], finv) << (8 * k);
-                }
-            }
-            xr.lo[m][i] = q;
-        }
         xr.f[m] = f;
         xr.mk[m] = marked;
         xr.xs[m] = xs;
+    }
+    // The residual planes (zero unless marked), in a second pass that
+    // reloads a marked chunk, so that no token's activations stay live
+    // beside another's pairs: per u4 word the entries of its low nibbles'
+    // inputs (x0 x2 x4 x6), then of its high ones'; per u8 word x0..x3.
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        uint32_t q[CODES / 4];
+#pragma unroll
+        for (int i = 0; i < CODES / 4; ++i) q[i] = 0u;
+        if (xr.mk[m]) {  // marked implies active and m < M
+            const float finv = 1.0f / xr.f[m];  // a power of two: exact
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                x + (int64_t)m * K + (int64_t)c * CODES);
+#pragma unroll
+            for (int j = 0; j < CODES / 8; ++j) {
+                const uint4 u = src[j];
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+                uint32_t e[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    e[2 * k] = i8_resid(bf16_lo(wv[k]), finv);
+                    e[2 * k + 1] = i8_resid(bf16_hi(wv[k]), finv);
+                }
+                // inputs 8j .. 8j + 7: u4 word j (two plane words), u8
+                // words 2j, 2j + 1
+                if constexpr (BITS == 4) {
+                    q[2 * j] = e[0] | (e[2] << 8) | (e[4] << 16) | (e[6] << 24);
+                    q[2 * j + 1] = e[1] | (e[3] << 8) | (e[5] << 16) | (e[7] << 24);
+                } else {
+                    q[2 * j] = e[0] | (e[1] << 8) | (e[2] << 16) | (e[3] << 24);
+                    q[2 * j + 1] = e[4] | (e[5] << 8) | (e[6] << 16) | (e[7] << 24);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < CODES / 4; ++i) {
+            // word i: code word i / 2, half i % 2 (u4); code word i (u8)
+            const int wd = BITS == 4 ? i >> 1 : i;
+            plane[((m * 4 + wd) * pstride + t) * kPlaneWords<BITS> +
+                  (BITS == 4 ? (i & 1) : 0)] = q[i];
+        }
     }
 }
 
 // Chunk dots of R rows against MT tokens: exact integer sums per chunk,
 // then (s * 2^E) * D + b * sum(x) in fp32.  The word loop is outside the row
 // loop so the rows' dp2a chains interleave; a word's code bytes are split
-// once and reused for every token.  With EX, the same words also meet the
-// tokens' int8 residual planes (common.cuh, "marked groups"; zero for
-// unmarked groups).
-template <int BITS, int MT, int R, bool EX>
+// once and reused for every token.
+template <int BITS, int MT, int R>
 __device__ __forceinline__ void batch_dot(const uint4 (&w)[R],
                                           const float (&s)[R],
                                           const float (&b)[R],
                                           const XRegs<BITS, MT> &xr,
                                           float (&out)[R][MT]) {
-    {
-        int d[R][MT][2];
+    int d[R][MT][2];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) d[r][m][0] = d[r][m][1] = 0;
+        for (int m = 0; m < MT; ++m) d[r][m][0] = d[r][m][1] = 0;
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
+    for (int wd = 0; wd < 4; ++wd) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint32_t word = wd == 0   ? w[r].x
-                                      : wd == 1 ? w[r].y
-                                      : wd == 2 ? w[r].z
-                                                : w[r].w;
-                if constexpr (BITS == 4) {
-                    // high nibbles stay in place (16 * q) and are summed apart
-                    const uint32_t lo = word & 0x0f0f0f0fu;
-                    const uint32_t hi = word & 0xf0f0f0f0u;
+        for (int r = 0; r < R; ++r) {
+            const uint32_t word = wd == 0   ? w[r].x
+                                  : wd == 1 ? w[r].y
+                                  : wd == 2 ? w[r].z
+                                            : w[r].w;
+            if constexpr (BITS == 4) {
+                // high nibbles stay in place (16 * q) and are summed apart
+                const uint32_t lo = word & 0x0f0f0f0fu;
+                const uint32_t hi = word & 0xf0f0f0f0u;
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const uint32_t *pr = xr.pr[m] + 4 * wd;
-                        d[r][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, d[r][m][0]));
-                        d[r][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, d[r][m][1]));
-                    }
-                } else {
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = xr.pr[m] + 4 * wd;
+                    d[r][m][0] = dp2a_hi(pr[1], lo, dp2a_lo(pr[0], lo, d[r][m][0]));
+                    d[r][m][1] = dp2a_hi(pr[3], hi, dp2a_lo(pr[2], hi, d[r][m][1]));
+                }
+            } else {
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const uint32_t *pr = xr.pr[m] + 2 * wd;
-                        int a = d[r][m][wd & 1];
-                        a = dp2a_lo(pr[0], word, a);
-                        d[r][m][wd & 1] = dp2a_hi(pr[1], word, a);
-                    }
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t *pr = xr.pr[m] + 2 * wd;
+                    int a = d[r][m][wd & 1];
+                    a = dp2a_lo(pr[0], word, a);
+                    d[r][m][wd & 1] = dp2a_hi(pr[1], word, a);
                 }
             }
         }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                // u4: the high-nibble sum is 16x the true sum, exactly
-                const int dsum = BITS == 4 ? d[r][m][0] + (d[r][m][1] >> 4)
-                                           : d[r][m][0] + d[r][m][1];
-                out[r][m] = fmaf(s[r] * xr.f[m], (float)dsum, b[r] * xr.xs[m]);
-            }
     }
-    if constexpr (EX) {
-        // the residual planes, 2^-7 of the scale, after the first dot so
-        // that the two sets of accumulators are never live together
-        int e[R][MT];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            // u4: the high-nibble sum is 16x the true sum, exactly
+            const int dsum = BITS == 4 ? d[r][m][0] + (d[r][m][1] >> 4)
+                                       : d[r][m][0] + d[r][m][1];
+            out[r][m] = fmaf(s[r] * xr.f[m], (float)dsum, b[r] * xr.xs[m]);
+        }
+}
+
+// The residual planes' share of the same chunk dots (two-plane path,
+// common.cuh "marked groups"; zero for unmarked groups), 2^-7 of the
+// scale, added to out.  A pass of its own, taken only by a warp with a
+// marked group, after batch_dot so that the two sets of accumulators are
+// never live together; the code words are read again from the stage (the
+// slot is still held) and the plane words from shared memory.  Rows go in
+// blocks of RB, so that two tokens' u4 accumulators and plane words fit
+// beside their pairs.
+template <int BITS, int MT, int R>
+__device__ __forceinline__ void batch_res(const float (&s)[R],
+                                       const XRegs<BITS, MT> &xr,
+                                       const unsigned char *base,
+                                       const uint32_t (&offw)[R],
+                                       const uint32_t *plane, int pstride,
+                                       int t, float (&out)[R][MT]) {
+    constexpr int RB = (BITS == 4 && MT == 2) ? 1 : R;
+#pragma unroll
+    for (int r0 = 0; r0 < R; r0 += RB) {
+        int e[RB][MT];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
 #pragma unroll
             for (int m = 0; m < MT; ++m) e[r][m] = 0;
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint32_t word = wd == 0   ? w[r].x
-                                      : wd == 1 ? w[r].y
-                                      : wd == 2 ? w[r].z
-                                                : w[r].w;
+            for (int m = 0; m < MT; ++m) {
+                const uint2 lo = plane_load<BITS>(plane, pstride, m, wd, t);
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
+                for (int r = 0; r < RB; ++r) {
+                    const uint32_t word = reinterpret_cast<const uint32_t *>(
+                        base + offw[r0 + r])[wd];
                     if constexpr (BITS == 4) {
                         // the high nibbles' products in place (16x), then
                         // the low ones' scaled to match
-                        const int t = dp4a_us(word & 0xf0f0f0f0u, xr.lo[m][2 * wd + 1], 0);
-                        e[r][m] = dp4a_us(word & 0x0f0f0f0fu, xr.lo[m][2 * wd],
-                                          e[r][m] + (t >> 4));
+                        const int h = dp4a_us(word & 0xf0f0f0f0u, lo.y, 0);
+                        e[r][m] = dp4a_us(word & 0x0f0f0f0fu, lo.x,
+                                          e[r][m] + (h >> 4));
                     } else {
-                        e[r][m] = dp4a_us(word, xr.lo[m][wd], e[r][m]);
+                        e[r][m] = dp4a_us(word, lo.x, e[r][m]);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+        for (int r = 0; r < RB; ++r)
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-                out[r][m] = fmaf(s[r] * xr.f[m] * 0.0078125f, (float)e[r][m], out[r][m]);
+                out[r0 + r][m] = fmaf(s[r0 + r] * xr.f[m] * 0.0078125f,
+                                      (float)e[r][m], out[r0 + r][m]);
     }
 }
 
@@ -256,7 +317,8 @@ constexpr int kRowsPerThread = 4;
 // four tokens need more and run one CTA per SM.
 template <int BITS, int MT, int MODE, int RPH>
 __global__ void __maxnreg__(MT == 4 ? 128 : 80)
-    qmv_stream_kernel(DenseParams p, int stages, int64_t units, int rs) {
+    qmv_stream_kernel(DenseParams p, int stages, int64_t units, int rs,
+                      uint32_t plane_off) {
     constexpr int HALVES = (MODE == kSGateUp || MODE == kSRope) ? 2 : 1;
     constexpr int UPT = RPH / HALVES;     // units per thread per stage
     constexpr int V = RPH * MT;           // values reduced per warp per stage
@@ -352,8 +414,9 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
         const int cc = active ? c : 0;
         const int g = (cc * CODES) / kGroup;
         XRegs<BITS, MT> xr;
+        uint32_t *plane = reinterpret_cast<uint32_t *>(smem + plane_off);
         pdl_wait_primary();  // x may be the previous kernel's output
-        load_x_regs<BITS, MT>(p.x, p.M, p.K, c, active, xr);
+        load_x_regs<BITS, MT>(p.x, p.M, p.K, c, active, xr, plane, ncons, tid);
         // This thread's rows are unit hg*UPT + u of each half of a stage;
         // their shared-memory offsets are the same in every stage.  Row
         // slots past the stage end hold stale data; their totals are
@@ -367,9 +430,13 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
             offw[j] = srow * rowbytes + (uint32_t)cc * 16u;
             offs[j] = rows_stage * rowbytes + (srow * (uint32_t)p.G + g) * 2u;
         }
-        // The stage loop, once with the residual-plane dot (EX) and once
-        // without it: a warp none of whose lanes holds a marked group runs
-        // the one-plane copy.
+        // A warp none of whose lanes holds a marked group runs the one-plane
+        // copy of the stage loop.
+        bool anymk = false;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) anymk |= xr.mk[m];
+        // The stage loop, once with the residual-plane pass (EX) and once
+        // without it, so that each copy gets its own register allocation.
         auto stage_loop = [&](auto ex) {
             constexpr bool EX = decltype(ex)::value;
             for (int st = 0; st < nst; ++st) {
@@ -393,7 +460,10 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
                         base + offs[j] + sb_delta));
                 }
                 float o[RPH][MT];
-                batch_dot<BITS, MT, RPH, EX>(w, sv, bv, xr, o);
+                batch_dot<BITS, MT, RPH>(w, sv, bv, xr, o);
+                if constexpr (EX)
+                    batch_res<BITS, MT, RPH>(sv, xr, base, offw, plane, ncons,
+                                             tid, o);
                 float v[V];
 #pragma unroll
                 for (int j = 0; j < RPH; ++j)
@@ -415,9 +485,6 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
                 }
             }
         };
-        bool anymk = false;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) anymk |= xr.mk[m];
         if (__any_sync(0xffffffffu, anymk))
             stage_loop(std::true_type{});
         else
@@ -466,9 +533,6 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
             uint16_t *o = p.sec_out[s] + (int64_t)m * size + j;
             o[0] = f32_to_bf16_bits(a);
             o[half] = f32_to_bf16_bits(b);
-        } else if constexpr (MODE == kSPlain) {
-            p.y[(int64_t)m * p.N + n] =
-                f32_to_bf16_bits(red_total(red, lu * MT + m, nwh));
         } else {
             int s = 0;
             while (s + 1 < p.nsec && n >= p.sec_start[s + 1]) ++s;
@@ -511,7 +575,11 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     const int64_t umax =
         (units + grid - 1) / grid + (MODE == kSRope ? rs * UPT : 0);
     const size_t red_bytes = (size_t)umax * HALVES * MT * 4 * nwh;
-    const size_t smem = stages * stage_bytes + 16 * stages + red_bytes;
+    // residual planes: per consumer thread and token, 8 (u4) or 4 (u8) words
+    const size_t ncons = (size_t)threads - kWarp;
+    const size_t plane_off =
+        (stages * stage_bytes + 16 * stages + red_bytes + 15) / 16 * 16;
+    const size_t smem = plane_off + ncons * MT * 4 * kPlaneWords<BITS> * 4;
     if (smem > kMaxDynSmem) return cudaSuccess;
     auto kern = qmv_stream_kernel<BITS, MT, MODE, RPH>;
     int dummy = 0;
@@ -520,7 +588,7 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     if (e != cudaSuccess) return e;
     *used = true;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, threads,
-                      smem, st, p, stages, units, rs);
+                      smem, st, p, stages, units, rs, (uint32_t)plane_off);
 }
 
 template <int BITS, int MT, int MODE>
@@ -545,14 +613,24 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
         !aligned16(p.wq))
         return cudaSuccess;
     const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;
+    // A plain projection runs as one section: the same kernel as the fused
+    // QKV projection, so that a layer's calls share their code.
+    DenseParams q = p;
+    if (mode == kSPlain) {
+        q.nsec = 1;
+        q.sec_start[0] = 0;
+        q.sec_start[1] = p.N;
+        q.sec_out[0] = p.y;
+        q.sec_bias[0] = nullptr;
+        mode = kSSections;
+    }
 #define GWA_STREAM_CASE(B, MTV)                                              \
     if (p.bits == B && mt == MTV) {                                          \
-        if (mode == kSPlain) return launch_stream_t<B, MTV, kSPlain>(p, st, used); \
         if (mode == kSSections)                                              \
-            return launch_stream_t<B, MTV, kSSections>(p, st, used);         \
+            return launch_stream_t<B, MTV, kSSections>(q, st, used);         \
         if (mode == kSRope)                                                  \
-            return launch_stream_t<B, MTV, kSRope>(p, st, used);             \
-        return launch_stream_t<B, MTV, kSGateUp>(p, st, used);               \
+            return launch_stream_t<B, MTV, kSRope>(q, st, used);             \
+        return launch_stream_t<B, MTV, kSGateUp>(q, st, used);               \
     }
     GWA_STREAM_CASE(4, 1)
     GWA_STREAM_CASE(4, 2)
