@@ -42,7 +42,7 @@ EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_pipeline_status", "gwa_debug_unpack", "gwa_debug_dequant",
            "gwa_qmv_affine_noalloc", "gwa_quantize_affine", "gwa_qmv_qkv_rope",
            "gwa_qkv_rope_workspace_bytes", "gwa_sdpa_dequant_v",
-           "gwa_sdpa_workspace_bytes")
+           "gwa_sdpa_workspace_bytes", "gwa_debug_bounded_wait")
 
 
 class GwaError(RuntimeError):
@@ -109,9 +109,11 @@ def load(path: str = LIB_PATH):
     lib.gwa_quantize_affine.restype = ctypes.c_int
     lib.gwa_debug_unpack.argtypes = [_QW, vp, vp]
     lib.gwa_debug_dequant.argtypes = [_QW, vp, vp]
+    lib.gwa_debug_bounded_wait.argtypes = [ctypes.c_uint32, vp, vp]
     for f in ("gwa_qmv_affine", "gwa_qmv_fused_sections",
               "gwa_qmv_gate_up_silu", "gwa_moe_qmv_gather",
-              "gwa_debug_unpack", "gwa_debug_dequant"):
+              "gwa_debug_unpack", "gwa_debug_dequant",
+              "gwa_debug_bounded_wait"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -489,6 +491,16 @@ def debug_unpack(w: QWeight, stream=None) -> torch.Tensor:
     codes = torch.empty((w.N, w.K), dtype=torch.uint8, device=w.wq.device)
     _check(load().gwa_debug_unpack(w.c(), _ptr(codes), _stream(stream)))
     return codes
+
+
+def debug_bounded_wait(limit_us: int, device=None, stream=None) -> torch.Tensor:
+    """gwa_debug_bounded_wait: int32[4] (gave up, waited us) for the plain
+    and the sleeping bounded wait, each made to run out after limit_us."""
+    out = torch.full((4,), -1, dtype=torch.int32,
+                     device=device if device is not None else "cuda")
+    _check(load().gwa_debug_bounded_wait(int(limit_us), _ptr(out),
+                                         _stream(stream)))
+    return out
 
 
 def debug_dequant(w: QWeight, stream=None) -> torch.Tensor:

@@ -704,6 +704,21 @@ size_t gwa_sdpa_workspace_bytes(int64_t B, int32_t Hq, int32_t Hkv, int32_t Lq,
     return attention_workspace_bytes((int)B, Hq, Hkv, Lq, (int)T, D);
 }
 
+int gwa_debug_bounded_wait(uint32_t limit_us, uint32_t *out, void *stream) {
+    const char *fn = "gwa_debug_bounded_wait";
+    g_last_error.clear();
+    if (limit_us < 1 || limit_us > 2000000u)
+        return fail(GWA_ERR_INVALID_ARG, "%s: limit_us=%u (1 .. 2000000)", fn,
+                    (unsigned)limit_us);
+    if (!out) return fail(GWA_ERR_INVALID_ARG, "%s: null out", fn);
+    if (!aligned(out, 4)) return fail(GWA_ERR_MISALIGNED, "%s: alignment", fn);
+    int rc = check_device();
+    if (rc) return rc;
+    cudaError_t e = launch_debug_wait(out, 1000ull * limit_us,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GWA_OK : cuda_fail(e, fn);
+}
+
 int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream) {
     const char *fn = "gwa_debug_dequant";
     g_last_error.clear();

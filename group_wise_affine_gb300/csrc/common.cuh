@@ -353,11 +353,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(
+    uint64_t *bar, uint32_t parity,
+    unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 
@@ -377,12 +379,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar,
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar,
-                                                uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_sleep(
+    uint64_t *bar, uint32_t parity,
+    unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait_sleep(bar, parity, 1000000u))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 

@@ -71,4 +71,35 @@ cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
     return cudaGetLastError();
 }
 
+// The bounded pipeline wait, made to run out: one CTA, an mbarrier that
+// expects one arrival which never comes.  Warp 0 waits with mbar_wait
+// (the streaming and decode kernels' wait), warp 1 with mbar_wait_sleep
+// (the tensor-core kernel's), both with `limit_ns` in place of the kernels'
+// 2 s.  out[2w] = 1 when warp w's wait gave up (0 if it completed),
+// out[2w + 1] = the microseconds it waited.  Nothing is left in flight: the
+// barrier guards no copy, so the CTA can simply return.
+__global__ void debug_wait_kernel(uint32_t *out, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int w = threadIdx.x / kWarp;
+    const unsigned long long t0 = global_ns();
+    const bool ok = w == 0 ? mbar_wait(&bar, 0, limit_ns)
+                           : mbar_wait_sleep(&bar, 0, limit_ns);
+    const unsigned long long t1 = global_ns();
+    if ((threadIdx.x & (kWarp - 1)) == 0) {
+        out[2 * w] = ok ? 0u : 1u;
+        out[2 * w + 1] = (uint32_t)((t1 - t0) / 1000ull);
+    }
+}
+
+cudaError_t launch_debug_wait(uint32_t *out, unsigned long long limit_ns,
+                              cudaStream_t st) {
+    debug_wait_kernel<<<1, 2 * kWarp, 0, st>>>(out, limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace gwa

@@ -176,5 +176,7 @@ cudaError_t launch_debug_dequant(const uint32_t *wq, const uint16_t *sc,
                                  const uint16_t *bi, int64_t N, int64_t K,
                                  int bits, int group, float *wf,
                                  cudaStream_t st);
+cudaError_t launch_debug_wait(uint32_t *out, unsigned long long limit_ns,
+                              cudaStream_t st);
 
 }  // namespace gwa

@@ -307,6 +307,18 @@ int gwa_pipeline_status(uint32_t *timeouts, int32_t reset);
 int gwa_debug_unpack(gwa_qweight w, uint8_t *codes, void *stream);
 int gwa_debug_dequant(gwa_qweight w, float *wf, void *stream);
 
+/* Test export: the kernels' bounded pipeline wait (see gwa_pipeline_status),
+ * made to run out on purpose.  One CTA waits on a shared-memory barrier
+ * that nothing completes, with `limit_us` microseconds (1 .. 2000000) in
+ * place of the kernels' 2 s: warp 0 with the wait of the decode kernels,
+ * warp 1 with the sleeping wait of the tensor-core kernel.  Writes the
+ * device uint32 out[4] (16 bytes, caller-owned, 4-byte aligned): out[0],
+ * out[2] = 1 when the respective wait gave up, out[1], out[3] = the
+ * microseconds it waited.  The kernel returns normally, so the context
+ * stays usable; the production timeout counters are not touched.
+ * Errors: GWA_ERR_INVALID_ARG (limit, null), GWA_ERR_MISALIGNED. */
+int gwa_debug_bounded_wait(uint32_t limit_us, uint32_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
