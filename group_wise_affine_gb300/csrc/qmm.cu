@@ -212,8 +212,9 @@ __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
 // largest |x| and |group sum| of the token) in the dequantizers' k order,
 // then per group g three bias columns (Xhi, Xlo, Xhi) of its scaled sum,
 // then zero padding; tscale[m] = 2^-e_m.  u4 order inside each 8-block:
-// 0 4 1 5 2 6 3 7; u8 inside each 4-block: 0 2 1 3.  One warp per token: a
-// pass for the scale, a pass (the loads hit the cache) for the conversion.
+// 0 4 1 5 2 6 3 7; u8 inside each 4-block: 0 2 1 3.  A CTA per token, a
+// thread per group: a pass for the scale (a block reduction), a pass (the
+// loads hit the cache) for the conversion.
 __device__ __forceinline__ void load_group64(const uint16_t *src, float (&v)[64]) {
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
 #pragma unroll
@@ -231,17 +232,16 @@ __device__ __forceinline__ void load_group64(const uint16_t *src, float (&v)[64]
 }
 
 template <int BITS>
-__global__ void qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M,
-                                   int K, int64_t kext, __half *xe,
-                                   float *tscale) {
+__global__ void __launch_bounds__(128)
+    qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M, int K,
+                       int64_t kext, __half *xe, float *tscale) {
+    __shared__ float s_t[4];
     const int G = K / 64;
-    const int lane = threadIdx.x & 31;
-    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
-    const int64_t nw = (int64_t)gridDim.x * blockDim.x / 32;
-    for (int64_t m = w0; m < M; m += nw) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const uint16_t *xr = x + m * K;
         float t = 0.f;
-        for (int g = lane; g < G; g += 32) {
+        for (int g = tid; g < G; g += blockDim.x) {
             float v[64];
             load_group64(xr + g * 64, v);
             float X = 0.f, mx = 0.f;
@@ -255,11 +255,15 @@ __global__ void qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M,
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+        if (lane == 0) s_t[warp] = t;
+        __syncthreads();
+        t = fmaxf(fmaxf(s_t[0], s_t[1]), fmaxf(s_t[2], s_t[3]));
+        __syncthreads();  // s_t is reused by the next token
         float up, down;
         range_scale(t, up, down);
-        if (lane == 0) tscale[m] = down;
+        if (tid == 0) tscale[m] = down;
         __half *row = xe + m * kext;
-        for (int g = lane; g < G; g += 32) {
+        for (int g = tid; g < G; g += blockDim.x) {
             float v[64];
             load_group64(xr + g * 64, v);
             float X = 0.f;
@@ -293,7 +297,7 @@ __global__ void qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M,
             bc[1] = xl;
             bc[2] = xh;
         }
-        for (int64_t c = K + 3 * G + lane; c < kext; c += 32)
+        for (int64_t c = K + 3 * G + tid; c < kext; c += blockDim.x)
             row[c] = __float2half_rn(0.f);
     }
 }
@@ -841,10 +845,10 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm status reset: %s",
                          cudaGetErrorString(e));
-    const int pthreads = 128;  // a warp per token
-    int64_t pblocks = (M * 32 + pthreads - 1) / pthreads;
+    // a CTA of four warps per token (a thread per group of 64 inputs)
+    int64_t pblocks = M;
     if (pblocks > (int64_t)num_sms() * 16) pblocks = (int64_t)num_sms() * 16;
-    qmm_prepass_kernel<BITS><<<(unsigned)pblocks, pthreads, 0, st>>>(
+    qmm_prepass_kernel<BITS><<<(unsigned)pblocks, 128, 0, st>>>(
         a.x, M, (int)K, kext, xe, tscale);
     e = cudaGetLastError();
     if (e != cudaSuccess)

@@ -57,7 +57,7 @@ extern "C" {
 enum {
     GWA_OK = 0,
     GWA_ERR_INVALID_ARG = 1, /* null pointer, bad size, sizes not adding up */
-    GWA_ERR_UNSUPPORTED = 2, /* bits not in {2,3,4,6,8}, group not in
+    GWA_ERR_UNSUPPORTED = 2, /* bits not in {2,3,4,6,8,GWA_FP8_E4M3}, group not in
                                 {32,64,128}; or a format an entry point does
                                 not take (experts, quantization: u4/u8 at
                                 group 64)                                  */
@@ -78,7 +78,15 @@ enum {
  * kernel for the dense
  * projections (all of gwa_qmv_affine, gwa_qmv_fused_sections,
  * gwa_qmv_gate_up_silu, gwa_qmv_qkv_rope, the debug exports); the experts
- * and the quantization take u4/u8 at group 64 only.                      */
+ * and the quantization take u4/u8 at group 64 only.
+ * bits = GWA_FP8_E4M3: 8-bit floating-point codes (OCP FP8 E4M3: 1 sign,
+ * 4 exponent bits of bias 7, 3 mantissa bits, subnormals, no infinities,
+ * S.1111.111 = NaN) packed four per word, lowest byte first, in the same
+ * container: w = scale * e4m3(q) + bias ("saragossa", "Quantization
+ * formats" lists fp8 (e4m3) beside the affine widths and gives it the u8
+ * footprint, ~8.5 bits per weight).  Dense projections only, any group, on
+ * the general decode kernel in fp32 (every product e4m3 * bf16 is exact). */
+#define GWA_FP8_E4M3 0x108
 typedef struct gwa_qweight {
     const uint32_t *wq;
     const uint16_t *scales;

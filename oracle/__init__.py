@@ -66,6 +66,8 @@ def _load():
         lib = ctypes.CDLL(build())
         lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.orc_bf16_to_f64.restype = ctypes.c_double
+        lib.orc_e4m3_value.argtypes = [ctypes.c_uint32]
+        lib.orc_e4m3_value.restype = ctypes.c_double
         lib.orc_silu.argtypes = [ctypes.c_double]
         lib.orc_silu.restype = ctypes.c_double
         lib.orc_max_threads.argtypes = []
@@ -123,6 +125,20 @@ def bf16_to_f64(h) -> np.ndarray:
 
 def silu(g: float) -> float:
     return float(_load().orc_silu(float(g)))
+
+
+# bits value selecting 8-bit OCP FP8 E4M3 codes (see oracle.c)
+FP8_E4M3 = 0x108
+
+
+def code_width(bits: int) -> int:
+    """Bits a code takes in the packed stream."""
+    return 8 if bits == FP8_E4M3 else bits
+
+
+def e4m3_value(byte: int) -> float:
+    """The OCP FP8 E4M3 number a byte stands for (NaN for S.1111.111)."""
+    return float(_load().orc_e4m3_value(int(byte) & 0xff))
 
 
 def unpack(wq, N: int, K: int, bits: int) -> np.ndarray:

@@ -42,7 +42,15 @@
  *   - gate rows come first, then up rows; SiLU(g) = g / (1 + exp(-g));
  *   - MoE: gate+up mode gives h[t,j,:] = SiLU(Wg[e] x_t) * (Wu[e] x_t) for
  *     e = ids[t,j]; down mode gives y[t,:] = sum_j r[t,j] * (Wd[e] h[t,j,:]),
- *     summed over j in slot order.
+ *     summed over j in slot order;
+ *   - fp8 (e4m3), listed by "saragossa", "Quantization formats" beside the
+ *     affine widths with the u8 footprint: 8-bit codes in the same container
+ *     (four per word, lowest byte first) whose value is the OCP FP8 E4M3
+ *     number of the byte (sign bit 7, exponent bits 6..3 with bias 7,
+ *     mantissa bits 2..0; exponent 0: subnormal m/8 * 2^-6; exponent 15 with
+ *     mantissa 7: NaN; no infinities), dequantized as scale * value + bias.
+ *     Selected by bits = ORC_FP8 (the library's GWA_FP8_E4M3 value, written
+ *     out here on its own).
  *
  * bf16 values arrive as their 16-bit patterns; widening bf16 -> fp32 -> fp64
  * is exact.  Compile with -ffp-contract=off so no multiply-add is fused.
@@ -67,14 +75,42 @@ double orc_bf16_to_f64(uint16_t h) {
     return (double)f;
 }
 
+#define ORC_FP8 0x108
+
 static int bits_ok(int bits) {
-    return bits == 2 || bits == 3 || bits == 4 || bits == 6 || bits == 8;
+    return bits == 2 || bits == 3 || bits == 4 || bits == 6 || bits == 8 ||
+           bits == ORC_FP8;
+}
+
+/* Bits a code takes in the stream. */
+static int code_width(int bits) { return bits == ORC_FP8 ? 8 : bits; }
+
+/* The OCP FP8 E4M3 number of a byte, from its fields. */
+double orc_e4m3_value(uint32_t byte) {
+    const int sign = (int)((byte >> 7) & 1u);
+    const int e = (int)((byte >> 3) & 15u);
+    const int m = (int)(byte & 7u);
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* The value a code stands for before the affine map: the integer itself,
+ * or its E4M3 number. */
+static double code_value(uint32_t code, int bits) {
+    return bits == ORC_FP8 ? orc_e4m3_value(code) : (double)code;
 }
 
 /* The integer code at (row n, input k): bits [b*k, b*k + b) of the row's
  * bit stream, word j holding stream bits [32j, 32j + 32). */
 static inline uint32_t code_at(const uint32_t *wq, int64_t words_per_row,
                                int64_t n, int64_t k, int bits) {
+    bits = code_width(bits);
     const uint32_t *row = wq + n * words_per_row;
     int64_t pos = (int64_t)bits * k;      /* stream position of the low bit */
     uint32_t shift = (uint32_t)(pos % 32);
@@ -88,7 +124,7 @@ static inline uint32_t code_at(const uint32_t *wq, int64_t words_per_row,
 static int shape_ok(int64_t N, int64_t K, int bits, int group) {
     if (N < 0 || K < 0 || !bits_ok(bits) || group <= 0) return 0;
     if (K % group != 0) return 0;
-    if ((K * bits) % 32 != 0) return 0;
+    if ((K * code_width(bits)) % 32 != 0) return 0;
     return 1;
 }
 
@@ -112,7 +148,7 @@ int orc_max_threads(void) {
 int orc_unpack(const uint32_t *wq, int64_t N, int64_t K, int bits,
                uint8_t *codes) {
     if (!shape_ok(N, K, bits, 1)) return ORC_BAD_ARG;
-    int64_t wpr = K * bits / 32;
+    int64_t wpr = K * code_width(bits) / 32;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k)
             codes[n * K + k] = (uint8_t)code_at(wq, wpr, n, k, bits);
@@ -124,12 +160,12 @@ int orc_dequant(const uint32_t *wq, const uint16_t *scales,
                 const uint16_t *biases, int64_t N, int64_t K, int bits,
                 int group, double *w) {
     if (!shape_ok(N, K, bits, group)) return ORC_BAD_ARG;
-    int64_t wpr = K * bits / 32, gpr = K / group;
+    int64_t wpr = K * code_width(bits) / 32, gpr = K / group;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k) {
             double s = orc_bf16_to_f64(scales[n * gpr + k / group]);
             double b = orc_bf16_to_f64(biases[n * gpr + k / group]);
-            double q = (double)code_at(wq, wpr, n, k, bits);
+            double q = code_value(code_at(wq, wpr, n, k, bits), bits);
             w[n * K + k] = s * q + b;
         }
     return ORC_OK;
@@ -139,12 +175,12 @@ int orc_dequant(const uint32_t *wq, const uint16_t *scales,
 static double dot_row(const uint16_t *xrow, const uint32_t *wq,
                       const uint16_t *scales, const uint16_t *biases,
                       int64_t n, int64_t K, int bits, int group) {
-    int64_t wpr = K * bits / 32, gpr = K / group;
+    int64_t wpr = K * code_width(bits) / 32, gpr = K / group;
     double acc = 0.0;
     for (int64_t k = 0; k < K; ++k) {
         double s = orc_bf16_to_f64(scales[n * gpr + k / group]);
         double b = orc_bf16_to_f64(biases[n * gpr + k / group]);
-        double q = (double)code_at(wq, wpr, n, k, bits);
+        double q = code_value(code_at(wq, wpr, n, k, bits), bits);
         double w = s * q + b;
         acc += orc_bf16_to_f64(xrow[k]) * w;
     }
@@ -221,7 +257,7 @@ int orc_moe_gate_up_silu(const uint16_t *x, int64_t M, int64_t topk,
     for (int64_t p = 0; p < M * topk; ++p)
         if (ids[p] < 0 || ids[p] >= E) return ORC_BAD_ARG;
     int64_t I = N2 / 2;
-    int64_t wpr = K * bits / 32, gpr = K / group;
+    int64_t wpr = K * code_width(bits) / 32, gpr = K / group;
     set_threads(nthreads);
 #pragma omp parallel for schedule(static) collapse(2)
     for (int64_t t = 0; t < M; ++t)
@@ -252,7 +288,7 @@ int orc_moe_down_combine(const uint16_t *hin, int64_t M, int64_t topk,
     if (!shape_ok(N, K, bits, group) || M < 0 || topk < 0) return ORC_BAD_ARG;
     for (int64_t p = 0; p < M * topk; ++p)
         if (ids[p] < 0 || ids[p] >= E) return ORC_BAD_ARG;
-    int64_t wpr = K * bits / 32, gpr = K / group;
+    int64_t wpr = K * code_width(bits) / 32, gpr = K / group;
     set_threads(nthreads);
 #pragma omp parallel for schedule(static) collapse(2)
     for (int64_t t = 0; t < M; ++t)
@@ -421,8 +457,8 @@ int orc_sdpa_dequant_v(const uint16_t *q, int64_t B, int64_t Hq, int64_t Lq,
                        const uint16_t *vb, int bits, int group, double scale,
                        int causal, double *out) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq < 0 || D <= 0 ||
-        T < 0 || !bits_ok(bits) || group <= 0 || D % group != 0 ||
-        D % (32 / bits) != 0 || (causal && Lq > T))
+        T < 0 || !bits_ok(bits) || bits == ORC_FP8 || group <= 0 ||
+        D % group != 0 || D % (32 / bits) != 0 || (causal && Lq > T))
         return ORC_BAD_ARG;
     const int64_t rep = Hq / Hkv, wpr = D * bits / 32, gpr = D / group;
     double *p = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
