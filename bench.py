@@ -588,12 +588,14 @@ def run_rope_extra(W, dev, steps, warmup, tokens=(1, 4, 512),
 
 
 def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
-                      formats=((2, 64), (3, 64), (6, 64), (4, 32), (4, 128))):
+                      formats=((2, 64), (3, 64), (6, 64), (4, 32), (4, 128),
+                               (0x108, 64))):
     """The gate+up shape (27648 x 5120, one token, SiLU epilogue) in code
     widths and group sizes outside group 64: u2, u3 and u6 on the
     general-format decode kernel, u4 in groups of 32 and 128 on the
-    one-token chunk kernel; eight back-to-back launches over distinct
-    weights so the timed bytes stream from HBM."""
+    one-token chunk kernel, fp8 (e4m3, bits 0x108) on the general kernel's
+    fp32 form; eight back-to-back launches over distinct weights so the
+    timed bytes stream from HBM."""
     import torch
     import group_wise_affine_gb300 as gwa
     import gwa_synth as synth
@@ -609,10 +611,12 @@ def run_formats_extra(dev, steps, warmup, N=27648, K=5120,
         graph = capture(lambda: [gwa.qmv_gate_up_silu(x, w, h=h) for w in ws])
         total, _ = time_graphs([graph], steps, warmup)
         us = 1e3 * total / (steps * len(ws))
-        byt = proj_bytes(N, K, bits, 1) if group == 64 else (
-            N * K * bits // 8 + N * (K // group) * 4 + K * 2)
+        width = 8 if bits == 0x108 else bits
+        byt = proj_bytes(N, K, width, 1) if group == 64 else (
+            N * K * width // 8 + N * (K // group) * 4 + K * 2)
         gbs = byt / (us * 1e-6) / 1e9
-        res[f"u{bits}_g{group}"] = {"us_per_launch": round(us, 2),
+        name = f"fp8_g{group}" if bits == 0x108 else f"u{bits}_g{group}"
+        res[name] = {"us_per_launch": round(us, 2),
                                      "GB/s": round(gbs, 1),
                                      "frac_of_measured_hbm": round(gbs / peak, 4)}
         del ws

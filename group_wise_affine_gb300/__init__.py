@@ -12,8 +12,9 @@ Names mirror the C entry points without the ``gwa_`` prefix:
 ``workspace_bytes``, ``last_error``,
 ``debug_unpack``, ``debug_dequant``.
 
-Weights: ``wq`` int32 [N, K*bits/32] (the packed uint32 words), ``scales`` and
-``biases`` bfloat16 [N, K/64].  Activations and outputs are bfloat16.
+Weights: ``wq`` int32 [N, K*bits/32] (the packed uint32 words; fp8 weights,
+``bits=GWA_FP8_E4M3``, hold four 8-bit codes a word), ``scales`` and
+``biases`` bfloat16 [N, K/group].  Activations and outputs are bfloat16.
 """
 from __future__ import annotations
 
@@ -36,6 +37,13 @@ GWA_ERR_WORKSPACE = 5
 GWA_NOALLOC_SCRATCH_BYTES = 8 << 20
 GWA_MOE_GATE_UP_SILU = 0
 GWA_MOE_DOWN_COMBINE = 1
+# ``bits`` of fp8 (e4m3) weights: 8-bit E4M3 codes in the affine container
+GWA_FP8_E4M3 = 0x108
+
+
+def code_bits(bits: int) -> int:
+    """Stream bits of one code of a format (fp8: 8)."""
+    return 8 if bits == GWA_FP8_E4M3 else bits
 
 EXPORTS = ("gwa_qmv_affine", "gwa_qmv_fused_sections", "gwa_qmv_gate_up_silu",
            "gwa_workspace_bytes", "gwa_moe_qmv_gather", "gwa_last_error",
@@ -160,7 +168,7 @@ class QWeight:
 def qweight(wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
             bits: int = 4, group: int = 64) -> QWeight:
     N = wq.shape[0]
-    K = wq.shape[-1] * 32 // bits
+    K = wq.shape[-1] * 32 // code_bits(bits)
     return QWeight(wq, scales, biases, N, K, bits, group)
 
 
@@ -210,9 +218,10 @@ def _check_weight(w: QWeight, copies: int = 1) -> None:
     """The library cannot see buffer sizes: refuse tensors whose sizes do not
     match (N, K, bits, group), so a wrong shape raises instead of reading
     past the end of a buffer.  `copies` = number of stacked experts."""
-    if w.bits not in (2, 3, 4, 6, 8) or w.group <= 0 or w.K % w.group:
+    if (w.bits not in (2, 3, 4, 6, 8, GWA_FP8_E4M3) or w.group <= 0
+            or w.K % w.group):
         return                                   # the C ABI reports these
-    words = copies * w.N * w.K * w.bits // 32
+    words = copies * w.N * w.K * code_bits(w.bits) // 32
     groups = copies * w.N * (w.K // w.group)
     if w.wq.dtype != torch.int32 or w.wq.numel() != words:
         raise ValueError(f"wq must be int32 with {words} elements "

@@ -150,10 +150,14 @@ static bool tuned_format(int bits, int group) {
     return (bits == 4 || bits == 8) && group == 64;
 }
 
+static_assert(GWA_FP8_E4M3 == kFp8, "fp8 format tag");
+
 static int check_qweight(const gwa_qweight &w, const char *fn) {
-    if (w.bits != 2 && w.bits != 3 && w.bits != 4 && w.bits != 6 && w.bits != 8)
-        return fail(GWA_ERR_UNSUPPORTED, "%s: bits=%d (supported: 2, 3, 4, 6, 8)",
-                    fn, (int)w.bits);
+    if (w.bits != 2 && w.bits != 3 && w.bits != 4 && w.bits != 6 &&
+        w.bits != 8 && w.bits != GWA_FP8_E4M3)
+        return fail(GWA_ERR_UNSUPPORTED,
+                    "%s: bits=%d (supported: 2, 3, 4, 6, 8, GWA_FP8_E4M3)", fn,
+                    (int)w.bits);
     if (w.group != 32 && w.group != 64 && w.group != 128)
         return fail(GWA_ERR_UNSUPPORTED,
                     "%s: group=%d (supported: 32, 64, 128)", fn, (int)w.group);
@@ -194,7 +198,7 @@ static DenseParams dense_base(const uint16_t *x, int64_t M,
     p.sc = w.scales;
     p.bi = w.biases;
     p.N = w.N;
-    p.nch = (int)(w.K * w.bits / 128);
+    p.nch = (int)(w.K * code_bits(w.bits) / 128);
     p.group = (int)w.group;
     p.G = (int)(w.K / w.group);
     return p;

@@ -10,6 +10,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,6 +31,15 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) {
 }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// The OCP FP8 E4M3 number of the low byte of `code` (fp8 weights): the
+// hardware conversion to fp16, which holds every E4M3 value exactly
+// (subnormals and NaN included), then to fp32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(
+        static_cast<__nv_fp8_storage_t>(code & 0xffu), __NV_E4M3);
+    return __half2float(__half(h));
 }
 
 // 16-byte streaming load of packed weights: read once, keep out of L1.

@@ -1,8 +1,9 @@
 // Test exports: the unpacked integer codes and the fp32 dequantized weights,
 // element by element, so the code layout and the dequantization step can be
 // compared bit for bit with the CPU reference.  Formula: w = scale*q + bias
-// ("saragossa", "Quantization formats": MLX affine integer weights), rounded
-// once to fp32 by a fused multiply-add.
+// ("saragossa", "Quantization formats": MLX affine integer weights; fp8
+// codes stand for their E4M3 numbers), rounded once to fp32 by a fused
+// multiply-add.
 #include "common.cuh"
 #include "internal.h"
 
@@ -13,6 +14,7 @@ namespace gwa {
 // bits of the next; the next word is read only then).
 __device__ __forceinline__ uint32_t row_code(const uint32_t *row, int64_t k,
                                              int bits) {
+    bits = code_bits(bits);
     const int64_t pos = (int64_t)bits * k;
     const int sh = (int)(pos & 31);
     const uint32_t lo = row[pos >> 5];
@@ -25,7 +27,7 @@ __device__ __forceinline__ uint32_t row_code(const uint32_t *row, int64_t k,
 __global__ void debug_unpack_kernel(const uint32_t *__restrict__ wq, int64_t N,
                                     int64_t K, int bits,
                                     uint8_t *__restrict__ codes) {
-    const int64_t wpr = K * bits / 32;
+    const int64_t wpr = K * code_bits(bits) / 32;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N * K;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / K, k = i - n * K;
@@ -38,13 +40,14 @@ __global__ void debug_dequant_kernel(const uint32_t *__restrict__ wq,
                                      const uint16_t *__restrict__ bi, int64_t N,
                                      int64_t K, int group, int bits,
                                      float *__restrict__ wf) {
-    const int64_t wpr = K * bits / 32, G = K / group;
+    const int64_t wpr = K * code_bits(bits) / 32, G = K / group;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N * K;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / K, k = i - n * K;
         const float s = bf16_bits_to_f32(sc[n * G + k / group]);
         const float b = bf16_bits_to_f32(bi[n * G + k / group]);
-        wf[i] = fmaf(s, (float)row_code(wq + n * wpr, k, bits), b);
+        const uint32_t c = row_code(wq + n * wpr, k, bits);
+        wf[i] = fmaf(s, bits == kFp8 ? e4m3_to_f32(c) : (float)c, b);
     }
 }
 

@@ -7,6 +7,13 @@
 
 namespace gwa {
 
+// `bits` of fp8 (e4m3) weights (GWA_FP8_E4M3), and the stream width of a
+// code of any format.
+constexpr int kFp8 = 0x108;
+__host__ __device__ constexpr int code_bits(int bits) {
+    return bits == kFp8 ? 8 : bits;
+}
+
 constexpr int kDenseThreads = 512;
 // Shared-memory budget (bytes) above which staged activations are kept as
 // bf16 instead of fp32.

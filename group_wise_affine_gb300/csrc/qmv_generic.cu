@@ -6,7 +6,9 @@
 // little-endian bit stream, code k at bits [b*k, b*k + b), lowest bits
 // first (field k mod 32/b of word k*b/32 for the widths that divide 32; a
 // u3 or u6 code may straddle two words); one bf16 scale and bias per group;
-// w = scale * q + bias.
+// w = scale * q + bias.  fp8 (e4m3) codes in the same container (bits =
+// GWA_FP8_E4M3, four bytes a word) take the fp32 kernel below with each
+// code's E4M3 value in place of the integer: w = scale * e4m3(q) + bias.
 //
 // One warp per output unit (a row, or a gate/up or rotary pair of rows):
 // the lanes stride over the row in code units -- one word (32/b codes) for
@@ -29,20 +31,22 @@ namespace gwa {
 constexpr int kGenTokens = 4;   // tokens per pass
 constexpr int kGenThreads = 256;
 
-// Words per code unit and codes per unit of a width.
+// Words per code unit and codes per unit of a width (fp8: four words, 16
+// codes, so that a lane's unit is one 16-byte load).
 template <int BITS>
 struct GenUnit {
-    static constexpr int kWords = 32 % BITS == 0 ? 1 : 3;
-    static constexpr int kCodes = 32 * kWords / BITS;
+    static constexpr int kWords = BITS == kFp8 ? 4 : 32 % BITS == 0 ? 1 : 3;
+    static constexpr int kCodes = 32 * kWords / code_bits(BITS);
 };
 
-// Code c of a unit held in w[0 .. kWords): stream bits [BITS*c, +BITS).
+// Code c of a unit held in w[0 .. kWords): stream bits [b*c, +b).
 template <int BITS>
 __device__ __forceinline__ uint32_t unit_code(const uint32_t (&w)[GenUnit<BITS>::kWords],
                                               int c) {
-    const int pos = BITS * c, i = pos >> 5, sh = pos & 31;
-    const uint32_t v = sh + BITS <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1], sh);
-    return v & ((1u << BITS) - 1u);
+    constexpr int B = code_bits(BITS);
+    const int pos = B * c, i = pos >> 5, sh = pos & 31;
+    const uint32_t v = sh + B <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1], sh);
+    return v & ((1u << B) - 1u);
 }
 
 // Warp reduction of the per-lane sums and the epilogue of one output unit:
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(kGenThreads)
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / kWarp;
-    const int64_t wpr = (int64_t)p.K * BITS / 32;  // words per row
+    const int64_t wpr = (int64_t)p.K * code_bits(BITS) / 32;  // words per row
     const int64_t upr = wpr / UW;                  // code units per row
     const int64_t I = p.N / 2;
     const int gshift = __ffs(p.group) - 1;  // groups are 32, 64 or 128
@@ -159,9 +163,13 @@ __global__ void __launch_bounds__(kGenThreads)
                     float wv[CU];
 #pragma unroll
                     for (int c = 0; c < CU; ++c) {
-                        // the code as a float: 2^23 + q minus 2^23 (exact)
-                        const float q = __uint_as_float(
-                            0x4b000000u | unit_code<BITS>(words[q4], c)) - 8388608.0f;
+                        // the code's value as a float: an integer as 2^23 + q
+                        // minus 2^23 (exact), an fp8 code as its E4M3 number
+                        const uint32_t code = unit_code<BITS>(words[q4], c);
+                        const float q = BITS == kFp8
+                                            ? e4m3_to_f32(code)
+                                            : __uint_as_float(0x4b000000u | code) -
+                                                  8388608.0f;
                         wv[c] = fmaf(s, q, b);
                     }
 #pragma unroll
@@ -532,6 +540,8 @@ cudaError_t launch_generic(int mode, const DenseParams &p, cudaStream_t st) {
         case 4: return launch_generic_w<4>(mode, p, st);
         case 6: return launch_generic_w<6>(mode, p, st);
         case 8: return launch_generic_w<8>(mode, p, st);
+        // fp8 codes: fp32 products (an E4M3 value is no integer)
+        case kFp8: return launch_generic_b<kFp8>(mode, p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -145,14 +145,26 @@ def scale_bias(rng: np.random.Generator, N: int, K: int, group: int = GROUP):
     return s, b
 
 
+# `bits` of fp8 (e4m3) weights: 8-bit codes in the same container
+FP8_E4M3 = 0x108
+
+
 def qweight(seed: int, N: int, K: int, bits: int = 4,
             group: int = GROUP) -> QWeight:
-    """A seeded packed weight of N output rows and K inputs."""
-    if K % group or (K * bits) % 32:
+    """A seeded packed weight of N output rows and K inputs.  fp8 weights
+    (bits = FP8_E4M3): uniform random code bytes other than the two NaN
+    codes (0x7f, 0xff become 0x7e, 0xfe), the same scales, biases
+    N(0, 1e-3) (the codes are signed)."""
+    width = 8 if bits == FP8_E4M3 else bits
+    if K % group or (K * width) % 32:
         raise ValueError("K must be a multiple of the group and of 32/bits")
     r = rng_for(seed)
-    wq = packed_words(r, N, K, bits)
+    wq = packed_words(r, N, K, width)
     s, b = scale_bias(r, N, K, group)
+    if bits == FP8_E4M3:
+        by = wq.view(np.uint8)
+        by[(by & 0x7f) == 0x7f] -= 1
+        b = bf16_bits(r.normal(0.0, 1e-3, size=s.shape).astype(np.float32))
     return QWeight(wq, s, b, N, K, bits, group)
 
 
@@ -189,13 +201,18 @@ def device_qweight(seed: int, N: int, K: int, bits: int = 4,
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    wpr = K * bits // 32
+    width = 8 if bits == FP8_E4M3 else bits
+    wpr = K * width // 32
     wq = torch.randint(0, 2**32, (N, wpr), generator=g, device=device,
                        dtype=torch.int64).to(torch.int32)
     G = K // group
     s = (torch.rand((N, G), generator=g, device=device) * 0.015 + 0.005)
     s = s.to(torch.bfloat16)
     noise = torch.randn((N, G), generator=g, device=device) * 1e-3
+    if bits == FP8_E4M3:  # no NaN codes; signed codes, small biases
+        by = wq.view(torch.uint8)
+        by -= ((by & 0x7f) == 0x7f).to(torch.uint8)
+        return wq, s, noise.to(torch.bfloat16)
     b = (-8.0 * s.float() + noise).to(torch.bfloat16)
     return wq, s, b
 
