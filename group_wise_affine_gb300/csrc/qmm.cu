@@ -147,6 +147,27 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 4 consecutive 32-bit columns of this warp's 32 tensor-memory lanes (the
+// 16-token tile's share of one phase).
+__device__ __forceinline__ void tc_ld4(uint32_t taddr, float (&v)[4]) {
+    uint32_t r[4];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <int CW>
+__device__ __forceinline__ void tc_ldn(uint32_t taddr, float (&v)[CW]) {
+    static_assert(CW == 4 || CW == 32, "tensor-memory load width");
+    if constexpr (CW == 4)
+        tc_ld4(taddr, v);
+    else
+        tc_ld32(taddr, v);
+}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
                                             int x, int y, uint64_t *bar) {
     asm volatile(
@@ -658,17 +679,20 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         const bool done = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
         if (done) tc_fence_after();
         const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
+        // columns a phase reads at a time: 32, or its whole share of a
+        // 16-token tile
+        constexpr int CW = NT / 4 < 32 ? NT / 4 : 32;
         if (gate_up) {
             // gate warps (rows 0-63) hand their accumulators to the up
             // warps through the (now idle) activation ring
             float *gbuf = reinterpret_cast<float *>(smem + L::XOFF);
             constexpr int GS = NT + 1;  // padded row stride: no bank conflicts
             if (done && r < 64) {
-                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                    float g[32];
-                    tc_ld32(tmem_d + lane_off + c0, g);
+                for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
+                    float g[CW];
+                    tc_ldn<CW>(tmem_d + lane_off + c0, g);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
+                    for (int j = 0; j < CW; ++j)
                         gbuf[r * GS + c0 + j] = g[j] * rdown * s_tok[c0 + j];
                 }
             }
@@ -676,11 +700,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             if (done && r >= 64) {
                 const int pr = r - 64;
                 const int64_t i = r0 + pr;
-                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                    float u[32];
-                    tc_ld32(tmem_d + lane_off + c0, u);
+                for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
+                    float u[CW];
+                    tc_ldn<CW>(tmem_d + lane_off + c0, u);
                     if (i >= p.I) continue;
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < CW; ++j) {
                         const int64_t m = m0 + c0 + j;
                         if (m >= p.M) break;
                         const float g = gbuf[pr * GS + c0 + j];
@@ -707,11 +731,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                         p.sec_bias[sidx][n - p.sec_start[sidx]]);
             }
             if (done) {
-                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                    float d[32];
-                    tc_ld32(tmem_d + lane_off + c0, d);
+                for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
+                    float d[CW];
+                    tc_ldn<CW>(tmem_d + lane_off + c0, d);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
+                    for (int j = 0; j < CW; ++j)
                         buf[r * GS + c0 + j] = d[j] * rdown * s_tok[c0 + j] + bias;
                 }
             }
@@ -725,17 +749,18 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 const bool rot = n < p.rope_end;
                 const int64_t jj = n - p.sec_start[sidx];
                 const int64_t size = p.sec_start[sidx + 1] - p.sec_start[sidx];
-                for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-                    // 16 (cos, sin) loads in flight together
-                    float2 tv[16];
+                constexpr int RW = NT / 4 < 16 ? NT / 4 : 16;
+                for (int c0 = c_lo; c0 < c_hi; c0 += RW) {
+                    // RW (cos, sin) loads in flight together
+                    float2 tv[RW];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < RW; ++j) {
                         const int64_t m = min(m0 + c0 + j, p.M - 1);
                         tv[j] = rot ? p.rope_cs[m * half + i]
                                     : make_float2(1.0f, 0.0f);
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < RW; ++j) {
                         const int64_t m = m0 + c0 + j;
                         if (m < p.M) {
                             const float own = buf[r * GS + c0 + j];
@@ -751,11 +776,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             int sidx = 0;
             if (p.mode == 1 && n >= 0)
                 while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1]) ++sidx;
-            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                float d[32];
-                tc_ld32(tmem_d + lane_off + c0, d);
+            for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
+                float d[CW];
+                tc_ldn<CW>(tmem_d + lane_off + c0, d);
                 if (n < 0) continue;
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < CW; ++j) {
                     const int64_t m = m0 + c0 + j;
                     if (m >= p.M) break;
                     const float dv = d[j] * rdown * s_tok[c0 + j];
@@ -934,7 +959,13 @@ int qmm_run(const QmmArgs &a, void *workspace, size_t workspace_bytes,
     if (a.M > 0x7fffffffLL)
         return set_error(GWA_ERR_INVALID_ARG, "M too large");
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    const bool wide = a.M > 128;  // 256-token tiles once there are enough
+    // 256-token tiles once there are enough; 16-token tiles for up to 16
+    // tokens (an MMA of N = 16: the tensor pipe does 8 times less padding
+    // work than at 128)
+    if (a.M <= 16)
+        return a.w.bits == 4 ? qmm_launch<4, 16>(a, ws, st)
+                             : qmm_launch<8, 16>(a, ws, st);
+    const bool wide = a.M > 128;
     if (a.w.bits == 4)
         return wide ? qmm_launch<4, 256>(a, ws, st) : qmm_launch<4, 128>(a, ws, st);
     return wide ? qmm_launch<8, 256>(a, ws, st) : qmm_launch<8, 128>(a, ws, st);

@@ -8,6 +8,7 @@ import torch
 import group_wise_affine_gb300 as gwa
 import gwa_synth as synth
 import oracle
+from bars import assert_within, tc_accumulation_bar
 from helpers import bf16_to_f64, dev_bf16, dev_qweight
 
 pytestmark = pytest.mark.gpu
@@ -137,30 +138,8 @@ def scaled_weight(seed, N, K, bits, scale, bias_abs):
 
 
 def assert_close_acc(got, ref, x, w, rows, what=""):
-    """The output bar plus the fp32 accumulation's own rounding.
-
-    Operands reach the tensor cores exactly, but the products are summed in
-    fp32: each of the MMA's K steps (kext/16, twice for u8's two code halves)
-    rounds at most 2^-23 of the magnitude of what it adds up.  The terms
-    summed are x * s(q - c) per input and b' X per group (b' = b + c s, c = 8
-    or 136, X a group sum), all bounded by |x| (|b| + 2 c |s|) per input.
-    Where an output cancels to far below those terms (a large common weight
-    offset, as with u8 biases of -8 s), that rounding is above 1e-2 |y|."""
-    K = w.K
-    G = K // 64
-    c = 8.0 if w.bits == 4 else 136.0
-    s = np.abs(synth.bf16_values(w.scales[rows]).astype(np.float64))
-    b = np.abs(synth.bf16_values(w.biases[rows]).astype(np.float64))
-    per_group = b + 2.0 * c * s                       # [rows, G]
-    per_input = np.repeat(per_group, 64, axis=1)      # [rows, K]
-    xa = np.abs(synth.bf16_values(x).astype(np.float64))
-    mag = xa @ per_input.T
-    kext = K + ((3 * G + 63) // 64) * 64
-    steps = (kext // 16) * (2 if w.bits == 8 else 1)
-    bar = TOL * np.maximum(1.0, np.abs(ref)) + steps * 2.0**-23 * mag
-    err = np.abs(got - ref)
-    worst = float((err / bar).max())
-    assert worst <= 1.0, f"{what}: max |err| {err.max():.3g}, worst err/bar {worst:.3g}"
+    """The output bar plus the fp32 accumulation's own rounding (bars.py)."""
+    assert_within(got, ref, tc_accumulation_bar(ref, x, w, rows), what)
 
 
 # Values far outside fp16's range (2^-14 .. 65504): every token and weight
