@@ -249,8 +249,11 @@ static int run_dense(int mode, DenseParams p, int64_t M, int64_t out_stride,
         bool used = false;
         if (generic) {
             // one token of u4 / u8 codes in groups of 32 or 128: the
-            // chunk-per-lane kernel when the shape allows it
+            // chunk-per-lane kernel when the shape allows it; fp8 codes in
+            // groups of 64: the streaming kernel (fp32 products)
             cudaError_t e = launch_group(mode, q, st, &used);
+            if (e == cudaSuccess && !used && q.bits == kFp8)
+                e = launch_stream(mode, q, st, &used);
             if (e == cudaSuccess && !used) e = launch_generic(mode, q, st);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             continue;

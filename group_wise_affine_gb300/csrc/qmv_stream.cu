@@ -28,6 +28,13 @@
 
 namespace gwa {
 
+// fp8 (e4m3) codes: bytes, like u8.
+template <>
+struct Fmt<kFp8> {
+    static constexpr int kCodesPerWord = 4;
+    static constexpr int kChunkCodes = 16;
+};
+
 static __device__ unsigned int g_stream_timeouts;
 
 // Modes as the host passes them (a plain projection runs as one section).
@@ -53,10 +60,11 @@ struct XRegs {
 
 // Residual plane words of a thread per token and code word: two for u4
 // (the entries of the word's low nibbles' inputs, then of its high ones'),
-// one for u8.  Layout in shared memory: [token][code word][thread], so the
-// threads of a warp read consecutive words.
+// one for u8, none for fp8 (no integer encoding).  Layout in shared memory:
+// [token][code word][thread], so the threads of a warp read consecutive
+// words.
 template <int BITS>
-constexpr int kPlaneWords = BITS == 4 ? 2 : 1;
+constexpr int kPlaneWords = BITS == 4 ? 2 : BITS == 8 ? 1 : 0;
 template <int BITS>
 __device__ __forceinline__ uint2 plane_load(const uint32_t *plane, int pstride,
                                             int m, int wd, int t) {
@@ -79,6 +87,31 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *__restrict__ x,
                                             int t) {
     constexpr int CODES = Fmt<BITS>::kChunkCodes;
     constexpr int CPG = kGroup / CODES;  // lanes sharing a group
+    if constexpr (BITS == kFp8) {
+        // fp8: the raw bf16 pairs (fp32 products, no encoding) and the sum
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            uint4 u[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if (active && m < M) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    x + (int64_t)m * K + (int64_t)c * CODES);
+                u[0] = src[0];
+                u[1] = src[1];
+            }
+            const uint32_t w8[8] = {u[0].x, u[0].y, u[0].z, u[0].w,
+                                    u[1].x, u[1].y, u[1].z, u[1].w};
+            float xs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                xr.pr[m][i] = w8[i];
+                xs += bf16_lo(w8[i]) + bf16_hi(w8[i]);
+            }
+            xr.f[m] = 1.f;
+            xr.mk[m] = false;
+            xr.xs[m] = xs;
+        }
+        return;
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float v[CODES];
@@ -197,6 +230,44 @@ __device__ __forceinline__ void batch_dot(const uint4 (&w)[R],
                                           const float (&b)[R],
                                           const XRegs<BITS, MT> &xr,
                                           float (&out)[R][MT]) {
+    if constexpr (BITS == kFp8) {
+        // each code's E4M3 value (hardware e4m3 -> fp16 pairs) times the raw
+        // bf16 activations, in fp32 (every product exact)
+        float2 a[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) a[r][m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t word = wd == 0   ? w[r].x
+                                      : wd == 1 ? w[r].y
+                                      : wd == 2 ? w[r].z
+                                                : w[r].w;
+                const __half2 h01 = __half2(__nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>(word & 0xffffu), __NV_E4M3));
+                const __half2 h23 = __half2(__nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>(word >> 16), __NV_E4M3));
+                const float2 q01 = __half22float2(h01), q23 = __half22float2(h23);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t x01 = xr.pr[m][2 * wd], x23 = xr.pr[m][2 * wd + 1];
+                    a[r][m] = __ffma2_rn(q01, make_float2(bf16_lo(x01), bf16_hi(x01)),
+                                         a[r][m]);
+                    a[r][m] = __ffma2_rn(q23, make_float2(bf16_lo(x23), bf16_hi(x23)),
+                                         a[r][m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                out[r][m] = fmaf(s[r], a[r][m].x + a[r][m].y, b[r] * xr.xs[m]);
+        return;
+    }
     int d[R][MT][2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -257,6 +328,7 @@ __device__ __forceinline__ void batch_res(const float (&s)[R],
                                        const uint32_t (&offw)[R],
                                        const uint32_t *plane, int pstride,
                                        int t, float (&out)[R][MT]) {
+    if constexpr (BITS == kFp8) return;  // never marked
     constexpr int RB = (BITS == 4 && MT == 2) ? 1 : R;
 #pragma unroll
     for (int r0 = 0; r0 < R; r0 += RB) {
@@ -331,7 +403,7 @@ __global__ void __maxnreg__(MT == 4 ? 128 : 80)
     const int nwh = ncpad / kWarp;         // warps per row group
     const int lane = tid & (kWarp - 1);
     const int ups = rs * UPT;              // units per stage
-    const uint32_t rowbytes = (uint32_t)p.K * BITS / 8;
+    const uint32_t rowbytes = (uint32_t)p.K * code_bits(BITS) / 8;
     const uint32_t sbrow = (uint32_t)p.G * 2;
     const uint32_t rows_stage = (uint32_t)(HALVES * ups);
     const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
@@ -553,7 +625,7 @@ static cudaError_t launch_stream_r(const DenseParams &p, cudaStream_t st,
     constexpr int UPT = RPH / HALVES;
     const int64_t units =
         MODE == kSGateUp ? p.I : MODE == kSRope ? p.N / 2 : p.N;
-    const size_t rowbytes = (size_t)p.K * BITS / 8;
+    const size_t rowbytes = (size_t)p.K * code_bits(BITS) / 8;
     const size_t sbrow = (size_t)p.G * 2;
     const int nwh = (p.nch + kWarp - 1) / kWarp;
     // row groups: aim for about ten consumer warps per CTA
@@ -610,7 +682,7 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
                           bool *used) {
     *used = false;
     if (p.M > 4 || (p.G % 8) != 0 || !aligned16(p.sc) || !aligned16(p.bi) ||
-        !aligned16(p.wq))
+        !aligned16(p.wq) || p.group != kGroup)
         return cudaSuccess;
     const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;
     // A plain projection runs as one section: the same kernel as the fused
@@ -638,6 +710,9 @@ cudaError_t launch_stream(int mode, const DenseParams &p, cudaStream_t st,
     GWA_STREAM_CASE(8, 1)
     GWA_STREAM_CASE(8, 2)
     GWA_STREAM_CASE(8, 4)
+    GWA_STREAM_CASE(kFp8, 1)
+    GWA_STREAM_CASE(kFp8, 2)
+    GWA_STREAM_CASE(kFp8, 4)
 #undef GWA_STREAM_CASE
     return cudaSuccess;
 }
