@@ -47,9 +47,10 @@ constexpr int kSlice = 16;  // lanes per reduction slice
 // an SM's warps are spread over its four schedulers, each with a quarter of
 // the register file (16K), so two CTAs of 11 warps put 6 warps on some
 // scheduler and can use 80 registers a thread at most (88 would need 16896).
-// The u4 loops fit in 80; the u8 ones keep 88 (one CTA of 11 warps per SM
-// with 88, against spills in the loop at 80).
+// The u4 loops fit in 80; the u8 ones keep 88 and take at most 9 warps a
+// CTA instead (two CTAs of 9 warps put 5 on a scheduler: 14080 registers).
 constexpr int kGroupMaxThreads = 352;
+constexpr int kGroupMaxThreadsU8 = 288;
 // Shared memory per CTA: two CTAs (228 KB per SM, 1 KB reserved each).
 constexpr size_t kGroupSmemCap = 110 * 1024;
 
@@ -441,12 +442,19 @@ static cudaError_t launch_group_r(const DenseParams &p, cudaStream_t st,
     const int nchunk = p.K / 64;
     const int slices = (nchunk + kSlice - 1) / kSlice;
     // row groups: as many as fit the thread limit with the producer warp
+    // (a power of two for the rotary mode, whose stages hold whole pairs of
+    // a head)
+    constexpr int kMax = BITS == 8 ? kGroupMaxThreadsU8 : kGroupMaxThreads;
     int rs = 1;
-    while (rs < 8 && 2 * rs * slices * kSlice <= kGroupMaxThreads - kWarp)
-        rs *= 2;
+    if (MODE == kGRope) {
+        while (rs < 8 && 2 * rs * slices * kSlice <= kMax - kWarp) rs *= 2;
+    } else {
+        rs = (kMax - kWarp) / (slices * kSlice);
+        rs = rs < 1 ? 1 : rs > 8 ? 8 : rs;
+    }
     const int ncons = ((rs * slices * kSlice + kWarp - 1) / kWarp) * kWarp;
     const int threads = ncons + kWarp;
-    if (threads > kGroupMaxThreads) return cudaSuccess;  // not used
+    if (threads > kMax) return cudaSuccess;  // not used
     // rope: stages of whole pairs within one head
     if (MODE == kGRope && ((p.rope_hd / 2) % (rs * UPT)) != 0)
         return cudaSuccess;  // not used
