@@ -237,25 +237,28 @@ __device__ __forceinline__ void encode_rows_shared(
 }
 
 // The int8 residual planes of the two-plane path (common.cuh, "marked
-// groups") for an image of one row: all `ncons` threads take the (chunk,
+// groups") for an image of R rows: all `ncons` threads take the (row, chunk,
 // quarter) items in turn, read the quarter's 16 raw bf16 activations from x
-// again (the encoder's pairs kept only their rounded values), and write its
-// residual entries, exact for every chunk, over the first half of the
-// image's pairs: slot group_lo_slot(q, chunk_rot(g)) of chunk g at
-// img + (slot * G + g) * 16.  Entries in dp4a order: per u4 word those of
-// its low nibbles' inputs (x0 x2 x4 x6), then of its high nibbles' (x1 x3
-// x5 x7); per u8 word x0..x3.  The caller brackets this with barriers: the
-// pairs must be in every lane's registers before, and the planes complete
-// after.  Each thread issues the loads of two items before using either
-// (the callers' pairs occupy 32 registers meanwhile).
+// again (row r from x + src(r) * K, src(r) = rowsrc ? rowsrc[r] : r; the
+// encoder's pairs kept only their rounded values), and write its residual
+// entries, exact for every chunk, marked or not: slot group_lo_slot(q,
+// chunk_rot(g)) of chunk g of row r at lo[(r * 4 + slot) * G + g].  Entries
+// in dp4a order: per u4 word those of its low nibbles' inputs (x0 x2 x4 x6),
+// then of its high nibbles' (x1 x3 x5 x7); per u8 word x0..x3.  The caller
+// brackets this with barriers (the planes may overwrite the image's pairs
+// once every lane holds them in registers: lo = the image itself, R = 1).
+// Each thread issues the loads of two items before using either (the
+// callers' pairs occupy 32 registers meanwhile).
 template <int BITS>
 __device__ __forceinline__ void group_plane_store(const uint16_t *__restrict__ x,
-                                                  int G, int tid, int ncons,
-                                                  unsigned char *img) {
+                                                  int K, int R, int G,
+                                                  const int *rowsrc, int tid,
+                                                  int ncons,
+                                                  const unsigned char *img,
+                                                  uint4 *lo) {
     const float *xf = reinterpret_cast<const float *>(
-        reinterpret_cast<const uint4 *>(img) + (size_t)8 * G);
-    uint4 *lo = reinterpret_cast<uint4 *>(img);
-    const int items = 4 * G;
+        reinterpret_cast<const uint4 *>(img) + (size_t)R * 8 * G);
+    const int items = R * 4 * G;
     constexpr int B = 2;
     for (int b0 = tid; b0 < items; b0 += B * ncons) {
         uint4 u[B][2];
@@ -263,7 +266,10 @@ __device__ __forceinline__ void group_plane_store(const uint16_t *__restrict__ x
         for (int j = 0; j < B; ++j) {
             const int it = b0 + j * ncons;
             if (it < items) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(x) + 2 * it;
+                const int r = it / (4 * G), rem = it - r * 4 * G;
+                const int sr = rowsrc ? rowsrc[r] : r;
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                                       x + (int64_t)sr * K) + 2 * rem;
                 u[j][0] = src[0];
                 u[j][1] = src[1];
             }
@@ -272,9 +278,11 @@ __device__ __forceinline__ void group_plane_store(const uint16_t *__restrict__ x
         for (int j = 0; j < B; ++j) {
             const int it = b0 + j * ncons;
             if (it >= items) break;
-            const int g = it >> 2, q = it & 3;
+            const int r = it / (4 * G), rem = it - r * 4 * G;
+            const int g = rem >> 2, q = rem & 3;
             // the pairs' unit: f as stored (u4: 2^E / 16), so 2^-E is
-            const float finv = 1.0f / (BITS == 4 ? 16.0f * xf[g] : xf[g]);
+            const float fs = fabsf(xf[(size_t)r * G + g]);
+            const float finv = 1.0f / (BITS == 4 ? 16.0f * fs : fs);
             uint32_t w4[4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -293,7 +301,7 @@ __device__ __forceinline__ void group_plane_store(const uint16_t *__restrict__ x
                     w4[2 * h + 1] = pack_bytes(e[4], e[5], e[6], e[7]);
                 }
             }
-            lo[(size_t)group_lo_slot<BITS>(q, chunk_rot<BITS>(g)) * G + g] =
+            lo[((size_t)r * 4 + group_lo_slot<BITS>(q, chunk_rot<BITS>(g))) * G + g] =
                 make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
     }

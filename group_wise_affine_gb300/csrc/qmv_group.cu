@@ -103,7 +103,8 @@ __device__ __forceinline__ void group_loop(
     static_assert(!EX || MT == 1, "two-plane path: one token");
     if constexpr (EX) {
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
-        group_plane_store<BITS>(x, nchunk, tid, ncons, xenc);
+        group_plane_store<BITS>(x, K, 1, nchunk, nullptr, tid, ncons, xenc,
+                                reinterpret_cast<uint4 *>(xenc));
         asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
     }
     // the lane's reads of stage row srow(j) = (j / UPT) ups + hg UPT + j % UPT
