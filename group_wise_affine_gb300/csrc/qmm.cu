@@ -11,7 +11,9 @@
 //   s*q + b = 16s*(qh-8) + s*(ql-8) + b',   b' = b + 136s   (u8, q = 16qh+ql)
 //   y[m,n] = sum_k x[m,k] w'[n,k] + sum_g b'[n,g] X[m,g],  X = per-group sum.
 // b' and X are split into fp16 hi + lo parts and the bias term is carried by
-// three extra columns per group (b'hi*Xhi + b'hi*Xlo + b'lo*Xhi).  Activations
+// three extra columns per group (b'hi*Xhi + b'hi*Xlo + b'lo*Xhi), laid out
+// as three sections of G columns (Xhi | Xlo | Xhi against b'hi | b'hi |
+// b'lo), so that 8 groups' columns come from one 16-byte load.  Activations
 // are converted to fp16 once per call by a pre-pass; products are exact and
 // accumulate in fp32 in tensor memory.
 //
@@ -27,14 +29,19 @@
 // below the fp32 rounding of a sum that holds it.
 //
 // Kernel shape.  A CTA computes one 128-row weight tile (for gate+up: 64 gate
-// rows and the matching 64 up rows) against NT = 128 or 256 tokens, one MMA
-// of M = 128, N = NT, K = 16 per 16 columns:
+// rows and the matching 64 up rows) against NT = 16, 128 or 256 tokens, one
+// MMA of M = 128, N = NT, K = 16 per 16 columns.  A K block's activation tile
+// (shared memory) and its A columns (tensor memory) share one ring slot, so
+// the MMA issuer waits on one barrier and commits to one per K block (a
+// lone issuing thread spends far more time on each wait and commit than on
+// an MMA):
 //   warp 0    allocates tensor memory and, from one thread, loads with TMA
-//             per 64-wide K block the activation tile (128-byte swizzle),
-//             the packed code tile of the 128 rows, and per 8 K blocks the
-//             rows' scale and bias tiles, into shared-memory rings;
+//             per 64-wide K block the activation tile (128-byte swizzle);
 //   warp 1    issues tcgen05.mma (A from tensor memory, B from smem);
-//   warps 2-17 dequantize: four warps per tensor-memory lane quarter take
+//   warp 2    loads, from one thread, the packed code tile of the 128 rows
+//             per K block and per 8 K blocks the rows' scale tiles, which run
+//             ahead as far as their own rings allow;
+//   warps 3-18 dequantize: four warps per tensor-memory lane quarter take
 //             every fourth K block, so each has four MMA periods for its
 //             block; a thread turns its row's codes into fp16 pairs and
 //             writes them to tensor memory with tcgen05.st (the A operand),
@@ -54,7 +61,8 @@
 namespace gwa {
 
 constexpr int kQmmDeqWarps = 16;     // four per tensor-memory lane quarter
-constexpr int kQmmThreads = (2 + kQmmDeqWarps) * 32;
+constexpr int kQmmDeq0 = 3;          // first dequantizing warp
+constexpr int kQmmThreads = (kQmmDeq0 + kQmmDeqWarps) * 32;
 constexpr int kQmmRows = 128;        // weight rows per CTA (MMA M)
 constexpr int kQmmSStages = 2;       // scale/bias-tile ring (8 K blocks each)
 constexpr int kStatusBytes = 256;
@@ -231,7 +239,8 @@ __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
 // ------------------------------------------------------------ pre-pass
 // x_ext[m, :] = fp16 activations of token m times 2^e_m (range_scale of the
 // largest |x| and |group sum| of the token) in the dequantizers' k order,
-// then per group g three bias columns (Xhi, Xlo, Xhi) of its scaled sum,
+// then the bias columns of its scaled group sums X: Xhi of every group, then
+// Xlo, then Xhi again (three sections of G columns),
 // then zero padding; tscale[m] = 2^-e_m.  u4 order inside each 8-block:
 // 0 4 1 5 2 6 3 7; u8 inside each 4-block: 0 2 1 3.  A CTA per token, a
 // thread per group: a pass for the scale (a block reduction), a pass (the
@@ -313,10 +322,10 @@ __global__ void __launch_bounds__(128)
             const float Xs = X * up;
             const __half xh = __float2half_rn(Xs);
             const __half xl = __float2half_rn(Xs - __half2float(xh));
-            __half *bc = row + K + 3 * g;
+            __half *bc = row + K + g;
             bc[0] = xh;
-            bc[1] = xl;
-            bc[2] = xh;
+            bc[G] = xl;
+            bc[2 * G] = xh;
         }
         for (int64_t c = K + 3 * G + tid; c < kext; c += blockDim.x)
             row[c] = __float2half_rn(0.f);
@@ -350,8 +359,12 @@ struct QmmParams {
 template <int BITS, int NT>
 struct QmmLayout {
     static constexpr int AW = BITS == 4 ? 32 : 64;  // A columns per K block
-    static constexpr int SA = (512 - NT) / AW > 8 ? 8 : (512 - NT) / AW;
-    static constexpr int XS = NT == 256 ? 4 : 6;      // activation tiles
+    // ring slots: an activation tile and a K block's A columns each; tensor
+    // memory holds NT accumulator columns and the A slots, shared memory the
+    // tiles
+    static constexpr int SA = (512 - NT) / AW;
+    static constexpr int SX = NT == 256 ? 4 : 8;
+    static constexpr int RS = SA < SX ? SA : SX;
     // code tiles; a smaller footprint leaves more of the SM's 256 KB to L1
     // (the bias blocks read scales and biases through it), and above
     // ~180 KB per CTA the kernel ran twice as slow
@@ -360,7 +373,7 @@ struct QmmLayout {
     static constexpr int WBYTES = kQmmRows * BITS * 8;  // 64 codes per row
     static constexpr int SBYTES = kQmmRows * 16;      // 8 bf16 per row
     static constexpr size_t XOFF = 0;
-    static constexpr size_t WOFF = XOFF + (size_t)XS * XBYTES;
+    static constexpr size_t WOFF = XOFF + (size_t)RS * XBYTES;
     static constexpr size_t SOFF = WOFF + (size_t)WS * WBYTES;
     static constexpr size_t BYTES = SOFF + (size_t)kQmmSStages * SBYTES;
     static constexpr size_t SMEM = BYTES + 1024;      // alignment slack
@@ -407,31 +420,41 @@ __device__ __forceinline__ void dequant_row(const uint32_t *w, float s,
 }
 
 // Bias block (K block kb >= G) for row n: column pair c holds bias columns
-// 2c, 2c+1 of the block; bias column j belongs to group j/3 (hi, hi, lo of
-// 2^f_n b', b' = b + 8s or b + 136s; up = 2^f_n).
+// 2c, 2c+1 of the block; bias column j is group j mod G of section j / G,
+// which holds the hi part of 2^f_n b' (sections 0 and 1) or its lo part
+// (section 2), b' = b + 8s or b + 136s, up = 2^f_n.  G is a multiple of 8,
+// so each run of 8 columns is 8 consecutive groups of one section.
 template <int BITS>
 __device__ __forceinline__ void bias_row(const QmmParams &p, int64_t n, int kb,
                                          float up, uint32_t *a) {
     const int base = (kb - p.G) * 64;
     const float k8 = BITS == 4 ? 8.f : 136.f;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        float e[2];
+    for (int c8 = 0; c8 < 8; ++c8) {
+        const int j0 = base + 8 * c8;
+        const int t = j0 / p.G, g0 = j0 - t * p.G;
+        float e[8];
+        if (n >= 0 && t < 3) {
+            const uint4 sv = *reinterpret_cast<const uint4 *>(p.sc + n * p.G + g0);
+            const uint4 bv = *reinterpret_cast<const uint4 *>(p.bi + n * p.G + g0);
+            const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int j = base + 2 * c + hh;
-            const int g = j / 3, which = j - 3 * g;
-            float val = 0.f;
-            if (n >= 0 && g < p.G) {
-                const float s = bf16_bits_to_f32(ld_u16(p.sc + n * p.G + g));
-                const float b = bf16_bits_to_f32(ld_u16(p.bi + n * p.G + g));
-                const float bp = fmaf(k8, s, b) * up;
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t sb = i & 1 ? sw[i >> 1] >> 16 : sw[i >> 1] & 0xffffu;
+                const uint32_t bb = i & 1 ? bw[i >> 1] >> 16 : bw[i >> 1] & 0xffffu;
+                const float bp = fmaf(k8, bf16_bits_to_f32((uint16_t)sb),
+                                      bf16_bits_to_f32((uint16_t)bb)) * up;
                 const float hi = __half2float(__float2half_rn(bp));
-                val = which < 2 ? hi : bp - hi;
+                e[i] = t < 2 ? hi : bp - hi;
             }
-            e[hh] = val;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[i] = 0.f;
         }
-        a[c] = h2_bits(__floats2half2_rn(e[0], e[1]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            a[4 * c8 + i] = h2_bits(__floats2half2_rn(e[2 * i], e[2 * i + 1]));
     }
 }
 
@@ -441,13 +464,15 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                   const __grid_constant__ CUtensorMap wmap,
                   const __grid_constant__ CUtensorMap smap, QmmParams p) {
     using L = QmmLayout<BITS, NT>;
-    constexpr int AW = L::AW, SA = L::SA, XS = L::XS;
+    constexpr int AW = L::AW, RS = L::RS;
     constexpr int WS = L::WS, SS = kQmmSStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t xfull[XS], xempty[XS], wfull[WS], wempty[WS];
-    __shared__ uint64_t sfull[SS], sempty[SS], afull[SA], aempty[SA], dfull;
+    // ready[s]: the slot's activation tile landed and its four dequantizing
+    // warps stored its A columns; done[s]: its MMAs completed
+    __shared__ uint64_t ready[RS], done[RS], wfull[WS], wempty[WS];
+    __shared__ uint64_t sfull[SS], sempty[SS], dfull;
     __shared__ uint32_t s_tmem;
     __shared__ int s_xn, s_wn, s_sn;  // TMA loads issued per ring
     __shared__ float s_rowt[4][kQmmRows];  // per phase: part of a row's range
@@ -461,9 +486,9 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const int G = p.G;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < XS; ++i) {
-            mbar_init(&xfull[i], 1);
-            mbar_init(&xempty[i], 1);
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(&ready[i], 1 + 4);
+            mbar_init(&done[i], 1);
         }
         for (int i = 0; i < WS; ++i) {
             mbar_init(&wfull[i], 1);
@@ -472,10 +497,6 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         for (int i = 0; i < SS; ++i) {
             mbar_init(&sfull[i], 1);
             mbar_init(&sempty[i], kQmmDeqWarps);
-        }
-        for (int i = 0; i < SA; ++i) {
-            mbar_init(&afull[i], 4);
-            mbar_init(&aempty[i], 1);
         }
         mbar_init(&dfull, 1);
         fence_mbar_init();
@@ -495,21 +516,22 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const uint32_t tmem_a = tmem + NT;  // A stages
 
     if (warp == 0) {
-        // -------------------------------------------- TMA loaders
-        // lane 0: activation tiles (paced by the MMA); lane 1: code and
-        // scale tiles, which run ahead as far as their own rings allow
+        // -------------------------------------------- activation loader
         if (lane == 0) {
             for (int kb = 0; kb < p.nkb; ++kb) {
-                const int sx = kb % XS;
-                if (kb >= XS &&
-                    !qmm_wait(&xempty[sx], ((kb / XS) & 1) ^ 1, p.status))
+                const int s = kb % RS;
+                if (kb >= RS &&
+                    !qmm_wait(&done[s], ((kb / RS) & 1) ^ 1, p.status))
                     break;
-                mbar_expect_tx(&xfull[sx], L::XBYTES);
-                tma_load_2d(smem + L::XOFF + (size_t)sx * L::XBYTES, &xmap,
-                            kb * 64, (int)m0, &xfull[sx]);
+                mbar_expect_tx(&ready[s], L::XBYTES);
+                tma_load_2d(smem + L::XOFF + (size_t)s * L::XBYTES, &xmap,
+                            kb * 64, (int)m0, &ready[s]);
                 s_xn = kb + 1;
             }
-        } else if (lane == 1) {
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------- code and scale loader
+        if (lane == 0) {
             const int rows = gate_up ? kQmmRows / 2 : kQmmRows;
             for (int kb = 0; kb < G; ++kb) {
                 if (kb % 8 == 0) {
@@ -546,23 +568,23 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         // -------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = qmm_idesc<NT>();
+            // descriptor of slot 0's tile; a slot, and 16 columns within
+            // it, move the start address (in 16-byte units) only
+            const uint64_t desc0 = smem_desc_sw128(smem_u32(smem + L::XOFF));
             for (int kb = 0; kb < p.nkb; ++kb) {
-                const int sx = kb % XS, sa = kb % SA;
-                if (!qmm_wait(&xfull[sx], (kb / XS) & 1, p.status) ||
-                    !qmm_wait(&afull[sa], (kb / SA) & 1, p.status))
-                    break;
+                const int s = kb % RS;
+                if (!qmm_wait(&ready[s], (kb / RS) & 1, p.status)) break;
                 tc_fence_after();
-                const uint32_t xs = smem_u32(smem + L::XOFF + (size_t)sx * L::XBYTES);
-                const int subs = (BITS == 8 && kb < G) ? 2 : 1;
-                for (int sub = 0; sub < subs; ++sub)
+                const uint64_t bd = desc0 + (uint64_t)(s * (L::XBYTES >> 4));
+                const uint32_t a = tmem_a + s * AW;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a = tmem_a + sa * AW + sub * 32 + kk * 8;
-                        const uint64_t bdesc = smem_desc_sw128(xs + kk * 32);
-                        tc_mma_ts(tmem_d, a, bdesc, idesc, (kb | sub | kk) != 0);
-                    }
-                tc_commit(&xempty[sx]);
-                tc_commit(&aempty[sa]);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
+                if (BITS == 8 && kb < G)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(tmem_d, a + 32 + kk * 8, bd + 2 * kk, idesc, 1u);
+                tc_commit(&done[s]);
             }
             // always signal the epilogue once every issued MMA is done
             tc_commit(&dfull);
@@ -570,7 +592,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     } else {
         // -------------------------------------------- dequantizers
         const int q = warp & 3;               // tensor-memory lane quarter
-        const int ph = (warp - 2) / 4;        // K blocks ph, ph+4, ...
+        const int ph = (warp - kQmmDeq0) / 4;  // K blocks ph, ph+4, ...
         const int r = q * 32 + lane;          // row within the tile
         int64_t n;                            // weight row (-1: none)
         if (gate_up) {
@@ -604,7 +626,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 }
             s_rowt[ph][r] = t;
             // and the tile's token factors
-            const int tix = threadIdx.x - 2 * kWarp;
+            const int tix = threadIdx.x - kQmmDeq0 * kWarp;
             for (int i = tix; i < NT; i += kQmmDeqWarps * kWarp)
                 s_tok[i] = m0 + i < p.M ? p.tscale[m0 + i] : 0.f;
         }
@@ -614,7 +636,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                           fmaxf(s_rowt[2][r], s_rowt[3][r])),
                     rup, rdown);
         for (int kb = ph; kb < p.nkb; kb += 4) {
-            const int sa = kb % SA;
+            const int sa = kb % RS;
             uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
             if (kb < G) {
                 const int ss = (kb / 8) % SS;
@@ -662,8 +684,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     for (int i = 0; i < 32; ++i) lo[i] = 0u;
             }
             // warp-uniform: tcgen05.st below is a warp-collective
-            if (kb >= SA &&
-                !__all_sync(0xffffffffu, qmm_wait(&aempty[sa], ((kb / SA) & 1) ^ 1,
+            if (kb >= RS &&
+                !__all_sync(0xffffffffu, qmm_wait(&done[sa], ((kb / RS) & 1) ^ 1,
                                                   p.status)))
                 break;
             const uint32_t col = tmem_a + sa * AW + lane_off;
@@ -672,12 +694,12 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[sa]);
+            if (lane == 0) mbar_arrive(&ready[sa]);
         }
         // -------------------------------------------- epilogue
         // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
-        const bool done = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
-        if (done) tc_fence_after();
+        const bool fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
+        if (fin) tc_fence_after();
         const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
         // columns a phase reads at a time: 32, or its whole share of a
         // 16-token tile
@@ -687,7 +709,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             // warps through the (now idle) activation ring
             float *gbuf = reinterpret_cast<float *>(smem + L::XOFF);
             constexpr int GS = NT + 1;  // padded row stride: no bank conflicts
-            if (done && r < 64) {
+            if (fin && r < 64) {
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                     float g[CW];
                     tc_ldn<CW>(tmem_d + lane_off + c0, g);
@@ -697,7 +719,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 }
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
-            if (done && r >= 64) {
+            if (fin && r >= 64) {
                 const int pr = r - 64;
                 const int64_t i = r0 + pr;
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
@@ -730,7 +752,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     bias = bf16_bits_to_f32(
                         p.sec_bias[sidx][n - p.sec_start[sidx]]);
             }
-            if (done) {
+            if (fin) {
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                     float d[CW];
                     tc_ldn<CW>(tmem_d + lane_off + c0, d);
@@ -740,7 +762,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 }
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
-            if (done && n >= 0) {
+            if (fin && n >= 0) {
                 const int half = p.rope_hd / 2;
                 const int rr = r % p.rope_hd;
                 const bool first = rr < half;
@@ -772,7 +794,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     }
                 }
             }
-        } else if (done) {
+        } else if (fin) {
             int sidx = 0;
             if (p.mode == 1 && n >= 0)
                 while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1]) ++sidx;
@@ -805,9 +827,15 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) {
         // nothing may still be landing in shared memory or tensor memory:
-        // the last loads of each ring (all complete unless a wait ran out)
-        for (int k = max(0, s_xn - XS); k < s_xn; ++k)
-            if (!mbar_wait(&xfull[k % XS], (k / XS) & 1)) break;
+        // the last loads of each ring (all complete unless a wait ran out).
+        // A slot's ready phase also needs its dequantizers' arrivals, so
+        // after a wait that ran out it may never complete; but the
+        // activation loader issues a tile only once the slot's previous
+        // MMAs are done, so every tile it issued either was consumed or
+        // preceded one of its own waits running out (2 s): by now it has
+        // landed, and a short bounded wait suffices
+        for (int k = max(0, s_xn - RS); k < s_xn; ++k)
+            if (!mbar_wait(&ready[k % RS], (k / RS) & 1, 1000000ull)) break;
         for (int k = max(0, s_wn - WS); k < s_wn; ++k)
             if (!mbar_wait(&wfull[k % WS], (k / WS) & 1)) break;
         for (int k = max(0, s_sn - SS); k < s_sn; ++k)
