@@ -229,10 +229,11 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) {
 }
 
 __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
-                                         unsigned int *status) {
+                                         unsigned int *status, int *fail) {
     if (mbar_wait_sleep(bar, parity)) return true;
     atomicAdd(&g_qmm_timeouts, 1u);
     atomicOr(status, kStTimeout);
+    *fail = 1;
     return false;
 }
 
@@ -240,94 +241,95 @@ __device__ __forceinline__ bool qmm_wait(uint64_t *bar, uint32_t parity,
 // x_ext[m, :] = fp16 activations of token m times 2^e_m (range_scale of the
 // largest |x| and |group sum| of the token) in the dequantizers' k order,
 // then the bias columns of its scaled group sums X: Xhi of every group, then
-// Xlo, then Xhi again (three sections of G columns),
-// then zero padding; tscale[m] = 2^-e_m.  u4 order inside each 8-block:
-// 0 4 1 5 2 6 3 7; u8 inside each 4-block: 0 2 1 3.  A CTA per token, a
-// thread per group: a pass for the scale (a block reduction), a pass (the
-// loads hit the cache) for the conversion.
-__device__ __forceinline__ void load_group64(const uint16_t *src, float (&v)[64]) {
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 u = s4[i];
-        v[8 * i + 0] = bf16_lo(u.x);
-        v[8 * i + 1] = bf16_hi(u.x);
-        v[8 * i + 2] = bf16_lo(u.y);
-        v[8 * i + 3] = bf16_hi(u.y);
-        v[8 * i + 4] = bf16_lo(u.z);
-        v[8 * i + 5] = bf16_hi(u.z);
-        v[8 * i + 6] = bf16_lo(u.w);
-        v[8 * i + 7] = bf16_hi(u.w);
-    }
+// Xlo, then Xhi again (three sections of G columns), then zero padding;
+// tscale[m] = 2^-e_m.  u4 order inside each 8-block: 0 4 1 5 2 6 3 7; u8
+// inside each 4-block: 0 2 1 3.  A CTA per token, a thread per 8 inputs (one
+// 16-byte load; eight lanes make a group, whose sum they form by shuffles):
+// a pass for the scale (a block reduction), a pass (the loads hit the
+// cache) for the conversion.
+constexpr int kPreThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+    v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+    v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+
+// Sum of a group of 64 inputs, eight per lane over eight consecutive lanes
+// (every lane of the warp takes part; the result is the same on all eight).
+__device__ __forceinline__ float group_sum8(const float (&v)[8]) {
+    float X = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    X += __shfl_xor_sync(0xffffffffu, X, 1);
+    X += __shfl_xor_sync(0xffffffffu, X, 2);
+    X += __shfl_xor_sync(0xffffffffu, X, 4);
+    return X;
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kPreThreads)
     qmm_prepass_kernel(const uint16_t *__restrict__ x, int64_t M, int K,
                        int64_t kext, __half *xe, float *tscale) {
-    __shared__ float s_t[4];
-    const int G = K / 64;
+    __shared__ float s_t[kPreThreads / 32];
+    // the projection kernel may start its prologue (it reads weights only
+    // until it waits for this grid)
+    pdl_launch_dependents();
+    const int G = K / 64, C = K / 8;  // groups, 8-input chunks
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
-        const uint16_t *xr = x + m * K;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + m * K);
         float t = 0.f;
-        for (int g = tid; g < G; g += blockDim.x) {
-            float v[64];
-            load_group64(xr + g * 64, v);
-            float X = 0.f, mx = 0.f;
+        for (int c0 = 0; c0 < C; c0 += kPreThreads) {
+            const int c = c0 + tid;
+            float v[8];
+            unpack8(c < C ? xr[c] : make_uint4(0u, 0u, 0u, 0u), v);
+            float mx = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                X += v[i];
-                mx = fmaxf(mx, fabsf(v[i]));
-            }
-            t = fmaxf(t, fmaxf(mx, fabsf(X)));
+            for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
+            t = fmaxf(t, fmaxf(mx, fabsf(group_sum8(v))));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
         if (lane == 0) s_t[warp] = t;
         __syncthreads();
-        t = fmaxf(fmaxf(s_t[0], s_t[1]), fmaxf(s_t[2], s_t[3]));
+        t = s_t[0];
+#pragma unroll
+        for (int w = 1; w < kPreThreads / 32; ++w) t = fmaxf(t, s_t[w]);
         __syncthreads();  // s_t is reused by the next token
         float up, down;
         range_scale(t, up, down);
         if (tid == 0) tscale[m] = down;
         __half *row = xe + m * kext;
-        for (int g = tid; g < G; g += blockDim.x) {
-            float v[64];
-            load_group64(xr + g * 64, v);
-            float X = 0.f;
+        for (int c0 = 0; c0 < C; c0 += kPreThreads) {
+            const int c = c0 + tid;
+            float v[8];
+            unpack8(c < C ? xr[c] : make_uint4(0u, 0u, 0u, 0u), v);
+            const float X = group_sum8(v);
+            if (c >= C) continue;
+            uint32_t o[4];
+            if constexpr (BITS == 4) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) X += v[i];
-            uint32_t o[32];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const float *vb = v + 8 * b;
-                if constexpr (BITS == 4) {
-                    o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0] * up, vb[4] * up));
-                    o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1] * up, vb[5] * up));
-                    o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[2] * up, vb[6] * up));
-                    o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[3] * up, vb[7] * up));
-                } else {
-                    o[4 * b + 0] = h2_bits(__floats2half2_rn(vb[0] * up, vb[2] * up));
-                    o[4 * b + 1] = h2_bits(__floats2half2_rn(vb[1] * up, vb[3] * up));
-                    o[4 * b + 2] = h2_bits(__floats2half2_rn(vb[4] * up, vb[6] * up));
-                    o[4 * b + 3] = h2_bits(__floats2half2_rn(vb[5] * up, vb[7] * up));
-                }
+                for (int i = 0; i < 4; ++i)
+                    o[i] = h2_bits(__floats2half2_rn(v[i] * up, v[i + 4] * up));
+            } else {
+                o[0] = h2_bits(__floats2half2_rn(v[0] * up, v[2] * up));
+                o[1] = h2_bits(__floats2half2_rn(v[1] * up, v[3] * up));
+                o[2] = h2_bits(__floats2half2_rn(v[4] * up, v[6] * up));
+                o[3] = h2_bits(__floats2half2_rn(v[5] * up, v[7] * up));
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(row + g * 64);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-            const float Xs = X * up;
-            const __half xh = __float2half_rn(Xs);
-            const __half xl = __float2half_rn(Xs - __half2float(xh));
-            __half *bc = row + K + g;
-            bc[0] = xh;
-            bc[G] = xl;
-            bc[2 * G] = xh;
+            reinterpret_cast<uint4 *>(row)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            if ((c & 7) == 0) {
+                const int g = c >> 3;
+                const float Xs = X * up;
+                const __half xh = __float2half_rn(Xs);
+                const __half xl = __float2half_rn(Xs - __half2float(xh));
+                row[K + g] = xh;
+                row[K + G + g] = xl;
+                row[K + 2 * G + g] = xh;
+            }
         }
-        for (int64_t c = K + 3 * G + tid; c < kext; c += blockDim.x)
+        for (int64_t c = K + 3 * G + tid; c < kext; c += kPreThreads)
             row[c] = __float2half_rn(0.f);
     }
 }
@@ -475,6 +477,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     __shared__ uint64_t sfull[SS], sempty[SS], dfull;
     __shared__ uint32_t s_tmem;
     __shared__ int s_xn, s_wn, s_sn;  // TMA loads issued per ring
+    __shared__ int s_fail;            // a wait of this CTA ran out
     __shared__ float s_rowt[4][kQmmRows];  // per phase: part of a row's range
     __shared__ float s_tok[NT];            // the tile's tokens' 2^-e_m
 
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         }
         mbar_init(&dfull, 1);
         fence_mbar_init();
-        s_xn = s_wn = s_sn = 0;
+        s_xn = s_wn = s_sn = s_fail = 0;
         const CUtensorMap *maps[3] = {&xmap, &wmap, &smap};
         for (int i = 0; i < 3; ++i)
             asm volatile("prefetch.tensormap [%0];" ::"l"(
@@ -518,10 +521,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     if (warp == 0) {
         // -------------------------------------------- activation loader
         if (lane == 0) {
+            pdl_wait_primary();  // the tiles are the pre-pass's output
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % RS;
                 if (kb >= RS &&
-                    !qmm_wait(&done[s], ((kb / RS) & 1) ^ 1, p.status))
+                    !qmm_wait(&done[s], ((kb / RS) & 1) ^ 1, p.status, &s_fail))
                     break;
                 mbar_expect_tx(&ready[s], L::XBYTES);
                 tma_load_2d(smem + L::XOFF + (size_t)s * L::XBYTES, &xmap,
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     // biases enter through the bias columns)
                     const int sb = kb / 8, s = sb % SS;
                     if (sb >= SS &&
-                        !qmm_wait(&sempty[s], ((sb / SS) & 1) ^ 1, p.status))
+                        !qmm_wait(&sempty[s], ((sb / SS) & 1) ^ 1, p.status, &s_fail))
                         break;
                     unsigned char *ds = smem + L::SOFF + (size_t)s * L::SBYTES;
                     mbar_expect_tx(&sfull[s], L::SBYTES);
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 // packed codes of the tile's rows
                 const int s = kb % WS;
                 if (kb >= WS &&
-                    !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status))
+                    !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status, &s_fail))
                     break;
                 unsigned char *dw = smem + L::WOFF + (size_t)s * L::WBYTES;
                 const int wx = kb * BITS * 2;  // 32-bit words
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             const uint64_t desc0 = smem_desc_sw128(smem_u32(smem + L::XOFF));
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % RS;
-                if (!qmm_wait(&ready[s], (kb / RS) & 1, p.status)) break;
+                if (!qmm_wait(&ready[s], (kb / RS) & 1, p.status, &s_fail)) break;
                 tc_fence_after();
                 const uint64_t bd = desc0 + (uint64_t)(s * (L::XBYTES >> 4));
                 const uint32_t a = tmem_a + s * AW;
@@ -625,10 +629,6 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     }
                 }
             s_rowt[ph][r] = t;
-            // and the tile's token factors
-            const int tix = threadIdx.x - kQmmDeq0 * kWarp;
-            for (int i = tix; i < NT; i += kQmmDeqWarps * kWarp)
-                s_tok[i] = m0 + i < p.M ? p.tscale[m0 + i] : 0.f;
         }
         asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
         float rup, rdown;  // 2^f_n, 2^-f_n
@@ -642,11 +642,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 const int ss = (kb / 8) % SS;
                 if ((kb & 7) == ph &&
                     !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (kb / 8 / SS) & 1,
-                                                      p.status)))
+                                                      p.status, &s_fail)))
                     break;
                 const int sw = kb % WS;
                 if (!__all_sync(0xffffffffu,
-                                qmm_wait(&wfull[sw], (kb / WS) & 1, p.status)))
+                                qmm_wait(&wfull[sw], (kb / WS) & 1, p.status, &s_fail)))
                     break;
                 const uint4 *ws = reinterpret_cast<const uint4 *>(
                     smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             // warp-uniform: tcgen05.st below is a warp-collective
             if (kb >= RS &&
                 !__all_sync(0xffffffffu, qmm_wait(&done[sa], ((kb / RS) & 1) ^ 1,
-                                                  p.status)))
+                                                  p.status, &s_fail)))
                 break;
             const uint32_t col = tmem_a + sa * AW + lane_off;
             tc_st32(col, hi);
@@ -698,8 +698,16 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         }
         // -------------------------------------------- epilogue
         // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
-        const bool fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status));
+        const bool fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status, &s_fail));
         if (fin) tc_fence_after();
+        {
+            // the tile's token factors, the pre-pass's output
+            pdl_wait_primary();
+            const int tix = threadIdx.x - kQmmDeq0 * kWarp;
+            for (int i = tix; i < NT; i += kQmmDeqWarps * kWarp)
+                s_tok[i] = m0 + i < p.M ? p.tscale[m0 + i] : 0.f;
+            asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
+        }
         const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
         // columns a phase reads at a time: 32, or its whole share of a
         // 16-token tile
@@ -825,9 +833,11 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     // ------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // nothing may still be landing in shared memory or tensor memory:
-        // the last loads of each ring (all complete unless a wait ran out).
+    if (threadIdx.x == 0 && s_fail) {
+        // nothing may still be landing in shared memory or tensor memory.
+        // Unless a wait ran out, every load was waited for by its consumer
+        // and the last MMA completed (dfull), so there is nothing to check;
+        // otherwise wait for the last loads of each ring.
         // A slot's ready phase also needs its dequantizers' arrivals, so
         // after a wait that ran out it may never complete; but the
         // activation loader issues a tile only once the slot's previous
@@ -898,10 +908,10 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm status reset: %s",
                          cudaGetErrorString(e));
-    // a CTA of four warps per token (a thread per group of 64 inputs)
+    // a CTA per token (a thread per 8 inputs)
     int64_t pblocks = M;
-    if (pblocks > (int64_t)num_sms() * 16) pblocks = (int64_t)num_sms() * 16;
-    qmm_prepass_kernel<BITS><<<(unsigned)pblocks, 128, 0, st>>>(
+    if (pblocks > (int64_t)num_sms() * 8) pblocks = (int64_t)num_sms() * 8;
+    qmm_prepass_kernel<BITS><<<(unsigned)pblocks, kPreThreads, 0, st>>>(
         a.x, M, (int)K, kext, xe, tscale);
     e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -955,8 +965,21 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     const int64_t rows = gate_up ? p.I : p.N;
     dim3 grid((unsigned)((rows + box_rows - 1) / box_rows),
               (unsigned)((M + NT - 1) / NT));
-    kern<<<grid, kQmmThreads, L::SMEM, st>>>(xmap, wmap, smap, p);
-    e = cudaGetLastError();
+    // programmatic dependent launch: the prologue (barriers, tensor memory,
+    // the rows' ranges from the scales) and the first code tiles overlap
+    // the pre-pass; the kernel waits for it before touching its output
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kQmmThreads);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, xmap, wmap, smap, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm launch: %s", cudaGetErrorString(e));
     return GWA_OK;
