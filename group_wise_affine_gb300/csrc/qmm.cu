@@ -30,11 +30,13 @@
 //
 // Kernel shape.  A CTA computes one 128-row weight tile (for gate+up: 64 gate
 // rows and the matching 64 up rows) against NT = 16, 128 or 256 tokens, one
-// MMA of M = 128, N = NT, K = 16 per 16 columns.  A K block's activation tile
-// (shared memory) and its A columns (tensor memory) share one ring slot, so
-// the MMA issuer waits on one barrier and commits to one per K block (a
-// lone issuing thread spends far more time on each wait and commit than on
-// an MMA):
+// MMA of M = 128, N = NT, K = 16 per 16 columns.  A K block's activation
+// tile (shared memory) and A columns (tensor memory) share one ring slot, so
+// the MMA issuer waits on one barrier and commits to one per K block; for
+// 16 tokens, whose MMAs are short, a slot holds two K blocks (a lone
+// issuing thread spends about as long on a wait or a commit as on an MMA,
+// while at 128 or 256 tokens the coarser slots cost more in pipeline depth
+// than they save):
 //   warp 0    allocates tensor memory and, from one thread, loads with TMA
 //             per 64-wide K block the activation tile (128-byte swizzle);
 //   warp 1    issues tcgen05.mma (A from tensor memory, B from smem);
@@ -72,9 +74,12 @@ constexpr unsigned kStTimeout = 1u;
 
 static __device__ unsigned int g_qmm_timeouts;
 
+// K plus the bias columns, padded to whole pairs of 64-column K blocks (K
+// itself is a multiple of 512), so a ring slot of two K blocks never holds
+// a lone one.
 static int64_t qmm_kext(int64_t K) {
     const int64_t G = K / 64;
-    return K + ((3 * G + 63) / 64) * 64;
+    return K + ((3 * G + 127) / 128) * 128;
 }
 
 // Workspace: status word (256 bytes), the fp16 activations with their bias
@@ -366,7 +371,9 @@ struct QmmLayout {
     // tiles
     static constexpr int SA = (512 - NT) / AW;
     static constexpr int SX = NT == 256 ? 4 : 8;
-    static constexpr int RS = SA < SX ? SA : SX;
+    static constexpr int KP = NT <= 16 ? 2 : 1;          // K blocks per slot
+    static constexpr int RS = (SA < SX ? SA : SX) / KP * KP;  // K blocks
+    static constexpr int RP = RS / KP;                   // slots
     // code tiles; a smaller footprint leaves more of the SM's 256 KB to L1
     // (the bias blocks read scales and biases through it), and above
     // ~180 KB per CTA the kernel ran twice as slow
@@ -466,14 +473,16 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                   const __grid_constant__ CUtensorMap wmap,
                   const __grid_constant__ CUtensorMap smap, QmmParams p) {
     using L = QmmLayout<BITS, NT>;
-    constexpr int AW = L::AW, RS = L::RS;
+    constexpr int AW = L::AW, RS = L::RS, RP = L::RP, KP = L::KP;
     constexpr int WS = L::WS, SS = kQmmSStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    // ready[s]: the slot's activation tile landed and its four dequantizing
-    // warps stored its A columns; done[s]: its MMAs completed
-    __shared__ uint64_t ready[RS], done[RS], wfull[WS], wempty[WS];
+    // ready[s]: the slot's activation tiles landed and the dequantizing warps
+    // (four per K block) stored its A columns; done[s]: its MMAs completed.
+    // K block kb sits in slot (kb / KP) % RP, its tile and A columns at
+    // position kb % RS.
+    __shared__ uint64_t ready[RP], done[RP], wfull[WS], wempty[WS];
     __shared__ uint64_t sfull[SS], sempty[SS], dfull;
     __shared__ uint32_t s_tmem;
     __shared__ int s_xn, s_wn, s_sn;  // TMA loads issued per ring
@@ -489,8 +498,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const int G = p.G;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < RS; ++i) {
-            mbar_init(&ready[i], 1 + 4);
+        for (int i = 0; i < RP; ++i) {
+            mbar_init(&ready[i], 1 + KP * 4);
             mbar_init(&done[i], 1);
         }
         for (int i = 0; i < WS; ++i) {
@@ -522,15 +531,18 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         // -------------------------------------------- activation loader
         if (lane == 0) {
             pdl_wait_primary();  // the tiles are the pre-pass's output
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const int s = kb % RS;
-                if (kb >= RS &&
-                    !qmm_wait(&done[s], ((kb / RS) & 1) ^ 1, p.status, &s_fail))
+            for (int kp = 0; kp < p.nkb / KP; ++kp) {
+                const int s = kp % RP;
+                if (kp >= RP &&
+                    !qmm_wait(&done[s], ((kp / RP) & 1) ^ 1, p.status, &s_fail))
                     break;
-                mbar_expect_tx(&ready[s], L::XBYTES);
-                tma_load_2d(smem + L::XOFF + (size_t)s * L::XBYTES, &xmap,
-                            kb * 64, (int)m0, &ready[s]);
-                s_xn = kb + 1;
+                mbar_expect_tx(&ready[s], KP * L::XBYTES);
+                for (int h = 0; h < KP; ++h) {
+                    const int kb = KP * kp + h;
+                    tma_load_2d(smem + L::XOFF + (size_t)(kb % RS) * L::XBYTES,
+                                &xmap, kb * 64, (int)m0, &ready[s]);
+                }
+                s_xn = KP * kp + KP;
             }
         }
     } else if (warp == 2) {
@@ -575,19 +587,23 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             // descriptor of slot 0's tile; a slot, and 16 columns within
             // it, move the start address (in 16-byte units) only
             const uint64_t desc0 = smem_desc_sw128(smem_u32(smem + L::XOFF));
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const int s = kb % RS;
-                if (!qmm_wait(&ready[s], (kb / RS) & 1, p.status, &s_fail)) break;
+            for (int kp = 0; kp < p.nkb / KP; ++kp) {
+                const int s = kp % RP;
+                if (!qmm_wait(&ready[s], (kp / RP) & 1, p.status, &s_fail)) break;
                 tc_fence_after();
-                const uint64_t bd = desc0 + (uint64_t)(s * (L::XBYTES >> 4));
-                const uint32_t a = tmem_a + s * AW;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
-                if (BITS == 8 && kb < G)
+                for (int h = 0; h < KP; ++h) {
+                    const int kb = KP * kp + h, t = kb % RS;
+                    const uint64_t bd = desc0 + (uint64_t)(t * (L::XBYTES >> 4));
+                    const uint32_t a = tmem_a + t * AW;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(tmem_d, a + 32 + kk * 8, bd + 2 * kk, idesc, 1u);
+                        tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
+                    if (BITS == 8 && kb < G)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_ts(tmem_d, a + 32 + kk * 8, bd + 2 * kk, idesc, 1u);
+                }
                 tc_commit(&done[s]);
             }
             // always signal the epilogue once every issued MMA is done
@@ -636,7 +652,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                           fmaxf(s_rowt[2][r], s_rowt[3][r])),
                     rup, rdown);
         for (int kb = ph; kb < p.nkb; kb += 4) {
-            const int sa = kb % RS;
+            const int sa = kb % RS, kp = kb / KP, sp = kp % RP;
             uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
             if (kb < G) {
                 const int ss = (kb / 8) % SS;
@@ -684,8 +700,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     for (int i = 0; i < 32; ++i) lo[i] = 0u;
             }
             // warp-uniform: tcgen05.st below is a warp-collective
-            if (kb >= RS &&
-                !__all_sync(0xffffffffu, qmm_wait(&done[sa], ((kb / RS) & 1) ^ 1,
+            if (kp >= RP &&
+                !__all_sync(0xffffffffu, qmm_wait(&done[sp], ((kp / RP) & 1) ^ 1,
                                                   p.status, &s_fail)))
                 break;
             const uint32_t col = tmem_a + sa * AW + lane_off;
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ready[sa]);
+            if (lane == 0) mbar_arrive(&ready[sp]);
         }
         // -------------------------------------------- epilogue
         // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
@@ -844,8 +860,9 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         // MMAs are done, so every tile it issued either was consumed or
         // preceded one of its own waits running out (2 s): by now it has
         // landed, and a short bounded wait suffices
-        for (int k = max(0, s_xn - RS); k < s_xn; ++k)
-            if (!mbar_wait(&ready[k % RS], (k / RS) & 1, 1000000ull)) break;
+        for (int k = max(0, s_xn - RS); k < s_xn; k += KP)
+            if (!mbar_wait(&ready[(k / KP) % RP], ((k / KP) / RP) & 1, 1000000ull))
+                break;
         for (int k = max(0, s_wn - WS); k < s_wn; ++k)
             if (!mbar_wait(&wfull[k % WS], (k / WS) & 1)) break;
         for (int k = max(0, s_sn - SS); k < s_sn; ++k)
