@@ -587,24 +587,37 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             // descriptor of slot 0's tile; a slot, and 16 columns within
             // it, move the start address (in 16-byte units) only
             const uint64_t desc0 = smem_desc_sw128(smem_u32(smem + L::XOFF));
-            for (int kp = 0; kp < p.nkb / KP; ++kp) {
-                const int s = kp % RP;
-                if (!qmm_wait(&ready[s], (kp / RP) & 1, p.status, &s_fail)) break;
-                tc_fence_after();
+            // unrolled over the ring's slots, so that a slot's barriers,
+            // tiles and A columns are constants (the lone issuing thread's
+            // instructions are the loop's cost)
+            const int nkp = p.nkb / KP;
+            bool ok = true;
+            for (int base = 0; ok && base < nkp; base += RP) {
+                const uint32_t par = (base / RP) & 1;
 #pragma unroll
-                for (int h = 0; h < KP; ++h) {
-                    const int kb = KP * kp + h, t = kb % RS;
-                    const uint64_t bd = desc0 + (uint64_t)(t * (L::XBYTES >> 4));
-                    const uint32_t a = tmem_a + t * AW;
+                for (int s = 0; s < RP; ++s) {
+                    const int kp = base + s;
+                    if (kp >= nkp) break;
+                    if (!qmm_wait(&ready[s], par, p.status, &s_fail)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
-                    if (BITS == 8 && kb < G)
+                    for (int h = 0; h < KP; ++h) {
+                        const int kb = KP * kp + h, t = KP * s + h;  // t = kb % RS
+                        const uint64_t bd = desc0 + (uint64_t)(t * (L::XBYTES >> 4));
+                        const uint32_t a = tmem_a + t * AW;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_ts(tmem_d, a + 32 + kk * 8, bd + 2 * kk, idesc, 1u);
+                            tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
+                        if (BITS == 8 && kb < G)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma_ts(tmem_d, a + 32 + kk * 8, bd + 2 * kk, idesc, 1u);
+                    }
+                    tc_commit(&done[s]);
                 }
-                tc_commit(&done[s]);
             }
             // always signal the epilogue once every issued MMA is done
             tc_commit(&dfull);
