@@ -31,4 +31,22 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local,
     return v;
 }
 
+// N fp32 values at local + j * stride (j < N), same offsets, in CTA `rank`
+// of the cluster: one address mapping, then all N loads issued before any
+// is used (each remote load's latency is long).
+template <int N>
+__device__ __forceinline__ void ld_cluster_f32_n(const float *local, uint32_t rank,
+                                                 uint32_t stride, float (&v)[N]) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(a)
+                 : "r"(smem_u32(local)), "r"(rank));
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(v[j])
+                     : "r"(a + (uint32_t)j * stride * 4u)
+                     : "memory");
+}
+
 }  // namespace gwa

@@ -55,8 +55,11 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "qmm.h"
 
@@ -67,6 +70,7 @@ constexpr int kQmmDeq0 = 3;          // first dequantizing warp
 constexpr int kQmmThreads = (kQmmDeq0 + kQmmDeqWarps) * 32;
 constexpr int kQmmRows = 128;        // weight rows per CTA (MMA M)
 constexpr int kQmmSStages = 2;       // scale/bias-tile ring (8 K blocks each)
+constexpr int kQmmMaxSplit = 4;      // CTAs per cluster splitting K
 constexpr int kStatusBytes = 256;
 
 // status word bit: a pipeline wait ran out
@@ -360,6 +364,7 @@ struct QmmParams {
     const float2 *rope_cs;
     const float *tscale;  // [M]: 2^-e_m of each token (pre-pass)
     unsigned int *status;
+    int ks;               // CTAs per cluster splitting a tile's K blocks
 };
 
 // Shared-memory layout (1024-byte aligned regions).
@@ -467,7 +472,9 @@ __device__ __forceinline__ void bias_row(const QmmParams &p, int64_t n, int kb,
     }
 }
 
-template <int BITS, int NT>
+// SPLIT: launched in clusters that split each tile's K blocks (p.ks CTAs);
+// without it the split's code compiles away.
+template <int BITS, int NT, bool SPLIT>
 __global__ void __launch_bounds__(kQmmThreads, 1)
     qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ CUtensorMap wmap,
@@ -493,8 +500,21 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.y * NT;
     const bool gate_up = p.mode == 2;
+    // K split: the ks CTAs of a cluster share a tile, rank j taking K blocks
+    // [kb0, kb1) (whole runs of 8, so a scale tile never straddles two
+    // CTAs); rank 0 adds the others' partial sums and writes the outputs
+    const int ks = SPLIT ? p.ks : 1;
+    const int rank = SPLIT ? (int)cluster_rank() : 0;
+    const int tile = SPLIT ? (int)blockIdx.x / ks : (int)blockIdx.x;
+    int kb0 = 0, kb1 = p.nkb;
+    if (SPLIT) {
+        const int n8 = (p.nkb + 7) / 8;
+        kb0 = min(p.nkb, rank * n8 / ks * 8);
+        kb1 = min(p.nkb, (rank + 1) * n8 / ks * 8);
+    }
+    const int nb = kb1 - kb0;  // this CTA's K blocks (an even count)
     // first row of the tile (gate+up: first gate/up pair)
-    const int64_t r0 = (int64_t)blockIdx.x * (gate_up ? kQmmRows / 2 : kQmmRows);
+    const int64_t r0 = (int64_t)tile * (gate_up ? kQmmRows / 2 : kQmmRows);
     const int G = p.G;
 
     if (threadIdx.x == 0) {
@@ -527,20 +547,35 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
     const uint32_t tmem_d = tmem;       // accumulators: cols [0, NT)
     const uint32_t tmem_a = tmem + NT;  // A stages
 
+    // a dequantizing thread's row (the other warps do not use these)
+    const int q = warp & 3;                // tensor-memory lane quarter
+    const int ph = (warp - kQmmDeq0) / 4;  // local K blocks ph, ph+4, ...
+    const int r = q * 32 + lane;           // row within the tile
+    int64_t n;                             // weight row (-1: none)
+    if (gate_up) {
+        const int64_t i = r0 + (r & 63);
+        n = i < p.I ? (r < 64 ? i : p.I + i) : -1;
+    } else {
+        n = r0 + r < p.N ? r0 + r : -1;
+    }
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    float rup = 1.f, rdown = 1.f;  // 2^f_n, 2^-f_n
+    bool fin = false;              // the accumulators are complete
+
     if (warp == 0) {
         // -------------------------------------------- activation loader
         if (lane == 0) {
             pdl_wait_primary();  // the tiles are the pre-pass's output
-            for (int kp = 0; kp < p.nkb / KP; ++kp) {
+            for (int kp = 0; kp < nb / KP; ++kp) {
                 const int s = kp % RP;
                 if (kp >= RP &&
                     !qmm_wait(&done[s], ((kp / RP) & 1) ^ 1, p.status, &s_fail))
                     break;
                 mbar_expect_tx(&ready[s], KP * L::XBYTES);
                 for (int h = 0; h < KP; ++h) {
-                    const int kb = KP * kp + h;
-                    tma_load_2d(smem + L::XOFF + (size_t)(kb % RS) * L::XBYTES,
-                                &xmap, kb * 64, (int)m0, &ready[s]);
+                    const int lb = KP * kp + h;  // local K block
+                    tma_load_2d(smem + L::XOFF + (size_t)(lb % RS) * L::XBYTES,
+                                &xmap, (kb0 + lb) * 64, (int)m0, &ready[s]);
                 }
                 s_xn = KP * kp + KP;
             }
@@ -549,11 +584,12 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         // -------------------------------------------- code and scale loader
         if (lane == 0) {
             const int rows = gate_up ? kQmmRows / 2 : kQmmRows;
-            for (int kb = 0; kb < G; ++kb) {
+            for (int kb = kb0; kb < min(kb1, G); ++kb) {
+                const int lb = kb - kb0;  // local K block
                 if (kb % 8 == 0) {
                     // scale tiles of K blocks kb .. kb+7 (the code blocks'
                     // biases enter through the bias columns)
-                    const int sb = kb / 8, s = sb % SS;
+                    const int sb = lb / 8, s = sb % SS;
                     if (sb >= SS &&
                         !qmm_wait(&sempty[s], ((sb / SS) & 1) ^ 1, p.status, &s_fail))
                         break;
@@ -566,9 +602,9 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     s_sn = sb + 1;
                 }
                 // packed codes of the tile's rows
-                const int s = kb % WS;
-                if (kb >= WS &&
-                    !qmm_wait(&wempty[s], ((kb / WS) & 1) ^ 1, p.status, &s_fail))
+                const int s = lb % WS;
+                if (lb >= WS &&
+                    !qmm_wait(&wempty[s], ((lb / WS) & 1) ^ 1, p.status, &s_fail))
                     break;
                 unsigned char *dw = smem + L::WOFF + (size_t)s * L::WBYTES;
                 const int wx = kb * BITS * 2;  // 32-bit words
@@ -577,7 +613,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 if (gate_up)
                     tma_load_2d(dw + rows * BITS * 8, &wmap, wx, (int)(p.I + r0),
                                 &wfull[s]);
-                s_wn = kb + 1;
+                s_wn = lb + 1;
             }
         }
     } else if (warp == 1) {
@@ -590,7 +626,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             // unrolled over the ring's slots, so that a slot's barriers,
             // tiles and A columns are constants (the lone issuing thread's
             // instructions are the loop's cost)
-            const int nkp = p.nkb / KP;
+            const int nkp = nb / KP;
             bool ok = true;
             for (int base = 0; ok && base < nkp; base += RP) {
                 const uint32_t par = (base / RP) & 1;
@@ -605,12 +641,13 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int h = 0; h < KP; ++h) {
-                        const int kb = KP * kp + h, t = KP * s + h;  // t = kb % RS
+                        // local K block lb, at position t = lb % RS
+                        const int lb = KP * kp + h, kb = kb0 + lb, t = KP * s + h;
                         const uint64_t bd = desc0 + (uint64_t)(t * (L::XBYTES >> 4));
                         const uint32_t a = tmem_a + t * AW;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, kb | kk);
+                            tc_mma_ts(tmem_d, a + kk * 8, bd + 2 * kk, idesc, lb | kk);
                         if (BITS == 8 && kb < G)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -624,17 +661,6 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         }
     } else {
         // -------------------------------------------- dequantizers
-        const int q = warp & 3;               // tensor-memory lane quarter
-        const int ph = (warp - kQmmDeq0) / 4;  // K blocks ph, ph+4, ...
-        const int r = q * 32 + lane;          // row within the tile
-        int64_t n;                            // weight row (-1: none)
-        if (gate_up) {
-            const int64_t i = r0 + (r & 63);
-            n = i < p.I ? (r < 64 ? i : p.I + i) : -1;
-        } else {
-            n = r0 + r < p.N ? r0 + r : -1;
-        }
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         // The row's range (see the file comment): the largest |s| * 8 (u4)
         // or 128 (u8) and |b'| over its groups, the four phases' threads of
         // a row taking every fourth 8-group piece of its scales and biases.
@@ -660,22 +686,22 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             s_rowt[ph][r] = t;
         }
         asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
-        float rup, rdown;  // 2^f_n, 2^-f_n
         range_scale(fmaxf(fmaxf(s_rowt[0][r], s_rowt[1][r]),
                           fmaxf(s_rowt[2][r], s_rowt[3][r])),
                     rup, rdown);
-        for (int kb = ph; kb < p.nkb; kb += 4) {
-            const int sa = kb % RS, kp = kb / KP, sp = kp % RP;
+        for (int lb = ph; lb < nb; lb += 4) {  // local K blocks
+            const int kb = kb0 + lb;
+            const int sa = lb % RS, kp = lb / KP, sp = kp % RP;
             uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
             if (kb < G) {
-                const int ss = (kb / 8) % SS;
+                const int ss = (lb / 8) % SS;
                 if ((kb & 7) == ph &&
-                    !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (kb / 8 / SS) & 1,
+                    !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (lb / 8 / SS) & 1,
                                                       p.status, &s_fail)))
                     break;
-                const int sw = kb % WS;
+                const int sw = lb % WS;
                 if (!__all_sync(0xffffffffu,
-                                qmm_wait(&wfull[sw], (kb / WS) & 1, p.status, &s_fail)))
+                                qmm_wait(&wfull[sw], (lb / WS) & 1, p.status, &s_fail)))
                     break;
                 const uint4 *ws = reinterpret_cast<const uint4 *>(
                     smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
@@ -725,9 +751,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ready[sp]);
         }
-        // -------------------------------------------- epilogue
-        // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
-        const bool fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status, &s_fail));
+        // all MMAs done
+        fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status, &s_fail));
         if (fin) tc_fence_after();
         {
             // the tile's token factors, the pre-pass's output
@@ -737,10 +762,44 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 s_tok[i] = m0 + i < p.M ? p.tscale[m0 + i] : 0.f;
             asm volatile("bar.sync 2, %0;" ::"r"(kQmmDeqWarps * kWarp) : "memory");
         }
+        if (SPLIT && rank > 0 && fin) {
+            // this CTA's partial sums, for rank 0 to add: red[c][r] (fp32)
+            float *red = reinterpret_cast<float *>(smem + L::XOFF);
+            static_assert((size_t)NT * kQmmRows * 4 <= (size_t)L::RS * L::XBYTES,
+                          "the partial sums must fit in the activation ring");
+            constexpr int CW = NT / 4 < 32 ? NT / 4 : 32;
+            for (int c0 = ph * (NT / 4); c0 < (ph + 1) * (NT / 4); c0 += CW) {
+                float d[CW];
+                tc_ldn<CW>(tmem_d + lane_off + c0, d);
+#pragma unroll
+                for (int j = 0; j < CW; ++j) red[(c0 + j) * kQmmRows + r] = d[j];
+            }
+        }
+    }
+    // every thread of the cluster: the partial sums are in place
+    if (SPLIT) cluster_sync_all();
+    if (warp >= kQmmDeq0 && rank == 0) {
+        // -------------------------------------------- epilogue
+        // accumulators are 2^(f_n + e_m) times the outputs: d * 2^-f_n * 2^-e_m
         const int c_lo = ph * (NT / 4), c_hi = c_lo + NT / 4;
         // columns a phase reads at a time: 32, or its whole share of a
         // 16-token tile
         constexpr int CW = NT / 4 < 32 ? NT / 4 : 32;
+        // this CTA's accumulators plus, under a K split, the other ranks'
+        // partial sums (distributed shared memory)
+        auto load_acc = [&](int c0, float (&v)[CW]) {
+            tc_ldn<CW>(tmem_d + lane_off + c0, v);
+            if (SPLIT) {
+                const float *red = reinterpret_cast<const float *>(smem + L::XOFF);
+                for (int j2 = 1; j2 < ks; ++j2) {
+                    float t[CW];
+                    ld_cluster_f32_n<CW>(red + c0 * kQmmRows + r, (uint32_t)j2,
+                                         kQmmRows, t);
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) v[j] += t[j];
+                }
+            }
+        };
         if (gate_up) {
             // gate warps (rows 0-63) hand their accumulators to the up
             // warps through the (now idle) activation ring
@@ -749,7 +808,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             if (fin && r < 64) {
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                     float g[CW];
-                    tc_ldn<CW>(tmem_d + lane_off + c0, g);
+                    load_acc(c0, g);
 #pragma unroll
                     for (int j = 0; j < CW; ++j)
                         gbuf[r * GS + c0 + j] = g[j] * rdown * s_tok[c0 + j];
@@ -761,7 +820,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 const int64_t i = r0 + pr;
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                     float u[CW];
-                    tc_ldn<CW>(tmem_d + lane_off + c0, u);
+                    load_acc(c0, u);
                     if (i >= p.I) continue;
                     for (int j = 0; j < CW; ++j) {
                         const int64_t m = m0 + c0 + j;
@@ -792,7 +851,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             if (fin) {
                 for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                     float d[CW];
-                    tc_ldn<CW>(tmem_d + lane_off + c0, d);
+                    load_acc(c0, d);
 #pragma unroll
                     for (int j = 0; j < CW; ++j)
                         buf[r * GS + c0 + j] = d[j] * rdown * s_tok[c0 + j] + bias;
@@ -837,7 +896,7 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                 while (sidx + 1 < p.nsec && n >= p.sec_start[sidx + 1]) ++sidx;
             for (int c0 = c_lo; c0 < c_hi; c0 += CW) {
                 float d[CW];
-                tc_ldn<CW>(tmem_d + lane_off + c0, d);
+                load_acc(c0, d);
                 if (n < 0) continue;
                 for (int j = 0; j < CW; ++j) {
                     const int64_t m = m0 + c0 + j;
@@ -858,6 +917,8 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             }
         }
     }
+    // the other ranks keep their shared memory until rank 0 has read it
+    if (SPLIT) cluster_sync_all();
 
     // ------------------------------------------------ teardown
     tc_fence_before();
@@ -925,6 +986,40 @@ static int encode_2d(CUtensorMap *map, CUtensorMapDataType type, int esize,
     return GWA_OK;
 }
 
+// Clusters of `cl` CTAs of `kern` that the GPU keeps resident at once (0:
+// none), cached per device, kernel, cluster size and shared memory.
+static int qmm_resident_clusters(const void *kern, int cl, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, kern, cl, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
+    cfg.blockDim = dim3(kQmmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
 template <int BITS, int NT>
 static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     using L = QmmLayout<BITS, NT>;
@@ -986,15 +1081,35 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     p.tscale = tscale;
     p.status = status;
 
-    auto kern = qmm_tc_kernel<BITS, NT>;
-    int dummy = 0;
+    auto kern = qmm_tc_kernel<BITS, NT, false>;
+    auto kern_split = qmm_tc_kernel<BITS, NT, true>;
+    int resident = 0;
     e = occupancy_grid(reinterpret_cast<const void *>(kern), kQmmThreads,
-                       L::SMEM, &dummy);
+                       L::SMEM, &resident);
+    if (e == cudaSuccess)
+        e = occupancy_grid(reinterpret_cast<const void *>(kern_split), kQmmThreads,
+                           L::SMEM, &resident);
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm setup: %s", cudaGetErrorString(e));
     const int64_t rows = gate_up ? p.I : p.N;
-    dim3 grid((unsigned)((rows + box_rows - 1) / box_rows),
-              (unsigned)((M + NT - 1) / NT));
+    const int64_t row_tiles = (rows + box_rows - 1) / box_rows;
+    const int64_t tiles = row_tiles * ((M + NT - 1) / NT);
+    // K split over a cluster of ks CTAs when the tiles leave SMs idle: the
+    // largest ks whose clusters all fit in one wave, each CTA taking 1/ks of
+    // a tile's K blocks.  (Splits that need a second wave of clusters lost:
+    // each CTA also pays the prologue, the partial sums' exchange and, on
+    // rank 0, the epilogue; at 512 tokens a 3-way split of 80 tiles took
+    // o_proj from 40 to 57 us.)
+    p.ks = 1;
+    if (tiles < resident) {
+        const int n8 = (p.nkb + 7) / 8;
+        for (int ks = 2; ks <= kQmmMaxSplit && n8 >= 2 * ks; ++ks) {
+            const int cap = qmm_resident_clusters(
+                reinterpret_cast<const void *>(kern_split), ks, L::SMEM);
+            if (cap >= tiles) p.ks = ks;
+        }
+    }
+    dim3 grid((unsigned)(row_tiles * p.ks), (unsigned)((M + NT - 1) / NT));
     // programmatic dependent launch: the prologue (barriers, tensor memory,
     // the rows' ranges from the scales) and the first code tiles overlap
     // the pre-pass; the kernel waits for it before touching its output
@@ -1003,12 +1118,17 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     cfg.blockDim = dim3(kQmmThreads);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, xmap, wmap, smap, p);
+    cfg.numAttrs = p.ks > 1 ? 2 : 1;
+    e = p.ks > 1 ? cudaLaunchKernelEx(&cfg, kern_split, xmap, wmap, smap, p)
+                 : cudaLaunchKernelEx(&cfg, kern, xmap, wmap, smap, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
         return set_error(GWA_ERR_CUDA, "qmm launch: %s", cudaGetErrorString(e));
