@@ -522,9 +522,10 @@ constexpr int kMmaMaxSplit = 4;  // CTAs per cluster along K
 // Rows of up to 5120 inputs run on one CTA each; longer rows of a plain
 // u8 projection on a cluster of KS CTAs along K, the smallest KS for which
 // K / KS is a multiple of 512 and at most 5120.  (For u4 the cluster kernel
-// is faster on its own, 27.9 against 39.8 us for the 13824-input down
+// is faster on its own, 28.4 against 40.6 us for the 13824-input down
 // projection at 8 tokens, but in a layer's kernel sequence the two 4-token
-// streaming passes finish the layer sooner; for u8 the split wins both
+// streaming passes finish the layer sooner: the 48-layer stack takes 4.79
+// ms with them and 4.99 ms with the split; for u8 the split wins both
 // ways.)  *used tells the caller whether it ran.
 cudaError_t launch_mma(int mode, const DenseParams &p, cudaStream_t st, bool *used) {
     *used = false;
