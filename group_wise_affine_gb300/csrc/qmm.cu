@@ -689,60 +689,16 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
         range_scale(fmaxf(fmaxf(s_rowt[0][r], s_rowt[1][r]),
                           fmaxf(s_rowt[2][r], s_rowt[3][r])),
                     rup, rdown);
-        for (int lb = ph; lb < nb; lb += 4) {  // local K blocks
-            const int kb = kb0 + lb;
+        // The block's A columns into its ring slot, once its previous MMAs
+        // are done (false: a wait ran out).
+        auto store_a = [&](int lb, const uint32_t (&hi)[32],
+                           const uint32_t (&lo)[BITS == 8 ? 32 : 1]) {
             const int sa = lb % RS, kp = lb / KP, sp = kp % RP;
-            uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
-            if (kb < G) {
-                const int ss = (lb / 8) % SS;
-                if ((kb & 7) == ph &&
-                    !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (lb / 8 / SS) & 1,
-                                                      p.status, &s_fail)))
-                    break;
-                const int sw = lb % WS;
-                if (!__all_sync(0xffffffffu,
-                                qmm_wait(&wfull[sw], (lb / WS) & 1, p.status, &s_fail)))
-                    break;
-                const uint4 *ws = reinterpret_cast<const uint4 *>(
-                    smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
-                uint32_t w[BITS * 2];
-                if constexpr (BITS == 4) {
-                    // rows 128 bytes apart read their two 16-byte chunks in
-                    // opposite order (different banks in one instruction)
-                    const bool rot = (r >> 2) & 1;
-                    const uint4 c0 = ws[rot ? 1 : 0], c1 = ws[rot ? 0 : 1];
-                    const uint4 lo4 = rot ? c1 : c0, hi4 = rot ? c0 : c1;
-                    w[0] = lo4.x; w[1] = lo4.y; w[2] = lo4.z; w[3] = lo4.w;
-                    w[4] = hi4.x; w[5] = hi4.y; w[6] = hi4.z; w[7] = hi4.w;
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 c = ws[v];
-                        w[4 * v] = c.x; w[4 * v + 1] = c.y;
-                        w[4 * v + 2] = c.z; w[4 * v + 3] = c.w;
-                    }
-                }
-                const uint16_t *st = reinterpret_cast<const uint16_t *>(
-                    smem + L::SOFF + (size_t)ss * L::SBYTES);
-                const float s = bf16_bits_to_f32(st[r * 8 + (kb & 7)]) * rup;
-                // the codes and scale of this block are in registers
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&wempty[sw]);
-                    if ((kb & 7) == 4 + ph || kb == G - 1) mbar_arrive(&sempty[ss]);
-                }
-                dequant_row<BITS>(w, s, hi, lo);
-            } else {
-                bias_row<BITS>(p, n, kb, rup, hi);
-                if constexpr (BITS == 8)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) lo[i] = 0u;
-            }
             // warp-uniform: tcgen05.st below is a warp-collective
             if (kp >= RP &&
                 !__all_sync(0xffffffffu, qmm_wait(&done[sp], ((kp / RP) & 1) ^ 1,
                                                   p.status, &s_fail)))
-                break;
+                return false;
             const uint32_t col = tmem_a + sa * AW + lane_off;
             tc_st32(col, hi);
             if constexpr (BITS == 8) tc_st32(col + 32, lo);
@@ -750,6 +706,66 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ready[sp]);
+            return true;
+        };
+        // code blocks, then bias blocks (two loops keep the bias columns'
+        // code out of the hot loop); local K blocks ph, ph + 4, ...
+        int lb = ph;
+        bool ok = true;
+        for (; ok && lb < nb && kb0 + lb < G; lb += 4) {
+            const int kb = kb0 + lb;
+            uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
+            const int ss = (lb / 8) % SS;
+            if ((kb & 7) == ph &&
+                !__all_sync(0xffffffffu, qmm_wait(&sfull[ss], (lb / 8 / SS) & 1,
+                                                  p.status, &s_fail))) {
+                ok = false;
+                break;
+            }
+            const int sw = lb % WS;
+            if (!__all_sync(0xffffffffu,
+                            qmm_wait(&wfull[sw], (lb / WS) & 1, p.status, &s_fail))) {
+                ok = false;
+                break;
+            }
+            const uint4 *ws = reinterpret_cast<const uint4 *>(
+                smem + L::WOFF + (size_t)sw * L::WBYTES + (size_t)r * BITS * 8);
+            uint32_t w[BITS * 2];
+            if constexpr (BITS == 4) {
+                // rows 128 bytes apart read their two 16-byte chunks in
+                // opposite order (different banks in one instruction)
+                const bool rot = (r >> 2) & 1;
+                const uint4 c0 = ws[rot ? 1 : 0], c1 = ws[rot ? 0 : 1];
+                const uint4 lo4 = rot ? c1 : c0, hi4 = rot ? c0 : c1;
+                w[0] = lo4.x; w[1] = lo4.y; w[2] = lo4.z; w[3] = lo4.w;
+                w[4] = hi4.x; w[5] = hi4.y; w[6] = hi4.z; w[7] = hi4.w;
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 c = ws[v];
+                    w[4 * v] = c.x; w[4 * v + 1] = c.y;
+                    w[4 * v + 2] = c.z; w[4 * v + 3] = c.w;
+                }
+            }
+            const uint16_t *st = reinterpret_cast<const uint16_t *>(
+                smem + L::SOFF + (size_t)ss * L::SBYTES);
+            const float s = bf16_bits_to_f32(st[r * 8 + (kb & 7)]) * rup;
+            // the codes and scale of this block are in registers
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&wempty[sw]);
+                if ((kb & 7) == 4 + ph || kb == G - 1) mbar_arrive(&sempty[ss]);
+            }
+            dequant_row<BITS>(w, s, hi, lo);
+            ok = store_a(lb, hi, lo);
+        }
+        for (; ok && lb < nb; lb += 4) {
+            uint32_t hi[32], lo[BITS == 8 ? 32 : 1];
+            bias_row<BITS>(p, n, kb0 + lb, rup, hi);
+            if constexpr (BITS == 8)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) lo[i] = 0u;
+            ok = store_a(lb, hi, lo);
         }
         // all MMAs done
         fin = __all_sync(0xffffffffu, qmm_wait(&dfull, 0, p.status, &s_fail));
