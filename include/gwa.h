@@ -187,7 +187,7 @@ int gwa_moe_qmv_gather(const uint16_t *x, int64_t M, int32_t topk,
  *   device, so gwa_pipeline_status reports it; the caller needs no access to
  *   the scratch.
  *   Size: gwa_workspace_bytes(M, K) is about 2.1 K bytes per token, so the
- *   scratch fits M <= 1925 at K = 2048, M <= 779 at K = 5120 and M <= 288
+ *   scratch fits M <= 1925 at K = 2048, M <= 779 at K = 5120 and M <= 287
  *   at K = 13824 (a down projection); larger problems need gwa_qmv_affine
  *   with a workspace. */
 #define GWA_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -26,7 +26,7 @@ def tc_accumulation_bar(ref, x, w, rows):
     per_input = np.repeat(b + 2.0 * c * s, 64, axis=1)      # [rows, K]
     xa = np.abs(synth.bf16_values(x).astype(np.float64))
     mag = xa @ per_input.T
-    kext = K + ((3 * G + 63) // 64) * 64
+    kext = K + ((3 * G + 127) // 128) * 128
     steps = (kext // 16) * (2 if w.bits == 8 else 1)
     return TOL * np.maximum(1.0, np.abs(ref)) + steps * 2.0**-23 * mag
 
