@@ -7,17 +7,15 @@ import gwa_synth as synth
 TOL = 1e-2
 
 
-def tc_accumulation_bar(ref, x, w, rows):
-    """1e-2 * max(1, |ref|) plus the fp32 accumulation's own rounding on the
-    tensor-core kernel.
+def tc_accumulation_term(x, w, rows):
+    """The fp32 accumulation's own rounding on the tensor-core kernel, per
+    output [M, len(rows)].
 
     Operands reach the tensor cores exactly, but the products are summed in
     fp32: each of the MMA's K steps (kext/16, twice for u8's two code halves)
     rounds at most 2^-23 of the magnitude of what it adds up.  The terms
     summed are x * s(q - c) per input and b' X per group (b' = b + c s, c = 8
-    or 136, X a group sum), all bounded by |x| (|b| + 2 c |s|) per input.
-    Where an output cancels to far below those terms (a large common weight
-    offset, as with u8 biases of -8 s), that rounding is above 1e-2 |y|."""
+    or 136, X a group sum), all bounded by |x| (|b| + 2 c |s|) per input."""
     K = w.K
     G = K // 64
     c = 8.0 if w.bits == 4 else 136.0
@@ -28,7 +26,37 @@ def tc_accumulation_bar(ref, x, w, rows):
     mag = xa @ per_input.T
     kext = K + ((3 * G + 127) // 128) * 128
     steps = (kext // 16) * (2 if w.bits == 8 else 1)
-    return TOL * np.maximum(1.0, np.abs(ref)) + steps * 2.0**-23 * mag
+    return steps * 2.0**-23 * mag
+
+
+def tc_accumulation_bar(ref, x, w, rows):
+    """1e-2 * max(1, |ref|) plus the fp32 accumulation's own rounding on the
+    tensor-core kernel (tc_accumulation_term).  Where an output cancels to
+    far below its terms (a large common weight offset, as with u8 biases of
+    -8 s), that rounding is above 1e-2 |y|."""
+    return TOL * np.maximum(1.0, np.abs(ref)) + tc_accumulation_term(x, w, rows)
+
+
+def tc_swiglu_bar(x, w, I):
+    """Reference h = SiLU(g) * u in fp64 for a gate+up weight of 2I rows on
+    the tensor-core kernel, and its bar: 1e-2 * max(1, |h|) plus the fp32
+    rounding of g and u (tc_accumulation_term) carried through the epilogue,
+    |SiLU'(g) u| e_g + |SiLU(g)| e_u.  That term matters where one factor
+    cancels to far below its terms while the other is large."""
+    import oracle
+    W = oracle.dequant(w.wq, w.scales, w.biases, w.N, w.K, w.bits)
+    xv = synth.bf16_values(x).astype(np.float64)
+    g = xv @ W[:I].T
+    u = xv @ W[I:].T
+    eg = tc_accumulation_term(x, w, np.arange(I))
+    eu = tc_accumulation_term(x, w, np.arange(I, 2 * I))
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    h = silu * u
+    bar = TOL * np.maximum(1.0, np.abs(h)) + np.abs(dsilu * u) * eg + np.abs(silu) * eu
+    return h, bar
 
 
 def assert_within(got, ref, bar, what=""):

@@ -8,7 +8,7 @@ import torch
 import group_wise_affine_gb300 as gwa
 import gwa_synth as synth
 import oracle
-from bars import assert_within, tc_accumulation_bar
+from bars import assert_within, tc_accumulation_bar, tc_swiglu_bar
 from helpers import bf16_to_f64, dev_bf16, dev_qweight
 
 pytestmark = pytest.mark.gpu
@@ -73,7 +73,63 @@ def test_qmm_gate_up_silu(bits, M, K, I):
     x = synth.activations(1610 + M, M, K)
     h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
     ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits)
-    assert_close(bf16_to_f64(h), ref, f"qmm gate_up M={M} u{bits}")
+    _, bar = tc_swiglu_bar(x, w, I)
+    assert_within(bf16_to_f64(h), ref, bar, f"qmm gate_up M={M} u{bits}")
+
+
+# Few tiles for the GPU: the kernel splits each tile's K blocks over a
+# cluster of up to 4 CTAs (rank 0 adds the others' partial sums through
+# distributed shared memory).  With K = 5120 (84 K blocks) or 13824 and at
+# most a handful of 128-row tiles, every shape below fits one wave of
+# 4-CTA clusters on a 152-SM GPU, so it takes the split.
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [16, 300])
+@pytest.mark.parametrize("mode", ["plain", "sections", "gate_up"])
+def test_qmm_cluster_k_split(bits, M, mode):
+    K = 5120
+    x = synth.activations(1700 + M, M, K)
+    if mode == "plain":
+        N = 200  # two tiles, the last one partial
+        w = synth.qweight(1710 + bits, N, K, bits)
+        y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w))
+        ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+        assert_close(bf16_to_f64(y), ref, f"split plain M={M} u{bits}")
+    elif mode == "sections":
+        secs = (128, 64, 72)
+        parts = [synth.qweight(1720 + i, n, K, bits) for i, n in enumerate(secs)]
+        fused = synth.stack_rows(parts)
+        bias = [synth.activations(1730 + i, 1, n)[0] for i, n in enumerate(secs)]
+        outs = gwa.qmv_fused_sections(dev_bf16(x), dev_qweight(fused), secs,
+                                      out_bias=[dev_bf16(b) for b in bias])
+        refs = oracle.fused_sections(x, fused.wq, fused.scales, fused.biases,
+                                     secs, K, bits, out_bias=bias)
+        for o, r in zip(outs, refs):
+            assert_close(bf16_to_f64(o), r, f"split sections M={M} u{bits}")
+    else:
+        I = 100  # two 64-pair tiles
+        w = synth.qweight(1740 + bits, 2 * I, K, bits)
+        h = gwa.qmv_gate_up_silu(dev_bf16(x), dev_qweight(w))
+        ref = oracle.gate_up_silu(x, w.wq, w.scales, w.biases, 2 * I, K, bits)
+        # where g or u cancels (u8 sums of ~6000 in magnitude reaching 0.01)
+        # its fp32 rounding moves h by more than 1e-2 |h|: the SwiGLU bar
+        href, bar = tc_swiglu_bar(x, w, I)
+        assert np.allclose(href, ref, rtol=1e-9, atol=1e-12)
+        assert_within(bf16_to_f64(h), ref, bar, f"split gate_up M={M} u{bits}")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qmm_cluster_k_split_long_rows(bits):
+    # one 128-row tile of a down projection's input width: four ranks of
+    # 7-8 runs of 8 K blocks each, the bias blocks on the last
+    M, N, K = 16, 128, 13824
+    w = synth.qweight(1750 + bits, N, K, bits)
+    x = synth.activations(1751, M, K)
+    ws = gwa.make_workspace(M, K)
+    y = gwa.qmv_affine(dev_bf16(x), dev_qweight(w), workspace=ws)
+    torch.cuda.synchronize()
+    assert status_of(ws) == 0
+    ref = oracle.qmv(x, w.wq, w.scales, w.biases, N, K, bits)
+    assert_close(bf16_to_f64(y), ref, f"split long rows u{bits}")
 
 
 def test_tensor_core_and_decode_paths_agree():
