@@ -355,6 +355,26 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     e2e_ms = e0.elapsed_time(e1) / KE
+    # the same with the 192 calls issued eagerly each step (no graph): the
+    # host-side cost of the binding and the C ABI included
+    KG = max(3, min(K, 20))
+    for _ in range(2):
+        for l in range(L):
+            for k in kinds:
+                call(k, l, stream=st)
+    torch.cuda.synchronize()
+    t_eager = time.perf_counter()
+    e0.record(st)
+    for _ in range(KG):
+        x.copy_(x_host, non_blocking=True)
+        for l in range(L):
+            for k in kinds:
+                call(k, l, stream=st)
+        y_host.copy_(bufs[-1]["y"], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    t_eager = time.perf_counter() - t_eager
+    eager_ms = e0.elapsed_time(e1) / KG
     extras = {}
     if not args.no_extras and bits == 4 and L == LAYERS and M == 1:
         # chained activations: down reads h = SiLU(gate) * up, whose spread
@@ -379,6 +399,7 @@ def run_gwa(args, rank: int, world: int, local_rank: int):
         extras["attention"] = run_attention_extra(dev, 20, 3)
     return dict(total_ms=total_ms, per_kind_ms=per_kind_ms, clocks=clk,
                 e2e_ms=e2e_ms, e2e_wall_ms=1e3 * t_wall / KE,
+                eager_ms=eager_ms, eager_wall_ms=1e3 * t_eager / KG,
                 h2d=M * HIDDEN * 2, d2h=M * HIDDEN * 2,
                 launches=K * 4 * L, extras=extras)
 
@@ -835,6 +856,7 @@ def main():
     if world > 1:
         total_ms = max_over_ranks(total_ms, "cuda")
         e2e_ms = max_over_ranks(e2e_ms, "cuda")
+        r["eager_ms"] = max_over_ranks(r["eager_ms"], "cuda")
     K, L, M, bits = args.steps, args.layers, args.tokens, args.bits
     lb = layer_bytes(bits, M)
     step_bytes = sum(lb.values()) * L
@@ -883,7 +905,16 @@ def main():
                 "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": round(e2e_ms, 4),
                 "how": "pinned x in, one graph replay of the 192 public API "
-                       "calls, last layer's y out, per step"},
+                       "calls, last layer's y out, per step",
+                "eager": {"value": round(whole_job_gbs(world, step_bytes,
+                                                       r["eager_ms"]), 1),
+                          "unit": "GB/s",
+                          "ms_per_step": round(r["eager_ms"], 4),
+                          "wall_ms_per_step": round(r["eager_wall_ms"], 4),
+                          "how": "the same copies with the 192 calls issued "
+                                 "from Python through the ctypes binding "
+                                 "every step (no graph), so the host-side "
+                                 "cost of the binding and the C ABI counts"}},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
