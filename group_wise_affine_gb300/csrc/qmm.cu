@@ -844,7 +844,9 @@ __global__ void __launch_bounds__(kQmmThreads, 1)
                         const float g = gbuf[pr * GS + c0 + j];
                         const float uv = u[j] * rdown * s_tok[c0 + j];
                         p.y[m * p.I + i] =
-                            f32_to_bf16_bits(g / (1.0f + __expf(-g)) * uv);
+                            // SiLU with the fast divide (two ulps; the
+                            // output is bf16; 0 once e^-g passes 2^126)
+                            f32_to_bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * uv);
                     }
                 }
             }
