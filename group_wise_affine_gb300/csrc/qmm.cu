@@ -50,6 +50,11 @@
 //             then reads the fp32 accumulators back with tcgen05.ld for the
 //             epilogue (gate+up: the gate warps pass their values to the up
 //             warps through shared memory).
+// K split: when a projection's tiles leave SMs idle and fit one wave of
+// clusters, the ks CTAs of a cluster share a tile, each taking a run of K
+// blocks; ranks 1.. leave their fp32 partial sums in shared memory and rank
+// 0 adds them through distributed shared memory before the epilogue
+// (qmm_tc_kernel<..., true>).
 // Every wait is bounded (2 s); a wait that runs out flags the workspace
 // status word and the kernel unwinds without hanging.
 #include <cuda.h>
