@@ -53,6 +53,13 @@ namespace gwa {
 static __device__ unsigned int g_mma_timeouts;
 
 constexpr int kMmaUnits = 8;          // units per stage: the MMAs' n
+// Padding after each row in a stage.  The eight rows of an MMA are read at
+// the same offset, four lanes a row (u4 8 bytes, u8 16 bytes each); rows a
+// multiple of 128 bytes apart would put all eight in the same banks, so a
+// row's stride is its bytes plus 32 (u4) or 64 (u8): the reads then take
+// the two (four) wavefronts their 256 (512) bytes need.
+template <int BITS>
+constexpr uint32_t kMmaRowPad = BITS == 4 ? 32u : 64u;
 constexpr int kMmaGroupsPerWarp = 8;  // 512 inputs per consumer warp
 constexpr int kMmaMaxWarps = 10;      // K <= 5120
 constexpr int kMmaTokens = 8;
@@ -164,7 +171,8 @@ __global__ void __maxnreg__(168)
     const uint32_t growbytes = (uint32_t)p.K * BITS / 8;
     const uint32_t gsbrow = (uint32_t)p.G * 2;
     const uint32_t rows_stage = (uint32_t)(HALVES * ups);
-    const uint32_t stage_bytes = rows_stage * (rowbytes + 2 * sbrow);
+    const uint32_t rowstride = rowbytes + kMmaRowPad<BITS>;
+    const uint32_t stage_bytes = rows_stage * (rowstride + 2 * sbrow);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
     uint64_t *empty = full + stages;
     float *red = reinterpret_cast<float *>(empty + stages);
@@ -207,7 +215,7 @@ __global__ void __maxnreg__(168)
                 const int64_t ua = u0 + (int64_t)st * ups;
                 const int n = (int)min((int64_t)ups, u1 - ua);
                 unsigned char *base = smem + (size_t)s * stage_bytes;
-                unsigned char *dsc = base + rows_stage * rowbytes;
+                unsigned char *dsc = base + rows_stage * rowstride;
                 unsigned char *dbi = dsc + rows_stage * sbrow;
                 mbar_expect_tx(&full[s], (uint32_t)(HALVES * n) * (rowbytes + 2 * sbrow));
 #pragma unroll
@@ -215,8 +223,11 @@ __global__ void __maxnreg__(168)
                     const int64_t r = MODE == kMRope ? rope_pair_row(ua, h, p.rope_hd)
                                                      : ua + (h ? p.I : 0);
                     if constexpr (KS == 1) {
-                        bulk_g2s(base + h * ups * rowbytes, wq + r * rowbytes,
-                                 n * rowbytes, &full[s]);
+                        // a copy per row (padded strides), one for the
+                        // stage's scales and one for its biases
+                        for (int i = 0; i < n; ++i)
+                            bulk_g2s(base + (uint32_t)(h * ups + i) * rowstride,
+                                     wq + (r + i) * rowbytes, rowbytes, &full[s]);
                         bulk_g2s(dsc + h * ups * sbrow, sc + r * sbrow, n * sbrow,
                                  &full[s]);
                         bulk_g2s(dbi + h * ups * sbrow, bi + r * sbrow, n * sbrow,
@@ -226,7 +237,7 @@ __global__ void __maxnreg__(168)
                         for (int i = 0; i < n; ++i) {
                             const int64_t ri = r + i;
                             const uint32_t d = (uint32_t)(h * ups + i);
-                            bulk_g2s(base + d * rowbytes,
+                            bulk_g2s(base + d * rowstride,
                                      wq + ri * growbytes + (uint32_t)rank * rowbytes,
                                      rowbytes, &full[s]);
                             bulk_g2s(dsc + d * sbrow,
@@ -258,7 +269,7 @@ __global__ void __maxnreg__(168)
             const int64_t ua = u0 + (int64_t)st * ups;
             const int n = (int)min((int64_t)ups, u1 - ua);
             const unsigned char *base = smem + (uint32_t)s * stage_bytes;
-            const unsigned char *scb = base + rows_stage * rowbytes;
+            const unsigned char *scb = base + rows_stage * rowstride;
             const unsigned char *bib = scb + rows_stage * sbrow;
             // rows past the stage's end hold stale data: their columns of
             // the products are dropped below
@@ -272,7 +283,7 @@ __global__ void __maxnreg__(168)
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
                     // lane (g, t) supplies weight row g's k slice t ...
-                    const unsigned char *wr = base + (uint32_t)(h * ups + g) * rowbytes +
+                    const unsigned char *wr = base + (uint32_t)(h * ups + g) * rowstride +
                                               (uint32_t)gg * GB + (uint32_t)t * (GB / 4);
                     float c[4] = {0.f, 0.f, 0.f, 0.f};
                     if constexpr (BITS == 4) {
@@ -462,7 +473,8 @@ static cudaError_t launch_mma_t(const DenseParams &p, cudaStream_t st, bool *use
     const int threads = (nw + 1) * kWarp;
     const size_t rowbytes = (size_t)Ks * BITS / 8;
     const size_t sbrow = (size_t)(Ks / kGroup) * 2;
-    const size_t stage_bytes = (size_t)HALVES * kMmaUnits * (rowbytes + 2 * sbrow);
+    const size_t stage_bytes =
+        (size_t)HALVES * kMmaUnits * (rowbytes + kMmaRowPad<BITS> + 2 * sbrow);
     const int64_t ualign = MODE == kMRope ? kMmaUnits : 1;
     int ncl = num_sms() / KS;  // clusters (CTAs when KS = 1)
     if ((int64_t)ncl > units / ualign) ncl = (int)(units / ualign);
