@@ -28,9 +28,10 @@
 //
 // Measured on the 27648 x 5120 gate+up weight: 36.9 us for 8 tokens in one
 // pass (the streaming kernel streams the weights twice: ~72 us), but only
-// level with the streaming kernel at 4 tokens (35.1 against 36.3 us): the
-// B-fragment reads of eight rows whose shared-memory stride is a multiple
-// of 128 bytes conflict eight ways, so it serves 5..8 tokens.
+// level with the streaming kernel at 4 tokens (35.1 against 36.3 us), so it
+// serves 5..8 tokens.  (Those figures predate the padded row stride below,
+// which removed the eight-way bank conflicts of the B-fragment reads: QKV
+// at 8 tokens 11.8 -> 10.9 us, gate+up unchanged.)
 //
 // k order: within a group, lane t's k-slice of k-step s (logical k 2t, 2t+1,
 // 2t+8, 2t+9) is the nibbles (j, j+4) and (j+1, j+5), j = 2 (s & 1), of word
