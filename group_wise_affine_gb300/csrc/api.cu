@@ -124,6 +124,43 @@ cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
     return cudaSuccess;
 }
 
+// Clusters of `cl` CTAs of `kernel` (`threads` threads, `smem` bytes of
+// dynamic shared memory each) that the GPU keeps resident at once, 0 if it
+// cannot launch them; cached per device, kernel, cluster size, block and
+// shared memory.  The kernel's shared-memory attribute must be set first
+// (occupancy_grid does).
+int resident_clusters(const void *kernel, int cl, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, kernel, cl, threads, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
 // Largest shared-memory carveout for a kernel whose CTAs (about 110 KB each)
 // must sit two to an SM: the next kernel's CTA then starts beside this
 // one's (programmatic dependent launch) instead of waiting for the SM to

@@ -123,6 +123,9 @@ cudaError_t launch_pdl_cluster(const void *kernel, unsigned grid,
 cudaError_t occupancy_grid(const void *kernel, int threads, size_t smem,
                            int *grid);
 int num_sms();
+// Clusters of `cl` CTAs of `kernel` the GPU keeps resident at once (0: none;
+// the kernel's shared-memory attribute set first, as occupancy_grid does).
+int resident_clusters(const void *kernel, int cl, int threads, size_t smem);
 // Largest shared-memory carveout for a streaming kernel (once per device).
 cudaError_t prefer_max_shared(const void *kernel);
 

@@ -35,9 +35,6 @@
 // the CTAs of the cluster add the accumulators of ranks 0, 1, ... through
 // distributed shared memory, so the combine is deterministic and needs no
 // atomics or global scratch.
-#include <map>
-#include <mutex>
-#include <tuple>
 
 #include "cluster.cuh"
 #include "group_dot.cuh"
@@ -504,39 +501,6 @@ __global__ void __maxnreg__(128)
 }
 
 // ------------------------------------------------------------ host side
-// Clusters of `cl` CTAs (one per SM) the GPU can keep resident at once
-// (cached per device, kernel, cluster size and shared memory).
-static int resident_clusters(const void *kern, int cl, size_t smem) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, kern, cl, smem);
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
-    cfg.blockDim = dim3(kMsThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        n = 0;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    cache[key] = n;
-    return n;
-}
 
 template <int BITS, int MODE, int W>
 static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
@@ -607,7 +571,8 @@ static cudaError_t launch_ms(const MoeParams &p, cudaStream_t st, bool *used) {
                 const int res =
                     cl == 1 ? clusters
                             : resident_clusters(
-                                  reinterpret_cast<const void *>(kern), cl, smem);
+                                  reinterpret_cast<const void *>(kern), cl,
+                                  kMsThreads, smem);
                 if (res >= clusters) {
                     ok = true;
                     grid = clusters * cl;

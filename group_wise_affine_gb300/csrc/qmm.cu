@@ -60,9 +60,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <map>
 #include <mutex>
-#include <tuple>
 
 #include "cluster.cuh"
 #include "common.cuh"
@@ -1009,39 +1007,6 @@ static int encode_2d(CUtensorMap *map, CUtensorMapDataType type, int esize,
     return GWA_OK;
 }
 
-// Clusters of `cl` CTAs of `kern` that the GPU keeps resident at once (0:
-// none), cached per device, kernel, cluster size and shared memory.
-static int qmm_resident_clusters(const void *kern, int cl, size_t smem) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, kern, cl, smem);
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
-    cfg.blockDim = dim3(kQmmThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        n = 0;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    cache[key] = n;
-    return n;
-}
 
 template <int BITS, int NT>
 static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
@@ -1127,8 +1092,8 @@ static int qmm_launch(const QmmArgs &a, unsigned char *ws, cudaStream_t st) {
     if (tiles < resident) {
         const int n8 = (p.nkb + 7) / 8;
         for (int ks = 2; ks <= kQmmMaxSplit && n8 >= 2 * ks; ++ks) {
-            const int cap = qmm_resident_clusters(
-                reinterpret_cast<const void *>(kern_split), ks, L::SMEM);
+            const int cap = resident_clusters(
+                reinterpret_cast<const void *>(kern_split), ks, kQmmThreads, L::SMEM);
             if (cap >= tiles) p.ks = ks;
         }
     }

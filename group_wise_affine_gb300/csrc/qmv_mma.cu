@@ -41,9 +41,6 @@
 // Itself", "The two fusions"; "saragossa", "Quantization formats").
 #include <cuda_bf16.h>
 
-#include <map>
-#include <mutex>
-#include <tuple>
 
 #include "cluster.cuh"
 #include "common.cuh"
@@ -427,40 +424,6 @@ __global__ void __maxnreg__(168)
 }
 
 // ------------------------------------------------------------ host side
-// Clusters of `cl` CTAs of `kern` the GPU can keep resident at once
-// (cached per device, kernel, cluster size, block and shared memory).
-static int mma_resident_clusters(const void *kern, int cl, int threads,
-                                 size_t smem) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, const void *, int, int, size_t>, int> cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, kern, cl, threads, smem);
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(cl * (num_sms() / cl)));
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        n = 0;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    cache[key] = n;
-    return n;
-}
 
 template <int BITS, int MODE, int KS>
 static cudaError_t launch_mma_t(const DenseParams &p, cudaStream_t st, bool *used) {
@@ -503,7 +466,7 @@ static cudaError_t launch_mma_t(const DenseParams &p, cudaStream_t st, bool *use
     if (e != cudaSuccess) return e;
     if constexpr (KS > 1) {
         // one wave: no more clusters than the GPU keeps resident
-        const int res = mma_resident_clusters(reinterpret_cast<const void *>(kern), KS,
+        const int res = resident_clusters(reinterpret_cast<const void *>(kern), KS,
                                               threads, smem);
         if (res < 1) return cudaSuccess;
         if (res < ncl) {
