@@ -376,15 +376,15 @@ struct QmmLayout {
     static constexpr int AW = BITS == 4 ? 32 : 64;  // A columns per K block
     // ring slots: an activation tile and a K block's A columns each; tensor
     // memory holds NT accumulator columns and the A slots, shared memory the
-    // tiles
+    // tiles (six tiles at 256 tokens, 213 KB per CTA, ran slower than four)
     static constexpr int SA = (512 - NT) / AW;
     static constexpr int SX = NT == 256 ? 4 : 8;
     static constexpr int KP = NT <= 16 ? 2 : 1;          // K blocks per slot
     static constexpr int RS = (SA < SX ? SA : SX) / KP * KP;  // K blocks
     static constexpr int RP = RS / KP;                   // slots
     // code tiles; a smaller footprint leaves more of the SM's 256 KB to L1
-    // (the bias blocks read scales and biases through it), and above
-    // ~180 KB per CTA the kernel ran twice as slow
+    // (the rows' range scan and the bias blocks read scales and biases
+    // through it), and above ~180 KB per CTA the kernel ran slower
     static constexpr int WS = 4;
     static constexpr int XBYTES = NT * 128;           // 64 fp16 per token
     static constexpr int WBYTES = kQmmRows * BITS * 8;  // 64 codes per row
