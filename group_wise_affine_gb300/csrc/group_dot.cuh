@@ -498,10 +498,25 @@ __device__ __forceinline__ void group_dot_lo_split(const uint4 (&w)[BITS / 2],
 // group_dot of token m of a marked chunk, in fp32 (common.cuh): the same
 // pairs hold raw bf16 activations and the same code bytes multiply them, so
 // the result has group_dot's scale (u4: 16 times the true sum).
+// Two fp32 products per instruction (FFMA2): a pair of raw bf16
+// activations times a pair of code bytes (bytes i, i + 1 of b, each exact as
+// 2^23 + byte - 2^23), into the two lanes of a float2 accumulator.
+template <int I>
+__device__ __forceinline__ float2 byte_pair_f32(uint32_t b) {
+    const float2 t = make_float2(__uint_as_float(__byte_perm(b, 0x4b000000u, 0x7440 | I)),
+                                 __uint_as_float(__byte_perm(b, 0x4b000000u, 0x7440 | (I + 1))));
+    return __fadd2_rn(t, make_float2(-8388608.0f, -8388608.0f));
+}
+__device__ __forceinline__ float2 bf16_pair_f32(uint32_t a) {
+    return make_float2(bf16_lo(a), bf16_hi(a));
+}
+
 template <int BITS, int MT>
 __device__ __forceinline__ float group_dot_f32(const uint4 (&w)[BITS / 2],
                                                const GroupX<MT> &gx, int m) {
-    float a[2] = {0.f, 0.f};
+    // u4: lanes of a0 sum the low nibbles' products, a1 the high ones'
+    // (16 q); u8: a0 bytes 0-1, a1 bytes 2-3 of each word
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < BITS / 2; ++v) {
 #pragma unroll
@@ -509,13 +524,22 @@ __device__ __forceinline__ float group_dot_f32(const uint4 (&w)[BITS / 2],
             const int wd = 4 * v + c;
             const uint32_t word = c == 0 ? w[v].x : c == 1 ? w[v].y
                                   : c == 2 ? w[v].z : w[v].w;
-            if constexpr (BITS == 4)
-                fword_dot_u4(word, gx.pr[m] + 4 * wd, a);
-            else
-                fword_dot_u8(word, gx.pr[m] + 2 * wd, a);
+            if constexpr (BITS == 4) {
+                const uint32_t *pr = gx.pr[m] + 4 * wd;
+                const uint32_t lo = word & 0x0f0f0f0fu, hi = word & 0xf0f0f0f0u;
+                a0 = __ffma2_rn(bf16_pair_f32(pr[0]), byte_pair_f32<0>(lo), a0);
+                a0 = __ffma2_rn(bf16_pair_f32(pr[1]), byte_pair_f32<2>(lo), a0);
+                a1 = __ffma2_rn(bf16_pair_f32(pr[2]), byte_pair_f32<0>(hi), a1);
+                a1 = __ffma2_rn(bf16_pair_f32(pr[3]), byte_pair_f32<2>(hi), a1);
+            } else {
+                const uint32_t *pr = gx.pr[m] + 2 * wd;
+                a0 = __ffma2_rn(bf16_pair_f32(pr[0]), byte_pair_f32<0>(word), a0);
+                a1 = __ffma2_rn(bf16_pair_f32(pr[1]), byte_pair_f32<2>(word), a1);
+            }
         }
     }
-    return BITS == 4 ? fmaf(a[0], 16.f, a[1]) : a[0] + a[1];
+    const float s0 = a0.x + a0.y, s1 = a1.x + a1.y;
+    return BITS == 4 ? fmaf(s0, 16.f, s1) : s0 + s1;
 }
 
 // The same dot split over the chunk's two halves (groups of 32): dl over
